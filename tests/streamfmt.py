@@ -1,0 +1,69 @@
+"""Independent reader of the refit stream wire format, for tests only.
+
+Layout (little-endian): a 64-byte stream header, 16-byte-aligned frames in
+ascending chunk order (each a 32-byte frame header plus body), then an index
+of u64 frame offsets.  Written from the format description alone; shares no
+code with the oracle or the CUDA library.
+"""
+import struct
+
+import numpy as np
+
+STREAM_MAGIC = b"DCRS"
+FRAME_MAGIC = b"DCRF"
+K_XOR_LZ4, K_XOR_RAW, K_OVERWRITE, K_OVERWRITE_DENSE = 1, 2, 3, 4
+FLAG_OVERWRITE_ONLY = 1
+FRAME_ZSRC = 1
+
+
+def parse(payload):
+    b = bytes(np.asarray(payload, dtype=np.uint8))
+    assert len(b) >= 64
+    (magic, fmt, plan_hash, base_v, target_v, window, flags, cb, cc, nf, total) = struct.unpack_from(
+        "<4sIQQQIIIIQQ", b, 0)
+    hdr = dict(magic=magic, format=fmt, plan_hash=plan_hash, base_version=base_v,
+               target_version=target_v, window=window, flags=flags, chunk_begin=cb,
+               chunk_count=cc, n_frames=nf, total=total)
+    idx_off = total - 8 * nf
+    offs = list(struct.unpack_from("<%dQ" % nf, b, idx_off)) if nf else []
+    frames = []
+    for o in offs:
+        fm, kind, bits, fflags, chunk, raw, bl, changed, res = struct.unpack_from("<4sBBHIIIIQ", b, o)
+        frames.append(dict(offset=o, magic=fm, kind=kind, elem_bits=bits, flags=fflags, chunk=chunk,
+                           raw_len=raw, body_len=bl, changed=changed, reserved=res,
+                           body=np.frombuffer(b[o + 32:o + 32 + bl], dtype=np.uint8)))
+    return hdr, frames, idx_off
+
+
+def check_structure(payload):
+    """Structural invariants every well-formed stream meets."""
+    hdr, frames, idx_off = parse(payload)
+    assert hdr["magic"] == STREAM_MAGIC and hdr["format"] == 1
+    assert hdr["total"] == len(payload)
+    pos = 64
+    prev = -1
+    for f in frames:
+        assert f["magic"] == FRAME_MAGIC
+        assert f["offset"] == pos, "frames are contiguous and in index order"
+        assert f["offset"] % 16 == 0
+        assert hdr["chunk_begin"] <= f["chunk"] < hdr["chunk_begin"] + hdr["chunk_count"]
+        assert f["chunk"] > prev, "ascending chunk order"
+        prev = f["chunk"]
+        assert f["kind"] in (1, 2, 3, 4) and f["reserved"] == 0 and f["changed"] > 0
+        flen = (32 + f["body_len"] + 15) // 16 * 16
+        pad = np.asarray(payload[f["offset"] + 32 + f["body_len"]:f["offset"] + flen])
+        assert not pad.any(), "frame padding is zero"
+        pos += flen
+    assert pos == idx_off
+    return hdr, frames
+
+
+def overwrite_records(f):
+    """(unit offsets, values as uint8 rows) of an OVERWRITE frame body."""
+    body = f["body"]
+    ub = 2 if f["elem_bits"] == 16 else 1
+    n = int(struct.unpack_from("<I", body.tobytes(), 0)[0])
+    offs = np.frombuffer(body[4:4 + 2 * n].tobytes(), dtype="<u2").astype(np.int64)
+    pad = (4 - (2 * n) % 4) % 4
+    vals = body[4 + 2 * n + pad:4 + 2 * n + pad + n * ub].reshape(n, ub)
+    return offs, vals
