@@ -1,0 +1,415 @@
+"""Benchmark: bit-exact delta-compressed refit (encode + apply) on GB300.
+
+One step = one full refit of the dense TP=2 transformer workload (hidden 1024,
+24 layers, FFN 4096, vocab 32768, bf16, 704 MiB canonical, 1 % of stored
+values changed with low-mantissa perturbations): dcr_encode of the trainer
+shards (gather + XOR + count + LZ4 + frame compaction) followed by dcr_apply
+on the receiver arena (decode + XOR in place + dedup + commit).  Steps
+alternate direction (old->new, new->old) so the receiver never needs a
+restore.  Inputs (1.4 GB read per encode) are larger than L2.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+                  [--workload dense|single|gqa|sweep|moe] [--frac F]
+
+Prints one JSON line.  --impl reference times the CPU oracle (the reference
+arm of this build) on the same workload.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+sys.path.insert(0, os.path.join(ROOT, "tests"))
+
+METRIC = "encode & apply GB/s of weight bytes on 1 GB300 (% HBM peak); payload bytes"
+UNIT = "GB/s"
+WORKLOAD_NAMES = {
+    "dense": "dense-tp2: bf16 transformer h1024 l24 ffn4096 v32768, TP=2 shards, 1% low-3-bit changes",
+    "single": "single-bf16: one 4096x4096 bf16 tensor, 1% +-1..4 changes + 0.01% signed zeros",
+    "gqa": "gqa-tp4: Llama GQA h4096 l32 32q/8kv hd128 ffn14336 v128256, TP=4, fused QKV residual, 3%",
+    "sweep": "sweep: one 8 GiB bf16 buffer, +-1..4 changes",
+    "moe": "nvfp4-moe: h6144 64 experts ffn2048 16 layers, e2m1 + e4m3 scales, 0.085%, 16 GiB windows",
+}
+
+
+def build_workload(name, frac=None):
+    from synth import configs
+    if name == "dense":
+        return configs.dense(frac=frac if frac is not None else 0.01)
+    if name == "single":
+        return configs.single(frac=frac if frac is not None else 0.01)
+    if name == "gqa":
+        return configs.gqa(frac=frac if frac is not None else 0.03)
+    if name == "sweep":
+        return configs.sweep(frac=frac if frac is not None else 0.01)
+    if name == "moe":
+        return configs.nvfp4_moe(frac=frac if frac is not None else 0.00085)
+    raise SystemExit("unknown workload " + name)
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def ncu_traffic():
+    """Per-launch DRAM bytes of the encode kernel from the committed ncu
+    summary, only if the kernel source is unchanged since it was taken."""
+    path = os.path.join(ROOT, "profiles", "encode_kernel_dense_tp2.md")
+    src = os.path.join(ROOT, "bit_exact_xor_gb300", "csrc", "encode.cu")
+    try:
+        text = open(path).read()
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        fields = dict(l.split(":", 1) for l in text.splitlines() if l.startswith(("traffic_bytes_per_launch:",
+                                                                                   "encode_cu_sha256_16:")))
+        if fields.get("encode_cu_sha256_16:".rstrip(":"), "").strip() == sha:
+            return int(fields["traffic_bytes_per_launch"].strip())
+    except Exception:
+        pass
+    return None
+
+
+class Clocks:
+    """nvidia-smi sampling during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.p = None
+
+    def __enter__(self):
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
+                                       "--format=csv,noheader,nounits", "-lms", "200"],
+                                      stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.p = None
+        return self
+
+    def __exit__(self, *a):
+        self.rows = []
+        if self.p is None:
+            return
+        time.sleep(0.25)
+        self.p.terminate()
+        try:
+            out, _ = self.p.communicate(timeout=5)
+        except Exception:
+            self.p.kill()
+            out = ""
+        for line in out.splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                self.rows.append(parts)
+
+    def summary(self):
+        if not getattr(self, "rows", None):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in self.rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in self.rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.rows)}
+
+
+# --------------------------------------------------------------------------
+# multi-process helpers (one rank per GPU, replicas of the single-GPU refit)
+# --------------------------------------------------------------------------
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def dist_max(value, ws):
+    """Maximum of a float over ranks (identity for one rank)."""
+    if ws == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def dist_barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# --------------------------------------------------------------------------
+# CPU oracle leg (baseline and reference arm)
+# --------------------------------------------------------------------------
+def oracle_runner(wl, threads):
+    import numpy as np
+    import oracle
+    orc = oracle.Oracle(wl)
+    olds, news = wl.host_arenas()
+    tgt = orc.receiver_dense(olds)
+    state = {"st": orc.state(0), "dir": 0, "v": 0}
+
+    def step():
+        a, b = (olds, news) if state["dir"] == 0 else (news, olds)
+        for w in range(orc.n_windows):
+            pl, _ = orc.encode(a, b, window=w, base_version=state["v"], target_version=state["v"] + 1,
+                               threads=threads)
+            rc = orc.apply(state["st"], pl, tgt, threads=threads)
+            assert rc == oracle.OK, rc
+        state["v"] += 1
+        state["dir"] ^= 1
+        return pl.size
+
+    return step
+
+
+def cpu_baseline(wl, budget_s=12.0):
+    threads = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    step = oracle_runner(wl, threads)
+    n, t0, payload = 0, time.perf_counter(), 0
+    while True:
+        payload = step()
+        n += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": round(wl.canonical_bytes * n / dt / 1e9, 4), "unit": UNIT, "cores": threads,
+            "kind": "oracle", "sample": "%d full refit steps (encode+apply) of the whole workload, "
+                                        "%.1f s" % (n, dt), "payload_bytes": payload}
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    wl = build_workload(args.workload, args.frac)
+    threads = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    step = oracle_runner(wl, threads)
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t0
+    value = wl.canonical_bytes * args.steps / dt / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "u8", "data": "synthetic",
+            "config": {"workload": WORKLOAD_NAMES[args.workload], "canonical_bytes": wl.canonical_bytes},
+            "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": threads, "kind": "oracle",
+                             "sample": "%d timed oracle refit steps of the whole workload" % args.steps},
+            "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+# --------------------------------------------------------------------------
+# GPU arm
+# --------------------------------------------------------------------------
+def run_gpu(args):
+    import torch
+
+    import bit_exact_xor_gb300 as dcr
+    from wl import descs_of
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    stream = torch.cuda.current_stream()
+
+    wl = build_workload(args.workload, args.frac)
+    N = wl.canonical_bytes
+    plan = dcr.Plan(descs_of(wl), window_bytes=wl.window_bytes)
+    plan.set_profiling(True)
+    olds, news = wl.device_arenas(torch)
+    target = torch.empty(plan.info.recv_bytes, dtype=torch.uint8, device=dev)
+    dcr.check(dcr.dense_refit(plan, olds, target))
+    nw = plan.n_windows
+    caps = [plan.window(w).payload_bound for w in range(nw)]
+    # payload buffers sized from a first encode (grown to the reported size)
+    payloads = []
+    for w in range(nw):
+        guess = max(plan.window(w).canonical_bytes // 8, 1 << 20)
+        buf = torch.empty(guess, dtype=torch.uint8, device=dev)
+        rc, size, _ = dcr.encode(plan, olds, news, buf, window=w)
+        if rc == dcr.ERR_CAPACITY:
+            buf = torch.empty(min(int(size * 1.25), caps[w]), dtype=torch.uint8, device=dev)
+        payloads.append(buf)
+    st = dcr.RecvState(plan, 0)
+    ver = [0]
+    d = [0]
+    enc_ms, app_ms, sizes, changed = [], [], [], []
+
+    def step(record):
+        a, b = (olds, news) if d[0] == 0 else (news, olds)
+        for w in range(nw):
+            rc, size, cnt = dcr.encode(plan, a, b, payloads[w], window=w, base_version=ver[0],
+                                       target_version=ver[0] + 1, counts=record)
+            dcr.check(rc)
+            p1 = plan.last_profile()
+            rc, res = dcr.apply(plan, st, payloads[w], size, target)
+            dcr.check(rc)
+            p2 = plan.last_profile()
+            if record:
+                enc_ms.append(p1.encode_ms)
+                app_ms.append(p2.apply_ms + p2.defer_ms)
+                sizes.append(size)
+                changed.append(sum(cnt))
+        ver[0] += 1
+        d[0] ^= 1
+
+    for _ in range(args.warmup):
+        step(False)
+    torch.cuda.synchronize()
+    dist_barrier(ws)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with Clocks(local) as clk:
+        torch.cuda.synchronize()
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step(True)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    dist_barrier(ws)
+    ms = ev0.elapsed_time(ev1)
+    ms_max = dist_max(ms, ws)
+    value = N * args.steps * ws / (ms_max / 1e3) / 1e9
+
+    # end to end through the public API with host buffers: H2D of old/new,
+    # encode, D2H of the payload, H2D of the payload, apply (status read inside)
+    e2e = None
+    if not args.no_e2e:
+        h_old = [x.cpu().pin_memory() for x in olds]
+        h_new = [x.cpu().pin_memory() for x in news]
+        h_pl = [torch.empty(p.numel(), dtype=torch.uint8).pin_memory() for p in payloads]
+        d_in = [torch.empty_like(x) for x in olds], [torch.empty_like(x) for x in news]
+        rx = [torch.empty_like(p) for p in payloads]
+        h2d = d2h = 0
+
+        def e2e_step():
+            nonlocal h2d, d2h
+            a, b = (h_old, h_new) if d[0] == 0 else (h_new, h_old)
+            for x, y in zip(d_in[0], a):
+                x.copy_(y, non_blocking=True)
+            for x, y in zip(d_in[1], b):
+                x.copy_(y, non_blocking=True)
+            h2d += sum(y.numel() for y in a) + sum(y.numel() for y in b)
+            for w in range(nw):
+                rc, size, _ = dcr.encode(plan, d_in[0], d_in[1], payloads[w], window=w,
+                                         base_version=ver[0], target_version=ver[0] + 1, counts=False)
+                dcr.check(rc)
+                h_pl[w][:size].copy_(payloads[w][:size], non_blocking=True)
+                rx[w][:size].copy_(h_pl[w][:size], non_blocking=True)
+                d2h += size
+                h2d += size
+                rc, res = dcr.apply(plan, st, rx[w], size, target)
+                dcr.check(rc)
+            ver[0] += 1
+            d[0] ^= 1
+
+        for _ in range(2):
+            e2e_step()
+        h2d = d2h = 0
+        torch.cuda.synchronize()
+        dist_barrier(ws)
+        k = max(2, min(args.steps, 5))
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(k):
+            e2e_step()
+        t1.record(stream)
+        torch.cuda.synchronize()
+        ems = dist_max(t0.elapsed_time(t1), ws)
+        e2e = {"value": round(N * k * ws / (ems / 1e3) / 1e9, 3), "unit": UNIT,
+               "h2d_bytes_per_step": h2d // k, "d2h_bytes_per_step": d2h // k}
+
+    # the receiver really holds the last step's target weights
+    ref = torch.empty_like(target)
+    dcr.check(dcr.dense_refit(plan, olds if d[0] == 0 else news, ref))
+    assert torch.equal(ref, target), "receiver arena differs from a dense refit"
+    del ref
+
+    P = statistics.mean(sizes)
+    peak, peak_kind = measured_peak()
+    alg_bytes = 2 * N / nw + P  # per encode launch: read old+new of the window, write payload
+    achieved = alg_bytes / (statistics.mean(enc_ms) / 1e3) / 1e9
+    traffic = ncu_traffic()
+    clocks = clk.summary()
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_max / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
+        "config": {"workload": WORKLOAD_NAMES[args.workload], "canonical_bytes": N,
+                   "tp": wl.tp, "windows": nw, "parallelism": "replicas" if ws > 1 else "single GPU",
+                   "l2": "inputs larger than L2 (2N = %.2f GB read per encode)" % (2 * N / 1e9)
+                   if 2 * N > 200e6 else "inputs fit in L2"},
+        "encode_gbs": round(N / (statistics.mean(enc_ms) * nw / 1e3) / 1e9, 3),
+        "apply_gbs": round(N / (statistics.mean(app_ms) * nw / 1e3) / 1e9, 3),
+        "encode_kernel_ms": round(statistics.mean(enc_ms), 4),
+        "apply_kernel_ms": round(statistics.mean(app_ms), 4),
+        "payload_bytes": int(P), "changed_values": int(statistics.mean(changed)),
+        "roofline": {"bound": "hbm", "kernel": "encode_kernel", "achieved": round(achieved, 1),
+                     "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "peak_source": peak_kind,
+                     "algorithmic_bytes_per_launch": int(alg_bytes)},
+        "gpu_launches": 5 * nw * args.steps,
+        "clocks": clocks,
+    }
+    if e2e:
+        line["e2e"] = e2e
+    if rank == 0 and not args.no_cpu_baseline:
+        cb = cpu_baseline(wl)
+        line["payload_vs_oracle"] = round(P / cb.pop("payload_bytes"), 4)
+        line["cpu_baseline"] = cb
+    if rank == 0:
+        print(json.dumps(line))
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--workload", default="dense", choices=sorted(WORKLOAD_NAMES))
+    ap.add_argument("--frac", type=float, default=None)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,262 @@
+"""Python binding of libdcr (bit-exact delta-compressed refit on GB300).
+
+Argument marshalling only: every step of the refit runs in the library's CUDA
+kernels.  Device buffers are passed as torch CUDA tensors (or raw integer
+device pointers); PyTorch is used for device memory and streams only.  The
+library must be built (``__graft_entry__.build()``); importing this package
+without it raises.
+"""
+import ctypes
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libdcr.so")
+
+MAX_TP = 16
+CHUNK_BYTES = 65536
+NO_FAULT = 2**64 - 1
+
+OK = 0
+ERR_INVALID, ERR_CAPACITY, ERR_CORRUPT, ERR_VERSION, ERR_ABORTED = -1, -2, -3, -4, -5
+ERR_CUDA, ERR_NOMEM, ERR_INCOMPLETE, ERR_TIMEOUT = -6, -7, -8, -9
+STATUS_NAMES = {0: "OK", -1: "INVALID", -2: "CAPACITY", -3: "CORRUPT", -4: "VERSION", -5: "ABORTED",
+                -6: "CUDA", -7: "NOMEM", -8: "INCOMPLETE", -9: "TIMEOUT"}
+
+REPLICATED, SPLIT_ROWS, SPLIT_COLS, RESIDUAL_QKV_INTERLEAVED = 0, 1, 2, 3
+LAYOUT_CANONICAL, LAYOUT_ROWGROUP_INTERLEAVE = 0, 1
+MODE_HYBRID, MODE_OVERWRITE_ONLY = 0, 1
+
+
+class DcrError(RuntimeError):
+    def __init__(self, code, msg):
+        super().__init__("%s (%d): %s" % (STATUS_NAMES.get(code, "?"), code, msg))
+        self.code = code
+
+
+class TensorDesc(ctypes.Structure):
+    _fields_ = [
+        ("name", ctypes.c_char_p),
+        ("elem_bits", ctypes.c_uint32), ("split", ctypes.c_uint32), ("tp", ctypes.c_uint32),
+        ("q_heads", ctypes.c_uint32), ("kv_heads", ctypes.c_uint32), ("head_dim", ctypes.c_uint32),
+        ("rows", ctypes.c_uint64), ("cols", ctypes.c_uint64),
+        ("shard_offset", ctypes.c_uint64 * MAX_TP),
+        ("recv_layout", ctypes.c_uint32), ("recv_group", ctypes.c_uint32),
+        ("recv_slot", ctypes.c_uint32), ("reserved", ctypes.c_uint32),
+        ("recv_offset", ctypes.c_uint64),
+    ]
+
+
+class PlanOpts(ctypes.Structure):
+    _fields_ = [("window_bytes", ctypes.c_uint64), ("reserved", ctypes.c_uint32 * 6)]
+
+
+class PlanInfo(ctypes.Structure):
+    _fields_ = [("n_tensors", ctypes.c_uint64), ("n_parts", ctypes.c_uint64),
+                ("n_chunks", ctypes.c_uint64), ("n_windows", ctypes.c_uint64),
+                ("canonical_bytes", ctypes.c_uint64), ("plan_hash", ctypes.c_uint64),
+                ("recv_bytes", ctypes.c_uint64), ("shard_bytes", ctypes.c_uint64 * MAX_TP),
+                ("tp", ctypes.c_uint32), ("reserved", ctypes.c_uint32)]
+
+
+class WindowInfo(ctypes.Structure):
+    _fields_ = [("chunk_begin", ctypes.c_uint64), ("chunk_count", ctypes.c_uint64),
+                ("canonical_bytes", ctypes.c_uint64), ("payload_bound", ctypes.c_uint64)]
+
+
+class Fault(ctypes.Structure):
+    _fields_ = [("abort_after_frames", ctypes.c_uint64), ("abort_split", ctypes.c_uint32),
+                ("reserved", ctypes.c_uint32)]
+
+
+class ApplyResult(ctypes.Structure):
+    _fields_ = [("target_version", ctypes.c_uint64), ("n_frames", ctypes.c_uint64),
+                ("frames_applied", ctypes.c_uint64), ("frames_skipped", ctypes.c_uint64),
+                ("pending", ctypes.c_uint64), ("window", ctypes.c_uint32),
+                ("committed", ctypes.c_uint32)]
+
+
+class Profile(ctypes.Structure):
+    _fields_ = [("encode_ms", ctypes.c_float), ("finalize_ms", ctypes.c_float),
+                ("apply_ms", ctypes.c_float), ("defer_ms", ctypes.c_float),
+                ("pending_ms", ctypes.c_float), ("encode_valid", ctypes.c_uint32),
+                ("apply_valid", ctypes.c_uint32)]
+
+
+EXPORTS = ["dcr_last_error", "dcr_plan_build", "dcr_plan_info_get", "dcr_window_info_get",
+           "dcr_plan_destroy", "dcr_recv_state_create", "dcr_recv_state_destroy",
+           "dcr_recv_state_version", "dcr_encode", "dcr_apply", "dcr_apply_retry",
+           "dcr_dense_refit", "dcr_plan_set_profiling", "dcr_plan_last_profile"]
+
+_lib = None
+
+
+def lib():
+    """Load libdcr.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError("libdcr.so is not built; run __graft_entry__.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        P, VP, U32, U64, SZ = ctypes.POINTER, ctypes.c_void_p, ctypes.c_uint32, ctypes.c_uint64, ctypes.c_size_t
+        L.dcr_last_error.restype = ctypes.c_char_p
+        L.dcr_plan_build.argtypes = [P(TensorDesc), SZ, P(PlanOpts), P(VP)]
+        L.dcr_plan_info_get.argtypes = [VP, P(PlanInfo)]
+        L.dcr_window_info_get.argtypes = [VP, U32, P(WindowInfo)]
+        L.dcr_plan_destroy.argtypes = [VP]
+        L.dcr_plan_destroy.restype = None
+        L.dcr_recv_state_create.argtypes = [VP, U64, P(VP)]
+        L.dcr_recv_state_destroy.argtypes = [VP]
+        L.dcr_recv_state_destroy.restype = None
+        L.dcr_recv_state_version.argtypes = [VP, P(U64)]
+        L.dcr_encode.argtypes = [VP, U32, U32, P(VP), P(VP), U64, U64, VP, SZ, P(SZ), P(U64), VP]
+        L.dcr_apply.argtypes = [VP, VP, VP, SZ, VP, P(Fault), P(ApplyResult), VP]
+        L.dcr_apply_retry.argtypes = [VP, VP, VP, SZ, VP, P(ApplyResult), VP]
+        L.dcr_dense_refit.argtypes = [VP, P(VP), VP, VP]
+        L.dcr_plan_set_profiling.argtypes = [VP, ctypes.c_int]
+        L.dcr_plan_last_profile.argtypes = [VP, P(Profile)]
+        _lib = L
+    return _lib
+
+
+def last_error():
+    return lib().dcr_last_error().decode()
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _ptr_array(xs):
+    arr = (ctypes.c_void_p * MAX_TP)()
+    for i, x in enumerate(xs):
+        arr[i] = _ptr(x)
+    return arr
+
+
+def check(rc):
+    if rc != OK:
+        raise DcrError(rc, last_error())
+    return rc
+
+
+class Plan:
+    """dcr_plan_build over a list of TensorDesc."""
+
+    def __init__(self, descs, window_bytes=0):
+        arr = (TensorDesc * len(descs))(*descs)
+        self._names = [d.name for d in descs]
+        opts = PlanOpts(window_bytes)
+        h = ctypes.c_void_p()
+        check(lib().dcr_plan_build(arr, len(descs), ctypes.byref(opts), ctypes.byref(h)))
+        self.h = h
+        self.info = PlanInfo()
+        check(lib().dcr_plan_info_get(self.h, ctypes.byref(self.info)))
+
+    @property
+    def n_windows(self):
+        return self.info.n_windows
+
+    def window(self, w):
+        wi = WindowInfo()
+        check(lib().dcr_window_info_get(self.h, w, ctypes.byref(wi)))
+        return wi
+
+    def set_profiling(self, on=True):
+        check(lib().dcr_plan_set_profiling(self.h, int(on)))
+
+    def last_profile(self):
+        p = Profile()
+        check(lib().dcr_plan_last_profile(self.h, ctypes.byref(p)))
+        return p
+
+    def close(self):
+        if getattr(self, "h", None):
+            lib().dcr_plan_destroy(self.h)
+            self.h = None
+
+    __del__ = close
+
+
+class RecvState:
+    def __init__(self, plan, version=0):
+        self.plan = plan
+        h = ctypes.c_void_p()
+        check(lib().dcr_recv_state_create(plan.h, version, ctypes.byref(h)))
+        self.h = h
+
+    @property
+    def version(self):
+        v = ctypes.c_uint64()
+        check(lib().dcr_recv_state_version(self.h, ctypes.byref(v)))
+        return v.value
+
+    def close(self):
+        if getattr(self, "h", None):
+            lib().dcr_recv_state_destroy(self.h)
+            self.h = None
+
+    __del__ = close
+
+
+def encode(plan, olds, news, payload, cap=None, window=0, mode=MODE_HYBRID, base_version=0,
+           target_version=1, counts=True, stream=None):
+    """dcr_encode.  Returns (status, payload_size, per-tensor changed counts)."""
+    size = ctypes.c_size_t()
+    n = plan.info.n_tensors
+    cnt = (ctypes.c_uint64 * n)() if counts else None
+    if cap is None:
+        cap = payload.numel() if payload is not None and not isinstance(payload, int) else 0
+    rc = lib().dcr_encode(plan.h, mode, window, _ptr_array(olds), _ptr_array(news), base_version,
+                          target_version, _ptr(payload), cap, ctypes.byref(size), cnt,
+                          _stream(stream))
+    return rc, size.value, (list(cnt) if counts else None)
+
+
+def apply(plan, state, payload, size, target, fault=None, stream=None):
+    """dcr_apply.  fault = (abort_after_frames, abort_split) or None.
+    Returns (status, ApplyResult)."""
+    res = ApplyResult()
+    f = None
+    if fault is not None:
+        f = ctypes.byref(Fault(fault[0], fault[1], 0))
+    rc = lib().dcr_apply(plan.h, state.h, _ptr(payload), size, _ptr(target), f, ctypes.byref(res),
+                         _stream(stream))
+    return rc, res
+
+
+def apply_retry(plan, state, payload, size, target, stream=None):
+    res = ApplyResult()
+    rc = lib().dcr_apply_retry(plan.h, state.h, _ptr(payload), size, _ptr(target), ctypes.byref(res),
+                               _stream(stream))
+    return rc, res
+
+
+def dense_refit(plan, shards, target, stream=None):
+    return lib().dcr_dense_refit(plan.h, _ptr_array(shards), _ptr(target), _stream(stream))
+
+
+def make_desc(name, elem_bits, rows, cols, split, tp, shard_offset, recv_offset, q_heads=0, kv_heads=0,
+              head_dim=0, recv_layout=LAYOUT_CANONICAL, recv_group=0, recv_slot=0):
+    d = TensorDesc()
+    d.name = name.encode() if isinstance(name, str) else name
+    d.elem_bits, d.split, d.tp = elem_bits, split, tp
+    d.q_heads, d.kv_heads, d.head_dim = q_heads, kv_heads, head_dim
+    d.rows, d.cols = rows, cols
+    for i, o in enumerate(shard_offset):
+        d.shard_offset[i] = o
+    d.recv_layout, d.recv_group, d.recv_slot = recv_layout, recv_group, recv_slot
+    d.recv_offset = recv_offset
+    return d

@@ -1,0 +1,571 @@
+// Receiver hot path: decode the frames of one window's stream and apply them
+// in place to the receiver arena through the plan's canonical->receiver
+// pieces, with per-chunk dedup, an overwrite-only retry mode, test-only fault
+// injection and the commit check.
+//
+// Method: NeMo-DCR paper summary, "Recoverable in-place apply" (XOR masks
+// flip the stored bits in place, overwrite records replace values, partial
+// writes are retried, joint commit); popular write-up, sections on XOR versus
+// overwrite, dedup by unique IDs, in-place apply without a backup copy and
+// overwrite-only retry; "GPU-accelerated weight teleportation", "A strong
+// baseline with the Blackwell-native DE" (one launch applies XOR to the whole
+// model from a host-prepared plan) and "Working with low-precision RL" (the
+// mask is remapped like the physical layout).
+//
+// Kernels:
+//   apply_kernel  one warp per frame.  XOR_RAW, OVERWRITE and OVERWRITE_DENSE
+//                 frames are applied lane-parallel.  LZ4 frames flagged ZSRC
+//                 (every match copies zero bytes, as the library's encoder
+//                 produces) are parsed by the warp in lock-step: only literal
+//                 bytes can be non-zero, so they are XORed straight into the
+//                 receiver arena and nothing is materialised; a bitmap of the
+//                 non-zero output bytes checks the ZSRC promise of every match.
+//   defer_kernel  one CTA per remaining LZ4 frame (any valid block, e.g. from
+//                 the CPU oracle): full decode into a 64 KiB shared buffer with
+//                 warp-parallel literal and match copies, then the XOR sweep.
+//   pending_kernel  counts framed chunks that are not DONE for the target
+//                 version (the commit rule).
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "dcr_internal.h"
+
+namespace dcr {
+namespace {
+
+constexpr int kAThreads = 256;
+constexpr int kAWarps = kAThreads / 32;
+constexpr int kBodyCache = 6144;            // bytes of LZ4 body cached per warp
+constexpr int kBitWords = kChunk / 32;      // non-zero output bitmap per warp
+constexpr int kDThreads = 256;
+constexpr uint32_t kCasLimit = 1u << 16;
+
+struct ApplyArgs {
+    const ChunkDesc* chunks;
+    const Seg* dst;
+    const uint64_t* win;
+    uint32_t n_windows;
+    int retry_only;
+    const uint8_t* payload;
+    uint64_t size;
+    uint8_t* target;
+    unsigned long long* state;
+    ApplyScratch* sc;
+    uint32_t* defer;
+    uint64_t plan_hash;
+    uint64_t version;
+    uint64_t abort_at;
+    uint32_t split;
+};
+
+struct Hdr {
+    uint64_t hash, base_v, target_v, n_frames, total, idx_off;
+    uint32_t window, flags, chunk_begin, chunk_count;
+};
+
+struct __align__(16) ASmem {
+    uint32_t bits[kAWarps][kBitWords];
+    uint8_t body[kAWarps][kBodyCache + 16];
+    Hdr hdr;
+    int ok;
+};
+
+__device__ __forceinline__ uint64_t ld64(const uint8_t* p)
+{
+    return *reinterpret_cast<const uint64_t*>(p);
+}
+
+__device__ __forceinline__ uint4 ld_nc16(const uint8_t* p)
+{
+    return __ldg(reinterpret_cast<const uint4*>(p));
+}
+
+__device__ __forceinline__ bool is_zero(uint4 v) { return (v.x | v.y | v.z | v.w) == 0; }
+
+// Stream header check, in the order: malformed -> plan/window mismatch ->
+// retry-mode mismatch -> version mismatch.  Returns 0 or a dcr_status.
+__device__ int check_header(const ApplyArgs& A, Hdr* h)
+{
+    const uint8_t* p = A.payload;
+    uint32_t magic = *reinterpret_cast<const uint32_t*>(p);
+    uint32_t fmt = *reinterpret_cast<const uint32_t*>(p + 4);
+    h->hash = ld64(p + 8);
+    h->base_v = ld64(p + 16);
+    h->target_v = ld64(p + 24);
+    h->window = *reinterpret_cast<const uint32_t*>(p + 32);
+    h->flags = *reinterpret_cast<const uint32_t*>(p + 36);
+    h->chunk_begin = *reinterpret_cast<const uint32_t*>(p + 40);
+    h->chunk_count = *reinterpret_cast<const uint32_t*>(p + 44);
+    h->n_frames = ld64(p + 48);
+    h->total = ld64(p + 56);
+    if (magic != kStreamMagic || fmt != kFormat || h->total > A.size || h->total < kStreamHdr ||
+        h->total % 8 || h->n_frames > (h->total - kStreamHdr) / 8)
+        return DCR_ERR_CORRUPT;
+    h->idx_off = h->total - 8 * h->n_frames;
+    if (h->hash != A.plan_hash || h->window >= A.n_windows ||
+        h->chunk_begin != A.win[h->window] ||
+        h->chunk_count != A.win[h->window + 1] - A.win[h->window])
+        return DCR_ERR_INVALID;
+    if (A.retry_only && !(h->flags & kStreamOverwriteOnly)) return DCR_ERR_INVALID;
+    if (h->base_v != A.version) return DCR_ERR_VERSION;
+    return 0;
+}
+
+__device__ __forceinline__ void report(ApplyScratch* sc, int code)
+{
+    atomicCAS(&sc->err, 0, code);
+}
+
+// receiver arena offset of canonical chunk byte x
+__device__ __forceinline__ uint64_t dst_of(const Seg* s, uint32_t n, uint32_t x)
+{
+    if (n == 1) return s[0].addr + (x - s[0].off);
+    int lo = 0, hi = int(n) - 1;
+    while (lo < hi) {
+        int mid = (lo + hi + 1) >> 1;
+        if (s[mid].off <= x) lo = mid;
+        else hi = mid - 1;
+    }
+    return s[lo].addr + (x - s[lo].off);
+}
+
+__device__ __forceinline__ void xor_byte(uint8_t* target, uint64_t a, uint32_t b)
+{
+    uintptr_t p = reinterpret_cast<uintptr_t>(target + a);
+    atomicXor(reinterpret_cast<unsigned*>(p & ~uintptr_t(3)), b << (8 * (p & 3)));
+}
+
+// XOR one 16-byte mask vector at canonical chunk offset x (bytes >= lim skipped)
+__device__ __forceinline__ void xor_vec(const ApplyArgs& A, const ChunkDesc& cd, const Seg* ds,
+                                        uint32_t x, uint4 m, uint32_t lim)
+{
+    if ((cd.flags & kDstVec) && x + 16 <= lim) {
+        uint4* d = reinterpret_cast<uint4*>(A.target + dst_of(ds, cd.dst_count, x));
+        uint4 t = *d;
+        *d = make_uint4(t.x ^ m.x, t.y ^ m.y, t.z ^ m.z, t.w ^ m.w);
+        return;
+    }
+    const uint32_t w[4] = {m.x, m.y, m.z, m.w};
+    for (int i = 0; i < 16; ++i) {
+        uint32_t b = (w[i >> 2] >> (8 * (i & 3))) & 0xFFu;
+        if (b && x + i < lim) xor_byte(A.target, dst_of(ds, cd.dst_count, x + i), b);
+    }
+}
+
+__device__ __forceinline__ void put_vec(const ApplyArgs& A, const ChunkDesc& cd, const Seg* ds,
+                                        uint32_t x, uint4 v, uint32_t lim, uint32_t raw)
+{
+    if ((cd.flags & kDstVec) && x + 16 <= lim) {
+        *reinterpret_cast<uint4*>(A.target + dst_of(ds, cd.dst_count, x)) = v;
+        return;
+    }
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    for (int i = 0; i < 16; ++i)
+        if (x + i < lim && x + i < raw)
+            A.target[dst_of(ds, cd.dst_count, x + i)] = uint8_t(w[i >> 2] >> (8 * (i & 3)));
+}
+
+// claim a chunk for target version V: true if this frame may apply its mask
+__device__ bool claim(unsigned long long* st, uint64_t V, bool* timeout)
+{
+    unsigned long long cur = *reinterpret_cast<volatile unsigned long long*>(st);
+    const unsigned long long want = (V << 2) | kClaimed;
+    for (uint32_t i = 0; i < kCasLimit; ++i) {
+        if ((cur >> 2) == V && (cur & 3) != kNotStarted) return false;
+        unsigned long long seen = atomicCAS(st, cur, want);
+        if (seen == cur) return true;
+        cur = seen;
+    }
+    *timeout = true;
+    return false;
+}
+
+// ---- warp-level LZ4 (ZSRC) decode fused with the XOR --------------------
+// Returns true if the block is well formed and kept its ZSRC promise.
+__device__ bool zsrc_decode_apply(const ApplyArgs& A, const ChunkDesc& cd, const Seg* ds,
+                                  const uint8_t* src, uint32_t n, uint32_t raw, uint32_t lim,
+                                  uint32_t* bits, int lane)
+{
+    for (uint32_t w = lane; w < (raw + 31) / 32; w += 32) bits[w] = 0;
+    __syncwarp();
+    uint32_t ip = 0, op = 0;
+    for (;;) {
+        if (ip >= n) return false;
+        const uint32_t tok = src[ip++];
+        uint32_t ll = tok >> 4;
+        if (ll == 15) {
+            for (;;) {
+                if (ip >= n) return false;
+                uint32_t b = src[ip++];
+                ll += b;
+                if (b != 255) break;
+            }
+        }
+        if (ll > n - ip || ll > raw - op) return false;
+        for (uint32_t i = lane; i < ll; i += 32) {
+            uint32_t b = src[ip + i];
+            if (b) {
+                uint32_t x = op + i;
+                atomicOr(&bits[x >> 5], 1u << (x & 31));
+                if (x < lim) xor_byte(A.target, dst_of(ds, cd.dst_count, x), b);
+            }
+        }
+        __syncwarp();
+        ip += ll;
+        op += ll;
+        if (ip == n) break;
+        if (n - ip < 2) return false;
+        const uint32_t off = uint32_t(src[ip]) | (uint32_t(src[ip + 1]) << 8);
+        ip += 2;
+        if (off == 0 || off > op) return false;
+        uint32_t ml = tok & 15u;
+        if (ml == 15) {
+            for (;;) {
+                if (ip >= n) return false;
+                uint32_t b = src[ip++];
+                ml += b;
+                if (b != 255) break;
+            }
+        }
+        ml += 4;
+        if (ml > raw - op) return false;
+        // the copy source [op - off, op - off + min(ml, off)) must be all zero
+        const uint32_t s = op - off, e = s + (ml < off ? ml : off);
+        bool viol = false;
+        for (uint32_t w = (s >> 5) + lane; w <= ((e - 1) >> 5); w += 32) {
+            uint32_t a = (w << 5) > s ? 0u : s - (w << 5);
+            uint32_t b = ((w + 1) << 5) < e ? 32u : e - (w << 5);
+            uint32_t m = (b == 32 ? 0xFFFFFFFFu : ((1u << b) - 1)) & ~((1u << a) - 1);
+            viol |= (bits[w] & m) != 0;
+        }
+        if (__any_sync(0xffffffffu, viol)) return false;
+        op += ml;
+    }
+    return op == raw;
+}
+
+// ================================================================ kernels ==
+__global__ void __launch_bounds__(kAThreads) apply_kernel(ApplyArgs A)
+{
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    ASmem& S = *reinterpret_cast<ASmem*>(smem_raw);
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    if (threadIdx.x == 0) {
+        int rc = check_header(A, &S.hdr);
+        S.ok = rc == 0;
+        if (rc) report(A.sc, rc);
+        else if (blockIdx.x == 0) {
+            A.sc->hdr_ok = 1;
+            A.sc->target_version = S.hdr.target_v;
+            A.sc->window = S.hdr.window;
+            A.sc->n_frames = S.hdr.n_frames;
+        }
+    }
+    __syncthreads();
+    if (!S.ok) return;
+    const Hdr H = S.hdr;
+    const uint64_t V = H.target_v;
+    uint32_t* bits = S.bits[wid];
+    uint8_t* cache = S.body[wid];
+
+    for (;;) {
+        uint32_t f = 0;
+        if (lane == 0) f = atomicAdd(&A.sc->frame_ticket, 1u);
+        f = __shfl_sync(0xffffffffu, f, 0);
+        if (f >= H.n_frames) break;
+        const uint64_t fo = ld64(A.payload + H.idx_off + 8ull * f);
+        if (fo < kStreamHdr || fo % 16 || fo + kFrameHdr > H.idx_off) {
+            if (lane == 0) report(A.sc, DCR_ERR_CORRUPT);
+            continue;
+        }
+        const uint4 h0 = ld_nc16(A.payload + fo), h1 = ld_nc16(A.payload + fo + 16);
+        const uint32_t kind = h0.y & 0xFFu, fbits = (h0.y >> 8) & 0xFFu, fflags = h0.y >> 16;
+        const uint32_t c = h0.z, raw = h0.w, bl = h1.x;
+        if (h0.x != kFrameMagic || kind < kXorLz4 || kind > kOverwriteDense || c < H.chunk_begin ||
+            c >= H.chunk_begin + H.chunk_count || bl > H.idx_off - fo - kFrameHdr) {
+            if (lane == 0) report(A.sc, DCR_ERR_CORRUPT);
+            continue;
+        }
+        const ChunkDesc cd = A.chunks[c];
+        if (raw != cd.raw_len || fbits != cd.bits) {
+            if (lane == 0) report(A.sc, DCR_ERR_CORRUPT);
+            continue;
+        }
+        const bool is_xor = kind == kXorLz4 || kind == kXorRaw;
+        if (A.retry_only && is_xor) {
+            if (lane == 0) report(A.sc, DCR_ERR_INVALID);
+            continue;
+        }
+        if (uint64_t(f) > A.abort_at) continue;  // injected fault: never reached
+        const bool cut = uint64_t(f) == A.abort_at;
+        const uint32_t ub = cd.bits == 16 ? 2u : 1u;
+        uint32_t lim = cut ? (A.split < raw ? A.split : raw) : raw;
+        lim -= lim % ub;
+        unsigned long long* st = &A.state[c];
+        if (is_xor) {
+            int got = 0;
+            if (lane == 0) {
+                bool to = false;
+                got = claim(st, V, &to);
+                if (to) report(A.sc, DCR_ERR_TIMEOUT);
+                if (!got && !to) atomicAdd(&A.sc->skipped, 1ull);
+            }
+            if (!__shfl_sync(0xffffffffu, got, 0)) continue;
+            if (kind == kXorLz4 && !(fflags & kFrameZsrc)) {
+                if (lane == 0) A.defer[atomicAdd(&A.sc->n_defer, 1u)] = f;
+                continue;
+            }
+        }
+        const Seg* ds = A.dst + cd.dst_begin;
+        const uint8_t* body = A.payload + fo + kFrameHdr;
+        bool good = true;
+        if (kind == kXorRaw) {
+            good = bl == raw;
+            if (good) {
+                for (uint32_t v = lane; v < raw / 16; v += 32) {
+                    uint4 m = ld_nc16(body + 16 * v);
+                    if (!is_zero(m)) xor_vec(A, cd, ds, 16 * v, m, lim);
+                }
+                for (uint32_t x = (raw & ~15u) + lane; x < raw; x += 32)
+                    if (body[x] && x < lim) xor_byte(A.target, dst_of(ds, cd.dst_count, x), body[x]);
+            }
+        } else if (kind == kXorLz4) {
+            const uint8_t* src = body;
+            if (bl <= uint32_t(kBodyCache)) {
+                for (uint32_t v = lane; v < bl / 16; v += 32)
+                    reinterpret_cast<uint4*>(cache)[v] = ld_nc16(body + 16 * v);
+                for (uint32_t x = (bl & ~15u) + lane; x < bl; x += 32) cache[x] = body[x];
+                __syncwarp();
+                src = cache;
+            }
+            good = zsrc_decode_apply(A, cd, ds, src, bl, raw, lim, bits, lane);
+        } else if (kind == kOverwriteDense) {
+            good = bl == raw;
+            if (good) {
+                for (uint32_t v = lane; v < raw / 16; v += 32)
+                    put_vec(A, cd, ds, 16 * v, ld_nc16(body + 16 * v), lim, raw);
+                for (uint32_t x = (raw & ~15u) + lane; x < raw; x += 32)
+                    if (x < lim) A.target[dst_of(ds, cd.dst_count, x)] = body[x];
+            }
+        } else {
+            // OVERWRITE records: n, ascending unit offsets, pad, values
+            uint32_t cnt = bl >= 4 ? *reinterpret_cast<const uint32_t*>(body) : 0u;
+            uint64_t pad = (4 - (2ull * cnt) % 4) % 4;
+            good = bl >= 4 && 4 + 2ull * cnt + pad + uint64_t(cnt) * ub == bl;
+            const uint16_t* offs = reinterpret_cast<const uint16_t*>(body + 4);
+            const uint8_t* vals = body + 4 + 2 * cnt + pad;
+            if (good) {
+                bool bad = false;
+                for (uint32_t i = lane; i < cnt; i += 32) {
+                    uint32_t u = offs[i];
+                    bad |= (u + 1) * ub > raw || (i && u <= offs[i - 1]);
+                }
+                good = !__any_sync(0xffffffffu, bad);
+            }
+            if (good) {
+                for (uint32_t i = lane; i < cnt; i += 32) {
+                    uint32_t x = uint32_t(offs[i]) * ub;
+                    if (x >= lim) continue;
+                    uint64_t a = dst_of(ds, cd.dst_count, x);
+                    if (ub == 2 && (a & 1) == 0 && dst_of(ds, cd.dst_count, x + 1) == a + 1)
+                        *reinterpret_cast<uint16_t*>(A.target + a) =
+                            uint16_t(vals[2 * i] | (uint32_t(vals[2 * i + 1]) << 8));
+                    else
+                        for (uint32_t e = 0; e < ub; ++e)
+                            A.target[dst_of(ds, cd.dst_count, x + e)] = vals[i * ub + e];
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) {
+            if (!good) {
+                report(A.sc, DCR_ERR_CORRUPT);
+            } else {
+                atomicAdd(&A.sc->applied, 1ull);
+                __threadfence();
+                if (cut) {
+                    A.sc->aborted = 1;
+                    if (!is_xor) atomicExch(st, (V << 2) | kClaimed);
+                } else {
+                    atomicExch(st, (V << 2) | kDone);
+                }
+            }
+        }
+    }
+}
+
+// General LZ4 frames (no ZSRC promise): full decode in shared memory.
+__global__ void __launch_bounds__(kDThreads) defer_kernel(ApplyArgs A)
+{
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    uint8_t* out = smem_raw;                       // kChunk bytes
+    __shared__ uint32_t s_f, s_good;
+    if (!A.sc->hdr_ok) return;
+    const uint8_t* p = A.payload;
+    const uint64_t total = ld64(p + 56), nf = ld64(p + 48), idx_off = total - 8 * nf;
+    const uint64_t V = ld64(p + 24);
+    const int lane = threadIdx.x & 31;
+    for (;;) {
+        if (threadIdx.x == 0) {
+            uint32_t j = atomicAdd(&A.sc->defer_ticket, 1u);
+            s_f = j < *reinterpret_cast<volatile uint32_t*>(&A.sc->n_defer) ? A.defer[j] : UINT32_MAX;
+        }
+        __syncthreads();
+        const uint32_t f = s_f;
+        if (f == UINT32_MAX) break;
+        const uint64_t fo = ld64(p + idx_off + 8ull * f);
+        const uint4 h0 = ld_nc16(p + fo), h1 = ld_nc16(p + fo + 16);
+        const uint32_t c = h0.z, raw = h0.w, n = h1.x;
+        const ChunkDesc cd = A.chunks[c];
+        const bool cut = uint64_t(f) == A.abort_at;
+        const uint32_t ub = cd.bits == 16 ? 2u : 1u;
+        uint32_t lim = cut ? (A.split < raw ? A.split : raw) : raw;
+        lim -= lim % ub;
+        const uint8_t* src = p + fo + kFrameHdr;
+        if (threadIdx.x < 32) {
+            bool good = false;
+            uint32_t ip = 0, op = 0;
+            for (;;) {
+                if (ip >= n) break;
+                const uint32_t tok = src[ip++];
+                uint32_t ll = tok >> 4;
+                bool ok = true;
+                if (ll == 15) {
+                    for (;;) {
+                        if (ip >= n) { ok = false; break; }
+                        uint32_t b = src[ip++];
+                        ll += b;
+                        if (b != 255) break;
+                    }
+                }
+                if (!ok || ll > n - ip || ll > raw - op) break;
+                for (uint32_t i = lane; i < ll; i += 32) out[op + i] = src[ip + i];
+                __syncwarp();
+                ip += ll;
+                op += ll;
+                if (ip == n) { good = op == raw; break; }
+                if (n - ip < 2) break;
+                const uint32_t off = uint32_t(src[ip]) | (uint32_t(src[ip + 1]) << 8);
+                ip += 2;
+                if (off == 0 || off > op) break;
+                uint32_t ml = tok & 15u;
+                if (ml == 15) {
+                    for (;;) {
+                        if (ip >= n) { ok = false; break; }
+                        uint32_t b = src[ip++];
+                        ml += b;
+                        if (b != 255) break;
+                    }
+                }
+                ml += 4;
+                if (!ok || ml > raw - op) break;
+                // forward copy semantics: the output repeats with period off
+                for (uint32_t i = lane; i < ml; i += 32) out[op + i] = out[op - off + (i % off)];
+                __syncwarp();
+                op += ml;
+            }
+            if (lane == 0) s_good = good;
+        }
+        __syncthreads();
+        if (s_good) {
+            const Seg* ds = A.dst + cd.dst_begin;
+            for (uint32_t v = threadIdx.x; v < raw / 16; v += kDThreads) {
+                uint4 m = reinterpret_cast<const uint4*>(out)[v];
+                if (!is_zero(m)) xor_vec(A, cd, ds, 16 * v, m, lim);
+            }
+            for (uint32_t x = (raw & ~15u) + threadIdx.x; x < raw; x += kDThreads)
+                if (out[x] && x < lim) xor_byte(A.target, dst_of(ds, cd.dst_count, x), out[x]);
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            if (!s_good) {
+                report(A.sc, DCR_ERR_CORRUPT);
+            } else {
+                atomicAdd(&A.sc->applied, 1ull);
+                __threadfence();
+                if (cut) A.sc->aborted = 1;
+                else atomicExch(&A.state[c], (V << 2) | kDone);
+            }
+        }
+        __syncthreads();
+    }
+}
+
+// Commit rule: every chunk with a frame in the stream is DONE for the target.
+__global__ void pending_kernel(ApplyArgs A)
+{
+    if (!A.sc->hdr_ok) return;
+    const uint8_t* p = A.payload;
+    const uint64_t total = ld64(p + 56), nf = ld64(p + 48), idx_off = total - 8 * nf;
+    const uint64_t V = ld64(p + 24);
+    const uint32_t cb = *reinterpret_cast<const uint32_t*>(p + 40);
+    const uint32_t cc = *reinterpret_cast<const uint32_t*>(p + 44);
+    unsigned long long pend = 0;
+    for (uint64_t f = blockIdx.x * uint64_t(blockDim.x) + threadIdx.x; f < nf;
+         f += uint64_t(gridDim.x) * blockDim.x) {
+        uint64_t fo = ld64(p + idx_off + 8 * f);
+        if (fo < kStreamHdr || fo % 16 || fo + kFrameHdr > idx_off) { ++pend; continue; }
+        uint32_t c = *reinterpret_cast<const uint32_t*>(p + fo + 8);
+        if (c < cb || c >= cb + cc) { ++pend; continue; }
+        if (*reinterpret_cast<volatile unsigned long long*>(&A.state[c]) != ((V << 2) | kDone)) ++pend;
+    }
+    pend = __reduce_add_sync(0xffffffffu, unsigned(pend));
+    if ((threadIdx.x & 31) == 0 && pend) atomicAdd(&A.sc->pending, pend);
+}
+
+}  // namespace
+
+int apply_kernel_config(KernelConfig* kc)
+{
+    cudaError_t e = cudaFuncSetAttribute(apply_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         int(sizeof(ASmem)));
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(defer_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kChunk));
+    if (e == cudaSuccess)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&kc->apply_blocks_per_sm, apply_kernel, kAThreads,
+                                                          sizeof(ASmem));
+    if (e == cudaSuccess)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&kc->defer_blocks_per_sm, defer_kernel, kDThreads,
+                                                          kChunk);
+    if (e != cudaSuccess) return cuda_error(e, "apply kernel configuration");
+    if (kc->apply_blocks_per_sm < 1) kc->apply_blocks_per_sm = 1;
+    if (kc->defer_blocks_per_sm < 1) kc->defer_blocks_per_sm = 1;
+    return DCR_OK;
+}
+
+int apply_launch(const dcr_plan* P, dcr_recv_state* st, const void* payload, size_t size, void* target,
+                 uint64_t abort_at, uint32_t split, int retry_only, cudaStream_t s)
+{
+    ApplyArgs A{};
+    A.chunks = P->d_chunks;
+    A.dst = P->d_dst;
+    A.win = P->d_win;
+    A.n_windows = uint32_t(P->win_start.size() - 1);
+    A.retry_only = retry_only;
+    A.payload = static_cast<const uint8_t*>(payload);
+    A.size = size;
+    A.target = static_cast<uint8_t*>(target);
+    A.state = reinterpret_cast<unsigned long long*>(st->d_chunk_state);
+    A.sc = st->d_scratch;
+    A.defer = st->d_defer;
+    A.plan_hash = P->hash;
+    A.version = st->version;
+    A.abort_at = abort_at;
+    A.split = split;
+    cudaError_t e = cudaMemsetAsync(st->d_scratch, 0, sizeof(ApplyScratch), s);
+    if (e != cudaSuccess) return cuda_error(e, "apply scratch reset");
+    const int sms = P->kc.num_sms;
+    if (P->profiling) cudaEventRecord(P->ev[3], s);
+    apply_kernel<<<sms * P->kc.apply_blocks_per_sm, kAThreads, sizeof(ASmem), s>>>(A);
+    if (P->profiling) cudaEventRecord(P->ev[4], s);
+    defer_kernel<<<sms * P->kc.defer_blocks_per_sm, kDThreads, kChunk, s>>>(A);
+    if (P->profiling) cudaEventRecord(P->ev[5], s);
+    pending_kernel<<<sms, 256, 0, s>>>(A);
+    if (P->profiling) cudaEventRecord(P->ev[6], s);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_error(e, "apply launch");
+    return DCR_OK;
+}
+
+}  // namespace dcr

@@ -1,0 +1,164 @@
+// Internal definitions shared by the DCR library's host plan builder and its
+// CUDA kernels (not part of the public C ABI in include/dcr.h).
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <string>
+#include <vector>
+
+#include "../../include/dcr.h"
+
+namespace dcr {
+
+constexpr uint32_t kChunk = DCR_CHUNK_BYTES;
+constexpr uint32_t kStreamHdr = DCR_STREAM_HEADER_BYTES;
+constexpr uint32_t kFrameHdr = DCR_FRAME_HEADER_BYTES;
+constexpr uint32_t kStreamMagic = 0x53524344u;  // "DCRS"
+constexpr uint32_t kFrameMagic = 0x46524344u;   // "DCRF"
+constexpr uint32_t kFormat = 1;
+constexpr uint32_t kStreamOverwriteOnly = 1;
+constexpr uint32_t kFrameZsrc = 1;  // every LZ4 match copies zero bytes
+enum FrameKind : uint32_t { kXorLz4 = 1, kXorRaw = 2, kOverwrite = 3, kOverwriteDense = 4 };
+
+// One contiguous piece of a chunk: canonical bytes [off, off + len) of the
+// chunk map to `addr`.  Sender pieces: addr = shard << 56 | byte offset in
+// that shard's arena.  Receiver pieces: byte offset in the receiver arena.
+struct Seg {
+    uint32_t off;
+    uint32_t len;
+    uint64_t addr;
+};
+constexpr int kShardShift = 56;
+constexpr uint64_t kAddrMask = (1ull << kShardShift) - 1;
+
+enum ChunkFlags : uint32_t {
+    kSrcVec = 1,  // every sender piece 16-byte aligned (offset, length, address)
+    kDstVec = 2,  // every receiver piece 16-byte aligned
+};
+
+struct ChunkDesc {
+    uint32_t src_begin, src_count;
+    uint32_t dst_begin, dst_count;
+    uint32_t raw_len;
+    uint32_t tensor;     // index of the tensor descriptor (changed counts)
+    uint32_t bits;       // 16, 8 or 4
+    uint32_t flags;      // ChunkFlags | residual << 8
+};
+constexpr uint32_t kResidualFlag = 1u << 8;
+
+// Look-back record of one chunk of the window being encoded:
+// bits 62-63 status (1 aggregate, 2 inclusive prefix), bits 40-61 frame
+// count, bits 0-39 frame bytes.  Sums of both fields stay in range for a
+// window of at most 256 GiB (2^22 chunks, < 2^40 frame bytes).
+constexpr uint64_t kLbAgg = 1ull << 62;
+constexpr uint64_t kLbInc = 2ull << 62;
+constexpr uint64_t kLbValMask = (1ull << 62) - 1;
+constexpr int kLbFrameShift = 40;
+constexpr uint64_t kLbByteMask = (1ull << kLbFrameShift) - 1;
+constexpr uint64_t kMaxWindowBytes = 256ull << 30;
+
+// Device scratch of one encode call (reset by a memset per call).
+struct EncScratch {
+    uint32_t ticket;
+    int32_t err;
+    uint64_t total;     // stream bytes
+    uint64_t n_frames;
+    uint64_t changed;   // changed elements in the window
+};
+
+// Device scratch of one apply call (reset by a memset per call).
+struct ApplyScratch {
+    int32_t err;
+    uint32_t hdr_ok;
+    uint32_t frame_ticket;
+    uint32_t n_defer;
+    uint32_t defer_ticket;
+    uint32_t aborted;
+    uint32_t window;
+    uint32_t pad;
+    unsigned long long applied;
+    unsigned long long skipped;
+    unsigned long long pending;
+    uint64_t target_version;
+    uint64_t n_frames;
+};
+
+// Chunk state of a receiver: (target_version << 2) | state.
+enum ChunkState : uint64_t { kNotStarted = 0, kClaimed = 1, kDone = 2 };
+
+struct Part {
+    uint32_t desc, sub, residual, bits;
+    uint64_t rows, cols, bytes, recv_off;
+    uint64_t chunk0, nchunks;
+};
+
+struct KernelConfig {
+    int num_sms = 0;
+    int enc_blocks_per_sm = 0;
+    int apply_blocks_per_sm = 0;
+    int defer_blocks_per_sm = 0;
+};
+
+// host entry points of the kernel translation units
+int encode_launch(const struct ::dcr_plan* plan, uint32_t mode, uint32_t window,
+                  const void* const* olds, const void* const* news, uint64_t base_version,
+                  uint64_t target_version, void* payload, size_t cap, cudaStream_t s);
+int encode_kernel_config(KernelConfig* kc);
+int apply_kernel_config(KernelConfig* kc);
+int apply_launch(const struct ::dcr_plan* plan, struct ::dcr_recv_state* st, const void* payload,
+                 size_t size, void* target, uint64_t abort_at, uint32_t split, int retry_only,
+                 cudaStream_t s);
+int dense_launch(const struct ::dcr_plan* plan, const void* const* shards, void* target,
+                 cudaStream_t s);
+
+int set_error(int code, const char* fmt, ...);
+int cuda_error(cudaError_t e, const char* what);
+
+}  // namespace dcr
+
+struct dcr_plan {
+    std::vector<dcr_tensor_desc> descs;
+    std::vector<std::string> names;
+    std::vector<dcr::Part> parts;
+    std::vector<dcr::ChunkDesc> chunks;
+    std::vector<uint64_t> win_start;  // n_windows + 1 chunk ids
+    uint64_t window_bytes = 0;
+    uint64_t n_chunks = 0;
+    uint64_t canonical_bytes = 0;
+    uint64_t hash = 0;
+    uint64_t recv_bytes = 0;
+    uint64_t shard_bytes[DCR_MAX_TP] = {};
+    uint32_t tp = 1;
+    uint64_t max_window_chunks = 0;
+    int device = 0;
+    dcr::KernelConfig kc;
+    // device tables
+    dcr::ChunkDesc* d_chunks = nullptr;
+    dcr::Seg* d_src = nullptr;
+    dcr::Seg* d_dst = nullptr;
+    uint64_t* d_win = nullptr;         // n_windows + 1 chunk ids
+    uint64_t n_src = 0, n_dst = 0;
+    // encode scratch: [EncScratch][u64 counts[n_tensors]] then lb[], fsize[]
+    void* d_enc = nullptr;
+    size_t enc_head_bytes = 0;
+    uint64_t* d_lb = nullptr;
+    uint32_t* d_fsize = nullptr;
+    void* h_enc = nullptr;  // pinned mirror of the scratch head
+    // kernel timing (dcr_plan_set_profiling)
+    bool profiling = false;
+    cudaEvent_t ev[8] = {};
+    mutable dcr_profile prof = {};
+};
+
+struct dcr_recv_state {
+    const dcr_plan* plan = nullptr;
+    uint64_t version = 0;
+    uint64_t pending = ~0ull;
+    std::vector<uint8_t> win_done;
+    uint64_t* d_chunk_state = nullptr;  // n_chunks
+    dcr::ApplyScratch* d_scratch = nullptr;
+    uint32_t* d_defer = nullptr;        // max_window_chunks
+    dcr::ApplyScratch* h_scratch = nullptr;  // pinned
+};

@@ -1,0 +1,258 @@
+/*
+ * dcr.h — bit-exact delta-compressed refit (DCR) of model weights on GB300.
+ *
+ * The method (NeMo-DCR paper summary, "Method"; popular write-up, sections on
+ * canonical coordinates, shard owners and XOR versus overwrite; paper
+ * abstract; "GPU-accelerated weight teleportation", sections "Delta update
+ * algebra", "A strong baseline with the Blackwell-native DE" and "Working
+ * with low-precision RL"):
+ *   sender:   mask = old XOR new over the raw stored bits of every trainer
+ *             shard, changed stored values counted bitwise, shard data
+ *             projected into canonical checkpoint coordinates by fixed affine
+ *             maps, masks LZ4-block encoded, non-affine pieces (fused QKV)
+ *             sent as overwrite records;
+ *   receiver: frames decoded and applied in place through a precomputed plan
+ *             (XOR or overwrite), per-chunk dedup so no mask lands twice, an
+ *             idempotent overwrite-only retry, and a commit that binds the new
+ *             version as the base of the next delta.
+ *
+ * Conventions for every entry point:
+ *   - Return value is a dcr_status (0 = DCR_OK, negative = error).  No call
+ *     aborts, exits or traps; dcr_last_error() gives the calling thread's
+ *     message for the last failure.
+ *   - Device buffers are plain CUDA device pointers owned by the caller; the
+ *     library never frees them.  Shard arenas, the receiver arena and the
+ *     payload must be 16-byte aligned.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Work is stream-ordered; dcr_encode, dcr_apply and
+ *     dcr_apply_retry end with one small device-to-host status read and a
+ *     synchronisation of `stream`, so their outputs (sizes, counts, status,
+ *     version) are final when they return.
+ *   - A plan's scratch (look-back state, counters) and a receiver state's
+ *     scratch are shared by every call that uses them: calls on one plan, or
+ *     on one receiver state, must not overlap in time.
+ *
+ * Wire format of a stream (one per window; little-endian):
+ *   header (64 B): "DCRS", u32 format=1, u64 plan_hash, u64 base_version,
+ *     u64 target_version, u32 window, u32 flags (1 = overwrite-only),
+ *     u32 chunk_begin, u32 chunk_count, u64 n_frames, u64 total_bytes;
+ *   frames, ascending chunk id, each 16-byte aligned: header (32 B) "DCRF",
+ *     u8 kind (1 XOR_LZ4, 2 XOR_RAW, 3 OVERWRITE, 4 OVERWRITE_DENSE),
+ *     u8 elem_bits, u16 flags (1 = every LZ4 match copies zero bytes),
+ *     u32 chunk_id, u32 raw_len, u32 body_len, u32 changed, u64 0; then the
+ *     body, zero padded to 16 bytes;
+ *   index: n_frames x u64 frame offsets from the stream start.
+ * A chunk is 64 KiB of one canonical tensor's row-major byte space (the last
+ * chunk of a tensor may be short).  A chunk with no change sends no frame.
+ */
+#ifndef DCR_H
+#define DCR_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DCR_MAX_TP 16
+#define DCR_CHUNK_BYTES 65536u
+#define DCR_STREAM_HEADER_BYTES 64u
+#define DCR_FRAME_HEADER_BYTES 32u
+#define DCR_NO_FAULT UINT64_MAX
+
+typedef enum {
+    DCR_OK = 0,
+    DCR_ERR_INVALID = -1,    /* bad argument, descriptor, plan/stream mismatch */
+    DCR_ERR_CAPACITY = -2,   /* payload buffer too small; *payload_size = required */
+    DCR_ERR_CORRUPT = -3,    /* malformed stream or frame */
+    DCR_ERR_VERSION = -4,    /* stream base_version != receiver version */
+    DCR_ERR_ABORTED = -5,    /* injected fault stopped the apply part way */
+    DCR_ERR_CUDA = -6,       /* a CUDA runtime call failed */
+    DCR_ERR_NOMEM = -7,      /* host or device allocation failed */
+    DCR_ERR_INCOMPLETE = -8, /* some framed chunks are not DONE: retry needed */
+    DCR_ERR_TIMEOUT = -9     /* a bounded device wait gave up */
+} dcr_status;
+
+/* How a trainer holds a tensor (paper summary, "Direct Projection"; popular
+ * write-up on fused Q/K/V). */
+enum {
+    DCR_REPLICATED = 0,   /* every rank holds it whole; shard 0 owns it */
+    DCR_SPLIT_ROWS = 1,   /* column-parallel: dim 0 split into tp equal parts */
+    DCR_SPLIT_COLS = 2,   /* row-parallel: dim 1 split into tp equal parts */
+    DCR_RESIDUAL_QKV_INTERLEAVED = 3 /* fused QKV, per-shard kv groups of
+                                        [q heads | k head | v head] rows;
+                                        sent as overwrite records */
+};
+
+/* How the receiver stores it in its arena (blog, "Working with low-precision
+ * RL"). */
+enum {
+    DCR_LAYOUT_CANONICAL = 0,        /* row-major canonical bytes */
+    DCR_LAYOUT_ROWGROUP_INTERLEAVE = 1 /* fused pair: canonical row r goes to
+                                          row (r/g)*2g + slot*g + r%g */
+};
+
+enum { DCR_MODE_HYBRID = 0, DCR_MODE_OVERWRITE_ONLY = 1 };
+
+typedef struct dcr_plan dcr_plan;             /* opaque, library owned */
+typedef struct dcr_recv_state dcr_recv_state; /* opaque, library owned */
+
+/* One tensor of the model, read by dcr_plan_build only (caller owned).
+ * elem_bits: 16 (bf16), 8 (e4m3 scales) or 4 (e2m1, two per byte, low
+ * nibble first).  Canonical shape [rows, cols] row-major; for a fused QKV,
+ * rows = (q_heads + 2 kv_heads) * head_dim and the canonical tensors are
+ * q_proj, k_proj, v_proj, stored at recv_offset in that order.
+ * shard_offset[r]: byte offset of shard r's local block in trainer arena r
+ * (local blocks are row-major [rows/tp, cols], [rows, cols/tp] or the fused
+ * QKV rows).  recv_offset: byte offset in the receiver arena (for a row-group
+ * pair, both tensors give the fused tensor's offset and slot 0 or 1). */
+typedef struct {
+    const char* name;
+    uint32_t elem_bits;
+    uint32_t split;
+    uint32_t tp;
+    uint32_t q_heads, kv_heads, head_dim;
+    uint64_t rows, cols;
+    uint64_t shard_offset[DCR_MAX_TP];
+    uint32_t recv_layout, recv_group, recv_slot, reserved;
+    uint64_t recv_offset;
+} dcr_tensor_desc;
+
+typedef struct {
+    uint64_t window_bytes;   /* 0 = 16 GiB.  Windows pack whole tensors in
+                                order; a tensor larger than a window is cut at
+                                chunk boundaries.  At most 256 GiB. */
+    uint32_t reserved[6];
+} dcr_plan_opts;
+
+typedef struct {
+    uint64_t n_tensors, n_parts, n_chunks, n_windows;
+    uint64_t canonical_bytes;   /* N: weight bytes of one version */
+    uint64_t plan_hash;         /* FNV-1a 64 of the canonical description */
+    uint64_t recv_bytes;        /* smallest receiver arena that fits */
+    uint64_t shard_bytes[DCR_MAX_TP]; /* smallest trainer arenas that fit */
+    uint32_t tp;
+    uint32_t reserved;
+} dcr_plan_info;
+
+typedef struct {
+    uint64_t chunk_begin, chunk_count;
+    uint64_t canonical_bytes;   /* weight bytes in this window */
+    uint64_t payload_bound;     /* worst-case stream size for this window */
+} dcr_window_info;
+
+/* Test-only fault injection for dcr_apply: frames whose index ordinal is
+ * greater than abort_after_frames are skipped, and frame abort_after_frames
+ * is applied only to canonical chunk bytes below abort_split and left
+ * unfinished.  DCR_NO_FAULT disables it. */
+typedef struct {
+    uint64_t abort_after_frames;
+    uint32_t abort_split;
+    uint32_t reserved;
+} dcr_fault;
+
+typedef struct {
+    uint64_t target_version;  /* from the stream header */
+    uint64_t n_frames;        /* frames listed in the index */
+    uint64_t frames_applied;  /* frames whose bytes were applied */
+    uint64_t frames_skipped;  /* XOR frames skipped by dedup */
+    uint64_t pending;         /* framed chunks not DONE after the call */
+    uint32_t window;
+    uint32_t committed;       /* 1 if this call committed target_version */
+} dcr_apply_result;
+
+/* Text of the calling thread's last error (never NULL). */
+const char* dcr_last_error(void);
+
+/* Plan build (blog, "A strong baseline with the Blackwell-native DE": tiling
+ * and address metadata prepared on the host, read by the apply kernel;
+ * paper summary, "Direct Projection" and "Residual Conversion").  Builds the
+ * chunk table, the shard->canonical gather segments (affine maps and the
+ * fused-QKV de-interleave), the canonical->receiver scatter segments
+ * (including row-group remaps), the windows and the plan hash, and uploads
+ * them to the current CUDA device.  *out is owned by the caller and freed
+ * with dcr_plan_destroy.  Errors: DCR_ERR_INVALID (bad descriptor: unknown
+ * dtype/split, tp > 16, shapes not divisible by tp or by the row group,
+ * odd e2m1 shard columns), DCR_ERR_NOMEM, DCR_ERR_CUDA. */
+int dcr_plan_build(const dcr_tensor_desc* tensors, size_t n, const dcr_plan_opts* opts,
+                   dcr_plan** out);
+int dcr_plan_info_get(const dcr_plan* plan, dcr_plan_info* out);
+int dcr_window_info_get(const dcr_plan* plan, uint32_t window, dcr_window_info* out);
+void dcr_plan_destroy(dcr_plan* plan);
+
+/* Receiver state (paper summary, "Recoverable in-place apply"; popular
+ * write-up on dedup by unique IDs and joint commit): the committed version
+ * and, per chunk, the version it was last claimed for with NOT_STARTED /
+ * CLAIMED / DONE, kept in device memory.  A frame's dedup ID is
+ * (target_version, chunk_id).  Freed with dcr_recv_state_destroy. */
+int dcr_recv_state_create(const dcr_plan* plan, uint64_t version, dcr_recv_state** out);
+void dcr_recv_state_destroy(dcr_recv_state* state);
+int dcr_recv_state_version(const dcr_recv_state* state, uint64_t* out);
+
+/* Encode one window (blog, "Delta update algebra"; paper summary, "Hybrid
+ * encoding and compression"; paper abstract).  old_shards[r] / new_shards[r]
+ * are the trainer arenas of shard r (device, read only).  For each chunk:
+ * gather old and new through the plan, mask = old XOR new, count changed
+ * elements, then emit an XOR_LZ4 frame (XOR_RAW if LZ4 is not smaller) for
+ * affine tensors, or OVERWRITE records (OVERWRITE_DENSE if not smaller) for
+ * residual tensors and in DCR_MODE_OVERWRITE_ONLY.  The stream is written to
+ * `payload` (device, payload_cap bytes); *payload_size gets its size.
+ * changed_per_tensor (host, n_tensors entries, nullable) receives the changed
+ * element counts of this window.  Errors: DCR_ERR_INVALID, DCR_ERR_CAPACITY
+ * (*payload_size = bytes required; the window's payload_bound always fits),
+ * DCR_ERR_CUDA, DCR_ERR_TIMEOUT. */
+int dcr_encode(const dcr_plan* plan, uint32_t mode, uint32_t window,
+               const void* const* old_shards, const void* const* new_shards,
+               uint64_t base_version, uint64_t target_version,
+               void* payload, size_t payload_cap, size_t* payload_size,
+               uint64_t* changed_per_tensor, void* stream);
+
+/* Apply one window's stream in place (paper summary, "Recoverable in-place
+ * apply"; popular write-up on in-place apply without a backup and on dedup).
+ * `payload` (device, `size` bytes) is checked against the plan hash and the
+ * state's version before any byte of `target` (device receiver arena) is
+ * touched.  XOR frames claim their chunk and are skipped if it was already
+ * claimed for this target version; overwrite frames always apply.  The
+ * version advances to target_version once every window of it has all its
+ * framed chunks DONE.  fault is test only (nullable); result is nullable.
+ * Errors: DCR_ERR_INVALID (plan hash, window, argument), DCR_ERR_VERSION,
+ * DCR_ERR_CORRUPT (malformed frames; the others are still applied),
+ * DCR_ERR_ABORTED, DCR_ERR_INCOMPLETE (claimed chunks left unfinished by an
+ * earlier abort: run dcr_apply_retry), DCR_ERR_CUDA. */
+int dcr_apply(const dcr_plan* plan, dcr_recv_state* state, const void* payload, size_t size,
+              void* target, const dcr_fault* fault, dcr_apply_result* result, void* stream);
+
+/* Overwrite-only retry (popular write-up: after a failure the change set is
+ * re-sent as overwrites, which are idempotent; paper abstract: retries
+ * overwrite partial writes).  Same as dcr_apply but accepts only streams
+ * encoded with DCR_MODE_OVERWRITE_ONLY; returns DCR_ERR_INVALID otherwise,
+ * before touching `target`. */
+int dcr_apply_retry(const dcr_plan* plan, dcr_recv_state* state, const void* payload, size_t size,
+                    void* target, dcr_apply_result* result, void* stream);
+
+/* Kernel timing (tracing aid).  When on, the library records CUDA events on
+ * the caller's stream around each of its kernels; after each dcr_encode /
+ * dcr_apply / dcr_apply_retry, dcr_plan_last_profile returns the durations
+ * in milliseconds of that call's kernels (valid = 1 if measured).  The
+ * record is per plan; off by default. */
+typedef struct {
+    float encode_ms;    /* gather + XOR + count + encode + frame write */
+    float finalize_ms;  /* frame index + stream header */
+    float apply_ms;     /* warp-per-frame decode and apply */
+    float defer_ms;     /* general LZ4 frames */
+    float pending_ms;   /* commit check */
+    uint32_t encode_valid, apply_valid;
+} dcr_profile;
+int dcr_plan_set_profiling(dcr_plan* plan, int on);
+int dcr_plan_last_profile(const dcr_plan* plan, dcr_profile* out);
+
+/* Dense refit: copy every canonical byte from the trainer arenas into the
+ * receiver arena (the full-checkpoint transfer the delta refit replaces;
+ * also how a receiver is first filled).  No status read, no sync. */
+int dcr_dense_refit(const dcr_plan* plan, const void* const* shards, void* target, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DCR_H */

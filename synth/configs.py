@@ -48,6 +48,7 @@ class Tensor:
     recv_offset: int = 0
     shard_offset: List[int] = field(default_factory=list)
     index: int = 0
+    gen_id: Optional[int] = None   # generator stream id (defaults to the position)
 
     @property
     def nbytes(self):
@@ -112,7 +113,8 @@ class Workload:
     def params(self, t, r, rule_override=None, frac_override=None):
         rule = t.rule if rule_override is None else rule_override
         frac = t.frac if frac_override is None else frac_override
-        return make_params(self.seed, t.index * 64 + r, t.value_kind, rule, frac, t.zero_frac)
+        gid = t.index if t.gen_id is None else t.gen_id
+        return make_params(self.seed, gid * 64 + r, t.value_kind, rule, frac, t.zero_frac)
 
     def host_arenas(self, rule_override=None, frac_override=None):
         """Old and new shard arenas as numpy uint8 arrays (small workloads)."""
@@ -223,6 +225,33 @@ def nvfp4_moe(hidden=6144, ffn=2048, experts=64, layers=16, frac=0.00085, group=
                       recv_slot=1, recv_offset=fs),
                    sc(p + "down_s", hidden, ffn // 16)]
     return Workload(name, seed, 1, ts, window_bytes=window_bytes).layout()
+
+
+def subset(wl, indices):
+    """A workload holding only the given tensors of wl, with the same generator
+    streams (so their bytes are identical) and a fresh arena layout."""
+    import copy
+    ts = []
+    for i in indices:
+        t = copy.deepcopy(wl.tensors[i])
+        t.gen_id = wl.tensors[i].index if wl.tensors[i].gen_id is None else wl.tensors[i].gen_id
+        if t.recv_layout == RECV_ROWGROUP:
+            t.recv_offset = ("fused", wl.tensors[i].recv_offset)
+        ts.append(t)
+    return Workload(wl.name + "-subset", wl.seed, wl.tp, ts, window_bytes=1 << 40).layout()
+
+
+def first_chunks(wl):
+    """Global id of the first chunk of every tensor (plan order)."""
+    out, c = [], 0
+    for t in wl.tensors:
+        out.append(c)
+        if t.split == RESIDUAL_QKV:
+            for rows in (t.q_heads * t.head_dim, t.kv_heads * t.head_dim, t.kv_heads * t.head_dim):
+                c += -(-rows * t.cols * t.elem_bits // 8 // CHUNK)
+        else:
+            c += -(-t.nbytes // CHUNK)
+    return out
 
 
 # ---- the five full-size workloads and their small structural twins --------

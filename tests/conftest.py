@@ -21,6 +21,9 @@ def _host_libs():
         oracle.build()
     if not os.path.exists(os.path.join(ROOT, "synth", "libsynth.so")):
         synth.build(gpu=False)
+    if not os.path.exists(os.path.join(ROOT, "bit_exact_xor_gb300", "libdcr.so")):
+        from bit_exact_xor_gb300 import build as dcr_build
+        dcr_build.build()
     yield
 
 

@@ -1,0 +1,244 @@
+"""GPU parity at the full sizes of the five workloads, in the launch
+configuration the benchmark times.  Where the CPU oracle can take the whole
+workload (4096^2 bf16, the TP=2 dense model) every frame and every receiver
+byte is compared; for the 16-20 GB workloads whole tensors are sampled
+(regenerated on the CPU from the same generator streams) and compared frame
+by frame, plus properties that hold at any size."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from synth import configs
+from parity import assert_same_frames, frames_by_chunk
+from streamfmt import check_structure, parse
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+import bit_exact_xor_gb300 as dcr  # noqa: E402
+from wl import descs_of, to_device  # noqa: E402
+
+
+def encode_fit(plan, olds, news, w=0, mode=dcr.MODE_HYBRID, base=0, target=1, guess=None):
+    """Encode with a payload buffer sized from a guess, growing it once on
+    DCR_ERR_CAPACITY to the size the library reports."""
+    cap = guess or plan.window(w).payload_bound
+    pl = torch.empty(cap, dtype=torch.uint8, device="cuda")
+    rc, size, counts = dcr.encode(plan, olds, news, pl, window=w, mode=mode, base_version=base,
+                                  target_version=target)
+    if rc == dcr.ERR_CAPACITY:
+        pl = torch.empty(size, dtype=torch.uint8, device="cuda")
+        rc, size, counts = dcr.encode(plan, olds, news, pl, window=w, mode=mode, base_version=base,
+                                      target_version=target)
+    dcr.check(rc)
+    return pl, size, counts
+
+
+def sub_frames(payload_np):
+    hdr, frames, _ = parse(payload_np)
+    return {f["chunk"]: f for f in frames}
+
+
+def compare_sampled(wl, picks, gpu_payloads, target, mode=dcr.MODE_HYBRID, gpu_counts=None):
+    """Regenerate the picked tensors on the CPU, run the oracle on them alone,
+    and compare frames (chunk ids shifted to the full plan) and the final
+    receiver bytes.  Returns (gpu bytes, oracle bytes) of the compared frames."""
+    firsts = configs.first_chunks(wl)
+    gbytes = obytes = 0
+    gframes = {}
+    for p in gpu_payloads:
+        gframes.update(sub_frames(p))
+    host_t = None
+    for group in picks:
+        sub = configs.subset(wl, group)
+        orc = oracle.Oracle(sub)
+        olds, news = sub.host_arenas()
+        o, oc = orc.encode(olds, news, mode=mode, threads=16)
+        of = sub_frames(o)
+        sub_firsts = configs.first_chunks(sub)
+        for k, i in enumerate(group):
+            t = wl.tensors[i]
+            if gpu_counts is not None:
+                assert gpu_counts[i] == int(oc[k]), t.name
+            nch = configs.first_chunks(sub)[k + 1] - sub_firsts[k] if k + 1 < len(group) else \
+                orc.n_chunks - sub_firsts[k]
+            for c in range(nch):
+                a, b = gframes.get(firsts[i] + c), of.get(sub_firsts[k] + c)
+                assert (a is None) == (b is None), (t.name, c)
+                if a is None:
+                    continue
+                b = dict(b)
+                b["chunk"] = a["chunk"]
+                ga = np.asarray(a["body"])
+                # compare through the independent reader: same mask / records
+                from parity import frame_content
+                ca, cb = frame_content(a), frame_content(b)
+                assert a["changed"] == b["changed"] and ca[0] == cb[0], (t.name, c)
+                assert np.array_equal(ca[1], cb[1]), (t.name, c)
+                gbytes += (32 + a["body_len"] + 15) // 16 * 16
+                obytes += (32 + b["body_len"] + 15) // 16 * 16
+        exp = orc.receiver_dense(news)
+        if host_t is None:
+            host_t = target
+        for k, i in enumerate(group):
+            t, st_ = wl.tensors[i], sub.tensors[k]
+            span = 2 * t.nbytes if t.recv_layout == configs.RECV_ROWGROUP else t.nbytes
+            got = host_t[t.recv_offset:t.recv_offset + span].cpu().numpy()
+            ref = exp[st_.recv_offset:st_.recv_offset + span]
+            if t.recv_layout == configs.RECV_ROWGROUP and len(group) == 1:
+                continue
+            assert np.array_equal(got, ref), t.name
+    return gbytes, obytes
+
+
+@pytest.mark.parametrize("n", [1, 2])
+def test_full_workload_every_byte(n):
+    wl = configs.full(n)
+    orc = oracle.Oracle(wl)
+    olds, news = wl.host_arenas()
+    plan = dcr.Plan(descs_of(wl))
+    assert plan.info.plan_hash == orc.plan_hash
+    d_old, d_new = to_device(olds), to_device(news)
+    pl, size, counts = encode_fit(plan, d_old, d_new, guess=wl.canonical_bytes // 8)
+    g = pl[:size].cpu().numpy()
+    o, oc = orc.encode(olds, news, threads=16)
+    check_structure(g)
+    assert counts == [int(x) for x in oc]
+    assert_same_frames(g, o)
+    assert g.size <= 1.15 * o.size, (g.size, o.size)
+    target = torch.empty(plan.info.recv_bytes, dtype=torch.uint8, device="cuda")
+    dcr.check(dcr.dense_refit(plan, d_old, target))
+    st = dcr.RecvState(plan, 0)
+    rc, res = dcr.apply(plan, st, pl, size, target)
+    assert rc == dcr.OK and res.committed
+    exp = orc.receiver_dense(news)
+    assert np.array_equal(target.cpu().numpy()[:exp.size], exp)
+    if n == 1:
+        t = wl.tensors[0]
+        assert counts[0] == synth.count_selected(wl.params(t, 0), t.rows * t.cols)
+
+
+def test_full_gqa_hybrid_abort_retry():
+    wl = configs.full(3)
+    plan = dcr.Plan(descs_of(wl))
+    assert plan.info.plan_hash == oracle.Oracle(wl).plan_hash
+    d_old, d_new = wl.device_arenas(torch)
+    target = torch.empty(plan.info.recv_bytes, dtype=torch.uint8, device="cuda")
+    dcr.check(dcr.dense_refit(plan, d_old, target))
+    pl, size, counts = encode_fit(plan, d_old, d_new, guess=wl.canonical_bytes // 6)
+    st = dcr.RecvState(plan, 0)
+    nf = int(pl[48:56].cpu().numpy().view("<u8")[0])
+    rc, res = dcr.apply(plan, st, pl, size, target, fault=(nf // 2, 1000))
+    assert rc == dcr.ERR_ABORTED and st.version == 0 and res.frames_applied == nf // 2 + 1
+    rc, res = dcr.apply(plan, st, pl, size, target)
+    assert rc in (dcr.OK, dcr.ERR_INCOMPLETE)
+    rp, rsize, rcounts = encode_fit(plan, d_old, d_new, mode=dcr.MODE_OVERWRITE_ONLY,
+                                    guess=wl.canonical_bytes // 8)
+    assert rcounts == counts
+    if rc != dcr.OK:
+        rc, res = dcr.apply_retry(plan, st, rp, rsize, target)
+        assert rc == dcr.OK, dcr.last_error()
+    assert st.version == 1
+    ref = torch.empty_like(target)
+    dcr.check(dcr.dense_refit(plan, d_new, ref))
+    assert torch.equal(ref, target), "final arena differs from a dense refit of new"
+    del ref
+    names = {t.name: i for i, t in enumerate(wl.tensors)}
+    picks = [[names["l0.qkv"]], [names["l7.o"]], [names["l31.down"]], [names["l3.gate"]],
+             [names["l15.norm1"]], [names["norm_f"]]]
+    g_np = pl[:size].cpu().numpy()
+    gb, ob = compare_sampled(wl, picks, [g_np], target, gpu_counts=counts)
+    assert gb <= 1.15 * ob
+    r_np = rp[:rsize].cpu().numpy()
+    compare_sampled(wl, picks[:2], [r_np], target, mode=dcr.MODE_OVERWRITE_ONLY)
+
+
+def _chunk_frame_oracle(old_b, new_b):
+    """Oracle frame of one canonical chunk (identity layout, one tensor)."""
+    t = configs.Tensor("c", elem_bits=16, rows=1, cols=old_b.size // 2, split=configs.REPLICATED,
+                       value_kind=0, rule=0, frac=0)
+    one = configs.Workload("chunk", 1, 1, [t]).layout()
+    o, _ = oracle.Oracle(one).encode([old_b], [new_b], threads=1)
+    fr = sub_frames(o)
+    return fr.get(0)
+
+
+@pytest.mark.parametrize("frac", list(configs.SWEEP_FRACS) + ["random"])
+def test_full_sweep_8gib(frac, sweep_state):
+    wl, plan, d_old, d_new, target = sweep_state
+    t = wl.tensors[0]
+    rule = synth.RULE_RANDOM if frac == "random" else synth.RULE_PM4
+    f = 0.0 if frac == "random" else frac
+    p = synth.make_params(wl.seed, t.index * 64, t.value_kind, rule, f, 0.0)
+    synth.fill_gpu(p, t.rows * t.cols, 0, d_new.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    target.copy_(d_old)
+    guess = wl.canonical_bytes // 4 if frac in ("random", 0.3, 0.1) else wl.canonical_bytes // 16
+    pl, size, counts = encode_fit(plan, [d_old], [d_new], guess=guess)
+    ref_changed = int((d_old.view(torch.int16) != d_new.view(torch.int16)).sum().item())
+    assert counts[0] == ref_changed
+    st = dcr.RecvState(plan, 0)
+    rc, res = dcr.apply(plan, st, pl, size, target)
+    assert rc == dcr.OK and res.committed
+    assert torch.equal(target, d_new)
+    g = sub_frames(pl[:size].cpu().numpy())
+    rng = np.random.default_rng(11)
+    n_chunks = t.nbytes // 65536
+    gb = ob = 0
+    for c in sorted(set([0, 1, n_chunks // 2, n_chunks - 1] + list(rng.integers(0, n_chunks, 8)))):
+        pc = synth.make_params(wl.seed, t.index * 64, t.value_kind, rule, f, 0.0, elem_base=c * 32768)
+        ob_, nb_ = synth.fill_cpu(pc, 32768)
+        of = _chunk_frame_oracle(ob_, nb_)
+        gf = g.get(c)
+        assert (gf is None) == (of is None)
+        if gf is None:
+            continue
+        from parity import frame_content
+        a, b = frame_content(gf), frame_content(of)
+        assert gf["changed"] == of["changed"] and a[0] == b[0] and np.array_equal(a[1], b[1])
+        gb += gf["body_len"]
+        ob += of["body_len"]
+        assert np.array_equal(target[c * 65536:(c + 1) * 65536].cpu().numpy(), nb_)
+    assert gb <= 1.15 * ob
+
+
+@pytest.fixture(scope="module")
+def sweep_state():
+    wl = configs.full(4)
+    plan = dcr.Plan(descs_of(wl))
+    t = wl.tensors[0]
+    d_old = torch.empty(t.nbytes, dtype=torch.uint8, device="cuda")
+    d_new = torch.empty_like(d_old)
+    target = torch.empty_like(d_old)
+    p = wl.params(t, 0)
+    synth.fill_gpu(p, t.rows * t.cols, d_old.data_ptr(), 0, torch.cuda.current_stream().cuda_stream)
+    yield wl, plan, d_old, d_new, target
+    del d_old, d_new, target
+    torch.cuda.empty_cache()
+
+
+def test_full_nvfp4_moe_windows():
+    wl = configs.full(5)
+    plan = dcr.Plan(descs_of(wl))
+    assert plan.n_windows == 2 and plan.info.plan_hash == oracle.Oracle(wl).plan_hash
+    d_old, d_new = wl.device_arenas(torch)
+    target = torch.empty(plan.info.recv_bytes, dtype=torch.uint8, device="cuda")
+    dcr.check(dcr.dense_refit(plan, d_old, target))
+    st = dcr.RecvState(plan, 0)
+    payloads, all_counts = [], np.zeros(len(wl.tensors), dtype=np.int64)
+    for w in range(2):
+        pl, size, counts = encode_fit(plan, d_old, d_new, w=w, guess=wl.canonical_bytes // 40)
+        all_counts += np.array(counts, dtype=np.int64)
+        rc, res = dcr.apply(plan, st, pl, size, target)
+        assert rc == dcr.OK and res.committed == (w == 1) and st.version == (1 if w == 1 else 0)
+        payloads.append(pl[:size].cpu().numpy())
+    ref = torch.empty_like(target)
+    dcr.check(dcr.dense_refit(plan, d_new, ref))
+    assert torch.equal(ref, target)
+    del ref
+    names = {t.name: i for i, t in enumerate(wl.tensors)}
+    picks = [[names["l0.e0.gate"], names["l0.e0.up"]], [names["l15.e63.gate"], names["l15.e63.up"]],
+             [names["l9.e31.down"]], [names["l0.e0.gate_s"], names["l0.e0.up_s"]],
+             [names["l11.e7.down_s"]]]
+    gb, ob = compare_sampled(wl, picks, payloads, target, gpu_counts=list(all_counts))
+    assert gb <= 1.15 * ob

@@ -1,0 +1,310 @@
+"""GPU parity on the small structural twins of the five workloads: the CUDA
+path, called through the C ABI, against the CPU oracle on the same seeded
+inputs.  Sizes span several 64 KiB chunks and ragged tails."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from synth import configs
+from parity import assert_same_frames, frames_by_chunk
+from streamfmt import check_structure, parse
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+import bit_exact_xor_gb300 as dcr  # noqa: E402
+from wl import descs_of, to_device  # noqa: E402
+
+
+class Case:
+    def __init__(self, wl, rule=None, frac=None):
+        self.wl = wl
+        self.orc = oracle.Oracle(wl)
+        self.olds, self.news = wl.host_arenas(rule_override=rule, frac_override=frac)
+        self.plan = dcr.Plan(descs_of(wl), window_bytes=wl.window_bytes)
+        self.d_old, self.d_new = to_device(self.olds), to_device(self.news)
+        self.exp = self.orc.receiver_dense(self.news)
+        self.start = self.orc.receiver_dense(self.olds)
+
+    def target(self):
+        t = torch.zeros(max(self.plan.info.recv_bytes, 16), dtype=torch.uint8, device="cuda")
+        dcr.check(dcr.dense_refit(self.plan, self.d_old, t))
+        return t
+
+    def encode(self, w=0, mode=dcr.MODE_HYBRID, base=0, target=1, olds=None, news=None):
+        wi = self.plan.window(w)
+        pl = torch.zeros(wi.payload_bound, dtype=torch.uint8, device="cuda")
+        rc, size, counts = dcr.encode(self.plan, olds or self.d_old, news or self.d_new, pl, window=w,
+                                      mode=mode, base_version=base, target_version=target)
+        dcr.check(rc)
+        return pl, size, counts
+
+    def host(self, t):
+        return t.cpu().numpy()[:self.exp.size]
+
+
+@pytest.fixture(scope="module", params=[1, 2, 3, 4, 5])
+def case(request):
+    return Case(configs.mini(request.param))
+
+
+def test_generator_twins_agree():
+    for vk, rule, fr, zf in [(synth.VAL_BF16_NORMAL, synth.RULE_PM4, 0.01, 0.0001),
+                             (synth.VAL_BF16_NORMAL, synth.RULE_LOW3, 0.05, 0.0),
+                             (synth.VAL_BF16_NORMAL, synth.RULE_RANDOM, 0.0, 0.0),
+                             (synth.VAL_BYTES, synth.RULE_NIBBLE, 0.01, 0.0),
+                             (synth.VAL_E4M3_SCALE, synth.RULE_BPM4, 0.01, 0.0)]:
+        p = synth.make_params(0xABC, 77, vk, rule, fr, zf, elem_base=123457)
+        n = 300001
+        o, w = synth.fill_cpu(p, n)
+        eb = synth.elem_bytes(vk)
+        go = torch.zeros(n * eb, dtype=torch.uint8, device="cuda")
+        gw = torch.zeros(n * eb, dtype=torch.uint8, device="cuda")
+        synth.fill_gpu(p, n, go.data_ptr(), gw.data_ptr(), torch.cuda.current_stream().cuda_stream)
+        torch.cuda.synchronize()
+        assert np.array_equal(go.cpu().numpy(), o) and np.array_equal(gw.cpu().numpy(), w)
+
+
+def test_plan_matches_oracle_layout(case):
+    assert case.plan.info.plan_hash == case.orc.plan_hash
+    assert case.plan.n_windows == case.orc.n_windows
+    assert case.plan.info.n_chunks == case.orc.n_chunks
+    assert case.plan.info.canonical_bytes == case.wl.canonical_bytes
+    for w in range(case.plan.n_windows):
+        wi = case.plan.window(w)
+        assert (wi.chunk_begin, wi.chunk_count) == case.orc.window_range(w)
+
+
+def test_dense_refit_matches_oracle(case):
+    assert np.array_equal(case.host(case.target()), case.start)
+
+
+@pytest.mark.parametrize("mode", [dcr.MODE_HYBRID, dcr.MODE_OVERWRITE_ONLY])
+def test_encode_parity(case, mode):
+    tot_g = tot_o = 0
+    for w in range(case.plan.n_windows):
+        pl, size, counts = case.encode(w, mode, base=3, target=4)
+        g = pl[:size].cpu().numpy()
+        o, oc = case.orc.encode(case.olds, case.news, window=w, mode=mode, base_version=3,
+                                target_version=4)
+        check_structure(g)
+        assert counts == [int(x) for x in oc]
+        hdr, gf, of = assert_same_frames(g, o)
+        if mode == dcr.MODE_OVERWRITE_ONLY:
+            assert np.array_equal(g, o), "overwrite streams are deterministic: byte-identical"
+        tot_g += g.size
+        tot_o += o.size
+    assert tot_g <= 1.15 * tot_o, (tot_g, tot_o)
+
+
+def test_gpu_stream_applies_on_gpu_and_oracle(case):
+    t = case.target()
+    st = dcr.RecvState(case.plan, 0)
+    ost = case.orc.state(0)
+    otgt = case.start.copy()
+    for w in range(case.plan.n_windows):
+        pl, size, _ = case.encode(w)
+        rc, res = dcr.apply(case.plan, st, pl, size, t)
+        assert rc == dcr.OK, dcr.last_error()
+        assert res.committed == (w == case.plan.n_windows - 1)
+        assert case.orc.apply(ost, pl[:size].cpu().numpy(), otgt) == oracle.OK
+    assert np.array_equal(case.host(t), case.exp)
+    assert np.array_equal(otgt, case.exp)
+    assert st.version == 1 and ost.version == 1
+
+
+def test_oracle_stream_applies_on_gpu(case):
+    t = case.target()
+    st = dcr.RecvState(case.plan, 5)
+    for w in range(case.plan.n_windows):
+        o, _ = case.orc.encode(case.olds, case.news, window=w, base_version=5, target_version=6)
+        d = torch.from_numpy(o).cuda()
+        rc, res = dcr.apply(case.plan, st, d, o.size, t)
+        assert rc == dcr.OK, dcr.last_error()
+    assert np.array_equal(case.host(t), case.exp) and st.version == 6
+
+
+def test_overwrite_retry_stream_reaches_new(case):
+    t = case.target()
+    st = dcr.RecvState(case.plan, 0)
+    for w in range(case.plan.n_windows):
+        pl, size, _ = case.encode(w, dcr.MODE_OVERWRITE_ONLY)
+        rc, _ = dcr.apply_retry(case.plan, st, pl, size, t)
+        assert rc == dcr.OK, dcr.last_error()
+    assert np.array_equal(case.host(t), case.exp)
+
+
+@pytest.mark.parametrize("n", [1, 3])
+def test_abort_state_matches_oracle_then_retry(n):
+    c = Case(configs.mini(n))
+    pl, size, _ = c.encode()
+    rp, rsize, _ = c.encode(mode=dcr.MODE_OVERWRITE_ONLY)
+    nf = parse(pl[:size].cpu().numpy())[0]["n_frames"]
+    g_pl = pl[:size].cpu().numpy()
+    for k in sorted(set([0, 1, nf // 2, nf - 1])):
+        for split in (0, 1001, 65536):
+            t = c.target()
+            st = dcr.RecvState(c.plan, 0)
+            rc, res = dcr.apply(c.plan, st, pl, size, t, fault=(k, split))
+            assert rc == dcr.ERR_ABORTED and st.version == 0
+            otgt = c.start.copy()
+            ost = c.orc.state(0)
+            assert c.orc.apply(ost, g_pl, otgt, abort_at=k, split=split) == oracle.E_ABORTED
+            assert np.array_equal(c.host(t), otgt), "mixed state after abort differs from oracle"
+            rc, _ = dcr.apply(c.plan, st, pl, size, t)           # re-sent XOR stream
+            assert rc in (dcr.OK, dcr.ERR_INCOMPLETE)
+            if rc == dcr.OK:
+                assert st.version == 1
+            else:
+                rc, _ = dcr.apply_retry(c.plan, st, rp, rsize, t)
+                assert rc == dcr.OK and st.version == 1
+            assert np.array_equal(c.host(t), c.exp)
+
+
+def _reindexed(pl_np, order):
+    hdr, frames, idx = parse(pl_np)
+    offs = np.array([frames[i]["offset"] for i in order], dtype="<u8")
+    out = np.concatenate([pl_np[:idx], offs.view(np.uint8)])
+    out[48:56] = np.array([len(order)], dtype="<u8").view(np.uint8)
+    out[56:64] = np.array([out.size], dtype="<u8").view(np.uint8)
+    return out
+
+
+def test_duplicate_frames_applied_once():
+    c = Case(configs.mini(2))
+    pl, size, _ = c.encode()
+    g = pl[:size].cpu().numpy()
+    nf = parse(g)[0]["n_frames"]
+    dup = _reindexed(g, list(range(nf)) * 3 + [0, nf - 1])
+    t = c.target()
+    st = dcr.RecvState(c.plan, 0)
+    rc, res = dcr.apply(c.plan, st, torch.from_numpy(dup).cuda(), dup.size, t)
+    assert rc == dcr.OK and res.frames_skipped == 2 * nf + 2 and st.version == 1
+    assert np.array_equal(c.host(t), c.exp)
+
+
+def test_duplicate_oracle_frames_applied_once():
+    c = Case(configs.mini(1))
+    o, _ = c.orc.encode(c.olds, c.news)
+    nf = parse(o)[0]["n_frames"]
+    dup = _reindexed(o, list(range(nf)) + list(range(nf)))
+    t = c.target()
+    st = dcr.RecvState(c.plan, 0)
+    rc, res = dcr.apply(c.plan, st, torch.from_numpy(dup).cuda(), dup.size, t)
+    assert rc == dcr.OK and res.frames_skipped == nf
+    assert np.array_equal(c.host(t), c.exp)
+
+
+def test_rejections_leave_target_untouched():
+    c = Case(configs.mini(1))
+    pl, size, _ = c.encode(base=3, target=4)
+    t = c.target()
+    before = c.host(t).copy()
+    rc, _ = dcr.apply(c.plan, dcr.RecvState(c.plan, 2), pl, size, t)
+    assert rc == dcr.ERR_VERSION
+    bad = pl.clone()
+    bad[8] ^= 1
+    rc, _ = dcr.apply(c.plan, dcr.RecvState(c.plan, 3), bad, size, t)
+    assert rc == dcr.ERR_INVALID
+    rc, _ = dcr.apply_retry(c.plan, dcr.RecvState(c.plan, 3), pl, size, t)
+    assert rc == dcr.ERR_INVALID
+    bad = pl.clone()
+    bad[0] ^= 1
+    rc, _ = dcr.apply(c.plan, dcr.RecvState(c.plan, 3), bad, size, t)
+    assert rc == dcr.ERR_CORRUPT
+    assert np.array_equal(c.host(t), before)
+    st = dcr.RecvState(c.plan, 3)
+    rc, _ = dcr.apply(c.plan, st, pl, size, t)
+    assert rc == dcr.OK and st.version == 4
+    rc, _ = dcr.apply(c.plan, st, pl, size, t)
+    assert rc == dcr.ERR_VERSION
+    assert np.array_equal(c.host(t), c.exp)
+
+
+def test_corrupt_lz4_frame_reported_and_retry_recovers():
+    c = Case(configs.mini(1))
+    pl, size, _ = c.encode()
+    g = pl[:size].cpu().numpy()
+    _, frames, _ = parse(g)
+    f = [f for f in frames if f["kind"] == 1][0]
+    bad = g.copy()
+    bad[f["offset"] + 32:f["offset"] + 40] = 0xFF
+    t = c.target()
+    st = dcr.RecvState(c.plan, 0)
+    rc, _ = dcr.apply(c.plan, st, torch.from_numpy(bad).cuda(), size, t)
+    assert rc == dcr.ERR_CORRUPT and st.version == 0
+    rp, rsize, _ = c.encode(mode=dcr.MODE_OVERWRITE_ONLY)
+    rc, _ = dcr.apply_retry(c.plan, st, rp, rsize, t)
+    assert rc == dcr.OK and np.array_equal(c.host(t), c.exp)
+
+
+def test_zsrc_flag_is_verified():
+    # a greedy (oracle) block whose matches copy non-zero bytes, relabelled
+    # as ZSRC, must be rejected rather than applied as zeros
+    c = Case(configs.mini(1))
+    o, _ = c.orc.encode(c.olds, c.news)
+    _, frames, _ = parse(o)
+    lied = o.copy()
+    n = 0
+    for f in frames:
+        if f["kind"] == 1:
+            m = oracle.lz4_decode(f["body"], f["raw_len"])
+            if oracle.lz4_decode(f["body"], f["raw_len"], zsrc=True) is None and m is not None:
+                lied[f["offset"] + 6] = 1
+                n += 1
+    assert n > 0
+    t = c.target()
+    rc, _ = dcr.apply(c.plan, dcr.RecvState(c.plan, 0), torch.from_numpy(lied).cuda(), o.size, t)
+    assert rc == dcr.ERR_CORRUPT
+
+
+def test_no_change_and_capacity():
+    c = Case(configs.mini(2))
+    wi = c.plan.window(0)
+    pl = torch.zeros(wi.payload_bound, dtype=torch.uint8, device="cuda")
+    rc, size, counts = dcr.encode(c.plan, c.d_old, c.d_old, pl)
+    assert rc == dcr.OK and size == 64 and not any(counts)
+    t = c.target()
+    st = dcr.RecvState(c.plan, 0)
+    rc, _ = dcr.apply(c.plan, st, pl, size, t)
+    assert rc == dcr.OK and st.version == 1 and np.array_equal(c.host(t), c.start)
+    _, need, _ = dcr.encode(c.plan, c.d_old, c.d_new, pl)
+    small = torch.zeros(need - 1, dtype=torch.uint8, device="cuda")
+    rc, size2, _ = dcr.encode(c.plan, c.d_old, c.d_new, small)
+    assert rc == dcr.ERR_CAPACITY and size2 == need
+    rc, size3, _ = dcr.encode(c.plan, c.d_old, c.d_new, pl, cap=need)
+    assert rc == dcr.OK and size3 == need
+
+
+@pytest.mark.parametrize("frac", [0.0, 0.00085, 0.05, 0.3, "random"])
+def test_change_rates_parity(frac):
+    wl = configs.mini(4)
+    c = Case(wl, rule=synth.RULE_RANDOM if frac == "random" else None,
+             frac=None if frac == "random" else frac)
+    pl, size, counts = c.encode()
+    g = pl[:size].cpu().numpy()
+    o, oc = c.orc.encode(c.olds, c.news)
+    assert counts == [int(x) for x in oc]
+    assert_same_frames(g, o)
+    assert g.size <= 1.15 * o.size + 64
+    t = c.target()
+    rc, _ = dcr.apply(c.plan, dcr.RecvState(c.plan, 0), pl, size, t)
+    assert rc == dcr.OK and np.array_equal(c.host(t), c.exp)
+
+
+def test_signed_zero_on_gpu():
+    t0 = configs.Tensor("z", elem_bits=16, rows=64, cols=1024, split=configs.REPLICATED,
+                        value_kind=0, rule=0, frac=0)
+    wl = configs.Workload("z", 1, 1, [t0]).layout()
+    old = np.zeros(wl.shard_bytes[0], dtype=np.uint8)
+    new = old.copy()
+    new[2 * 777 + 1] = 0x80
+    plan = dcr.Plan(descs_of(wl))
+    d_old, d_new = to_device([old]), to_device([new])
+    pl = torch.zeros(plan.window(0).payload_bound, dtype=torch.uint8, device="cuda")
+    rc, size, counts = dcr.encode(plan, d_old, d_new, pl)
+    assert rc == dcr.OK and counts == [1]
+    tgt = to_device([old])[0]
+    rc, _ = dcr.apply(plan, dcr.RecvState(plan, 0), pl, size, tgt)
+    assert rc == dcr.OK and np.array_equal(tgt.cpu().numpy(), new)
