@@ -245,7 +245,7 @@ def run_gpu(args):
     plan = dcr.Plan(descs_of(wl), window_bytes=wl.window_bytes)
     plan.set_profiling(True)
     olds, news = wl.device_arenas(torch)
-    target = torch.empty(plan.info.recv_bytes, dtype=torch.uint8, device=dev)
+    target = torch.empty(max(plan.info.recv_bytes, wl.recv_bytes), dtype=torch.uint8, device=dev)
     dcr.check(dcr.dense_refit(plan, olds, target))
     nw = plan.n_windows
     caps = [plan.window(w).payload_bound for w in range(nw)]

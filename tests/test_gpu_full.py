@@ -107,7 +107,7 @@ def test_full_workload_every_byte(n):
     assert counts == [int(x) for x in oc]
     assert_same_frames(g, o)
     assert g.size <= 1.15 * o.size, (g.size, o.size)
-    target = torch.empty(plan.info.recv_bytes, dtype=torch.uint8, device="cuda")
+    target = torch.empty(max(plan.info.recv_bytes, wl.recv_bytes), dtype=torch.uint8, device="cuda")
     dcr.check(dcr.dense_refit(plan, d_old, target))
     st = dcr.RecvState(plan, 0)
     rc, res = dcr.apply(plan, st, pl, size, target)
@@ -124,7 +124,7 @@ def test_full_gqa_hybrid_abort_retry():
     plan = dcr.Plan(descs_of(wl))
     assert plan.info.plan_hash == oracle.Oracle(wl).plan_hash
     d_old, d_new = wl.device_arenas(torch)
-    target = torch.empty(plan.info.recv_bytes, dtype=torch.uint8, device="cuda")
+    target = torch.empty(max(plan.info.recv_bytes, wl.recv_bytes), dtype=torch.uint8, device="cuda")
     dcr.check(dcr.dense_refit(plan, d_old, target))
     pl, size, counts = encode_fit(plan, d_old, d_new, guess=wl.canonical_bytes // 6)
     st = dcr.RecvState(plan, 0)
@@ -222,7 +222,7 @@ def test_full_nvfp4_moe_windows():
     plan = dcr.Plan(descs_of(wl))
     assert plan.n_windows == 2 and plan.info.plan_hash == oracle.Oracle(wl).plan_hash
     d_old, d_new = wl.device_arenas(torch)
-    target = torch.empty(plan.info.recv_bytes, dtype=torch.uint8, device="cuda")
+    target = torch.empty(max(plan.info.recv_bytes, wl.recv_bytes), dtype=torch.uint8, device="cuda")
     dcr.check(dcr.dense_refit(plan, d_old, target))
     st = dcr.RecvState(plan, 0)
     payloads, all_counts = [], np.zeros(len(wl.tensors), dtype=np.int64)

@@ -28,7 +28,8 @@ class Case:
         self.start = self.orc.receiver_dense(self.olds)
 
     def target(self):
-        t = torch.zeros(max(self.plan.info.recv_bytes, 16), dtype=torch.uint8, device="cuda")
+        t = torch.zeros(max(self.plan.info.recv_bytes, self.wl.recv_bytes, 16), dtype=torch.uint8,
+                        device="cuda")
         dcr.check(dcr.dense_refit(self.plan, self.d_old, t))
         return t
 
