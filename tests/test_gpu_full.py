@@ -20,6 +20,14 @@ import bit_exact_xor_gb300 as dcr  # noqa: E402
 from wl import descs_of, to_device  # noqa: E402
 
 
+@pytest.fixture(autouse=True)
+def _release_memory():
+    yield
+    import gc
+    gc.collect()
+    torch.cuda.empty_cache()
+
+
 def encode_fit(plan, olds, news, w=0, mode=dcr.MODE_HYBRID, base=0, target=1, guess=None):
     """Encode with a payload buffer sized from a guess, growing it once on
     DCR_ERR_CAPACITY to the size the library reports."""
