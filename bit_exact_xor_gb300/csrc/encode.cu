@@ -1,10 +1,12 @@
-// Sender hot path: one persistent kernel that, per 64 KiB canonical chunk,
-// gathers old and new through the plan's shard->canonical pieces, forms
-// mask = old XOR new in shared memory, counts changed stored values, encodes
-// the chunk (LZ4 block, raw mask, overwrite records or dense overwrite) and
-// writes the frame straight to its final place in the stream, found by a
-// decoupled look-back over the frame sizes of earlier chunks.  A small second
-// kernel writes the frame index and the stream header.
+// Sender hot path: one persistent, warp-specialised kernel per window.
+//
+// Per 64 KiB canonical chunk it gathers old and new through the plan's
+// shard->canonical pieces, forms mask = old XOR new in shared memory, counts
+// changed stored values, encodes the chunk (LZ4 block, raw mask, overwrite
+// records or dense overwrite) and writes the frame straight to its final
+// place in the stream, found by a decoupled look-back over the frame sizes
+// of earlier chunks.  A small second kernel writes the frame index and the
+// stream header.
 //
 // Method: "GPU-accelerated weight teleportation", "Delta update algebra"
 // (mask = old XOR new on raw bits) and "A strong baseline with the
@@ -13,15 +15,26 @@
 // "Residual Conversion" and "Hybrid encoding and compression" (XOR masks for
 // affine changes, overwrites for residual ones).
 //
+// Structure.  One CTA per SM: 16 loader warps and 2 encoder warps share two
+// chunk buffers in shared memory.  Loader warp w gathers the contiguous 4 KiB
+// slice [4096 w, 4096 w + 4096) of the chunk with 16-byte streaming loads,
+// XORs old and new, counts changes, and appends the positions of the
+// non-zero mask bytes of its slice, in order, to its own list.  Encoder warp
+// b owns buffer b: it parses the chunk from those lists alone (work grows
+// with the number of non-zero bytes, not with the chunk size), waits for its
+// place in the stream and writes the frame, while the loaders already fill
+// the other buffer.  Named barriers hand the buffers back and forth.
+//
 // LZ4 parse.  The masks are long zero runs around sparse non-zero bytes, so
-// the encoder turns every zero run of at least 4 bytes into one match and
-// leaves everything else as literals.  A run is copied from the longest
-// earlier zero run when that one is long enough (non-overlapping copy), else
-// it keeps its first zero as a literal and copies from it with offset 1.
-// Every match therefore copies zero bytes only (frame flag ZSRC), the block
-// obeys the format's end rules (last 5 bytes literals, no match start in the
-// last 12 bytes), and the parse needs only three block-wide scans, so all
-// 512 threads of the CTA encode their own 128-byte slice in parallel.
+// every zero run of at least 4 bytes becomes one match and everything else
+// stays literal.  A run is copied from the longest earlier zero run when that
+// one is long enough (non-overlapping copy), else it keeps its first zero as a
+// literal and copies from it with offset 1.  Every match therefore copies zero
+// bytes only (frame flag ZSRC), and the block obeys the format's end rules
+// (last 5 bytes literals, no match start in the last 12 bytes).  Each of the
+// 32 encoder lanes walks an equal share of the non-zero positions; three warp
+// scans connect the shares (last non-zero byte and longest run so far, last
+// match end, output offset).
 #include <cuda_runtime.h>
 
 #include <climits>
@@ -32,12 +45,22 @@
 namespace dcr {
 namespace {
 
-constexpr int kThreads = 512;
-constexpr int kWarps = kThreads / 32;
-constexpr int kNVec = kChunk / 16;            // 16-byte vectors per chunk
-constexpr int kVPT = kNVec / kThreads;        // vectors per thread (8)
-constexpr int kSegCache = 128;                // sender pieces cached in smem
-constexpr uint32_t kSpinLimit = 1u << 22;     // bounded look-back wait
+constexpr int kLoaders = 16;                      // loader warps
+constexpr int kEncoders = 3;                      // encoder warps = chunk buffers
+constexpr int kThreads = 32 * (kLoaders + kEncoders);
+constexpr int kLoaderThreads = 32 * kLoaders;
+constexpr int kNVec = kChunk / 16;                // 16-byte vectors per chunk
+constexpr int kVecPerWarp = kNVec / kLoaders;     // 256: a 4 KiB slice
+constexpr int kVPL = kVecPerWarp / 32;            // 8 vectors per lane
+constexpr int kWords = kChunk / 32;               // bitmap words per chunk
+constexpr int kWordsPerLane = kWords / 32;        // 64: encoder lane share = 2 KiB
+constexpr uint32_t kEnd = 0xFFFFFFFFu;
+constexpr uint32_t kSpinLimit = 1u << 22;         // bounded look-back wait
+
+// named barriers (0 is left to __syncthreads, unused here)
+constexpr int kBarLoaders = 1;
+constexpr int kBarEmpty = 2;                   // + buffer
+constexpr int kBarFull = 2 + kEncoders;        // + buffer
 
 struct EncArgs {
     const ChunkDesc* chunks;
@@ -54,16 +77,16 @@ struct EncArgs {
     uint32_t* fsize;
 };
 
+struct __align__(16) Buf {
+    uint4 data[kNVec];                 // mask (XOR chunks) or new bytes (overwrite chunks)
+    uint32_t bits[kWords];             // bit i set iff mask byte i != 0
+    uint32_t chg[kLoaders];            // changed stored values per slice
+    uint32_t k;                        // window-relative chunk, or kEnd
+    uint32_t pad[3];
+};
+
 struct __align__(16) Smem {
-    uint4 buf[kNVec];          // mask (XOR chunks) or new bytes (overwrite chunks)
-    uint16_t nz[kNVec];        // per vector: bit i set iff mask byte i != 0
-    Seg segs[kSegCache];
-    int scan_i[2][kWarps];
-    unsigned long long scan_u[2][kWarps];
-    uint32_t red;
-    uint32_t k;
-    uint32_t flag;
-    uint64_t frame_off;
+    Buf buf[kEncoders];
 };
 
 // ---------------------------------------------------------------- helpers --
@@ -88,6 +111,16 @@ __device__ __forceinline__ uint64_t ld_acquire(const uint64_t* p)
     return v;
 }
 
+__device__ __forceinline__ void bar_sync(int id, int n)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+__device__ __forceinline__ void bar_arrive(int id, int n)
+{
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
 // 4-bit mask of the non-zero bytes of w (bit i <-> byte i)
 __device__ __forceinline__ uint32_t nz4(uint32_t w)
 {
@@ -100,14 +133,14 @@ __device__ __forceinline__ uint32_t nz16(uint4 v)
     return nz4(v.x) | (nz4(v.y) << 4) | (nz4(v.z) << 8) | (nz4(v.w) << 12);
 }
 
-// changed stored values in a 16-byte vector whose non-zero-byte mask is m
-// (bf16: 16-bit words; e4m3: bytes) or whose words are w (e2m1: nibbles)
+// changed stored values in a 16-byte mask vector with non-zero-byte mask m
+// (bf16: 16-bit words; e4m3: bytes; e2m1: nibbles)
 __device__ __forceinline__ uint32_t changed_in(uint32_t m, uint4 v, uint32_t bits)
 {
     if (bits == 16) return __popc((m | (m >> 1)) & 0x5555u);
     if (bits == 8) return __popc(m);
     uint32_t c = 0;
-    uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         uint32_t t = w[i] | (w[i] >> 1);
@@ -139,10 +172,10 @@ __device__ __forceinline__ uint32_t seq_bytes(uint32_t ll, uint32_t ml)
     return 1 + ext_len(ll) + ll + 2 + ext_len(ml - 4);
 }
 
-// ---- block-wide scans --------------------------------------------------
-// zero-run summary of a byte range: first/last non-zero position and the
-// longest zero run strictly between two non-zero bytes, packed (len << 32 |
-// start).  first == INT_MAX marks a range without non-zero bytes.
+// ---- zero-run summaries ----------------------------------------------------
+// first/last non-zero position of a range and the longest zero run strictly
+// between two of its non-zero bytes, packed (len << 32 | start).
+// first == INT_MAX marks a range without non-zero bytes.
 struct RunSum {
     int first, last;
     unsigned long long best;
@@ -162,90 +195,88 @@ __device__ __forceinline__ RunSum combine(RunSum a, RunSum b)
     return r;
 }
 
-__device__ __forceinline__ RunSum shfl_up_sum(RunSum v, int d)
+__device__ __forceinline__ RunSum warp_excl_runs(RunSum v, int lane)
 {
-    RunSum r;
-    r.first = __shfl_up_sync(0xffffffffu, v.first, d);
-    r.last = __shfl_up_sync(0xffffffffu, v.last, d);
-    r.best = __shfl_up_sync(0xffffffffu, v.best, d);
-    return r;
-}
-
-// exclusive scan of RunSum over the block (thread order = byte order)
-__device__ RunSum scan_runs(RunSum v, Smem& S)
-{
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     RunSum inc = v;
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
-        RunSum o = shfl_up_sum(inc, d);
+        RunSum o;
+        o.first = __shfl_up_sync(0xffffffffu, inc.first, d);
+        o.last = __shfl_up_sync(0xffffffffu, inc.last, d);
+        o.best = __shfl_up_sync(0xffffffffu, inc.best, d);
         if (lane >= d) inc = combine(o, inc);
     }
-    RunSum exc = shfl_up_sum(inc, 1);
-    if (lane == 0) exc = RunSum{INT_MAX, 0, 0ull};
-    if (lane == 31) {
-        S.scan_i[0][w] = inc.first;
-        S.scan_i[1][w] = inc.last;
-        S.scan_u[0][w] = inc.best;
-    }
-    __syncthreads();
-    RunSum pre{INT_MAX, 0, 0ull};
-    for (int k = 0; k < w; ++k) pre = combine(pre, RunSum{S.scan_i[0][k], S.scan_i[1][k], S.scan_u[0][k]});
-    __syncthreads();
-    return combine(pre, exc);
+    RunSum e;
+    e.first = __shfl_up_sync(0xffffffffu, inc.first, 1);
+    e.last = __shfl_up_sync(0xffffffffu, inc.last, 1);
+    e.best = __shfl_up_sync(0xffffffffu, inc.best, 1);
+    if (lane == 0) e = RunSum{INT_MAX, 0, 0ull};
+    return e;
 }
 
-// exclusive max (of non-negative ints) over the block
-__device__ int scan_max(int v, Smem& S)
+__device__ __forceinline__ int warp_excl_max(int v, int lane)
 {
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     int inc = v;
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
         int o = __shfl_up_sync(0xffffffffu, inc, d);
         if (lane >= d) inc = max(inc, o);
     }
-    int exc = __shfl_up_sync(0xffffffffu, inc, 1);
-    if (lane == 0) exc = 0;
-    if (lane == 31) S.scan_i[0][w] = inc;
-    __syncthreads();
-    int pre = 0;
-    for (int k = 0; k < w; ++k) pre = max(pre, S.scan_i[0][k]);
-    __syncthreads();
-    return max(pre, exc);
+    int e = __shfl_up_sync(0xffffffffu, inc, 1);
+    return lane == 0 ? INT_MIN : e;
 }
 
-// exclusive sum over the block; *total gets the block total
-__device__ uint32_t scan_sum(uint32_t v, Smem& S, uint32_t* total)
+__device__ __forceinline__ uint32_t warp_excl_sum(uint32_t v, int lane, uint32_t* total)
 {
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     uint32_t inc = v;
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
         uint32_t o = __shfl_up_sync(0xffffffffu, inc, d);
         if (lane >= d) inc += o;
     }
-    if (lane == 31) S.scan_i[0][w] = int(inc);
-    __syncthreads();
-    uint32_t pre = 0, tot = 0;
-    for (int k = 0; k < kWarps; ++k) {
-        uint32_t x = uint32_t(S.scan_i[0][k]);
-        if (k < w) pre += x;
-        tot += x;
-    }
-    __syncthreads();
-    *total = tot;
-    return pre + inc - v;
+    *total = __shfl_sync(0xffffffffu, inc, 31);
+    return inc - v;
 }
 
-// ---- per-thread zero-run walk --------------------------------------------
-// Decides, for every zero run that ends in this thread's slice, whether it
-// becomes a match.  prev: last non-zero byte before the slice (-1: virtual
-// non-zero before the chunk); best: longest earlier zero run (len << 32 |
-// start).  Emit(ms, me, off) is called for every match in order.
+// Calls f(position) for every set bit of a lane's bitmap share, in order
+// (the lane owns bytes [2048 lane, 2048 lane + 2048) of the chunk).  Empty
+// 128-byte stretches are skipped four words at a time.
+template <class F>
+__device__ __forceinline__ void for_bits(const Buf* B, int lane, F f)
+{
+    const uint4* q = reinterpret_cast<const uint4*>(B->bits) + lane * (kWordsPerLane / 4);
+#pragma unroll 1
+    for (int i = 0; i < kWordsPerLane / 4; ++i) {
+        const uint4 v = q[i];
+        if ((v.x | v.y | v.z | v.w) == 0) continue;
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        const int base = (lane * kWordsPerLane + 4 * i) * 32;
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+            uint32_t b = w[h];
+            while (b) {
+                const int t = __ffs(b) - 1;
+                b &= b - 1;
+                f(base + 32 * h + t);
+            }
+        }
+    }
+}
+
+// overwrite units of a bitmap word: bit i set iff unit starting at byte i
+// (ub = 2: even i only) has a non-zero mask byte
+__device__ __forceinline__ uint32_t unit_bits(uint32_t b, uint32_t ub)
+{
+    return ub == 2 ? (b | (b >> 1)) & 0x55555555u : b;
+}
+
+// Decides, for every zero run that ends at one of this lane's non-zero bytes
+// (and the trailing run for the last lane), whether it becomes a match.
+// prev: last non-zero byte before the share (-1: virtual non-zero before the
+// chunk); best: longest earlier zero run.  emit(ms, me, off) per match.
 template <class Emit>
-__device__ __forceinline__ void walk_runs(const uint32_t bm[4], int lo, int raw, bool last_thread,
-                                          int prev, unsigned long long best, Emit emit)
+__device__ __forceinline__ void walk_runs(const Buf* B, int lane, int raw, bool tail, int prev,
+                                          unsigned long long best, Emit emit)
 {
     auto gap = [&](int q) {
         int gs = prev + 1;
@@ -264,20 +295,12 @@ __device__ __forceinline__ void walk_runs(const uint32_t bm[4], int lo, int raw,
         }
         prev = q;
     };
-#pragma unroll 1
-    for (int k = 0; k < 4; ++k) {
-        uint32_t b = bm[k];
-        while (b) {
-            int i = __ffs(b) - 1;
-            b &= b - 1;
-            gap(lo + 32 * k + i);
-        }
-    }
-    if (last_thread) gap(raw);
+    for_bits(B, lane, gap);
+    if (tail) gap(raw);
 }
 
-// Byte writer confined to one thread's slice [p, end) of the frame body: a
-// sequence that would not fit is dropped and flagged instead of written.
+// Byte writer confined to one lane's part [p, end) of the frame body: bytes
+// that would fall outside are dropped and flagged instead of written.
 struct Out {
     uint8_t* o;
     uint32_t p, end;
@@ -314,294 +337,307 @@ __device__ __forceinline__ void put_seq(Out& w, const uint8_t* mask, uint32_t li
     if (mc >= 15) put_len(w, mc);
 }
 
+// ---------------------------------------------------------------- loaders --
+// Gather, XOR, count and list one chunk's 4 KiB slice (loader warp w).
+__device__ __forceinline__ void load_slice(const EncArgs& A, Buf& B, const ChunkDesc& cd, bool overwrite,
+                                           int w, int lane)
+{
+    const int raw = int(cd.raw_len);
+    const Seg* segs = A.src + cd.src_begin;
+    const int nseg = int(cd.src_count);
+    uint8_t* bytes = reinterpret_cast<uint8_t*>(B.data);
+    uint32_t changed = 0;
+    const int v0 = w * kVecPerWarp;
+
+    // bitmap word of the vector pair (v, v + 1) held by lanes (even, odd)
+    auto list_vec = [&](int v, uint32_t z) {
+        const uint32_t hi = __shfl_down_sync(0xffffffffu, z, 1);
+        if ((lane & 1) == 0) B.bits[v >> 1] = z | (hi << 16);
+    };
+
+    if (cd.flags & kSrcVec) {
+        const int nvec = raw >> 4;
+        uint4 o[kVPL], n[kVPL];
+        int cur = 0;
+#pragma unroll
+        for (int j = 0; j < kVPL; ++j) {
+            const int v = v0 + j * 32 + lane;
+            o[j] = n[j] = make_uint4(0, 0, 0, 0);
+            if (v < nvec) {
+                const uint32_t x = uint32_t(v) << 4;
+                if (nseg > 1) {
+                    if (j == 0) cur = find_seg(segs, nseg, x);
+                    while (cur + 1 < nseg && segs[cur + 1].off <= x) ++cur;
+                }
+                const Seg sg = segs[cur];
+                const uint32_t r = uint32_t(sg.addr >> kShardShift);
+                const uint64_t a = (sg.addr & kAddrMask) + (x - sg.off);
+                o[j] = ld_stream(A.olds[r] + a);
+                n[j] = ld_stream(A.news[r] + a);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < kVPL; ++j) {
+            const int v = v0 + j * 32 + lane;
+            uint4 m = make_uint4(o[j].x ^ n[j].x, o[j].y ^ n[j].y, o[j].z ^ n[j].z, o[j].w ^ n[j].w);
+            uint32_t z = nz16(m);
+            changed += changed_in(z, m, cd.bits);
+            B.data[v] = overwrite ? n[j] : m;
+            list_vec(v, z);
+        }
+    } else {
+        // unaligned pieces: byte-wise gather (layouts with odd row sizes).
+        // The mask is staged first; overwrite chunks then restage new bytes.
+        for (int pass = 0; pass < (overwrite ? 2 : 1); ++pass) {
+            for (int i = lane; i < 16 * kVecPerWarp; i += 32) {
+                const int x = 16 * v0 + i;
+                uint8_t ob = 0, nb = 0;
+                if (x < raw) {
+                    const Seg sg = segs[find_seg(segs, nseg, uint32_t(x))];
+                    const uint32_t r = uint32_t(sg.addr >> kShardShift);
+                    const uint64_t a = (sg.addr & kAddrMask) + (uint32_t(x) - sg.off);
+                    ob = A.olds[r][a];
+                    nb = A.news[r][a];
+                }
+                bytes[x] = pass == 1 ? nb : uint8_t(ob ^ nb);
+            }
+            __syncwarp();
+            if (pass == 0) {
+                for (int j = 0; j < kVPL; ++j) {
+                    const int v = v0 + j * 32 + lane;
+                    const uint4 m = B.data[v];
+                    const uint32_t z = nz16(m);
+                    changed += changed_in(z, m, cd.bits);
+                    list_vec(v, z);
+                }
+                __syncwarp();
+            }
+        }
+    }
+    changed = __reduce_add_sync(0xffffffffu, changed);
+    if (lane == 0) B.chg[w] = changed;
+}
+
+// ---------------------------------------------------------------- encoder --
+// Parse, place and write the frame of the chunk held in buffer B.
+__device__ __forceinline__ void encode_chunk(const EncArgs& A, Buf& B, uint32_t k, int lane)
+{
+    const ChunkDesc cd = A.chunks[A.chunk_begin + k];
+    const int raw = int(cd.raw_len);
+    const bool overwrite = (cd.flags & kResidualFlag) || A.mode == DCR_MODE_OVERWRITE_ONLY;
+    const uint8_t* bytes = reinterpret_cast<const uint8_t*>(B.data);
+
+    uint32_t chg = lane < kLoaders ? B.chg[lane] : 0u;
+    chg = __reduce_add_sync(0xffffffffu, chg);
+    if (lane == 0 && chg) {
+        atomicAdd(&A.counts[cd.tensor], (unsigned long long)chg);
+        atomicAdd(reinterpret_cast<unsigned long long*>(&A.sc->changed), (unsigned long long)chg);
+    }
+
+    uint32_t kind = 0, body_len = 0, my_off = 0, my_sz = 0;
+    int prev_last = -1, lit0 = 0;
+    unsigned long long best0 = 0ull;
+    uint32_t n_units = 0;
+
+    if (chg && !overwrite) {
+        // pass 1: run summary of this lane's share
+        RunSum mine{INT_MAX, 0, 0ull};
+        for_bits(&B, lane, [&](int p) { mine = combine(mine, RunSum{p, p, 0ull}); });
+        if (lane == 0) mine = combine(RunSum{-1, -1, 0ull}, mine);
+        const RunSum pr = warp_excl_runs(mine, lane);
+        prev_last = lane == 0 ? -1 : pr.last;
+        best0 = lane == 0 ? 0ull : pr.best;
+        // pass 2: matches of this share
+        int first_ms = -1, first_ml = 0, last_me = 0;
+        uint32_t rest = 0;
+        walk_runs(&B, lane, raw, lane == 31, prev_last, best0, [&](int ms, int me, int) {
+            if (first_ms < 0) {
+                first_ms = ms;
+                first_ml = me - ms;
+            } else {
+                rest += seq_bytes(uint32_t(ms - last_me), uint32_t(me - ms));
+            }
+            last_me = me;
+        });
+        lit0 = max(warp_excl_max(first_ms >= 0 ? last_me : 0, lane), 0);
+        uint32_t sz = 0;
+        if (first_ms >= 0) sz = seq_bytes(uint32_t(first_ms - lit0), uint32_t(first_ml)) + rest;
+        if (lane == 31) {
+            const uint32_t ll = uint32_t(raw - (first_ms >= 0 ? last_me : lit0));
+            sz += 1 + ext_len(ll) + ll;
+        }
+        uint32_t total;
+        my_off = warp_excl_sum(sz, lane, &total);
+        my_sz = sz;
+        if (total < uint32_t(raw)) {
+            kind = kXorLz4;
+            body_len = total;
+        } else {
+            kind = kXorRaw;
+            body_len = uint32_t(raw);
+        }
+    } else if (chg) {
+        // overwrite records: one per changed unit (2 bytes for bf16, else 1)
+        const uint32_t ub = cd.bits == 16 ? 2u : 1u;
+        uint32_t units = 0;
+        const uint32_t* wb = B.bits + lane * kWordsPerLane;
+        for (int i = 0; i < kWordsPerLane; ++i) units += __popc(unit_bits(wb[i], ub));
+        uint32_t total;
+        my_off = warp_excl_sum(units, lane, &total);
+        n_units = total;
+        const uint32_t pad = (4 - (2 * total) % 4) % 4;
+        const uint32_t rec = 4 + 2 * total + pad + total * ub;
+        if (rec < uint32_t(raw)) {
+            kind = kOverwrite;
+            body_len = rec;
+        } else {
+            kind = kOverwriteDense;
+            body_len = uint32_t(raw);
+        }
+    }
+    const uint32_t fsz = chg ? (kFrameHdr + body_len + 15) / 16 * 16 : 0u;
+
+    // ---- decoupled look-back for the frame's place in the stream
+    uint64_t excl = 0;
+    int ok = 1;
+    if (lane == 0) {
+        const uint64_t agg = fsz ? ((1ull << kLbFrameShift) | fsz) : 0ull;
+        if (k == 0) {
+            st_release(&A.lb[0], kLbInc | agg);
+        } else {
+            st_release(&A.lb[k], kLbAgg | agg);
+            for (int64_t j = int64_t(k) - 1; j >= 0; --j) {
+                uint64_t v = ld_acquire(&A.lb[j]);
+                uint32_t spins = 0;
+                while ((v >> 62) == 0) {
+                    if (++spins > kSpinLimit || *(volatile int32_t*)&A.sc->err) {
+                        ok = 0;
+                        break;
+                    }
+                    __nanosleep(64);
+                    v = ld_acquire(&A.lb[j]);
+                }
+                if (!ok) break;
+                excl += v & kLbValMask;
+                if ((v >> 62) == 2) break;
+            }
+            if (ok) st_release(&A.lb[k], kLbInc | (excl + agg));
+            else atomicCAS(reinterpret_cast<int*>(&A.sc->err), 0, DCR_ERR_TIMEOUT);
+        }
+        A.fsize[k] = fsz;
+    }
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    excl = __shfl_sync(0xffffffffu, excl, 0);
+    if (!ok) return;
+
+    // ---- write the frame
+    const uint64_t foff = kStreamHdr + (excl & kLbByteMask);
+    if (!fsz || foff + fsz > A.cap) return;
+    uint8_t* f = A.payload + foff;
+    uint8_t* body = f + kFrameHdr;
+    if (lane == 0) {
+        const uint32_t h1 = kind | (cd.bits << 8) | ((kind == kXorLz4 ? kFrameZsrc : 0u) << 16);
+        reinterpret_cast<uint4*>(f)[0] = make_uint4(kFrameMagic, h1, A.chunk_begin + k, uint32_t(raw));
+        reinterpret_cast<uint4*>(f)[1] = make_uint4(body_len, chg, 0u, 0u);
+    }
+    for (uint32_t i = kFrameHdr + body_len + lane; i < fsz; i += 32) f[i] = 0;
+    if (kind == kXorLz4) {
+        const uint32_t end = my_off + my_sz < body_len ? my_off + my_sz : body_len;
+        Out o{body, my_off, end, false};
+        int lit = lit0;
+        walk_runs(&B, lane, raw, lane == 31, prev_last, best0, [&](int ms, int me, int off) {
+            put_seq(o, bytes, uint32_t(lit), uint32_t(ms - lit), uint32_t(off), uint32_t(me - ms), false);
+            lit = me;
+        });
+        if (lane == 31) put_seq(o, bytes, uint32_t(lit), uint32_t(raw - lit), 0, 0, true);
+        if (o.over || o.p != my_off + my_sz)   // sizing and emission disagree
+            atomicCAS(reinterpret_cast<int*>(&A.sc->err), 0, DCR_ERR_CORRUPT);
+    } else if (kind == kXorRaw || kind == kOverwriteDense) {
+        const int nfull = raw >> 4;
+        for (int v = lane; v < nfull; v += 32) reinterpret_cast<uint4*>(body)[v] = B.data[v];
+        for (int x = (nfull << 4) + lane; x < raw; x += 32) body[x] = bytes[x];
+    } else {
+        const uint32_t ub = cd.bits == 16 ? 2u : 1u;
+        const uint32_t pad = (4 - (2 * n_units) % 4) % 4;
+        if (lane == 0) {
+            *reinterpret_cast<uint32_t*>(body) = n_units;
+            for (uint32_t i = 0; i < pad; ++i) body[4 + 2 * n_units + i] = 0;
+        }
+        uint8_t* offs = body + 4;
+        uint8_t* vals = body + 4 + 2 * n_units + pad;
+        uint32_t u_i = my_off;
+        const uint32_t* wb = B.bits + lane * kWordsPerLane;
+        for (int i = 0; i < kWordsPerLane; ++i) {
+            uint32_t b = unit_bits(wb[i], ub);
+            while (b) {
+                const uint32_t x = uint32_t((lane * kWordsPerLane + i) * 32 + __ffs(b) - 1);
+                b &= b - 1;
+                const uint32_t u = x / ub;
+                if (u_i < n_units) {
+                    offs[2 * u_i] = uint8_t(u);
+                    offs[2 * u_i + 1] = uint8_t(u >> 8);
+                    for (uint32_t e = 0; e < ub; ++e) vals[u_i * ub + e] = bytes[x + e];
+                }
+                ++u_i;
+            }
+        }
+    }
+}
+
 // ================================================================ kernel ==
-__global__ void __launch_bounds__(kThreads, 2) encode_kernel(EncArgs A)
+__global__ void __launch_bounds__(kThreads, 1) encode_kernel(EncArgs A)
 {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     Smem& S = *reinterpret_cast<Smem*>(smem_raw);
-    const int t = threadIdx.x;
-    uint8_t* bytes = reinterpret_cast<uint8_t*>(S.buf);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    for (;;) {
-        if (t == 0) {
+    if (warp >= kLoaders) {
+        // encoder warp: owns buffer b
+        const int b = warp - kLoaders;
+        Buf& B = S.buf[b];
+        __threadfence_block();
+        bar_arrive(kBarEmpty + b, kLoaderThreads + 32);
+        for (;;) {
+            bar_sync(kBarFull + b, kLoaderThreads + 32);
+            const uint32_t k = B.k;
+            if (k == kEnd) break;
+            encode_chunk(A, B, k, lane);
+            __syncwarp();
+            __threadfence_block();
+            bar_arrive(kBarEmpty + b, kLoaderThreads + 32);
+        }
+        return;
+    }
+
+    // loader warps
+    for (int b = 0;; b = b + 1 == kEncoders ? 0 : b + 1) {
+        Buf& B = S.buf[b];
+        bar_sync(kBarEmpty + b, kLoaderThreads + 32);
+        if (threadIdx.x == 0) {
             uint32_t k = atomicAdd(&A.sc->ticket, 1u);
-            if (*(volatile int32_t*)&A.sc->err) k = UINT32_MAX;
-            S.k = k;
-            S.red = 0;
+            if (k >= A.chunk_count || *(volatile int32_t*)&A.sc->err) k = kEnd;
+            B.k = k;
         }
-        __syncthreads();
-        const uint32_t k = S.k;
-        if (k >= A.chunk_count) break;
+        bar_sync(kBarLoaders, kLoaderThreads);
+        const uint32_t k = B.k;
+        if (k == kEnd) {
+            // no chunk left: release every encoder warp, each once it is idle
+            __threadfence_block();
+            bar_arrive(kBarFull + b, kLoaderThreads + 32);
+            for (int d = 1; d < kEncoders; ++d) {
+                const int o = (b + d) % kEncoders;
+                bar_sync(kBarEmpty + o, kLoaderThreads + 32);
+                if (threadIdx.x == 0) S.buf[o].k = kEnd;
+                __threadfence_block();
+                bar_arrive(kBarFull + o, kLoaderThreads + 32);
+            }
+            break;
+        }
         const ChunkDesc cd = A.chunks[A.chunk_begin + k];
-        const int raw = int(cd.raw_len);
         const bool overwrite = (cd.flags & kResidualFlag) || A.mode == DCR_MODE_OVERWRITE_ONLY;
-        const Seg* segs = A.src + cd.src_begin;
-        const int nseg = int(cd.src_count);
-        if (nseg > 1 && nseg <= kSegCache) {
-            for (int i = t; i < nseg; i += kThreads) S.segs[i] = segs[i];
-            __syncthreads();
-            segs = S.segs;
-        }
-
-        // ---- gather old/new through the plan, XOR, per-vector masks, counts
-        uint32_t my_changed = 0;
-        if (cd.flags & kSrcVec) {
-            const int nvec = raw >> 4;
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                uint4 o[kVPT / 2], n[kVPT / 2];
-#pragma unroll
-                for (int j = 0; j < kVPT / 2; ++j) {
-                    int v = t + (h * (kVPT / 2) + j) * kThreads;
-                    o[j] = n[j] = make_uint4(0, 0, 0, 0);
-                    if (v < nvec) {
-                        uint32_t x = uint32_t(v) << 4;
-                        const Seg sg = nseg == 1 ? segs[0] : segs[find_seg(segs, nseg, x)];
-                        uint32_t r = uint32_t(sg.addr >> kShardShift);
-                        uint64_t a = (sg.addr & kAddrMask) + (x - sg.off);
-                        o[j] = ld_stream(A.olds[r] + a);
-                        n[j] = ld_stream(A.news[r] + a);
-                    }
-                }
-#pragma unroll
-                for (int j = 0; j < kVPT / 2; ++j) {
-                    int v = t + (h * (kVPT / 2) + j) * kThreads;
-                    uint4 m = make_uint4(o[j].x ^ n[j].x, o[j].y ^ n[j].y, o[j].z ^ n[j].z, o[j].w ^ n[j].w);
-                    uint32_t z = nz16(m);
-                    my_changed += changed_in(z, m, cd.bits);
-                    S.buf[v] = overwrite ? n[j] : m;
-                    S.nz[v] = uint16_t(z);
-                }
-            }
-        } else {
-            // unaligned pieces: byte-wise gather (layouts with odd row sizes).
-            // Pass 1 stages the mask; overwrite chunks then restage new bytes.
-            for (int pass = 0; pass < (overwrite ? 2 : 1); ++pass) {
-                if (pass == 1) {
-                    for (int v = t; v < kNVec; v += kThreads) {
-                        uint4 m = S.buf[v];
-                        uint32_t z = nz16(m);
-                        my_changed += changed_in(z, m, cd.bits);
-                        S.nz[v] = uint16_t(z);
-                    }
-                    __syncthreads();
-                }
-                for (int x = t; x < int(kChunk); x += kThreads) {
-                    uint8_t ob = 0, nb = 0;
-                    if (x < raw) {
-                        const Seg sg = segs[find_seg(segs, nseg, uint32_t(x))];
-                        uint32_t r = uint32_t(sg.addr >> kShardShift);
-                        uint64_t a = (sg.addr & kAddrMask) + (uint32_t(x) - sg.off);
-                        ob = A.olds[r][a];
-                        nb = A.news[r][a];
-                    }
-                    bytes[x] = pass == 1 ? nb : uint8_t(ob ^ nb);
-                }
-                __syncthreads();
-            }
-            if (!overwrite) {
-                for (int v = t; v < kNVec; v += kThreads) {
-                    uint4 m = S.buf[v];
-                    uint32_t z = nz16(m);
-                    my_changed += changed_in(z, m, cd.bits);
-                    S.nz[v] = uint16_t(z);
-                }
-            }
-        }
-        my_changed = __reduce_add_sync(0xffffffffu, my_changed);
-        if ((t & 31) == 0 && my_changed) atomicAdd(&S.red, my_changed);
-        __syncthreads();
-        const uint32_t changed = S.red;
-        if (t == 0 && changed) {
-            atomicAdd(&A.counts[cd.tensor], (unsigned long long)changed);
-            atomicAdd(reinterpret_cast<unsigned long long*>(&A.sc->changed), (unsigned long long)changed);
-        }
-
-        // ---- plan this chunk's frame body
-        const int lo = t * 128;
-        uint32_t bm[4];
-        {
-            uint4 z = reinterpret_cast<const uint4*>(S.nz)[t];
-            bm[0] = z.x; bm[1] = z.y; bm[2] = z.z; bm[3] = z.w;
-        }
-        const int t_last = raw > 0 ? (raw - 1) >> 7 : 0;
-        uint32_t kind = 0, body_len = 0, my_off = 0, my_first_lit = 0, n_units = 0, my_sz = 0;
-        int prev_last = -1;
-        unsigned long long best0 = 0ull;
-        if (changed) {
-            if (!overwrite) {
-                // scan A: zero-run summaries (thread 0 starts after a virtual
-                // non-zero byte at -1, so the leading run counts as a run)
-                RunSum mine{INT_MAX, 0, 0ull};
-#pragma unroll 1
-                for (int q = 0; q < 4; ++q) {
-                    uint32_t b = bm[q];
-                    while (b) {
-                        int i = __ffs(b) - 1;
-                        b &= b - 1;
-                        RunSum one{lo + 32 * q + i, lo + 32 * q + i, 0ull};
-                        mine = combine(mine, one);
-                    }
-                }
-                if (t == 0) mine = combine(RunSum{-1, -1, 0ull}, mine);
-                RunSum pre = scan_runs(mine, S);
-                prev_last = t == 0 ? -1 : pre.last;
-                best0 = t == 0 ? 0ull : pre.best;
-                // pass 1: matches of this slice -> last match end (scan C)
-                int first_ms = -1, first_ml = 0, last_me = 0;
-                uint32_t rest = 0;
-                bool active = lo < raw;
-                if (active) {
-                    walk_runs(bm, lo, raw, t == t_last, prev_last, best0, [&](int ms, int me, int) {
-                        if (first_ms < 0) {
-                            first_ms = ms;
-                            first_ml = me - ms;
-                        } else {
-                            rest += seq_bytes(uint32_t(ms - last_me), uint32_t(me - ms));
-                        }
-                        last_me = me;
-                    });
-                }
-                int lit0 = scan_max(first_ms >= 0 ? last_me : 0, S);
-                // sizes (scan D)
-                uint32_t sz = 0;
-                if (first_ms >= 0) sz = seq_bytes(uint32_t(first_ms - lit0), uint32_t(first_ml)) + rest;
-                if (active && t == t_last) {
-                    uint32_t ll = uint32_t(raw - (first_ms >= 0 ? last_me : lit0));
-                    sz += 1 + ext_len(ll) + ll;
-                }
-                uint32_t total;
-                my_off = scan_sum(sz, S, &total);
-                my_sz = sz;
-                my_first_lit = uint32_t(lit0);
-                if (total < uint32_t(raw)) {
-                    kind = kXorLz4;
-                    body_len = total;
-                } else {
-                    kind = kXorRaw;
-                    body_len = uint32_t(raw);
-                }
-            } else {
-                const uint32_t ub = cd.bits == 16 ? 2u : 1u;
-                uint32_t units = 0;
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    units += ub == 2 ? __popc((bm[q] | (bm[q] >> 1)) & 0x55555555u) : __popc(bm[q]);
-                uint32_t total;
-                my_off = scan_sum(units, S, &total);
-                n_units = total;
-                uint32_t pad = (4 - (2 * total) % 4) % 4;
-                uint32_t rec = 4 + 2 * total + pad + total * ub;
-                if (rec < uint32_t(raw)) {
-                    kind = kOverwrite;
-                    body_len = rec;
-                } else {
-                    kind = kOverwriteDense;
-                    body_len = uint32_t(raw);
-                }
-            }
-        }
-        const uint32_t fsz = changed ? (kFrameHdr + body_len + 15) / 16 * 16 : 0u;
-
-        // ---- decoupled look-back for the frame's place in the stream
-        if (t == 0) {
-            uint64_t agg = fsz ? ((1ull << kLbFrameShift) | fsz) : 0ull;
-            uint64_t excl = 0;
-            bool ok = true;
-            if (k == 0) {
-                st_release(&A.lb[0], kLbInc | agg);
-            } else {
-                st_release(&A.lb[k], kLbAgg | agg);
-                for (int64_t j = int64_t(k) - 1; j >= 0; --j) {
-                    uint64_t v = ld_acquire(&A.lb[j]);
-                    uint32_t spins = 0;
-                    while ((v >> 62) == 0) {
-                        if (++spins > kSpinLimit || *(volatile int32_t*)&A.sc->err) {
-                            ok = false;
-                            break;
-                        }
-                        __nanosleep(64);
-                        v = ld_acquire(&A.lb[j]);
-                    }
-                    if (!ok) break;
-                    excl += v & kLbValMask;
-                    if ((v >> 62) == 2) break;
-                }
-                if (ok) st_release(&A.lb[k], kLbInc | (excl + agg));
-                else atomicCAS(reinterpret_cast<int*>(&A.sc->err), 0, DCR_ERR_TIMEOUT);
-            }
-            A.fsize[k] = fsz;
-            S.frame_off = excl & kLbByteMask;
-            S.flag = ok;
-        }
-        __syncthreads();
-        if (!S.flag) break;
-
-        // ---- write the frame
-        const uint64_t foff = kStreamHdr + S.frame_off;
-        if (fsz && foff + fsz <= A.cap) {
-            uint8_t* f = A.payload + foff;
-            uint8_t* body = f + kFrameHdr;
-            if (t == 0) {
-                uint32_t h[8];
-                h[0] = kFrameMagic;
-                h[1] = kind | (cd.bits << 8) | ((kind == kXorLz4 ? kFrameZsrc : 0u) << 16);
-                h[2] = A.chunk_begin + k;
-                h[3] = uint32_t(raw);
-                h[4] = body_len;
-                h[5] = changed;
-                h[6] = 0;
-                h[7] = 0;
-                reinterpret_cast<uint4*>(f)[0] = make_uint4(h[0], h[1], h[2], h[3]);
-                reinterpret_cast<uint4*>(f)[1] = make_uint4(h[4], h[5], h[6], h[7]);
-                for (uint32_t i = kFrameHdr + body_len; i < fsz; ++i) f[i] = 0;
-            }
-            if (kind == kXorLz4) {
-                if (lo < raw) {
-                    const uint32_t end = my_off + my_sz < body_len ? my_off + my_sz : body_len;
-                    Out w{body, my_off, end, false};
-                    int lit = int(my_first_lit);
-                    walk_runs(bm, lo, raw, t == t_last, prev_last, best0, [&](int ms, int me, int off) {
-                        put_seq(w, bytes, uint32_t(lit), uint32_t(ms - lit), uint32_t(off), uint32_t(me - ms),
-                                false);
-                        lit = me;
-                    });
-                    if (t == t_last) put_seq(w, bytes, uint32_t(lit), uint32_t(raw - lit), 0, 0, true);
-                    if (w.over || w.p != my_off + my_sz)   // sizing and emission disagree
-                        atomicCAS(reinterpret_cast<int*>(&A.sc->err), 0, DCR_ERR_CORRUPT);
-                }
-            } else if (kind == kXorRaw || kind == kOverwriteDense) {
-                const int nfull = raw >> 4;
-                for (int v = t; v < nfull; v += kThreads) reinterpret_cast<uint4*>(body)[v] = S.buf[v];
-                for (int x = (nfull << 4) + t; x < raw; x += kThreads) body[x] = bytes[x];
-            } else {
-                const uint32_t ub = cd.bits == 16 ? 2u : 1u;
-                const uint32_t total_units = n_units;
-                if (t == 0) *reinterpret_cast<uint32_t*>(body) = total_units;
-                uint32_t pad = (4 - (2 * total_units) % 4) % 4;
-                uint8_t* offs = body + 4;
-                uint8_t* vals = body + 4 + 2 * total_units + pad;
-                if (t == 0)
-                    for (uint32_t i = 0; i < pad; ++i) offs[2 * total_units + i] = 0;
-                uint32_t u = my_off;
-#pragma unroll 1
-                for (int q = 0; q < 4; ++q) {
-                    uint32_t b = bm[q];
-                    if (ub == 2) b = (b | (b >> 1)) & 0x55555555u;
-                    while (b) {
-                        int i = __ffs(b) - 1;
-                        b &= b - 1;
-                        uint32_t x = uint32_t(lo + 32 * q + i);   // first byte of the unit
-                        uint32_t unit = x / ub;
-                        offs[2 * u] = uint8_t(unit);
-                        offs[2 * u + 1] = uint8_t(unit >> 8);
-                        for (uint32_t e = 0; e < ub; ++e) vals[u * ub + e] = bytes[x + e];
-                        ++u;
-                    }
-                }
-            }
-        }
-        __syncthreads();
+        load_slice(A, B, cd, overwrite, warp, lane);
+        __threadfence_block();
+        bar_arrive(kBarFull + b, kLoaderThreads + 32);
     }
 }
 
@@ -662,7 +698,7 @@ int encode_kernel_config(KernelConfig* kc)
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&kc->enc_blocks_per_sm, encode_kernel, kThreads,
                                                           sizeof(Smem));
     if (e != cudaSuccess) return cuda_error(e, "encode kernel configuration");
-    if (kc->enc_blocks_per_sm < 1) kc->enc_blocks_per_sm = 1;
+    if (kc->enc_blocks_per_sm < 1) return set_error(DCR_ERR_CUDA, "encode kernel does not fit on an SM");
     return DCR_OK;
 }
 
