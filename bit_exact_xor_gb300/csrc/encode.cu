@@ -497,37 +497,48 @@ __device__ __forceinline__ void encode_chunk(const EncArgs& A, Buf& B, uint32_t 
     }
     const uint32_t fsz = chg ? (kFrameHdr + body_len + 15) / 16 * 16 : 0u;
 
-    // ---- decoupled look-back for the frame's place in the stream
+    // ---- decoupled look-back for the frame's place in the stream: the warp
+    // reads 32 predecessors per round trip, newest first, and sums them up to
+    // the nearest one that already holds an inclusive prefix
     uint64_t excl = 0;
     int ok = 1;
+    const uint64_t agg = fsz ? ((1ull << kLbFrameShift) | fsz) : 0ull;
     if (lane == 0) {
-        const uint64_t agg = fsz ? ((1ull << kLbFrameShift) | fsz) : 0ull;
-        if (k == 0) {
-            st_release(&A.lb[0], kLbInc | agg);
-        } else {
-            st_release(&A.lb[k], kLbAgg | agg);
-            for (int64_t j = int64_t(k) - 1; j >= 0; --j) {
-                uint64_t v = ld_acquire(&A.lb[j]);
-                uint32_t spins = 0;
-                while ((v >> 62) == 0) {
-                    if (++spins > kSpinLimit || *(volatile int32_t*)&A.sc->err) {
-                        ok = 0;
-                        break;
-                    }
-                    __nanosleep(64);
-                    v = ld_acquire(&A.lb[j]);
+        A.fsize[k] = fsz;
+        st_release(&A.lb[k], (k == 0 ? kLbInc : kLbAgg) | agg);
+    }
+    if (k > 0) {
+        for (int64_t j = int64_t(k) - 1;; j -= 32) {
+            const int64_t idx = j - lane;
+            uint64_t v = 0;
+            uint32_t spins = 0;
+            for (;;) {
+                v = idx >= 0 ? ld_acquire(&A.lb[idx]) : kLbInc;   // before chunk 0: prefix 0
+                const uint32_t inc = __ballot_sync(0xffffffffu, (v >> 62) == 2);
+                const uint32_t upto = inc ? (2u << (__ffs(inc) - 1)) - 1u : 0xffffffffu;
+                const uint32_t missing = __ballot_sync(0xffffffffu, (v >> 62) == 0) & upto;
+                if (!missing) break;
+                const bool quit = ++spins > kSpinLimit || *(volatile int32_t*)&A.sc->err != 0;
+                if (__any_sync(0xffffffffu, quit)) {   // warp-uniform exit
+                    ok = 0;
+                    break;
                 }
-                if (!ok) break;
-                excl += v & kLbValMask;
-                if ((v >> 62) == 2) break;
+                __nanosleep(64);
             }
+            if (!ok) break;
+            const uint32_t inc = __ballot_sync(0xffffffffu, (v >> 62) == 2);
+            const uint32_t upto = inc ? (2u << (__ffs(inc) - 1)) - 1u : 0xffffffffu;
+            uint64_t part = ((upto >> lane) & 1u) ? (v & kLbValMask) : 0ull;
+#pragma unroll
+            for (int d = 16; d > 0; d >>= 1) part += __shfl_xor_sync(0xffffffffu, part, d);
+            excl += part;
+            if (inc) break;
+        }
+        if (lane == 0) {
             if (ok) st_release(&A.lb[k], kLbInc | (excl + agg));
             else atomicCAS(reinterpret_cast<int*>(&A.sc->err), 0, DCR_ERR_TIMEOUT);
         }
-        A.fsize[k] = fsz;
     }
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-    excl = __shfl_sync(0xffffffffu, excl, 0);
     if (!ok) return;
 
     // ---- write the frame
@@ -609,14 +620,18 @@ __global__ void __launch_bounds__(kThreads, 1) encode_kernel(EncArgs A)
         return;
     }
 
-    // loader warps
+    // loader warps.  Thread 0 takes each chunk's ticket one iteration ahead,
+    // so the atomic's round trip overlaps the previous chunk's loads.
+    uint32_t next = 0;
+    if (threadIdx.x == 0) next = atomicAdd(&A.sc->ticket, 1u);
     for (int b = 0;; b = b + 1 == kEncoders ? 0 : b + 1) {
         Buf& B = S.buf[b];
         bar_sync(kBarEmpty + b, kLoaderThreads + 32);
         if (threadIdx.x == 0) {
-            uint32_t k = atomicAdd(&A.sc->ticket, 1u);
+            uint32_t k = next;
             if (k >= A.chunk_count || *(volatile int32_t*)&A.sc->err) k = kEnd;
             B.k = k;
+            if (k != kEnd) next = atomicAdd(&A.sc->ticket, 1u);
         }
         bar_sync(kBarLoaders, kLoaderThreads);
         const uint32_t k = B.k;
