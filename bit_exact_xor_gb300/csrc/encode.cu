@@ -238,16 +238,25 @@ __device__ __forceinline__ uint32_t warp_excl_sum(uint32_t v, int lane, uint32_t
     return inc - v;
 }
 
+// Bitmap word w lives at bsw(w): each encoder lane reads its own 2 KiB share
+// (64 words), so without the swizzle all lanes would hit the same banks.
+__device__ __forceinline__ int bsw(int w) { return w ^ (((w >> 6) & 7) << 2); }
+
+// The i-th group of four bitmap words of a lane's share.
+__device__ __forceinline__ uint4 bit_group(const Buf* B, int lane, int i)
+{
+    return reinterpret_cast<const uint4*>(B->bits)[bsw(lane * kWordsPerLane + 4 * i) >> 2];
+}
+
 // Calls f(position) for every set bit of a lane's bitmap share, in order
 // (the lane owns bytes [2048 lane, 2048 lane + 2048) of the chunk).  Empty
 // 128-byte stretches are skipped four words at a time.
 template <class F>
 __device__ __forceinline__ void for_bits(const Buf* B, int lane, F f)
 {
-    const uint4* q = reinterpret_cast<const uint4*>(B->bits) + lane * (kWordsPerLane / 4);
 #pragma unroll 1
     for (int i = 0; i < kWordsPerLane / 4; ++i) {
-        const uint4 v = q[i];
+        const uint4 v = bit_group(B, lane, i);
         if ((v.x | v.y | v.z | v.w) == 0) continue;
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
         const int base = (lane * kWordsPerLane + 4 * i) * 32;
@@ -352,7 +361,7 @@ __device__ __forceinline__ void load_slice(const EncArgs& A, Buf& B, const Chunk
     // bitmap word of the vector pair (v, v + 1) held by lanes (even, odd)
     auto list_vec = [&](int v, uint32_t z) {
         const uint32_t hi = __shfl_down_sync(0xffffffffu, z, 1);
-        if ((lane & 1) == 0) B.bits[v >> 1] = z | (hi << 16);
+        if ((lane & 1) == 0) B.bits[bsw(v >> 1)] = z | (hi << 16);
     };
 
     if (cd.flags & kSrcVec) {
@@ -480,8 +489,11 @@ __device__ __forceinline__ void encode_chunk(const EncArgs& A, Buf& B, uint32_t 
         // overwrite records: one per changed unit (2 bytes for bf16, else 1)
         const uint32_t ub = cd.bits == 16 ? 2u : 1u;
         uint32_t units = 0;
-        const uint32_t* wb = B.bits + lane * kWordsPerLane;
-        for (int i = 0; i < kWordsPerLane; ++i) units += __popc(unit_bits(wb[i], ub));
+        for (int i = 0; i < kWordsPerLane / 4; ++i) {
+            const uint4 g = bit_group(&B, lane, i);
+            units += __popc(unit_bits(g.x, ub)) + __popc(unit_bits(g.y, ub)) + __popc(unit_bits(g.z, ub)) +
+                     __popc(unit_bits(g.w, ub));
+        }
         uint32_t total;
         my_off = warp_excl_sum(units, lane, &total);
         n_units = total;
@@ -577,9 +589,8 @@ __device__ __forceinline__ void encode_chunk(const EncArgs& A, Buf& B, uint32_t 
         uint8_t* offs = body + 4;
         uint8_t* vals = body + 4 + 2 * n_units + pad;
         uint32_t u_i = my_off;
-        const uint32_t* wb = B.bits + lane * kWordsPerLane;
         for (int i = 0; i < kWordsPerLane; ++i) {
-            uint32_t b = unit_bits(wb[i], ub);
+            uint32_t b = unit_bits(B.bits[bsw(lane * kWordsPerLane + i)], ub);
             while (b) {
                 const uint32_t x = uint32_t((lane * kWordsPerLane + i) * 32 + __ffs(b) - 1);
                 b &= b - 1;
