@@ -18,12 +18,14 @@
 // Structure.  One CTA per SM: 16 loader warps and 2 encoder warps share two
 // chunk buffers in shared memory.  Loader warp w gathers the contiguous 4 KiB
 // slice [4096 w, 4096 w + 4096) of the chunk with 16-byte streaming loads,
-// XORs old and new, counts changes, and appends the positions of the
-// non-zero mask bytes of its slice, in order, to its own list.  Encoder warp
-// b owns buffer b: it parses the chunk from those lists alone (work grows
-// with the number of non-zero bytes, not with the chunk size), waits for its
-// place in the stream and writes the frame, while the loaders already fill
-// the other buffer.  Named barriers hand the buffers back and forth.
+// XORs old and new, counts changes, and sets one bitmap bit per non-zero mask
+// byte.  The next chunk's ticket, descriptor and pieces are staged one
+// iteration ahead, so the data loads of a chunk issue at once.  Encoder warp
+// b owns buffer b: it compacts the bitmap into a sorted list of non-zero byte
+// positions ("events"), parses the chunk from the events 32 at a time (one per
+// lane, connected by warp scans), waits for its place in the stream and writes
+// the frame, while the loaders fill the other buffer.  Named barriers hand the
+// buffers back and forth.
 //
 // LZ4 parse.  The masks are long zero runs around sparse non-zero bytes, so
 // every zero run of at least 4 bytes becomes one match and everything else
@@ -31,10 +33,7 @@
 // one is long enough (non-overlapping copy), else it keeps its first zero as a
 // literal and copies from it with offset 1.  Every match therefore copies zero
 // bytes only (frame flag ZSRC), and the block obeys the format's end rules
-// (last 5 bytes literals, no match start in the last 12 bytes).  Each of the
-// 32 encoder lanes walks an equal share of the non-zero positions; three warp
-// scans connect the shares (last non-zero byte and longest run so far, last
-// match end, output offset).
+// (last 5 bytes literals, no match start in the last 12 bytes).
 #include <cuda_runtime.h>
 
 #include <climits>
@@ -46,14 +45,16 @@ namespace dcr {
 namespace {
 
 constexpr int kLoaders = 16;                      // loader warps
-constexpr int kEncoders = 3;                      // encoder warps = chunk buffers
+constexpr int kEncoders = 2;                      // encoder warps = chunk buffers
 constexpr int kThreads = 32 * (kLoaders + kEncoders);
 constexpr int kLoaderThreads = 32 * kLoaders;
 constexpr int kNVec = kChunk / 16;                // 16-byte vectors per chunk
 constexpr int kVecPerWarp = kNVec / kLoaders;     // 256: a 4 KiB slice
 constexpr int kVPL = kVecPerWarp / 32;            // 8 vectors per lane
 constexpr int kWords = kChunk / 32;               // bitmap words per chunk
-constexpr int kWordsPerLane = kWords / 32;        // 64: encoder lane share = 2 KiB
+constexpr int kSteps = kWords / 32;               // 64 warp steps over the bitmap
+constexpr int kEvCap = 6144;                      // events listed per batch
+constexpr int kSegCache = 64;                     // sender pieces staged in smem
 constexpr uint32_t kEnd = 0xFFFFFFFFu;
 constexpr uint32_t kSpinLimit = 1u << 22;         // bounded look-back wait
 
@@ -77,16 +78,25 @@ struct EncArgs {
     uint32_t* fsize;
 };
 
+// chunk metadata staged in shared memory
+struct __align__(16) Meta {
+    ChunkDesc cd;
+    uint32_t k;                        // window-relative chunk, or kEnd
+    uint32_t pad[3];
+    Seg segs[kSegCache];               // first pieces (all of them if src_count <= kSegCache)
+};
+
 struct __align__(16) Buf {
     uint4 data[kNVec];                 // mask (XOR chunks) or new bytes (overwrite chunks)
     uint32_t bits[kWords];             // bit i set iff mask byte i != 0
+    uint16_t ev[kEvCap + 16];          // event list (sorted non-zero byte positions)
     uint32_t chg[kLoaders];            // changed stored values per slice
-    uint32_t k;                        // window-relative chunk, or kEnd
-    uint32_t pad[3];
+    Meta meta;
 };
 
 struct __align__(16) Smem {
     Buf buf[kEncoders];
+    Meta next;                         // the loaders' next chunk, staged ahead
 };
 
 // ---------------------------------------------------------------- helpers --
@@ -150,6 +160,13 @@ __device__ __forceinline__ uint32_t changed_in(uint32_t m, uint4 v, uint32_t bit
     return c;
 }
 
+// overwrite units of a bitmap word: bit i set iff the unit starting at byte i
+// (ub = 2: even i only) has a non-zero mask byte
+__device__ __forceinline__ uint32_t unit_bits(uint32_t b, uint32_t ub)
+{
+    return ub == 2 ? (b | (b >> 1)) & 0x55555555u : b;
+}
+
 // piece of the chunk holding canonical byte x: last piece with off <= x
 __device__ __forceinline__ int find_seg(const Seg* s, int n, uint32_t x)
 {
@@ -172,196 +189,197 @@ __device__ __forceinline__ uint32_t seq_bytes(uint32_t ll, uint32_t ml)
     return 1 + ext_len(ll) + ll + 2 + ext_len(ml - 4);
 }
 
-// ---- zero-run summaries ----------------------------------------------------
-// first/last non-zero position of a range and the longest zero run strictly
-// between two of its non-zero bytes, packed (len << 32 | start).
-// first == INT_MAX marks a range without non-zero bytes.
-struct RunSum {
-    int first, last;
-    unsigned long long best;
+// ---- warp scans -------------------------------------------------------------
+__device__ __forceinline__ uint32_t warp_incl_sum(uint32_t v, int lane)
+{
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        uint32_t o = __shfl_up_sync(0xffffffffu, v, d);
+        if (lane >= d) v += o;
+    }
+    return v;
+}
+
+__device__ __forceinline__ unsigned long long warp_incl_max64(unsigned long long v, int lane)
+{
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        unsigned long long o = __shfl_up_sync(0xffffffffu, v, d);
+        if (lane >= d && o > v) v = o;
+    }
+    return v;
+}
+
+__device__ __forceinline__ int warp_incl_max(int v, int lane)
+{
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        int o = __shfl_up_sync(0xffffffffu, v, d);
+        if (lane >= d) v = max(v, o);
+    }
+    return v;
+}
+
+// ---- events -------------------------------------------------------------------
+// Appends the positions of the set bits of bitmap steps [t, ...) to B.ev,
+// in order, until a further step might not fit.  Returns the step reached.
+__device__ __forceinline__ int list_events(Buf& B, int t, int lane, int* n_out)
+{
+    int n = 0;
+    for (; t < kSteps; ++t) {
+        const uint32_t w = B.bits[32 * t + lane];
+        const uint32_t c = __popc(w);
+        const uint32_t incl = warp_incl_sum(c, lane);
+        const uint32_t tot = __shfl_sync(0xffffffffu, incl, 31);
+        if (n + int(tot) > kEvCap) break;
+        uint32_t at = uint32_t(n) + incl - c, b = w;
+        while (b) {
+            const int i = __ffs(b) - 1;
+            b &= b - 1;
+            B.ev[at++] = uint16_t((32 * t + lane) * 32 + i);
+        }
+        n += int(tot);
+    }
+    __syncwarp();
+    *n_out = n;
+    return t;
+}
+
+// Carried parse state between groups of 32 events.
+struct Parse {
+    int prev;                  // last non-zero byte so far (-1: before the chunk)
+    unsigned long long best;   // longest zero run so far: len << 32 | start
+    int lit;                   // end of the last match (start of pending literals)
+    uint32_t out;              // block bytes so far
 };
 
-__device__ __forceinline__ RunSum combine(RunSum a, RunSum b)
+// Zero-run parse of n listed events (plus the virtual event at raw when
+// final), 32 at a time.  With body != nullptr the sequences are written.
+__device__ __forceinline__ void parse_events(const Buf& B, int n, bool final, int raw, Parse& P,
+                                             uint8_t* body, uint32_t body_len, int lane, bool* bad)
 {
-    if (a.first == INT_MAX) return b;
-    if (b.first == INT_MAX) return a;
-    RunSum r;
-    r.first = a.first;
-    r.last = b.last;
-    unsigned long long g = ((unsigned long long)(uint32_t)(b.first - a.last - 1) << 32) |
-                           (uint32_t)(a.last + 1);
-    r.best = a.best > b.best ? a.best : b.best;
-    if (g > r.best) r.best = g;
-    return r;
-}
-
-__device__ __forceinline__ RunSum warp_excl_runs(RunSum v, int lane)
-{
-    RunSum inc = v;
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-        RunSum o;
-        o.first = __shfl_up_sync(0xffffffffu, inc.first, d);
-        o.last = __shfl_up_sync(0xffffffffu, inc.last, d);
-        o.best = __shfl_up_sync(0xffffffffu, inc.best, d);
-        if (lane >= d) inc = combine(o, inc);
-    }
-    RunSum e;
-    e.first = __shfl_up_sync(0xffffffffu, inc.first, 1);
-    e.last = __shfl_up_sync(0xffffffffu, inc.last, 1);
-    e.best = __shfl_up_sync(0xffffffffu, inc.best, 1);
-    if (lane == 0) e = RunSum{INT_MAX, 0, 0ull};
-    return e;
-}
-
-__device__ __forceinline__ int warp_excl_max(int v, int lane)
-{
-    int inc = v;
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-        int o = __shfl_up_sync(0xffffffffu, inc, d);
-        if (lane >= d) inc = max(inc, o);
-    }
-    int e = __shfl_up_sync(0xffffffffu, inc, 1);
-    return lane == 0 ? INT_MIN : e;
-}
-
-__device__ __forceinline__ uint32_t warp_excl_sum(uint32_t v, int lane, uint32_t* total)
-{
-    uint32_t inc = v;
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-        uint32_t o = __shfl_up_sync(0xffffffffu, inc, d);
-        if (lane >= d) inc += o;
-    }
-    *total = __shfl_sync(0xffffffffu, inc, 31);
-    return inc - v;
-}
-
-// Bitmap word w lives at bsw(w): each encoder lane reads its own 2 KiB share
-// (64 words), so without the swizzle all lanes would hit the same banks.
-__device__ __forceinline__ int bsw(int w) { return w ^ (((w >> 6) & 7) << 2); }
-
-// The i-th group of four bitmap words of a lane's share.
-__device__ __forceinline__ uint4 bit_group(const Buf* B, int lane, int i)
-{
-    return reinterpret_cast<const uint4*>(B->bits)[bsw(lane * kWordsPerLane + 4 * i) >> 2];
-}
-
-// Calls f(position) for every set bit of a lane's bitmap share, in order
-// (the lane owns bytes [2048 lane, 2048 lane + 2048) of the chunk).  Empty
-// 128-byte stretches are skipped four words at a time.
-template <class F>
-__device__ __forceinline__ void for_bits(const Buf* B, int lane, F f)
-{
-#pragma unroll 1
-    for (int i = 0; i < kWordsPerLane / 4; ++i) {
-        const uint4 v = bit_group(B, lane, i);
-        if ((v.x | v.y | v.z | v.w) == 0) continue;
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-        const int base = (lane * kWordsPerLane + 4 * i) * 32;
-#pragma unroll
-        for (int h = 0; h < 4; ++h) {
-            uint32_t b = w[h];
-            while (b) {
-                const int t = __ffs(b) - 1;
-                b &= b - 1;
-                f(base + 32 * h + t);
+    const uint8_t* bytes = reinterpret_cast<const uint8_t*>(B.data);
+    const int total = n + (final ? 1 : 0);
+    for (int g = 0; g < total; g += 32) {
+        const int i = g + lane;
+        const bool active = i < total;
+        const bool last = final && i == total - 1;
+        const int p = !active ? raw : (last ? raw : int(B.ev[i]));
+        int pp = __shfl_up_sync(0xffffffffu, p, 1);
+        if (lane == 0) pp = P.prev;
+        const int gs = pp + 1;
+        const int L = p - gs;
+        const unsigned long long cand =
+            active && L > 0 ? ((unsigned long long)(uint32_t)L << 32) | uint32_t(gs) : 0ull;
+        const unsigned long long cmax = warp_incl_max64(cand, lane);
+        unsigned long long bb = __shfl_up_sync(0xffffffffu, cmax, 1);
+        if (lane == 0 || bb < P.best) bb = P.best;
+        // match decision for the zero run [gs, p)
+        const int me = p < raw - 5 ? p : raw - 5;
+        int ms = -1, off = 0;
+        if (active && L > 0) {
+            if (me - gs >= 4 && gs <= raw - 12 && uint32_t(bb >> 32) >= uint32_t(me - gs)) {
+                ms = gs;
+                off = gs - int(uint32_t(bb));
+            } else if (me - gs - 1 >= 4 && gs + 1 <= raw - 12) {
+                ms = gs + 1;
+                off = 1;
             }
         }
-    }
-}
-
-// overwrite units of a bitmap word: bit i set iff unit starting at byte i
-// (ub = 2: even i only) has a non-zero mask byte
-__device__ __forceinline__ uint32_t unit_bits(uint32_t b, uint32_t ub)
-{
-    return ub == 2 ? (b | (b >> 1)) & 0x55555555u : b;
-}
-
-// Decides, for every zero run that ends at one of this lane's non-zero bytes
-// (and the trailing run for the last lane), whether it becomes a match.
-// prev: last non-zero byte before the share (-1: virtual non-zero before the
-// chunk); best: longest earlier zero run.  emit(ms, me, off) per match.
-template <class Emit>
-__device__ __forceinline__ void walk_runs(const Buf* B, int lane, int raw, bool tail, int prev,
-                                          unsigned long long best, Emit emit)
-{
-    auto gap = [&](int q) {
-        int gs = prev + 1;
-        int L = q - gs;
-        if (L > 0) {
-            int me = q < raw - 5 ? q : raw - 5;
-            uint32_t blen = uint32_t(best >> 32);
-            int bstart = int(uint32_t(best));
-            if (me - gs >= 4 && gs <= raw - 12 && blen >= uint32_t(me - gs)) {
-                emit(gs, me, gs - bstart);
-            } else if (me - (gs + 1) >= 4 && gs + 1 <= raw - 12) {
-                emit(gs + 1, me, 1);
+        const bool has = ms >= 0;
+        const int mend = warp_incl_max(has ? me : 0, lane);
+        int lit = __shfl_up_sync(0xffffffffu, mend, 1);
+        if (lane == 0 || lit < P.lit) lit = P.lit;
+        uint32_t sz = has ? seq_bytes(uint32_t(ms - lit), uint32_t(me - ms)) : 0u;
+        const int flit = has ? me : lit;    // literals after this event's match
+        if (last) sz += 1 + ext_len(uint32_t(raw - flit)) + uint32_t(raw - flit);
+        const uint32_t incl = warp_incl_sum(sz, lane);
+        if (body && (has || last)) {
+            const uint32_t o0 = P.out + incl - sz;
+            uint32_t o = o0;
+            const uint32_t end = o0 + sz < body_len ? o0 + sz : body_len;
+            auto put = [&](uint32_t v) {
+                if (o < end) body[o] = uint8_t(v);
+                ++o;
+            };
+            auto put_len = [&](uint32_t v) {
+                v -= 15;
+                for (; v >= 255; v -= 255) put(255);
+                put(v);
+            };
+            if (has) {
+                const uint32_t ll = uint32_t(ms - lit), mc = uint32_t(me - ms - 4);
+                put(((ll >= 15 ? 15u : ll) << 4) | (mc >= 15 ? 15u : mc));
+                if (ll >= 15) put_len(ll);
+                for (uint32_t q = 0; q < ll; ++q) put(bytes[lit + int(q)]);
+                put(uint32_t(off) & 0xFFu);
+                put(uint32_t(off) >> 8);
+                if (mc >= 15) put_len(mc);
             }
-            unsigned long long cand = ((unsigned long long)(uint32_t)L << 32) | uint32_t(gs);
-            if (cand > best) best = cand;
+            if (last) {
+                const uint32_t ll = uint32_t(raw - flit);
+                put((ll >= 15 ? 15u : ll) << 4);
+                if (ll >= 15) put_len(ll);
+                for (uint32_t q = 0; q < ll; ++q) put(bytes[flit + int(q)]);
+            }
+            if (o != o0 + sz || o > body_len) *bad = true;
         }
-        prev = q;
-    };
-    for_bits(B, lane, gap);
-    if (tail) gap(raw);
+        // carry
+        const int lastlane = (total - g < 32 ? total - g : 32) - 1;
+        P.prev = __shfl_sync(0xffffffffu, p, lastlane);
+        const unsigned long long call = __shfl_sync(0xffffffffu, cmax, 31);
+        if (call > P.best) P.best = call;
+        const int mall = __shfl_sync(0xffffffffu, mend, 31);
+        if (mall > P.lit) P.lit = mall;
+        P.out += __shfl_sync(0xffffffffu, incl, 31);
+    }
 }
 
-// Byte writer confined to one lane's part [p, end) of the frame body: bytes
-// that would fall outside are dropped and flagged instead of written.
-struct Out {
-    uint8_t* o;
-    uint32_t p, end;
-    bool over;
-    __device__ __forceinline__ void put(uint32_t b)
-    {
-        if (p < end) o[p] = uint8_t(b);
-        else over = true;
-        ++p;
-    }
-};
-
-__device__ __forceinline__ void put_len(Out& w, uint32_t v)
+// LZ4 block size (pass 1) or block bytes (pass 2) of the chunk in B.
+// Events that fit are listed once; larger event sets are listed in batches.
+__device__ uint32_t lz4_block(Buf& B, int raw, uint8_t* body, uint32_t body_len, bool reuse, int n_reuse,
+                              int lane, bool* bad, int* n_listed, bool* complete)
 {
-    // v >= 15 was stored as 15 in the token
-    v -= 15;
-    while (v >= 255) {
-        w.put(255);
-        v -= 255;
+    Parse P{-1, 0ull, 0, 0u};
+    if (reuse) {
+        parse_events(B, n_reuse, true, raw, P, body, body_len, lane, bad);
+        return P.out;
     }
-    w.put(v);
-}
-
-__device__ __forceinline__ void put_seq(Out& w, const uint8_t* mask, uint32_t lit0, uint32_t ll,
-                                        uint32_t off, uint32_t ml, bool last)
-{
-    uint32_t mc = last ? 0u : ml - 4;
-    w.put(((ll >= 15 ? 15u : ll) << 4) | (mc >= 15 ? 15u : mc));
-    if (ll >= 15) put_len(w, ll);
-    for (uint32_t i = 0; i < ll; ++i) w.put(mask[lit0 + i]);
-    if (last) return;
-    w.put(off & 0xFFu);
-    w.put(off >> 8);
-    if (mc >= 15) put_len(w, mc);
+    int t = 0, n = 0;
+    bool first = true;
+    while (true) {
+        t = list_events(B, t, lane, &n);
+        const bool fin = t >= kSteps;
+        if (first) {
+            *n_listed = n;
+            *complete = fin;
+            first = false;
+        }
+        parse_events(B, n, fin, raw, P, body, body_len, lane, bad);
+        if (fin) break;
+    }
+    return P.out;
 }
 
 // ---------------------------------------------------------------- loaders --
-// Gather, XOR, count and list one chunk's 4 KiB slice (loader warp w).
-__device__ __forceinline__ void load_slice(const EncArgs& A, Buf& B, const ChunkDesc& cd, bool overwrite,
-                                           int w, int lane)
+// Gather, XOR, count and map one chunk's 4 KiB slice (loader warp w).
+// between() runs after the slice's loads are issued, before they are used.
+template <class Between>
+__device__ __forceinline__ void load_slice(const EncArgs& A, Buf& B, const Meta& M, bool overwrite,
+                                           int w, int lane, Between between)
 {
+    const ChunkDesc& cd = M.cd;
     const int raw = int(cd.raw_len);
-    const Seg* segs = A.src + cd.src_begin;
     const int nseg = int(cd.src_count);
+    const Seg* segs = nseg <= kSegCache ? M.segs : A.src + cd.src_begin;
     uint8_t* bytes = reinterpret_cast<uint8_t*>(B.data);
     uint32_t changed = 0;
     const int v0 = w * kVecPerWarp;
 
     // bitmap word of the vector pair (v, v + 1) held by lanes (even, odd)
-    auto list_vec = [&](int v, uint32_t z) {
+    auto map_vec = [&](int v, uint32_t z) {
         const uint32_t hi = __shfl_down_sync(0xffffffffu, z, 1);
-        if ((lane & 1) == 0) B.bits[bsw(v >> 1)] = z | (hi << 16);
+        if ((lane & 1) == 0) B.bits[v >> 1] = z | (hi << 16);
     };
 
     if (cd.flags & kSrcVec) {
@@ -385,6 +403,7 @@ __device__ __forceinline__ void load_slice(const EncArgs& A, Buf& B, const Chunk
                 n[j] = ld_stream(A.news[r] + a);
             }
         }
+        between();
 #pragma unroll
         for (int j = 0; j < kVPL; ++j) {
             const int v = v0 + j * 32 + lane;
@@ -392,11 +411,12 @@ __device__ __forceinline__ void load_slice(const EncArgs& A, Buf& B, const Chunk
             uint32_t z = nz16(m);
             changed += changed_in(z, m, cd.bits);
             B.data[v] = overwrite ? n[j] : m;
-            list_vec(v, z);
+            map_vec(v, z);
         }
     } else {
         // unaligned pieces: byte-wise gather (layouts with odd row sizes).
         // The mask is staged first; overwrite chunks then restage new bytes.
+        between();
         for (int pass = 0; pass < (overwrite ? 2 : 1); ++pass) {
             for (int i = lane; i < 16 * kVecPerWarp; i += 32) {
                 const int x = 16 * v0 + i;
@@ -417,7 +437,7 @@ __device__ __forceinline__ void load_slice(const EncArgs& A, Buf& B, const Chunk
                     const uint4 m = B.data[v];
                     const uint32_t z = nz16(m);
                     changed += changed_in(z, m, cd.bits);
-                    list_vec(v, z);
+                    map_vec(v, z);
                 }
                 __syncwarp();
             }
@@ -427,11 +447,31 @@ __device__ __forceinline__ void load_slice(const EncArgs& A, Buf& B, const Chunk
     if (lane == 0) B.chg[w] = changed;
 }
 
+// Loader warp 0: stage the next chunk's descriptor and pieces.  `ticket`
+// (lane 0) holds the chunk taken one call earlier; a new one is taken here.
+__device__ __forceinline__ void stage_next(const EncArgs& A, Meta& M, int lane, uint32_t& ticket)
+{
+    uint32_t k = 0;
+    if (lane == 0) {
+        k = ticket;
+        if (k >= A.chunk_count || *(volatile int32_t*)&A.sc->err) k = kEnd;
+        if (k != kEnd) ticket = atomicAdd(&A.sc->ticket, 1u);
+    }
+    k = __shfl_sync(0xffffffffu, k, 0);
+    if (lane == 0) M.k = k;
+    if (k == kEnd) return;
+    const ChunkDesc cd = A.chunks[A.chunk_begin + k];
+    if (lane == 0) M.cd = cd;
+    const uint32_t ns = cd.src_count < uint32_t(kSegCache) ? cd.src_count : uint32_t(kSegCache);
+    for (uint32_t i = lane; i < ns; i += 32) M.segs[i] = A.src[cd.src_begin + i];
+}
+
 // ---------------------------------------------------------------- encoder --
 // Parse, place and write the frame of the chunk held in buffer B.
-__device__ __forceinline__ void encode_chunk(const EncArgs& A, Buf& B, uint32_t k, int lane)
+__device__ __forceinline__ void encode_chunk(const EncArgs& A, Buf& B, int lane)
 {
-    const ChunkDesc cd = A.chunks[A.chunk_begin + k];
+    const ChunkDesc cd = B.meta.cd;
+    const uint32_t k = B.meta.k;
     const int raw = int(cd.raw_len);
     const bool overwrite = (cd.flags & kResidualFlag) || A.mode == DCR_MODE_OVERWRITE_ONLY;
     const uint8_t* bytes = reinterpret_cast<const uint8_t*>(B.data);
@@ -443,41 +483,12 @@ __device__ __forceinline__ void encode_chunk(const EncArgs& A, Buf& B, uint32_t 
         atomicAdd(reinterpret_cast<unsigned long long*>(&A.sc->changed), (unsigned long long)chg);
     }
 
-    uint32_t kind = 0, body_len = 0, my_off = 0, my_sz = 0;
-    int prev_last = -1, lit0 = 0;
-    unsigned long long best0 = 0ull;
-    uint32_t n_units = 0;
-
+    uint32_t kind = 0, body_len = 0, n_units = 0;
+    int n_listed = 0;
+    bool complete = false, bad = false;
+    const uint32_t ub = cd.bits == 16 ? 2u : 1u;
     if (chg && !overwrite) {
-        // pass 1: run summary of this lane's share
-        RunSum mine{INT_MAX, 0, 0ull};
-        for_bits(&B, lane, [&](int p) { mine = combine(mine, RunSum{p, p, 0ull}); });
-        if (lane == 0) mine = combine(RunSum{-1, -1, 0ull}, mine);
-        const RunSum pr = warp_excl_runs(mine, lane);
-        prev_last = lane == 0 ? -1 : pr.last;
-        best0 = lane == 0 ? 0ull : pr.best;
-        // pass 2: matches of this share
-        int first_ms = -1, first_ml = 0, last_me = 0;
-        uint32_t rest = 0;
-        walk_runs(&B, lane, raw, lane == 31, prev_last, best0, [&](int ms, int me, int) {
-            if (first_ms < 0) {
-                first_ms = ms;
-                first_ml = me - ms;
-            } else {
-                rest += seq_bytes(uint32_t(ms - last_me), uint32_t(me - ms));
-            }
-            last_me = me;
-        });
-        lit0 = max(warp_excl_max(first_ms >= 0 ? last_me : 0, lane), 0);
-        uint32_t sz = 0;
-        if (first_ms >= 0) sz = seq_bytes(uint32_t(first_ms - lit0), uint32_t(first_ml)) + rest;
-        if (lane == 31) {
-            const uint32_t ll = uint32_t(raw - (first_ms >= 0 ? last_me : lit0));
-            sz += 1 + ext_len(ll) + ll;
-        }
-        uint32_t total;
-        my_off = warp_excl_sum(sz, lane, &total);
-        my_sz = sz;
+        const uint32_t total = lz4_block(B, raw, nullptr, 0, false, 0, lane, &bad, &n_listed, &complete);
         if (total < uint32_t(raw)) {
             kind = kXorLz4;
             body_len = total;
@@ -487,18 +498,11 @@ __device__ __forceinline__ void encode_chunk(const EncArgs& A, Buf& B, uint32_t 
         }
     } else if (chg) {
         // overwrite records: one per changed unit (2 bytes for bf16, else 1)
-        const uint32_t ub = cd.bits == 16 ? 2u : 1u;
         uint32_t units = 0;
-        for (int i = 0; i < kWordsPerLane / 4; ++i) {
-            const uint4 g = bit_group(&B, lane, i);
-            units += __popc(unit_bits(g.x, ub)) + __popc(unit_bits(g.y, ub)) + __popc(unit_bits(g.z, ub)) +
-                     __popc(unit_bits(g.w, ub));
-        }
-        uint32_t total;
-        my_off = warp_excl_sum(units, lane, &total);
-        n_units = total;
-        const uint32_t pad = (4 - (2 * total) % 4) % 4;
-        const uint32_t rec = 4 + 2 * total + pad + total * ub;
+        for (int t = 0; t < kSteps; ++t) units += __popc(unit_bits(B.bits[32 * t + lane], ub));
+        n_units = __reduce_add_sync(0xffffffffu, units);
+        const uint32_t pad = (4 - (2 * n_units) % 4) % 4;
+        const uint32_t rec = 4 + 2 * n_units + pad + n_units * ub;
         if (rec < uint32_t(raw)) {
             kind = kOverwrite;
             body_len = rec;
@@ -565,22 +569,16 @@ __device__ __forceinline__ void encode_chunk(const EncArgs& A, Buf& B, uint32_t 
     }
     for (uint32_t i = kFrameHdr + body_len + lane; i < fsz; i += 32) f[i] = 0;
     if (kind == kXorLz4) {
-        const uint32_t end = my_off + my_sz < body_len ? my_off + my_sz : body_len;
-        Out o{body, my_off, end, false};
-        int lit = lit0;
-        walk_runs(&B, lane, raw, lane == 31, prev_last, best0, [&](int ms, int me, int off) {
-            put_seq(o, bytes, uint32_t(lit), uint32_t(ms - lit), uint32_t(off), uint32_t(me - ms), false);
-            lit = me;
-        });
-        if (lane == 31) put_seq(o, bytes, uint32_t(lit), uint32_t(raw - lit), 0, 0, true);
-        if (o.over || o.p != my_off + my_sz)   // sizing and emission disagree
-            atomicCAS(reinterpret_cast<int*>(&A.sc->err), 0, DCR_ERR_CORRUPT);
+        int nl;
+        bool cp;
+        const uint32_t got = lz4_block(B, raw, body, body_len, complete, n_listed, lane, &bad, &nl, &cp);
+        if (__any_sync(0xffffffffu, bad) || got != body_len)   // sizing and emission disagree
+            if (lane == 0) atomicCAS(reinterpret_cast<int*>(&A.sc->err), 0, DCR_ERR_CORRUPT);
     } else if (kind == kXorRaw || kind == kOverwriteDense) {
         const int nfull = raw >> 4;
         for (int v = lane; v < nfull; v += 32) reinterpret_cast<uint4*>(body)[v] = B.data[v];
         for (int x = (nfull << 4) + lane; x < raw; x += 32) body[x] = bytes[x];
     } else {
-        const uint32_t ub = cd.bits == 16 ? 2u : 1u;
         const uint32_t pad = (4 - (2 * n_units) % 4) % 4;
         if (lane == 0) {
             *reinterpret_cast<uint32_t*>(body) = n_units;
@@ -588,11 +586,15 @@ __device__ __forceinline__ void encode_chunk(const EncArgs& A, Buf& B, uint32_t 
         }
         uint8_t* offs = body + 4;
         uint8_t* vals = body + 4 + 2 * n_units + pad;
-        uint32_t u_i = my_off;
-        for (int i = 0; i < kWordsPerLane; ++i) {
-            uint32_t b = unit_bits(B.bits[bsw(lane * kWordsPerLane + i)], ub);
+        uint32_t base = 0;
+        for (int t = 0; t < kSteps; ++t) {
+            const int wi = 32 * t + lane;
+            uint32_t b = unit_bits(B.bits[wi], ub);
+            const uint32_t c = __popc(b);
+            const uint32_t incl = warp_incl_sum(c, lane);
+            uint32_t u_i = base + incl - c;
             while (b) {
-                const uint32_t x = uint32_t((lane * kWordsPerLane + i) * 32 + __ffs(b) - 1);
+                const uint32_t x = uint32_t(wi * 32 + __ffs(b) - 1);
                 b &= b - 1;
                 const uint32_t u = x / ub;
                 if (u_i < n_units) {
@@ -602,6 +604,7 @@ __device__ __forceinline__ void encode_chunk(const EncArgs& A, Buf& B, uint32_t 
                 }
                 ++u_i;
             }
+            base += __shfl_sync(0xffffffffu, incl, 31);
         }
     }
 }
@@ -621,9 +624,8 @@ __global__ void __launch_bounds__(kThreads, 1) encode_kernel(EncArgs A)
         bar_arrive(kBarEmpty + b, kLoaderThreads + 32);
         for (;;) {
             bar_sync(kBarFull + b, kLoaderThreads + 32);
-            const uint32_t k = B.k;
-            if (k == kEnd) break;
-            encode_chunk(A, B, k, lane);
+            if (B.meta.k == kEnd) break;
+            encode_chunk(A, B, lane);
             __syncwarp();
             __threadfence_block();
             bar_arrive(kBarEmpty + b, kLoaderThreads + 32);
@@ -631,21 +633,27 @@ __global__ void __launch_bounds__(kThreads, 1) encode_kernel(EncArgs A)
         return;
     }
 
-    // loader warps.  Thread 0 takes each chunk's ticket one iteration ahead,
-    // so the atomic's round trip overlaps the previous chunk's loads.
-    uint32_t next = 0;
-    if (threadIdx.x == 0) next = atomicAdd(&A.sc->ticket, 1u);
+    // loader warps.  Warp 0 stages each chunk's ticket, descriptor and
+    // pieces one iteration ahead, so they are in shared memory when the
+    // chunk's loads issue.
+    uint32_t ticket = 0;
+    if (threadIdx.x == 0) ticket = atomicAdd(&A.sc->ticket, 1u);
+    if (warp == 0) stage_next(A, S.next, lane, ticket);
+    bar_sync(kBarLoaders, kLoaderThreads);
     for (int b = 0;; b = b + 1 == kEncoders ? 0 : b + 1) {
         Buf& B = S.buf[b];
         bar_sync(kBarEmpty + b, kLoaderThreads + 32);
-        if (threadIdx.x == 0) {
-            uint32_t k = next;
-            if (k >= A.chunk_count || *(volatile int32_t*)&A.sc->err) k = kEnd;
-            B.k = k;
-            if (k != kEnd) next = atomicAdd(&A.sc->ticket, 1u);
+        if (warp == 0) {
+            if (lane == 0) {
+                B.meta.k = S.next.k;
+                B.meta.cd = S.next.cd;
+            }
+            const uint32_t ns = S.next.k == kEnd ? 0u
+                : (S.next.cd.src_count < uint32_t(kSegCache) ? S.next.cd.src_count : uint32_t(kSegCache));
+            for (uint32_t i = lane; i < ns; i += 32) B.meta.segs[i] = S.next.segs[i];
         }
         bar_sync(kBarLoaders, kLoaderThreads);
-        const uint32_t k = B.k;
+        const uint32_t k = B.meta.k;
         if (k == kEnd) {
             // no chunk left: release every encoder warp, each once it is idle
             __threadfence_block();
@@ -653,15 +661,17 @@ __global__ void __launch_bounds__(kThreads, 1) encode_kernel(EncArgs A)
             for (int d = 1; d < kEncoders; ++d) {
                 const int o = (b + d) % kEncoders;
                 bar_sync(kBarEmpty + o, kLoaderThreads + 32);
-                if (threadIdx.x == 0) S.buf[o].k = kEnd;
+                if (threadIdx.x == 0) S.buf[o].meta.k = kEnd;
                 __threadfence_block();
                 bar_arrive(kBarFull + o, kLoaderThreads + 32);
             }
             break;
         }
-        const ChunkDesc cd = A.chunks[A.chunk_begin + k];
-        const bool overwrite = (cd.flags & kResidualFlag) || A.mode == DCR_MODE_OVERWRITE_ONLY;
-        load_slice(A, B, cd, overwrite, warp, lane);
+        const bool overwrite = (B.meta.cd.flags & kResidualFlag) || A.mode == DCR_MODE_OVERWRITE_ONLY;
+        // warp 0 stages the next chunk while this chunk's loads are in flight
+        load_slice(A, B, B.meta, overwrite, warp, lane, [&] {
+            if (warp == 0) stage_next(A, S.next, lane, ticket);
+        });
         __threadfence_block();
         bar_arrive(kBarFull + b, kLoaderThreads + 32);
     }
