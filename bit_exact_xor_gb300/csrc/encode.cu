@@ -91,6 +91,7 @@ struct __align__(16) Buf {
     uint32_t bits[kWords];             // bit i set iff mask byte i != 0
     uint16_t ev[kEvCap + 16];          // event list (sorted non-zero byte positions)
     uint32_t chg[kLoaders];            // changed stored values per slice
+    uint32_t cnt[kLoaders];            // non-zero mask bytes per slice
     Meta meta;
 };
 
@@ -248,18 +249,22 @@ __device__ __forceinline__ int list_events(Buf& B, int t, int lane, int* n_out)
 // Carried parse state between groups of 32 events.
 struct Parse {
     int prev;                  // last non-zero byte so far (-1: before the chunk)
-    unsigned long long best;   // longest zero run so far: len << 32 | start
+    unsigned long long best;   // longest zero run of earlier groups: len << 32 | start
     int lit;                   // end of the last match (start of pending literals)
     uint32_t out;              // block bytes so far
 };
 
 // Zero-run parse of n listed events (plus the virtual event at raw when
-// final), 32 at a time.  With body != nullptr the sequences are written.
+// final), 32 at a time, one per lane.  A run copies from the longest zero run
+// of the earlier groups, so every lane decides with carried state only; the
+// literal start of a match is the end of the nearest earlier match, found with
+// one ballot.  With body != nullptr the sequences are also written.
 __device__ __forceinline__ void parse_events(const Buf& B, int n, bool final, int raw, Parse& P,
                                              uint8_t* body, uint32_t body_len, int lane, bool* bad)
 {
     const uint8_t* bytes = reinterpret_cast<const uint8_t*>(B.data);
     const int total = n + (final ? 1 : 0);
+    const uint32_t lt = (1u << lane) - 1u;
     for (int g = 0; g < total; g += 32) {
         const int i = g + lane;
         const bool active = i < total;
@@ -269,69 +274,75 @@ __device__ __forceinline__ void parse_events(const Buf& B, int n, bool final, in
         if (lane == 0) pp = P.prev;
         const int gs = pp + 1;
         const int L = p - gs;
-        const unsigned long long cand =
-            active && L > 0 ? ((unsigned long long)(uint32_t)L << 32) | uint32_t(gs) : 0ull;
-        const unsigned long long cmax = warp_incl_max64(cand, lane);
-        unsigned long long bb = __shfl_up_sync(0xffffffffu, cmax, 1);
-        if (lane == 0 || bb < P.best) bb = P.best;
-        // match decision for the zero run [gs, p)
         const int me = p < raw - 5 ? p : raw - 5;
+        const uint32_t bl = uint32_t(P.best >> 32);
+        const int bs = int(uint32_t(P.best));
         int ms = -1, off = 0;
         if (active && L > 0) {
-            if (me - gs >= 4 && gs <= raw - 12 && uint32_t(bb >> 32) >= uint32_t(me - gs)) {
+            if (me - gs >= 4 && gs <= raw - 12 && bl >= uint32_t(me - gs)) {
                 ms = gs;
-                off = gs - int(uint32_t(bb));
+                off = gs - bs;
             } else if (me - gs - 1 >= 4 && gs + 1 <= raw - 12) {
                 ms = gs + 1;
                 off = 1;
             }
         }
         const bool has = ms >= 0;
-        const int mend = warp_incl_max(has ? me : 0, lane);
-        int lit = __shfl_up_sync(0xffffffffu, mend, 1);
-        if (lane == 0 || lit < P.lit) lit = P.lit;
+        const uint32_t M = __ballot_sync(0xffffffffu, has);
+        const uint32_t below = M & lt;
+        const int src = below ? 31 - __clz(below) : lane;
+        int lit = __shfl_sync(0xffffffffu, me, src);
+        if (!below) lit = P.lit;
         uint32_t sz = has ? seq_bytes(uint32_t(ms - lit), uint32_t(me - ms)) : 0u;
         const int flit = has ? me : lit;    // literals after this event's match
         if (last) sz += 1 + ext_len(uint32_t(raw - flit)) + uint32_t(raw - flit);
-        const uint32_t incl = warp_incl_sum(sz, lane);
-        if (body && (has || last)) {
-            const uint32_t o0 = P.out + incl - sz;
-            uint32_t o = o0;
-            const uint32_t end = o0 + sz < body_len ? o0 + sz : body_len;
-            auto put = [&](uint32_t v) {
-                if (o < end) body[o] = uint8_t(v);
-                ++o;
-            };
-            auto put_len = [&](uint32_t v) {
-                v -= 15;
-                for (; v >= 255; v -= 255) put(255);
-                put(v);
-            };
-            if (has) {
-                const uint32_t ll = uint32_t(ms - lit), mc = uint32_t(me - ms - 4);
-                put(((ll >= 15 ? 15u : ll) << 4) | (mc >= 15 ? 15u : mc));
-                if (ll >= 15) put_len(ll);
-                for (uint32_t q = 0; q < ll; ++q) put(bytes[lit + int(q)]);
-                put(uint32_t(off) & 0xFFu);
-                put(uint32_t(off) >> 8);
-                if (mc >= 15) put_len(mc);
+        uint32_t gsum;
+        if (body) {
+            const uint32_t incl = warp_incl_sum(sz, lane);
+            gsum = __shfl_sync(0xffffffffu, incl, 31);
+            if (has || last) {
+                const uint32_t o0 = P.out + incl - sz;
+                uint32_t o = o0;
+                const uint32_t end = o0 + sz < body_len ? o0 + sz : body_len;
+                auto put = [&](uint32_t v) {
+                    if (o < end) body[o] = uint8_t(v);
+                    ++o;
+                };
+                auto put_len = [&](uint32_t v) {
+                    v -= 15;
+                    for (; v >= 255; v -= 255) put(255);
+                    put(v);
+                };
+                if (has) {
+                    const uint32_t ll = uint32_t(ms - lit), mc = uint32_t(me - ms - 4);
+                    put(((ll >= 15 ? 15u : ll) << 4) | (mc >= 15 ? 15u : mc));
+                    if (ll >= 15) put_len(ll);
+                    for (uint32_t q = 0; q < ll; ++q) put(bytes[lit + int(q)]);
+                    put(uint32_t(off) & 0xFFu);
+                    put(uint32_t(off) >> 8);
+                    if (mc >= 15) put_len(mc);
+                }
+                if (last) {
+                    const uint32_t ll = uint32_t(raw - flit);
+                    put((ll >= 15 ? 15u : ll) << 4);
+                    if (ll >= 15) put_len(ll);
+                    for (uint32_t q = 0; q < ll; ++q) put(bytes[flit + int(q)]);
+                }
+                if (o != o0 + sz || o > body_len) *bad = true;
             }
-            if (last) {
-                const uint32_t ll = uint32_t(raw - flit);
-                put((ll >= 15 ? 15u : ll) << 4);
-                if (ll >= 15) put_len(ll);
-                for (uint32_t q = 0; q < ll; ++q) put(bytes[flit + int(q)]);
-            }
-            if (o != o0 + sz || o > body_len) *bad = true;
+        } else {
+            gsum = __reduce_add_sync(0xffffffffu, sz);
         }
-        // carry
+        // carry to the next group
         const int lastlane = (total - g < 32 ? total - g : 32) - 1;
         P.prev = __shfl_sync(0xffffffffu, p, lastlane);
-        const unsigned long long call = __shfl_sync(0xffffffffu, cmax, 31);
-        if (call > P.best) P.best = call;
-        const int mall = __shfl_sync(0xffffffffu, mend, 31);
-        if (mall > P.lit) P.lit = mall;
-        P.out += __shfl_sync(0xffffffffu, incl, 31);
+        const uint32_t clen = active && L > 0 ? uint32_t(L) : 0u;
+        const uint32_t mlen = __reduce_max_sync(0xffffffffu, clen);
+        const uint32_t mst = __reduce_max_sync(0xffffffffu, clen == mlen && mlen ? uint32_t(gs) : 0u);
+        const unsigned long long gbest = ((unsigned long long)mlen << 32) | mst;
+        if (gbest > P.best) P.best = gbest;
+        if (M) P.lit = __shfl_sync(0xffffffffu, me, 31 - __clz(M));
+        P.out += gsum;
     }
 }
 
@@ -373,7 +384,7 @@ __device__ __forceinline__ void load_slice(const EncArgs& A, Buf& B, const Meta&
     const int nseg = int(cd.src_count);
     const Seg* segs = nseg <= kSegCache ? M.segs : A.src + cd.src_begin;
     uint8_t* bytes = reinterpret_cast<uint8_t*>(B.data);
-    uint32_t changed = 0;
+    uint32_t changed = 0, events = 0;
     const int v0 = w * kVecPerWarp;
 
     // bitmap word of the vector pair (v, v + 1) held by lanes (even, odd)
@@ -410,6 +421,7 @@ __device__ __forceinline__ void load_slice(const EncArgs& A, Buf& B, const Meta&
             uint4 m = make_uint4(o[j].x ^ n[j].x, o[j].y ^ n[j].y, o[j].z ^ n[j].z, o[j].w ^ n[j].w);
             uint32_t z = nz16(m);
             changed += changed_in(z, m, cd.bits);
+            events += __popc(z);
             B.data[v] = overwrite ? n[j] : m;
             map_vec(v, z);
         }
@@ -437,6 +449,7 @@ __device__ __forceinline__ void load_slice(const EncArgs& A, Buf& B, const Meta&
                     const uint4 m = B.data[v];
                     const uint32_t z = nz16(m);
                     changed += changed_in(z, m, cd.bits);
+                    events += __popc(z);
                     map_vec(v, z);
                 }
                 __syncwarp();
@@ -444,7 +457,46 @@ __device__ __forceinline__ void load_slice(const EncArgs& A, Buf& B, const Meta&
         }
     }
     changed = __reduce_add_sync(0xffffffffu, changed);
-    if (lane == 0) B.chg[w] = changed;
+    events = __reduce_add_sync(0xffffffffu, events);
+    if (lane == 0) {
+        B.chg[w] = changed;
+        B.cnt[w] = events;
+    }
+}
+
+// Second loader phase, after every slice has been counted: write the sorted
+// positions of this slice's non-zero mask bytes at the slice's place in the
+// chunk's event list (skipped when the whole list would not fit).  The
+// in-warp prefix of the per-lane counts comes from five independent ballots
+// on the bits of the count.
+__device__ __forceinline__ void list_slice(Buf& B, int w, int lane)
+{
+    const uint32_t c_all = lane < kLoaders ? B.cnt[lane] : 0u;
+    const uint32_t total = __reduce_add_sync(0xffffffffu, c_all);
+    if (total > uint32_t(kEvCap)) return;
+    uint32_t base = __reduce_add_sync(0xffffffffu, lane < w ? c_all : 0u);
+    const uint32_t lt = (1u << lane) - 1u;
+    const int v0 = w * kVecPerWarp;
+#pragma unroll
+    for (int j = 0; j < kVPL; ++j) {
+        const int v = v0 + j * 32 + lane;
+        uint32_t z = (B.bits[v >> 1] >> (16 * (v & 1))) & 0xFFFFu;
+        const uint32_t c = __popc(z);
+        uint32_t pre = 0, tot = 0;
+#pragma unroll
+        for (int k = 0; k < 5; ++k) {
+            const uint32_t b = __ballot_sync(0xffffffffu, (c >> k) & 1u);
+            pre += __popc(b & lt) << k;
+            tot += __popc(b) << k;
+        }
+        uint32_t at = base + pre;
+        while (z) {
+            const int i = __ffs(z) - 1;
+            z &= z - 1;
+            B.ev[at++] = uint16_t(16 * v + i);
+        }
+        base += tot;
+    }
 }
 
 // Loader warp 0: stage the next chunk's descriptor and pieces.  `ticket`
@@ -488,7 +540,11 @@ __device__ __forceinline__ void encode_chunk(const EncArgs& A, Buf& B, int lane)
     bool complete = false, bad = false;
     const uint32_t ub = cd.bits == 16 ? 2u : 1u;
     if (chg && !overwrite) {
-        const uint32_t total = lz4_block(B, raw, nullptr, 0, false, 0, lane, &bad, &n_listed, &complete);
+        const uint32_t m = __reduce_add_sync(0xffffffffu, lane < kLoaders ? B.cnt[lane] : 0u);
+        complete = m <= uint32_t(kEvCap);   // the loaders listed every event
+        n_listed = int(m);
+        const uint32_t total =
+            lz4_block(B, raw, nullptr, 0, complete, n_listed, lane, &bad, &n_listed, &complete);
         if (total < uint32_t(raw)) {
             kind = kXorLz4;
             body_len = total;
@@ -672,6 +728,10 @@ __global__ void __launch_bounds__(kThreads, 1) encode_kernel(EncArgs A)
         load_slice(A, B, B.meta, overwrite, warp, lane, [&] {
             if (warp == 0) stage_next(A, S.next, lane, ticket);
         });
+        if (!overwrite) {
+            bar_sync(kBarLoaders, kLoaderThreads);
+            list_slice(B, warp, lane);
+        }
         __threadfence_block();
         bar_arrive(kBarFull + b, kLoaderThreads + 32);
     }
