@@ -91,7 +91,6 @@ struct __align__(16) Buf {
     uint32_t bits[kWords];             // bit i set iff mask byte i != 0
     uint16_t ev[kEvCap + 16];          // event list (sorted non-zero byte positions)
     uint32_t chg[kLoaders];            // changed stored values per slice
-    uint32_t cnt[kLoaders];            // non-zero mask bytes per slice
     Meta meta;
 };
 
@@ -384,7 +383,7 @@ __device__ __forceinline__ void load_slice(const EncArgs& A, Buf& B, const Meta&
     const int nseg = int(cd.src_count);
     const Seg* segs = nseg <= kSegCache ? M.segs : A.src + cd.src_begin;
     uint8_t* bytes = reinterpret_cast<uint8_t*>(B.data);
-    uint32_t changed = 0, events = 0;
+    uint32_t changed = 0;
     const int v0 = w * kVecPerWarp;
 
     // bitmap word of the vector pair (v, v + 1) held by lanes (even, odd)
@@ -421,7 +420,6 @@ __device__ __forceinline__ void load_slice(const EncArgs& A, Buf& B, const Meta&
             uint4 m = make_uint4(o[j].x ^ n[j].x, o[j].y ^ n[j].y, o[j].z ^ n[j].z, o[j].w ^ n[j].w);
             uint32_t z = nz16(m);
             changed += changed_in(z, m, cd.bits);
-            events += __popc(z);
             B.data[v] = overwrite ? n[j] : m;
             map_vec(v, z);
         }
@@ -449,7 +447,6 @@ __device__ __forceinline__ void load_slice(const EncArgs& A, Buf& B, const Meta&
                     const uint4 m = B.data[v];
                     const uint32_t z = nz16(m);
                     changed += changed_in(z, m, cd.bits);
-                    events += __popc(z);
                     map_vec(v, z);
                 }
                 __syncwarp();
@@ -457,46 +454,7 @@ __device__ __forceinline__ void load_slice(const EncArgs& A, Buf& B, const Meta&
         }
     }
     changed = __reduce_add_sync(0xffffffffu, changed);
-    events = __reduce_add_sync(0xffffffffu, events);
-    if (lane == 0) {
-        B.chg[w] = changed;
-        B.cnt[w] = events;
-    }
-}
-
-// Second loader phase, after every slice has been counted: write the sorted
-// positions of this slice's non-zero mask bytes at the slice's place in the
-// chunk's event list (skipped when the whole list would not fit).  The
-// in-warp prefix of the per-lane counts comes from five independent ballots
-// on the bits of the count.
-__device__ __forceinline__ void list_slice(Buf& B, int w, int lane)
-{
-    const uint32_t c_all = lane < kLoaders ? B.cnt[lane] : 0u;
-    const uint32_t total = __reduce_add_sync(0xffffffffu, c_all);
-    if (total > uint32_t(kEvCap)) return;
-    uint32_t base = __reduce_add_sync(0xffffffffu, lane < w ? c_all : 0u);
-    const uint32_t lt = (1u << lane) - 1u;
-    const int v0 = w * kVecPerWarp;
-#pragma unroll
-    for (int j = 0; j < kVPL; ++j) {
-        const int v = v0 + j * 32 + lane;
-        uint32_t z = (B.bits[v >> 1] >> (16 * (v & 1))) & 0xFFFFu;
-        const uint32_t c = __popc(z);
-        uint32_t pre = 0, tot = 0;
-#pragma unroll
-        for (int k = 0; k < 5; ++k) {
-            const uint32_t b = __ballot_sync(0xffffffffu, (c >> k) & 1u);
-            pre += __popc(b & lt) << k;
-            tot += __popc(b) << k;
-        }
-        uint32_t at = base + pre;
-        while (z) {
-            const int i = __ffs(z) - 1;
-            z &= z - 1;
-            B.ev[at++] = uint16_t(16 * v + i);
-        }
-        base += tot;
-    }
+    if (lane == 0) B.chg[w] = changed;
 }
 
 // Loader warp 0: stage the next chunk's descriptor and pieces.  `ticket`
@@ -540,11 +498,7 @@ __device__ __forceinline__ void encode_chunk(const EncArgs& A, Buf& B, int lane)
     bool complete = false, bad = false;
     const uint32_t ub = cd.bits == 16 ? 2u : 1u;
     if (chg && !overwrite) {
-        const uint32_t m = __reduce_add_sync(0xffffffffu, lane < kLoaders ? B.cnt[lane] : 0u);
-        complete = m <= uint32_t(kEvCap);   // the loaders listed every event
-        n_listed = int(m);
-        const uint32_t total =
-            lz4_block(B, raw, nullptr, 0, complete, n_listed, lane, &bad, &n_listed, &complete);
+        const uint32_t total = lz4_block(B, raw, nullptr, 0, false, 0, lane, &bad, &n_listed, &complete);
         if (total < uint32_t(raw)) {
             kind = kXorLz4;
             body_len = total;
@@ -728,10 +682,6 @@ __global__ void __launch_bounds__(kThreads, 1) encode_kernel(EncArgs A)
         load_slice(A, B, B.meta, overwrite, warp, lane, [&] {
             if (warp == 0) stage_next(A, S.next, lane, ticket);
         });
-        if (!overwrite) {
-            bar_sync(kBarLoaders, kLoaderThreads);
-            list_slice(B, warp, lane);
-        }
         __threadfence_block();
         bar_arrive(kBarFull + b, kLoaderThreads + 32);
     }
