@@ -183,9 +183,9 @@ __device__ bool claim(unsigned long long* st, uint64_t V, bool* timeout)
 
 // ---- warp-level LZ4 (ZSRC) decode fused with the XOR --------------------
 // Returns true if the block is well formed and kept its ZSRC promise.
-__device__ bool zsrc_decode_apply(const ApplyArgs& A, const ChunkDesc& cd, const Seg* ds,
-                                  const uint8_t* src, uint32_t n, uint32_t raw, uint32_t lim,
-                                  uint32_t* bits, int lane)
+__device__ bool zsrc_decode_once(const ApplyArgs& A, const ChunkDesc& cd, const Seg* ds,
+                                 const uint8_t* src, uint32_t n, uint32_t raw, uint32_t lim,
+                                 uint32_t* bits, int lane, uint32_t& runs)
 {
     for (uint32_t w = lane; w < (raw + 31) / 32; w += 32) bits[w] = 0;
     __syncwarp();
@@ -212,6 +212,7 @@ __device__ bool zsrc_decode_apply(const ApplyArgs& A, const ChunkDesc& cd, const
             }
         }
         __syncwarp();
+        ++runs;
         ip += ll;
         op += ll;
         if (ip == n) break;
@@ -243,6 +244,59 @@ __device__ bool zsrc_decode_apply(const ApplyArgs& A, const ChunkDesc& cd, const
         op += ml;
     }
     return op == raw;
+}
+
+// XOR is its own inverse: re-applying the first `runs` literal runs of a frame
+// that failed part-way restores every byte the failed pass touched, so a
+// corrupt frame leaves its chunk exactly as it was (the overwrite-only retry
+// rewrites changed units only and could not repair bytes outside them).  The
+// runs replayed passed every bounds check the first time.
+__device__ void zsrc_undo(const ApplyArgs& A, const ChunkDesc& cd, const Seg* ds,
+                          const uint8_t* src, uint32_t lim, uint32_t runs, int lane)
+{
+    uint32_t ip = 0, op = 0;
+    for (uint32_t r = 0; r < runs; ++r) {
+        const uint32_t tok = src[ip++];
+        uint32_t ll = tok >> 4;
+        if (ll == 15) {
+            uint32_t b;
+            do {
+                b = src[ip++];
+                ll += b;
+            } while (b == 255);
+        }
+        for (uint32_t i = lane; i < ll; i += 32) {
+            uint32_t b = src[ip + i];
+            uint32_t x = op + i;
+            if (b && x < lim) xor_byte(A.target, dst_of(ds, cd.dst_count, x), b);
+        }
+        __syncwarp();
+        ip += ll;
+        op += ll;
+        if (r + 1 == runs) break;
+        ip += 2;
+        uint32_t ml = tok & 15u;
+        if (ml == 15) {
+            uint32_t b;
+            do {
+                b = src[ip++];
+                ml += b;
+            } while (b == 255);
+        }
+        op += ml + 4;
+    }
+}
+
+// Decode a ZSRC frame, XOR-ing its literal bytes into the target as they are
+// parsed; on any error the partial apply is undone before returning false.
+__device__ bool zsrc_decode_apply(const ApplyArgs& A, const ChunkDesc& cd, const Seg* ds,
+                                  const uint8_t* src, uint32_t n, uint32_t raw, uint32_t lim,
+                                  uint32_t* bits, int lane)
+{
+    uint32_t runs = 0;
+    if (zsrc_decode_once(A, cd, ds, src, n, raw, lim, bits, lane, runs)) return true;
+    if (runs) zsrc_undo(A, cd, ds, src, lim, runs, lane);
+    return false;
 }
 
 // ================================================================ kernels ==

@@ -240,6 +240,56 @@ def test_corrupt_lz4_frame_reported_and_retry_recovers():
     assert rc == dcr.OK and np.array_equal(c.host(t), c.exp)
 
 
+def _last_match_offset(body):
+    """Byte position of the offset field of the last match in an LZ4 block."""
+    ip, last = 0, None
+    while True:
+        tok = int(body[ip]); ip += 1
+        ll = tok >> 4
+        if ll == 15:
+            while True:
+                b = int(body[ip]); ip += 1; ll += b
+                if b != 255:
+                    break
+        ip += ll
+        if ip == body.size:
+            return last
+        last = ip
+        ip += 2
+        if tok & 15 == 15:
+            while int(body[ip]) == 255:
+                ip += 1
+            ip += 1
+
+
+def test_frame_failing_late_leaves_its_chunk_untouched():
+    # a ZSRC frame whose last match offset is zeroed fails only after most of
+    # its literals were XOR-ed in; the chunk must come back exactly as it was,
+    # otherwise the overwrite-only retry (changed units only) cannot repair it
+    c = Case(configs.mini(1))
+    pl, size, _ = c.encode()
+    g = pl[:size].cpu().numpy()
+    _, frames, _ = parse(g)
+    k = next(i for i, f in enumerate(frames)
+             if f["kind"] == 1 and f["flags"] & 1 and _last_match_offset(f["body"]) not in (None, 0))
+    f = frames[k]
+    bad = g.copy()
+    at = f["offset"] + 32 + _last_match_offset(f["body"])
+    bad[at:at + 2] = 0
+    t = c.target()
+    st = dcr.RecvState(c.plan, 0)
+    rc, _ = dcr.apply(c.plan, st, torch.from_numpy(bad).cuda(), size, t)
+    assert rc == dcr.ERR_CORRUPT and st.version == 0
+    # the oracle applying every other frame gives the expected bytes
+    rest = _reindexed(g, [i for i in range(len(frames)) if i != k])
+    ref = c.start.copy()
+    assert c.orc.apply(c.orc.state(0), rest, ref) == oracle.OK
+    assert np.array_equal(c.host(t), ref)
+    rp, rsize, _ = c.encode(mode=dcr.MODE_OVERWRITE_ONLY)
+    rc, _ = dcr.apply_retry(c.plan, st, rp, rsize, t)
+    assert rc == dcr.OK and st.version == 1 and np.array_equal(c.host(t), c.exp)
+
+
 def test_zsrc_flag_is_verified():
     # a greedy (oracle) block whose matches copy non-zero bytes, relabelled
     # as ZSRC, must be rejected rather than applied as zeros
