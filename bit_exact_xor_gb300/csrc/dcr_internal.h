@@ -66,6 +66,19 @@ struct EncScratch {
     uint64_t total;     // stream bytes
     uint64_t n_frames;
     uint64_t changed;   // changed elements in the window
+    uint32_t n_spill;   // chunks whose frame body the spill kernel writes
+    uint32_t pad;
+};
+
+// A chunk whose frame is placed and sized but whose body did not fit the
+// encoder warp's staging buffer: the spill kernel re-derives and writes it.
+struct SpillRec {
+    uint32_t k;          // window-relative chunk
+    uint32_t kind;       // FrameKind
+    uint32_t body_len;
+    uint32_t n_units;    // overwrite records: unit count
+    uint64_t foff;       // frame offset in the stream
+    uint64_t pad;
 };
 
 // Device scratch of one apply call (reset by a memset per call).
@@ -97,6 +110,7 @@ struct Part {
 struct KernelConfig {
     int num_sms = 0;
     int enc_blocks_per_sm = 0;
+    int spill_blocks_per_sm = 0;
     int apply_blocks_per_sm = 0;
     int defer_blocks_per_sm = 0;
 };
@@ -145,6 +159,7 @@ struct dcr_plan {
     size_t enc_head_bytes = 0;
     uint64_t* d_lb = nullptr;
     uint32_t* d_fsize = nullptr;
+    dcr::SpillRec* d_spill = nullptr;  // max_window_chunks
     void* h_enc = nullptr;  // pinned mirror of the scratch head
     // kernel timing (dcr_plan_set_profiling)
     bool profiling = false;

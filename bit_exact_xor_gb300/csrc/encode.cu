@@ -1,12 +1,13 @@
-// Sender hot path: one persistent, warp-specialised kernel per window.
+// Sender hot path: per window, one persistent kernel encodes every chunk,
+// a second one writes the few frame bodies that did not fit on chip, and a
+// third writes the frame index and the stream header.
 //
-// Per 64 KiB canonical chunk it gathers old and new through the plan's
-// shard->canonical pieces, forms mask = old XOR new in shared memory, counts
-// changed stored values, encodes the chunk (LZ4 block, raw mask, overwrite
-// records or dense overwrite) and writes the frame straight to its final
-// place in the stream, found by a decoupled look-back over the frame sizes
-// of earlier chunks.  A small second kernel writes the frame index and the
-// stream header.
+// Per 64 KiB canonical chunk the encoder gathers old and new through the
+// plan's shard->canonical pieces, forms mask = old XOR new, counts changed
+// stored values, encodes the chunk (LZ4 block, raw mask, overwrite records or
+// dense overwrite) and writes the frame straight to its final place in the
+// stream, found by a decoupled look-back over the frame sizes of earlier
+// chunks.
 //
 // Method: "GPU-accelerated weight teleportation", "Delta update algebra"
 // (mask = old XOR new on raw bits) and "A strong baseline with the
@@ -15,25 +16,34 @@
 // "Residual Conversion" and "Hybrid encoding and compression" (XOR masks for
 // affine changes, overwrites for residual ones).
 //
-// Structure.  One CTA per SM: 16 loader warps and 2 encoder warps share two
-// chunk buffers in shared memory.  Loader warp w gathers the contiguous 4 KiB
-// slice [4096 w, 4096 w + 4096) of the chunk with 16-byte streaming loads,
-// XORs old and new, counts changes, and sets one bitmap bit per non-zero mask
-// byte.  The next chunk's ticket, descriptor and pieces are staged one
-// iteration ahead, so the data loads of a chunk issue at once.  Encoder warp
-// b owns buffer b: it compacts the bitmap into a sorted list of non-zero byte
-// positions ("events"), parses the chunk from the events 32 at a time (one per
-// lane, connected by warp scans), waits for its place in the stream and writes
-// the frame, while the loaders fill the other buffer.  Named barriers hand the
-// buffers back and forth.
+// encode_kernel.  One warp per chunk, chunks taken in ticket order, 20 warps
+// per SM.  The warp streams its chunk in 2 KiB steps (four 16-byte loads of
+// old and new per lane), XORs and counts, and appends the positions and
+// values of the non-zero mask bytes ("events") to a ring in shared memory.
+// Every 32 events it runs one parse group (one event per lane, connected by
+// ballots and warp sums) that writes the LZ4 sequences into a 6 KiB staging
+// buffer.  Overwrite chunks stage their records instead.  When the stream
+// end is reached the warp publishes the frame size, looks back for its
+// offset and copies the staged body out with 16-byte stores.  A chunk whose
+// body or pending literals outgrow the staging buffer or the ring is sized
+// all the same (the parse carries on without writing) and is listed for the
+// spill kernel.
+//
+// spill_kernel.  One CTA per listed chunk: 16 warps gather the mask into
+// shared memory (64 KiB plus a bitmap of its non-zero bytes), then one warp
+// re-runs the same parse over the bitmap's event list, reading literal bytes
+// from the mask, and writes the body at the place the encoder reserved; raw
+// and dense frames are copied by the whole CTA.  Both kernels call the same
+// parse_group with groups of 32 consecutive events from the first one, so
+// their sizes agree by construction (a disagreement is reported).
 //
 // LZ4 parse.  The masks are long zero runs around sparse non-zero bytes, so
 // every zero run of at least 4 bytes becomes one match and everything else
-// stays literal.  A run is copied from the longest earlier zero run when that
-// one is long enough (non-overlapping copy), else it keeps its first zero as a
-// literal and copies from it with offset 1.  Every match therefore copies zero
-// bytes only (frame flag ZSRC), and the block obeys the format's end rules
-// (last 5 bytes literals, no match start in the last 12 bytes).
+// stays literal.  A run is copied from the longest zero run of the earlier
+// groups when that one is long enough (non-overlapping copy), else it keeps
+// its first zero as a literal and copies from it with offset 1.  Every match
+// therefore copies zero bytes only (frame flag ZSRC), and the block obeys the
+// format's end rules (last 5 bytes literals, no match start in the last 12).
 #include <cuda_runtime.h>
 
 #include <climits>
@@ -44,24 +54,26 @@
 namespace dcr {
 namespace {
 
-constexpr int kLoaders = 16;                      // loader warps
-constexpr int kEncoders = 2;                      // encoder warps = chunk buffers
-constexpr int kThreads = 32 * (kLoaders + kEncoders);
-constexpr int kLoaderThreads = 32 * kLoaders;
+constexpr uint32_t kFull = 0xffffffffu;
+// encode_kernel
+constexpr int kMWarps = 10;                       // warps per CTA, one chunk each
+constexpr int kMThreads = 32 * kMWarps;
+constexpr int kRing = 1024;                       // event ring entries per warp (power of two)
+constexpr int kStage = 6144;                      // staged frame body bytes per warp
+constexpr int kMVPL = 4;                          // 16-byte vectors per lane per step
+constexpr int kStepVec = 32 * kMVPL;              // 2 KiB per step
+constexpr int kMSegCache = 64;                    // sender pieces cached per warp
+// spill_kernel
+constexpr int kSWarps = 16;                       // each gathers one 4 KiB slice
+constexpr int kSThreads = 32 * kSWarps;
 constexpr int kNVec = kChunk / 16;                // 16-byte vectors per chunk
-constexpr int kVecPerWarp = kNVec / kLoaders;     // 256: a 4 KiB slice
+constexpr int kVecPerWarp = kNVec / kSWarps;      // 256
 constexpr int kVPL = kVecPerWarp / 32;            // 8 vectors per lane
 constexpr int kWords = kChunk / 32;               // bitmap words per chunk
 constexpr int kSteps = kWords / 32;               // 64 warp steps over the bitmap
 constexpr int kEvCap = 6144;                      // events listed per batch
-constexpr int kSegCache = 64;                     // sender pieces staged in smem
-constexpr uint32_t kEnd = 0xFFFFFFFFu;
+constexpr int kSegCache = 64;
 constexpr uint32_t kSpinLimit = 1u << 22;         // bounded look-back wait
-
-// named barriers (0 is left to __syncthreads, unused here)
-constexpr int kBarLoaders = 1;
-constexpr int kBarEmpty = 2;                   // + buffer
-constexpr int kBarFull = 2 + kEncoders;        // + buffer
 
 struct EncArgs {
     const ChunkDesc* chunks;
@@ -76,27 +88,29 @@ struct EncArgs {
     unsigned long long* counts;
     uint64_t* lb;
     uint32_t* fsize;
+    SpillRec* spill;
 };
 
-// chunk metadata staged in shared memory
+// encode_kernel: one warp's shared memory
+struct __align__(16) WarpSmem {
+    uint8_t stage[kStage];             // LZ4 body, or unit offsets then values
+    uint16_t pos[kRing];               // event ring: byte position in the chunk
+    uint8_t val[kRing];                //             mask byte
+    Seg segs[kMSegCache];              // the chunk's sender pieces
+};
+
+// spill_kernel: one chunk in shared memory
 struct __align__(16) Meta {
     ChunkDesc cd;
-    uint32_t k;                        // window-relative chunk, or kEnd
-    uint32_t pad[3];
+    uint32_t pad[4];
     Seg segs[kSegCache];               // first pieces (all of them if src_count <= kSegCache)
 };
 
 struct __align__(16) Buf {
     uint4 data[kNVec];                 // mask (XOR chunks) or new bytes (overwrite chunks)
     uint32_t bits[kWords];             // bit i set iff mask byte i != 0
-    uint16_t ev[kEvCap + 16];          // event list (sorted non-zero byte positions)
-    uint32_t chg[kLoaders];            // changed stored values per slice
+    uint16_t ev[kEvCap + 32];          // event list (sorted non-zero byte positions)
     Meta meta;
-};
-
-struct __align__(16) Smem {
-    Buf buf[kEncoders];
-    Meta next;                         // the loaders' next chunk, staged ahead
 };
 
 // ---------------------------------------------------------------- helpers --
@@ -121,14 +135,16 @@ __device__ __forceinline__ uint64_t ld_acquire(const uint64_t* p)
     return v;
 }
 
-__device__ __forceinline__ void bar_sync(int id, int n)
+__device__ __forceinline__ uint4 xor4(uint4 a, uint4 b)
 {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+    return make_uint4(a.x ^ b.x, a.y ^ b.y, a.z ^ b.z, a.w ^ b.w);
 }
 
-__device__ __forceinline__ void bar_arrive(int id, int n)
+// byte i (0..15) of v, without dynamic register indexing
+__device__ __forceinline__ uint32_t byte_of(uint4 v, uint32_t i)
 {
-    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory");
+    const uint32_t w = i < 8 ? (i < 4 ? v.x : v.y) : (i < 12 ? v.z : v.w);
+    return (w >> (8 * (i & 3))) & 0xFFu;
 }
 
 // 4-bit mask of the non-zero bytes of w (bit i <-> byte i)
@@ -160,8 +176,8 @@ __device__ __forceinline__ uint32_t changed_in(uint32_t m, uint4 v, uint32_t bit
     return c;
 }
 
-// overwrite units of a bitmap word: bit i set iff the unit starting at byte i
-// (ub = 2: even i only) has a non-zero mask byte
+// overwrite units of a non-zero-byte mask: bit i set iff the unit starting at
+// byte i (ub = 2: even i only) has a non-zero mask byte
 __device__ __forceinline__ uint32_t unit_bits(uint32_t b, uint32_t ub)
 {
     return ub == 2 ? (b | (b >> 1)) & 0x55555555u : b;
@@ -189,206 +205,459 @@ __device__ __forceinline__ uint32_t seq_bytes(uint32_t ll, uint32_t ml)
     return 1 + ext_len(ll) + ll + 2 + ext_len(ml - 4);
 }
 
-// ---- warp scans -------------------------------------------------------------
 __device__ __forceinline__ uint32_t warp_incl_sum(uint32_t v, int lane)
 {
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
-        uint32_t o = __shfl_up_sync(0xffffffffu, v, d);
+        uint32_t o = __shfl_up_sync(kFull, v, d);
         if (lane >= d) v += o;
     }
     return v;
 }
 
-__device__ __forceinline__ unsigned long long warp_incl_max64(unsigned long long v, int lane)
+// exclusive warp prefix of c (0..31) from five independent ballots; *tot = sum
+__device__ __forceinline__ uint32_t ballot_prefix(uint32_t c, int lane, uint32_t* tot)
 {
+    const uint32_t lt = (1u << lane) - 1u;
+    uint32_t pre = 0, t = 0;
 #pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-        unsigned long long o = __shfl_up_sync(0xffffffffu, v, d);
-        if (lane >= d && o > v) v = o;
+    for (int k = 0; k < 5; ++k) {
+        const uint32_t b = __ballot_sync(kFull, (c >> k) & 1u);
+        pre += uint32_t(__popc(b & lt)) << k;
+        t += uint32_t(__popc(b)) << k;
     }
-    return v;
+    *tot = t;
+    return pre;
 }
 
-__device__ __forceinline__ int warp_incl_max(int v, int lane)
+__device__ __forceinline__ void report(EncScratch* sc, int code)
 {
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-        int o = __shfl_up_sync(0xffffffffu, v, d);
-        if (lane >= d) v = max(v, o);
-    }
-    return v;
+    atomicCAS(reinterpret_cast<int*>(&sc->err), 0, code);
 }
 
-// ---- events -------------------------------------------------------------------
-// Appends the positions of the set bits of bitmap steps [t, ...) to B.ev,
-// in order, until a further step might not fit.  Returns the step reached.
-__device__ __forceinline__ int list_events(Buf& B, int t, int lane, int* n_out)
-{
-    int n = 0;
-    for (; t < kSteps; ++t) {
-        const uint32_t w = B.bits[32 * t + lane];
-        const uint32_t c = __popc(w);
-        const uint32_t incl = warp_incl_sum(c, lane);
-        const uint32_t tot = __shfl_sync(0xffffffffu, incl, 31);
-        if (n + int(tot) > kEvCap) break;
-        uint32_t at = uint32_t(n) + incl - c, b = w;
-        while (b) {
-            const int i = __ffs(b) - 1;
-            b &= b - 1;
-            B.ev[at++] = uint16_t((32 * t + lane) * 32 + i);
-        }
-        n += int(tot);
-    }
-    __syncwarp();
-    *n_out = n;
-    return t;
-}
-
+// ------------------------------------------------------------------ parse --
 // Carried parse state between groups of 32 events.
 struct Parse {
     int prev;                  // last non-zero byte so far (-1: before the chunk)
     unsigned long long best;   // longest zero run of earlier groups: len << 32 | start
     int lit;                   // end of the last match (start of pending literals)
+    int lit_ev;                // first event at or after lit
     uint32_t out;              // block bytes so far
 };
 
-// Zero-run parse of n listed events (plus the virtual event at raw when
-// final), 32 at a time, one per lane.  A run copies from the longest zero run
-// of the earlier groups, so every lane decides with carried state only; the
-// literal start of a match is the end of the nearest earlier match, found with
-// one ballot.  With body != nullptr the sequences are also written.
-__device__ __forceinline__ void parse_events(const Buf& B, int n, bool final, int raw, Parse& P,
-                                             uint8_t* body, uint32_t body_len, int lane, bool* bad)
+// Events of encode_kernel: the warp's ring of positions and mask bytes.
+struct RingSrc {
+    const uint16_t* pos;
+    const uint8_t* val;
+    __device__ __forceinline__ int at(int e) const { return pos[e & (kRing - 1)]; }
+    // put the literal bytes [a, b), which hold events [e, e_end); false if
+    // those events do not fall inside
+    template <class Put>
+    __device__ __forceinline__ bool lits(int a, int b, int e, int e_end, Put& put) const
+    {
+        for (int q = a; q < b; ++q) {
+            uint32_t v = 0;
+            if (e < e_end && int(pos[e & (kRing - 1)]) == q) {
+                v = val[e & (kRing - 1)];
+                ++e;
+            }
+            put(v);
+        }
+        return e == e_end;
+    }
+};
+
+// Events of spill_kernel: the listed positions, literal bytes from the mask.
+struct MaskSrc {
+    const uint16_t* ev;
+    const uint8_t* bytes;
+    __device__ __forceinline__ int at(int e) const { return ev[e]; }
+    template <class Put>
+    __device__ __forceinline__ bool lits(int a, int b, int, int, Put& put) const
+    {
+        for (int q = a; q < b; ++q) put(bytes[q]);
+        return true;
+    }
+};
+
+// One parse group: events e0 .. e0 + cnt - 1, one per lane, plus the virtual
+// event at raw when final (cnt + final <= 32).  A run copies from the longest
+// zero run of the earlier groups, so every lane decides with carried state
+// only; the literal start of a match is the end of the nearest earlier match,
+// found with one ballot.  Sizes add up in P.out.  With emit, the sequences
+// are written to out[0, cap); *over is set when one does not fit and *bad
+// when sizing and writing disagree.
+template <class Src>
+__device__ __forceinline__ void parse_group(const Src& S, int e0, int cnt, bool final, int raw, Parse& P,
+                                            uint8_t* out, uint32_t cap, bool emit, int lane, bool* over,
+                                            bool* bad)
 {
-    const uint8_t* bytes = reinterpret_cast<const uint8_t*>(B.data);
-    const int total = n + (final ? 1 : 0);
+    const int total = cnt + (final ? 1 : 0);
     const uint32_t lt = (1u << lane) - 1u;
-    for (int g = 0; g < total; g += 32) {
-        const int i = g + lane;
-        const bool active = i < total;
-        const bool last = final && i == total - 1;
-        const int p = !active ? raw : (last ? raw : int(B.ev[i]));
-        int pp = __shfl_up_sync(0xffffffffu, p, 1);
-        if (lane == 0) pp = P.prev;
-        const int gs = pp + 1;
-        const int L = p - gs;
-        const int me = p < raw - 5 ? p : raw - 5;
-        const uint32_t bl = uint32_t(P.best >> 32);
-        const int bs = int(uint32_t(P.best));
-        int ms = -1, off = 0;
-        if (active && L > 0) {
-            if (me - gs >= 4 && gs <= raw - 12 && bl >= uint32_t(me - gs)) {
-                ms = gs;
-                off = gs - bs;
-            } else if (me - gs - 1 >= 4 && gs + 1 <= raw - 12) {
-                ms = gs + 1;
-                off = 1;
-            }
+    const bool active = lane < total;
+    const bool last = final && lane == total - 1;
+    const int e = e0 + lane;
+    const int p = (!active || last) ? raw : S.at(e);
+    int pp = __shfl_up_sync(kFull, p, 1);
+    if (lane == 0) pp = P.prev;
+    const int gs = pp + 1;
+    const int L = p - gs;
+    const int me = p < raw - 5 ? p : raw - 5;
+    const uint32_t bl = uint32_t(P.best >> 32);
+    const int bs = int(uint32_t(P.best));
+    int ms = -1, off = 0;
+    if (active && L > 0) {
+        if (me - gs >= 4 && gs <= raw - 12 && bl >= uint32_t(me - gs)) {
+            ms = gs;
+            off = gs - bs;
+        } else if (me - gs - 1 >= 4 && gs + 1 <= raw - 12) {
+            ms = gs + 1;
+            off = 1;
         }
-        const bool has = ms >= 0;
-        const uint32_t M = __ballot_sync(0xffffffffu, has);
-        const uint32_t below = M & lt;
-        const int src = below ? 31 - __clz(below) : lane;
-        int lit = __shfl_sync(0xffffffffu, me, src);
-        if (!below) lit = P.lit;
-        uint32_t sz = has ? seq_bytes(uint32_t(ms - lit), uint32_t(me - ms)) : 0u;
-        const int flit = has ? me : lit;    // literals after this event's match
-        if (last) sz += 1 + ext_len(uint32_t(raw - flit)) + uint32_t(raw - flit);
-        uint32_t gsum;
-        if (body) {
-            const uint32_t incl = warp_incl_sum(sz, lane);
-            gsum = __shfl_sync(0xffffffffu, incl, 31);
-            if (has || last) {
-                const uint32_t o0 = P.out + incl - sz;
-                uint32_t o = o0;
-                const uint32_t end = o0 + sz < body_len ? o0 + sz : body_len;
-                auto put = [&](uint32_t v) {
-                    if (o < end) body[o] = uint8_t(v);
-                    ++o;
-                };
-                auto put_len = [&](uint32_t v) {
-                    v -= 15;
-                    for (; v >= 255; v -= 255) put(255);
-                    put(v);
-                };
-                if (has) {
-                    const uint32_t ll = uint32_t(ms - lit), mc = uint32_t(me - ms - 4);
-                    put(((ll >= 15 ? 15u : ll) << 4) | (mc >= 15 ? 15u : mc));
-                    if (ll >= 15) put_len(ll);
-                    for (uint32_t q = 0; q < ll; ++q) put(bytes[lit + int(q)]);
-                    put(uint32_t(off) & 0xFFu);
-                    put(uint32_t(off) >> 8);
-                    if (mc >= 15) put_len(mc);
-                }
-                if (last) {
-                    const uint32_t ll = uint32_t(raw - flit);
-                    put((ll >= 15 ? 15u : ll) << 4);
-                    if (ll >= 15) put_len(ll);
-                    for (uint32_t q = 0; q < ll; ++q) put(bytes[flit + int(q)]);
-                }
-                if (o != o0 + sz || o > body_len) *bad = true;
-            }
-        } else {
-            gsum = __reduce_add_sync(0xffffffffu, sz);
-        }
-        // carry to the next group
-        const int lastlane = (total - g < 32 ? total - g : 32) - 1;
-        P.prev = __shfl_sync(0xffffffffu, p, lastlane);
-        const uint32_t clen = active && L > 0 ? uint32_t(L) : 0u;
-        const uint32_t mlen = __reduce_max_sync(0xffffffffu, clen);
-        const uint32_t mst = __reduce_max_sync(0xffffffffu, clen == mlen && mlen ? uint32_t(gs) : 0u);
-        const unsigned long long gbest = ((unsigned long long)mlen << 32) | mst;
-        if (gbest > P.best) P.best = gbest;
-        if (M) P.lit = __shfl_sync(0xffffffffu, me, 31 - __clz(M));
-        P.out += gsum;
     }
+    const bool has = ms >= 0;
+    const uint32_t M = __ballot_sync(kFull, has);
+    const uint32_t below = M & lt;
+    const int src = below ? 31 - __clz(below) : lane;
+    int lit = __shfl_sync(kFull, me, src);
+    int lev = e0 + src;
+    if (!below) {
+        lit = P.lit;
+        lev = P.lit_ev;
+    }
+    uint32_t sz = has ? seq_bytes(uint32_t(ms - lit), uint32_t(me - ms)) : 0u;
+    const int flit = has ? me : lit;    // literals after this event's match
+    if (last) sz += 1 + ext_len(uint32_t(raw - flit)) + uint32_t(raw - flit);
+    uint32_t gsum;
+    if (emit) {
+        const uint32_t incl = warp_incl_sum(sz, lane);
+        gsum = __shfl_sync(kFull, incl, 31);
+        const uint32_t o0 = P.out + incl - sz;
+        const bool fits = o0 + sz <= cap;
+        if ((has || last) && !fits) *over = true;
+        if ((has || last) && fits) {
+            uint32_t o = o0;
+            auto put = [&](uint32_t v) { out[o++] = uint8_t(v); };
+            auto put_len = [&](uint32_t v) {
+                v -= 15;
+                for (; v >= 255; v -= 255) put(255);
+                put(v);
+            };
+            bool ok = true;
+            if (has) {
+                const uint32_t ll = uint32_t(ms - lit), mc = uint32_t(me - ms - 4);
+                put(((ll >= 15 ? 15u : ll) << 4) | (mc >= 15 ? 15u : mc));
+                if (ll >= 15) put_len(ll);
+                ok &= S.lits(lit, ms, lev, e, put);
+                put(uint32_t(off) & 0xFFu);
+                put(uint32_t(off) >> 8);
+                if (mc >= 15) put_len(mc);
+            }
+            if (last) {
+                const uint32_t ll = uint32_t(raw - flit);
+                put((ll >= 15 ? 15u : ll) << 4);
+                if (ll >= 15) put_len(ll);
+                ok &= S.lits(flit, raw, has ? e : lev, e, put);
+            }
+            if (!ok || o != o0 + sz) *bad = true;
+        }
+    } else {
+        gsum = __reduce_add_sync(kFull, sz);
+    }
+    // carry to the next group
+    P.prev = __shfl_sync(kFull, p, total - 1);
+    const uint32_t clen = active && L > 0 ? uint32_t(L) : 0u;
+    const uint32_t mlen = __reduce_max_sync(kFull, clen);
+    const uint32_t mst = __reduce_max_sync(kFull, clen == mlen && mlen ? uint32_t(gs) : 0u);
+    const unsigned long long gbest = ((unsigned long long)mlen << 32) | mst;
+    if (gbest > P.best) P.best = gbest;
+    if (M) {
+        const int hi = 31 - __clz(M);
+        P.lit = __shfl_sync(kFull, me, hi);
+        P.lit_ev = e0 + hi;
+    }
+    P.out += gsum;
 }
 
-// LZ4 block size (pass 1) or block bytes (pass 2) of the chunk in B.
-// Events that fit are listed once; larger event sets are listed in batches.
-__device__ uint32_t lz4_block(Buf& B, int raw, uint8_t* body, uint32_t body_len, bool reuse, int n_reuse,
-                              int lane, bool* bad, int* n_listed, bool* complete)
+// ------------------------------------------------------------- look-back --
+// Publish this chunk's frame size and find its offset: the warp reads 32
+// predecessors per round trip, newest first, and sums them up to the nearest
+// one that already holds an inclusive prefix.  False after a bounded wait.
+__device__ __forceinline__ bool look_back(const EncArgs& A, uint32_t k, uint32_t fsz, int lane, uint64_t* out)
 {
-    Parse P{-1, 0ull, 0, 0u};
-    if (reuse) {
-        parse_events(B, n_reuse, true, raw, P, body, body_len, lane, bad);
-        return P.out;
+    uint64_t excl = 0;
+    int ok = 1;
+    const uint64_t agg = fsz ? ((1ull << kLbFrameShift) | fsz) : 0ull;
+    if (lane == 0) {
+        A.fsize[k] = fsz;
+        st_release(&A.lb[k], (k == 0 ? kLbInc : kLbAgg) | agg);
     }
-    int t = 0, n = 0;
-    bool first = true;
-    while (true) {
-        t = list_events(B, t, lane, &n);
-        const bool fin = t >= kSteps;
-        if (first) {
-            *n_listed = n;
-            *complete = fin;
-            first = false;
+    if (k > 0) {
+        for (int64_t j = int64_t(k) - 1;; j -= 32) {
+            const int64_t idx = j - lane;
+            uint64_t v = 0;
+            uint32_t spins = 0;
+            for (;;) {
+                v = idx >= 0 ? ld_acquire(&A.lb[idx]) : kLbInc;   // before chunk 0: prefix 0
+                const uint32_t inc = __ballot_sync(kFull, (v >> 62) == 2);
+                const uint32_t upto = inc ? (2u << (__ffs(inc) - 1)) - 1u : kFull;
+                const uint32_t missing = __ballot_sync(kFull, (v >> 62) == 0) & upto;
+                if (!missing) break;
+                const bool quit = ++spins > kSpinLimit || *(volatile int32_t*)&A.sc->err != 0;
+                if (__any_sync(kFull, quit)) {   // warp-uniform exit
+                    ok = 0;
+                    break;
+                }
+                __nanosleep(64);
+            }
+            if (!ok) break;
+            const uint32_t inc = __ballot_sync(kFull, (v >> 62) == 2);
+            const uint32_t upto = inc ? (2u << (__ffs(inc) - 1)) - 1u : kFull;
+            uint64_t part = ((upto >> lane) & 1u) ? (v & kLbValMask) : 0ull;
+#pragma unroll
+            for (int d = 16; d > 0; d >>= 1) part += __shfl_xor_sync(kFull, part, d);
+            excl += part;
+            if (inc) break;
         }
-        parse_events(B, n, fin, raw, P, body, body_len, lane, bad);
-        if (fin) break;
+        if (lane == 0) {
+            if (ok) st_release(&A.lb[k], kLbInc | (excl + agg));
+            else report(A.sc, DCR_ERR_TIMEOUT);
+        }
     }
-    return P.out;
+    *out = excl;
+    return ok != 0;
 }
 
-// ---------------------------------------------------------------- loaders --
-// Gather, XOR, count and map one chunk's 4 KiB slice (loader warp w).
-// between() runs after the slice's loads are issued, before they are used.
-template <class Between>
-__device__ __forceinline__ void load_slice(const EncArgs& A, Buf& B, const Meta& M, bool overwrite,
-                                           int w, int lane, Between between)
+__device__ __forceinline__ void write_header(uint8_t* f, uint32_t kind, uint32_t bits, uint32_t chunk,
+                                             uint32_t raw, uint32_t body_len, uint32_t chg)
 {
-    const ChunkDesc& cd = M.cd;
+    const uint32_t h1 = kind | (bits << 8) | ((kind == kXorLz4 ? kFrameZsrc : 0u) << 16);
+    reinterpret_cast<uint4*>(f)[0] = make_uint4(kFrameMagic, h1, chunk, raw);
+    reinterpret_cast<uint4*>(f)[1] = make_uint4(body_len, chg, 0u, 0u);
+}
+
+// ---------------------------------------------------------- encode_kernel --
+// Byte-wise gather of one 16-byte vector at canonical byte x0 (chunks whose
+// pieces are not all 16-byte aligned); bytes at or past raw read as zero.
+__device__ __forceinline__ void gather_bytes(const EncArgs& A, const Seg* segs, int nseg, int& cur,
+                                             uint32_t x0, int raw, uint4& o, uint4& n)
+{
+    uint32_t ow[4] = {0u, 0u, 0u, 0u}, nw[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+    for (int b = 0; b < 16; ++b) {
+        const uint32_t x = x0 + uint32_t(b);
+        if (x < uint32_t(raw)) {
+            while (cur + 1 < nseg && segs[cur + 1].off <= x) ++cur;
+            const Seg sg = segs[cur];
+            const uint32_t r = uint32_t(sg.addr >> kShardShift);
+            const uint64_t a = (sg.addr & kAddrMask) + (x - sg.off);
+            ow[b >> 2] |= uint32_t(A.olds[r][a]) << (8 * (b & 3));
+            nw[b >> 2] |= uint32_t(A.news[r][a]) << (8 * (b & 3));
+        }
+    }
+    o = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+    n = make_uint4(nw[0], nw[1], nw[2], nw[3]);
+}
+
+__device__ __forceinline__ void encode_chunk(const EncArgs& A, WarpSmem& W, uint32_t k, int lane)
+{
+    const ChunkDesc cd = A.chunks[A.chunk_begin + k];
     const int raw = int(cd.raw_len);
     const int nseg = int(cd.src_count);
-    const Seg* segs = nseg <= kSegCache ? M.segs : A.src + cd.src_begin;
-    uint8_t* bytes = reinterpret_cast<uint8_t*>(B.data);
+    const bool cached = nseg <= kMSegCache;
+    if (cached)
+        for (int i = lane; i < nseg; i += 32) W.segs[i] = A.src[cd.src_begin + i];
+    __syncwarp();
+    const Seg* segs = cached ? W.segs : A.src + cd.src_begin;
+    const bool overwrite = (cd.flags & kResidualFlag) || A.mode == DCR_MODE_OVERWRITE_ONLY;
+    const bool vec = (cd.flags & kSrcVec) != 0;
+    const uint32_t ub = cd.bits == 16 ? 2u : 1u;
+    const int ncap = kStage / int(2 + ub);   // staged records: offsets at 0, values at 2 * ncap
+    const int nvec = (raw + 15) >> 4;
+    const RingSrc R{W.pos, W.val};
+
     uint32_t changed = 0;
+    Parse P{-1, 0ull, 0, 0, 0u};
+    int tail = 0, np = 0, units = 0, cur = 0;
+    bool spill = false, bad = false;
+    for (int v0 = 0; v0 < nvec; v0 += kStepVec) {
+        uint4 o[kMVPL], n[kMVPL];
+#pragma unroll
+        for (int j = 0; j < kMVPL; ++j) {
+            const int v = v0 + j * 32 + lane;
+            o[j] = n[j] = make_uint4(0u, 0u, 0u, 0u);
+            if (v < nvec) {
+                const uint32_t x = uint32_t(v) << 4;
+                if (vec) {
+                    while (cur + 1 < nseg && segs[cur + 1].off <= x) ++cur;
+                    const Seg sg = segs[cur];
+                    const uint32_t r = uint32_t(sg.addr >> kShardShift);
+                    const uint64_t a = (sg.addr & kAddrMask) + (x - sg.off);
+                    o[j] = ld_stream(A.olds[r] + a);
+                    n[j] = ld_stream(A.news[r] + a);
+                } else {
+                    gather_bytes(A, segs, nseg, cur, x, raw, o[j], n[j]);
+                }
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < kMVPL; ++j) {
+            const uint32_t v = uint32_t(v0 + j * 32 + lane);
+            const uint4 m = xor4(o[j], n[j]);
+            const uint32_t z = nz16(m);
+            changed += changed_in(z, m, cd.bits);
+            if (!overwrite) {
+                uint32_t tot;
+                const uint32_t pre = ballot_prefix(__popc(z), lane, &tot);
+                if (tot) {
+                    // the ring keeps the pending literals' events, or only the
+                    // unparsed ones once the chunk spills
+                    if (!spill && tail + int(tot) - P.lit_ev > kRing) spill = true;
+                    int e = tail + int(pre);
+                    for (uint32_t b = z; b; b &= b - 1) {
+                        const uint32_t i = __ffs(b) - 1;
+                        W.pos[e & (kRing - 1)] = uint16_t(16u * v + i);
+                        W.val[e & (kRing - 1)] = uint8_t(byte_of(m, i));
+                        ++e;
+                    }
+                    tail += int(tot);
+                    __syncwarp();
+                    while (tail - np >= 32) {
+                        bool over = false;
+                        parse_group(R, np, 32, false, raw, P, W.stage, kStage, !spill, lane, &over, &bad);
+                        np += 32;
+                        if (__any_sync(kFull, over)) spill = true;
+                    }
+                }
+            } else {
+                const uint32_t ubits = unit_bits(z, ub);
+                uint32_t tot;
+                const uint32_t pre = ballot_prefix(__popc(ubits), lane, &tot);
+                int r = units + int(pre);
+                for (uint32_t b = ubits; b; b &= b - 1) {
+                    const uint32_t i = __ffs(b) - 1;
+                    if (r < ncap) {
+                        const uint32_t u = (16u * v + i) / ub;
+                        W.stage[2 * r] = uint8_t(u);
+                        W.stage[2 * r + 1] = uint8_t(u >> 8);
+                        W.stage[2 * ncap + r * int(ub)] = uint8_t(byte_of(n[j], i));
+                        if (ub == 2) W.stage[2 * ncap + r * 2 + 1] = uint8_t(byte_of(n[j], i + 1));
+                    }
+                    ++r;
+                }
+                units += int(tot);
+            }
+        }
+    }
+    changed = __reduce_add_sync(kFull, changed);
+    if (lane == 0 && changed) {
+        atomicAdd(&A.counts[cd.tensor], (unsigned long long)changed);
+        atomicAdd(reinterpret_cast<unsigned long long*>(&A.sc->changed), (unsigned long long)changed);
+    }
+
+    uint32_t kind = 0, body_len = 0;
+    bool staged = false;
+    if (changed && !overwrite) {
+        bool over = false;
+        parse_group(R, np, tail - np, true, raw, P, W.stage, kStage, !spill, lane, &over, &bad);
+        if (__any_sync(kFull, over)) spill = true;
+        if (P.out < uint32_t(raw)) {
+            kind = kXorLz4;
+            body_len = P.out;
+            staged = !spill;
+        } else {
+            kind = kXorRaw;
+            body_len = uint32_t(raw);
+        }
+    } else if (changed) {
+        const uint32_t pad = (4 - (2 * uint32_t(units)) % 4) % 4;
+        const uint32_t rec = 4 + 2 * uint32_t(units) + pad + uint32_t(units) * ub;
+        if (rec < uint32_t(raw)) {
+            kind = kOverwrite;
+            body_len = rec;
+            staged = units <= ncap;
+        } else {
+            kind = kOverwriteDense;
+            body_len = uint32_t(raw);
+        }
+    }
+    if (__any_sync(kFull, bad) && lane == 0) report(A.sc, DCR_ERR_CORRUPT);
+    const uint32_t fsz = kind ? (kFrameHdr + body_len + 15) / 16 * 16 : 0u;
+
+    uint64_t excl;
+    if (!look_back(A, k, fsz, lane, &excl)) return;
+    const uint64_t foff = kStreamHdr + (excl & kLbByteMask);
+    if (!fsz || foff + fsz > A.cap) return;
+    uint8_t* f = A.payload + foff;
+    uint4* body = reinterpret_cast<uint4*>(f + kFrameHdr);
+    if (lane == 0) write_header(f, kind, cd.bits, A.chunk_begin + k, uint32_t(raw), body_len, changed);
+    const uint32_t nv = (body_len + 15) / 16;   // body and padding, in 16-byte vectors
+    if (!staged) {
+        if (lane == 0) {
+            const uint32_t i = atomicAdd(&A.sc->n_spill, 1u);
+            A.spill[i] = SpillRec{k, kind, body_len, uint32_t(units), foff, 0ull};
+        }
+    } else if (kind == kXorLz4) {
+        for (uint32_t i = body_len + lane; i < 16 * nv; i += 32) W.stage[i] = 0;
+        __syncwarp();
+        for (uint32_t i = lane; i < nv; i += 32) body[i] = reinterpret_cast<const uint4*>(W.stage)[i];
+    } else {
+        // records: count | unit offsets | pad to 4 | values, 16 bytes per lane
+        const uint32_t nu = uint32_t(units);
+        const uint32_t voff = 4 + 2 * nu + (4 - (2 * nu) % 4) % 4;
+        for (uint32_t i = lane; i < nv; i += 32) {
+            uint32_t w[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                uint32_t word = 0;
+#pragma unroll
+                for (int b = 0; b < 4; ++b) {
+                    const uint32_t t = 16 * i + 4 * q + b;
+                    uint32_t x = 0;
+                    if (t < 4) x = (nu >> (8 * t)) & 0xFFu;
+                    else if (t < 4 + 2 * nu) x = W.stage[t - 4];
+                    else if (t >= voff && t < body_len) x = W.stage[2 * ncap + (t - voff)];
+                    word |= x << (8 * b);
+                }
+                w[q] = word;
+            }
+            body[i] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+    }
+    __syncwarp();   // the staging buffer is reused by the next chunk
+}
+
+__global__ void __launch_bounds__(kMThreads, 2) encode_kernel(EncArgs A)
+{
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    const int lane = threadIdx.x & 31;
+    WarpSmem& W = reinterpret_cast<WarpSmem*>(smem_raw)[threadIdx.x >> 5];
+    for (;;) {
+        uint32_t k = 0;
+        if (lane == 0) {
+            k = atomicAdd(&A.sc->ticket, 1u);
+            if (*(volatile int32_t*)&A.sc->err) k = UINT_MAX;
+        }
+        k = __shfl_sync(kFull, k, 0);
+        if (k >= A.chunk_count) break;
+        encode_chunk(A, W, k, lane);
+    }
+}
+
+// ----------------------------------------------------------- spill_kernel --
+// Gather, XOR and map one chunk's 4 KiB slice (warp w).
+__device__ __forceinline__ void load_slice(const EncArgs& A, Buf& B, bool overwrite, int w, int lane)
+{
+    const ChunkDesc& cd = B.meta.cd;
+    const int raw = int(cd.raw_len);
+    const int nseg = int(cd.src_count);
+    const Seg* segs = nseg <= kSegCache ? B.meta.segs : A.src + cd.src_begin;
+    uint8_t* bytes = reinterpret_cast<uint8_t*>(B.data);
     const int v0 = w * kVecPerWarp;
 
     // bitmap word of the vector pair (v, v + 1) held by lanes (even, odd)
     auto map_vec = [&](int v, uint32_t z) {
-        const uint32_t hi = __shfl_down_sync(0xffffffffu, z, 1);
+        const uint32_t hi = __shfl_down_sync(kFull, z, 1);
         if ((lane & 1) == 0) B.bits[v >> 1] = z | (hi << 16);
     };
 
@@ -413,20 +682,16 @@ __device__ __forceinline__ void load_slice(const EncArgs& A, Buf& B, const Meta&
                 n[j] = ld_stream(A.news[r] + a);
             }
         }
-        between();
 #pragma unroll
         for (int j = 0; j < kVPL; ++j) {
             const int v = v0 + j * 32 + lane;
-            uint4 m = make_uint4(o[j].x ^ n[j].x, o[j].y ^ n[j].y, o[j].z ^ n[j].z, o[j].w ^ n[j].w);
-            uint32_t z = nz16(m);
-            changed += changed_in(z, m, cd.bits);
+            const uint4 m = xor4(o[j], n[j]);
             B.data[v] = overwrite ? n[j] : m;
-            map_vec(v, z);
+            map_vec(v, nz16(m));
         }
     } else {
-        // unaligned pieces: byte-wise gather (layouts with odd row sizes).
-        // The mask is staged first; overwrite chunks then restage new bytes.
-        between();
+        // unaligned pieces: byte-wise gather.  The mask is staged first;
+        // overwrite chunks then restage new bytes.
         for (int pass = 0; pass < (overwrite ? 2 : 1); ++pass) {
             for (int i = lane; i < 16 * kVecPerWarp; i += 32) {
                 const int x = 16 * v0 + i;
@@ -444,246 +709,134 @@ __device__ __forceinline__ void load_slice(const EncArgs& A, Buf& B, const Meta&
             if (pass == 0) {
                 for (int j = 0; j < kVPL; ++j) {
                     const int v = v0 + j * 32 + lane;
-                    const uint4 m = B.data[v];
-                    const uint32_t z = nz16(m);
-                    changed += changed_in(z, m, cd.bits);
-                    map_vec(v, z);
+                    map_vec(v, nz16(B.data[v]));
                 }
                 __syncwarp();
             }
         }
     }
-    changed = __reduce_add_sync(0xffffffffu, changed);
-    if (lane == 0) B.chg[w] = changed;
 }
 
-// Loader warp 0: stage the next chunk's descriptor and pieces.  `ticket`
-// (lane 0) holds the chunk taken one call earlier; a new one is taken here.
-__device__ __forceinline__ void stage_next(const EncArgs& A, Meta& M, int lane, uint32_t& ticket)
+// Appends the positions of the set bits of bitmap steps [t, ...) to B.ev
+// after its first n entries, in order, until a further step might not fit.
+// Returns the step reached; *n_out = entries listed in all.
+__device__ __forceinline__ int list_events(Buf& B, int t, int n, int lane, int* n_out)
 {
-    uint32_t k = 0;
-    if (lane == 0) {
-        k = ticket;
-        if (k >= A.chunk_count || *(volatile int32_t*)&A.sc->err) k = kEnd;
-        if (k != kEnd) ticket = atomicAdd(&A.sc->ticket, 1u);
+    for (; t < kSteps; ++t) {
+        const uint32_t w = B.bits[32 * t + lane];
+        const uint32_t c = __popc(w);
+        const uint32_t incl = warp_incl_sum(c, lane);
+        const uint32_t tot = __shfl_sync(kFull, incl, 31);
+        if (n + int(tot) > kEvCap) break;
+        uint32_t at = uint32_t(n) + incl - c, b = w;
+        while (b) {
+            const int i = __ffs(b) - 1;
+            b &= b - 1;
+            B.ev[at++] = uint16_t((32 * t + lane) * 32 + i);
+        }
+        n += int(tot);
     }
-    k = __shfl_sync(0xffffffffu, k, 0);
-    if (lane == 0) M.k = k;
-    if (k == kEnd) return;
-    const ChunkDesc cd = A.chunks[A.chunk_begin + k];
-    if (lane == 0) M.cd = cd;
-    const uint32_t ns = cd.src_count < uint32_t(kSegCache) ? cd.src_count : uint32_t(kSegCache);
-    for (uint32_t i = lane; i < ns; i += 32) M.segs[i] = A.src[cd.src_begin + i];
+    __syncwarp();
+    *n_out = n;
+    return t;
 }
 
-// ---------------------------------------------------------------- encoder --
-// Parse, place and write the frame of the chunk held in buffer B.
-__device__ __forceinline__ void encode_chunk(const EncArgs& A, Buf& B, int lane)
+// LZ4 block of the chunk in B written to body[0, body_len); returns its size.
+// Events are listed in batches; a batch's partial last group moves to the
+// front of the next one, so the groups are those of encode_kernel.
+__device__ uint32_t lz4_block(Buf& B, int raw, uint8_t* body, uint32_t body_len, int lane, bool* bad)
 {
-    const ChunkDesc cd = B.meta.cd;
-    const uint32_t k = B.meta.k;
-    const int raw = int(cd.raw_len);
-    const bool overwrite = (cd.flags & kResidualFlag) || A.mode == DCR_MODE_OVERWRITE_ONLY;
-    const uint8_t* bytes = reinterpret_cast<const uint8_t*>(B.data);
-
-    uint32_t chg = lane < kLoaders ? B.chg[lane] : 0u;
-    chg = __reduce_add_sync(0xffffffffu, chg);
-    if (lane == 0 && chg) {
-        atomicAdd(&A.counts[cd.tensor], (unsigned long long)chg);
-        atomicAdd(reinterpret_cast<unsigned long long*>(&A.sc->changed), (unsigned long long)chg);
-    }
-
-    uint32_t kind = 0, body_len = 0, n_units = 0;
-    int n_listed = 0;
-    bool complete = false, bad = false;
-    const uint32_t ub = cd.bits == 16 ? 2u : 1u;
-    if (chg && !overwrite) {
-        const uint32_t total = lz4_block(B, raw, nullptr, 0, false, 0, lane, &bad, &n_listed, &complete);
-        if (total < uint32_t(raw)) {
-            kind = kXorLz4;
-            body_len = total;
-        } else {
-            kind = kXorRaw;
-            body_len = uint32_t(raw);
-        }
-    } else if (chg) {
-        // overwrite records: one per changed unit (2 bytes for bf16, else 1)
-        uint32_t units = 0;
-        for (int t = 0; t < kSteps; ++t) units += __popc(unit_bits(B.bits[32 * t + lane], ub));
-        n_units = __reduce_add_sync(0xffffffffu, units);
-        const uint32_t pad = (4 - (2 * n_units) % 4) % 4;
-        const uint32_t rec = 4 + 2 * n_units + pad + n_units * ub;
-        if (rec < uint32_t(raw)) {
-            kind = kOverwrite;
-            body_len = rec;
-        } else {
-            kind = kOverwriteDense;
-            body_len = uint32_t(raw);
-        }
-    }
-    const uint32_t fsz = chg ? (kFrameHdr + body_len + 15) / 16 * 16 : 0u;
-
-    // ---- decoupled look-back for the frame's place in the stream: the warp
-    // reads 32 predecessors per round trip, newest first, and sums them up to
-    // the nearest one that already holds an inclusive prefix
-    uint64_t excl = 0;
-    int ok = 1;
-    const uint64_t agg = fsz ? ((1ull << kLbFrameShift) | fsz) : 0ull;
-    if (lane == 0) {
-        A.fsize[k] = fsz;
-        st_release(&A.lb[k], (k == 0 ? kLbInc : kLbAgg) | agg);
-    }
-    if (k > 0) {
-        for (int64_t j = int64_t(k) - 1;; j -= 32) {
-            const int64_t idx = j - lane;
-            uint64_t v = 0;
-            uint32_t spins = 0;
-            for (;;) {
-                v = idx >= 0 ? ld_acquire(&A.lb[idx]) : kLbInc;   // before chunk 0: prefix 0
-                const uint32_t inc = __ballot_sync(0xffffffffu, (v >> 62) == 2);
-                const uint32_t upto = inc ? (2u << (__ffs(inc) - 1)) - 1u : 0xffffffffu;
-                const uint32_t missing = __ballot_sync(0xffffffffu, (v >> 62) == 0) & upto;
-                if (!missing) break;
-                const bool quit = ++spins > kSpinLimit || *(volatile int32_t*)&A.sc->err != 0;
-                if (__any_sync(0xffffffffu, quit)) {   // warp-uniform exit
-                    ok = 0;
-                    break;
-                }
-                __nanosleep(64);
-            }
-            if (!ok) break;
-            const uint32_t inc = __ballot_sync(0xffffffffu, (v >> 62) == 2);
-            const uint32_t upto = inc ? (2u << (__ffs(inc) - 1)) - 1u : 0xffffffffu;
-            uint64_t part = ((upto >> lane) & 1u) ? (v & kLbValMask) : 0ull;
-#pragma unroll
-            for (int d = 16; d > 0; d >>= 1) part += __shfl_xor_sync(0xffffffffu, part, d);
-            excl += part;
-            if (inc) break;
-        }
-        if (lane == 0) {
-            if (ok) st_release(&A.lb[k], kLbInc | (excl + agg));
-            else atomicCAS(reinterpret_cast<int*>(&A.sc->err), 0, DCR_ERR_TIMEOUT);
-        }
-    }
-    if (!ok) return;
-
-    // ---- write the frame
-    const uint64_t foff = kStreamHdr + (excl & kLbByteMask);
-    if (!fsz || foff + fsz > A.cap) return;
-    uint8_t* f = A.payload + foff;
-    uint8_t* body = f + kFrameHdr;
-    if (lane == 0) {
-        const uint32_t h1 = kind | (cd.bits << 8) | ((kind == kXorLz4 ? kFrameZsrc : 0u) << 16);
-        reinterpret_cast<uint4*>(f)[0] = make_uint4(kFrameMagic, h1, A.chunk_begin + k, uint32_t(raw));
-        reinterpret_cast<uint4*>(f)[1] = make_uint4(body_len, chg, 0u, 0u);
-    }
-    for (uint32_t i = kFrameHdr + body_len + lane; i < fsz; i += 32) f[i] = 0;
-    if (kind == kXorLz4) {
-        int nl;
-        bool cp;
-        const uint32_t got = lz4_block(B, raw, body, body_len, complete, n_listed, lane, &bad, &nl, &cp);
-        if (__any_sync(0xffffffffu, bad) || got != body_len)   // sizing and emission disagree
-            if (lane == 0) atomicCAS(reinterpret_cast<int*>(&A.sc->err), 0, DCR_ERR_CORRUPT);
-    } else if (kind == kXorRaw || kind == kOverwriteDense) {
-        const int nfull = raw >> 4;
-        for (int v = lane; v < nfull; v += 32) reinterpret_cast<uint4*>(body)[v] = B.data[v];
-        for (int x = (nfull << 4) + lane; x < raw; x += 32) body[x] = bytes[x];
-    } else {
-        const uint32_t pad = (4 - (2 * n_units) % 4) % 4;
-        if (lane == 0) {
-            *reinterpret_cast<uint32_t*>(body) = n_units;
-            for (uint32_t i = 0; i < pad; ++i) body[4 + 2 * n_units + i] = 0;
-        }
-        uint8_t* offs = body + 4;
-        uint8_t* vals = body + 4 + 2 * n_units + pad;
-        uint32_t base = 0;
-        for (int t = 0; t < kSteps; ++t) {
-            const int wi = 32 * t + lane;
-            uint32_t b = unit_bits(B.bits[wi], ub);
-            const uint32_t c = __popc(b);
-            const uint32_t incl = warp_incl_sum(c, lane);
-            uint32_t u_i = base + incl - c;
-            while (b) {
-                const uint32_t x = uint32_t(wi * 32 + __ffs(b) - 1);
-                b &= b - 1;
-                const uint32_t u = x / ub;
-                if (u_i < n_units) {
-                    offs[2 * u_i] = uint8_t(u);
-                    offs[2 * u_i + 1] = uint8_t(u >> 8);
-                    for (uint32_t e = 0; e < ub; ++e) vals[u_i * ub + e] = bytes[x + e];
-                }
-                ++u_i;
-            }
-            base += __shfl_sync(0xffffffffu, incl, 31);
-        }
-    }
-}
-
-// ================================================================ kernel ==
-__global__ void __launch_bounds__(kThreads, 1) encode_kernel(EncArgs A)
-{
-    extern __shared__ __align__(16) unsigned char smem_raw[];
-    Smem& S = *reinterpret_cast<Smem*>(smem_raw);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-    if (warp >= kLoaders) {
-        // encoder warp: owns buffer b
-        const int b = warp - kLoaders;
-        Buf& B = S.buf[b];
-        __threadfence_block();
-        bar_arrive(kBarEmpty + b, kLoaderThreads + 32);
-        for (;;) {
-            bar_sync(kBarFull + b, kLoaderThreads + 32);
-            if (B.meta.k == kEnd) break;
-            encode_chunk(A, B, lane);
-            __syncwarp();
-            __threadfence_block();
-            bar_arrive(kBarEmpty + b, kLoaderThreads + 32);
-        }
-        return;
-    }
-
-    // loader warps.  Warp 0 stages each chunk's ticket, descriptor and
-    // pieces one iteration ahead, so they are in shared memory when the
-    // chunk's loads issue.
-    uint32_t ticket = 0;
-    if (threadIdx.x == 0) ticket = atomicAdd(&A.sc->ticket, 1u);
-    if (warp == 0) stage_next(A, S.next, lane, ticket);
-    bar_sync(kBarLoaders, kLoaderThreads);
-    for (int b = 0;; b = b + 1 == kEncoders ? 0 : b + 1) {
-        Buf& B = S.buf[b];
-        bar_sync(kBarEmpty + b, kLoaderThreads + 32);
-        if (warp == 0) {
-            if (lane == 0) {
-                B.meta.k = S.next.k;
-                B.meta.cd = S.next.cd;
-            }
-            const uint32_t ns = S.next.k == kEnd ? 0u
-                : (S.next.cd.src_count < uint32_t(kSegCache) ? S.next.cd.src_count : uint32_t(kSegCache));
-            for (uint32_t i = lane; i < ns; i += 32) B.meta.segs[i] = S.next.segs[i];
-        }
-        bar_sync(kBarLoaders, kLoaderThreads);
-        const uint32_t k = B.meta.k;
-        if (k == kEnd) {
-            // no chunk left: release every encoder warp, each once it is idle
-            __threadfence_block();
-            bar_arrive(kBarFull + b, kLoaderThreads + 32);
-            for (int d = 1; d < kEncoders; ++d) {
-                const int o = (b + d) % kEncoders;
-                bar_sync(kBarEmpty + o, kLoaderThreads + 32);
-                if (threadIdx.x == 0) S.buf[o].meta.k = kEnd;
-                __threadfence_block();
-                bar_arrive(kBarFull + o, kLoaderThreads + 32);
-            }
+    const MaskSrc S{B.ev, reinterpret_cast<const uint8_t*>(B.data)};
+    Parse P{-1, 0ull, 0, 0, 0u};
+    bool over = false;
+    int t = 0, keep = 0;
+    for (;;) {
+        int n;
+        t = list_events(B, t, keep, lane, &n);
+        const bool fin = t >= kSteps;
+        int g = 0;
+        for (; g + 32 <= n; g += 32) parse_group(S, g, 32, false, raw, P, body, body_len, true, lane, &over, bad);
+        if (fin) {
+            parse_group(S, g, n - g, true, raw, P, body, body_len, true, lane, &over, bad);
             break;
         }
-        const bool overwrite = (B.meta.cd.flags & kResidualFlag) || A.mode == DCR_MODE_OVERWRITE_ONLY;
-        // warp 0 stages the next chunk while this chunk's loads are in flight
-        load_slice(A, B, B.meta, overwrite, warp, lane, [&] {
-            if (warp == 0) stage_next(A, S.next, lane, ticket);
-        });
-        __threadfence_block();
-        bar_arrive(kBarFull + b, kLoaderThreads + 32);
+        const int rem = n - g;   // < 32, and g >= 32 since a batch stops only near kEvCap
+        const uint16_t x = lane < rem ? B.ev[g + lane] : uint16_t(0);
+        __syncwarp();
+        if (lane < rem) B.ev[lane] = x;
+        __syncwarp();
+        keep = rem;
+    }
+    if (over) *bad = true;
+    return P.out;
+}
+
+__global__ void __launch_bounds__(kSThreads, 2) spill_kernel(EncArgs A)
+{
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    Buf& B = *reinterpret_cast<Buf*>(smem_raw);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t n_spill = A.sc->n_spill;   // final: written by encode_kernel only
+    for (uint32_t s = blockIdx.x; s < n_spill; s += gridDim.x) {
+        const SpillRec R = A.spill[s];
+        const ChunkDesc cd = A.chunks[A.chunk_begin + R.k];
+        if (warp == 0) {
+            if (lane == 0) B.meta.cd = cd;
+            const uint32_t ns = cd.src_count < uint32_t(kSegCache) ? cd.src_count : uint32_t(kSegCache);
+            for (uint32_t i = lane; i < ns; i += 32) B.meta.segs[i] = A.src[cd.src_begin + i];
+        }
+        __syncthreads();
+        const bool overwrite = (cd.flags & kResidualFlag) || A.mode == DCR_MODE_OVERWRITE_ONLY;
+        load_slice(A, B, overwrite, warp, lane);
+        __syncthreads();
+        const int raw = int(cd.raw_len);
+        const uint8_t* bytes = reinterpret_cast<const uint8_t*>(B.data);
+        uint8_t* f = A.payload + R.foff;
+        uint8_t* body = f + kFrameHdr;
+        const uint32_t fsz = (kFrameHdr + R.body_len + 15) / 16 * 16;
+        if (R.kind == kXorRaw || R.kind == kOverwriteDense) {
+            const int nfull = raw >> 4;
+            for (int v = threadIdx.x; v < nfull; v += kSThreads) reinterpret_cast<uint4*>(body)[v] = B.data[v];
+            for (int x = (nfull << 4) + threadIdx.x; x < raw; x += kSThreads) body[x] = bytes[x];
+        } else if (warp == 0 && R.kind == kXorLz4) {
+            bool bad = false;
+            const uint32_t got = lz4_block(B, raw, body, R.body_len, lane, &bad);
+            if ((__any_sync(kFull, bad) || got != R.body_len) && lane == 0) report(A.sc, DCR_ERR_CORRUPT);
+        } else if (warp == 0) {
+            // overwrite records: count | unit offsets | pad to 4 | values
+            const uint32_t ub = cd.bits == 16 ? 2u : 1u;
+            const uint32_t nu = R.n_units;
+            const uint32_t pad = (4 - (2 * nu) % 4) % 4;
+            if (lane == 0) {
+                *reinterpret_cast<uint32_t*>(body) = nu;
+                for (uint32_t i = 0; i < pad; ++i) body[4 + 2 * nu + i] = 0;
+            }
+            uint8_t* offs = body + 4;
+            uint8_t* vals = body + 4 + 2 * nu + pad;
+            uint32_t base = 0;
+            for (int t = 0; t < kSteps; ++t) {
+                const int wi = 32 * t + lane;
+                uint32_t b = unit_bits(B.bits[wi], ub);
+                const uint32_t c = __popc(b);
+                const uint32_t incl = warp_incl_sum(c, lane);
+                uint32_t u_i = base + incl - c;
+                while (b) {
+                    const uint32_t x = uint32_t(wi * 32 + __ffs(b) - 1);
+                    b &= b - 1;
+                    const uint32_t u = x / ub;
+                    if (u_i < nu) {
+                        offs[2 * u_i] = uint8_t(u);
+                        offs[2 * u_i + 1] = uint8_t(u >> 8);
+                        for (uint32_t e = 0; e < ub; ++e) vals[u_i * ub + e] = bytes[x + e];
+                    }
+                    ++u_i;
+                }
+                base += __shfl_sync(kFull, incl, 31);
+            }
+            if (base != nu && lane == 0) report(A.sc, DCR_ERR_CORRUPT);
+        }
+        for (uint32_t x = kFrameHdr + R.body_len + threadIdx.x; x < fsz; x += kSThreads) f[x] = 0;
+        __syncthreads();
     }
 }
 
@@ -731,6 +884,8 @@ __global__ void finalize_kernel(EncArgs A, uint64_t plan_hash, uint64_t base_v, 
     }
 }
 
+constexpr size_t kMainSmem = sizeof(WarpSmem) * kMWarps;
+
 }  // namespace
 
 int encode_kernel_config(KernelConfig* kc)
@@ -739,12 +894,18 @@ int encode_kernel_config(KernelConfig* kc)
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&kc->num_sms, cudaDevAttrMultiProcessorCount, dev);
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(encode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sizeof(Smem)));
+        e = cudaFuncSetAttribute(encode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kMainSmem));
     if (e == cudaSuccess)
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&kc->enc_blocks_per_sm, encode_kernel, kThreads,
-                                                          sizeof(Smem));
+        e = cudaFuncSetAttribute(spill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sizeof(Buf)));
+    if (e == cudaSuccess)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&kc->enc_blocks_per_sm, encode_kernel, kMThreads,
+                                                          kMainSmem);
+    if (e == cudaSuccess)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&kc->spill_blocks_per_sm, spill_kernel, kSThreads,
+                                                          sizeof(Buf));
     if (e != cudaSuccess) return cuda_error(e, "encode kernel configuration");
-    if (kc->enc_blocks_per_sm < 1) return set_error(DCR_ERR_CUDA, "encode kernel does not fit on an SM");
+    if (kc->enc_blocks_per_sm < 1 || kc->spill_blocks_per_sm < 1)
+        return set_error(DCR_ERR_CUDA, "encode kernels do not fit on an SM");
     return DCR_OK;
 }
 
@@ -768,14 +929,17 @@ int encode_launch(const dcr_plan* P, uint32_t mode, uint32_t window, const void*
     A.counts = reinterpret_cast<unsigned long long*>(static_cast<char*>(P->d_enc) + sizeof(EncScratch));
     A.lb = P->d_lb;
     A.fsize = P->d_fsize;
+    A.spill = P->d_spill;
     size_t reset = reinterpret_cast<char*>(P->d_lb) - static_cast<char*>(P->d_enc) + A.chunk_count * 8ull;
     cudaError_t e = cudaMemsetAsync(P->d_enc, 0, reset, s);
     if (e != cudaSuccess) return cuda_error(e, "encode scratch reset");
+    const unsigned warps = unsigned(P->kc.num_sms * P->kc.enc_blocks_per_sm * kMWarps);
     unsigned grid = unsigned(P->kc.num_sms * P->kc.enc_blocks_per_sm);
-    if (grid > A.chunk_count) grid = A.chunk_count;
+    if (warps > A.chunk_count) grid = (A.chunk_count + kMWarps - 1) / kMWarps;
     if (P->profiling) cudaEventRecord(P->ev[0], s);
-    encode_kernel<<<grid, kThreads, sizeof(Smem), s>>>(A);
+    encode_kernel<<<grid, kMThreads, kMainSmem, s>>>(A);
     if (P->profiling) cudaEventRecord(P->ev[1], s);
+    spill_kernel<<<unsigned(P->kc.num_sms * P->kc.spill_blocks_per_sm), kSThreads, sizeof(Buf), s>>>(A);
     unsigned fgrid = (A.chunk_count + 255) / 256;
     if (fgrid > 1024) fgrid = 1024;
     finalize_kernel<<<fgrid, 256, 0, s>>>(A, P->hash, base_v, target_v, window);

@@ -356,10 +356,12 @@ extern "C" int dcr_plan_build(const dcr_tensor_desc* tensors, size_t n, const dc
         delete P;
         return rc;
     }
-    // encode scratch: head = EncScratch + per-tensor counts, then look-back + sizes
+    // encode scratch: head = EncScratch + per-tensor counts, then look-back,
+    // sizes and the spill list
     P->enc_head_bytes = (sizeof(EncScratch) + 8 * n + 255) / 256 * 256;
     size_t lb_bytes = (P->max_window_chunks * 8 + 255) / 256 * 256;
-    size_t total = P->enc_head_bytes + lb_bytes + P->max_window_chunks * 4 + 256;
+    size_t fs_bytes = (P->max_window_chunks * 4 + 255) / 256 * 256;
+    size_t total = P->enc_head_bytes + lb_bytes + fs_bytes + P->max_window_chunks * sizeof(SpillRec) + 256;
     if ((e = cudaMalloc(&P->d_enc, total)) != cudaSuccess ||
         (e = cudaMallocHost(&P->h_enc, P->enc_head_bytes)) != cudaSuccess) {
         plan_free_device(P);
@@ -368,6 +370,8 @@ extern "C" int dcr_plan_build(const dcr_tensor_desc* tensors, size_t n, const dc
     }
     P->d_lb = reinterpret_cast<uint64_t*>(static_cast<char*>(P->d_enc) + P->enc_head_bytes);
     P->d_fsize = reinterpret_cast<uint32_t*>(static_cast<char*>(P->d_enc) + P->enc_head_bytes + lb_bytes);
+    P->d_spill = reinterpret_cast<SpillRec*>(static_cast<char*>(P->d_enc) + P->enc_head_bytes + lb_bytes +
+                                             fs_bytes);
     if ((rc = encode_kernel_config(&P->kc)) || (rc = apply_kernel_config(&P->kc))) {
         plan_free_device(P);
         delete P;

@@ -237,8 +237,8 @@ int dcr_apply_retry(const dcr_plan* plan, dcr_recv_state* state, const void* pay
  * in milliseconds of that call's kernels (valid = 1 if measured).  The
  * record is per plan; off by default. */
 typedef struct {
-    float encode_ms;    /* gather + XOR + count + encode + frame write */
-    float finalize_ms;  /* frame index + stream header */
+    float encode_ms;    /* gather + XOR + count + encode + frame write (main kernel) */
+    float finalize_ms;  /* spilled (dense) chunk bodies, frame index, stream header */
     float apply_ms;     /* warp-per-frame decode and apply */
     float defer_ms;     /* general LZ4 frames */
     float pending_ms;   /* commit check */
