@@ -13,16 +13,22 @@
 // mask is remapped like the physical layout).
 //
 // Kernels:
-//   apply_kernel  one warp per frame.  XOR_RAW, OVERWRITE and OVERWRITE_DENSE
-//                 frames are applied lane-parallel.  LZ4 frames flagged ZSRC
-//                 (every match copies zero bytes, as the library's encoder
-//                 produces) are parsed by the warp in lock-step: only literal
-//                 bytes can be non-zero, so they are XORed straight into the
-//                 receiver arena and nothing is materialised; a bitmap of the
-//                 non-zero output bytes checks the ZSRC promise of every match.
+//   apply_kernel  one warp per frame, 20 warps per SM.  XOR_RAW, OVERWRITE
+//                 and OVERWRITE_DENSE frames are applied lane-parallel.  LZ4
+//                 frames flagged ZSRC (every match copies zero bytes, as the
+//                 library's encoder produces) have only literal bytes that can
+//                 be non-zero, so nothing is materialised: lane 0 walks the
+//                 tokens 32 sequences at a time, then the lanes XOR their
+//                 sequences' non-zero literal bytes straight into the receiver
+//                 arena and check every match against the sorted list of
+//                 non-zero output bytes so far.  A frame that fails part-way is
+//                 undone (XOR is self-inverse) before it is reported.
 //   defer_kernel  one CTA per remaining LZ4 frame (any valid block, e.g. from
-//                 the CPU oracle): full decode into a 64 KiB shared buffer with
-//                 warp-parallel literal and match copies, then the XOR sweep.
+//                 the CPU oracle, and ZSRC frames too large for the warp
+//                 path): full decode into a 64 KiB shared buffer with
+//                 warp-parallel literal and match copies (a ZSRC frame whose
+//                 match copies a non-zero byte is rejected), then the XOR
+//                 sweep.
 //   pending_kernel  counts framed chunks that are not DONE for the target
 //                 version (the commit rule).
 #include <cuda_runtime.h>
@@ -34,10 +40,11 @@
 namespace dcr {
 namespace {
 
-constexpr int kAThreads = 256;
-constexpr int kAWarps = kAThreads / 32;
+constexpr uint32_t kFull = 0xffffffffu;
+constexpr int kAWarps = 10;                 // warps per CTA, one frame each; 2 CTAs per SM
+constexpr int kAThreads = 32 * kAWarps;
 constexpr int kBodyCache = 6144;            // bytes of LZ4 body cached per warp
-constexpr int kBitWords = kChunk / 32;      // non-zero output bitmap per warp
+constexpr int kAEvCap = 2048;               // non-zero output bytes listed per frame
 constexpr int kDThreads = 256;
 constexpr uint32_t kCasLimit = 1u << 16;
 
@@ -64,9 +71,17 @@ struct Hdr {
     uint32_t window, flags, chunk_begin, chunk_count;
 };
 
+// one warp's shared memory: the frame body, the sorted positions of its
+// non-zero output bytes so far, and one batch of up to 32 sequences (literal
+// run in the body and the output, match source range [s, e))
+struct __align__(16) AWarp {
+    uint8_t body[kBodyCache];
+    uint16_t ev[kAEvCap];
+    uint32_t r_ip[32], r_op[32], r_ll[32], r_s[32], r_e[32];
+};
+
 struct __align__(16) ASmem {
-    uint32_t bits[kAWarps][kBitWords];
-    uint8_t body[kAWarps][kBodyCache + 16];
+    AWarp w[kAWarps];
     Hdr hdr;
     int ok;
 };
@@ -181,71 +196,6 @@ __device__ bool claim(unsigned long long* st, uint64_t V, bool* timeout)
     return false;
 }
 
-// ---- warp-level LZ4 (ZSRC) decode fused with the XOR --------------------
-// Returns true if the block is well formed and kept its ZSRC promise.
-__device__ bool zsrc_decode_once(const ApplyArgs& A, const ChunkDesc& cd, const Seg* ds,
-                                 const uint8_t* src, uint32_t n, uint32_t raw, uint32_t lim,
-                                 uint32_t* bits, int lane, uint32_t& runs)
-{
-    for (uint32_t w = lane; w < (raw + 31) / 32; w += 32) bits[w] = 0;
-    __syncwarp();
-    uint32_t ip = 0, op = 0;
-    for (;;) {
-        if (ip >= n) return false;
-        const uint32_t tok = src[ip++];
-        uint32_t ll = tok >> 4;
-        if (ll == 15) {
-            for (;;) {
-                if (ip >= n) return false;
-                uint32_t b = src[ip++];
-                ll += b;
-                if (b != 255) break;
-            }
-        }
-        if (ll > n - ip || ll > raw - op) return false;
-        for (uint32_t i = lane; i < ll; i += 32) {
-            uint32_t b = src[ip + i];
-            if (b) {
-                uint32_t x = op + i;
-                atomicOr(&bits[x >> 5], 1u << (x & 31));
-                if (x < lim) xor_byte(A.target, dst_of(ds, cd.dst_count, x), b);
-            }
-        }
-        __syncwarp();
-        ++runs;
-        ip += ll;
-        op += ll;
-        if (ip == n) break;
-        if (n - ip < 2) return false;
-        const uint32_t off = uint32_t(src[ip]) | (uint32_t(src[ip + 1]) << 8);
-        ip += 2;
-        if (off == 0 || off > op) return false;
-        uint32_t ml = tok & 15u;
-        if (ml == 15) {
-            for (;;) {
-                if (ip >= n) return false;
-                uint32_t b = src[ip++];
-                ml += b;
-                if (b != 255) break;
-            }
-        }
-        ml += 4;
-        if (ml > raw - op) return false;
-        // the copy source [op - off, op - off + min(ml, off)) must be all zero
-        const uint32_t s = op - off, e = s + (ml < off ? ml : off);
-        bool viol = false;
-        for (uint32_t w = (s >> 5) + lane; w <= ((e - 1) >> 5); w += 32) {
-            uint32_t a = (w << 5) > s ? 0u : s - (w << 5);
-            uint32_t b = ((w + 1) << 5) < e ? 32u : e - (w << 5);
-            uint32_t m = (b == 32 ? 0xFFFFFFFFu : ((1u << b) - 1)) & ~((1u << a) - 1);
-            viol |= (bits[w] & m) != 0;
-        }
-        if (__any_sync(0xffffffffu, viol)) return false;
-        op += ml;
-    }
-    return op == raw;
-}
-
 // XOR is its own inverse: re-applying the first `runs` literal runs of a frame
 // that failed part-way restores every byte the failed pass touched, so a
 // corrupt frame leaves its chunk exactly as it was (the overwrite-only retry
@@ -287,16 +237,137 @@ __device__ void zsrc_undo(const ApplyArgs& A, const ChunkDesc& cd, const Seg* ds
     }
 }
 
-// Decode a ZSRC frame, XOR-ing its literal bytes into the target as they are
-// parsed; on any error the partial apply is undone before returning false.
-__device__ bool zsrc_decode_apply(const ApplyArgs& A, const ChunkDesc& cd, const Seg* ds,
-                                  const uint8_t* src, uint32_t n, uint32_t raw, uint32_t lim,
-                                  uint32_t* bits, int lane)
+__device__ __forceinline__ uint32_t warp_incl_sum(uint32_t v, int lane)
 {
-    uint32_t runs = 0;
-    if (zsrc_decode_once(A, cd, ds, src, n, raw, lim, bits, lane, runs)) return true;
-    if (runs) zsrc_undo(A, cd, ds, src, lim, runs, lane);
-    return false;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        uint32_t o = __shfl_up_sync(kFull, v, d);
+        if (lane >= d) v += o;
+    }
+    return v;
+}
+
+// ---- ZSRC frames: serial token walk, parallel apply ---------------------
+// Lane 0 walks up to 32 sequences per batch into records.  Then each lane
+// XORs the non-zero literal bytes of its record into the receiver, lists
+// their positions (the warp's list of non-zero output bytes stays sorted,
+// since literal runs come in output order), and checks that its match copies
+// zero bytes only: no listed position falls in the match's source range.
+// Returns 1 if the frame was applied, 0 if it is malformed or breaks its
+// ZSRC promise, 2 if it holds more non-zero bytes than the list (the caller
+// defers it); in the last two cases the partial apply has been undone.
+__device__ int zsrc_apply(const ApplyArgs& A, const ChunkDesc& cd, const Seg* ds, const uint8_t* src,
+                          uint32_t n, uint32_t raw, uint32_t lim, AWarp& W, int lane)
+{
+    uint32_t ip = 0, op = 0;      // lane 0's walk
+    uint32_t nev = 0, runs = 0;   // listed positions, literal runs applied
+    int status = 1;
+    for (;;) {
+        uint32_t nrec = 0, fin = 0, bad = 0;
+        if (lane == 0) {
+            for (; nrec < 32; ++nrec) {
+                if (ip >= n) { bad = 1; break; }
+                const uint32_t tok = src[ip++];
+                uint32_t ll = tok >> 4;
+                if (ll == 15) {
+                    uint32_t b;
+                    do {
+                        if (ip >= n) { bad = 1; break; }
+                        b = src[ip++];
+                        ll += b;
+                    } while (b == 255);
+                    if (bad) break;
+                }
+                if (ll > n - ip || ll > raw - op) { bad = 1; break; }
+                W.r_ip[nrec] = ip;
+                W.r_op[nrec] = op;
+                W.r_ll[nrec] = ll;
+                ip += ll;
+                op += ll;
+                if (ip == n) {   // last sequence: literals only
+                    W.r_s[nrec] = W.r_e[nrec] = 0;
+                    ++nrec;
+                    fin = 1;
+                    if (op != raw) bad = 1;
+                    break;
+                }
+                if (n - ip < 2) { bad = 1; break; }
+                const uint32_t off = uint32_t(src[ip]) | (uint32_t(src[ip + 1]) << 8);
+                ip += 2;
+                if (off == 0 || off > op) { bad = 1; break; }
+                uint32_t ml = tok & 15u;
+                if (ml == 15) {
+                    uint32_t b;
+                    do {
+                        if (ip >= n) { bad = 1; break; }
+                        b = src[ip++];
+                        ml += b;
+                    } while (b == 255);
+                    if (bad) break;
+                }
+                ml += 4;
+                if (ml > raw - op) { bad = 1; break; }
+                // bytes copied: [op - off, op - off + min(ml, off)), repeated
+                W.r_s[nrec] = op - off;
+                W.r_e[nrec] = op - off + (ml < off ? ml : off);
+                op += ml;
+            }
+        }
+        nrec = __shfl_sync(kFull, nrec, 0);
+        fin = __shfl_sync(kFull, fin, 0);
+        bad = __shfl_sync(kFull, bad, 0);
+        if (bad) {
+            status = 0;
+            break;
+        }
+        __syncwarp();
+        uint32_t ipl = 0, opl = 0, ll = 0, c = 0;
+        if (lane < int(nrec)) {
+            ipl = W.r_ip[lane];
+            opl = W.r_op[lane];
+            ll = W.r_ll[lane];
+            for (uint32_t q = 0; q < ll; ++q) c += src[ipl + q] != 0;
+        }
+        const uint32_t incl = warp_incl_sum(c, lane);
+        const uint32_t tot = __shfl_sync(kFull, incl, 31);
+        if (nev + tot > uint32_t(kAEvCap)) {
+            status = 2;
+            break;
+        }
+        uint32_t at = nev + incl - c;
+        for (uint32_t q = 0; q < ll; ++q) {
+            const uint32_t b = src[ipl + q];
+            if (b) {
+                const uint32_t x = opl + q;
+                W.ev[at++] = uint16_t(x);
+                if (x < lim) xor_byte(A.target, dst_of(ds, cd.dst_count, x), b);
+            }
+        }
+        nev += tot;
+        runs += nrec;
+        __syncwarp();
+        bool viol = false;
+        if (lane < int(nrec)) {
+            const uint32_t s0 = W.r_s[lane], e0 = W.r_e[lane];
+            if (e0 > s0) {
+                uint32_t lo = 0, hi = nev;   // first listed position >= s0
+                while (lo < hi) {
+                    const uint32_t mid = (lo + hi) >> 1;
+                    if (W.ev[mid] < s0) lo = mid + 1;
+                    else hi = mid;
+                }
+                viol = lo < nev && W.ev[lo] < e0;
+            }
+        }
+        if (__any_sync(kFull, viol)) {
+            status = 0;
+            break;
+        }
+        if (fin) break;
+        __syncwarp();   // lane 0 rewrites the records
+    }
+    if (status != 1 && runs) zsrc_undo(A, cd, ds, src, lim, runs, lane);
+    return status;
 }
 
 // ================================================================ kernels ==
@@ -320,8 +391,7 @@ __global__ void __launch_bounds__(kAThreads) apply_kernel(ApplyArgs A)
     if (!S.ok) return;
     const Hdr H = S.hdr;
     const uint64_t V = H.target_v;
-    uint32_t* bits = S.bits[wid];
-    uint8_t* cache = S.body[wid];
+    AWarp& W = S.w[wid];
 
     for (;;) {
         uint32_t f = 0;
@@ -366,7 +436,9 @@ __global__ void __launch_bounds__(kAThreads) apply_kernel(ApplyArgs A)
                 if (!got && !to) atomicAdd(&A.sc->skipped, 1ull);
             }
             if (!__shfl_sync(0xffffffffu, got, 0)) continue;
-            if (kind == kXorLz4 && !(fflags & kFrameZsrc)) {
+            // general LZ4 frames, and ZSRC frames larger than the body cache,
+            // go to the full decode
+            if (kind == kXorLz4 && (!(fflags & kFrameZsrc) || bl > uint32_t(kBodyCache))) {
                 if (lane == 0) A.defer[atomicAdd(&A.sc->n_defer, 1u)] = f;
                 continue;
             }
@@ -385,15 +457,17 @@ __global__ void __launch_bounds__(kAThreads) apply_kernel(ApplyArgs A)
                     if (body[x] && x < lim) xor_byte(A.target, dst_of(ds, cd.dst_count, x), body[x]);
             }
         } else if (kind == kXorLz4) {
-            const uint8_t* src = body;
-            if (bl <= uint32_t(kBodyCache)) {
-                for (uint32_t v = lane; v < bl / 16; v += 32)
-                    reinterpret_cast<uint4*>(cache)[v] = ld_nc16(body + 16 * v);
-                for (uint32_t x = (bl & ~15u) + lane; x < bl; x += 32) cache[x] = body[x];
-                __syncwarp();
-                src = cache;
+            for (uint32_t v = lane; v < bl / 16; v += 32)
+                reinterpret_cast<uint4*>(W.body)[v] = ld_nc16(body + 16 * v);
+            for (uint32_t x = (bl & ~15u) + lane; x < bl; x += 32) W.body[x] = body[x];
+            __syncwarp();
+            const int r = zsrc_apply(A, cd, ds, W.body, bl, raw, lim, W, lane);
+            __syncwarp();   // the body cache is reused by the next frame
+            if (r == 2) {
+                if (lane == 0) A.defer[atomicAdd(&A.sc->n_defer, 1u)] = f;
+                continue;
             }
-            good = zsrc_decode_apply(A, cd, ds, src, bl, raw, lim, bits, lane);
+            good = r == 1;
         } else if (kind == kOverwriteDense) {
             good = bl == raw;
             if (good) {
@@ -471,6 +545,7 @@ __global__ void __launch_bounds__(kDThreads) defer_kernel(ApplyArgs A)
         const uint64_t fo = ld64(p + idx_off + 8ull * f);
         const uint4 h0 = ld_nc16(p + fo), h1 = ld_nc16(p + fo + 16);
         const uint32_t c = h0.z, raw = h0.w, n = h1.x;
+        const bool zs = ((h0.y >> 16) & kFrameZsrc) != 0;   // matches must copy zeros
         const ChunkDesc cd = A.chunks[c];
         const bool cut = uint64_t(f) == A.abort_at;
         const uint32_t ub = cd.bits == 16 ? 2u : 1u;
@@ -515,8 +590,13 @@ __global__ void __launch_bounds__(kDThreads) defer_kernel(ApplyArgs A)
                 ml += 4;
                 if (!ok || ml > raw - op) break;
                 // forward copy semantics: the output repeats with period off
-                for (uint32_t i = lane; i < ml; i += 32) out[op + i] = out[op - off + (i % off)];
-                __syncwarp();
+                bool viol = false;
+                for (uint32_t i = lane; i < ml; i += 32) {
+                    const uint8_t b = out[op - off + (i % off)];
+                    out[op + i] = b;
+                    viol |= b != 0;
+                }
+                if (__any_sync(kFull, zs && viol)) break;
                 op += ml;
             }
             if (lane == 0) s_good = good;
