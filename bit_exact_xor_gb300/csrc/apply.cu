@@ -71,13 +71,18 @@ struct Hdr {
     uint32_t window, flags, chunk_begin, chunk_count;
 };
 
+constexpr uint32_t kWin = 128;                // candidate sequence starts per walk window
+constexpr uint32_t kEndFinal = 0x80000000u;   // the sequence is the block's last
+constexpr uint32_t kEndBad = 0x7FFFFFFFu;     // no valid sequence starts here
+
 // one warp's shared memory: the frame body, the sorted positions of its
-// non-zero output bytes so far, and one batch of up to 32 sequences (literal
-// run in the body and the output, match source range [s, e))
+// non-zero output bytes so far, where a sequence starting at each byte of the
+// current window would end, and the starts of one batch of sequences
 struct __align__(16) AWarp {
     uint8_t body[kBodyCache];
     uint16_t ev[kAEvCap];
-    uint32_t r_ip[32], r_op[32], r_ll[32], r_s[32], r_e[32];
+    uint32_t nxt[kWin];
+    uint32_t r_ip[32];
 };
 
 struct __align__(16) ASmem {
@@ -145,10 +150,13 @@ __device__ __forceinline__ uint64_t dst_of(const Seg* s, uint32_t n, uint32_t x)
     return s[lo].addr + (x - s[lo].off);
 }
 
+// XOR one byte into the receiver: a fire-and-forget reduction on its 32-bit
+// word (neighbouring bytes may belong to other frames' chunks)
 __device__ __forceinline__ void xor_byte(uint8_t* target, uint64_t a, uint32_t b)
 {
-    uintptr_t p = reinterpret_cast<uintptr_t>(target + a);
-    atomicXor(reinterpret_cast<unsigned*>(p & ~uintptr_t(3)), b << (8 * (p & 3)));
+    const uintptr_t p = reinterpret_cast<uintptr_t>(target + a);
+    asm volatile("red.global.xor.b32 [%0], %1;" ::"l"(p & ~uintptr_t(3)), "r"(b << (8 * (p & 3)))
+                 : "memory");
 }
 
 // XOR one 16-byte mask vector at canonical chunk offset x (bytes >= lim skipped)
@@ -247,87 +255,134 @@ __device__ __forceinline__ uint32_t warp_incl_sum(uint32_t v, int lane)
     return v;
 }
 
-// ---- ZSRC frames: serial token walk, parallel apply ---------------------
-// Lane 0 walks up to 32 sequences per batch into records.  Then each lane
-// XORs the non-zero literal bytes of its record into the receiver, lists
-// their positions (the warp's list of non-zero output bytes stays sorted,
-// since literal runs come in output order), and checks that its match copies
-// zero bytes only: no listed position falls in the match's source range.
-// Returns 1 if the frame was applied, 0 if it is malformed or breaks its
-// ZSRC promise, 2 if it holds more non-zero bytes than the list (the caller
-// defers it); in the last two cases the partial apply has been undone.
+// ---- ZSRC frames: chained walk, parallel apply ---------------------------
+// End of the sequence starting at body byte p (where the next one starts),
+// | kEndFinal for a literals-only last sequence, or kEndBad.
+__device__ __forceinline__ uint32_t seq_end(const uint8_t* src, uint32_t n, uint32_t p)
+{
+    if (p >= n) return kEndBad;
+    const uint32_t tok = src[p];
+    uint32_t q = p + 1, ll = tok >> 4;
+    if (ll == 15) {
+        uint32_t b;
+        do {
+            if (q >= n) return kEndBad;
+            b = src[q++];
+            ll += b;
+        } while (b == 255);
+    }
+    if (ll > n - q) return kEndBad;
+    q += ll;
+    if (q == n) return q | kEndFinal;
+    if (n - q < 2) return kEndBad;
+    q += 2;
+    if ((tok & 15u) == 15u) {
+        uint32_t b;
+        do {
+            if (q >= n) return kEndBad;
+            b = src[q++];
+        } while (b == 255);
+    }
+    return q;
+}
+
+// The warp takes the block a window of kWin body bytes at a time: every lane
+// works out where a sequence starting at each of its window bytes would end,
+// lane 0 follows the chain of ends from the current sequence (one shared
+// load per sequence), and up to 32 sequences found that way are decoded one
+// per lane, their output positions given by a warp prefix sum.  Then each
+// lane XORs the non-zero literal bytes of its sequence into the receiver,
+// lists their positions (the warp's list of non-zero output bytes stays
+// sorted, since literal runs come in output order), and checks that its
+// match copies zero bytes only: no listed position falls in the match's
+// source range.  Returns 1 if the frame was applied, 0 if it is malformed or
+// breaks its ZSRC promise, 2 if it holds more non-zero bytes than the list
+// (the caller defers it); in the last two cases the partial apply has been
+// undone.
 __device__ int zsrc_apply(const ApplyArgs& A, const ChunkDesc& cd, const Seg* ds, const uint8_t* src,
                           uint32_t n, uint32_t raw, uint32_t lim, AWarp& W, int lane)
 {
-    uint32_t ip = 0, op = 0;      // lane 0's walk
+    const bool one = cd.dst_count == 1;
+    const uint64_t base = one ? ds[0].addr - ds[0].off : 0ull;   // single receiver piece
+    uint32_t ip = 0, op = 0;      // next sequence in the body; its output position
     uint32_t nev = 0, runs = 0;   // listed positions, literal runs applied
     int status = 1;
     for (;;) {
-        uint32_t nrec = 0, fin = 0, bad = 0;
+        uint32_t e[kWin / 32];
+#pragma unroll
+        for (uint32_t j = 0; j < kWin / 32; ++j) e[j] = seq_end(src, n, ip + 32 * j + lane);
+#pragma unroll
+        for (uint32_t j = 0; j < kWin / 32; ++j) W.nxt[32 * j + lane] = e[j];
+        __syncwarp();
+        uint32_t cnt = 0, fin = 0, bad = 0, cur = ip;
         if (lane == 0) {
-            for (; nrec < 32; ++nrec) {
-                if (ip >= n) { bad = 1; break; }
-                const uint32_t tok = src[ip++];
-                uint32_t ll = tok >> 4;
-                if (ll == 15) {
-                    uint32_t b;
-                    do {
-                        if (ip >= n) { bad = 1; break; }
-                        b = src[ip++];
-                        ll += b;
-                    } while (b == 255);
-                    if (bad) break;
-                }
-                if (ll > n - ip || ll > raw - op) { bad = 1; break; }
-                W.r_ip[nrec] = ip;
-                W.r_op[nrec] = op;
-                W.r_ll[nrec] = ll;
-                ip += ll;
-                op += ll;
-                if (ip == n) {   // last sequence: literals only
-                    W.r_s[nrec] = W.r_e[nrec] = 0;
-                    ++nrec;
-                    fin = 1;
-                    if (op != raw) bad = 1;
-                    break;
-                }
-                if (n - ip < 2) { bad = 1; break; }
-                const uint32_t off = uint32_t(src[ip]) | (uint32_t(src[ip + 1]) << 8);
-                ip += 2;
-                if (off == 0 || off > op) { bad = 1; break; }
-                uint32_t ml = tok & 15u;
-                if (ml == 15) {
-                    uint32_t b;
-                    do {
-                        if (ip >= n) { bad = 1; break; }
-                        b = src[ip++];
-                        ml += b;
-                    } while (b == 255);
-                    if (bad) break;
-                }
-                ml += 4;
-                if (ml > raw - op) { bad = 1; break; }
-                // bytes copied: [op - off, op - off + min(ml, off)), repeated
-                W.r_s[nrec] = op - off;
-                W.r_e[nrec] = op - off + (ml < off ? ml : off);
-                op += ml;
+            while (cnt < 32 && cur < ip + kWin) {
+                const uint32_t x = W.nxt[cur - ip];
+                if (x == kEndBad) { bad = 1; break; }
+                W.r_ip[cnt++] = cur;
+                cur = x & ~kEndFinal;
+                if (x & kEndFinal) { fin = 1; break; }
+                if (cur >= n) { bad = 1; break; }   // a block ends with a literals-only sequence
             }
         }
-        nrec = __shfl_sync(kFull, nrec, 0);
+        cnt = __shfl_sync(kFull, cnt, 0);
         fin = __shfl_sync(kFull, fin, 0);
         bad = __shfl_sync(kFull, bad, 0);
+        cur = __shfl_sync(kFull, cur, 0);
         if (bad) {
             status = 0;
             break;
         }
         __syncwarp();
-        uint32_t ipl = 0, opl = 0, ll = 0, c = 0;
-        if (lane < int(nrec)) {
-            ipl = W.r_ip[lane];
-            opl = W.r_op[lane];
-            ll = W.r_ll[lane];
-            for (uint32_t q = 0; q < ll; ++q) c += src[ipl + q] != 0;
+        // one sequence per lane (its bytes were bounds-checked by seq_end)
+        const bool mine = lane < int(cnt);
+        const bool lastseq = fin && lane == int(cnt) - 1;
+        uint32_t ipl = 0, ll = 0, off = 0, ml = 0;
+        if (mine) {
+            uint32_t q = W.r_ip[lane];
+            const uint32_t tok = src[q++];
+            ll = tok >> 4;
+            if (ll == 15) {
+                uint32_t b;
+                do {
+                    b = src[q++];
+                    ll += b;
+                } while (b == 255);
+            }
+            ipl = q;
+            q += ll;
+            if (!lastseq) {
+                off = uint32_t(src[q]) | (uint32_t(src[q + 1]) << 8);
+                q += 2;
+                ml = tok & 15u;
+                if (ml == 15) {
+                    uint32_t b;
+                    do {
+                        b = src[q++];
+                        ml += b;
+                    } while (b == 255);
+                }
+                ml += 4;
+            }
         }
+        const uint32_t len = ll + ml;
+        const uint32_t lincl = warp_incl_sum(len, lane);
+        const uint32_t opl = op + lincl - len;   // output position of the literals
+        const uint32_t mop = opl + ll;           // ... and of the match
+        bool wrong = false;
+        if (mine) {
+            if (lastseq) wrong = opl > raw || ll != raw - opl;
+            else wrong = opl > raw || ll > raw - opl || off == 0 || off > mop || ml > raw - mop;
+        }
+        if (__any_sync(kFull, wrong)) {
+            status = 0;
+            break;
+        }
+        op += __shfl_sync(kFull, lincl, 31);
+        ip = cur;
+        // literals: XOR into the receiver and list the non-zero ones
+        uint32_t c = 0;
+        for (uint32_t q = 0; q < ll; ++q) c += src[ipl + q] != 0;
         const uint32_t incl = warp_incl_sum(c, lane);
         const uint32_t tot = __shfl_sync(kFull, incl, 31);
         if (nev + tot > uint32_t(kAEvCap)) {
@@ -340,31 +395,30 @@ __device__ int zsrc_apply(const ApplyArgs& A, const ChunkDesc& cd, const Seg* ds
             if (b) {
                 const uint32_t x = opl + q;
                 W.ev[at++] = uint16_t(x);
-                if (x < lim) xor_byte(A.target, dst_of(ds, cd.dst_count, x), b);
+                if (x < lim) xor_byte(A.target, one ? base + x : dst_of(ds, cd.dst_count, x), b);
             }
         }
         nev += tot;
-        runs += nrec;
+        runs += cnt;
         __syncwarp();
+        // the match copies [mop - off, mop - off + min(ml, off)), repeated
         bool viol = false;
-        if (lane < int(nrec)) {
-            const uint32_t s0 = W.r_s[lane], e0 = W.r_e[lane];
-            if (e0 > s0) {
-                uint32_t lo = 0, hi = nev;   // first listed position >= s0
-                while (lo < hi) {
-                    const uint32_t mid = (lo + hi) >> 1;
-                    if (W.ev[mid] < s0) lo = mid + 1;
-                    else hi = mid;
-                }
-                viol = lo < nev && W.ev[lo] < e0;
+        if (mine && !lastseq) {
+            const uint32_t s0 = mop - off, e0 = s0 + (ml < off ? ml : off);
+            uint32_t lo = 0, hi = nev;   // first listed position >= s0
+            while (lo < hi) {
+                const uint32_t mid = (lo + hi) >> 1;
+                if (W.ev[mid] < s0) lo = mid + 1;
+                else hi = mid;
             }
+            viol = lo < nev && W.ev[lo] < e0;
         }
         if (__any_sync(kFull, viol)) {
             status = 0;
             break;
         }
         if (fin) break;
-        __syncwarp();   // lane 0 rewrites the records
+        __syncwarp();   // the window and the batch are rewritten
     }
     if (status != 1 && runs) zsrc_undo(A, cd, ds, src, lim, runs, lane);
     return status;
