@@ -13,7 +13,7 @@
 // mask is remapped like the physical layout).
 //
 // Kernels:
-//   apply_kernel  one warp per frame, 20 warps per SM.  XOR_RAW, OVERWRITE
+//   apply_kernel  one warp per frame, 32 warps per SM.  XOR_RAW, OVERWRITE
 //                 and OVERWRITE_DENSE frames are applied lane-parallel.  LZ4
 //                 frames flagged ZSRC (every match copies zero bytes, as the
 //                 library's encoder produces) have only literal bytes that can
@@ -41,10 +41,10 @@ namespace dcr {
 namespace {
 
 constexpr uint32_t kFull = 0xffffffffu;
-constexpr int kAWarps = 10;                 // warps per CTA, one frame each; 2 CTAs per SM
+constexpr int kAWarps = 16;                 // warps per CTA, one frame each; 2 CTAs per SM
 constexpr int kAThreads = 32 * kAWarps;
-constexpr int kBodyCache = 6144;            // bytes of LZ4 body cached per warp
-constexpr int kAEvCap = 2048;               // non-zero output bytes listed per frame
+constexpr int kBodyCache = 3072;            // bytes of LZ4 body cached per warp
+constexpr int kAEvCap = 1024;               // non-zero output bytes listed per frame
 constexpr int kDThreads = 256;
 constexpr uint32_t kCasLimit = 1u << 16;
 

@@ -70,15 +70,21 @@ struct EncScratch {
     uint32_t pad;
 };
 
-// A chunk whose frame is placed and sized but whose body did not fit the
-// encoder warp's staging buffer: the spill kernel re-derives and writes it.
+// The encoder writes each chunk's frame into a slot of its own in device
+// scratch (kEncSlot bytes per chunk of the window); a compaction pass copies
+// the slots into the stream once the frame offsets are known.
+constexpr uint32_t kEncSlot = 6144;
+constexpr uint32_t kSpilled = 1u << 31;   // frame-size flag: body not in the slot
+
+// A chunk whose frame is sized but whose body did not fit its slot: the
+// spill kernel re-derives it and writes the frame into the stream.
 struct SpillRec {
     uint32_t k;          // window-relative chunk
     uint32_t kind;       // FrameKind
     uint32_t body_len;
     uint32_t n_units;    // overwrite records: unit count
-    uint64_t foff;       // frame offset in the stream
-    uint64_t pad;
+    uint32_t changed;    // changed stored values (frame header)
+    uint32_t pad[3];
 };
 
 // Device scratch of one apply call (reset by a memset per call).
@@ -160,6 +166,7 @@ struct dcr_plan {
     uint64_t* d_lb = nullptr;
     uint32_t* d_fsize = nullptr;
     dcr::SpillRec* d_spill = nullptr;  // max_window_chunks
+    uint8_t* d_slots = nullptr;        // max_window_chunks * kEncSlot frame slots
     void* h_enc = nullptr;  // pinned mirror of the scratch head
     // kernel timing (dcr_plan_set_profiling)
     bool profiling = false;

@@ -16,24 +16,28 @@
 // "Residual Conversion" and "Hybrid encoding and compression" (XOR masks for
 // affine changes, overwrites for residual ones).
 //
-// encode_kernel.  One warp per chunk, chunks taken in ticket order, 20 warps
-// per SM.  The warp streams its chunk in 2 KiB steps (four 16-byte loads of
-// old and new per lane), XORs and counts, and appends the positions and
-// values of the non-zero mask bytes ("events") to a ring in shared memory.
-// Every 32 events it runs one parse group (one event per lane, connected by
-// ballots and warp sums) that writes the LZ4 sequences into a 6 KiB staging
-// buffer.  Overwrite chunks stage their records instead.  When the stream
-// end is reached the warp publishes the frame size, looks back for its
-// offset and copies the staged body out with 16-byte stores.  A chunk whose
-// body or pending literals outgrow the staging buffer or the ring is sized
-// all the same (the parse carries on without writing) and is listed for the
-// spill kernel.
+// encode_kernel.  One warp per chunk, chunks taken in ticket order, 18 warps
+// per SM.  The warp streams its chunk in 1 KiB steps: cp.async copies old
+// and new into a four-stage landing buffer in shared memory, so three steps
+// are in flight while one is processed.  It XORs and counts, and appends the
+// positions and values of the non-zero mask bytes ("events") to a ring in
+// shared memory.  Every 32 events it runs one parse group (one event per
+// lane, connected by ballots and warp sums) that writes the LZ4 sequences
+// straight into the chunk's frame slot in device scratch.  Overwrite chunks
+// write their records there instead.  A chunk whose body or pending literals
+// outgrow the slot or the ring is sized all the same (the parse carries on
+// without writing) and is listed for the spill kernel.  No warp waits for
+// another: frame sizes go to a per-chunk array.
+//
+// scan_kernel / copy_kernel.  One CTA scans the frame sizes into offsets
+// and writes the stream header; then one warp per chunk copies its slot to
+// its place in the stream with 16-byte stores and writes its index entry.
 //
 // spill_kernel.  One CTA per listed chunk: 16 warps gather the mask into
 // shared memory (64 KiB plus a bitmap of its non-zero bytes), then one warp
 // re-runs the same parse over the bitmap's event list, reading literal bytes
-// from the mask, and writes the body at the place the encoder reserved; raw
-// and dense frames are copied by the whole CTA.  Both kernels call the same
+// from the mask, and writes the frame at its place in the stream; raw and
+// dense frames are copied by the whole CTA.  Both kernels call the same
 // parse_group with groups of 32 consecutive events from the first one, so
 // their sizes agree by construction (a disagreement is reported).
 //
@@ -47,6 +51,7 @@
 #include <cuda_runtime.h>
 
 #include <climits>
+#include <cstddef>
 #include <cstdint>
 
 #include "dcr_internal.h"
@@ -56,13 +61,14 @@ namespace {
 
 constexpr uint32_t kFull = 0xffffffffu;
 // encode_kernel
-constexpr int kMWarps = 10;                       // warps per CTA, one chunk each
+constexpr int kMWarps = 9;                        // warps per CTA, one chunk each; 2 CTAs per SM
 constexpr int kMThreads = 32 * kMWarps;
 constexpr int kRing = 1024;                       // event ring entries per warp (power of two)
-constexpr int kStage = 6144;                      // staged frame body bytes per warp
-constexpr int kMVPL = 4;                          // 16-byte vectors per lane per step
-constexpr int kStepVec = 32 * kMVPL;              // 2 KiB per step
+constexpr int kMVPL = 2;                          // 16-byte vectors per lane per step
+constexpr int kStepVec = 32 * kMVPL;              // 1 KiB per step
+constexpr int kNS = 4;                            // landing stages: kNS - 1 steps in flight
 constexpr int kMSegCache = 64;                    // sender pieces cached per warp
+constexpr uint32_t kSlotBody = kEncSlot - kFrameHdr;   // frame body bytes a slot holds
 // spill_kernel
 constexpr int kSWarps = 16;                       // each gathers one 4 KiB slice
 constexpr int kSThreads = 32 * kSWarps;
@@ -73,7 +79,6 @@ constexpr int kWords = kChunk / 32;               // bitmap words per chunk
 constexpr int kSteps = kWords / 32;               // 64 warp steps over the bitmap
 constexpr int kEvCap = 6144;                      // events listed per batch
 constexpr int kSegCache = 64;
-constexpr uint32_t kSpinLimit = 1u << 22;         // bounded look-back wait
 
 struct EncArgs {
     const ChunkDesc* chunks;
@@ -86,18 +91,25 @@ struct EncArgs {
     uint64_t cap;
     EncScratch* sc;
     unsigned long long* counts;
-    uint64_t* lb;
-    uint32_t* fsize;
+    uint64_t* lb;              // frame offsets: frames before << 40 | bytes before
+    uint32_t* fsize;           // frame size (| kSpilled), 0: no frame
     SpillRec* spill;
+    uint8_t* slots;            // kEncSlot bytes per chunk
 };
 
 // encode_kernel: one warp's shared memory
 struct __align__(16) WarpSmem {
-    uint8_t stage[kStage];             // LZ4 body, or unit offsets then values
+    uint4 land[kNS][2][kStepVec];      // landing stages: old, new; lane's vectors at j * 32 + lane
     uint16_t pos[kRing];               // event ring: byte position in the chunk
     uint8_t val[kRing];                //             mask byte
     Seg segs[kMSegCache];              // the chunk's sender pieces
 };
+// overwrite chunks keep their record values in the ring's storage
+constexpr int kValStage = int(sizeof(uint16_t) + sizeof(uint8_t)) * kRing;
+static_assert(offsetof(WarpSmem, val) == offsetof(WarpSmem, pos) + sizeof(uint16_t) * kRing,
+              "ring storage is contiguous");
+static_assert(2 * ((kSlotBody - 8) / 4) <= uint32_t(kValStage) && (kSlotBody - 8) / 3 <= uint32_t(kValStage),
+              "the values of the records a slot holds fit the ring's storage");
 
 // spill_kernel: one chunk in shared memory
 struct __align__(16) Meta {
@@ -123,16 +135,18 @@ __device__ __forceinline__ uint4 ld_stream(const void* p)
     return v;
 }
 
-__device__ __forceinline__ void st_release(uint64_t* p, uint64_t v)
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem)
 {
-    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+    const uint32_t sa = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(gmem) : "memory");
 }
 
-__device__ __forceinline__ uint64_t ld_acquire(const uint64_t* p)
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+
+template <int N>
+__device__ __forceinline__ void cp_async_wait()
 {
-    uint64_t v;
-    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-    return v;
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 __device__ __forceinline__ uint4 xor4(uint4 a, uint4 b)
@@ -379,55 +393,6 @@ __device__ __forceinline__ void parse_group(const Src& S, int e0, int cnt, bool 
     P.out += gsum;
 }
 
-// ------------------------------------------------------------- look-back --
-// Publish this chunk's frame size and find its offset: the warp reads 32
-// predecessors per round trip, newest first, and sums them up to the nearest
-// one that already holds an inclusive prefix.  False after a bounded wait.
-__device__ __forceinline__ bool look_back(const EncArgs& A, uint32_t k, uint32_t fsz, int lane, uint64_t* out)
-{
-    uint64_t excl = 0;
-    int ok = 1;
-    const uint64_t agg = fsz ? ((1ull << kLbFrameShift) | fsz) : 0ull;
-    if (lane == 0) {
-        A.fsize[k] = fsz;
-        st_release(&A.lb[k], (k == 0 ? kLbInc : kLbAgg) | agg);
-    }
-    if (k > 0) {
-        for (int64_t j = int64_t(k) - 1;; j -= 32) {
-            const int64_t idx = j - lane;
-            uint64_t v = 0;
-            uint32_t spins = 0;
-            for (;;) {
-                v = idx >= 0 ? ld_acquire(&A.lb[idx]) : kLbInc;   // before chunk 0: prefix 0
-                const uint32_t inc = __ballot_sync(kFull, (v >> 62) == 2);
-                const uint32_t upto = inc ? (2u << (__ffs(inc) - 1)) - 1u : kFull;
-                const uint32_t missing = __ballot_sync(kFull, (v >> 62) == 0) & upto;
-                if (!missing) break;
-                const bool quit = ++spins > kSpinLimit || *(volatile int32_t*)&A.sc->err != 0;
-                if (__any_sync(kFull, quit)) {   // warp-uniform exit
-                    ok = 0;
-                    break;
-                }
-                __nanosleep(64);
-            }
-            if (!ok) break;
-            const uint32_t inc = __ballot_sync(kFull, (v >> 62) == 2);
-            const uint32_t upto = inc ? (2u << (__ffs(inc) - 1)) - 1u : kFull;
-            uint64_t part = ((upto >> lane) & 1u) ? (v & kLbValMask) : 0ull;
-#pragma unroll
-            for (int d = 16; d > 0; d >>= 1) part += __shfl_xor_sync(kFull, part, d);
-            excl += part;
-            if (inc) break;
-        }
-        if (lane == 0) {
-            if (ok) st_release(&A.lb[k], kLbInc | (excl + agg));
-            else report(A.sc, DCR_ERR_TIMEOUT);
-        }
-    }
-    *out = excl;
-    return ok != 0;
-}
-
 __device__ __forceinline__ void write_header(uint8_t* f, uint32_t kind, uint32_t bits, uint32_t chunk,
                                              uint32_t raw, uint32_t body_len, uint32_t chg)
 {
@@ -472,49 +437,80 @@ __device__ __forceinline__ void encode_chunk(const EncArgs& A, WarpSmem& W, uint
     const bool overwrite = (cd.flags & kResidualFlag) || A.mode == DCR_MODE_OVERWRITE_ONLY;
     const bool vec = (cd.flags & kSrcVec) != 0;
     const uint32_t ub = cd.bits == 16 ? 2u : 1u;
-    const int ncap = kStage / int(2 + ub);   // staged records: offsets at 0, values at 2 * ncap
+    const int ncap = int((kSlotBody - 8) / (2 + ub));   // records that fit the slot
     const int nvec = (raw + 15) >> 4;
+    const int nsteps = (nvec + kStepVec - 1) / kStepVec;
+    uint8_t* slot = A.slots + size_t(k) * kEncSlot;
+    uint8_t* body = slot + kFrameHdr;
+    uint8_t* vstage = reinterpret_cast<uint8_t*>(W.pos);   // overwrite values
     const RingSrc R{W.pos, W.val};
 
-    uint32_t changed = 0;
-    Parse P{-1, 0ull, 0, 0, 0u};
-    int tail = 0, np = 0, units = 0, cur = 0;
-    bool spill = false, bad = false;
-    for (int v0 = 0; v0 < nvec; v0 += kStepVec) {
-        uint4 o[kMVPL], n[kMVPL];
+    // step s of the chunk into landing stage s % kNS (one commit group per step)
+    int cur = 0;
+    auto issue = [&](int s) {
+        if (s < nsteps) {
 #pragma unroll
-        for (int j = 0; j < kMVPL; ++j) {
-            const int v = v0 + j * 32 + lane;
-            o[j] = n[j] = make_uint4(0u, 0u, 0u, 0u);
-            if (v < nvec) {
-                const uint32_t x = uint32_t(v) << 4;
-                if (vec) {
+            for (int j = 0; j < kMVPL; ++j) {
+                const int v = s * kStepVec + j * 32 + lane;
+                uint4* lo = &W.land[s % kNS][0][j * 32 + lane];
+                uint4* ln = &W.land[s % kNS][1][j * 32 + lane];
+                if (v >= nvec) {
+                    *lo = *ln = make_uint4(0u, 0u, 0u, 0u);
+                } else if (vec) {
+                    const uint32_t x = uint32_t(v) << 4;
                     while (cur + 1 < nseg && segs[cur + 1].off <= x) ++cur;
                     const Seg sg = segs[cur];
                     const uint32_t r = uint32_t(sg.addr >> kShardShift);
                     const uint64_t a = (sg.addr & kAddrMask) + (x - sg.off);
-                    o[j] = ld_stream(A.olds[r] + a);
-                    n[j] = ld_stream(A.news[r] + a);
+                    cp_async16(lo, A.olds[r] + a);
+                    cp_async16(ln, A.news[r] + a);
                 } else {
-                    gather_bytes(A, segs, nseg, cur, x, raw, o[j], n[j]);
+                    uint4 o, n;
+                    gather_bytes(A, segs, nseg, cur, uint32_t(v) << 4, raw, o, n);
+                    *lo = o;
+                    *ln = n;
                 }
             }
         }
+        cp_async_commit();
+    };
+
+    uint32_t changed = 0;
+    Parse P{-1, 0ull, 0, 0, 0u};
+    int tail = 0, np = 0, units = 0;
+    bool spill = false, bad = false;
 #pragma unroll
-        for (int j = 0; j < kMVPL; ++j) {
-            const uint32_t v = uint32_t(v0 + j * 32 + lane);
-            const uint4 m = xor4(o[j], n[j]);
-            const uint32_t z = nz16(m);
-            changed += changed_in(z, m, cd.bits);
-            if (!overwrite) {
-                uint32_t tot;
-                const uint32_t pre = ballot_prefix(__popc(z), lane, &tot);
-                if (tot) {
+    for (int s = 0; s < kNS - 1; ++s) issue(s);
+    for (int s = 0;; ++s) {
+        const bool more = s < nsteps;
+        if (more) {
+            issue(s + kNS - 1);
+            cp_async_wait<kNS - 1>();   // this lane's copies of step s have landed
+        }
+        for (int j = 0; j < (more ? kMVPL : 1); ++j) {
+            if (more) {
+                const uint32_t v = uint32_t(s * kStepVec + j * 32 + lane);
+                const uint4 n = W.land[s % kNS][1][j * 32 + lane];
+                const uint4 m = xor4(W.land[s % kNS][0][j * 32 + lane], n);
+                const uint32_t z = nz16(m);
+                changed += changed_in(z, m, cd.bits);
+                const uint32_t bits = overwrite ? unit_bits(z, ub) : z;
+                // warp prefix of the per-lane counts: two ballots when no lane
+                // has more than one
+                uint32_t pre, tot;
+                const uint32_t any = __ballot_sync(kFull, bits != 0);
+                if (__ballot_sync(kFull, (bits & (bits - 1)) != 0) == 0) {
+                    pre = __popc(any & ((1u << lane) - 1u));
+                    tot = __popc(any);
+                } else {
+                    pre = ballot_prefix(__popc(bits), lane, &tot);
+                }
+                if (!overwrite && tot) {
                     // the ring keeps the pending literals' events, or only the
                     // unparsed ones once the chunk spills
                     if (!spill && tail + int(tot) - P.lit_ev > kRing) spill = true;
                     int e = tail + int(pre);
-                    for (uint32_t b = z; b; b &= b - 1) {
+                    for (uint32_t b = bits; b; b &= b - 1) {
                         const uint32_t i = __ffs(b) - 1;
                         W.pos[e & (kRing - 1)] = uint16_t(16u * v + i);
                         W.val[e & (kRing - 1)] = uint8_t(byte_of(m, i));
@@ -522,32 +518,39 @@ __device__ __forceinline__ void encode_chunk(const EncArgs& A, WarpSmem& W, uint
                     }
                     tail += int(tot);
                     __syncwarp();
-                    while (tail - np >= 32) {
-                        bool over = false;
-                        parse_group(R, np, 32, false, raw, P, W.stage, kStage, !spill, lane, &over, &bad);
-                        np += 32;
-                        if (__any_sync(kFull, over)) spill = true;
+                } else if (overwrite) {
+                    // unit offsets straight to the slot, values staged until
+                    // the count is known
+                    int r = units + int(pre);
+                    for (uint32_t b = bits; b; b &= b - 1) {
+                        const uint32_t i = __ffs(b) - 1;
+                        if (r < ncap) {
+                            const uint32_t u = (16u * v + i) / ub;
+                            *reinterpret_cast<uint16_t*>(body + 4 + 2 * r) = uint16_t(u);
+                            vstage[r * int(ub)] = uint8_t(byte_of(n, i));
+                            if (ub == 2) vstage[r * 2 + 1] = uint8_t(byte_of(n, i + 1));
+                        }
+                        ++r;
                     }
+                    units += int(tot);
+                    continue;
                 }
-            } else {
-                const uint32_t ubits = unit_bits(z, ub);
-                uint32_t tot;
-                const uint32_t pre = ballot_prefix(__popc(ubits), lane, &tot);
-                int r = units + int(pre);
-                for (uint32_t b = ubits; b; b &= b - 1) {
-                    const uint32_t i = __ffs(b) - 1;
-                    if (r < ncap) {
-                        const uint32_t u = (16u * v + i) / ub;
-                        W.stage[2 * r] = uint8_t(u);
-                        W.stage[2 * r + 1] = uint8_t(u >> 8);
-                        W.stage[2 * ncap + r * int(ub)] = uint8_t(byte_of(n[j], i));
-                        if (ub == 2) W.stage[2 * ncap + r * 2 + 1] = uint8_t(byte_of(n[j], i + 1));
-                    }
-                    ++r;
-                }
-                units += int(tot);
+            }
+            if (overwrite) continue;
+            // parse every full group; after the last step, the rest and the
+            // virtual end event
+            while (tail - np >= 32 || !more) {
+                const int cnt = tail - np < 32 ? tail - np : 32;
+                const bool fin = !more && tail - np < 32;
+                if (fin && tail == 0) break;   // no change: no frame
+                bool over = false;
+                parse_group(R, np, cnt, fin, raw, P, body, kSlotBody, !spill, lane, &over, &bad);
+                np += cnt;
+                if (__any_sync(kFull, over)) spill = true;
+                if (fin) break;
             }
         }
+        if (!more) break;
     }
     changed = __reduce_add_sync(kFull, changed);
     if (lane == 0 && changed) {
@@ -558,9 +561,6 @@ __device__ __forceinline__ void encode_chunk(const EncArgs& A, WarpSmem& W, uint
     uint32_t kind = 0, body_len = 0;
     bool staged = false;
     if (changed && !overwrite) {
-        bool over = false;
-        parse_group(R, np, tail - np, true, raw, P, W.stage, kStage, !spill, lane, &over, &bad);
-        if (__any_sync(kFull, over)) spill = true;
         if (P.out < uint32_t(raw)) {
             kind = kXorLz4;
             body_len = P.out;
@@ -583,48 +583,27 @@ __device__ __forceinline__ void encode_chunk(const EncArgs& A, WarpSmem& W, uint
     }
     if (__any_sync(kFull, bad) && lane == 0) report(A.sc, DCR_ERR_CORRUPT);
     const uint32_t fsz = kind ? (kFrameHdr + body_len + 15) / 16 * 16 : 0u;
-
-    uint64_t excl;
-    if (!look_back(A, k, fsz, lane, &excl)) return;
-    const uint64_t foff = kStreamHdr + (excl & kLbByteMask);
-    if (!fsz || foff + fsz > A.cap) return;
-    uint8_t* f = A.payload + foff;
-    uint4* body = reinterpret_cast<uint4*>(f + kFrameHdr);
-    if (lane == 0) write_header(f, kind, cd.bits, A.chunk_begin + k, uint32_t(raw), body_len, changed);
-    const uint32_t nv = (body_len + 15) / 16;   // body and padding, in 16-byte vectors
-    if (!staged) {
+    if (kind && !staged) {
         if (lane == 0) {
-            const uint32_t i = atomicAdd(&A.sc->n_spill, 1u);
-            A.spill[i] = SpillRec{k, kind, body_len, uint32_t(units), foff, 0ull};
+            A.fsize[k] = fsz | kSpilled;
+            A.spill[atomicAdd(&A.sc->n_spill, 1u)] =
+                SpillRec{k, kind, body_len, uint32_t(units), changed, {0u, 0u, 0u}};
         }
-    } else if (kind == kXorLz4) {
-        for (uint32_t i = body_len + lane; i < 16 * nv; i += 32) W.stage[i] = 0;
-        __syncwarp();
-        for (uint32_t i = lane; i < nv; i += 32) body[i] = reinterpret_cast<const uint4*>(W.stage)[i];
-    } else {
-        // records: count | unit offsets | pad to 4 | values, 16 bytes per lane
+        return;
+    }
+    if (kind == kOverwrite) {
         const uint32_t nu = uint32_t(units);
         const uint32_t voff = 4 + 2 * nu + (4 - (2 * nu) % 4) % 4;
-        for (uint32_t i = lane; i < nv; i += 32) {
-            uint32_t w[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                uint32_t word = 0;
-#pragma unroll
-                for (int b = 0; b < 4; ++b) {
-                    const uint32_t t = 16 * i + 4 * q + b;
-                    uint32_t x = 0;
-                    if (t < 4) x = (nu >> (8 * t)) & 0xFFu;
-                    else if (t < 4 + 2 * nu) x = W.stage[t - 4];
-                    else if (t >= voff && t < body_len) x = W.stage[2 * ncap + (t - voff)];
-                    word |= x << (8 * b);
-                }
-                w[q] = word;
-            }
-            body[i] = make_uint4(w[0], w[1], w[2], w[3]);
-        }
+        for (uint32_t i = 4 + 2 * nu + lane; i < voff; i += 32) body[i] = 0;
+        for (uint32_t i = lane; i < nu * ub; i += 32) body[voff + i] = vstage[i];
+        if (lane == 0) *reinterpret_cast<uint32_t*>(body) = nu;
     }
-    __syncwarp();   // the staging buffer is reused by the next chunk
+    if (kind) {
+        for (uint32_t i = kFrameHdr + body_len + lane; i < fsz; i += 32) slot[i] = 0;   // padding
+        if (lane == 0) write_header(slot, kind, cd.bits, A.chunk_begin + k, uint32_t(raw), body_len, changed);
+    }
+    if (lane == 0) A.fsize[k] = fsz;
+    __syncwarp();   // the ring is reused by the next chunk
 }
 
 __global__ void __launch_bounds__(kMThreads, 2) encode_kernel(EncArgs A)
@@ -641,6 +620,97 @@ __global__ void __launch_bounds__(kMThreads, 2) encode_kernel(EncArgs A)
         k = __shfl_sync(kFull, k, 0);
         if (k >= A.chunk_count) break;
         encode_chunk(A, W, k, lane);
+    }
+}
+
+// ---------------------------------------------------------- scan / copy --
+// Frame offsets from the sizes (one CTA), totals and the stream header.
+__global__ void __launch_bounds__(1024) scan_kernel(EncArgs A, uint64_t plan_hash, uint64_t base_v,
+                                                   uint64_t target_v, uint32_t window)
+{
+    __shared__ unsigned long long wsum[32];
+    const uint32_t n = A.chunk_count;
+    const uint32_t per = (n + 1023) / 1024;
+    const uint32_t b = threadIdx.x * per, e = b + per < n ? b + per : n;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    auto rec = [](uint32_t fs) -> unsigned long long {
+        fs &= ~kSpilled;
+        return fs ? ((1ull << kLbFrameShift) | fs) : 0ull;
+    };
+    unsigned long long sum = 0;
+    for (uint32_t k = b; k < e; ++k) sum += rec(A.fsize[k]);
+    // block exclusive scan of the per-thread sums
+    unsigned long long incl = sum;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const unsigned long long o = __shfl_up_sync(kFull, incl, d);
+        if (lane >= d) incl += o;
+    }
+    if (lane == 31) wsum[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        unsigned long long w = wsum[lane], wi = w;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const unsigned long long o = __shfl_up_sync(kFull, wi, d);
+            if (lane >= d) wi += o;
+        }
+        wsum[lane] = wi - w;
+    }
+    __syncthreads();
+    unsigned long long run = wsum[warp] + incl - sum;
+    for (uint32_t k = b; k < e; ++k) {
+        A.lb[k] = run;
+        run += rec(A.fsize[k]);
+    }
+    if (threadIdx.x == 1023) {
+        const uint64_t fbytes = run & kLbByteMask, nframes = run >> kLbFrameShift;
+        const uint64_t total = kStreamHdr + fbytes + 8 * nframes;
+        A.sc->total = total;
+        A.sc->n_frames = nframes;
+        if (total <= A.cap && !*(volatile int32_t*)&A.sc->err) {
+            uint32_t h[16];
+            h[0] = kStreamMagic;
+            h[1] = kFormat;
+            h[2] = uint32_t(plan_hash);
+            h[3] = uint32_t(plan_hash >> 32);
+            h[4] = uint32_t(base_v);
+            h[5] = uint32_t(base_v >> 32);
+            h[6] = uint32_t(target_v);
+            h[7] = uint32_t(target_v >> 32);
+            h[8] = window;
+            h[9] = A.mode == DCR_MODE_OVERWRITE_ONLY ? kStreamOverwriteOnly : 0u;
+            h[10] = A.chunk_begin;
+            h[11] = A.chunk_count;
+            h[12] = uint32_t(nframes);
+            h[13] = uint32_t(nframes >> 32);
+            h[14] = uint32_t(total);
+            h[15] = uint32_t(total >> 32);
+            uint4* d = reinterpret_cast<uint4*>(A.payload);
+            for (int i = 0; i < 4; ++i) d[i] = make_uint4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
+        }
+    }
+}
+
+// One warp per chunk: the slot's frame to its place in the stream, and the
+// frame's index entry (spilled frames: the entry only).
+__global__ void copy_kernel(EncArgs A)
+{
+    const uint64_t total = A.sc->total, nframes = A.sc->n_frames;
+    if (total > A.cap || *(volatile int32_t*)&A.sc->err) return;
+    uint64_t* index = reinterpret_cast<uint64_t*>(A.payload + total - 8 * nframes);
+    const int lane = threadIdx.x & 31;
+    const uint32_t nw = gridDim.x * (blockDim.x >> 5);
+    for (uint32_t k = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); k < A.chunk_count; k += nw) {
+        const uint32_t fs = A.fsize[k];
+        if (!(fs & ~kSpilled)) continue;
+        const uint64_t ex = A.lb[k];
+        const uint64_t foff = kStreamHdr + (ex & kLbByteMask);
+        if (lane == 0) index[ex >> kLbFrameShift] = foff;
+        if (fs & kSpilled) continue;
+        const uint4* src = reinterpret_cast<const uint4*>(A.slots + size_t(k) * kEncSlot);
+        uint4* dst = reinterpret_cast<uint4*>(A.payload + foff);
+        for (uint32_t i = lane; i < fs / 16; i += 32) dst[i] = src[i];
     }
 }
 
@@ -777,8 +847,10 @@ __global__ void __launch_bounds__(kSThreads, 2) spill_kernel(EncArgs A)
     Buf& B = *reinterpret_cast<Buf*>(smem_raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t n_spill = A.sc->n_spill;   // final: written by encode_kernel only
+    if (A.sc->total > A.cap) return;          // final: written by scan_kernel
     for (uint32_t s = blockIdx.x; s < n_spill; s += gridDim.x) {
         const SpillRec R = A.spill[s];
+        const uint64_t foff = kStreamHdr + (A.lb[R.k] & kLbByteMask);
         const ChunkDesc cd = A.chunks[A.chunk_begin + R.k];
         if (warp == 0) {
             if (lane == 0) B.meta.cd = cd;
@@ -791,9 +863,10 @@ __global__ void __launch_bounds__(kSThreads, 2) spill_kernel(EncArgs A)
         __syncthreads();
         const int raw = int(cd.raw_len);
         const uint8_t* bytes = reinterpret_cast<const uint8_t*>(B.data);
-        uint8_t* f = A.payload + R.foff;
+        uint8_t* f = A.payload + foff;
         uint8_t* body = f + kFrameHdr;
         const uint32_t fsz = (kFrameHdr + R.body_len + 15) / 16 * 16;
+        if (threadIdx.x == 0) write_header(f, R.kind, cd.bits, A.chunk_begin + R.k, uint32_t(raw), R.body_len, R.changed);
         if (R.kind == kXorRaw || R.kind == kOverwriteDense) {
             const int nfull = raw >> 4;
             for (int v = threadIdx.x; v < nfull; v += kSThreads) reinterpret_cast<uint4*>(body)[v] = B.data[v];
@@ -837,50 +910,6 @@ __global__ void __launch_bounds__(kSThreads, 2) spill_kernel(EncArgs A)
         }
         for (uint32_t x = kFrameHdr + R.body_len + threadIdx.x; x < fsz; x += kSThreads) f[x] = 0;
         __syncthreads();
-    }
-}
-
-// Frame index and stream header, once every chunk's prefix is known.
-__global__ void finalize_kernel(EncArgs A, uint64_t plan_hash, uint64_t base_v, uint64_t target_v,
-                                uint32_t window)
-{
-    if (*(volatile int32_t*)&A.sc->err) return;
-    const uint64_t last = ld_acquire(&A.lb[A.chunk_count - 1]) & kLbValMask;
-    const uint64_t fbytes = last & kLbByteMask, nframes = last >> kLbFrameShift;
-    const uint64_t total = kStreamHdr + fbytes + 8 * nframes;
-    const bool fits = total <= A.cap;
-    uint64_t* index = reinterpret_cast<uint64_t*>(A.payload + kStreamHdr + fbytes);
-    for (uint32_t k = blockIdx.x * blockDim.x + threadIdx.x; k < A.chunk_count;
-         k += gridDim.x * blockDim.x) {
-        uint32_t fs = A.fsize[k];
-        if (!fs || !fits) continue;
-        uint64_t inc = A.lb[k] & kLbValMask;
-        index[(inc >> kLbFrameShift) - 1] = kStreamHdr + (inc & kLbByteMask) - fs;
-    }
-    if (blockIdx.x == 0 && threadIdx.x == 0) {
-        A.sc->total = total;
-        A.sc->n_frames = nframes;
-        if (fits) {
-            uint32_t h[16];
-            h[0] = kStreamMagic;
-            h[1] = kFormat;
-            h[2] = uint32_t(plan_hash);
-            h[3] = uint32_t(plan_hash >> 32);
-            h[4] = uint32_t(base_v);
-            h[5] = uint32_t(base_v >> 32);
-            h[6] = uint32_t(target_v);
-            h[7] = uint32_t(target_v >> 32);
-            h[8] = window;
-            h[9] = A.mode == DCR_MODE_OVERWRITE_ONLY ? kStreamOverwriteOnly : 0u;
-            h[10] = A.chunk_begin;
-            h[11] = A.chunk_count;
-            h[12] = uint32_t(nframes);
-            h[13] = uint32_t(nframes >> 32);
-            h[14] = uint32_t(total);
-            h[15] = uint32_t(total >> 32);
-            uint4* d = reinterpret_cast<uint4*>(A.payload);
-            for (int i = 0; i < 4; ++i) d[i] = make_uint4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
-        }
     }
 }
 
@@ -930,8 +959,9 @@ int encode_launch(const dcr_plan* P, uint32_t mode, uint32_t window, const void*
     A.lb = P->d_lb;
     A.fsize = P->d_fsize;
     A.spill = P->d_spill;
-    size_t reset = reinterpret_cast<char*>(P->d_lb) - static_cast<char*>(P->d_enc) + A.chunk_count * 8ull;
-    cudaError_t e = cudaMemsetAsync(P->d_enc, 0, reset, s);
+    A.slots = P->d_slots;
+    // ticket, error, totals, spill count and per-tensor counts start at zero
+    cudaError_t e = cudaMemsetAsync(P->d_enc, 0, P->enc_head_bytes, s);
     if (e != cudaSuccess) return cuda_error(e, "encode scratch reset");
     const unsigned warps = unsigned(P->kc.num_sms * P->kc.enc_blocks_per_sm * kMWarps);
     unsigned grid = unsigned(P->kc.num_sms * P->kc.enc_blocks_per_sm);
@@ -939,10 +969,11 @@ int encode_launch(const dcr_plan* P, uint32_t mode, uint32_t window, const void*
     if (P->profiling) cudaEventRecord(P->ev[0], s);
     encode_kernel<<<grid, kMThreads, kMainSmem, s>>>(A);
     if (P->profiling) cudaEventRecord(P->ev[1], s);
+    scan_kernel<<<1, 1024, 0, s>>>(A, P->hash, base_v, target_v, window);
+    unsigned cgrid = (A.chunk_count + 7) / 8;
+    if (cgrid > unsigned(P->kc.num_sms * 8)) cgrid = unsigned(P->kc.num_sms * 8);
+    copy_kernel<<<cgrid, 256, 0, s>>>(A);
     spill_kernel<<<unsigned(P->kc.num_sms * P->kc.spill_blocks_per_sm), kSThreads, sizeof(Buf), s>>>(A);
-    unsigned fgrid = (A.chunk_count + 255) / 256;
-    if (fgrid > 1024) fgrid = 1024;
-    finalize_kernel<<<fgrid, 256, 0, s>>>(A, P->hash, base_v, target_v, window);
     if (P->profiling) cudaEventRecord(P->ev[2], s);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_error(e, "encode launch");

@@ -191,10 +191,12 @@ void plan_free_device(dcr_plan* p)
     cudaFree(p->d_win);
     p->d_win = nullptr;
     cudaFree(p->d_enc);
+    cudaFree(p->d_slots);
     if (p->h_enc) cudaFreeHost(p->h_enc);
     p->d_chunks = nullptr;
     p->d_src = p->d_dst = nullptr;
     p->d_enc = nullptr;
+    p->d_slots = nullptr;
     p->h_enc = nullptr;
 }
 
@@ -363,6 +365,7 @@ extern "C" int dcr_plan_build(const dcr_tensor_desc* tensors, size_t n, const dc
     size_t fs_bytes = (P->max_window_chunks * 4 + 255) / 256 * 256;
     size_t total = P->enc_head_bytes + lb_bytes + fs_bytes + P->max_window_chunks * sizeof(SpillRec) + 256;
     if ((e = cudaMalloc(&P->d_enc, total)) != cudaSuccess ||
+        (e = cudaMalloc(&P->d_slots, P->max_window_chunks * size_t(kEncSlot))) != cudaSuccess ||
         (e = cudaMallocHost(&P->h_enc, P->enc_head_bytes)) != cudaSuccess) {
         plan_free_device(P);
         delete P;
