@@ -85,7 +85,7 @@ class Profile(ctypes.Structure):
 EXPORTS = ["dcr_last_error", "dcr_plan_build", "dcr_plan_info_get", "dcr_window_info_get",
            "dcr_plan_destroy", "dcr_recv_state_create", "dcr_recv_state_destroy",
            "dcr_recv_state_version", "dcr_encode", "dcr_apply", "dcr_apply_retry",
-           "dcr_dense_refit", "dcr_plan_set_profiling", "dcr_plan_last_profile"]
+           "dcr_dense_refit", "dcr_plan_set_profiling", "dcr_plan_last_profile", "dcr_apply_noalloc"]
 
 _lib = None
 
@@ -111,6 +111,7 @@ def lib():
         L.dcr_encode.argtypes = [VP, U32, U32, P(VP), P(VP), U64, U64, VP, SZ, P(SZ), P(U64), VP]
         L.dcr_apply.argtypes = [VP, VP, VP, SZ, VP, P(Fault), P(ApplyResult), VP]
         L.dcr_apply_retry.argtypes = [VP, VP, VP, SZ, VP, P(ApplyResult), VP]
+        L.dcr_apply_noalloc.argtypes = [VP, VP, VP, SZ, VP, P(ApplyResult), VP]
         L.dcr_dense_refit.argtypes = [VP, P(VP), VP, VP]
         L.dcr_plan_set_profiling.argtypes = [VP, ctypes.c_int]
         L.dcr_plan_last_profile.argtypes = [VP, P(Profile)]
@@ -241,6 +242,14 @@ def apply_retry(plan, state, payload, size, target, stream=None):
     res = ApplyResult()
     rc = lib().dcr_apply_retry(plan.h, state.h, _ptr(payload), size, _ptr(target), ctypes.byref(res),
                                _stream(stream))
+    return rc, res
+
+
+def apply_noalloc(plan, state, payload, size, target, stream=None):
+    """dcr_apply without allocation: scratch in the library's static device array."""
+    res = ApplyResult()
+    rc = lib().dcr_apply_noalloc(plan.h, state.h, _ptr(payload), size, _ptr(target), ctypes.byref(res),
+                                 _stream(stream))
     return rc, res
 
 

@@ -33,7 +33,10 @@
 //                 version (the commit rule).
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdint>
+#include <cstring>
+#include <mutex>
 
 #include "dcr_internal.h"
 
@@ -756,4 +759,138 @@ int apply_launch(const dcr_plan* P, dcr_recv_state* st, const void* payload, siz
     return DCR_OK;
 }
 
+// ---- apply without allocation ---------------------------------------------
+// dcr_apply_noalloc runs the same three kernels as dcr_apply, but the call's
+// scratch (the ApplyScratch counters and the list of deferred frames) lives
+// in the file-scope device array below instead of the receiver state's
+// buffers.  Its callers cannot allocate device memory when a refit arrives:
+// an inference engine typically reserves nearly all free HBM for its KV cache
+// at start-up and runs the weight update from a hook where a cudaMalloc (or
+// PyTorch's caching allocator growing its pool) would fail or stall serving.
+// The call itself neither allocates nor frees device or pinned memory; the
+// status comes back through a stack buffer.
+namespace {
+
+constexpr uint32_t kNoallocMaxChunks = 65536;    // window limit: 4 GiB of canonical bytes
+constexpr size_t kNoallocHead = 256;             // ApplyScratch, padded
+static_assert(sizeof(ApplyScratch) <= kNoallocHead, "counters fit the head");
+constexpr size_t kNoallocBytes = kNoallocHead + 4 * (size_t(kNoallocMaxChunks) + 1);   // 256 KiB + 260 B
+
+// [0, 256): ApplyScratch, cleared by a memset on the caller's stream at the
+// start of every call; [256, ...): deferred frame list, written before read.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of this device's copy of the array, looked up once per
+// device with that device current.  The lookup may load the module, so the
+// first call on each device should come before any stream capture.
+int noalloc_scratch(int dev, void** out)
+{
+    if (dev < 0 || dev >= kMaxDevices) return set_error(DCR_ERR_INVALID, "device %d out of range", dev);
+    std::lock_guard<std::mutex> g(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void* ptr = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+        if (e != cudaSuccess) return cuda_error(e, "cudaGetSymbolAddress of the static apply scratch");
+        g_noalloc_ptr[dev] = ptr;
+    }
+    *out = g_noalloc_ptr[dev];
+    return DCR_OK;
+}
+
+}  // namespace
+
+int apply_launch_noalloc(const dcr_plan* P, dcr_recv_state* st, const void* payload, size_t size,
+                         void* target, ApplyScratch** sc_out, cudaStream_t s)
+{
+    if (P->max_window_chunks > kNoallocMaxChunks)
+        return set_error(DCR_ERR_CAPACITY,
+                         "dcr_apply_noalloc: windows of %llu chunks exceed the static scratch limit of %u "
+                         "chunks (build the plan with window_bytes <= 4 GiB)",
+                         (unsigned long long)P->max_window_chunks, kNoallocMaxChunks);
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_error(e, "cudaGetDevice");
+    if (dev != P->device) return set_error(DCR_ERR_INVALID, "dcr_apply_noalloc: plan belongs to device %d", P->device);
+    void* base = nullptr;
+    int rc = noalloc_scratch(dev, &base);
+    if (rc) return rc;
+    ApplyArgs A{};
+    A.chunks = P->d_chunks;
+    A.dst = P->d_dst;
+    A.win = P->d_win;
+    A.n_windows = uint32_t(P->win_start.size() - 1);
+    A.retry_only = 0;
+    A.payload = static_cast<const uint8_t*>(payload);
+    A.size = size;
+    A.target = static_cast<uint8_t*>(target);
+    A.state = reinterpret_cast<unsigned long long*>(st->d_chunk_state);
+    A.sc = static_cast<ApplyScratch*>(base);
+    A.defer = reinterpret_cast<uint32_t*>(static_cast<unsigned char*>(base) + kNoallocHead);
+    A.plan_hash = P->hash;
+    A.version = st->version;
+    A.abort_at = DCR_NO_FAULT;
+    A.split = 0;
+    e = cudaMemsetAsync(A.sc, 0, sizeof(ApplyScratch), s);
+    if (e != cudaSuccess) return cuda_error(e, "static apply scratch reset");
+    const int sms = P->kc.num_sms;
+    apply_kernel<<<sms * P->kc.apply_blocks_per_sm, kAThreads, sizeof(ASmem), s>>>(A);
+    defer_kernel<<<sms * P->kc.defer_blocks_per_sm, kDThreads, kChunk, s>>>(A);
+    pending_kernel<<<sms, 256, 0, s>>>(A);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_error(e, "apply launch");
+    *sc_out = A.sc;
+    return DCR_OK;
+}
+
 }  // namespace dcr
+
+extern "C" int dcr_apply_noalloc(const dcr_plan* p, dcr_recv_state* st, const void* payload, size_t size,
+                                 void* target, dcr_apply_result* result, void* stream)
+{
+    using namespace dcr;
+    if (result) memset(result, 0, sizeof(*result));
+    if (!p || !st || !payload || !target) return set_error(DCR_ERR_INVALID, "dcr_apply_noalloc: NULL argument");
+    if (st->plan != p) return set_error(DCR_ERR_INVALID, "dcr_apply_noalloc: state belongs to another plan");
+    if (size < kStreamHdr) return set_error(DCR_ERR_CORRUPT, "dcr_apply_noalloc: stream shorter than its header");
+    if ((reinterpret_cast<uintptr_t>(payload) | reinterpret_cast<uintptr_t>(target)) & 15)
+        return set_error(DCR_ERR_INVALID, "dcr_apply_noalloc: payload/target not 16-byte aligned");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    ApplyScratch* dsc = nullptr;
+    int rc = apply_launch_noalloc(p, st, payload, size, target, &dsc, s);
+    if (rc) return rc;
+    ApplyScratch a;   // pageable stack copy of the counters
+    cudaError_t e = cudaMemcpyAsync(&a, dsc, sizeof(a), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_error(e, "dcr_apply_noalloc status read");
+    if (result) {
+        result->target_version = a.target_version;
+        result->n_frames = a.n_frames;
+        result->frames_applied = a.applied;
+        result->frames_skipped = a.skipped;
+        result->pending = a.pending;
+        result->window = a.window;
+    }
+    if (a.err) return set_error(a.err, "dcr_apply_noalloc: device reported error %d", a.err);
+    if (a.pending)
+        return set_error(DCR_ERR_INCOMPLETE, "dcr_apply_noalloc: %llu framed chunks not done",
+                         (unsigned long long)a.pending);
+    // commit rule of dcr_apply: the version advances once every window of the
+    // target version has been applied
+    if (a.target_version != st->pending) {
+        std::fill(st->win_done.begin(), st->win_done.end(), 0);
+        st->pending = a.target_version;
+    }
+    st->win_done[a.window] = 1;
+    bool all = true;
+    for (uint8_t d : st->win_done) all = all && d;
+    if (all) {
+        st->version = a.target_version;
+        st->pending = ~0ull;
+        if (result) result->committed = 1;
+    }
+    return DCR_OK;
+}

@@ -231,6 +231,28 @@ int dcr_apply(const dcr_plan* plan, dcr_recv_state* state, const void* payload, 
 int dcr_apply_retry(const dcr_plan* plan, dcr_recv_state* state, const void* payload, size_t size,
                     void* target, dcr_apply_result* result, void* stream);
 
+/* dcr_apply without allocation.  No counterpart in the method's pages: it is
+ * a deployment variant for receivers that cannot allocate device memory when
+ * a refit arrives (an inference engine that reserved nearly all free HBM for
+ * its KV cache at start-up).  Same arguments, decode, dedup, commit rule and
+ * errors as dcr_apply with fault == NULL, but the call's scratch (its
+ * counters and the list of deferred frames) is a static device array of the
+ * library (256 KiB + 260 B per device) instead of the receiver state's
+ * buffers, and the status is read back into a stack buffer: the call
+ * neither allocates nor frees device or pinned memory.
+ *   - Limit: windows of at most 65536 chunks (4 GiB of canonical bytes);
+ *     plans with larger windows get DCR_ERR_CAPACITY before anything runs.
+ *   - The counters are cleared by a memset on `stream` at the start of each
+ *     call; nothing has to be zeroed by the caller.
+ *   - The first call on each device looks up the array's device address
+ *     (once, with that device current); make that first call before any
+ *     stream capture.
+ *   - The static scratch is shared by every call on a device, whatever the
+ *     plan or receiver state: calls on one device must not overlap in time
+ *     (concurrent calls race on the counters). */
+int dcr_apply_noalloc(const dcr_plan* plan, dcr_recv_state* state, const void* payload, size_t size,
+                      void* target, dcr_apply_result* result, void* stream);
+
 /* Kernel timing (tracing aid).  When on, the library records CUDA events on
  * the caller's stream around each of its kernels; after each dcr_encode /
  * dcr_apply / dcr_apply_retry, dcr_plan_last_profile returns the durations

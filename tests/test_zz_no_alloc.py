@@ -1,0 +1,64 @@
+"""dcr_apply_noalloc (dcr_apply with the library's static device scratch)
+against dcr_apply on the same streams, two refits in a row, through the C
+ABI; and its window limit.  Kept in a file of its own, collected last, so it
+also runs after every other GPU test in the same process."""
+import numpy as np
+import pytest
+
+import oracle
+from synth import configs
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+import bit_exact_xor_gb300 as dcr  # noqa: E402
+from wl import descs_of, to_device  # noqa: E402
+
+
+def _target(plan, wl, shards):
+    t = torch.zeros(max(plan.info.recv_bytes, wl.recv_bytes, 16), dtype=torch.uint8, device="cuda")
+    dcr.check(dcr.dense_refit(plan, shards, t))
+    return t
+
+
+@pytest.mark.parametrize("n", [1, 2, 3])
+def test_noalloc_matches_apply_two_calls_in_a_row(n):
+    wl = configs.mini(n)
+    orc = oracle.Oracle(wl)
+    olds, news = wl.host_arenas()
+    plan = dcr.Plan(descs_of(wl), window_bytes=wl.window_bytes)
+    d_old, d_new = to_device(olds), to_device(news)
+    ref_t, got_t = _target(plan, wl, d_old), _target(plan, wl, d_old)
+    ref_st, got_st = dcr.RecvState(plan, 0), dcr.RecvState(plan, 0)
+    # refit 0 -> 1 (old -> new), then 1 -> 2 (new -> old)
+    for v, (a, b, host_b) in enumerate([(d_old, d_new, news), (d_new, d_old, olds)]):
+        for w in range(plan.info.n_windows):
+            pl = torch.zeros(plan.window(w).payload_bound, dtype=torch.uint8, device="cuda")
+            rc, size, _ = dcr.encode(plan, a, b, pl, window=w, base_version=v, target_version=v + 1)
+            dcr.check(rc)
+            rc1, r1 = dcr.apply(plan, ref_st, pl, size, ref_t)
+            rc2, r2 = dcr.apply_noalloc(plan, got_st, pl, size, got_t)
+            assert rc1 == dcr.OK and rc2 == dcr.OK, (rc1, rc2, dcr.last_error())
+            fields = ("target_version", "n_frames", "frames_applied", "frames_skipped", "pending", "window",
+                      "committed")
+            assert [getattr(r2, f) for f in fields] == [getattr(r1, f) for f in fields]
+        torch.cuda.synchronize()
+        assert torch.equal(ref_t, got_t)
+        assert ref_st.version == got_st.version == v + 1
+        exp = orc.receiver_dense(host_b)
+        assert np.array_equal(got_t.cpu().numpy()[:exp.size], exp)
+
+
+def test_noalloc_rejects_windows_beyond_its_limit():
+    # one 4 GiB + 64 KiB tensor: a window of 65537 chunks, one more than the
+    # static scratch holds; rejected before any kernel runs
+    d = dcr.make_desc("big", 8, 65537, 65536, dcr.REPLICATED, 1, [0], 0)
+    plan = dcr.Plan([d])
+    assert plan.window(0).chunk_count == 65537
+    st = dcr.RecvState(plan, 0)
+    pl = torch.zeros(64, dtype=torch.uint8, device="cuda")
+    t = torch.full((64,), 7, dtype=torch.uint8, device="cuda")
+    rc, _ = dcr.apply_noalloc(plan, st, pl, 64, t)
+    assert rc == dcr.ERR_CAPACITY
+    assert "static scratch limit" in dcr.last_error()
+    assert st.version == 0 and bool((t == 7).all())
