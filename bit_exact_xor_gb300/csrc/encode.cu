@@ -16,9 +16,9 @@
 // "Residual Conversion" and "Hybrid encoding and compression" (XOR masks for
 // affine changes, overwrites for residual ones).
 //
-// encode_kernel.  One warp per chunk, chunks taken in ticket order, 18 warps
+// encode_kernel.  One warp per chunk, chunks taken in ticket order, 21 warps
 // per SM.  The warp streams its chunk in 1 KiB steps: cp.async copies old
-// and new into a four-stage landing buffer in shared memory, so three steps
+// and new into a three-stage landing buffer in shared memory, so two steps
 // are in flight while one is processed.  It XORs and counts, and appends the
 // positions and values of the non-zero mask bytes ("events") to a ring in
 // shared memory.  Every 32 events it runs one parse group (one event per
@@ -61,12 +61,11 @@ namespace {
 
 constexpr uint32_t kFull = 0xffffffffu;
 // encode_kernel
-constexpr int kMWarps = 9;                        // warps per CTA, one chunk each; 2 CTAs per SM
+constexpr int kMWarps = 7;                        // warps per CTA, one chunk each; 3 CTAs per SM
 constexpr int kMThreads = 32 * kMWarps;
 constexpr int kRing = 1024;                       // event ring entries per warp (power of two)
-constexpr int kMVPL = 2;                          // 16-byte vectors per lane per step
-constexpr int kStepVec = 32 * kMVPL;              // 1 KiB per step
-constexpr int kNS = 4;                            // landing stages: kNS - 1 steps in flight
+constexpr int kStep = 1024;                       // bytes per step: 32 contiguous bytes per lane
+constexpr int kNS = 3;                            // landing stages: kNS - 1 steps in flight
 constexpr int kMSegCache = 64;                    // sender pieces cached per warp
 constexpr uint32_t kSlotBody = kEncSlot - kFrameHdr;   // frame body bytes a slot holds
 // spill_kernel
@@ -99,7 +98,8 @@ struct EncArgs {
 
 // encode_kernel: one warp's shared memory
 struct __align__(16) WarpSmem {
-    uint4 land[kNS][2][kStepVec];      // landing stages: old, new; lane's vectors at j * 32 + lane
+    uint4 land[kNS][2][64];            // landing stages [stage][old, new][16-byte slot]: the
+                                       // step's bytes 32 L + 16 h in slot land_slot(L, h)
     uint16_t pos[kRing];               // event ring: byte position in the chunk
     uint8_t val[kRing];                //             mask byte
     Seg segs[kMSegCache];              // the chunk's sender pieces
@@ -173,21 +173,30 @@ __device__ __forceinline__ uint32_t nz16(uint4 v)
     return nz4(v.x) | (nz4(v.y) << 4) | (nz4(v.z) << 8) | (nz4(v.w) << 12);
 }
 
-// changed stored values in a 16-byte mask vector with non-zero-byte mask m
-// (bf16: 16-bit words; e4m3: bytes; e2m1: nibbles)
-__device__ __forceinline__ uint32_t changed_in(uint32_t m, uint4 v, uint32_t bits)
+// 32 mask bytes (a: bytes 0-15, b: bytes 16-31): bit i set iff byte i is
+// non-zero.  Per word, bit 7 of each byte is set iff the byte is non-zero
+// (the low 7 bits plus 0x7F carry into bit 7, or bit 7 was set); one
+// multiply then gathers the eight flags of two words into one byte.
+__device__ __forceinline__ uint32_t nz32(uint4 a, uint4 b)
 {
-    if (bits == 16) return __popc((m | (m >> 1)) & 0x5555u);
-    if (bits == 8) return __popc(m);
-    uint32_t c = 0;
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        uint32_t t = w[i] | (w[i] >> 1);
-        t |= t >> 2;
-        c += __popc(t & 0x11111111u);
-    }
-    return c;
+    auto hb = [](uint32_t w) { return (((w & 0x7F7F7F7Fu) + 0x7F7F7F7Fu) | w) & 0x80808080u; };
+    auto pair = [&](uint32_t lo, uint32_t hi) { return ((hb(hi) | (hb(lo) >> 4)) * 0x00204081u) >> 24; };
+    return pair(a.x, a.y) | (pair(a.z, a.w) << 8) | (pair(b.x, b.y) << 16) | (pair(b.z, b.w) << 24);
+}
+
+// byte i (0..31) of the 32 bytes (a, b)
+__device__ __forceinline__ uint32_t byte_of32(uint4 a, uint4 b, uint32_t i)
+{
+    const uint4 v = (i & 16) ? b : a;
+    return byte_of(v, i & 15);
+}
+
+// non-zero 4-bit nibbles of a word
+__device__ __forceinline__ uint32_t nibbles_nz(uint32_t w)
+{
+    uint32_t t = w | (w >> 1);
+    t |= t >> 2;
+    return __popc(t & 0x11111111u);
 }
 
 // overwrite units of a non-zero-byte mask: bit i set iff the unit starting at
@@ -227,21 +236,6 @@ __device__ __forceinline__ uint32_t warp_incl_sum(uint32_t v, int lane)
         if (lane >= d) v += o;
     }
     return v;
-}
-
-// exclusive warp prefix of c (0..31) from five independent ballots; *tot = sum
-__device__ __forceinline__ uint32_t ballot_prefix(uint32_t c, int lane, uint32_t* tot)
-{
-    const uint32_t lt = (1u << lane) - 1u;
-    uint32_t pre = 0, t = 0;
-#pragma unroll
-    for (int k = 0; k < 5; ++k) {
-        const uint32_t b = __ballot_sync(kFull, (c >> k) & 1u);
-        pre += uint32_t(__popc(b & lt)) << k;
-        t += uint32_t(__popc(b)) << k;
-    }
-    *tot = t;
-    return pre;
 }
 
 __device__ __forceinline__ void report(EncScratch* sc, int code)
@@ -402,6 +396,11 @@ __device__ __forceinline__ void write_header(uint8_t* f, uint32_t kind, uint32_t
 }
 
 // ---------------------------------------------------------- encode_kernel --
+// Slot of the step's bytes [32 L + 16 h, + 16): the two halves of every
+// fourth-lane group are swapped, so that lanes reading their own 32 bytes
+// (one 16-byte load per half) hit distinct banks.
+__device__ __forceinline__ int land_slot(int L, int h) { return 2 * L + (h ^ ((L >> 2) & 1)); }
+
 // Byte-wise gather of one 16-byte vector at canonical byte x0 (chunks whose
 // pieces are not all 16-byte aligned); bytes at or past raw read as zero.
 __device__ __forceinline__ void gather_bytes(const EncArgs& A, const Seg* segs, int nseg, int& cur,
@@ -438,26 +437,27 @@ __device__ __forceinline__ void encode_chunk(const EncArgs& A, WarpSmem& W, uint
     const bool vec = (cd.flags & kSrcVec) != 0;
     const uint32_t ub = cd.bits == 16 ? 2u : 1u;
     const int ncap = int((kSlotBody - 8) / (2 + ub));   // records that fit the slot
-    const int nvec = (raw + 15) >> 4;
-    const int nsteps = (nvec + kStepVec - 1) / kStepVec;
+    const int nsteps = (raw + kStep - 1) / kStep;
     uint8_t* slot = A.slots + size_t(k) * kEncSlot;
     uint8_t* body = slot + kFrameHdr;
     uint8_t* vstage = reinterpret_cast<uint8_t*>(W.pos);   // overwrite values
     const RingSrc R{W.pos, W.val};
 
-    // step s of the chunk into landing stage s % kNS (one commit group per step)
+    // step s of the chunk into landing stage s % kNS (one commit group per
+    // step); each copy instruction covers 512 contiguous bytes
     int cur = 0;
     auto issue = [&](int s) {
         if (s < nsteps) {
 #pragma unroll
-            for (int j = 0; j < kMVPL; ++j) {
-                const int v = s * kStepVec + j * 32 + lane;
-                uint4* lo = &W.land[s % kNS][0][j * 32 + lane];
-                uint4* ln = &W.land[s % kNS][1][j * 32 + lane];
-                if (v >= nvec) {
+            for (int g = 0; g < 2; ++g) {
+                const uint32_t q = 512u * g + 16u * lane;   // byte of the step
+                const uint32_t x = uint32_t(s) * kStep + q;
+                const int slot = land_slot(int(q >> 5), int(lane & 1));
+                uint4* lo = &W.land[s % kNS][0][slot];
+                uint4* ln = &W.land[s % kNS][1][slot];
+                if (x >= uint32_t(raw)) {
                     *lo = *ln = make_uint4(0u, 0u, 0u, 0u);
                 } else if (vec) {
-                    const uint32_t x = uint32_t(v) << 4;
                     while (cur + 1 < nseg && segs[cur + 1].off <= x) ++cur;
                     const Seg sg = segs[cur];
                     const uint32_t r = uint32_t(sg.addr >> kShardShift);
@@ -466,7 +466,7 @@ __device__ __forceinline__ void encode_chunk(const EncArgs& A, WarpSmem& W, uint
                     cp_async16(ln, A.news[r] + a);
                 } else {
                     uint4 o, n;
-                    gather_bytes(A, segs, nseg, cur, uint32_t(v) << 4, raw, o, n);
+                    gather_bytes(A, segs, nseg, cur, x, raw, o, n);
                     *lo = o;
                     *ln = n;
                 }
@@ -479,66 +479,93 @@ __device__ __forceinline__ void encode_chunk(const EncArgs& A, WarpSmem& W, uint
     Parse P{-1, 0ull, 0, 0, 0u};
     int tail = 0, np = 0, units = 0;
     bool spill = false, bad = false;
+    const uint32_t lt = (1u << lane) - 1u;
 #pragma unroll
     for (int s = 0; s < kNS - 1; ++s) issue(s);
     for (int s = 0;; ++s) {
         const bool more = s < nsteps;
+        const uint32_t x = uint32_t(s) * kStep + 32u * lane;   // the lane's first byte
+        uint4 m0 = make_uint4(0u, 0u, 0u, 0u), m1 = m0, n0 = m0, n1 = m0;
+        uint32_t z = 0;   // non-zero mask bytes (XOR) or changed units (overwrite) of the lane's 32
         if (more) {
             issue(s + kNS - 1);
             cp_async_wait<kNS - 1>();   // this lane's copies of step s have landed
+            const int s0 = land_slot(lane, 0), s1 = land_slot(lane, 1);
+            // a lane reads 16-byte slots that other lanes' copies filled
+            __syncwarp();
+            n0 = W.land[s % kNS][1][s0];
+            n1 = W.land[s % kNS][1][s1];
+            m0 = xor4(W.land[s % kNS][0][s0], n0);
+            m1 = xor4(W.land[s % kNS][0][s1], n1);
+            z = nz32(m0, m1);
+            if (cd.bits == 16) {
+                changed += __popc((z | (z >> 1)) & 0x55555555u);
+            } else if (cd.bits == 8) {
+                changed += __popc(z);
+            } else {
+                changed += nibbles_nz(m0.x) + nibbles_nz(m0.y) + nibbles_nz(m0.z) + nibbles_nz(m0.w) +
+                           nibbles_nz(m1.x) + nibbles_nz(m1.y) + nibbles_nz(m1.z) + nibbles_nz(m1.w);
+            }
+            if (overwrite) z = unit_bits(z, ub);
         }
-        for (int j = 0; j < (more ? kMVPL : 1); ++j) {
-            if (more) {
-                const uint32_t v = uint32_t(s * kStepVec + j * 32 + lane);
-                const uint4 n = W.land[s % kNS][1][j * 32 + lane];
-                const uint4 m = xor4(W.land[s % kNS][0][j * 32 + lane], n);
-                const uint32_t z = nz16(m);
-                changed += changed_in(z, m, cd.bits);
-                const uint32_t bits = overwrite ? unit_bits(z, ub) : z;
-                // warp prefix of the per-lane counts: two ballots when no lane
-                // has more than one
-                uint32_t pre, tot;
-                const uint32_t any = __ballot_sync(kFull, bits != 0);
-                if (__ballot_sync(kFull, (bits & (bits - 1)) != 0) == 0) {
-                    pre = __popc(any & ((1u << lane) - 1u));
-                    tot = __popc(any);
-                } else {
-                    pre = ballot_prefix(__popc(bits), lane, &tot);
+        // warp prefix of the per-lane counts: two ballots when no lane has more
+        // than one
+        const uint32_t c = __popc(z);
+        uint32_t pre, tot, t16;
+        if (__ballot_sync(kFull, c > 1) == 0) {
+            const uint32_t any = __ballot_sync(kFull, c != 0);
+            pre = __popc(any & lt);
+            tot = __popc(any);
+            t16 = __popc(any & 0xFFFFu);
+        } else {
+            const uint32_t incl = warp_incl_sum(c, lane);
+            pre = incl - c;
+            tot = __shfl_sync(kFull, incl, 31);
+            t16 = __shfl_sync(kFull, incl, 15);
+        }
+        if (overwrite) {
+            // unit offsets straight to the slot, values staged until the
+            // count is known
+            int r = units + int(pre);
+            for (uint32_t b = z; b; b &= b - 1) {
+                const uint32_t i = __ffs(b) - 1;
+                if (r < ncap) {
+                    const uint32_t u = (x + i) / ub;
+                    *reinterpret_cast<uint16_t*>(body + 4 + 2 * r) = uint16_t(u);
+                    vstage[r * int(ub)] = uint8_t(byte_of32(n0, n1, i));
+                    if (ub == 2) vstage[r * 2 + 1] = uint8_t(byte_of32(n0, n1, i + 1));
                 }
-                if (!overwrite && tot) {
-                    // the ring keeps the pending literals' events, or only the
-                    // unparsed ones once the chunk spills
-                    if (!spill && tail + int(tot) - P.lit_ev > kRing) spill = true;
-                    int e = tail + int(pre);
-                    for (uint32_t b = bits; b; b &= b - 1) {
+                ++r;
+            }
+            units += int(tot);
+            if (!more) break;
+            continue;
+        }
+        // events to the ring (in two halves when there are many, so that the
+        // ring never holds more than 512 new ones), each half followed by the
+        // parse of every full group; after the last step, the rest and the
+        // virtual end event
+        const int halves = tot > 512u ? 2 : 1;
+        const int tail0 = tail;
+        for (int hf = 0; hf < halves; ++hf) {
+            if (more) {
+                const bool mine = halves == 1 || (lane >> 4) == hf;
+                const int end = tail0 + int(halves == 1 || hf == 1 ? tot : t16);
+                // the ring keeps the pending literals' events, or only the
+                // unparsed ones once the chunk spills
+                if (!spill && end - P.lit_ev > kRing) spill = true;
+                if (mine) {
+                    int e = tail0 + int(pre);
+                    for (uint32_t b = z; b; b &= b - 1) {
                         const uint32_t i = __ffs(b) - 1;
-                        W.pos[e & (kRing - 1)] = uint16_t(16u * v + i);
-                        W.val[e & (kRing - 1)] = uint8_t(byte_of(m, i));
+                        W.pos[e & (kRing - 1)] = uint16_t(x + i);
+                        W.val[e & (kRing - 1)] = uint8_t(byte_of32(m0, m1, i));
                         ++e;
                     }
-                    tail += int(tot);
-                    __syncwarp();
-                } else if (overwrite) {
-                    // unit offsets straight to the slot, values staged until
-                    // the count is known
-                    int r = units + int(pre);
-                    for (uint32_t b = bits; b; b &= b - 1) {
-                        const uint32_t i = __ffs(b) - 1;
-                        if (r < ncap) {
-                            const uint32_t u = (16u * v + i) / ub;
-                            *reinterpret_cast<uint16_t*>(body + 4 + 2 * r) = uint16_t(u);
-                            vstage[r * int(ub)] = uint8_t(byte_of(n, i));
-                            if (ub == 2) vstage[r * 2 + 1] = uint8_t(byte_of(n, i + 1));
-                        }
-                        ++r;
-                    }
-                    units += int(tot);
-                    continue;
                 }
+                tail = end;
+                __syncwarp();
             }
-            if (overwrite) continue;
-            // parse every full group; after the last step, the rest and the
-            // virtual end event
             while (tail - np >= 32 || !more) {
                 const int cnt = tail - np < 32 ? tail - np : 32;
                 const bool fin = !more && tail - np < 32;
@@ -606,7 +633,7 @@ __device__ __forceinline__ void encode_chunk(const EncArgs& A, WarpSmem& W, uint
     __syncwarp();   // the ring is reused by the next chunk
 }
 
-__global__ void __launch_bounds__(kMThreads, 2) encode_kernel(EncArgs A)
+__global__ void __launch_bounds__(kMThreads, 3) encode_kernel(EncArgs A)
 {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     const int lane = threadIdx.x & 31;
