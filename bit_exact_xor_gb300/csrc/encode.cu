@@ -16,7 +16,7 @@
 // "Residual Conversion" and "Hybrid encoding and compression" (XOR masks for
 // affine changes, overwrites for residual ones).
 //
-// encode_kernel.  One warp per chunk, chunks taken in ticket order, 21 warps
+// encode_kernel.  One warp per chunk, chunks taken in ticket order, 24 warps
 // per SM.  The warp streams its chunk in 1 KiB steps: cp.async copies old
 // and new into a three-stage landing buffer in shared memory, so two steps
 // are in flight while one is processed.  It XORs and counts, and appends the
@@ -61,9 +61,10 @@ namespace {
 
 constexpr uint32_t kFull = 0xffffffffu;
 // encode_kernel
-constexpr int kMWarps = 7;                        // warps per CTA, one chunk each; 3 CTAs per SM
+constexpr int kMWarps = 6;                        // warps per CTA, one chunk each; 4 CTAs per SM
 constexpr int kMThreads = 32 * kMWarps;
-constexpr int kRing = 1024;                       // event ring entries per warp (power of two)
+constexpr int kRing = 512;                        // event ring entries per warp (power of two)
+constexpr int kAppend = 256;                      // events appended to the ring at most at once
 constexpr int kStep = 1024;                       // bytes per step: 32 contiguous bytes per lane
 constexpr int kNS = 3;                            // landing stages: kNS - 1 steps in flight
 constexpr int kMSegCache = 64;                    // sender pieces cached per warp
@@ -108,8 +109,7 @@ struct __align__(16) WarpSmem {
 constexpr int kValStage = int(sizeof(uint16_t) + sizeof(uint8_t)) * kRing;
 static_assert(offsetof(WarpSmem, val) == offsetof(WarpSmem, pos) + sizeof(uint16_t) * kRing,
               "ring storage is contiguous");
-static_assert(2 * ((kSlotBody - 8) / 4) <= uint32_t(kValStage) && (kSlotBody - 8) / 3 <= uint32_t(kValStage),
-              "the values of the records a slot holds fit the ring's storage");
+static_assert(kAppend + 31 <= kRing, "a spilled chunk's unparsed events fit the ring");
 
 // spill_kernel: one chunk in shared memory
 struct __align__(16) Meta {
@@ -436,7 +436,9 @@ __device__ __forceinline__ void encode_chunk(const EncArgs& A, WarpSmem& W, uint
     const bool overwrite = (cd.flags & kResidualFlag) || A.mode == DCR_MODE_OVERWRITE_ONLY;
     const bool vec = (cd.flags & kSrcVec) != 0;
     const uint32_t ub = cd.bits == 16 ? 2u : 1u;
-    const int ncap = int((kSlotBody - 8) / (2 + ub));   // records that fit the slot
+    // records that fit the slot and whose values fit the ring's storage
+    const int ncap = int((kSlotBody - 8) / (2 + ub)) < kValStage / int(ub) ? int((kSlotBody - 8) / (2 + ub))
+                                                                           : kValStage / int(ub);
     const int nsteps = (raw + kStep - 1) / kStep;
     uint8_t* slot = A.slots + size_t(k) * kEncSlot;
     uint8_t* body = slot + kFrameHdr;
@@ -511,17 +513,16 @@ __device__ __forceinline__ void encode_chunk(const EncArgs& A, WarpSmem& W, uint
         // warp prefix of the per-lane counts: two ballots when no lane has more
         // than one
         const uint32_t c = __popc(z);
-        uint32_t pre, tot, t16;
+        uint32_t pre, tot, incl;
         if (__ballot_sync(kFull, c > 1) == 0) {
             const uint32_t any = __ballot_sync(kFull, c != 0);
             pre = __popc(any & lt);
             tot = __popc(any);
-            t16 = __popc(any & 0xFFFFu);
+            incl = pre + c;
         } else {
-            const uint32_t incl = warp_incl_sum(c, lane);
+            incl = warp_incl_sum(c, lane);
             pre = incl - c;
             tot = __shfl_sync(kFull, incl, 31);
-            t16 = __shfl_sync(kFull, incl, 15);
         }
         if (overwrite) {
             // unit offsets straight to the slot, values staged until the
@@ -541,16 +542,16 @@ __device__ __forceinline__ void encode_chunk(const EncArgs& A, WarpSmem& W, uint
             if (!more) break;
             continue;
         }
-        // events to the ring (in two halves when there are many, so that the
-        // ring never holds more than 512 new ones), each half followed by the
-        // parse of every full group; after the last step, the rest and the
-        // virtual end event
-        const int halves = tot > 512u ? 2 : 1;
+        // events to the ring (by groups of 8 lanes when there are many, so
+        // that at most kAppend new ones arrive at once), each part followed by
+        // the parse of every full group; after the last step, the rest and
+        // the virtual end event
+        const int parts = tot > uint32_t(kAppend) ? 4 : 1;
         const int tail0 = tail;
-        for (int hf = 0; hf < halves; ++hf) {
+        for (int hf = 0; hf < parts; ++hf) {
             if (more) {
-                const bool mine = halves == 1 || (lane >> 4) == hf;
-                const int end = tail0 + int(halves == 1 || hf == 1 ? tot : t16);
+                const bool mine = parts == 1 || (lane >> 3) == hf;
+                const int end = tail0 + int(parts == 1 ? tot : __shfl_sync(kFull, incl, 8 * hf + 7));
                 // the ring keeps the pending literals' events, or only the
                 // unparsed ones once the chunk spills
                 if (!spill && end - P.lit_ev > kRing) spill = true;
@@ -633,7 +634,7 @@ __device__ __forceinline__ void encode_chunk(const EncArgs& A, WarpSmem& W, uint
     __syncwarp();   // the ring is reused by the next chunk
 }
 
-__global__ void __launch_bounds__(kMThreads, 3) encode_kernel(EncArgs A)
+__global__ void __launch_bounds__(kMThreads, 4) encode_kernel(EncArgs A)
 {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     const int lane = threadIdx.x & 31;
