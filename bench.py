@@ -194,10 +194,20 @@ def cpu_baseline(wl, budget_s=12.0):
                                         "%.1f s" % (n, dt), "payload_bytes": payload}
 
 
+def run_config(args, wl, nw, ws):
+    """The workload description both arms print."""
+    N = wl.canonical_bytes
+    return {"workload": WORKLOAD_NAMES[args.workload], "canonical_bytes": N,
+            "tp": wl.tp, "windows": nw, "parallelism": "replicas" if ws > 1 else "single GPU",
+            "l2": "inputs larger than L2 (2N = %.2f GB read per encode)" % (2 * N / 1e9)
+            if 2 * N > 200e6 else "inputs fit in L2"}
+
+
 def run_reference(args):
     ws, rank, _ = dist_env()
     if rank != 0:
         return 0
+    import oracle
     wl = build_workload(args.workload, args.frac)
     threads = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
     step = oracle_runner(wl, threads)
@@ -212,7 +222,7 @@ def run_reference(args):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "u8", "data": "synthetic",
-            "config": {"workload": WORKLOAD_NAMES[args.workload], "canonical_bytes": wl.canonical_bytes},
+            "config": run_config(args, wl, oracle.Oracle(wl).n_windows, 1),
             "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": threads, "kind": "oracle",
                              "sample": "%d timed oracle refit steps of the whole workload" % args.steps},
             "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
@@ -363,10 +373,7 @@ def run_gpu(args):
         "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_max / args.steps, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
-        "config": {"workload": WORKLOAD_NAMES[args.workload], "canonical_bytes": N,
-                   "tp": wl.tp, "windows": nw, "parallelism": "replicas" if ws > 1 else "single GPU",
-                   "l2": "inputs larger than L2 (2N = %.2f GB read per encode)" % (2 * N / 1e9)
-                   if 2 * N > 200e6 else "inputs fit in L2"},
+        "config": run_config(args, wl, nw, ws),
         "encode_gbs": round(N / (statistics.mean(enc_ms) * nw / 1e3) / 1e9, 3),
         "apply_gbs": round(N / (statistics.mean(app_ms) * nw / 1e3) / 1e9, 3),
         "encode_kernel_ms": round(statistics.mean(enc_ms), 4),
