@@ -423,64 +423,80 @@ __device__ __forceinline__ void gather_bytes(const EncArgs& A, const Seg* segs, 
     n = make_uint4(nw[0], nw[1], nw[2], nw[3]);
 }
 
-__device__ __forceinline__ void encode_chunk(const EncArgs& A, WarpSmem& W, uint32_t k, int lane)
+// The chunk's stream loop.  kKind 0 serves every chunk; kKind 16 / 8 is the
+// common case compiled on its own: an XOR chunk with 16-byte-aligned pieces
+// and 16- or 8-bit elements, with one piece lookup per step for the warp.
+template <int kKind>
+__device__ __forceinline__ void stream_chunk(const EncArgs& A, WarpSmem& W, const ChunkDesc& cd, const Seg* segs,
+                                             int lane, uint8_t* body, int ncap, uint32_t& changed, Parse& P,
+                                             int& tail, int& np, int& units, bool& spill, bool& bad)
 {
-    const ChunkDesc cd = A.chunks[A.chunk_begin + k];
+    constexpr bool kFast = kKind != 0;
     const int raw = int(cd.raw_len);
     const int nseg = int(cd.src_count);
-    const bool cached = nseg <= kMSegCache;
-    if (cached)
-        for (int i = lane; i < nseg; i += 32) W.segs[i] = A.src[cd.src_begin + i];
-    __syncwarp();
-    const Seg* segs = cached ? W.segs : A.src + cd.src_begin;
-    const bool overwrite = (cd.flags & kResidualFlag) || A.mode == DCR_MODE_OVERWRITE_ONLY;
-    const bool vec = (cd.flags & kSrcVec) != 0;
-    const uint32_t ub = cd.bits == 16 ? 2u : 1u;
-    // records that fit the slot and whose values fit the ring's storage
-    const int ncap = int((kSlotBody - 8) / (2 + ub)) < kValStage / int(ub) ? int((kSlotBody - 8) / (2 + ub))
-                                                                           : kValStage / int(ub);
+    const bool overwrite = !kFast && ((cd.flags & kResidualFlag) || A.mode == DCR_MODE_OVERWRITE_ONLY);
+    const bool vec = kFast || (cd.flags & kSrcVec) != 0;
+    const uint32_t bits = kFast ? uint32_t(kKind) : cd.bits;
+    const uint32_t ub = bits == 16 ? 2u : 1u;
     const int nsteps = (raw + kStep - 1) / kStep;
-    uint8_t* slot = A.slots + size_t(k) * kEncSlot;
-    uint8_t* body = slot + kFrameHdr;
     uint8_t* vstage = reinterpret_cast<uint8_t*>(W.pos);   // overwrite values
     const RingSrc R{W.pos, W.val};
 
     // step s of the chunk into landing stage s % kNS (one commit group per
     // step); each copy instruction covers 512 contiguous bytes
-    int cur = 0;
+    int cur = 0, cur_u = 0;
     auto issue = [&](int s) {
         if (s < nsteps) {
-#pragma unroll
-            for (int g = 0; g < 2; ++g) {
-                const uint32_t q = 512u * g + 16u * lane;   // byte of the step
-                const uint32_t x = uint32_t(s) * kStep + q;
-                const int slot = land_slot(int(q >> 5), int(lane & 1));
-                uint4* lo = &W.land[s % kNS][0][slot];
-                uint4* ln = &W.land[s % kNS][1][slot];
-                if (x >= uint32_t(raw)) {
-                    *lo = *ln = make_uint4(0u, 0u, 0u, 0u);
-                } else if (vec) {
-                    while (cur + 1 < nseg && segs[cur + 1].off <= x) ++cur;
-                    const Seg sg = segs[cur];
+            const uint32_t x0 = uint32_t(s) * kStep;
+            bool whole = false;
+            if constexpr (kFast) {
+                // the whole step inside one piece: one base address for the warp
+                while (cur_u + 1 < nseg && segs[cur_u + 1].off <= x0) ++cur_u;
+                const Seg sg = segs[cur_u];
+                whole = x0 + kStep <= sg.off + sg.len;
+                if (whole) {
                     const uint32_t r = uint32_t(sg.addr >> kShardShift);
-                    const uint64_t a = (sg.addr & kAddrMask) + (x - sg.off);
-                    cp_async16(lo, A.olds[r] + a);
-                    cp_async16(ln, A.news[r] + a);
-                } else {
-                    uint4 o, n;
-                    gather_bytes(A, segs, nseg, cur, x, raw, o, n);
-                    *lo = o;
-                    *ln = n;
+                    const uint64_t a = (sg.addr & kAddrMask) + (x0 - sg.off);
+                    const uint8_t* po = A.olds[r] + a;
+                    const uint8_t* pn = A.news[r] + a;
+#pragma unroll
+                    for (int g = 0; g < 2; ++g) {
+                        const uint32_t q = 512u * g + 16u * lane;
+                        const int slot = land_slot(int(q >> 5), int(lane & 1));
+                        cp_async16(&W.land[s % kNS][0][slot], po + q);
+                        cp_async16(&W.land[s % kNS][1][slot], pn + q);
+                    }
+                }
+            }
+            if (!whole) {
+#pragma unroll
+                for (int g = 0; g < 2; ++g) {
+                    const uint32_t q = 512u * g + 16u * lane;   // byte of the step
+                    const uint32_t x = x0 + q;
+                    const int slot = land_slot(int(q >> 5), int(lane & 1));
+                    uint4* lo = &W.land[s % kNS][0][slot];
+                    uint4* ln = &W.land[s % kNS][1][slot];
+                    if (x >= uint32_t(raw)) {
+                        *lo = *ln = make_uint4(0u, 0u, 0u, 0u);
+                    } else if (vec) {
+                        while (cur + 1 < nseg && segs[cur + 1].off <= x) ++cur;
+                        const Seg sg = segs[cur];
+                        const uint32_t r = uint32_t(sg.addr >> kShardShift);
+                        const uint64_t a = (sg.addr & kAddrMask) + (x - sg.off);
+                        cp_async16(lo, A.olds[r] + a);
+                        cp_async16(ln, A.news[r] + a);
+                    } else if constexpr (!kFast) {
+                        uint4 o, n;
+                        gather_bytes(A, segs, nseg, cur, x, raw, o, n);
+                        *lo = o;
+                        *ln = n;
+                    }
                 }
             }
         }
         cp_async_commit();
     };
 
-    uint32_t changed = 0;
-    Parse P{-1, 0ull, 0, 0, 0u};
-    int tail = 0, np = 0, units = 0;
-    bool spill = false, bad = false;
     const uint32_t lt = (1u << lane) - 1u;
 #pragma unroll
     for (int s = 0; s < kNS - 1; ++s) issue(s);
@@ -500,9 +516,9 @@ __device__ __forceinline__ void encode_chunk(const EncArgs& A, WarpSmem& W, uint
             m0 = xor4(W.land[s % kNS][0][s0], n0);
             m1 = xor4(W.land[s % kNS][0][s1], n1);
             z = nz32(m0, m1);
-            if (cd.bits == 16) {
+            if (bits == 16) {
                 changed += __popc((z | (z >> 1)) & 0x55555555u);
-            } else if (cd.bits == 8) {
+            } else if (bits == 8) {
                 changed += __popc(z);
             } else {
                 changed += nibbles_nz(m0.x) + nibbles_nz(m0.y) + nibbles_nz(m0.z) + nibbles_nz(m0.w) +
@@ -580,6 +596,38 @@ __device__ __forceinline__ void encode_chunk(const EncArgs& A, WarpSmem& W, uint
         }
         if (!more) break;
     }
+}
+
+__device__ __forceinline__ void encode_chunk(const EncArgs& A, WarpSmem& W, uint32_t k, int lane)
+{
+    const ChunkDesc cd = A.chunks[A.chunk_begin + k];
+    const int raw = int(cd.raw_len);
+    const int nseg = int(cd.src_count);
+    const bool cached = nseg <= kMSegCache;
+    if (cached)
+        for (int i = lane; i < nseg; i += 32) W.segs[i] = A.src[cd.src_begin + i];
+    __syncwarp();
+    const Seg* segs = cached ? W.segs : A.src + cd.src_begin;
+    const bool overwrite = (cd.flags & kResidualFlag) || A.mode == DCR_MODE_OVERWRITE_ONLY;
+    const bool vec = (cd.flags & kSrcVec) != 0;
+    const uint32_t ub = cd.bits == 16 ? 2u : 1u;
+    // records that fit the slot and whose values fit the ring's storage
+    const int ncap = int((kSlotBody - 8) / (2 + ub)) < kValStage / int(ub) ? int((kSlotBody - 8) / (2 + ub))
+                                                                           : kValStage / int(ub);
+    uint8_t* slot = A.slots + size_t(k) * kEncSlot;
+    uint8_t* body = slot + kFrameHdr;
+    const uint8_t* vstage = reinterpret_cast<const uint8_t*>(W.pos);   // overwrite values
+
+    uint32_t changed = 0;
+    Parse P{-1, 0ull, 0, 0, 0u};
+    int tail = 0, np = 0, units = 0;
+    bool spill = false, bad = false;
+    if (!overwrite && vec && cd.bits == 16)
+        stream_chunk<16>(A, W, cd, segs, lane, body, ncap, changed, P, tail, np, units, spill, bad);
+    else if (!overwrite && vec && cd.bits == 8)
+        stream_chunk<8>(A, W, cd, segs, lane, body, ncap, changed, P, tail, np, units, spill, bad);
+    else
+        stream_chunk<0>(A, W, cd, segs, lane, body, ncap, changed, P, tail, np, units, spill, bad);
     changed = __reduce_add_sync(kFull, changed);
     if (lane == 0 && changed) {
         atomicAdd(&A.counts[cd.tensor], (unsigned long long)changed);
