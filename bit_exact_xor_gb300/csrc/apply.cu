@@ -23,12 +23,15 @@
 //                 arena and check every match against the sorted list of
 //                 non-zero output bytes so far.  A frame that fails part-way is
 //                 undone (XOR is self-inverse) before it is reported.
-//   defer_kernel  one CTA per remaining LZ4 frame (any valid block, e.g. from
-//                 the CPU oracle, and ZSRC frames too large for the warp
-//                 path): full decode into a 64 KiB shared buffer with
-//                 warp-parallel literal and match copies (a ZSRC frame whose
-//                 match copies a non-zero byte is rejected), then the XOR
-//                 sweep.
+//   big_kernel    one warp per ZSRC frame too large for apply_kernel's
+//                 body cache or non-zero list (denser masks): the same walk
+//                 with the body read from global memory and the matches
+//                 checked against a bitmap of the non-zero output bytes.
+//   defer_kernel  one CTA per general LZ4 frame (any valid block, e.g. from
+//                 the CPU oracle): full decode into a 64 KiB shared buffer
+//                 with warp-parallel literal and match copies (a ZSRC frame
+//                 whose match copies a non-zero byte is rejected), then the
+//                 XOR sweep.
 //   pending_kernel  counts framed chunks that are not DONE for the target
 //                 version (the commit rule).
 #include <cuda_runtime.h>
@@ -62,7 +65,8 @@ struct ApplyArgs {
     uint8_t* target;
     unsigned long long* state;
     ApplyScratch* sc;
-    uint32_t* defer;
+    uint32_t* defer;          // deferred frames: general LZ4 from the front, large ZSRC from the back
+    uint32_t defer_len;
     uint64_t plan_hash;
     uint64_t version;
     uint64_t abort_at;
@@ -87,6 +91,17 @@ struct __align__(16) AWarp {
     uint32_t nxt[kWin];
     uint32_t r_ip[32];
 };
+
+// big_kernel: one warp's shared memory.  Large ZSRC frames are read from
+// global memory and their matches checked against a bitmap of the non-zero
+// output bytes, which has no capacity limit.
+struct __align__(16) BWarp {
+    uint32_t bits[kChunk / 32];
+    uint32_t nxt[kWin];
+    uint32_t r_ip[32];
+};
+constexpr int kBWarps = 8;
+constexpr int kBThreads = 32 * kBWarps;
 
 struct __align__(16) ASmem {
     AWarp w[kAWarps];
@@ -302,11 +317,20 @@ __device__ __forceinline__ uint32_t seq_end(const uint8_t* src, uint32_t n, uint
 // breaks its ZSRC promise, 2 if it holds more non-zero bytes than the list
 // (the caller defers it); in the last two cases the partial apply has been
 // undone.
+//
+// kBitmap (big_kernel): the non-zero output bytes are kept as a bitmap over
+// the chunk instead of a sorted list, so there is no capacity limit, and src
+// may be the frame body in global memory.
+template <bool kBitmap, class WS>
 __device__ int zsrc_apply(const ApplyArgs& A, const ChunkDesc& cd, const Seg* ds, const uint8_t* src,
-                          uint32_t n, uint32_t raw, uint32_t lim, AWarp& W, int lane)
+                          uint32_t n, uint32_t raw, uint32_t lim, WS& W, int lane)
 {
     const bool one = cd.dst_count == 1;
     const uint64_t base = one ? ds[0].addr - ds[0].off : 0ull;   // single receiver piece
+    if constexpr (kBitmap) {
+        for (uint32_t w = lane; w < (raw + 31) / 32; w += 32) W.bits[w] = 0;
+        __syncwarp();
+    }
     uint32_t ip = 0, op = 0;      // next sequence in the body; its output position
     uint32_t nev = 0, runs = 0;   // listed positions, literal runs applied
     int status = 1;
@@ -383,38 +407,58 @@ __device__ int zsrc_apply(const ApplyArgs& A, const ChunkDesc& cd, const Seg* ds
         }
         op += __shfl_sync(kFull, lincl, 31);
         ip = cur;
-        // literals: XOR into the receiver and list the non-zero ones
-        uint32_t c = 0;
-        for (uint32_t q = 0; q < ll; ++q) c += src[ipl + q] != 0;
-        const uint32_t incl = warp_incl_sum(c, lane);
-        const uint32_t tot = __shfl_sync(kFull, incl, 31);
-        if (nev + tot > uint32_t(kAEvCap)) {
-            status = 2;
-            break;
-        }
-        uint32_t at = nev + incl - c;
-        for (uint32_t q = 0; q < ll; ++q) {
-            const uint32_t b = src[ipl + q];
-            if (b) {
-                const uint32_t x = opl + q;
-                W.ev[at++] = uint16_t(x);
-                if (x < lim) xor_byte(A.target, one ? base + x : dst_of(ds, cd.dst_count, x), b);
+        // literals: XOR into the receiver and record the non-zero ones
+        if constexpr (kBitmap) {
+            for (uint32_t q = 0; q < ll; ++q) {
+                const uint32_t b = src[ipl + q];
+                if (b) {
+                    const uint32_t x = opl + q;
+                    atomicOr(&W.bits[x >> 5], 1u << (x & 31));
+                    if (x < lim) xor_byte(A.target, one ? base + x : dst_of(ds, cd.dst_count, x), b);
+                }
             }
+        } else {
+            uint32_t c = 0;
+            for (uint32_t q = 0; q < ll; ++q) c += src[ipl + q] != 0;
+            const uint32_t incl = warp_incl_sum(c, lane);
+            const uint32_t tot = __shfl_sync(kFull, incl, 31);
+            if (nev + tot > uint32_t(kAEvCap)) {
+                status = 2;
+                break;
+            }
+            uint32_t at = nev + incl - c;
+            for (uint32_t q = 0; q < ll; ++q) {
+                const uint32_t b = src[ipl + q];
+                if (b) {
+                    const uint32_t x = opl + q;
+                    W.ev[at++] = uint16_t(x);
+                    if (x < lim) xor_byte(A.target, one ? base + x : dst_of(ds, cd.dst_count, x), b);
+                }
+            }
+            nev += tot;
         }
-        nev += tot;
         runs += cnt;
         __syncwarp();
         // the match copies [mop - off, mop - off + min(ml, off)), repeated
         bool viol = false;
         if (mine && !lastseq) {
             const uint32_t s0 = mop - off, e0 = s0 + (ml < off ? ml : off);
-            uint32_t lo = 0, hi = nev;   // first listed position >= s0
-            while (lo < hi) {
-                const uint32_t mid = (lo + hi) >> 1;
-                if (W.ev[mid] < s0) lo = mid + 1;
-                else hi = mid;
+            if constexpr (kBitmap) {
+                for (uint32_t w = s0 >> 5; w <= (e0 - 1) >> 5 && !viol; ++w) {
+                    const uint32_t a = (w << 5) > s0 ? 0u : s0 - (w << 5);
+                    const uint32_t b = ((w + 1) << 5) < e0 ? 32u : e0 - (w << 5);
+                    const uint32_t m = (b == 32 ? 0xFFFFFFFFu : ((1u << b) - 1)) & ~((1u << a) - 1);
+                    viol = (W.bits[w] & m) != 0;
+                }
+            } else {
+                uint32_t lo = 0, hi = nev;   // first listed position >= s0
+                while (lo < hi) {
+                    const uint32_t mid = (lo + hi) >> 1;
+                    if (W.ev[mid] < s0) lo = mid + 1;
+                    else hi = mid;
+                }
+                viol = lo < nev && W.ev[lo] < e0;
             }
-            viol = lo < nev && W.ev[lo] < e0;
         }
         if (__any_sync(kFull, viol)) {
             status = 0;
@@ -493,10 +537,14 @@ __global__ void __launch_bounds__(kAThreads) apply_kernel(ApplyArgs A)
                 if (!got && !to) atomicAdd(&A.sc->skipped, 1ull);
             }
             if (!__shfl_sync(0xffffffffu, got, 0)) continue;
-            // general LZ4 frames, and ZSRC frames larger than the body cache,
-            // go to the full decode
-            if (kind == kXorLz4 && (!(fflags & kFrameZsrc) || bl > uint32_t(kBodyCache))) {
+            // general LZ4 frames go to the full decode, ZSRC frames larger
+            // than the body cache to big_kernel
+            if (kind == kXorLz4 && !(fflags & kFrameZsrc)) {
                 if (lane == 0) A.defer[atomicAdd(&A.sc->n_defer, 1u)] = f;
+                continue;
+            }
+            if (kind == kXorLz4 && bl > uint32_t(kBodyCache)) {
+                if (lane == 0) A.defer[A.defer_len - 1 - atomicAdd(&A.sc->n_big, 1u)] = f;
                 continue;
             }
         }
@@ -518,10 +566,10 @@ __global__ void __launch_bounds__(kAThreads) apply_kernel(ApplyArgs A)
                 reinterpret_cast<uint4*>(W.body)[v] = ld_nc16(body + 16 * v);
             for (uint32_t x = (bl & ~15u) + lane; x < bl; x += 32) W.body[x] = body[x];
             __syncwarp();
-            const int r = zsrc_apply(A, cd, ds, W.body, bl, raw, lim, W, lane);
+            const int r = zsrc_apply<false>(A, cd, ds, W.body, bl, raw, lim, W, lane);
             __syncwarp();   // the body cache is reused by the next frame
-            if (r == 2) {
-                if (lane == 0) A.defer[atomicAdd(&A.sc->n_defer, 1u)] = f;
+            if (r == 2) {   // more non-zero bytes than the list holds (undone)
+                if (lane == 0) A.defer[A.defer_len - 1 - atomicAdd(&A.sc->n_big, 1u)] = f;
                 continue;
             }
             good = r == 1;
@@ -683,6 +731,49 @@ __global__ void __launch_bounds__(kDThreads) defer_kernel(ApplyArgs A)
     }
 }
 
+// Large ZSRC frames (body beyond the cache, or more non-zero bytes than the
+// list holds): one warp per frame, body read from global memory, matches
+// checked against a bitmap of the non-zero output bytes.  The frames were
+// validated and claimed by apply_kernel.
+__global__ void __launch_bounds__(kBThreads) big_kernel(ApplyArgs A)
+{
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    BWarp& W = reinterpret_cast<BWarp*>(smem_raw)[threadIdx.x >> 5];
+    const int lane = threadIdx.x & 31;
+    if (!A.sc->hdr_ok) return;
+    const uint8_t* p = A.payload;
+    const uint64_t total = ld64(p + 56), nf = ld64(p + 48), idx_off = total - 8 * nf;
+    const uint64_t V = ld64(p + 24);
+    const uint32_t nbig = A.sc->n_big;   // final: written by apply_kernel only
+    for (;;) {
+        uint32_t j = 0;
+        if (lane == 0) j = atomicAdd(&A.sc->big_ticket, 1u);
+        j = __shfl_sync(kFull, j, 0);
+        if (j >= nbig) break;
+        const uint32_t f = A.defer[A.defer_len - 1 - j];
+        const uint64_t fo = ld64(p + idx_off + 8ull * f);
+        const uint4 h0 = ld_nc16(p + fo), h1 = ld_nc16(p + fo + 16);
+        const uint32_t c = h0.z, raw = h0.w, bl = h1.x;
+        const ChunkDesc cd = A.chunks[c];
+        const bool cut = uint64_t(f) == A.abort_at;
+        const uint32_t ub = cd.bits == 16 ? 2u : 1u;
+        uint32_t lim = cut ? (A.split < raw ? A.split : raw) : raw;
+        lim -= lim % ub;
+        const int r = zsrc_apply<true>(A, cd, A.dst + cd.dst_begin, p + fo + kFrameHdr, bl, raw, lim, W, lane);
+        __syncwarp();   // the bitmap is reused by the next frame
+        if (lane == 0) {
+            if (r != 1) {
+                report(A.sc, DCR_ERR_CORRUPT);
+            } else {
+                atomicAdd(&A.sc->applied, 1ull);
+                __threadfence();
+                if (cut) A.sc->aborted = 1;
+                else atomicExch(&A.state[c], (V << 2) | kDone);
+            }
+        }
+    }
+}
+
 // Commit rule: every chunk with a frame in the stream is DONE for the target.
 __global__ void pending_kernel(ApplyArgs A)
 {
@@ -719,8 +810,15 @@ int apply_kernel_config(KernelConfig* kc)
     if (e == cudaSuccess)
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&kc->defer_blocks_per_sm, defer_kernel, kDThreads,
                                                           kChunk);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(big_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 int(sizeof(BWarp) * kBWarps));
+    if (e == cudaSuccess)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&kc->big_blocks_per_sm, big_kernel, kBThreads,
+                                                          sizeof(BWarp) * kBWarps);
     if (e != cudaSuccess) return cuda_error(e, "apply kernel configuration");
     if (kc->apply_blocks_per_sm < 1) kc->apply_blocks_per_sm = 1;
+    if (kc->big_blocks_per_sm < 1) kc->big_blocks_per_sm = 1;
     if (kc->defer_blocks_per_sm < 1) kc->defer_blocks_per_sm = 1;
     return DCR_OK;
 }
@@ -740,6 +838,7 @@ int apply_launch(const dcr_plan* P, dcr_recv_state* st, const void* payload, siz
     A.state = reinterpret_cast<unsigned long long*>(st->d_chunk_state);
     A.sc = st->d_scratch;
     A.defer = st->d_defer;
+    A.defer_len = uint32_t(P->max_window_chunks + 1);
     A.plan_hash = P->hash;
     A.version = st->version;
     A.abort_at = abort_at;
@@ -751,6 +850,7 @@ int apply_launch(const dcr_plan* P, dcr_recv_state* st, const void* payload, siz
     apply_kernel<<<sms * P->kc.apply_blocks_per_sm, kAThreads, sizeof(ASmem), s>>>(A);
     if (P->profiling) cudaEventRecord(P->ev[4], s);
     defer_kernel<<<sms * P->kc.defer_blocks_per_sm, kDThreads, kChunk, s>>>(A);
+    big_kernel<<<sms * P->kc.big_blocks_per_sm, kBThreads, sizeof(BWarp) * kBWarps, s>>>(A);
     if (P->profiling) cudaEventRecord(P->ev[5], s);
     pending_kernel<<<sms, 256, 0, s>>>(A);
     if (P->profiling) cudaEventRecord(P->ev[6], s);
@@ -830,6 +930,7 @@ int apply_launch_noalloc(const dcr_plan* P, dcr_recv_state* st, const void* payl
     A.state = reinterpret_cast<unsigned long long*>(st->d_chunk_state);
     A.sc = static_cast<ApplyScratch*>(base);
     A.defer = reinterpret_cast<uint32_t*>(static_cast<unsigned char*>(base) + kNoallocHead);
+    A.defer_len = kNoallocMaxChunks + 1;
     A.plan_hash = P->hash;
     A.version = st->version;
     A.abort_at = DCR_NO_FAULT;
@@ -839,6 +940,7 @@ int apply_launch_noalloc(const dcr_plan* P, dcr_recv_state* st, const void* payl
     const int sms = P->kc.num_sms;
     apply_kernel<<<sms * P->kc.apply_blocks_per_sm, kAThreads, sizeof(ASmem), s>>>(A);
     defer_kernel<<<sms * P->kc.defer_blocks_per_sm, kDThreads, kChunk, s>>>(A);
+    big_kernel<<<sms * P->kc.big_blocks_per_sm, kBThreads, sizeof(BWarp) * kBWarps, s>>>(A);
     pending_kernel<<<sms, 256, 0, s>>>(A);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_error(e, "apply launch");

@@ -96,12 +96,14 @@ struct ApplyScratch {
     uint32_t defer_ticket;
     uint32_t aborted;
     uint32_t window;
-    uint32_t pad;
+    uint32_t n_big;         // large ZSRC frames, listed from the end of the deferred list
     unsigned long long applied;
     unsigned long long skipped;
     unsigned long long pending;
     uint64_t target_version;
     uint64_t n_frames;
+    uint32_t big_ticket;
+    uint32_t pad;
 };
 
 // Chunk state of a receiver: (target_version << 2) | state.
@@ -119,6 +121,7 @@ struct KernelConfig {
     int spill_blocks_per_sm = 0;
     int apply_blocks_per_sm = 0;
     int defer_blocks_per_sm = 0;
+    int big_blocks_per_sm = 0;
 };
 
 // host entry points of the kernel translation units

@@ -290,10 +290,12 @@ def test_frame_failing_late_leaves_its_chunk_untouched():
     assert rc == dcr.OK and st.version == 1 and np.array_equal(c.host(t), c.exp)
 
 
-def test_zsrc_flag_is_verified():
+@pytest.mark.parametrize("frac", [None, 0.05])
+def test_zsrc_flag_is_verified(frac):
     # a greedy (oracle) block whose matches copy non-zero bytes, relabelled
-    # as ZSRC, must be rejected rather than applied as zeros
-    c = Case(configs.mini(1))
+    # as ZSRC, must be rejected rather than applied as zeros; at 5 % change the
+    # bodies are larger than the warp path's cache (the large-frame kernel)
+    c = Case(configs.mini(1) if frac is None else configs.mini(4), frac=frac)
     o, _ = c.orc.encode(c.olds, c.news)
     _, frames, _ = parse(o)
     lied = o.copy()
@@ -304,7 +306,10 @@ def test_zsrc_flag_is_verified():
             if oracle.lz4_decode(f["body"], f["raw_len"], zsrc=True) is None and m is not None:
                 lied[f["offset"] + 6] = 1
                 n += 1
+                big = f["body_len"] > 3072 if frac else False
     assert n > 0
+    if frac:
+        assert big
     t = c.target()
     rc, _ = dcr.apply(c.plan, dcr.RecvState(c.plan, 0), torch.from_numpy(lied).cuda(), o.size, t)
     assert rc == dcr.ERR_CORRUPT
