@@ -271,7 +271,7 @@ def run_gpu(args):
     st = dcr.RecvState(plan, 0)
     ver = [0]
     d = [0]
-    enc_ms, app_ms, sizes, changed = [], [], [], []
+    enc_ms, app_ms, rest_ms, sizes, changed = [], [], [], [], []
 
     def step(record):
         a, b = (olds, news) if d[0] == 0 else (news, olds)
@@ -286,6 +286,7 @@ def run_gpu(args):
             if record:
                 enc_ms.append(p1.encode_ms)
                 app_ms.append(p2.apply_ms + p2.defer_ms)
+                rest_ms.append(p1.finalize_ms + p2.pending_ms)
                 sizes.append(size)
                 changed.append(sum(cnt))
         ver[0] += 1
@@ -378,6 +379,11 @@ def run_gpu(args):
         "apply_gbs": round(N / (statistics.mean(app_ms) * nw / 1e3) / 1e9, 3),
         "encode_kernel_ms": round(statistics.mean(enc_ms), 4),
         "apply_kernel_ms": round(statistics.mean(app_ms), 4),
+        # the rest of the library's GPU time per window: frame scan, copy and
+        # spill kernels after the encode, commit check after the apply
+        "other_kernels_ms": round(statistics.mean(rest_ms), 4),
+        # apply against the dense byte model (reads N + P, writes N)
+        "apply_model_frac": round((2 * N / nw + P) / (statistics.mean(app_ms) / 1e3) / 1e9 / peak, 4),
         "payload_bytes": int(P), "changed_values": int(statistics.mean(changed)),
         "roofline": {"bound": "hbm", "kernel": "encode_kernel", "achieved": round(achieved, 1),
                      "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
