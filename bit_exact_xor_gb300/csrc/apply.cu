@@ -81,6 +81,7 @@ struct Hdr {
 constexpr uint32_t kWin = 128;                // candidate sequence starts per walk window
 constexpr uint32_t kEndFinal = 0x80000000u;   // the sequence is the block's last
 constexpr uint32_t kEndBad = 0x7FFFFFFFu;     // no valid sequence starts here
+constexpr uint8_t kStop = 0xFF;               // jump: the chain stops (end, error, window left)
 
 // one warp's shared memory: the frame body, the sorted positions of its
 // non-zero output bytes so far, where a sequence starting at each byte of the
@@ -90,6 +91,8 @@ struct __align__(16) AWarp {
     uint16_t ev[kAEvCap];
     uint32_t nxt[kWin];
     uint32_t r_ip[32];
+    uint8_t jmp[3][kWin];    // window-relative start 1, 2 and 4 sequences on, or kStop
+    uint32_t base[8];
 };
 
 // big_kernel: one warp's shared memory.  Large ZSRC frames are read from
@@ -99,6 +102,8 @@ struct __align__(16) BWarp {
     uint32_t bits[kChunk / 32];
     uint32_t nxt[kWin];
     uint32_t r_ip[32];
+    uint8_t jmp[3][kWin];
+    uint32_t base[8];
 };
 constexpr int kBWarps = 8;
 constexpr int kBThreads = 32 * kBWarps;
@@ -305,10 +310,11 @@ __device__ __forceinline__ uint32_t seq_end(const uint8_t* src, uint32_t n, uint
 }
 
 // The warp takes the block a window of kWin body bytes at a time: every lane
-// works out where a sequence starting at each of its window bytes would end,
-// lane 0 follows the chain of ends from the current sequence (one shared
-// load per sequence), and up to 32 sequences found that way are decoded one
-// per lane, their output positions given by a warp prefix sum.  Then each
+// works out where a sequence starting at each of its window bytes would end
+// (and, in two more passes, where the sequence two and four on starts), lane
+// 0 follows the chain from the current sequence four sequences per shared
+// load, and up to 32 sequences found that way are decoded one per lane, their
+// output positions given by a warp prefix sum.  Then each
 // lane XORs the non-zero literal bytes of its sequence into the receiver,
 // lists their positions (the warp's list of non-zero output bytes stays
 // sorted, since literal runs come in output order), and checks that its
@@ -339,23 +345,62 @@ __device__ int zsrc_apply(const ApplyArgs& A, const ChunkDesc& cd, const Seg* ds
 #pragma unroll
         for (uint32_t j = 0; j < kWin / 32; ++j) e[j] = seq_end(src, n, ip + 32 * j + lane);
 #pragma unroll
-        for (uint32_t j = 0; j < kWin / 32; ++j) W.nxt[32 * j + lane] = e[j];
+        for (uint32_t j = 0; j < kWin / 32; ++j) {
+            const uint32_t x = e[j];
+            W.nxt[32 * j + lane] = x;
+            W.jmp[0][32 * j + lane] =
+                (x == kEndBad || (x & kEndFinal) || x >= n || x - ip >= kWin) ? kStop : uint8_t(x - ip);
+        }
         __syncwarp();
-        uint32_t cnt = 0, fin = 0, bad = 0, cur = ip;
+        // two and four sequences on, for every window byte
+#pragma unroll
+        for (int t = 1; t < 3; ++t) {
+            uint8_t y[kWin / 32];
+#pragma unroll
+            for (uint32_t j = 0; j < kWin / 32; ++j) {
+                const uint8_t a = W.jmp[t - 1][32 * j + lane];
+                y[j] = a == kStop ? kStop : W.jmp[t - 1][a];
+            }
+#pragma unroll
+            for (uint32_t j = 0; j < kWin / 32; ++j) W.jmp[t][32 * j + lane] = y[j];
+            __syncwarp();
+        }
+        // lane 0 follows the chain four sequences at a time, then one at a
+        // time for its last few; the other lanes fill in the skipped starts
+        uint32_t nb = 0, cnt = 0, fin = 0, bad = 0, cur = ip;
         if (lane == 0) {
-            while (cnt < 32 && cur < ip + kWin) {
-                const uint32_t x = W.nxt[cur - ip];
-                if (x == kEndBad) { bad = 1; break; }
-                W.r_ip[cnt++] = cur;
-                cur = x & ~kEndFinal;
-                if (x & kEndFinal) { fin = 1; break; }
-                if (cur >= n) { bad = 1; break; }   // a block ends with a literals-only sequence
+            uint32_t p = 0;
+            while (nb < 8 && W.jmp[2][p] != kStop) {
+                W.base[nb++] = p;
+                p = W.jmp[2][p];
+            }
+            cnt = 4 * nb;
+            if (nb == 8) {
+                cur = ip + p;
+            } else {
+                for (int t = 0; t < 4; ++t) {
+                    const uint32_t x = W.nxt[p];
+                    if (x == kEndBad) { bad = 1; break; }
+                    W.r_ip[cnt++] = ip + p;
+                    if (x & kEndFinal) { fin = 1; cur = x & ~kEndFinal; break; }
+                    if (x >= n) { bad = 1; break; }   // a block ends with a literals-only sequence
+                    if (x - ip >= kWin) { cur = x; break; }
+                    p = x - ip;
+                }
             }
         }
+        nb = __shfl_sync(kFull, nb, 0);
         cnt = __shfl_sync(kFull, cnt, 0);
         fin = __shfl_sync(kFull, fin, 0);
         bad = __shfl_sync(kFull, bad, 0);
         cur = __shfl_sync(kFull, cur, 0);
+        __syncwarp();
+        if (lane < int(4 * nb)) {
+            const uint32_t b = W.base[lane >> 2];
+            const uint32_t k = lane & 3;
+            const uint32_t q = k == 0 ? b : k == 1 ? W.jmp[0][b] : k == 2 ? W.jmp[1][b] : W.jmp[0][W.jmp[1][b]];
+            W.r_ip[lane] = ip + q;
+        }
         if (bad) {
             status = 0;
             break;
