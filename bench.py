@@ -389,7 +389,7 @@ def run_gpu(args):
                      "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                      "peak_source": peak_kind,
                      "algorithmic_bytes_per_launch": int(alg_bytes)},
-        "gpu_launches": 7 * nw * args.steps,
+        "gpu_launches": 8 * nw * args.steps,
         "clocks": clocks,
     }
     if e2e:
