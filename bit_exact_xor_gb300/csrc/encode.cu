@@ -428,20 +428,17 @@ __device__ __forceinline__ void gather_bytes(const EncArgs& A, const Seg* segs, 
     n = make_uint4(nw[0], nw[1], nw[2], nw[3]);
 }
 
-// The chunk's stream loop.  kKind 0 serves every chunk; kKind 16 / 8 is the
-// common case compiled on its own: an XOR chunk with 16-byte-aligned pieces
-// and 16- or 8-bit elements, with one piece lookup per step for the warp.
-template <int kKind>
+// The stream loop of any chunk (overwrite records, 4-bit elements, pieces
+// that are not 16-byte aligned); stream_fast below is the common case.
 __device__ __forceinline__ void stream_chunk(const EncArgs& A, WarpSmem& W, const ChunkDesc& cd, const Seg* segs,
                                              int lane, uint8_t* body, int ncap, uint32_t& changed, Parse& P,
                                              int& tail, int& np, int& units, bool& spill, bool& bad)
 {
-    constexpr bool kFast = kKind != 0;
     const int raw = int(cd.raw_len);
     const int nseg = int(cd.src_count);
-    const bool overwrite = !kFast && ((cd.flags & kResidualFlag) || A.mode == DCR_MODE_OVERWRITE_ONLY);
-    const bool vec = kFast || (cd.flags & kSrcVec) != 0;
-    const uint32_t bits = kFast ? uint32_t(kKind) : cd.bits;
+    const bool overwrite = (cd.flags & kResidualFlag) || A.mode == DCR_MODE_OVERWRITE_ONLY;
+    const bool vec = (cd.flags & kSrcVec) != 0;
+    const uint32_t bits = cd.bits;
     const uint32_t ub = bits == 16 ? 2u : 1u;
     const int nsteps = (raw + kStep - 1) / kStep;
     uint8_t* vstage = reinterpret_cast<uint8_t*>(W.pos);   // overwrite values
@@ -449,31 +446,11 @@ __device__ __forceinline__ void stream_chunk(const EncArgs& A, WarpSmem& W, cons
 
     // step s of the chunk into landing stage s % kNS (one commit group per
     // step); each copy instruction covers 512 contiguous bytes
-    int cur = 0, cur_u = 0;
+    int cur = 0;
     auto issue = [&](int s) {
         if (s < nsteps) {
             const uint32_t x0 = uint32_t(s) * kStep;
-            bool whole = false;
-            if constexpr (kFast) {
-                // the whole step inside one piece: one base address for the warp
-                while (cur_u + 1 < nseg && segs[cur_u + 1].off <= x0) ++cur_u;
-                const Seg sg = segs[cur_u];
-                whole = x0 + kStep <= sg.off + sg.len;
-                if (whole) {
-                    const uint32_t r = uint32_t(sg.addr >> kShardShift);
-                    const uint64_t a = (sg.addr & kAddrMask) + (x0 - sg.off);
-                    const uint8_t* po = A.olds[r] + a;
-                    const uint8_t* pn = A.news[r] + a;
-#pragma unroll
-                    for (int g = 0; g < 2; ++g) {
-                        const uint32_t q = 512u * g + 16u * lane;
-                        const int slot = land_slot(int(q >> 5), int(lane & 1));
-                        cp_async16(&W.land[s % kNS][0][slot], po + q);
-                        cp_async16(&W.land[s % kNS][1][slot], pn + q);
-                    }
-                }
-            }
-            if (!whole) {
+            {
 #pragma unroll
                 for (int g = 0; g < 2; ++g) {
                     const uint32_t q = 512u * g + 16u * lane;   // byte of the step
@@ -490,7 +467,7 @@ __device__ __forceinline__ void stream_chunk(const EncArgs& A, WarpSmem& W, cons
                         const uint64_t a = (sg.addr & kAddrMask) + (x - sg.off);
                         cp_async16(lo, A.olds[r] + a);
                         cp_async16(ln, A.news[r] + a);
-                    } else if constexpr (!kFast) {
+                    } else {
                         uint4 o, n;
                         gather_bytes(A, segs, nseg, cur, x, raw, o, n);
                         *lo = o;
@@ -764,7 +741,7 @@ __device__ __forceinline__ void encode_chunk(const EncArgs& A, WarpSmem& W, uint
     else if (!overwrite && vec && cd.bits == 8)
         stream_fast<8>(A, W, cd, segs, lane, body, changed, P, tail, np, spill, bad);
     else
-        stream_chunk<0>(A, W, cd, segs, lane, body, ncap, changed, P, tail, np, units, spill, bad);
+        stream_chunk(A, W, cd, segs, lane, body, ncap, changed, P, tail, np, units, spill, bad);
     changed = __reduce_add_sync(kFull, changed);
     if (lane == 0 && changed) {
         atomicAdd(&A.counts[cd.tensor], (unsigned long long)changed);
