@@ -66,7 +66,9 @@ struct EncScratch {
     uint64_t total;     // stream bytes
     uint64_t n_frames;
     uint64_t changed;   // changed elements in the window
-    uint32_t n_spill;   // chunks whose frame body the spill kernel writes
+    uint32_t n_spill;        // chunks whose frame body did not fit its slot
+    uint32_t spill_ticket;   // restream pass: next spill record
+    uint32_t n_deep;         // spill records left to the spill kernel
     uint32_t pad;
 };
 
@@ -76,8 +78,10 @@ struct EncScratch {
 constexpr uint32_t kEncSlot = 6144;
 constexpr uint32_t kSpilled = 1u << 31;   // frame-size flag: body not in the slot
 
-// A chunk whose frame is sized but whose body did not fit its slot: the
-// spill kernel re-derives it and writes the frame into the stream.
+// A chunk whose frame is sized but whose body did not fit its slot: a
+// restream pass re-derives it and writes the frame into the stream (the
+// spill kernel takes raw and dense frames and LZ4 chunks with very long
+// literal runs).
 struct SpillRec {
     uint32_t k;          // window-relative chunk
     uint32_t kind;       // FrameKind
@@ -118,6 +122,7 @@ struct Part {
 struct KernelConfig {
     int num_sms = 0;
     int enc_blocks_per_sm = 0;
+    int restream_blocks_per_sm = 0;
     int spill_blocks_per_sm = 0;
     int apply_blocks_per_sm = 0;
     int defer_blocks_per_sm = 0;
@@ -169,6 +174,7 @@ struct dcr_plan {
     uint64_t* d_lb = nullptr;
     uint32_t* d_fsize = nullptr;
     dcr::SpillRec* d_spill = nullptr;  // max_window_chunks
+    uint32_t* d_deep = nullptr;        // max_window_chunks spill record ids
     uint8_t* d_slots = nullptr;        // max_window_chunks * kEncSlot frame slots
     void* h_enc = nullptr;  // pinned mirror of the scratch head
     // kernel timing (dcr_plan_set_profiling)

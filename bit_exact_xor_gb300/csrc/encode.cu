@@ -1,6 +1,7 @@
-// Sender hot path: per window, one persistent kernel encodes every chunk,
-// a second one writes the few frame bodies that did not fit on chip, and a
-// third writes the frame index and the stream header.
+// Sender hot path: per window, one persistent kernel encodes every chunk
+// into per-chunk slots, a scan places the frames and writes the stream
+// header, a copy pass moves the slots into the stream, and two more passes
+// write the frame bodies that outgrew their slots.
 //
 // Per 64 KiB canonical chunk the encoder gathers old and new through the
 // plan's shard->canonical pieces, forms mask = old XOR new, counts changed
@@ -26,20 +27,29 @@
 // straight into the chunk's frame slot in device scratch.  Overwrite chunks
 // write their records there instead.  A chunk whose body or pending literals
 // outgrow the slot or the ring is sized all the same (the parse carries on
-// without writing) and is listed for the spill kernel.  No warp waits for
+// without writing) and is listed for the restream pass.  No warp waits for
 // another: frame sizes go to a per-chunk array.
 //
 // scan_kernel / copy_kernel.  One CTA scans the frame sizes into offsets
 // and writes the stream header; then one warp per chunk copies its slot to
 // its place in the stream with 16-byte stores and writes its index entry.
 //
-// spill_kernel.  One CTA per listed chunk: 16 warps gather the mask into
-// shared memory (64 KiB plus a bitmap of its non-zero bytes), then one warp
-// re-runs the same parse over the bitmap's event list, reading literal bytes
-// from the mask, and writes the frame at its place in the stream; raw and
-// dense frames are copied by the whole CTA.  Both kernels call the same
-// parse_group with groups of 32 consecutive events from the first one, so
-// their sizes agree by construction (a disagreement is reported).
+// restream_kernel.  One warp per chunk whose body outgrew its slot (masks
+// above a few percent change): it runs the chunk's stream loop again, now
+// that the frame's offset and size are known, and the parse writes the body
+// straight into the stream.  Same loop, same groups, so the sizes agree by
+// construction (checked).  What it cannot write (raw and dense frames, LZ4
+// chunks whose pending literals outgrow the event ring) it lists for
+// spill_kernel.
+//
+// spill_kernel.  One CTA per chunk listed by restream_kernel: 16 warps
+// gather the mask into shared memory (64 KiB plus a bitmap of its non-zero
+// bytes), then one warp re-runs the same parse over the bitmap's event list,
+// reading literal bytes from the mask, and writes the frame at its place in
+// the stream; raw and dense frames are copied by the whole CTA.  All three
+// encoders call the same parse_group with groups of 32 consecutive events
+// from the first one, so their sizes agree by construction (a disagreement
+// is reported).
 //
 // LZ4 parse.  The masks are long zero runs around sparse non-zero bytes, so
 // every zero run of at least 4 bytes becomes one match and everything else
@@ -94,6 +104,7 @@ struct EncArgs {
     uint64_t* lb;              // frame offsets: frames before << 40 | bytes before
     uint32_t* fsize;           // frame size (| kSpilled), 0: no frame
     SpillRec* spill;
+    uint32_t* deep;            // spill records left to spill_kernel
     uint8_t* slots;            // kEncSlot bytes per chunk
 };
 
@@ -431,8 +442,9 @@ __device__ __forceinline__ void gather_bytes(const EncArgs& A, const Seg* segs, 
 // The stream loop of any chunk (overwrite records, 4-bit elements, pieces
 // that are not 16-byte aligned); stream_fast below is the common case.
 __device__ __forceinline__ void stream_chunk(const EncArgs& A, WarpSmem& W, const ChunkDesc& cd, const Seg* segs,
-                                             int lane, uint8_t* body, int ncap, uint32_t& changed, Parse& P,
-                                             int& tail, int& np, int& units, bool& spill, bool& bad)
+                                             int lane, uint8_t* body, uint32_t cap, uint8_t* vals, int ncap,
+                                             uint32_t& changed, Parse& P, int& tail, int& np, int& units,
+                                             bool& spill, bool& bad)
 {
     const int raw = int(cd.raw_len);
     const int nseg = int(cd.src_count);
@@ -441,7 +453,6 @@ __device__ __forceinline__ void stream_chunk(const EncArgs& A, WarpSmem& W, cons
     const uint32_t bits = cd.bits;
     const uint32_t ub = bits == 16 ? 2u : 1u;
     const int nsteps = (raw + kStep - 1) / kStep;
-    uint8_t* vstage = reinterpret_cast<uint8_t*>(W.pos);   // overwrite values
     const RingSrc R{W.pos, W.val};
 
     // step s of the chunk into landing stage s % kNS (one commit group per
@@ -523,16 +534,16 @@ __device__ __forceinline__ void stream_chunk(const EncArgs& A, WarpSmem& W, cons
             tot = __shfl_sync(kFull, incl, 31);
         }
         if (overwrite) {
-            // unit offsets straight to the slot, values staged until the
-            // count is known
+            // unit offsets straight to the body, values to `vals` (staged
+            // until the count is known, or in place once it is)
             int r = units + int(pre);
             for (uint32_t b = z; b; b &= b - 1) {
                 const uint32_t i = __ffs(b) - 1;
                 if (r < ncap) {
                     const uint32_t u = (x + i) / ub;
                     *reinterpret_cast<uint16_t*>(body + 4 + 2 * r) = uint16_t(u);
-                    vstage[r * int(ub)] = uint8_t(byte_of32(n0, n1, i));
-                    if (ub == 2) vstage[r * 2 + 1] = uint8_t(byte_of32(n0, n1, i + 1));
+                    vals[r * int(ub)] = uint8_t(byte_of32(n0, n1, i));
+                    if (ub == 2) vals[r * 2 + 1] = uint8_t(byte_of32(n0, n1, i + 1));
                 }
                 ++r;
             }
@@ -570,7 +581,7 @@ __device__ __forceinline__ void stream_chunk(const EncArgs& A, WarpSmem& W, cons
                 const bool fin = !more && tail - np < 32;
                 if (fin && tail == 0) break;   // no change: no frame
                 bool over = false;
-                parse_group(R, np, cnt, fin, raw, P, body, kSlotBody, !spill, lane, &over, &bad);
+                parse_group(R, np, cnt, fin, raw, P, body, cap, !spill, lane, &over, &bad);
                 np += cnt;
                 if (__any_sync(kFull, over)) spill = true;
                 if (fin) break;
@@ -588,8 +599,8 @@ __device__ __forceinline__ void stream_chunk(const EncArgs& A, WarpSmem& W, cons
 // after the loop.
 template <int kBits>
 __device__ __forceinline__ void stream_fast(const EncArgs& A, WarpSmem& W, const ChunkDesc& cd, const Seg* segs,
-                                            int lane, uint8_t* body, uint32_t& changed, Parse& P, int& tail,
-                                            int& np, bool& spill, bool& bad)
+                                            int lane, uint8_t* body, uint32_t cap, uint32_t& changed, Parse& P,
+                                            int& tail, int& np, bool& spill, bool& bad)
 {
     const int raw = int(cd.raw_len);
     const int nseg = int(cd.src_count);
@@ -694,7 +705,7 @@ __device__ __forceinline__ void stream_fast(const EncArgs& A, WarpSmem& W, const
             __syncwarp();
             while (tail - np >= 32) {
                 bool over = false;
-                parse_group(R, np, 32, false, raw, P, body, kSlotBody, !spill, lane, &over, &bad);
+                parse_group(R, np, 32, false, raw, P, body, cap, !spill, lane, &over, &bad);
                 np += 32;
                 if (__any_sync(kFull, over)) spill = true;
             }
@@ -705,7 +716,7 @@ __device__ __forceinline__ void stream_fast(const EncArgs& A, WarpSmem& W, const
         const int cnt = tail - np < 32 ? tail - np : 32;
         const bool fin = tail - np < 32;
         bool over = false;
-        parse_group(R, np, cnt, fin, raw, P, body, kSlotBody, !spill, lane, &over, &bad);
+        parse_group(R, np, cnt, fin, raw, P, body, cap, !spill, lane, &over, &bad);
         np += cnt;
         if (__any_sync(kFull, over)) spill = true;
         if (fin) break;
@@ -730,18 +741,18 @@ __device__ __forceinline__ void encode_chunk(const EncArgs& A, WarpSmem& W, uint
                                                                            : kValStage / int(ub);
     uint8_t* slot = A.slots + size_t(k) * kEncSlot;
     uint8_t* body = slot + kFrameHdr;
-    const uint8_t* vstage = reinterpret_cast<const uint8_t*>(W.pos);   // overwrite values
+    uint8_t* vstage = reinterpret_cast<uint8_t*>(W.pos);   // overwrite values
 
     uint32_t changed = 0;
     Parse P{-1, 0ull, 0, 0, 0u};
     int tail = 0, np = 0, units = 0;
     bool spill = false, bad = false;
     if (!overwrite && vec && cd.bits == 16)
-        stream_fast<16>(A, W, cd, segs, lane, body, changed, P, tail, np, spill, bad);
+        stream_fast<16>(A, W, cd, segs, lane, body, kSlotBody, changed, P, tail, np, spill, bad);
     else if (!overwrite && vec && cd.bits == 8)
-        stream_fast<8>(A, W, cd, segs, lane, body, changed, P, tail, np, spill, bad);
+        stream_fast<8>(A, W, cd, segs, lane, body, kSlotBody, changed, P, tail, np, spill, bad);
     else
-        stream_chunk(A, W, cd, segs, lane, body, ncap, changed, P, tail, np, units, spill, bad);
+        stream_chunk(A, W, cd, segs, lane, body, kSlotBody, vstage, ncap, changed, P, tail, np, units, spill, bad);
     changed = __reduce_add_sync(kFull, changed);
     if (lane == 0 && changed) {
         atomicAdd(&A.counts[cd.tensor], (unsigned long long)changed);
@@ -810,6 +821,89 @@ __global__ void __launch_bounds__(kMThreads, 4) encode_kernel(EncArgs A)
         k = __shfl_sync(kFull, k, 0);
         if (k >= A.chunk_count) break;
         encode_chunk(A, W, k, lane);
+    }
+}
+
+// --------------------------------------------------------- restream_kernel --
+// One listed chunk streamed again by one warp, once the frame offsets are
+// known: the same stream loop and parse groups as encode_chunk, writing the
+// body straight to its place in the stream (capacity: the size found the
+// first time).  Overwrite values go to their place directly, the unit count
+// being known.  Raw and dense frames, and LZ4 chunks whose pending literals
+// outgrow the event ring, are listed for spill_kernel.
+__device__ __forceinline__ void restream_chunk(const EncArgs& A, WarpSmem& W, uint32_t s, int lane)
+{
+    const SpillRec R = A.spill[s];
+    if (R.kind == kXorRaw || R.kind == kOverwriteDense) {
+        if (lane == 0) A.deep[atomicAdd(&A.sc->n_deep, 1u)] = s;
+        return;
+    }
+    const ChunkDesc cd = A.chunks[A.chunk_begin + R.k];
+    const int nseg = int(cd.src_count);
+    const bool cached = nseg <= kMSegCache;
+    if (cached)
+        for (int i = lane; i < nseg; i += 32) W.segs[i] = A.src[cd.src_begin + i];
+    __syncwarp();
+    const Seg* segs = cached ? W.segs : A.src + cd.src_begin;
+    const bool vec = (cd.flags & kSrcVec) != 0;
+    const uint32_t ub = cd.bits == 16 ? 2u : 1u;
+    uint8_t* f = A.payload + kStreamHdr + (A.lb[R.k] & kLbByteMask);
+    uint8_t* body = f + kFrameHdr;
+    const uint32_t nu = R.n_units;
+    const uint32_t voff = 4 + 2 * nu + (4 - (2 * nu) % 4) % 4;
+
+    uint32_t changed = 0;
+    Parse P{-1, 0ull, 0, 0, 0u};
+    int tail = 0, np = 0, units = 0;
+    bool spill = false, bad = false;
+    if (R.kind == kOverwrite)
+        stream_chunk(A, W, cd, segs, lane, body, R.body_len, body + voff, int(nu), changed, P, tail, np, units,
+                     spill, bad);
+    else if (vec && cd.bits == 16)
+        stream_fast<16>(A, W, cd, segs, lane, body, R.body_len, changed, P, tail, np, spill, bad);
+    else if (vec && cd.bits == 8)
+        stream_fast<8>(A, W, cd, segs, lane, body, R.body_len, changed, P, tail, np, spill, bad);
+    else
+        stream_chunk(A, W, cd, segs, lane, body, R.body_len, nullptr, 0, changed, P, tail, np, units, spill, bad);
+    changed = __reduce_add_sync(kFull, changed);
+    if (R.kind == kOverwrite) {
+        bad |= uint32_t(units) != nu;
+        for (uint32_t i = 4 + 2 * nu + lane; i < voff; i += 32) body[i] = 0;
+        if (lane == 0) *reinterpret_cast<uint32_t*>(body) = nu;
+    } else {
+        bad |= P.out != R.body_len;
+    }
+    bad |= changed != R.changed;
+    if (__any_sync(kFull, bad)) {
+        if (lane == 0) report(A.sc, DCR_ERR_CORRUPT);
+        return;
+    }
+    if (R.kind == kXorLz4 && spill) {   // the ring could not hold the pending literals
+        if (lane == 0) A.deep[atomicAdd(&A.sc->n_deep, 1u)] = s;
+        return;
+    }
+    const uint32_t fsz = (kFrameHdr + R.body_len + 15) / 16 * 16;
+    for (uint32_t i = kFrameHdr + R.body_len + lane; i < fsz; i += 32) f[i] = 0;   // padding
+    if (lane == 0) write_header(f, R.kind, cd.bits, A.chunk_begin + R.k, cd.raw_len, R.body_len, R.changed);
+    __syncwarp();   // the ring is reused by the next chunk
+}
+
+__global__ void __launch_bounds__(kMThreads, 4) restream_kernel(EncArgs A)
+{
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    const int lane = threadIdx.x & 31;
+    WarpSmem& W = reinterpret_cast<WarpSmem*>(smem_raw)[threadIdx.x >> 5];
+    const uint32_t n_spill = A.sc->n_spill;   // final: written by encode_kernel only
+    if (n_spill == 0 || A.sc->total > A.cap) return;
+    for (;;) {
+        uint32_t s = 0;
+        if (lane == 0) {
+            s = atomicAdd(&A.sc->spill_ticket, 1u);
+            if (*(volatile int32_t*)&A.sc->err) s = UINT_MAX;
+        }
+        s = __shfl_sync(kFull, s, 0);
+        if (s >= n_spill) break;
+        restream_chunk(A, W, s, lane);
     }
 }
 
@@ -1036,10 +1130,10 @@ __global__ void __launch_bounds__(kSThreads, 2) spill_kernel(EncArgs A)
     extern __shared__ __align__(16) unsigned char smem_raw[];
     Buf& B = *reinterpret_cast<Buf*>(smem_raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint32_t n_spill = A.sc->n_spill;   // final: written by encode_kernel only
+    const uint32_t n_deep = A.sc->n_deep;     // final: written by restream_kernel only
     if (A.sc->total > A.cap) return;          // final: written by scan_kernel
-    for (uint32_t s = blockIdx.x; s < n_spill; s += gridDim.x) {
-        const SpillRec R = A.spill[s];
+    for (uint32_t i = blockIdx.x; i < n_deep; i += gridDim.x) {
+        const SpillRec R = A.spill[A.deep[i]];
         const uint64_t foff = kStreamHdr + (A.lb[R.k] & kLbByteMask);
         const ChunkDesc cd = A.chunks[A.chunk_begin + R.k];
         if (warp == 0) {
@@ -1065,38 +1159,6 @@ __global__ void __launch_bounds__(kSThreads, 2) spill_kernel(EncArgs A)
             bool bad = false;
             const uint32_t got = lz4_block(B, raw, body, R.body_len, lane, &bad);
             if ((__any_sync(kFull, bad) || got != R.body_len) && lane == 0) report(A.sc, DCR_ERR_CORRUPT);
-        } else if (warp == 0) {
-            // overwrite records: count | unit offsets | pad to 4 | values
-            const uint32_t ub = cd.bits == 16 ? 2u : 1u;
-            const uint32_t nu = R.n_units;
-            const uint32_t pad = (4 - (2 * nu) % 4) % 4;
-            if (lane == 0) {
-                *reinterpret_cast<uint32_t*>(body) = nu;
-                for (uint32_t i = 0; i < pad; ++i) body[4 + 2 * nu + i] = 0;
-            }
-            uint8_t* offs = body + 4;
-            uint8_t* vals = body + 4 + 2 * nu + pad;
-            uint32_t base = 0;
-            for (int t = 0; t < kSteps; ++t) {
-                const int wi = 32 * t + lane;
-                uint32_t b = unit_bits(B.bits[wi], ub);
-                const uint32_t c = __popc(b);
-                const uint32_t incl = warp_incl_sum(c, lane);
-                uint32_t u_i = base + incl - c;
-                while (b) {
-                    const uint32_t x = uint32_t(wi * 32 + __ffs(b) - 1);
-                    b &= b - 1;
-                    const uint32_t u = x / ub;
-                    if (u_i < nu) {
-                        offs[2 * u_i] = uint8_t(u);
-                        offs[2 * u_i + 1] = uint8_t(u >> 8);
-                        for (uint32_t e = 0; e < ub; ++e) vals[u_i * ub + e] = bytes[x + e];
-                    }
-                    ++u_i;
-                }
-                base += __shfl_sync(kFull, incl, 31);
-            }
-            if (base != nu && lane == 0) report(A.sc, DCR_ERR_CORRUPT);
         }
         for (uint32_t x = kFrameHdr + R.body_len + threadIdx.x; x < fsz; x += kSThreads) f[x] = 0;
         __syncthreads();
@@ -1115,15 +1177,20 @@ int encode_kernel_config(KernelConfig* kc)
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(encode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kMainSmem));
     if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(restream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kMainSmem));
+    if (e == cudaSuccess)
         e = cudaFuncSetAttribute(spill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sizeof(Buf)));
     if (e == cudaSuccess)
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&kc->enc_blocks_per_sm, encode_kernel, kMThreads,
                                                           kMainSmem);
     if (e == cudaSuccess)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&kc->restream_blocks_per_sm, restream_kernel, kMThreads,
+                                                          kMainSmem);
+    if (e == cudaSuccess)
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&kc->spill_blocks_per_sm, spill_kernel, kSThreads,
                                                           sizeof(Buf));
     if (e != cudaSuccess) return cuda_error(e, "encode kernel configuration");
-    if (kc->enc_blocks_per_sm < 1 || kc->spill_blocks_per_sm < 1)
+    if (kc->enc_blocks_per_sm < 1 || kc->restream_blocks_per_sm < 1 || kc->spill_blocks_per_sm < 1)
         return set_error(DCR_ERR_CUDA, "encode kernels do not fit on an SM");
     return DCR_OK;
 }
@@ -1149,6 +1216,7 @@ int encode_launch(const dcr_plan* P, uint32_t mode, uint32_t window, const void*
     A.lb = P->d_lb;
     A.fsize = P->d_fsize;
     A.spill = P->d_spill;
+    A.deep = P->d_deep;
     A.slots = P->d_slots;
     // ticket, error, totals, spill count and per-tensor counts start at zero
     cudaError_t e = cudaMemsetAsync(P->d_enc, 0, P->enc_head_bytes, s);
@@ -1163,6 +1231,9 @@ int encode_launch(const dcr_plan* P, uint32_t mode, uint32_t window, const void*
     unsigned cgrid = (A.chunk_count + 7) / 8;
     if (cgrid > unsigned(P->kc.num_sms * 8)) cgrid = unsigned(P->kc.num_sms * 8);
     copy_kernel<<<cgrid, 256, 0, s>>>(A);
+    unsigned rgrid = unsigned(P->kc.num_sms * P->kc.restream_blocks_per_sm);
+    if (rgrid > grid) rgrid = grid;
+    restream_kernel<<<rgrid, kMThreads, kMainSmem, s>>>(A);
     spill_kernel<<<unsigned(P->kc.num_sms * P->kc.spill_blocks_per_sm), kSThreads, sizeof(Buf), s>>>(A);
     if (P->profiling) cudaEventRecord(P->ev[2], s);
     e = cudaGetLastError();

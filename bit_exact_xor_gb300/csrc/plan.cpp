@@ -359,11 +359,12 @@ extern "C" int dcr_plan_build(const dcr_tensor_desc* tensors, size_t n, const dc
         return rc;
     }
     // encode scratch: head = EncScratch + per-tensor counts, then look-back,
-    // sizes and the spill list
+    // sizes, the spill list and the spill kernel's share of it
     P->enc_head_bytes = (sizeof(EncScratch) + 8 * n + 255) / 256 * 256;
     size_t lb_bytes = (P->max_window_chunks * 8 + 255) / 256 * 256;
     size_t fs_bytes = (P->max_window_chunks * 4 + 255) / 256 * 256;
-    size_t total = P->enc_head_bytes + lb_bytes + fs_bytes + P->max_window_chunks * sizeof(SpillRec) + 256;
+    size_t sp_bytes = (P->max_window_chunks * sizeof(SpillRec) + 255) / 256 * 256;
+    size_t total = P->enc_head_bytes + lb_bytes + fs_bytes + sp_bytes + P->max_window_chunks * 4 + 256;
     if ((e = cudaMalloc(&P->d_enc, total)) != cudaSuccess ||
         (e = cudaMalloc(&P->d_slots, P->max_window_chunks * size_t(kEncSlot))) != cudaSuccess ||
         (e = cudaMallocHost(&P->h_enc, P->enc_head_bytes)) != cudaSuccess) {
@@ -375,6 +376,7 @@ extern "C" int dcr_plan_build(const dcr_tensor_desc* tensors, size_t n, const dc
     P->d_fsize = reinterpret_cast<uint32_t*>(static_cast<char*>(P->d_enc) + P->enc_head_bytes + lb_bytes);
     P->d_spill = reinterpret_cast<SpillRec*>(static_cast<char*>(P->d_enc) + P->enc_head_bytes + lb_bytes +
                                              fs_bytes);
+    P->d_deep = reinterpret_cast<uint32_t*>(reinterpret_cast<char*>(P->d_spill) + sp_bytes);
     if ((rc = encode_kernel_config(&P->kc)) || (rc = apply_kernel_config(&P->kc))) {
         plan_free_device(P);
         delete P;
