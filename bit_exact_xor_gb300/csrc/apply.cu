@@ -309,6 +309,29 @@ __device__ __forceinline__ uint32_t seq_end(const uint8_t* src, uint32_t n, uint
     return q;
 }
 
+__device__ __noinline__ uint32_t seq_end_rare(const uint8_t* src, uint32_t n, uint32_t p)
+{
+    return seq_end(src, n, p);
+}
+
+// seq_end for a body in global memory: the common shape (literal length
+// below 15, at most one match-length byte, below 255) without branches, both
+// bytes it may need read at once, clamped into the body (n >= 1).
+__device__ __forceinline__ uint32_t seq_end_ldg(const uint8_t* src, uint32_t n, uint32_t p)
+{
+    const uint32_t tok = src[p < n ? p : n - 1];
+    const uint32_t ll = tok >> 4;
+    const uint32_t q = p + 1 + ll;   // end of the literals
+    const uint32_t x = src[q + 2 < n ? q + 2 : n - 1];
+    const bool mlx = (tok & 15u) == 15u;
+    if (p >= n) return kEndBad;
+    if (ll == 15 || (mlx && x == 255)) return seq_end_rare(src, n, p);
+    if (q > n) return kEndBad;
+    if (q == n) return q | kEndFinal;
+    if (n - q < 2 || (mlx && n - q < 3)) return kEndBad;
+    return q + (mlx ? 3u : 2u);
+}
+
 // The warp takes the block a window of kWin body bytes at a time: every lane
 // works out where a sequence starting at each of its window bytes would end
 // (and, in two more passes, where the sequence two and four on starts), lane
@@ -331,6 +354,7 @@ template <bool kBitmap, class WS>
 __device__ int zsrc_apply(const ApplyArgs& A, const ChunkDesc& cd, const Seg* ds, const uint8_t* src,
                           uint32_t n, uint32_t raw, uint32_t lim, WS& W, int lane)
 {
+    if (n == 0) return 0;   // an LZ4 block holds at least one token
     const bool one = cd.dst_count == 1;
     const uint64_t base = one ? ds[0].addr - ds[0].off : 0ull;   // single receiver piece
     if constexpr (kBitmap) {
@@ -339,11 +363,13 @@ __device__ int zsrc_apply(const ApplyArgs& A, const ChunkDesc& cd, const Seg* ds
     }
     uint32_t ip = 0, op = 0;      // next sequence in the body; its output position
     uint32_t nev = 0, runs = 0;   // listed positions, literal runs applied
+    uint32_t cs = 0, ce = 0;      // output bytes [cs, ce) known to be zero
     int status = 1;
     for (;;) {
         uint32_t e[kWin / 32];
 #pragma unroll
-        for (uint32_t j = 0; j < kWin / 32; ++j) e[j] = seq_end(src, n, ip + 32 * j + lane);
+        for (uint32_t j = 0; j < kWin / 32; ++j)
+            e[j] = kBitmap ? seq_end_ldg(src, n, ip + 32 * j + lane) : seq_end(src, n, ip + 32 * j + lane);
 #pragma unroll
         for (uint32_t j = 0; j < kWin / 32; ++j) {
             const uint32_t x = e[j];
@@ -454,6 +480,8 @@ __device__ int zsrc_apply(const ApplyArgs& A, const ChunkDesc& cd, const Seg* ds
         ip = cur;
         // literals: XOR into the receiver and record the non-zero ones
         if constexpr (kBitmap) {
+            // the first four literal bytes are read at once (clamped into
+            // the body), the rest one by one
             for (uint32_t q = 0; q < ll; ++q) {
                 const uint32_t b = src[ipl + q];
                 if (b) {
@@ -486,26 +514,56 @@ __device__ int zsrc_apply(const ApplyArgs& A, const ChunkDesc& cd, const Seg* ds
         __syncwarp();
         // the match copies [mop - off, mop - off + min(ml, off)), repeated
         bool viol = false;
-        if (mine && !lastseq) {
-            const uint32_t s0 = mop - off, e0 = s0 + (ml < off ? ml : off);
-            if constexpr (kBitmap) {
+        if constexpr (kBitmap) {
+            if (mine && !lastseq) {
+                const uint32_t s0 = mop - off, e0 = s0 + (ml < off ? ml : off);
                 for (uint32_t w = s0 >> 5; w <= (e0 - 1) >> 5 && !viol; ++w) {
                     const uint32_t a = (w << 5) > s0 ? 0u : s0 - (w << 5);
                     const uint32_t b = ((w + 1) << 5) < e0 ? 32u : e0 - (w << 5);
                     const uint32_t m = (b == 32 ? 0xFFFFFFFFu : ((1u << b) - 1)) & ~((1u << a) - 1);
                     viol = (W.bits[w] & m) != 0;
                 }
-            } else {
-                uint32_t lo = 0, hi = nev;   // first listed position >= s0
-                while (lo < hi) {
-                    const uint32_t mid = (lo + hi) >> 1;
-                    if (W.ev[mid] < s0) lo = mid + 1;
-                    else hi = mid;
+            }
+        } else {
+            // a source inside the sequence's own literals (offset 1 after a
+            // kept zero) is checked there, one inside [cs, ce) needs no check,
+            // the rest are looked up in the list; the longest zero stretch
+            // found that way is kept
+            bool look = false;
+            uint32_t s0 = 0, e0 = 0, zs = 0, ze = 0;
+            if (mine && !lastseq) {
+                s0 = mop - off;
+                e0 = s0 + (ml < off ? ml : off);
+                if (off <= ll && e0 - s0 <= 4u) {
+                    for (uint32_t q = ll - off; q < ll - off + (e0 - s0); ++q) viol |= src[ipl + q] != 0;
+                } else {
+                    look = s0 < cs || e0 > ce;
                 }
-                viol = lo < nev && W.ev[lo] < e0;
+            }
+            if (__any_sync(kFull, look)) {
+                if (look) {
+                    uint32_t lo = 0, hi = nev;   // first listed position >= s0
+                    while (lo < hi) {
+                        const uint32_t mid = (lo + hi) >> 1;
+                        if (W.ev[mid] < s0) lo = mid + 1;
+                        else hi = mid;
+                    }
+                    viol = lo < nev && W.ev[lo] < e0;
+                    // the zero stretch between the listed neighbours (every
+                    // non-zero output byte before op is listed)
+                    zs = lo ? uint32_t(W.ev[lo - 1]) + 1u : 0u;
+                    ze = lo < nev ? uint32_t(W.ev[lo]) : op;
+                }
+                const uint32_t zl = look && !viol ? ze - zs : 0u;
+                const uint32_t best = __reduce_max_sync(kFull, zl);
+                if (best > ce - cs) {
+                    const int from = __ffs(__ballot_sync(kFull, zl == best)) - 1;
+                    cs = __shfl_sync(kFull, zs, from);
+                    ce = __shfl_sync(kFull, ze, from);
+                }
             }
         }
-        if (__any_sync(kFull, viol)) {
+        if (__reduce_or_sync(kFull, uint32_t(viol))) {
             status = 0;
             break;
         }
@@ -780,7 +838,7 @@ __global__ void __launch_bounds__(kDThreads) defer_kernel(ApplyArgs A)
 // list holds): one warp per frame, body read from global memory, matches
 // checked against a bitmap of the non-zero output bytes.  The frames were
 // validated and claimed by apply_kernel.
-__global__ void __launch_bounds__(kBThreads) big_kernel(ApplyArgs A)
+__global__ void __launch_bounds__(kBThreads, 3) big_kernel(ApplyArgs A)
 {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     BWarp& W = reinterpret_cast<BWarp*>(smem_raw)[threadIdx.x >> 5];
