@@ -47,6 +47,8 @@ def build_workload(name, frac=None):
     if name == "gqa":
         return configs.gqa(frac=frac if frac is not None else 0.03)
     if name == "sweep":
+        if frac is not None and frac >= 1.0:   # the incompressible case: a fully random new buffer
+            return configs.sweep(random_new=True)
         return configs.sweep(frac=frac if frac is not None else 0.01)
     if name == "moe":
         return configs.nvfp4_moe(frac=frac if frac is not None else 0.00085)
@@ -389,7 +391,7 @@ def run_gpu(args):
                      "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                      "peak_source": peak_kind,
                      "algorithmic_bytes_per_launch": int(alg_bytes)},
-        "gpu_launches": 8 * nw * args.steps,
+        "gpu_launches": 9 * nw * args.steps,
         "clocks": clocks,
     }
     if e2e:
@@ -413,7 +415,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default="dense", choices=sorted(WORKLOAD_NAMES))
-    ap.add_argument("--frac", type=float, default=None)
+    ap.add_argument("--frac", type=float, default=None,
+                    help="change rate (sweep: 1 or more = fully random new buffer)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
