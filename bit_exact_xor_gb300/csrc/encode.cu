@@ -326,6 +326,12 @@ __device__ __forceinline__ void parse_group(const Src& S, int e0, int cnt, bool 
     if (lane == 0) pp = P.prev;
     const int gs = pp + 1;
     const int L = p - gs;
+    if (!final && __all_sync(kFull, L == 0)) {
+        // 32 back-to-back non-zero bytes: no zero run, no sequence, nothing
+        // to carry but the last position
+        P.prev = __shfl_sync(kFull, p, 31);
+        return;
+    }
     const int me = p < raw - 5 ? p : raw - 5;
     const uint32_t bl = uint32_t(P.best >> 32);
     const int bs = int(uint32_t(P.best));
