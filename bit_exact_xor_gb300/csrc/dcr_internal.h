@@ -181,6 +181,7 @@ struct dcr_plan {
     bool profiling = false;
     cudaEvent_t ev[8] = {};
     mutable dcr_profile prof = {};
+    mutable bool prof_encode_due = false, prof_apply_due = false;   // events recorded, durations not read
 };
 
 struct dcr_recv_state {

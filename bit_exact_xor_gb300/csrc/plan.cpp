@@ -495,8 +495,7 @@ extern "C" int dcr_encode(const dcr_plan* p, uint32_t mode, uint32_t window,
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return cuda_error(e, "dcr_encode status read");
     if (p->profiling) {
-        cudaEventElapsedTime(&p->prof.encode_ms, p->ev[0], p->ev[1]);
-        cudaEventElapsedTime(&p->prof.finalize_ms, p->ev[1], p->ev[2]);
+        p->prof_encode_due = true;   // durations read from the events when asked for
         p->prof.encode_valid = 1;
     }
     const EncScratch* st = static_cast<const EncScratch*>(p->h_enc);
@@ -531,9 +530,7 @@ static int apply_common(const dcr_plan* p, dcr_recv_state* st, const void* paylo
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return cuda_error(e, "dcr_apply status read");
     if (p->profiling) {
-        cudaEventElapsedTime(&p->prof.apply_ms, p->ev[3], p->ev[4]);
-        cudaEventElapsedTime(&p->prof.defer_ms, p->ev[4], p->ev[5]);
-        cudaEventElapsedTime(&p->prof.pending_ms, p->ev[5], p->ev[6]);
+        p->prof_apply_due = true;
         p->prof.apply_valid = 1;
     }
     const ApplyScratch& a = *st->h_scratch;
@@ -589,12 +586,25 @@ extern "C" int dcr_plan_set_profiling(dcr_plan* p, int on)
     }
     p->profiling = on != 0;
     p->prof = dcr_profile{};
+    p->prof_encode_due = p->prof_apply_due = false;
     return DCR_OK;
 }
 
 extern "C" int dcr_plan_last_profile(const dcr_plan* p, dcr_profile* out)
 {
     if (!p || !out) return set_error(DCR_ERR_INVALID, "dcr_plan_last_profile: NULL argument");
+    // the calls that recorded these events synchronised their stream
+    if (p->prof_encode_due) {
+        cudaEventElapsedTime(&p->prof.encode_ms, p->ev[0], p->ev[1]);
+        cudaEventElapsedTime(&p->prof.finalize_ms, p->ev[1], p->ev[2]);
+        p->prof_encode_due = false;
+    }
+    if (p->prof_apply_due) {
+        cudaEventElapsedTime(&p->prof.apply_ms, p->ev[3], p->ev[4]);
+        cudaEventElapsedTime(&p->prof.defer_ms, p->ev[4], p->ev[5]);
+        cudaEventElapsedTime(&p->prof.pending_ms, p->ev[5], p->ev[6]);
+        p->prof_apply_due = false;
+    }
     *out = p->prof;
     return DCR_OK;
 }

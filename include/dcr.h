@@ -254,10 +254,13 @@ int dcr_apply_noalloc(const dcr_plan* plan, dcr_recv_state* state, const void* p
                       void* target, dcr_apply_result* result, void* stream);
 
 /* Kernel timing (tracing aid).  When on, the library records CUDA events on
- * the caller's stream around each of its kernels; after each dcr_encode /
- * dcr_apply / dcr_apply_retry, dcr_plan_last_profile returns the durations
- * in milliseconds of that call's kernels (valid = 1 if measured).  The
- * record is per plan; off by default. */
+ * the caller's stream around each of its kernels; dcr_plan_last_profile
+ * returns the durations in milliseconds of the kernels of the latest
+ * dcr_encode (encode_ms, finalize_ms) and of the latest dcr_apply /
+ * dcr_apply_retry (apply_ms, defer_ms, pending_ms), valid = 1 if measured;
+ * the durations are read from the events when it is called, so one call
+ * after an encode and its apply returns both.  The record is per plan; off
+ * by default. */
 typedef struct {
     float encode_ms;    /* gather + XOR + count + encode + frame write (main kernel) */
     float finalize_ms;  /* spilled (dense) chunk bodies, frame index, stream header */

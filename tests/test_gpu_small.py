@@ -364,3 +364,21 @@ def test_signed_zero_on_gpu():
     tgt = to_device([old])[0]
     rc, _ = dcr.apply(plan, dcr.RecvState(plan, 0), pl, size, tgt)
     assert rc == dcr.OK and np.array_equal(tgt.cpu().numpy(), new)
+
+
+def test_kernel_timing_profile():
+    c = Case(configs.mini(2))
+    p0 = c.plan.last_profile()
+    assert p0.encode_valid == 0 and p0.apply_valid == 0
+    c.plan.set_profiling(True)
+    pl, size, _ = c.encode()
+    t = c.target()
+    rc, _ = dcr.apply(c.plan, dcr.RecvState(c.plan, 0), pl, size, t)
+    assert rc == dcr.OK
+    p = c.plan.last_profile()   # one read after encode and apply returns both
+    assert p.encode_valid == 1 and p.apply_valid == 1
+    assert p.encode_ms > 0 and p.apply_ms > 0 and p.finalize_ms >= 0 and p.pending_ms >= 0
+    assert p.encode_ms < 1000 and p.apply_ms < 1000
+    c.plan.set_profiling(False)
+    q = c.plan.last_profile()
+    assert q.encode_valid == 0 and q.apply_valid == 0
