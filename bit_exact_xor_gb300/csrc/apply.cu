@@ -737,7 +737,8 @@ __global__ void __launch_bounds__(kDThreads) defer_kernel(ApplyArgs A)
     extern __shared__ __align__(16) unsigned char smem_raw[];
     uint8_t* out = smem_raw;                       // kChunk bytes
     __shared__ uint32_t s_f, s_good;
-    if (!A.sc->hdr_ok) return;
+    // final: apply_kernel alone lists deferred frames
+    if (!A.sc->hdr_ok || *reinterpret_cast<volatile uint32_t*>(&A.sc->n_defer) == 0) return;
     const uint8_t* p = A.payload;
     const uint64_t total = ld64(p + 56), nf = ld64(p + 48), idx_off = total - 8 * nf;
     const uint64_t V = ld64(p + 24);
@@ -848,6 +849,7 @@ __global__ void __launch_bounds__(kBThreads, 3) big_kernel(ApplyArgs A)
     const uint64_t total = ld64(p + 56), nf = ld64(p + 48), idx_off = total - 8 * nf;
     const uint64_t V = ld64(p + 24);
     const uint32_t nbig = A.sc->n_big;   // final: written by apply_kernel only
+    if (nbig == 0) return;
     for (;;) {
         uint32_t j = 0;
         if (lane == 0) j = atomicAdd(&A.sc->big_ticket, 1u);

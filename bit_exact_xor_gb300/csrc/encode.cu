@@ -927,8 +927,15 @@ __global__ void __launch_bounds__(1024) scan_kernel(EncArgs A, uint64_t plan_has
         fs &= ~kSpilled;
         return fs ? ((1ull << kLbFrameShift) | fs) : 0ull;
     };
+    // sizes read eight at a time (independent loads)
     unsigned long long sum = 0;
-    for (uint32_t k = b; k < e; ++k) sum += rec(A.fsize[k]);
+    for (uint32_t k0 = b; k0 < e; k0 += 8) {
+        uint32_t v[8];
+#pragma unroll
+        for (uint32_t j = 0; j < 8; ++j) v[j] = k0 + j < e ? A.fsize[k0 + j] : 0u;
+#pragma unroll
+        for (uint32_t j = 0; j < 8; ++j) sum += rec(v[j]);
+    }
     // block exclusive scan of the per-thread sums
     unsigned long long incl = sum;
 #pragma unroll
@@ -949,9 +956,15 @@ __global__ void __launch_bounds__(1024) scan_kernel(EncArgs A, uint64_t plan_has
     }
     __syncthreads();
     unsigned long long run = wsum[warp] + incl - sum;
-    for (uint32_t k = b; k < e; ++k) {
-        A.lb[k] = run;
-        run += rec(A.fsize[k]);
+    for (uint32_t k0 = b; k0 < e; k0 += 8) {
+        uint32_t v[8];
+#pragma unroll
+        for (uint32_t j = 0; j < 8; ++j) v[j] = k0 + j < e ? A.fsize[k0 + j] : 0u;
+#pragma unroll
+        for (uint32_t j = 0; j < 8; ++j) {
+            if (k0 + j < e) A.lb[k0 + j] = run;
+            run += rec(v[j]);
+        }
     }
     if (threadIdx.x == 1023) {
         const uint64_t fbytes = run & kLbByteMask, nframes = run >> kLbFrameShift;
@@ -998,9 +1011,18 @@ __global__ void copy_kernel(EncArgs A)
         const uint64_t foff = kStreamHdr + (ex & kLbByteMask);
         if (lane == 0) index[ex >> kLbFrameShift] = foff;
         if (fs & kSpilled) continue;
-        const uint4* src = reinterpret_cast<const uint4*>(A.slots + size_t(k) * kEncSlot);
-        uint4* dst = reinterpret_cast<uint4*>(A.payload + foff);
-        for (uint32_t i = lane; i < fs / 16; i += 32) dst[i] = src[i];
+        const uint4* __restrict__ src = reinterpret_cast<const uint4*>(A.slots + size_t(k) * kEncSlot);
+        uint4* __restrict__ dst = reinterpret_cast<uint4*>(A.payload + foff);
+        const uint32_t nv = fs / 16;
+        for (uint32_t i0 = lane; i0 < nv; i0 += 128) {   // four loads in flight per lane
+            uint4 v[4];
+#pragma unroll
+            for (uint32_t j = 0; j < 4; ++j)
+                if (i0 + 32 * j < nv) v[j] = src[i0 + 32 * j];
+#pragma unroll
+            for (uint32_t j = 0; j < 4; ++j)
+                if (i0 + 32 * j < nv) dst[i0 + 32 * j] = v[j];
+        }
     }
 }
 
