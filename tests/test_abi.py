@@ -36,3 +36,61 @@ def test_last_error_without_gpu_work():
     rc = dcr.lib().dcr_plan_build(None, 0, None, None)
     assert rc == dcr.ERR_INVALID
     assert "NULL" in dcr.last_error() or "no tensors" in dcr.last_error()
+
+
+def _build(descs, window_bytes=0):
+    """dcr_plan_build on descriptors that fail validation (rejected before
+    any CUDA call, so this runs without a GPU)."""
+    import ctypes
+    arr = (dcr.TensorDesc * len(descs))(*descs)
+    opts = dcr.PlanOpts(window_bytes)
+    h = ctypes.c_void_p()
+    rc = dcr.lib().dcr_plan_build(arr, len(descs), ctypes.byref(opts), ctypes.byref(h))
+    return rc, dcr.last_error(), h.value
+
+
+def test_plan_rejects_degenerate_tensors():
+    ok = dict(split=dcr.REPLICATED, tp=1, shard_offset=[0], recv_offset=0)
+    cases = [
+        (dcr.make_desc("empty_rows", 16, 0, 64, **ok), "empty tensor"),
+        (dcr.make_desc("empty_cols", 16, 64, 0, **ok), "empty tensor"),
+        (dcr.make_desc("bits", 12, 64, 64, **ok), "elem_bits"),
+        (dcr.make_desc("odd_e2m1", 4, 64, 63, **ok), "even column"),
+        (dcr.make_desc("tp0", 16, 64, 64, dcr.REPLICATED, 0, [0], 0), "tp must be"),
+        (dcr.make_desc("tp17", 16, 64, 64, dcr.REPLICATED, 17, [0] * 16, 0), "tp must be"),
+        (dcr.make_desc("rows", 16, 65, 64, dcr.SPLIT_ROWS, 2, [0, 0], 0), "rows not divisible"),
+        (dcr.make_desc("cols", 16, 64, 65, dcr.SPLIT_COLS, 2, [0, 0], 0), "cols not divisible"),
+        (dcr.make_desc("qkv0", 16, 64, 64, dcr.RESIDUAL_QKV_INTERLEAVED, 2, [0, 0], 0), "head counts"),
+        (dcr.make_desc("qkv_rows", 16, 100, 64, dcr.RESIDUAL_QKV_INTERLEAVED, 2, [0, 0], 0, q_heads=4, kv_heads=2,
+                       head_dim=8), "qkv rows"),
+        (dcr.make_desc("qkv_div", 16, (3 + 2) * 8, 64, dcr.RESIDUAL_QKV_INTERLEAVED, 1, [0], 0, q_heads=3, kv_heads=1,
+                       head_dim=8, recv_layout=dcr.LAYOUT_ROWGROUP_INTERLEAVE, recv_group=8), "receiver layout"),
+        (dcr.make_desc("group", 16, 60, 64, dcr.REPLICATED, 1, [0], 0, recv_layout=dcr.LAYOUT_ROWGROUP_INTERLEAVE,
+                       recv_group=8), "row-group"),
+    ]
+    for d, why in cases:
+        rc, msg, h = _build([d])
+        assert rc == dcr.ERR_INVALID and h is None, (d.name, rc)
+        assert why in msg and d.name.decode() in msg, (why, msg)
+
+
+def test_plan_rejects_window_sizes_out_of_range():
+    d = dcr.make_desc("t", 16, 64, 64, dcr.REPLICATED, 1, [0], 0)
+    for w in (1, 65535, (256 << 30) + 1):
+        rc, msg, h = _build([d], window_bytes=w)
+        assert rc == dcr.ERR_INVALID and "window_bytes" in msg and h is None
+
+
+def test_calls_reject_null_handles():
+    import ctypes
+    L = dcr.lib()
+    size = ctypes.c_size_t()
+    assert L.dcr_encode(None, 0, 0, None, None, 0, 1, None, 0, ctypes.byref(size), None, None) == dcr.ERR_INVALID
+    assert L.dcr_apply(None, None, None, 0, None, None, None, None) == dcr.ERR_INVALID
+    assert L.dcr_apply_retry(None, None, None, 0, None, None, None) == dcr.ERR_INVALID
+    assert L.dcr_apply_noalloc(None, None, None, 0, None, None, None) == dcr.ERR_INVALID
+    assert L.dcr_dense_refit(None, None, None, None) == dcr.ERR_INVALID
+    h = ctypes.c_void_p()
+    assert L.dcr_recv_state_create(None, 0, ctypes.byref(h)) == dcr.ERR_INVALID
+    assert L.dcr_plan_set_profiling(None, 1) == dcr.ERR_INVALID
+    assert "NULL" in dcr.last_error()

@@ -382,3 +382,60 @@ def test_kernel_timing_profile():
     c.plan.set_profiling(False)
     q = c.plan.last_profile()
     assert q.encode_valid == 0 and q.apply_valid == 0
+
+
+def _flip_case(elem_bits, rows, cols, flips, seed=5):
+    """One replicated tensor, old random, new = old XOR a non-zero byte at
+    each canonical byte offset in `flips`; encode, compare with the oracle
+    and apply both streams on the GPU."""
+    t0 = configs.Tensor("e", elem_bits=elem_bits, rows=rows, cols=cols, split=configs.REPLICATED,
+                        value_kind=synth.VAL_BYTES, rule=0, frac=0)
+    wl = configs.Workload("edge", 1, 1, [t0]).layout()
+    rng = np.random.RandomState(seed)
+    old = rng.randint(0, 256, size=wl.shard_bytes[0]).astype(np.uint8)
+    new = old.copy()
+    for x in flips:
+        new[x] ^= np.uint8(rng.randint(1, 256))
+    orc = oracle.Oracle(wl)
+    plan = dcr.Plan(descs_of(wl))
+    d_old, d_new = to_device([old]), to_device([new])
+    pl = torch.zeros(plan.window(0).payload_bound, dtype=torch.uint8, device="cuda")
+    rc, size, counts = dcr.encode(plan, d_old, d_new, pl)
+    assert rc == dcr.OK, dcr.last_error()
+    g = pl[:size].cpu().numpy()
+    o, oc = orc.encode([old], [new])
+    check_structure(g)
+    assert counts == [int(x) for x in oc]
+    assert_same_frames(g, o)
+    exp = orc.receiver_dense([new])
+    for stream in (g, o):
+        t = torch.zeros(max(exp.size, 16), dtype=torch.uint8, device="cuda")
+        t[:exp.size] = torch.from_numpy(orc.receiver_dense([old])).cuda()
+        rc, _ = dcr.apply(plan, dcr.RecvState(plan, 0), torch.from_numpy(stream).cuda(), stream.size, t)
+        assert rc == dcr.OK, dcr.last_error()
+        assert np.array_equal(t.cpu().numpy()[:exp.size], exp)
+    return g, o
+
+
+@pytest.mark.parametrize("shape", [(16, 1, 1, [0]), (16, 1, 1, [1]), (8, 1, 13, [0, 5, 12]),
+                                   (8, 1, 13, list(range(13))), (16, 1, 32769, [7, 65536, 65537]),
+                                   (8, 1, 65536, [65535]), (8, 1, 65537, [65536])])
+def test_tiny_and_ragged_tensors(shape):
+    bits, rows, cols, flips = shape
+    _flip_case(bits, rows, cols, flips)
+
+
+def test_changes_near_the_end_of_a_chunk():
+    # chunk i: one change i + 1 bytes before its end (the block's end rules:
+    # last five bytes literal, no match starting in the last twelve), chunks
+    # 20..39 the same after an early change (a long zero run to copy from),
+    # chunk 40 its last five bytes changed, chunk 41 its last thirteen
+    flips = []
+    for i in range(20):
+        flips.append(i * 65536 + 65536 - 1 - i)
+    for i in range(20):
+        flips += [(20 + i) * 65536 + 3, (20 + i) * 65536 + 65536 - 1 - i]
+    flips += [40 * 65536 + 65536 - 1 - k for k in range(5)]
+    flips += [41 * 65536 + 65536 - 1 - k for k in range(13)]
+    g, o = _flip_case(8, 42, 65536, flips)
+    assert len(frames_by_chunk(g)[1]) == 42
