@@ -316,39 +316,57 @@ def run_gpu(args):
     value = N * args.steps * ws / (ms_max / 1e3) / 1e9
 
     # end to end through the public API with host buffers: H2D of old/new,
-    # encode, D2H of the payload, H2D of the payload, apply (status read inside)
+    # encode, D2H of the payload, H2D of the payload, apply (status read
+    # inside).  Each step's inputs are copied on a second stream while the
+    # previous step computes (two device input buffers); every copy of every
+    # timed step, the first one included, is inside the timed region.
     e2e = None
     if not args.no_e2e:
         h_old = [x.cpu().pin_memory() for x in olds]
         h_new = [x.cpu().pin_memory() for x in news]
         h_pl = [torch.empty(p.numel(), dtype=torch.uint8).pin_memory() for p in payloads]
-        d_in = [torch.empty_like(x) for x in olds], [torch.empty_like(x) for x in news]
+        d_in = [([torch.empty_like(x) for x in olds], [torch.empty_like(x) for x in news]) for _ in range(2)]
         rx = [torch.empty_like(p) for p in payloads]
+        cs = torch.cuda.Stream()
         h2d = d2h = 0
 
-        def e2e_step():
-            nonlocal h2d, d2h
-            a, b = (h_old, h_new) if d[0] == 0 else (h_new, h_old)
-            for x, y in zip(d_in[0], a):
-                x.copy_(y, non_blocking=True)
-            for x, y in zip(d_in[1], b):
-                x.copy_(y, non_blocking=True)
+        def copy_inputs(slot, direction):
+            nonlocal h2d
+            a, b = (h_old, h_new) if direction == 0 else (h_new, h_old)
+            with torch.cuda.stream(cs):
+                for x, y in zip(d_in[slot][0], a):
+                    x.copy_(y, non_blocking=True)
+                for x, y in zip(d_in[slot][1], b):
+                    x.copy_(y, non_blocking=True)
+                ev = torch.cuda.Event()
+                ev.record(cs)
             h2d += sum(y.numel() for y in a) + sum(y.numel() for y in b)
-            for w in range(nw):
-                rc, size, _ = dcr.encode(plan, d_in[0], d_in[1], payloads[w], window=w,
-                                         base_version=ver[0], target_version=ver[0] + 1, counts=False)
-                dcr.check(rc)
-                h_pl[w][:size].copy_(payloads[w][:size], non_blocking=True)
-                rx[w][:size].copy_(h_pl[w][:size], non_blocking=True)
-                d2h += size
-                h2d += size
-                rc, res = dcr.apply(plan, st, rx[w], size, target)
-                dcr.check(rc)
-            ver[0] += 1
-            d[0] ^= 1
+            return ev
 
-        for _ in range(2):
-            e2e_step()
+        def e2e_steps(k):
+            nonlocal d2h, h2d
+            cs.wait_stream(stream)   # the first copy starts after the timer's start event
+            ready = copy_inputs(0, d[0])
+            for i in range(k):
+                slot = i & 1
+                stream.wait_event(ready)
+                if i + 1 < k:   # the next step's inputs, into the other buffer (free: its step returned)
+                    ready = copy_inputs(slot ^ 1, d[0] ^ 1)
+                for w in range(nw):
+                    rc, size, _ = dcr.encode(plan, d_in[slot][0], d_in[slot][1], payloads[w], window=w,
+                                             base_version=ver[0], target_version=ver[0] + 1, counts=False,
+                                             stream=sh)
+                    dcr.check(rc)
+                    h_pl[w][:size].copy_(payloads[w][:size], non_blocking=True)
+                    rx[w][:size].copy_(h_pl[w][:size], non_blocking=True)
+                    d2h += size
+                    h2d += size
+                    rc, res = dcr.apply(plan, st, rx[w], size, target, stream=sh)
+                    dcr.check(rc)
+                ver[0] += 1
+                d[0] ^= 1
+
+        e2e_steps(2)
         h2d = d2h = 0
         torch.cuda.synchronize()
         dist_barrier(ws)
@@ -356,8 +374,7 @@ def run_gpu(args):
         t0 = torch.cuda.Event(enable_timing=True)
         t1 = torch.cuda.Event(enable_timing=True)
         t0.record(stream)
-        for _ in range(k):
-            e2e_step()
+        e2e_steps(k)
         t1.record(stream)
         torch.cuda.synchronize()
         ems = dist_max(t0.elapsed_time(t1), ws)
