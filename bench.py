@@ -254,7 +254,7 @@ def run_gpu(args):
 
     wl = build_workload(args.workload, args.frac)
     N = wl.canonical_bytes
-    plan = dcr.Plan(descs_of(wl), window_bytes=wl.window_bytes)
+    plan = dcr.Plan(descs_of(wl), window_bytes=(args.window_mb << 20) or wl.window_bytes)
     plan.set_profiling(True)
     olds, news = wl.device_arenas(torch)
     target = torch.empty(max(plan.info.recv_bytes, wl.recv_bytes), dtype=torch.uint8, device=dev)
@@ -381,6 +381,61 @@ def run_gpu(args):
         e2e = {"value": round(N * k * ws / (ems / 1e3) / 1e9, 3), "unit": UNIT,
                "h2d_bytes_per_step": h2d // k, "d2h_bytes_per_step": d2h // k}
 
+    # pipelined refit of every window through pinned host memory
+    # (dcr_refit_pipelined) against the same windows in series: encode, copy
+    # the stream to host and back, apply (one GPU, rank 0 of a single run)
+    pipe = None
+    if args.pipeline and ws == 1:
+        dev_b, host_b = dcr.pipeline_sizes(plan)
+        pdev = torch.empty(dev_b, dtype=torch.uint8, device=dev)
+        phost = torch.empty(host_b, dtype=torch.uint8).pin_memory()
+        stage = [torch.empty(p.numel(), dtype=torch.uint8).pin_memory() for p in payloads]
+        rxs = [torch.empty_like(p) for p in payloads]
+        last = {}
+
+        def serial_refit():
+            a, b = (olds, news) if d[0] == 0 else (news, olds)
+            for w in range(nw):
+                rc, size, _ = dcr.encode(plan, a, b, payloads[w], window=w, base_version=ver[0],
+                                         target_version=ver[0] + 1, counts=False, stream=sh)
+                dcr.check(rc)
+                stage[w][:size].copy_(payloads[w][:size], non_blocking=True)
+                rxs[w][:size].copy_(stage[w][:size], non_blocking=True)
+                rc, _ = dcr.apply(plan, st, rxs[w], size, target, stream=sh)
+                dcr.check(rc)
+            ver[0] += 1
+            d[0] ^= 1
+
+        def piped_refit():
+            a, b = (olds, news) if d[0] == 0 else (news, olds)
+            rc, stats, _ = dcr.refit_pipelined(plan, st, a, b, target, pdev, phost, base_version=ver[0],
+                                               target_version=ver[0] + 1, counts=False, stream=sh)
+            dcr.check(rc)
+            assert stats.committed == 1
+            last["payload"] = stats.payload_bytes
+            ver[0] += 1
+            d[0] ^= 1
+
+        def timed(fn, k):
+            for _ in range(2):
+                fn()
+            torch.cuda.synchronize()
+            a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a0.record(stream)
+            for _ in range(k):
+                fn()
+            a1.record(stream)
+            torch.cuda.synchronize()
+            return a0.elapsed_time(a1) / k
+
+        k = max(2, min(args.steps, 5))
+        ser_ms = timed(serial_refit, k)
+        pip_ms = timed(piped_refit, k)
+        pipe = {"windows": nw, "value": round(N / (pip_ms / 1e3) / 1e9, 3), "unit": UNIT,
+                "ms_per_refit": round(pip_ms, 4), "serial_ms_per_refit": round(ser_ms, 4),
+                "payload_bytes_per_refit": int(last["payload"])}
+        del pdev, phost, stage, rxs
+
     # the receiver really holds the last step's target weights
     ref = torch.empty_like(target)
     dcr.check(dcr.dense_refit(plan, olds if d[0] == 0 else news, ref))
@@ -417,6 +472,8 @@ def run_gpu(args):
     }
     if e2e:
         line["e2e"] = e2e
+    if pipe:
+        line["pipelined"] = pipe
     if rank == 0 and not args.no_cpu_baseline:
         cb = cpu_baseline(wl)
         line["payload_vs_oracle"] = round(P / cb.pop("payload_bytes"), 4)
@@ -439,6 +496,9 @@ def main():
     ap.add_argument("--frac", type=float, default=None,
                     help="change rate (sweep: 1 or more = fully random new buffer)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--window-mb", type=int, default=0, help="window size in MiB (0: the workload's)")
+    ap.add_argument("--pipeline", action="store_true",
+                    help="also time dcr_refit_pipelined against the same windows in series")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:

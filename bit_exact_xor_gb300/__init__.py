@@ -82,10 +82,17 @@ class Profile(ctypes.Structure):
                 ("apply_valid", ctypes.c_uint32)]
 
 
+class PipelineStats(ctypes.Structure):
+    _fields_ = [("windows", ctypes.c_uint64), ("payload_bytes", ctypes.c_uint64),
+                ("max_window_payload", ctypes.c_uint64), ("committed", ctypes.c_uint32),
+                ("reserved", ctypes.c_uint32)]
+
+
 EXPORTS = ["dcr_last_error", "dcr_plan_build", "dcr_plan_info_get", "dcr_window_info_get",
            "dcr_plan_destroy", "dcr_recv_state_create", "dcr_recv_state_destroy",
            "dcr_recv_state_version", "dcr_encode", "dcr_apply", "dcr_apply_retry",
-           "dcr_dense_refit", "dcr_plan_set_profiling", "dcr_plan_last_profile", "dcr_apply_noalloc"]
+           "dcr_dense_refit", "dcr_plan_set_profiling", "dcr_plan_last_profile", "dcr_apply_noalloc",
+           "dcr_pipeline_sizes", "dcr_refit_pipelined"]
 
 _lib = None
 
@@ -115,6 +122,9 @@ def lib():
         L.dcr_dense_refit.argtypes = [VP, P(VP), VP, VP]
         L.dcr_plan_set_profiling.argtypes = [VP, ctypes.c_int]
         L.dcr_plan_last_profile.argtypes = [VP, P(Profile)]
+        L.dcr_pipeline_sizes.argtypes = [VP, P(SZ), P(SZ)]
+        L.dcr_refit_pipelined.argtypes = [VP, VP, U32, P(VP), P(VP), U64, U64, VP, VP, SZ, VP, SZ, P(U64),
+                                          P(PipelineStats), VP]
         _lib = L
     return _lib
 
@@ -251,6 +261,27 @@ def apply_noalloc(plan, state, payload, size, target, stream=None):
     rc = lib().dcr_apply_noalloc(plan.h, state.h, _ptr(payload), size, _ptr(target), ctypes.byref(res),
                                  _stream(stream))
     return rc, res
+
+
+def pipeline_sizes(plan):
+    """dcr_pipeline_sizes: (device bytes, pinned host bytes) dcr_refit_pipelined needs."""
+    dev, host = ctypes.c_size_t(), ctypes.c_size_t()
+    check(lib().dcr_pipeline_sizes(plan.h, ctypes.byref(dev), ctypes.byref(host)))
+    return dev.value, host.value
+
+
+def refit_pipelined(plan, state, olds, news, target, device_buf, host_buf, mode=MODE_HYBRID, base_version=0,
+                    target_version=1, counts=True, stream=None):
+    """dcr_refit_pipelined.  device_buf: a device tensor, host_buf: a pinned
+    host tensor (pipeline_sizes bytes each).  Returns (status, PipelineStats,
+    per-tensor changed counts)."""
+    n = plan.info.n_tensors
+    cnt = (ctypes.c_uint64 * n)() if counts else None
+    st = PipelineStats()
+    rc = lib().dcr_refit_pipelined(plan.h, state.h, mode, _ptr_array(olds), _ptr_array(news), base_version,
+                                   target_version, _ptr(target), _ptr(device_buf), device_buf.numel(),
+                                   _ptr(host_buf), host_buf.numel(), cnt, ctypes.byref(st), _stream(stream))
+    return rc, st, (list(cnt) if counts else None)
 
 
 def dense_refit(plan, shards, target, stream=None):

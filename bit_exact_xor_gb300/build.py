@@ -7,7 +7,7 @@ import sys
 HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OUT = os.path.join(HERE, "libdcr.so")
-SOURCES = ["plan.cpp", "encode.cu", "apply.cu", "dense.cu"]
+SOURCES = ["plan.cpp", "pipeline.cpp", "encode.cu", "apply.cu", "dense.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2", "-I", os.path.join(HERE, "..", "include")]
 

@@ -141,6 +141,13 @@ int apply_launch(const struct ::dcr_plan* plan, struct ::dcr_recv_state* st, con
 int dense_launch(const struct ::dcr_plan* plan, const void* const* shards, void* target,
                  cudaStream_t s);
 
+// status of one encode / apply from the host mirror of its device scratch
+int encode_result(const struct ::dcr_plan* plan, const void* head, size_t cap, size_t* payload_size,
+                  uint64_t* changed, bool accumulate);
+int apply_result(struct ::dcr_recv_state* st, const ApplyScratch& a, dcr_apply_result* result);
+
+void pipe_release(const struct ::dcr_plan* plan);
+
 int set_error(int code, const char* fmt, ...);
 int cuda_error(cudaError_t e, const char* what);
 
@@ -182,6 +189,9 @@ struct dcr_plan {
     cudaEvent_t ev[8] = {};
     mutable dcr_profile prof = {};
     mutable bool prof_encode_due = false, prof_apply_due = false;   // events recorded, durations not read
+    // dcr_refit_pipelined: its copy stream and events (created on first use)
+    mutable cudaStream_t pipe_copy = nullptr;
+    mutable cudaEvent_t pipe_ev[8] = {};
 };
 
 struct dcr_recv_state {

@@ -185,6 +185,7 @@ void plan_free_device(dcr_plan* p)
         if (e) cudaEventDestroy(e);
         e = nullptr;
     }
+    pipe_release(p);
     cudaFree(p->d_chunks);
     cudaFree(p->d_src);
     cudaFree(p->d_dst);
@@ -498,42 +499,33 @@ extern "C" int dcr_encode(const dcr_plan* p, uint32_t mode, uint32_t window,
         p->prof_encode_due = true;   // durations read from the events when asked for
         p->prof.encode_valid = 1;
     }
-    const EncScratch* st = static_cast<const EncScratch*>(p->h_enc);
+    return encode_result(p, p->h_enc, payload ? cap : 0, payload_size, changed_per_tensor, false);
+}
+
+namespace dcr {
+
+int encode_result(const dcr_plan* p, const void* head, size_t cap, size_t* payload_size, uint64_t* changed,
+                  bool accumulate)
+{
+    const EncScratch* st = static_cast<const EncScratch*>(head);
     *payload_size = st->total;
-    if (changed_per_tensor) {
-        const uint64_t* cnt = reinterpret_cast<const uint64_t*>(static_cast<const char*>(p->h_enc) +
+    if (changed) {
+        const uint64_t* cnt = reinterpret_cast<const uint64_t*>(static_cast<const char*>(head) +
                                                                 sizeof(EncScratch));
-        memcpy(changed_per_tensor, cnt, p->descs.size() * 8);
+        if (accumulate)
+            for (size_t i = 0; i < p->descs.size(); ++i) changed[i] += cnt[i];
+        else
+            memcpy(changed, cnt, p->descs.size() * 8);
     }
     if (st->err) return set_error(st->err, "dcr_encode: device error %d", st->err);
-    if (st->total > cap || !payload)
+    if (st->total > cap)
         return set_error(DCR_ERR_CAPACITY, "dcr_encode: payload needs %llu bytes, capacity %zu",
                          (unsigned long long)st->total, cap);
     return DCR_OK;
 }
 
-static int apply_common(const dcr_plan* p, dcr_recv_state* st, const void* payload, size_t size,
-                        void* target, uint64_t abort_at, uint32_t split, int retry_only,
-                        dcr_apply_result* result, void* stream)
+int apply_result(dcr_recv_state* st, const ApplyScratch& a, dcr_apply_result* result)
 {
-    if (result) memset(result, 0, sizeof(*result));
-    if (!p || !st || !payload || !target) return set_error(DCR_ERR_INVALID, "dcr_apply: NULL argument");
-    if (st->plan != p) return set_error(DCR_ERR_INVALID, "dcr_apply: state belongs to another plan");
-    if (size < kStreamHdr) return set_error(DCR_ERR_CORRUPT, "dcr_apply: stream shorter than its header");
-    if (!aligned16(payload) || !aligned16(target))
-        return set_error(DCR_ERR_INVALID, "dcr_apply: payload/target not 16-byte aligned");
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    int rc = apply_launch(p, st, payload, size, target, abort_at, split, retry_only, s);
-    if (rc) return rc;
-    cudaError_t e = cudaMemcpyAsync(st->h_scratch, st->d_scratch, sizeof(ApplyScratch),
-                                    cudaMemcpyDeviceToHost, s);
-    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
-    if (e != cudaSuccess) return cuda_error(e, "dcr_apply status read");
-    if (p->profiling) {
-        p->prof_apply_due = true;
-        p->prof.apply_valid = 1;
-    }
-    const ApplyScratch& a = *st->h_scratch;
     if (result) {
         result->target_version = a.target_version;
         result->n_frames = a.n_frames;
@@ -559,6 +551,32 @@ static int apply_common(const dcr_plan* p, dcr_recv_state* st, const void* paylo
         if (result) result->committed = 1;
     }
     return DCR_OK;
+}
+
+}  // namespace dcr
+
+static int apply_common(const dcr_plan* p, dcr_recv_state* st, const void* payload, size_t size,
+                        void* target, uint64_t abort_at, uint32_t split, int retry_only,
+                        dcr_apply_result* result, void* stream)
+{
+    if (result) memset(result, 0, sizeof(*result));
+    if (!p || !st || !payload || !target) return set_error(DCR_ERR_INVALID, "dcr_apply: NULL argument");
+    if (st->plan != p) return set_error(DCR_ERR_INVALID, "dcr_apply: state belongs to another plan");
+    if (size < kStreamHdr) return set_error(DCR_ERR_CORRUPT, "dcr_apply: stream shorter than its header");
+    if (!aligned16(payload) || !aligned16(target))
+        return set_error(DCR_ERR_INVALID, "dcr_apply: payload/target not 16-byte aligned");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int rc = apply_launch(p, st, payload, size, target, abort_at, split, retry_only, s);
+    if (rc) return rc;
+    cudaError_t e = cudaMemcpyAsync(st->h_scratch, st->d_scratch, sizeof(ApplyScratch),
+                                    cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_error(e, "dcr_apply status read");
+    if (p->profiling) {
+        p->prof_apply_due = true;
+        p->prof.apply_valid = 1;
+    }
+    return apply_result(st, *st->h_scratch, result);
 }
 
 extern "C" int dcr_apply(const dcr_plan* p, dcr_recv_state* st, const void* payload, size_t size,

@@ -253,6 +253,40 @@ int dcr_apply_retry(const dcr_plan* plan, dcr_recv_state* state, const void* pay
 int dcr_apply_noalloc(const dcr_plan* plan, dcr_recv_state* state, const void* payload, size_t size,
                       void* target, dcr_apply_result* result, void* stream);
 
+/* Pipelined refit of every window through host memory (paper summary,
+ * "Pipelined transfer": a window's stream is built while the previous one
+ * is sent; popular write-up, the transfer step).  Same frames, dedup, commit
+ * rule and errors as calling, window by window in order, dcr_encode, a copy
+ * of the stream from device to pinned host memory and back, and dcr_apply
+ * (dcr_apply_retry for DCR_MODE_OVERWRITE_ONLY); with two buffers of each
+ * kind, window k's copies run on a second stream while window k+1 is encoded
+ * and window k-1 applied on `stream`.  device_buf (device, 256-byte aligned)
+ * and host_buf (pinned host memory from cudaMallocHost or cudaHostAlloc,
+ * 256-byte aligned) are caller-owned scratch of at least the sizes
+ * dcr_pipeline_sizes gives; the call returns after all its work has finished.
+ * changed_per_tensor (host, n_tensors entries, nullable) gets the counts of
+ * all windows; stats (nullable) the totals.  On an error the work already in
+ * flight finishes first, and the receiver state records only windows whose
+ * apply status was checked.  The plan keeps the call's copy stream and
+ * events (created on first use): calls on one plan must not overlap, as for
+ * dcr_encode.  Kernel timing (dcr_plan_last_profile) covers dcr_encode /
+ * dcr_apply calls only.  Errors: DCR_ERR_INVALID (arguments,
+ * buffers too small, unaligned or not pinned), the errors of dcr_encode and
+ * dcr_apply, DCR_ERR_CUDA. */
+typedef struct {
+    uint64_t windows;             /* windows applied and checked */
+    uint64_t payload_bytes;       /* stream bytes of all windows (each crossed host memory twice) */
+    uint64_t max_window_payload;
+    uint32_t committed;           /* 1 if target_version was committed */
+    uint32_t reserved;
+} dcr_pipeline_stats;
+int dcr_pipeline_sizes(const dcr_plan* plan, size_t* device_bytes, size_t* host_bytes);
+int dcr_refit_pipelined(const dcr_plan* plan, dcr_recv_state* state, uint32_t mode,
+                        const void* const* old_shards, const void* const* new_shards,
+                        uint64_t base_version, uint64_t target_version, void* target,
+                        void* device_buf, size_t device_bytes, void* host_buf, size_t host_bytes,
+                        uint64_t* changed_per_tensor, dcr_pipeline_stats* stats, void* stream);
+
 /* Kernel timing (tracing aid).  When on, the library records CUDA events on
  * the caller's stream around each of its kernels; dcr_plan_last_profile
  * returns the durations in milliseconds of the kernels of the latest

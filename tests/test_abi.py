@@ -93,4 +93,8 @@ def test_calls_reject_null_handles():
     h = ctypes.c_void_p()
     assert L.dcr_recv_state_create(None, 0, ctypes.byref(h)) == dcr.ERR_INVALID
     assert L.dcr_plan_set_profiling(None, 1) == dcr.ERR_INVALID
+    dev, host = ctypes.c_size_t(), ctypes.c_size_t()
+    assert L.dcr_pipeline_sizes(None, ctypes.byref(dev), ctypes.byref(host)) == dcr.ERR_INVALID
+    assert L.dcr_refit_pipelined(None, None, 0, None, None, 0, 1, None, None, 0, None, 0, None, None,
+                                 None) == dcr.ERR_INVALID
     assert "NULL" in dcr.last_error()
