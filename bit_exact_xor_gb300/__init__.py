@@ -25,6 +25,7 @@ STATUS_NAMES = {0: "OK", -1: "INVALID", -2: "CAPACITY", -3: "CORRUPT", -4: "VERS
 REPLICATED, SPLIT_ROWS, SPLIT_COLS, RESIDUAL_QKV_INTERLEAVED = 0, 1, 2, 3
 LAYOUT_CANONICAL, LAYOUT_ROWGROUP_INTERLEAVE = 0, 1
 MODE_HYBRID, MODE_OVERWRITE_ONLY = 0, 1
+ENCODER_AUTO, ENCODER_WIDE, ENCODER_DEEP = 0, 1, 2
 
 
 class DcrError(RuntimeError):
@@ -47,7 +48,7 @@ class TensorDesc(ctypes.Structure):
 
 
 class PlanOpts(ctypes.Structure):
-    _fields_ = [("window_bytes", ctypes.c_uint64), ("reserved", ctypes.c_uint32 * 6)]
+    _fields_ = [("window_bytes", ctypes.c_uint64), ("encoder", ctypes.c_uint32), ("reserved", ctypes.c_uint32 * 5)]
 
 
 class PlanInfo(ctypes.Structure):
@@ -166,10 +167,10 @@ def check(rc):
 class Plan:
     """dcr_plan_build over a list of TensorDesc."""
 
-    def __init__(self, descs, window_bytes=0):
+    def __init__(self, descs, window_bytes=0, encoder=0):
         arr = (TensorDesc * len(descs))(*descs)
         self._names = [d.name for d in descs]
-        opts = PlanOpts(window_bytes)
+        opts = PlanOpts(window_bytes, encoder)
         h = ctypes.c_void_p()
         check(lib().dcr_plan_build(arr, len(descs), ctypes.byref(opts), ctypes.byref(h)))
         self.h = h

@@ -122,6 +122,7 @@ struct Part {
 struct KernelConfig {
     int num_sms = 0;
     int enc_blocks_per_sm = 0;
+    int enc_deep_blocks_per_sm = 0;
     int restream_blocks_per_sm = 0;
     int spill_blocks_per_sm = 0;
     int apply_blocks_per_sm = 0;
@@ -160,6 +161,7 @@ struct dcr_plan {
     std::vector<dcr::ChunkDesc> chunks;
     std::vector<uint64_t> win_start;  // n_windows + 1 chunk ids
     uint64_t window_bytes = 0;
+    uint32_t encoder = DCR_ENCODER_AUTO;
     uint64_t n_chunks = 0;
     uint64_t canonical_bytes = 0;
     uint64_t hash = 0;

@@ -77,6 +77,8 @@ constexpr int kRing = 512;                        // event ring entries per warp
 constexpr int kAppend = 256;                      // events appended to the ring at most at once
 constexpr int kStep = 1024;                       // bytes per step: 32 contiguous bytes per lane
 constexpr int kNS = 3;                            // landing stages: kNS - 1 steps in flight
+constexpr int kNSDeep = 12;                       // ... in the deep variant for windows of few chunks
+constexpr int kDeepWarps = 2;                     // warps per CTA of the deep variant
 constexpr int kMSegCache = 64;                    // sender pieces cached per warp
 constexpr uint32_t kSlotBody = kEncSlot - kFrameHdr;   // frame body bytes a slot holds
 // spill_kernel
@@ -108,17 +110,22 @@ struct EncArgs {
     uint8_t* slots;            // kEncSlot bytes per chunk
 };
 
-// encode_kernel: one warp's shared memory
-struct __align__(16) WarpSmem {
-    uint4 land[kNS][2][64];            // landing stages [stage][old, new][16-byte slot]: the
+// encode_kernel: one warp's shared memory with NS landing stages
+template <int NS>
+struct __align__(16) WarpSmemT {
+    uint4 land[NS][2][64];             // landing stages [stage][old, new][16-byte slot]: the
                                        // step's bytes 32 L + 16 h in slot land_slot(L, h)
     uint16_t pos[kRing];               // event ring: byte position in the chunk
     uint8_t val[kRing];                //             mask byte
     Seg segs[kMSegCache];              // the chunk's sender pieces
 };
+using WarpSmem = WarpSmemT<kNS>;
+using WarpSmemDeep = WarpSmemT<kNSDeep>;
 // overwrite chunks keep their record values in the ring's storage
 constexpr int kValStage = int(sizeof(uint16_t) + sizeof(uint8_t)) * kRing;
 static_assert(offsetof(WarpSmem, val) == offsetof(WarpSmem, pos) + sizeof(uint16_t) * kRing,
+              "ring storage is contiguous");
+static_assert(offsetof(WarpSmemDeep, val) == offsetof(WarpSmemDeep, pos) + sizeof(uint16_t) * kRing,
               "ring storage is contiguous");
 static_assert(kAppend + 31 <= kRing, "a spilled chunk's unparsed events fit the ring");
 
@@ -447,7 +454,8 @@ __device__ __forceinline__ void gather_bytes(const EncArgs& A, const Seg* segs, 
 
 // The stream loop of any chunk (overwrite records, 4-bit elements, pieces
 // that are not 16-byte aligned); stream_fast below is the common case.
-__device__ __forceinline__ void stream_chunk(const EncArgs& A, WarpSmem& W, const ChunkDesc& cd, const Seg* segs,
+template <int NS>
+__device__ __forceinline__ void stream_chunk(const EncArgs& A, WarpSmemT<NS>& W, const ChunkDesc& cd, const Seg* segs,
                                              int lane, uint8_t* body, uint32_t cap, uint8_t* vals, int ncap,
                                              uint32_t& changed, Parse& P, int& tail, int& np, int& units,
                                              bool& spill, bool& bad)
@@ -461,7 +469,7 @@ __device__ __forceinline__ void stream_chunk(const EncArgs& A, WarpSmem& W, cons
     const int nsteps = (raw + kStep - 1) / kStep;
     const RingSrc R{W.pos, W.val};
 
-    // step s of the chunk into landing stage s % kNS (one commit group per
+    // step s of the chunk into landing stage s % NS (one commit group per
     // step); each copy instruction covers 512 contiguous bytes
     int cur = 0;
     auto issue = [&](int s) {
@@ -473,8 +481,8 @@ __device__ __forceinline__ void stream_chunk(const EncArgs& A, WarpSmem& W, cons
                     const uint32_t q = 512u * g + 16u * lane;   // byte of the step
                     const uint32_t x = x0 + q;
                     const int slot = land_slot(int(q >> 5), int(lane & 1));
-                    uint4* lo = &W.land[s % kNS][0][slot];
-                    uint4* ln = &W.land[s % kNS][1][slot];
+                    uint4* lo = &W.land[s % NS][0][slot];
+                    uint4* ln = &W.land[s % NS][1][slot];
                     if (x >= uint32_t(raw)) {
                         *lo = *ln = make_uint4(0u, 0u, 0u, 0u);
                     } else if (vec) {
@@ -498,22 +506,22 @@ __device__ __forceinline__ void stream_chunk(const EncArgs& A, WarpSmem& W, cons
 
     const uint32_t lt = (1u << lane) - 1u;
 #pragma unroll
-    for (int s = 0; s < kNS - 1; ++s) issue(s);
+    for (int s = 0; s < NS - 1; ++s) issue(s);
     for (int s = 0;; ++s) {
         const bool more = s < nsteps;
         const uint32_t x = uint32_t(s) * kStep + 32u * lane;   // the lane's first byte
         uint4 m0 = make_uint4(0u, 0u, 0u, 0u), m1 = m0, n0 = m0, n1 = m0;
         uint32_t z = 0;   // non-zero mask bytes (XOR) or changed units (overwrite) of the lane's 32
         if (more) {
-            issue(s + kNS - 1);
-            cp_async_wait<kNS - 1>();   // this lane's copies of step s have landed
+            issue(s + NS - 1);
+            cp_async_wait<NS - 1>();   // this lane's copies of step s have landed
             const int s0 = land_slot(lane, 0), s1 = land_slot(lane, 1);
             // a lane reads 16-byte slots that other lanes' copies filled
             __syncwarp();
-            n0 = W.land[s % kNS][1][s0];
-            n1 = W.land[s % kNS][1][s1];
-            m0 = xor4(W.land[s % kNS][0][s0], n0);
-            m1 = xor4(W.land[s % kNS][0][s1], n1);
+            n0 = W.land[s % NS][1][s0];
+            n1 = W.land[s % NS][1][s1];
+            m0 = xor4(W.land[s % NS][0][s0], n0);
+            m1 = xor4(W.land[s % NS][0][s1], n1);
             z = nz32(m0, m1);
             if (bits == 16) {
                 changed += __popc((z | (z >> 1)) & 0x55555555u);
@@ -600,11 +608,11 @@ __device__ __forceinline__ void stream_chunk(const EncArgs& A, WarpSmem& W, cons
 // The stream loop of the common chunk (XOR, 16-byte-aligned pieces, 16- or
 // 8-bit elements): the same steps, events and parse groups as stream_chunk
 // with less work per step.  Landing stages rotate instead of being indexed
-// modulo kNS, this lane's copy and read addresses are worked out once, the
+// modulo NS, this lane's copy and read addresses are worked out once, the
 // warp looks up the piece of a step once, and the last groups are parsed
 // after the loop.
-template <int kBits>
-__device__ __forceinline__ void stream_fast(const EncArgs& A, WarpSmem& W, const ChunkDesc& cd, const Seg* segs,
+template <int kBits, int NS>
+__device__ __forceinline__ void stream_fast(const EncArgs& A, WarpSmemT<NS>& W, const ChunkDesc& cd, const Seg* segs,
                                             int lane, uint8_t* body, uint32_t cap, uint32_t& changed, Parse& P,
                                             int& tail, int& np, bool& spill, bool& bad)
 {
@@ -658,18 +666,17 @@ __device__ __forceinline__ void stream_fast(const EncArgs& A, WarpSmem& W, const
         cp_async_commit();
     };
 
-    static_assert(kNS == 3, "two steps ahead");
-    issue(0, 0);
-    issue(1, 1);
-    uint32_t st_in = 2, st_out = 0;
+#pragma unroll
+    for (int i = 0; i < NS - 1; ++i) issue(i, uint32_t(i));   // NS - 1 steps ahead
+    uint32_t st_in = NS - 1, st_out = 0;
     for (int s = 0; s < nsteps; ++s) {
-        issue(s + 2, st_in);
-        st_in = st_in == kNS - 1 ? 0u : st_in + 1;
-        cp_async_wait<kNS - 1>();   // this lane's copies of step s have landed
+        issue(s + NS - 1, st_in);
+        st_in = st_in == NS - 1 ? 0u : st_in + 1;
+        cp_async_wait<NS - 1>();   // this lane's copies of step s have landed
         __syncwarp();               // ... and the other lanes' (read below)
         const uint4 n0 = W.land[st_out][1][rs0], n1 = W.land[st_out][1][rs1];
         const uint4 m0 = xor4(W.land[st_out][0][rs0], n0), m1 = xor4(W.land[st_out][0][rs1], n1);
-        st_out = st_out == kNS - 1 ? 0u : st_out + 1;
+        st_out = st_out == NS - 1 ? 0u : st_out + 1;
         const uint32_t z = nz32(m0, m1);
         changed += kBits == 16 ? __popc((z | (z >> 1)) & 0x55555555u) : __popc(z);
         // warp prefix of the per-lane counts: two ballots when no lane has
@@ -729,7 +736,8 @@ __device__ __forceinline__ void stream_fast(const EncArgs& A, WarpSmem& W, const
     }
 }
 
-__device__ __forceinline__ void encode_chunk(const EncArgs& A, WarpSmem& W, uint32_t k, int lane)
+template <int NS>
+__device__ __forceinline__ void encode_chunk(const EncArgs& A, WarpSmemT<NS>& W, uint32_t k, int lane)
 {
     const ChunkDesc cd = A.chunks[A.chunk_begin + k];
     const int raw = int(cd.raw_len);
@@ -754,9 +762,9 @@ __device__ __forceinline__ void encode_chunk(const EncArgs& A, WarpSmem& W, uint
     int tail = 0, np = 0, units = 0;
     bool spill = false, bad = false;
     if (!overwrite && vec && cd.bits == 16)
-        stream_fast<16>(A, W, cd, segs, lane, body, kSlotBody, changed, P, tail, np, spill, bad);
+        stream_fast<16, NS>(A, W, cd, segs, lane, body, kSlotBody, changed, P, tail, np, spill, bad);
     else if (!overwrite && vec && cd.bits == 8)
-        stream_fast<8>(A, W, cd, segs, lane, body, kSlotBody, changed, P, tail, np, spill, bad);
+        stream_fast<8, NS>(A, W, cd, segs, lane, body, kSlotBody, changed, P, tail, np, spill, bad);
     else
         stream_chunk(A, W, cd, segs, lane, body, kSlotBody, vstage, ncap, changed, P, tail, np, units, spill, bad);
     changed = __reduce_add_sync(kFull, changed);
@@ -813,11 +821,12 @@ __device__ __forceinline__ void encode_chunk(const EncArgs& A, WarpSmem& W, uint
     __syncwarp();   // the ring is reused by the next chunk
 }
 
+template <int NS>
 __global__ void __launch_bounds__(kMThreads, 4) encode_kernel(EncArgs A)
 {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     const int lane = threadIdx.x & 31;
-    WarpSmem& W = reinterpret_cast<WarpSmem*>(smem_raw)[threadIdx.x >> 5];
+    WarpSmemT<NS>& W = reinterpret_cast<WarpSmemT<NS>*>(smem_raw)[threadIdx.x >> 5];
     for (;;) {
         uint32_t k = 0;
         if (lane == 0) {
@@ -866,9 +875,9 @@ __device__ __forceinline__ void restream_chunk(const EncArgs& A, WarpSmem& W, ui
         stream_chunk(A, W, cd, segs, lane, body, R.body_len, body + voff, int(nu), changed, P, tail, np, units,
                      spill, bad);
     else if (vec && cd.bits == 16)
-        stream_fast<16>(A, W, cd, segs, lane, body, R.body_len, changed, P, tail, np, spill, bad);
+        stream_fast<16, kNS>(A, W, cd, segs, lane, body, R.body_len, changed, P, tail, np, spill, bad);
     else if (vec && cd.bits == 8)
-        stream_fast<8>(A, W, cd, segs, lane, body, R.body_len, changed, P, tail, np, spill, bad);
+        stream_fast<8, kNS>(A, W, cd, segs, lane, body, R.body_len, changed, P, tail, np, spill, bad);
     else
         stream_chunk(A, W, cd, segs, lane, body, R.body_len, nullptr, 0, changed, P, tail, np, units, spill, bad);
     changed = __reduce_add_sync(kFull, changed);
@@ -1194,6 +1203,7 @@ __global__ void __launch_bounds__(kSThreads, 2) spill_kernel(EncArgs A)
 }
 
 constexpr size_t kMainSmem = sizeof(WarpSmem) * kMWarps;
+constexpr size_t kDeepSmem = sizeof(WarpSmemDeep) * kDeepWarps;
 
 }  // namespace
 
@@ -1203,14 +1213,20 @@ int encode_kernel_config(KernelConfig* kc)
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&kc->num_sms, cudaDevAttrMultiProcessorCount, dev);
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(encode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kMainSmem));
+        e = cudaFuncSetAttribute(encode_kernel<kNS>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kMainSmem));
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(encode_kernel<kNSDeep>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 int(kDeepSmem));
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(restream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kMainSmem));
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(spill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sizeof(Buf)));
     if (e == cudaSuccess)
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&kc->enc_blocks_per_sm, encode_kernel, kMThreads,
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&kc->enc_blocks_per_sm, encode_kernel<kNS>, kMThreads,
                                                           kMainSmem);
+    if (e == cudaSuccess)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&kc->enc_deep_blocks_per_sm, encode_kernel<kNSDeep>,
+                                                          32 * kDeepWarps, kDeepSmem);
     if (e == cudaSuccess)
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&kc->restream_blocks_per_sm, restream_kernel, kMThreads,
                                                           kMainSmem);
@@ -1218,7 +1234,8 @@ int encode_kernel_config(KernelConfig* kc)
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&kc->spill_blocks_per_sm, spill_kernel, kSThreads,
                                                           sizeof(Buf));
     if (e != cudaSuccess) return cuda_error(e, "encode kernel configuration");
-    if (kc->enc_blocks_per_sm < 1 || kc->restream_blocks_per_sm < 1 || kc->spill_blocks_per_sm < 1)
+    if (kc->enc_blocks_per_sm < 1 || kc->enc_deep_blocks_per_sm < 1 || kc->restream_blocks_per_sm < 1 ||
+        kc->spill_blocks_per_sm < 1)
         return set_error(DCR_ERR_CUDA, "encode kernels do not fit on an SM");
     return DCR_OK;
 }
@@ -1252,8 +1269,18 @@ int encode_launch(const dcr_plan* P, uint32_t mode, uint32_t window, const void*
     const unsigned warps = unsigned(P->kc.num_sms * P->kc.enc_blocks_per_sm * kMWarps);
     unsigned grid = unsigned(P->kc.num_sms * P->kc.enc_blocks_per_sm);
     if (warps > A.chunk_count) grid = (A.chunk_count + kMWarps - 1) / kMWarps;
+    // a window of few chunks leaves most warp slots empty: then one chunk per
+    // warp of the deep variant, spread over all SMs, is faster
+    const unsigned deep_warps = unsigned(P->kc.num_sms * P->kc.enc_deep_blocks_per_sm * kDeepWarps);
+    const bool deep = P->encoder == DCR_ENCODER_DEEP || (P->encoder == DCR_ENCODER_AUTO && A.chunk_count <= deep_warps);
+    unsigned dgrid = (A.chunk_count + kDeepWarps - 1) / kDeepWarps;
+    if (dgrid > deep_warps / kDeepWarps) dgrid = deep_warps / kDeepWarps;
+    if (dgrid == 0) dgrid = 1;
     if (P->profiling) cudaEventRecord(P->ev[0], s);
-    encode_kernel<<<grid, kMThreads, kMainSmem, s>>>(A);
+    if (deep)
+        encode_kernel<kNSDeep><<<dgrid, 32 * kDeepWarps, kDeepSmem, s>>>(A);
+    else
+        encode_kernel<kNS><<<grid, kMThreads, kMainSmem, s>>>(A);
     if (P->profiling) cudaEventRecord(P->ev[1], s);
     scan_kernel<<<1, 1024, 0, s>>>(A, P->hash, base_v, target_v, window);
     unsigned cgrid = (A.chunk_count + 7) / 8;

@@ -94,6 +94,11 @@ enum {
 };
 
 enum { DCR_MODE_HYBRID = 0, DCR_MODE_OVERWRITE_ONLY = 1 };
+/* Encoder kernel variant (dcr_plan_opts.encoder); both produce the same
+ * frames.  WIDE: many warps per SM, three landing stages each; DEEP: fewer
+ * warps with twelve landing stages, faster when a window has fewer chunks
+ * than the GPU has warp slots; AUTO picks by window size. */
+enum { DCR_ENCODER_AUTO = 0, DCR_ENCODER_WIDE = 1, DCR_ENCODER_DEEP = 2 };
 
 typedef struct dcr_plan dcr_plan;             /* opaque, library owned */
 typedef struct dcr_recv_state dcr_recv_state; /* opaque, library owned */
@@ -123,7 +128,8 @@ typedef struct {
     uint64_t window_bytes;   /* 0 = 16 GiB.  Windows pack whole tensors in
                                 order; a tensor larger than a window is cut at
                                 chunk boundaries.  At most 256 GiB. */
-    uint32_t reserved[6];
+    uint32_t encoder;        /* DCR_ENCODER_AUTO (0), _WIDE or _DEEP */
+    uint32_t reserved[5];
 } dcr_plan_opts;
 
 typedef struct {

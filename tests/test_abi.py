@@ -98,3 +98,13 @@ def test_calls_reject_null_handles():
     assert L.dcr_refit_pipelined(None, None, 0, None, None, 0, 1, None, None, 0, None, 0, None, None,
                                  None) == dcr.ERR_INVALID
     assert "NULL" in dcr.last_error()
+
+
+def test_plan_rejects_unknown_encoder_variant():
+    import ctypes
+    d = dcr.make_desc("t", 16, 64, 64, dcr.REPLICATED, 1, [0], 0)
+    arr = (dcr.TensorDesc * 1)(d)
+    opts = dcr.PlanOpts(0, 3)
+    h = ctypes.c_void_p()
+    rc = dcr.lib().dcr_plan_build(arr, 1, ctypes.byref(opts), ctypes.byref(h))
+    assert rc == dcr.ERR_INVALID and "encoder" in dcr.last_error() and h.value is None

@@ -77,8 +77,9 @@ def test_random_workloads_are_valid_for_the_oracle():
 
 
 @pytest.mark.gpu
+@pytest.mark.parametrize("encoder", ["wide", "deep"])
 @pytest.mark.parametrize("seed", SEEDS)
-def test_random_workload_parity(seed):
+def test_random_workload_parity(seed, encoder):
     wl = random_workload(seed)
     orc = oracle.Oracle(wl)
     olds, news = wl.host_arenas()
@@ -86,7 +87,8 @@ def test_random_workload_parity(seed):
     # 4-bit data the greedy matcher also finds repeated non-zero bytes, which
     # the zero-run parse leaves literal (up to ~1.25x there; bit-exact all the same)
     dense_bytes = any(t.elem_bits != 16 and t.frac > 0.1 for t in wl.tensors)
-    plan = dcr.Plan(descs_of(wl), window_bytes=wl.window_bytes)
+    plan = dcr.Plan(descs_of(wl), window_bytes=wl.window_bytes,
+                    encoder=dcr.ENCODER_WIDE if encoder == "wide" else dcr.ENCODER_DEEP)
     assert plan.info.plan_hash == orc.plan_hash and plan.n_windows == orc.n_windows
     d_old, d_new = to_device(olds), to_device(news)
     exp = orc.receiver_dense(news)

@@ -98,15 +98,17 @@ def test_crafted_workload_reaches_every_route():
 
 
 @pytest.mark.gpu
+@pytest.mark.parametrize("encoder", ["wide", "deep"])
 @pytest.mark.parametrize("mode", ["hybrid", "overwrite"])
-def test_every_route_matches_oracle(mode):
+def test_every_route_matches_oracle(mode, encoder):
     torch = pytest.importorskip("torch")
     import bit_exact_xor_gb300 as dcr
     from wl import descs_of, to_device
 
     wl, olds, news = crafted()
     orc = oracle.Oracle(wl)
-    plan = dcr.Plan(descs_of(wl), window_bytes=wl.window_bytes)
+    plan = dcr.Plan(descs_of(wl), window_bytes=wl.window_bytes,
+                    encoder=dcr.ENCODER_WIDE if encoder == "wide" else dcr.ENCODER_DEEP)
     assert plan.info.plan_hash == orc.plan_hash
     d_old, d_new = to_device(olds), to_device(news)
     dm = dcr.MODE_HYBRID if mode == "hybrid" else dcr.MODE_OVERWRITE_ONLY

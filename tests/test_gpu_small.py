@@ -384,7 +384,7 @@ def test_kernel_timing_profile():
     assert q.encode_valid == 0 and q.apply_valid == 0
 
 
-def _flip_case(elem_bits, rows, cols, flips, seed=5):
+def _flip_case(elem_bits, rows, cols, flips, seed=5, encoder=0):
     """One replicated tensor, old random, new = old XOR a non-zero byte at
     each canonical byte offset in `flips`; encode, compare with the oracle
     and apply both streams on the GPU."""
@@ -397,7 +397,7 @@ def _flip_case(elem_bits, rows, cols, flips, seed=5):
     for x in flips:
         new[x] ^= np.uint8(rng.randint(1, 256))
     orc = oracle.Oracle(wl)
-    plan = dcr.Plan(descs_of(wl))
+    plan = dcr.Plan(descs_of(wl), encoder=encoder)
     d_old, d_new = to_device([old]), to_device([new])
     pl = torch.zeros(plan.window(0).payload_bound, dtype=torch.uint8, device="cuda")
     rc, size, counts = dcr.encode(plan, d_old, d_new, pl)
@@ -425,7 +425,8 @@ def test_tiny_and_ragged_tensors(shape):
     _flip_case(bits, rows, cols, flips)
 
 
-def test_changes_near_the_end_of_a_chunk():
+@pytest.mark.parametrize("encoder", [dcr.ENCODER_WIDE, dcr.ENCODER_DEEP])
+def test_changes_near_the_end_of_a_chunk(encoder):
     # chunk i: one change i + 1 bytes before its end (the block's end rules:
     # last five bytes literal, no match starting in the last twelve), chunks
     # 20..39 the same after an early change (a long zero run to copy from),
@@ -437,5 +438,5 @@ def test_changes_near_the_end_of_a_chunk():
         flips += [(20 + i) * 65536 + 3, (20 + i) * 65536 + 65536 - 1 - i]
     flips += [40 * 65536 + 65536 - 1 - k for k in range(5)]
     flips += [41 * 65536 + 65536 - 1 - k for k in range(13)]
-    g, o = _flip_case(8, 42, 65536, flips)
+    g, o = _flip_case(8, 42, 65536, flips, encoder=encoder)
     assert len(frames_by_chunk(g)[1]) == 42
