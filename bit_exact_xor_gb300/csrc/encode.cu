@@ -20,7 +20,8 @@
 // encode_kernel.  One warp per chunk, chunks taken in ticket order, 24 warps
 // per SM.  The warp streams its chunk in 1 KiB steps: cp.async copies old
 // and new into a three-stage landing buffer in shared memory, so two steps
-// are in flight while one is processed.  It XORs and counts, and appends the
+// are in flight while one is processed.  (A second instantiation with twelve
+// stages and 2-warp CTAs serves windows with fewer chunks than warp slots.)  It XORs and counts, and appends the
 // positions and values of the non-zero mask bytes ("events") to a ring in
 // shared memory.  Every 32 events it runs one parse group (one event per
 // lane, connected by ballots and warp sums) that writes the LZ4 sequences
