@@ -78,7 +78,8 @@ struct Hdr {
     uint32_t window, flags, chunk_begin, chunk_count;
 };
 
-constexpr uint32_t kWin = 128;                // candidate sequence starts per walk window
+constexpr uint32_t kWinA = 128;               // candidate sequence starts per walk window: apply_kernel
+constexpr uint32_t kWinB = 160;               //                                          big_kernel
 constexpr uint32_t kEndFinal = 0x80000000u;   // the sequence is the block's last
 constexpr uint32_t kEndBad = 0x7FFFFFFFu;     // no valid sequence starts here
 constexpr uint8_t kStop = 0xFF;               // jump: the chain stops (end, error, window left)
@@ -87,6 +88,7 @@ constexpr uint8_t kStop = 0xFF;               // jump: the chain stops (end, err
 // non-zero output bytes so far, where a sequence starting at each byte of the
 // current window would end, and the starts of one batch of sequences
 struct __align__(16) AWarp {
+    static constexpr uint32_t kWin = kWinA;
     uint8_t body[kBodyCache];
     uint16_t ev[kAEvCap];
     uint32_t nxt[kWin];
@@ -99,6 +101,7 @@ struct __align__(16) AWarp {
 // global memory and their matches checked against a bitmap of the non-zero
 // output bytes, which has no capacity limit.
 struct __align__(16) BWarp {
+    static constexpr uint32_t kWin = kWinB;   // denser masks: ~32 sequences per window
     uint32_t bits[kChunk / 32];
     uint32_t nxt[kWin];
     uint32_t r_ip[32];
@@ -332,7 +335,8 @@ __device__ __forceinline__ uint32_t seq_end_ldg(const uint8_t* src, uint32_t n, 
     return q + (mlx ? 3u : 2u);
 }
 
-// The warp takes the block a window of kWin body bytes at a time: every lane
+// The warp takes the block a window of kWin body bytes at a time (WS::kWin:
+// 128 for apply_kernel, 160 for the denser frames of big_kernel): every lane
 // works out where a sequence starting at each of its window bytes would end
 // (and, in two more passes, where the sequence two and four on starts), lane
 // 0 follows the chain from the current sequence four sequences per shared
@@ -355,6 +359,8 @@ __device__ int zsrc_apply(const ApplyArgs& A, const ChunkDesc& cd, const Seg* ds
                           uint32_t n, uint32_t raw, uint32_t lim, WS& W, int lane)
 {
     if (n == 0) return 0;   // an LZ4 block holds at least one token
+    constexpr uint32_t kWin = WS::kWin;
+    static_assert(kWin % 32 == 0 && kWin < kStop, "window: whole lane groups, offsets below kStop");
     const bool one = cd.dst_count == 1;
     const uint64_t base = one ? ds[0].addr - ds[0].off : 0ull;   // single receiver piece
     if constexpr (kBitmap) {
