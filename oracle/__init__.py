@@ -20,7 +20,8 @@ CHUNK = 65536
 OK, E_INVALID, E_CAPACITY, E_CORRUPT, E_VERSION, E_ABORTED, E_NOMEM, E_INCOMPLETE = (
     0, -1, -2, -3, -4, -5, -7, -8)
 MODE_HYBRID, MODE_OVERWRITE_ONLY = 0, 1
-K_XOR_LZ4, K_XOR_RAW, K_OVERWRITE, K_OVERWRITE_DENSE = 1, 2, 3, 4
+K_XOR_LZ4, K_XOR_RAW, K_OVERWRITE, K_OVERWRITE_DENSE, K_XOR_SNAPPY = 1, 2, 3, 4, 5
+CODEC_LZ4, CODEC_SNAPPY = 0, 1
 NO_FAULT = 2**64 - 1
 
 
@@ -73,7 +74,10 @@ def lib():
         L.orc_lz4_encode.argtypes = [VP, U64, VP, U64]
         L.orc_lz4_encode.restype = U64
         L.orc_lz4_decode.argtypes = [VP, U64, VP, U64, U32]
-        L.orc_encode.argtypes = [T, U32, U64, VP, VP, U32, U32, U64, U64, U32, VP, U64, P(U64), VP]
+        L.orc_snappy_encode.argtypes = [VP, U64, VP, U64]
+        L.orc_snappy_encode.restype = U64
+        L.orc_snappy_decode.argtypes = [VP, U64, VP, U64, U32]
+        L.orc_encode.argtypes = [T, U32, U64, VP, VP, U32, U32, U32, U64, U64, U32, VP, U64, P(U64), VP]
         L.orc_state_new.argtypes = [T, U32, U64, U64]
         L.orc_state_new.restype = VP
         L.orc_state_free.argtypes = [VP]
@@ -171,12 +175,12 @@ class Oracle:
         return out
 
     def encode(self, olds, news, window=0, mode=MODE_HYBRID, base_version=0, target_version=1,
-               threads=4, cap=None):
+               threads=4, cap=None, codec=CODEC_LZ4):
         size = ctypes.c_uint64()
         changed = np.zeros(self.n, dtype=np.uint64)
         if cap is None:
             rc = lib().orc_encode(self.t, self.n, self.W, self._shard_ptrs(olds),
-                                  self._shard_ptrs(news), mode, window, base_version,
+                                  self._shard_ptrs(news), mode, codec, window, base_version,
                                   target_version, threads, None, 0, ctypes.byref(size),
                                   _ptr(changed))
             if rc not in (OK, E_CAPACITY):
@@ -184,7 +188,7 @@ class Oracle:
             cap = size.value
         out = np.zeros(max(cap, 1), dtype=np.uint8)
         rc = lib().orc_encode(self.t, self.n, self.W, self._shard_ptrs(olds), self._shard_ptrs(news),
-                              mode, window, base_version, target_version, threads, _ptr(out), cap,
+                              mode, codec, window, base_version, target_version, threads, _ptr(out), cap,
                               ctypes.byref(size), _ptr(changed))
         if rc:
             raise ValueError("oracle encode failed (%d)" % rc)
@@ -242,4 +246,22 @@ def lz4_decode(block, raw_len, zsrc=False):
     block = np.ascontiguousarray(block, dtype=np.uint8)
     out = np.zeros(max(raw_len, 1), dtype=np.uint8)
     rc = lib().orc_lz4_decode(_ptr(block), block.size, _ptr(out), raw_len, int(zsrc))
+    return out[:raw_len] if rc == OK else None
+
+
+def snappy_encode(data):
+    data = np.ascontiguousarray(data, dtype=np.uint8)
+    cap = data.size + data.size // 60 + 16
+    out = np.zeros(cap, dtype=np.uint8)
+    n = lib().orc_snappy_encode(_ptr(data), data.size, _ptr(out), cap)
+    if n == 0:
+        raise ValueError("snappy encode overflow")
+    return out[:n].copy()
+
+
+def snappy_decode(block, raw_len, zsrc=False):
+    """Decoded bytes, or None if the block is malformed."""
+    block = np.ascontiguousarray(block, dtype=np.uint8)
+    out = np.zeros(max(raw_len, 1), dtype=np.uint8)
+    rc = lib().orc_snappy_decode(_ptr(block), block.size, _ptr(out), raw_len, int(zsrc))
     return out[:raw_len] if rc == OK else None

@@ -531,6 +531,159 @@ int orc_lz4_decode(const uint8_t* in, uint64_t n, uint8_t* out, uint64_t raw_len
     return op == raw_len ? ORC_OK : ORC_E_CORRUPT;
 }
 
+/* ---- Snappy block format ([P4] "A strong baseline with the Blackwell-
+ * native DE", footnote 4: LZ4 and Snappy are byte-oriented LZ77 codecs with
+ * literals and back copies and no entropy stage; one Snappy copy covers at
+ * most 64 bytes).  A block is the uncompressed length as a little-endian
+ * base-128 varint, then elements whose tag byte's low two bits give the type:
+ *   0 literal: length - 1 in the upper six bits when below 60; 60..63 mean
+ *     that 1..4 following bytes (little-endian) hold length - 1;
+ *   1 copy: length 4..11 as length - 4 in bits 2..4, offset bits 8..10 in
+ *     bits 5..7, then the offset's low byte;
+ *   2 copy: length 1..64 as length - 1 in the upper six bits, then a 2-byte
+ *     little-endian offset;
+ *   3 copy: the same with a 4-byte offset.
+ * Copies replicate forward byte by byte when they overlap. */
+static uint64_t sn_literal(uint8_t* out, uint64_t o, uint64_t cap, const uint8_t* lit, uint64_t ll, int* ovf)
+{
+    if (ll == 0) return o;
+    uint64_t v = ll - 1, nb = v < 60 ? 0 : v < 256 ? 1 : v < 65536 ? 2 : v < (1ull << 24) ? 3 : 4;
+    if (o + 1 + nb + ll > cap) { *ovf = 1; return o; }
+    out[o++] = (uint8_t)((nb ? 59 + nb : v) << 2);
+    for (uint64_t i = 0; i < nb; ++i) out[o++] = (uint8_t)(v >> (8 * i));
+    memcpy(out + o, lit, ll);
+    return o + ll;
+}
+
+static uint64_t sn_copy(uint8_t* out, uint64_t o, uint64_t cap, uint64_t off, uint64_t len, int* ovf)
+{
+    if (len >= 4 && len <= 11 && off < 2048) {
+        if (o + 2 > cap) { *ovf = 1; return o; }
+        out[o++] = (uint8_t)(1 | ((len - 4) << 2) | ((off >> 8) << 5));
+        out[o++] = (uint8_t)off;
+    } else {
+        if (o + 3 > cap) { *ovf = 1; return o; }
+        out[o++] = (uint8_t)(2 | ((len - 1) << 2));
+        out[o++] = (uint8_t)off;
+        out[o++] = (uint8_t)(off >> 8);
+    }
+    return o;
+}
+
+/* a match of len >= 4 bytes as copies of at most 64: 64 while at least 68
+ * remain, 60 if more than 64 remain, then the rest (never below 4) */
+static uint64_t sn_match(uint8_t* out, uint64_t o, uint64_t cap, uint64_t off, uint64_t len, int* ovf)
+{
+    while (len >= 68 && !*ovf) {
+        o = sn_copy(out, o, cap, off, 64, ovf);
+        len -= 64;
+    }
+    if (len > 64 && !*ovf) {
+        o = sn_copy(out, o, cap, off, 60, ovf);
+        len -= 60;
+    }
+    if (!*ovf) o = sn_copy(out, o, cap, off, len, ovf);
+    return o;
+}
+
+/* Plain greedy encoder with the same match finder as orc_lz4_encode (2^14
+ * slots of the most recent position of each 4-byte word's hash, every
+ * position inserted, forward extension only, offsets up to 65535); the
+ * format has no end-of-block rules, so matches may reach the last byte.
+ * Returns the block size, or 0 if cap is too small. */
+uint64_t orc_snappy_encode(const uint8_t* in, uint64_t n, uint8_t* out, uint64_t cap)
+{
+    int32_t* tab = (int32_t*)malloc(sizeof(int32_t) << LZ4_HASHLOG);
+    if (!tab) return 0;
+    for (uint32_t i = 0; i < (1u << LZ4_HASHLOG); ++i) tab[i] = -1;
+    int ovf = 0;
+    uint64_t o = 0, anchor = 0, p = 0;
+    for (uint64_t v = n;; v >>= 7) {   /* preamble */
+        if (o >= cap) { ovf = 1; break; }
+        out[o++] = (uint8_t)((v & 127) | (v >= 128 ? 128 : 0));
+        if (v < 128) break;
+    }
+    while (!ovf && p + 4 <= n) {
+        uint32_t w = rd32(in + p);
+        uint32_t h = (uint32_t)(w * 2654435761u) >> (32 - LZ4_HASHLOG);
+        int32_t cand = tab[h];
+        tab[h] = (int32_t)p;
+        if (cand >= 0 && p - (uint64_t)cand <= 65535 && rd32(in + cand) == w) {
+            uint64_t len = 4;
+            while (p + len < n && in[cand + len] == in[p + len]) ++len;
+            o = sn_literal(out, o, cap, in + anchor, p - anchor, &ovf);
+            if (!ovf) o = sn_match(out, o, cap, p - (uint64_t)cand, len, &ovf);
+            for (uint64_t q = p + 1; q < p + len && q + 4 <= n; ++q) {
+                uint32_t wq = rd32(in + q);
+                tab[(uint32_t)(wq * 2654435761u) >> (32 - LZ4_HASHLOG)] = (int32_t)q;
+            }
+            p += len;
+            anchor = p;
+        } else {
+            ++p;
+        }
+    }
+    if (!ovf) o = sn_literal(out, o, cap, in + anchor, n - anchor, &ovf);
+    free(tab);
+    return ovf ? 0 : o;
+}
+
+/* Strict decoder: the preamble must equal raw_len and fit in five bytes;
+ * every element must stay inside the block and the output; offsets must be
+ * non-zero and within the bytes produced so far; the block must produce
+ * exactly raw_len bytes.  With zsrc set, every copy must copy zero bytes. */
+int orc_snappy_decode(const uint8_t* in, uint64_t n, uint8_t* out, uint64_t raw_len, uint32_t zsrc)
+{
+    uint64_t ip = 0, op = 0, v = 0;
+    for (uint32_t shift = 0;; shift += 7) {
+        if (ip >= n || shift > 28) return ORC_E_CORRUPT;
+        uint32_t b = in[ip++];
+        v |= (uint64_t)(b & 127) << shift;
+        if (!(b & 128)) break;
+    }
+    if (v != raw_len) return ORC_E_CORRUPT;
+    while (ip < n) {
+        uint32_t tag = in[ip++];
+        uint64_t len, off;
+        if ((tag & 3) == 0) {
+            len = (uint64_t)(tag >> 2) + 1;
+            if ((tag >> 2) >= 60) {
+                uint32_t nb = (tag >> 2) - 59;
+                if (nb > n - ip) return ORC_E_CORRUPT;
+                len = 0;
+                for (uint32_t i = 0; i < nb; ++i) len |= (uint64_t)in[ip + i] << (8 * i);
+                len += 1;
+                ip += nb;
+            }
+            if (len > n - ip || len > raw_len - op) return ORC_E_CORRUPT;
+            memcpy(out + op, in + ip, len);
+            ip += len;
+            op += len;
+            continue;
+        }
+        if ((tag & 3) == 1) {
+            if (ip >= n) return ORC_E_CORRUPT;
+            len = ((tag >> 2) & 7) + 4;
+            off = ((uint64_t)(tag >> 5) << 8) | in[ip++];
+        } else {
+            uint32_t nb = (tag & 3) == 2 ? 2 : 4;
+            if (nb > n - ip) return ORC_E_CORRUPT;
+            len = (uint64_t)(tag >> 2) + 1;
+            off = 0;
+            for (uint32_t i = 0; i < nb; ++i) off |= (uint64_t)in[ip + i] << (8 * i);
+            ip += nb;
+        }
+        if (off == 0 || off > op || len > raw_len - op) return ORC_E_CORRUPT;
+        for (uint64_t k = 0; k < len; ++k) {
+            uint8_t b = out[op + k - off];
+            if (zsrc && b) return ORC_E_CORRUPT;
+            out[op + k] = b;
+        }
+        op += len;
+    }
+    return op == raw_len ? ORC_OK : ORC_E_CORRUPT;
+}
+
 /* ------------------------------------------------------------------------ */
 /* stream encode                                                            */
 /* ------------------------------------------------------------------------ */
@@ -559,6 +712,7 @@ typedef struct {
     const uint8_t* const* olds;
     const uint8_t* const* news;
     uint32_t mode;
+    uint32_t codec;
     uint64_t cb, cc;
     uint8_t** frames;
     uint64_t* flen;
@@ -622,13 +776,14 @@ static int encode_chunk(enc_job* J, uint64_t c, uint8_t* old_c, uint8_t* new_c, 
             body_len = rec;
         }
     } else {
-        uint64_t lz = orc_lz4_encode(mask, len, tmp, tmp_cap);
+        const int sn = J->codec == ORC_CODEC_SNAPPY;
+        uint64_t lz = sn ? orc_snappy_encode(mask, len, tmp, tmp_cap) : orc_lz4_encode(mask, len, tmp, tmp_cap);
         if (lz == 0 || lz >= len) {
             kind = ORC_K_XOR_RAW;
             body = mask;
             body_len = len;
         } else {
-            kind = ORC_K_XOR_LZ4;
+            kind = sn ? ORC_K_XOR_SNAPPY : ORC_K_XOR_LZ4;
             body = tmp;
             body_len = lz;
         }
@@ -685,11 +840,12 @@ static void run_pool(void* (*fn)(void*), void* arg, uint32_t threads)
  * A chunk whose mask is all zero sends no frame. */
 int orc_encode(const orc_tensor* t, uint32_t n, uint64_t window_bytes,
                const uint8_t* const* old_shards, const uint8_t* const* new_shards,
-               uint32_t mode, uint32_t window, uint64_t base_version, uint64_t target_version,
-               uint32_t threads, uint8_t* out, uint64_t cap, uint64_t* size,
+               uint32_t mode, uint32_t codec, uint32_t window, uint64_t base_version,
+               uint64_t target_version, uint32_t threads, uint8_t* out, uint64_t cap, uint64_t* size,
                uint64_t* changed_per_tensor)
 {
-    if (!old_shards || !new_shards || !size || mode > ORC_MODE_OVERWRITE_ONLY) return ORC_E_INVALID;
+    if (!old_shards || !new_shards || !size || mode > ORC_MODE_OVERWRITE_ONLY || codec > ORC_CODEC_SNAPPY)
+        return ORC_E_INVALID;
     layout_t L;
     int rc = layout_build(t, n, window_bytes, &L);
     if (rc) return rc;
@@ -701,6 +857,7 @@ int orc_encode(const orc_tensor* t, uint32_t n, uint64_t window_bytes,
     J.olds = old_shards;
     J.news = new_shards;
     J.mode = mode;
+    J.codec = codec;
     J.cb = L.win_start[window];
     J.cc = L.win_start[window + 1] - J.cb;
     J.frames = (uint8_t**)calloc(J.cc + 1, sizeof(uint8_t*));
@@ -861,14 +1018,14 @@ static int apply_frame(app_job* A, uint64_t f, uint8_t* mask)
     const uint8_t* h = pl + fo;
     uint32_t kind = h[4], bits = h[5], flags = (uint32_t)h[6] | ((uint32_t)h[7] << 8);
     uint64_t c = get32(h + 8), raw = get32(h + 12), bl = get32(h + 16);
-    if (get32(h) != FRAME_MAGIC || kind < ORC_K_XOR_LZ4 || kind > ORC_K_OVERWRITE_DENSE)
+    if (get32(h) != FRAME_MAGIC || kind < ORC_K_XOR_LZ4 || kind > ORC_K_XOR_SNAPPY)
         return ORC_E_CORRUPT;
     if (c < A->cb || c >= A->cb + A->cc || bl > A->frames_end - fo - FRAME_HDR) return ORC_E_CORRUPT;
     const part_t* p = &A->L->parts[A->L->chunk_part[c]];
     uint64_t off = (c - p->chunk0) * ORC_CHUNK;
     uint64_t len = p->bytes - off < ORC_CHUNK ? p->bytes - off : ORC_CHUNK;
     if (raw != len || bits != p->bits) return ORC_E_CORRUPT;
-    int is_xor = kind == ORC_K_XOR_LZ4 || kind == ORC_K_XOR_RAW;
+    int is_xor = kind == ORC_K_XOR_LZ4 || kind == ORC_K_XOR_RAW || kind == ORC_K_XOR_SNAPPY;
     if (A->retry_only && is_xor) return ORC_E_INVALID;
     if (f > A->abort_at) return ORC_OK; /* injected fault: never reached */
     int cut = f == A->abort_at;
@@ -890,6 +1047,8 @@ static int apply_frame(app_job* A, uint64_t f, uint8_t* mask)
         if (kind == ORC_K_XOR_RAW) {
             if (bl != raw) return ORC_E_CORRUPT;
             memcpy(mask, body, raw);
+        } else if (kind == ORC_K_XOR_SNAPPY) {
+            if (orc_snappy_decode(body, bl, mask, raw, flags & FRAME_ZSRC) != ORC_OK) return ORC_E_CORRUPT;
         } else if (orc_lz4_decode(body, bl, mask, raw, flags & FRAME_ZSRC) != ORC_OK) {
             return ORC_E_CORRUPT;
         }

@@ -8,7 +8,7 @@
  * accelerated weight teleportation" blog, section "Delta update algebra"):
  *   mask = old XOR new over the raw stored bits, changed values counted
  *   bitwise, shard data projected into canonical checkpoint coordinates,
- *   XOR masks LZ4-block encoded, non-affine (fused QKV) pieces sent as
+ *   XOR masks LZ4-block (or Snappy) encoded, non-affine (fused QKV) pieces sent as
  *   overwrite records; the receiver decodes and applies in place, with
  *   per-chunk dedup and an idempotent overwrite-only retry.
  * Each function in oracle.c cites the passage it follows.
@@ -27,7 +27,9 @@ extern "C" {
 enum { ORC_REPLICATED = 0, ORC_SPLIT_ROWS = 1, ORC_SPLIT_COLS = 2, ORC_RESIDUAL_QKV = 3 };
 enum { ORC_RECV_CANONICAL = 0, ORC_RECV_ROWGROUP = 1 };
 enum { ORC_MODE_HYBRID = 0, ORC_MODE_OVERWRITE_ONLY = 1 };
-enum { ORC_K_XOR_LZ4 = 1, ORC_K_XOR_RAW = 2, ORC_K_OVERWRITE = 3, ORC_K_OVERWRITE_DENSE = 4 };
+enum { ORC_K_XOR_LZ4 = 1, ORC_K_XOR_RAW = 2, ORC_K_OVERWRITE = 3, ORC_K_OVERWRITE_DENSE = 4,
+       ORC_K_XOR_SNAPPY = 5 };
+enum { ORC_CODEC_LZ4 = 0, ORC_CODEC_SNAPPY = 1 };   /* block codec of XOR masks */
 enum { ORC_OK = 0, ORC_E_INVALID = -1, ORC_E_CAPACITY = -2, ORC_E_CORRUPT = -3,
        ORC_E_VERSION = -4, ORC_E_ABORTED = -5, ORC_E_NOMEM = -7, ORC_E_INCOMPLETE = -8 };
 
@@ -63,12 +65,14 @@ void orc_xor(const uint8_t* a, const uint8_t* b, uint8_t* out, uint64_t n);
 uint64_t orc_count_changed(const uint8_t* mask, uint64_t nbytes, uint32_t elem_bits);
 uint64_t orc_lz4_encode(const uint8_t* in, uint64_t n, uint8_t* out, uint64_t cap);
 int orc_lz4_decode(const uint8_t* in, uint64_t n, uint8_t* out, uint64_t raw_len, uint32_t zsrc);
+uint64_t orc_snappy_encode(const uint8_t* in, uint64_t n, uint8_t* out, uint64_t cap);
+int orc_snappy_decode(const uint8_t* in, uint64_t n, uint8_t* out, uint64_t raw_len, uint32_t zsrc);
 
 /* stream */
 int orc_encode(const orc_tensor* t, uint32_t n, uint64_t window_bytes,
                const uint8_t* const* old_shards, const uint8_t* const* new_shards,
-               uint32_t mode, uint32_t window, uint64_t base_version, uint64_t target_version,
-               uint32_t threads, uint8_t* out, uint64_t cap, uint64_t* size,
+               uint32_t mode, uint32_t codec, uint32_t window, uint64_t base_version,
+               uint64_t target_version, uint32_t threads, uint8_t* out, uint64_t cap, uint64_t* size,
                uint64_t* changed_per_tensor);
 
 orc_state* orc_state_new(const orc_tensor* t, uint32_t n, uint64_t window_bytes, uint64_t version);

@@ -2,7 +2,7 @@
 import numpy as np
 
 import oracle
-from streamfmt import K_OVERWRITE, K_OVERWRITE_DENSE, K_XOR_LZ4, K_XOR_RAW, FRAME_ZSRC, parse
+from streamfmt import K_OVERWRITE, K_OVERWRITE_DENSE, K_XOR_LZ4, K_XOR_RAW, K_XOR_SNAPPY, FRAME_ZSRC, parse
 
 
 def frame_content(f):
@@ -11,6 +11,10 @@ def frame_content(f):
     overwrite records, ('dense', bytes) for dense overwrites."""
     if f["kind"] == K_XOR_LZ4:
         m = oracle.lz4_decode(f["body"], f["raw_len"], zsrc=bool(f["flags"] & FRAME_ZSRC))
+        assert m is not None, "oracle decoder rejected frame of chunk %d" % f["chunk"]
+        return ("mask", m)
+    if f["kind"] == K_XOR_SNAPPY:
+        m = oracle.snappy_decode(f["body"], f["raw_len"], zsrc=bool(f["flags"] & FRAME_ZSRC))
         assert m is not None, "oracle decoder rejected frame of chunk %d" % f["chunk"]
         return ("mask", m)
     if f["kind"] == K_XOR_RAW:

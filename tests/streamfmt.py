@@ -11,7 +11,7 @@ import numpy as np
 
 STREAM_MAGIC = b"DCRS"
 FRAME_MAGIC = b"DCRF"
-K_XOR_LZ4, K_XOR_RAW, K_OVERWRITE, K_OVERWRITE_DENSE = 1, 2, 3, 4
+K_XOR_LZ4, K_XOR_RAW, K_OVERWRITE, K_OVERWRITE_DENSE, K_XOR_SNAPPY = 1, 2, 3, 4, 5
 FLAG_OVERWRITE_ONLY = 1
 FRAME_ZSRC = 1
 
@@ -49,7 +49,7 @@ def check_structure(payload):
         assert hdr["chunk_begin"] <= f["chunk"] < hdr["chunk_begin"] + hdr["chunk_count"]
         assert f["chunk"] > prev, "ascending chunk order"
         prev = f["chunk"]
-        assert f["kind"] in (1, 2, 3, 4) and f["reserved"] == 0 and f["changed"] > 0
+        assert f["kind"] in (1, 2, 3, 4, 5) and f["reserved"] == 0 and f["changed"] > 0
         flen = (32 + f["body_len"] + 15) // 16 * 16
         pad = np.asarray(payload[f["offset"] + 32 + f["body_len"]:f["offset"] + flen])
         assert not pad.any(), "frame padding is zero"

@@ -165,6 +165,121 @@ def test_lz4_decoder_rejects_truncations_of_valid_blocks():
         assert oracle.lz4_decode(blk[:cut], d.size) is None or cut == blk.size
 
 
+# --------------------------------------------------------------------------
+# Snappy block format (same footnote: the other byte-oriented LZ77 codec; one
+# copy covers at most 64 bytes)
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("row", read_table("snappy_block_vectors.txt"), ids=lambda r: r[0])
+def test_snappy_decoder_hand_vectors(row):
+    name, blk, raw, exp = row
+    out = oracle.snappy_decode(np.frombuffer(bytes.fromhex(blk), dtype=np.uint8), int(raw))
+    if exp == "ERR":
+        assert out is None
+    else:
+        assert out is not None and bytes(out) == bytes.fromhex(exp)
+
+
+def test_snappy_greedy_encoder_hand_vectors():
+    enc = lambda b: bytes(oracle.snappy_encode(np.frombuffer(b, dtype=np.uint8)))
+    # shorter than a 4-byte word: one literal element
+    assert enc(b"xyz") == bytes([0x03, 0x08]) + b"xyz"
+    # "abcd" then a 4-byte copy at offset 4: a 1-byte-offset copy (tag 0x01)
+    assert enc(b"abcdabcd") == bytes([0x08, 0x0C]) + b"abcd" + bytes([0x01, 0x04])
+    # 11 x 'a': literal 'a', then 10 bytes at offset 1 (tag 1 | 6 << 2)
+    assert enc(b"a" * 11) == bytes([0x0B, 0x00, 0x61, 0x19, 0x01])
+    # 64 KiB of zeros: preamble 80 80 04, literal 00, then the 65535-byte
+    # match at offset 1 as 1023 copies of 64 (tag 2 | 63 << 2) and one of 63
+    z = enc(bytes(65536))
+    assert z == bytes([0x80, 0x80, 0x04, 0x00, 0x00]) + bytes([0xFE, 0x01, 0x00]) * 1023 + bytes([0xFA, 0x01, 0x00])
+
+
+def walk_snappy(blk):
+    """Independent element walker: (preamble, [(kind, length, offset)])."""
+    b = bytes(blk)
+    ip, v, shift = 0, 0, 0
+    while True:
+        x = b[ip]; ip += 1
+        v |= (x & 127) << shift
+        shift += 7
+        if not x & 128:
+            break
+    els = []
+    while ip < len(b):
+        tag = b[ip]; ip += 1
+        t = tag & 3
+        if t == 0:
+            n = (tag >> 2) + 1
+            if (tag >> 2) >= 60:
+                nb = (tag >> 2) - 59
+                n = int.from_bytes(b[ip:ip + nb], "little") + 1
+                ip += nb
+            els.append(("lit", n, 0))
+            ip += n
+        elif t == 1:
+            els.append(("copy", ((tag >> 2) & 7) + 4, ((tag >> 5) << 8) | b[ip]))
+            ip += 1
+        else:
+            nb = 2 if t == 2 else 4
+            els.append(("copy", (tag >> 2) + 1, int.from_bytes(b[ip:ip + nb], "little")))
+            ip += nb
+    return v, els
+
+
+def test_snappy_exhaustive_small_round_trips():
+    count = 0
+    for n in range(0, 7):
+        for tup in itertools.product((0x00, 0x01, 0xFF), repeat=n):
+            d = np.array(tup, dtype=np.uint8)
+            blk = oracle.snappy_encode(d)
+            pre, els = walk_snappy(blk)
+            assert pre == n and sum(e[1] for e in els) == n
+            out = oracle.snappy_decode(blk, n)
+            assert out is not None and np.array_equal(out, d)
+            count += 1
+    assert count == sum(3 ** n for n in range(7))
+
+
+@pytest.mark.parametrize("density", [0.0, 0.001, 0.01, 0.1, 0.5, 1.0])
+def test_snappy_random_round_trips(density):
+    rng = np.random.default_rng(int(density * 1000) + 11)
+    for n in list(rng.integers(0, 301, 40)) + [65536]:
+        d = np.zeros(int(n), dtype=np.uint8)
+        k = rng.random(int(n)) < density
+        d[k] = rng.integers(1, 256, int(k.sum()), dtype=np.uint8)
+        blk = oracle.snappy_encode(d)
+        pre, els = walk_snappy(blk)
+        assert pre == n and sum(e[1] for e in els) == n
+        assert all(1 <= e[1] <= 64 and e[2] >= 1 for e in els if e[0] == "copy")
+        out = oracle.snappy_decode(blk, int(n))
+        assert np.array_equal(out, d)
+
+
+def test_snappy_decoder_rejects_truncations_and_nonzero_copies_under_zsrc():
+    d = np.zeros(4000, dtype=np.uint8)
+    d[::97] = 3
+    blk = oracle.snappy_encode(d)
+    for cut in range(1, blk.size):
+        assert oracle.snappy_decode(blk[:cut], d.size) is None
+    e = np.zeros(200, dtype=np.uint8)
+    e[10] = 7
+    e[110] = 7  # the greedy encoder copies "07 00 00 .." from position 10
+    blk = oracle.snappy_encode(e)
+    assert oracle.snappy_decode(blk, 200) is not None
+    assert oracle.snappy_decode(blk, 200, zsrc=True) is None
+
+
+def test_lz4_is_smaller_than_snappy_on_zero_run_masks():
+    # the pages' reading: masks are mostly long zero runs, which one LZ4 match
+    # covers while Snappy needs a copy per 64 bytes.  (At a few percent of
+    # non-zero bytes the runs are short and Snappy's 2-byte copies win.)
+    rng = np.random.default_rng(3)
+    for density in (0.00085, 0.01):
+        d = np.zeros(65536, dtype=np.uint8)
+        k = rng.random(65536) < density
+        d[k] = rng.integers(1, 256, int(k.sum()), dtype=np.uint8)
+        assert oracle.lz4_encode(d).size < oracle.snappy_encode(d).size
+
+
 def test_zsrc_decoder_flag_rejects_nonzero_copies():
     d = np.zeros(200, dtype=np.uint8)
     d[10] = 7
