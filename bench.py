@@ -199,7 +199,7 @@ def cpu_baseline(wl, budget_s=12.0):
 def run_config(args, wl, nw, ws):
     """The workload description both arms print."""
     N = wl.canonical_bytes
-    return {"workload": WORKLOAD_NAMES[args.workload], "canonical_bytes": N,
+    return {"workload": WORKLOAD_NAMES[args.workload], "canonical_bytes": N, "codec": getattr(args, "codec", "lz4"),
             "tp": wl.tp, "windows": nw, "parallelism": "replicas" if ws > 1 else "single GPU",
             "l2": "inputs larger than L2 (2N = %.2f GB read per encode)" % (2 * N / 1e9)
             if 2 * N > 200e6 else "inputs fit in L2"}
@@ -254,7 +254,8 @@ def run_gpu(args):
 
     wl = build_workload(args.workload, args.frac)
     N = wl.canonical_bytes
-    plan = dcr.Plan(descs_of(wl), window_bytes=(args.window_mb << 20) or wl.window_bytes)
+    plan = dcr.Plan(descs_of(wl), window_bytes=(args.window_mb << 20) or wl.window_bytes,
+                    codec=dcr.CODEC_SNAPPY if args.codec == "snappy" else dcr.CODEC_LZ4)
     plan.set_profiling(True)
     olds, news = wl.device_arenas(torch)
     target = torch.empty(max(plan.info.recv_bytes, wl.recv_bytes), dtype=torch.uint8, device=dev)
@@ -497,6 +498,7 @@ def main():
                     help="change rate (sweep: 1 or more = fully random new buffer)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--window-mb", type=int, default=0, help="window size in MiB (0: the workload's)")
+    ap.add_argument("--codec", default="lz4", choices=["lz4", "snappy"], help="block codec of the XOR masks")
     ap.add_argument("--pipeline", action="store_true",
                     help="also time dcr_refit_pipelined against the same windows in series")
     ap.add_argument("--no-cpu-baseline", action="store_true")

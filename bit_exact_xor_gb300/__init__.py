@@ -26,6 +26,7 @@ REPLICATED, SPLIT_ROWS, SPLIT_COLS, RESIDUAL_QKV_INTERLEAVED = 0, 1, 2, 3
 LAYOUT_CANONICAL, LAYOUT_ROWGROUP_INTERLEAVE = 0, 1
 MODE_HYBRID, MODE_OVERWRITE_ONLY = 0, 1
 ENCODER_AUTO, ENCODER_WIDE, ENCODER_DEEP = 0, 1, 2
+CODEC_LZ4, CODEC_SNAPPY = 0, 1
 
 
 class DcrError(RuntimeError):
@@ -48,7 +49,8 @@ class TensorDesc(ctypes.Structure):
 
 
 class PlanOpts(ctypes.Structure):
-    _fields_ = [("window_bytes", ctypes.c_uint64), ("encoder", ctypes.c_uint32), ("reserved", ctypes.c_uint32 * 5)]
+    _fields_ = [("window_bytes", ctypes.c_uint64), ("encoder", ctypes.c_uint32), ("codec", ctypes.c_uint32),
+                ("reserved", ctypes.c_uint32 * 4)]
 
 
 class PlanInfo(ctypes.Structure):
@@ -167,10 +169,10 @@ def check(rc):
 class Plan:
     """dcr_plan_build over a list of TensorDesc."""
 
-    def __init__(self, descs, window_bytes=0, encoder=0):
+    def __init__(self, descs, window_bytes=0, encoder=0, codec=0):
         arr = (TensorDesc * len(descs))(*descs)
         self._names = [d.name for d in descs]
-        opts = PlanOpts(window_bytes, encoder)
+        opts = PlanOpts(window_bytes, encoder, codec)
         h = ctypes.c_void_p()
         check(lib().dcr_plan_build(arr, len(descs), ctypes.byref(opts), ctypes.byref(h)))
         self.h = h

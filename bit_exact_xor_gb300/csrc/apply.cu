@@ -28,7 +28,7 @@
 //                 with the body read from global memory and the matches
 //                 checked against a bitmap of the non-zero output bytes.
 //   defer_kernel  one CTA per general LZ4 frame (any valid block, e.g. from
-//                 the CPU oracle): full decode into a 64 KiB shared buffer
+//                 the CPU oracle) or Snappy frame: full decode into a 64 KiB shared buffer
 //                 with warp-parallel literal and match copies (a ZSRC frame
 //                 whose match copies a non-zero byte is rejected), then the
 //                 XOR sweep.
@@ -616,7 +616,7 @@ __global__ void __launch_bounds__(kAThreads) apply_kernel(ApplyArgs A)
         const uint4 h0 = ld_nc16(A.payload + fo), h1 = ld_nc16(A.payload + fo + 16);
         const uint32_t kind = h0.y & 0xFFu, fbits = (h0.y >> 8) & 0xFFu, fflags = h0.y >> 16;
         const uint32_t c = h0.z, raw = h0.w, bl = h1.x;
-        if (h0.x != kFrameMagic || kind < kXorLz4 || kind > kOverwriteDense || c < H.chunk_begin ||
+        if (h0.x != kFrameMagic || kind < kXorLz4 || kind > kXorSnappy || c < H.chunk_begin ||
             c >= H.chunk_begin + H.chunk_count || bl > H.idx_off - fo - kFrameHdr) {
             if (lane == 0) report(A.sc, DCR_ERR_CORRUPT);
             continue;
@@ -626,7 +626,7 @@ __global__ void __launch_bounds__(kAThreads) apply_kernel(ApplyArgs A)
             if (lane == 0) report(A.sc, DCR_ERR_CORRUPT);
             continue;
         }
-        const bool is_xor = kind == kXorLz4 || kind == kXorRaw;
+        const bool is_xor = kind == kXorLz4 || kind == kXorRaw || kind == kXorSnappy;
         if (A.retry_only && is_xor) {
             if (lane == 0) report(A.sc, DCR_ERR_INVALID);
             continue;
@@ -648,7 +648,7 @@ __global__ void __launch_bounds__(kAThreads) apply_kernel(ApplyArgs A)
             if (!__shfl_sync(0xffffffffu, got, 0)) continue;
             // general LZ4 frames go to the full decode, ZSRC frames larger
             // than the body cache to big_kernel
-            if (kind == kXorLz4 && !(fflags & kFrameZsrc)) {
+            if ((kind == kXorLz4 && !(fflags & kFrameZsrc)) || kind == kXorSnappy) {
                 if (lane == 0) A.defer[atomicAdd(&A.sc->n_defer, 1u)] = f;
                 continue;
             }
@@ -761,13 +761,73 @@ __global__ void __launch_bounds__(kDThreads) defer_kernel(ApplyArgs A)
         const uint4 h0 = ld_nc16(p + fo), h1 = ld_nc16(p + fo + 16);
         const uint32_t c = h0.z, raw = h0.w, n = h1.x;
         const bool zs = ((h0.y >> 16) & kFrameZsrc) != 0;   // matches must copy zeros
+        const bool snappy = (h0.y & 0xFFu) == kXorSnappy;
         const ChunkDesc cd = A.chunks[c];
         const bool cut = uint64_t(f) == A.abort_at;
         const uint32_t ub = cd.bits == 16 ? 2u : 1u;
         uint32_t lim = cut ? (A.split < raw ? A.split : raw) : raw;
         lim -= lim % ub;
         const uint8_t* src = p + fo + kFrameHdr;
-        if (threadIdx.x < 32) {
+        if (threadIdx.x < 32 && snappy) {
+            // Snappy block: varint length, then literal and copy elements
+            bool good = false;
+            uint32_t ip = 0, op = 0;
+            uint64_t v = 0;
+            bool pre = false;
+            for (uint32_t shift = 0; shift <= 28 && ip < n; shift += 7) {
+                const uint64_t b = src[ip++];
+                v |= (b & 127u) << shift;
+                if (!(b & 128u)) {
+                    pre = true;
+                    break;
+                }
+            }
+            bool ok = pre && v == raw;
+            while (ok && ip < n) {
+                const uint32_t tag = src[ip++];
+                uint32_t len, off;
+                if ((tag & 3u) == 0) {
+                    len = (tag >> 2) + 1;
+                    if ((tag >> 2) >= 60) {
+                        const uint32_t nb = (tag >> 2) - 59;
+                        if (nb > n - ip) { ok = false; break; }
+                        len = 0;
+                        for (uint32_t i = 0; i < nb; ++i) len |= uint32_t(src[ip + i]) << (8 * i);
+                        len += 1;   // at most 2^32: wraps to 0 only for a 4-byte length, rejected below
+                        ip += nb;
+                    }
+                    if (len == 0 || len > n - ip || len > raw - op) { ok = false; break; }
+                    for (uint32_t i = lane; i < len; i += 32) out[op + i] = src[ip + i];
+                    __syncwarp();
+                    ip += len;
+                    op += len;
+                    continue;
+                }
+                if ((tag & 3u) == 1) {
+                    if (ip >= n) { ok = false; break; }
+                    len = ((tag >> 2) & 7u) + 4;
+                    off = ((tag >> 5) << 8) | src[ip++];
+                } else {
+                    const uint32_t nb = (tag & 3u) == 2 ? 2u : 4u;
+                    if (nb > n - ip) { ok = false; break; }
+                    len = (tag >> 2) + 1;
+                    off = 0;
+                    for (uint32_t i = 0; i < nb; ++i) off |= uint32_t(src[ip + i]) << (8 * i);
+                    ip += nb;
+                }
+                if (off == 0 || off > op || len > raw - op) { ok = false; break; }
+                bool viol = false;   // forward copy semantics: the output repeats with period off
+                for (uint32_t i = lane; i < len; i += 32) {
+                    const uint8_t b = out[op - off + (i % off)];
+                    out[op + i] = b;
+                    viol |= b != 0;
+                }
+                if (__any_sync(kFull, zs && viol)) { ok = false; break; }
+                op += len;
+            }
+            good = ok && op == raw;
+            if (lane == 0) s_good = good;
+        } else if (threadIdx.x < 32) {
             bool good = false;
             uint32_t ip = 0, op = 0;
             for (;;) {

@@ -20,7 +20,7 @@ constexpr uint32_t kFrameMagic = 0x46524344u;   // "DCRF"
 constexpr uint32_t kFormat = 1;
 constexpr uint32_t kStreamOverwriteOnly = 1;
 constexpr uint32_t kFrameZsrc = 1;  // every LZ4 match copies zero bytes
-enum FrameKind : uint32_t { kXorLz4 = 1, kXorRaw = 2, kOverwrite = 3, kOverwriteDense = 4 };
+enum FrameKind : uint32_t { kXorLz4 = 1, kXorRaw = 2, kOverwrite = 3, kOverwriteDense = 4, kXorSnappy = 5 };
 
 // One contiguous piece of a chunk: canonical bytes [off, off + len) of the
 // chunk map to `addr`.  Sender pieces: addr = shard << 56 | byte offset in
@@ -162,6 +162,7 @@ struct dcr_plan {
     std::vector<uint64_t> win_start;  // n_windows + 1 chunk ids
     uint64_t window_bytes = 0;
     uint32_t encoder = DCR_ENCODER_AUTO;
+    uint32_t codec = DCR_CODEC_LZ4;
     uint64_t n_chunks = 0;
     uint64_t canonical_bytes = 0;
     uint64_t hash = 0;

@@ -252,6 +252,124 @@ __device__ __forceinline__ uint32_t seq_bytes(uint32_t ll, uint32_t ml)
     return 1 + ext_len(ll) + ll + 2 + ext_len(ml - 4);
 }
 
+// Block codecs of the XOR masks.  Both encode the parse's sequences (a
+// literal run, then a copy of zero bytes); only the byte layout differs.
+//
+// LZ4 block: per sequence a token (literal length << 4 | match length - 4,
+// 15 = more length bytes of 255 follow), literals, a 2-byte offset, match
+// length bytes; the last sequence is literals only.
+struct CodecLz4 {
+    static constexpr uint32_t kKind = kXorLz4;
+    static constexpr bool kNearCopy = false;   // see CodecSnappy
+    __device__ static uint32_t preamble(uint32_t) { return 0u; }
+    __device__ static uint32_t seq(uint32_t ll, uint32_t ml, uint32_t) { return seq_bytes(ll, ml); }
+    __device__ static uint32_t tail(uint32_t ll) { return 1 + ext_len(ll) + ll; }
+    template <class Put>
+    __device__ static void put_len(Put& put, uint32_t v)
+    {
+        v -= 15;
+        for (; v >= 255; v -= 255) put(255);
+        put(v);
+    }
+    // the sequence's bytes; lits(put) writes its literal bytes
+    template <class Put, class Lits>
+    __device__ static void emit_seq(Put& put, uint32_t ll, Lits&& lits, uint32_t off, uint32_t ml)
+    {
+        const uint32_t mc = ml - 4;
+        put(((ll >= 15 ? 15u : ll) << 4) | (mc >= 15 ? 15u : mc));
+        if (ll >= 15) put_len(put, ll);
+        lits(put);
+        put(off & 0xFFu);
+        put(off >> 8);
+        if (mc >= 15) put_len(put, mc);
+    }
+    template <class Put, class Lits>
+    __device__ static void emit_tail(Put& put, uint32_t ll, Lits&& lits)
+    {
+        put((ll >= 15 ? 15u : ll) << 4);
+        if (ll >= 15) put_len(put, ll);
+        lits(put);
+    }
+    template <class Put>
+    __device__ static void emit_preamble(Put&, uint32_t) {}
+};
+
+// Snappy block ("A strong baseline with the Blackwell-native DE", footnote
+// 4): the chunk length as a base-128 varint, then literal elements (tag
+// (length - 1) << 2 below 60, else 60..63 and 1..4 length bytes) and copy
+// elements of at most 64 bytes (tag 1: length 4..11 and an 11-bit offset in
+// 2 bytes; tag 2: length 1..64 and a 2-byte offset).  A match becomes copies
+// of 64 while at least 68 bytes remain, one of 60 if more than 64 remain,
+// then the rest (4 or more).
+struct CodecSnappy {
+    static constexpr uint32_t kKind = kXorSnappy;
+    // a copy of 4..11 bytes at an offset below 2048 takes 2 bytes instead of
+    // 3, so a run may also copy from the zero gap just before the previous
+    // event (all bytes between two events are zero), usually close by
+    static constexpr bool kNearCopy = true;
+    __device__ static uint32_t preamble(uint32_t raw) { return raw < 128 ? 1u : raw < 16384 ? 2u : 3u; }
+    __device__ static uint32_t lit_bytes(uint32_t ll)
+    {
+        return ll == 0 ? 0u : 1u + (ll <= 60 ? 0u : ll <= 256 ? 1u : ll <= 65536 ? 2u : 3u) + ll;
+    }
+    __device__ static uint32_t copy_bytes(uint32_t ml, uint32_t off)
+    {
+        const uint32_t k = ml >= 68 ? (ml - 68) / 64 + 1 : 0u;
+        uint32_t r = ml - 64 * k, c = 3 * k;
+        if (r > 64) {
+            c += 3;
+            r -= 60;
+        }
+        return c + (r <= 11 && off < 2048 ? 2u : 3u);
+    }
+    __device__ static uint32_t seq(uint32_t ll, uint32_t ml, uint32_t off) { return lit_bytes(ll) + copy_bytes(ml, off); }
+    __device__ static uint32_t tail(uint32_t ll) { return lit_bytes(ll); }
+    template <class Put, class Lits>
+    __device__ static void emit_lits(Put& put, uint32_t ll, Lits&& lits)
+    {
+        if (ll) {
+            const uint32_t v = ll - 1, nb = v < 60 ? 0u : v < 256 ? 1u : v < 65536 ? 2u : 3u;
+            put((nb ? 59 + nb : v) << 2);
+            for (uint32_t i = 0; i < nb; ++i) put((v >> (8 * i)) & 0xFFu);
+        }
+        lits(put);
+    }
+    template <class Put>
+    __device__ static void emit_copy(Put& put, uint32_t len, uint32_t off)
+    {
+        if (len <= 11 && off < 2048) {
+            put(1u | ((len - 4) << 2) | ((off >> 8) << 5));
+            put(off & 0xFFu);
+        } else {
+            put(2u | ((len - 1) << 2));
+            put(off & 0xFFu);
+            put(off >> 8);
+        }
+    }
+    template <class Put, class Lits>
+    __device__ static void emit_seq(Put& put, uint32_t ll, Lits&& lits, uint32_t off, uint32_t ml)
+    {
+        emit_lits(put, ll, lits);
+        for (; ml >= 68; ml -= 64) emit_copy(put, 64, off);
+        if (ml > 64) {
+            emit_copy(put, 60, off);
+            ml -= 60;
+        }
+        emit_copy(put, ml, off);
+    }
+    template <class Put, class Lits>
+    __device__ static void emit_tail(Put& put, uint32_t ll, Lits&& lits)
+    {
+        emit_lits(put, ll, lits);
+    }
+    template <class Put>
+    __device__ static void emit_preamble(Put& put, uint32_t raw)
+    {
+        for (; raw >= 128; raw >>= 7) put((raw & 127u) | 128u);
+        put(raw);
+    }
+};
+
 __device__ __forceinline__ uint32_t warp_incl_sum(uint32_t v, int lane)
 {
 #pragma unroll
@@ -319,7 +437,7 @@ struct MaskSrc {
 // found with one ballot.  Sizes add up in P.out.  With emit, the sequences
 // are written to out[0, cap); *over is set when one does not fit and *bad
 // when sizing and writing disagree.
-template <class Src>
+template <class Codec, class Src>
 __device__ __forceinline__ void parse_group(const Src& S, int e0, int cnt, bool final, int raw, Parse& P,
                                             uint8_t* out, uint32_t cap, bool emit, int lane, bool* over,
                                             bool* bad)
@@ -344,7 +462,15 @@ __device__ __forceinline__ void parse_group(const Src& S, int e0, int cnt, bool 
     const uint32_t bl = uint32_t(P.best >> 32);
     const int bs = int(uint32_t(P.best));
     int ms = -1, off = 0;
-    if (active && L > 0) {
+    int pgs = 0, pL = 0;   // the previous lane's zero gap (Snappy)
+    if constexpr (Codec::kNearCopy) {
+        pgs = __shfl_up_sync(kFull, gs, 1);
+        pL = __shfl_up_sync(kFull, L, 1);
+    }
+    if (Codec::kNearCopy && active && lane > 0 && L > 0 && me - gs >= 4 && gs <= raw - 12 && pL >= me - gs) {
+        ms = gs;
+        off = gs - pgs;
+    } else if (active && L > 0) {
         if (me - gs >= 4 && gs <= raw - 12 && bl >= uint32_t(me - gs)) {
             ms = gs;
             off = gs - bs;
@@ -363,9 +489,9 @@ __device__ __forceinline__ void parse_group(const Src& S, int e0, int cnt, bool 
         lit = P.lit;
         lev = P.lit_ev;
     }
-    uint32_t sz = has ? seq_bytes(uint32_t(ms - lit), uint32_t(me - ms)) : 0u;
+    uint32_t sz = has ? Codec::seq(uint32_t(ms - lit), uint32_t(me - ms), uint32_t(off)) : 0u;
     const int flit = has ? me : lit;    // literals after this event's match
-    if (last) sz += 1 + ext_len(uint32_t(raw - flit)) + uint32_t(raw - flit);
+    if (last) sz += Codec::tail(uint32_t(raw - flit));
     uint32_t gsum;
     if (emit) {
         const uint32_t incl = warp_incl_sum(sz, lane);
@@ -376,27 +502,13 @@ __device__ __forceinline__ void parse_group(const Src& S, int e0, int cnt, bool 
         if ((has || last) && fits) {
             uint32_t o = o0;
             auto put = [&](uint32_t v) { out[o++] = uint8_t(v); };
-            auto put_len = [&](uint32_t v) {
-                v -= 15;
-                for (; v >= 255; v -= 255) put(255);
-                put(v);
-            };
             bool ok = true;
-            if (has) {
-                const uint32_t ll = uint32_t(ms - lit), mc = uint32_t(me - ms - 4);
-                put(((ll >= 15 ? 15u : ll) << 4) | (mc >= 15 ? 15u : mc));
-                if (ll >= 15) put_len(ll);
-                ok &= S.lits(lit, ms, lev, e, put);
-                put(uint32_t(off) & 0xFFu);
-                put(uint32_t(off) >> 8);
-                if (mc >= 15) put_len(mc);
-            }
-            if (last) {
-                const uint32_t ll = uint32_t(raw - flit);
-                put((ll >= 15 ? 15u : ll) << 4);
-                if (ll >= 15) put_len(ll);
-                ok &= S.lits(flit, raw, has ? e : lev, e, put);
-            }
+            if (has)
+                Codec::emit_seq(put, uint32_t(ms - lit), [&](decltype(put)& p) { ok &= S.lits(lit, ms, lev, e, p); },
+                                uint32_t(off), uint32_t(me - ms));
+            if (last)
+                Codec::emit_tail(put, uint32_t(raw - flit),
+                                 [&](decltype(put)& p) { ok &= S.lits(flit, raw, has ? e : lev, e, p); });
             if (!ok || o != o0 + sz) *bad = true;
         }
     } else {
@@ -420,7 +532,7 @@ __device__ __forceinline__ void parse_group(const Src& S, int e0, int cnt, bool 
 __device__ __forceinline__ void write_header(uint8_t* f, uint32_t kind, uint32_t bits, uint32_t chunk,
                                              uint32_t raw, uint32_t body_len, uint32_t chg)
 {
-    const uint32_t h1 = kind | (bits << 8) | ((kind == kXorLz4 ? kFrameZsrc : 0u) << 16);
+    const uint32_t h1 = kind | (bits << 8) | ((kind == kXorLz4 || kind == kXorSnappy ? kFrameZsrc : 0u) << 16);
     reinterpret_cast<uint4*>(f)[0] = make_uint4(kFrameMagic, h1, chunk, raw);
     reinterpret_cast<uint4*>(f)[1] = make_uint4(body_len, chg, 0u, 0u);
 }
@@ -455,7 +567,7 @@ __device__ __forceinline__ void gather_bytes(const EncArgs& A, const Seg* segs, 
 
 // The stream loop of any chunk (overwrite records, 4-bit elements, pieces
 // that are not 16-byte aligned); stream_fast below is the common case.
-template <int NS>
+template <int NS, class Codec>
 __device__ __forceinline__ void stream_chunk(const EncArgs& A, WarpSmemT<NS>& W, const ChunkDesc& cd, const Seg* segs,
                                              int lane, uint8_t* body, uint32_t cap, uint8_t* vals, int ncap,
                                              uint32_t& changed, Parse& P, int& tail, int& np, int& units,
@@ -596,7 +708,7 @@ __device__ __forceinline__ void stream_chunk(const EncArgs& A, WarpSmemT<NS>& W,
                 const bool fin = !more && tail - np < 32;
                 if (fin && tail == 0) break;   // no change: no frame
                 bool over = false;
-                parse_group(R, np, cnt, fin, raw, P, body, cap, !spill, lane, &over, &bad);
+                parse_group<Codec>(R, np, cnt, fin, raw, P, body, cap, !spill, lane, &over, &bad);
                 np += cnt;
                 if (__any_sync(kFull, over)) spill = true;
                 if (fin) break;
@@ -612,7 +724,7 @@ __device__ __forceinline__ void stream_chunk(const EncArgs& A, WarpSmemT<NS>& W,
 // modulo NS, this lane's copy and read addresses are worked out once, the
 // warp looks up the piece of a step once, and the last groups are parsed
 // after the loop.
-template <int kBits, int NS>
+template <int kBits, int NS, class Codec>
 __device__ __forceinline__ void stream_fast(const EncArgs& A, WarpSmemT<NS>& W, const ChunkDesc& cd, const Seg* segs,
                                             int lane, uint8_t* body, uint32_t cap, uint32_t& changed, Parse& P,
                                             int& tail, int& np, bool& spill, bool& bad)
@@ -719,7 +831,7 @@ __device__ __forceinline__ void stream_fast(const EncArgs& A, WarpSmemT<NS>& W, 
             __syncwarp();
             while (tail - np >= 32) {
                 bool over = false;
-                parse_group(R, np, 32, false, raw, P, body, cap, !spill, lane, &over, &bad);
+                parse_group<Codec>(R, np, 32, false, raw, P, body, cap, !spill, lane, &over, &bad);
                 np += 32;
                 if (__any_sync(kFull, over)) spill = true;
             }
@@ -730,14 +842,14 @@ __device__ __forceinline__ void stream_fast(const EncArgs& A, WarpSmemT<NS>& W, 
         const int cnt = tail - np < 32 ? tail - np : 32;
         const bool fin = tail - np < 32;
         bool over = false;
-        parse_group(R, np, cnt, fin, raw, P, body, cap, !spill, lane, &over, &bad);
+        parse_group<Codec>(R, np, cnt, fin, raw, P, body, cap, !spill, lane, &over, &bad);
         np += cnt;
         if (__any_sync(kFull, over)) spill = true;
         if (fin) break;
     }
 }
 
-template <int NS>
+template <int NS, class Codec>
 __device__ __forceinline__ void encode_chunk(const EncArgs& A, WarpSmemT<NS>& W, uint32_t k, int lane)
 {
     const ChunkDesc cd = A.chunks[A.chunk_begin + k];
@@ -759,15 +871,21 @@ __device__ __forceinline__ void encode_chunk(const EncArgs& A, WarpSmemT<NS>& W,
     uint8_t* vstage = reinterpret_cast<uint8_t*>(W.pos);   // overwrite values
 
     uint32_t changed = 0;
-    Parse P{-1, 0ull, 0, 0, 0u};
+    Parse P{-1, 0ull, 0, 0, Codec::preamble(uint32_t(raw))};
     int tail = 0, np = 0, units = 0;
     bool spill = false, bad = false;
+    if (!overwrite && lane == 0) {   // the block's preamble (Snappy: the chunk length)
+        uint32_t o = 0;
+        auto put = [&](uint32_t v) { body[o++] = uint8_t(v); };
+        Codec::emit_preamble(put, uint32_t(raw));
+    }
     if (!overwrite && vec && cd.bits == 16)
-        stream_fast<16, NS>(A, W, cd, segs, lane, body, kSlotBody, changed, P, tail, np, spill, bad);
+        stream_fast<16, NS, Codec>(A, W, cd, segs, lane, body, kSlotBody, changed, P, tail, np, spill, bad);
     else if (!overwrite && vec && cd.bits == 8)
-        stream_fast<8, NS>(A, W, cd, segs, lane, body, kSlotBody, changed, P, tail, np, spill, bad);
+        stream_fast<8, NS, Codec>(A, W, cd, segs, lane, body, kSlotBody, changed, P, tail, np, spill, bad);
     else
-        stream_chunk(A, W, cd, segs, lane, body, kSlotBody, vstage, ncap, changed, P, tail, np, units, spill, bad);
+        stream_chunk<NS, Codec>(A, W, cd, segs, lane, body, kSlotBody, vstage, ncap, changed, P, tail, np, units,
+                                spill, bad);
     changed = __reduce_add_sync(kFull, changed);
     if (lane == 0 && changed) {
         atomicAdd(&A.counts[cd.tensor], (unsigned long long)changed);
@@ -778,7 +896,7 @@ __device__ __forceinline__ void encode_chunk(const EncArgs& A, WarpSmemT<NS>& W,
     bool staged = false;
     if (changed && !overwrite) {
         if (P.out < uint32_t(raw)) {
-            kind = kXorLz4;
+            kind = Codec::kKind;
             body_len = P.out;
             staged = !spill;
         } else {
@@ -822,7 +940,7 @@ __device__ __forceinline__ void encode_chunk(const EncArgs& A, WarpSmemT<NS>& W,
     __syncwarp();   // the ring is reused by the next chunk
 }
 
-template <int NS>
+template <int NS, class Codec>
 __global__ void __launch_bounds__(kMThreads, 4) encode_kernel(EncArgs A)
 {
     extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -836,7 +954,7 @@ __global__ void __launch_bounds__(kMThreads, 4) encode_kernel(EncArgs A)
         }
         k = __shfl_sync(kFull, k, 0);
         if (k >= A.chunk_count) break;
-        encode_chunk(A, W, k, lane);
+        encode_chunk<NS, Codec>(A, W, k, lane);
     }
 }
 
@@ -847,6 +965,7 @@ __global__ void __launch_bounds__(kMThreads, 4) encode_kernel(EncArgs A)
 // first time).  Overwrite values go to their place directly, the unit count
 // being known.  Raw and dense frames, and LZ4 chunks whose pending literals
 // outgrow the event ring, are listed for spill_kernel.
+template <class Codec>
 __device__ __forceinline__ void restream_chunk(const EncArgs& A, WarpSmem& W, uint32_t s, int lane)
 {
     const SpillRec R = A.spill[s];
@@ -869,18 +988,24 @@ __device__ __forceinline__ void restream_chunk(const EncArgs& A, WarpSmem& W, ui
     const uint32_t voff = 4 + 2 * nu + (4 - (2 * nu) % 4) % 4;
 
     uint32_t changed = 0;
-    Parse P{-1, 0ull, 0, 0, 0u};
+    Parse P{-1, 0ull, 0, 0, R.kind == kOverwrite ? 0u : Codec::preamble(cd.raw_len)};
     int tail = 0, np = 0, units = 0;
     bool spill = false, bad = false;
+    if (R.kind != kOverwrite && lane == 0) {   // the block's preamble
+        uint32_t o = 0;
+        auto put = [&](uint32_t v) { body[o++] = uint8_t(v); };
+        Codec::emit_preamble(put, cd.raw_len);
+    }
     if (R.kind == kOverwrite)
-        stream_chunk(A, W, cd, segs, lane, body, R.body_len, body + voff, int(nu), changed, P, tail, np, units,
-                     spill, bad);
+        stream_chunk<kNS, Codec>(A, W, cd, segs, lane, body, R.body_len, body + voff, int(nu), changed, P, tail, np,
+                                 units, spill, bad);
     else if (vec && cd.bits == 16)
-        stream_fast<16, kNS>(A, W, cd, segs, lane, body, R.body_len, changed, P, tail, np, spill, bad);
+        stream_fast<16, kNS, Codec>(A, W, cd, segs, lane, body, R.body_len, changed, P, tail, np, spill, bad);
     else if (vec && cd.bits == 8)
-        stream_fast<8, kNS>(A, W, cd, segs, lane, body, R.body_len, changed, P, tail, np, spill, bad);
+        stream_fast<8, kNS, Codec>(A, W, cd, segs, lane, body, R.body_len, changed, P, tail, np, spill, bad);
     else
-        stream_chunk(A, W, cd, segs, lane, body, R.body_len, nullptr, 0, changed, P, tail, np, units, spill, bad);
+        stream_chunk<kNS, Codec>(A, W, cd, segs, lane, body, R.body_len, nullptr, 0, changed, P, tail, np, units,
+                                 spill, bad);
     changed = __reduce_add_sync(kFull, changed);
     if (R.kind == kOverwrite) {
         bad |= uint32_t(units) != nu;
@@ -894,7 +1019,7 @@ __device__ __forceinline__ void restream_chunk(const EncArgs& A, WarpSmem& W, ui
         if (lane == 0) report(A.sc, DCR_ERR_CORRUPT);
         return;
     }
-    if (R.kind == kXorLz4 && spill) {   // the ring could not hold the pending literals
+    if (R.kind == Codec::kKind && spill) {   // the ring could not hold the pending literals
         if (lane == 0) A.deep[atomicAdd(&A.sc->n_deep, 1u)] = s;
         return;
     }
@@ -904,6 +1029,7 @@ __device__ __forceinline__ void restream_chunk(const EncArgs& A, WarpSmem& W, ui
     __syncwarp();   // the ring is reused by the next chunk
 }
 
+template <class Codec>
 __global__ void __launch_bounds__(kMThreads, 4) restream_kernel(EncArgs A)
 {
     extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -919,7 +1045,7 @@ __global__ void __launch_bounds__(kMThreads, 4) restream_kernel(EncArgs A)
         }
         s = __shfl_sync(kFull, s, 0);
         if (s >= n_spill) break;
-        restream_chunk(A, W, s, lane);
+        restream_chunk<Codec>(A, W, s, lane);
     }
 }
 
@@ -1136,10 +1262,16 @@ __device__ __forceinline__ int list_events(Buf& B, int t, int n, int lane, int* 
 // LZ4 block of the chunk in B written to body[0, body_len); returns its size.
 // Events are listed in batches; a batch's partial last group moves to the
 // front of the next one, so the groups are those of encode_kernel.
-__device__ uint32_t lz4_block(Buf& B, int raw, uint8_t* body, uint32_t body_len, int lane, bool* bad)
+template <class Codec>
+__device__ uint32_t mask_block(Buf& B, int raw, uint8_t* body, uint32_t body_len, int lane, bool* bad)
 {
     const MaskSrc S{B.ev, reinterpret_cast<const uint8_t*>(B.data)};
-    Parse P{-1, 0ull, 0, 0, 0u};
+    Parse P{-1, 0ull, 0, 0, Codec::preamble(uint32_t(raw))};
+    if (lane == 0) {   // the block's preamble
+        uint32_t o = 0;
+        auto put = [&](uint32_t v) { body[o++] = uint8_t(v); };
+        Codec::emit_preamble(put, uint32_t(raw));
+    }
     bool over = false;
     int t = 0, keep = 0;
     for (;;) {
@@ -1147,9 +1279,10 @@ __device__ uint32_t lz4_block(Buf& B, int raw, uint8_t* body, uint32_t body_len,
         t = list_events(B, t, keep, lane, &n);
         const bool fin = t >= kSteps;
         int g = 0;
-        for (; g + 32 <= n; g += 32) parse_group(S, g, 32, false, raw, P, body, body_len, true, lane, &over, bad);
+        for (; g + 32 <= n; g += 32)
+            parse_group<Codec>(S, g, 32, false, raw, P, body, body_len, true, lane, &over, bad);
         if (fin) {
-            parse_group(S, g, n - g, true, raw, P, body, body_len, true, lane, &over, bad);
+            parse_group<Codec>(S, g, n - g, true, raw, P, body, body_len, true, lane, &over, bad);
             break;
         }
         const int rem = n - g;   // < 32, and g >= 32 since a batch stops only near kEvCap
@@ -1163,6 +1296,7 @@ __device__ uint32_t lz4_block(Buf& B, int raw, uint8_t* body, uint32_t body_len,
     return P.out;
 }
 
+template <class Codec>
 __global__ void __launch_bounds__(kSThreads, 2) spill_kernel(EncArgs A)
 {
     extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -1193,9 +1327,9 @@ __global__ void __launch_bounds__(kSThreads, 2) spill_kernel(EncArgs A)
             const int nfull = raw >> 4;
             for (int v = threadIdx.x; v < nfull; v += kSThreads) reinterpret_cast<uint4*>(body)[v] = B.data[v];
             for (int x = (nfull << 4) + threadIdx.x; x < raw; x += kSThreads) body[x] = bytes[x];
-        } else if (warp == 0 && R.kind == kXorLz4) {
+        } else if (warp == 0 && R.kind == Codec::kKind) {
             bool bad = false;
-            const uint32_t got = lz4_block(B, raw, body, R.body_len, lane, &bad);
+            const uint32_t got = mask_block<Codec>(B, raw, body, R.body_len, lane, &bad);
             if ((__any_sync(kFull, bad) || got != R.body_len) && lane == 0) report(A.sc, DCR_ERR_CORRUPT);
         }
         for (uint32_t x = kFrameHdr + R.body_len + threadIdx.x; x < fsz; x += kSThreads) f[x] = 0;
@@ -1208,32 +1342,48 @@ constexpr size_t kDeepSmem = sizeof(WarpSmemDeep) * kDeepWarps;
 
 }  // namespace
 
+namespace {
+
+// shared-memory limits of one codec's kernels
+template <class Codec>
+cudaError_t codec_attributes()
+{
+    cudaError_t e = cudaFuncSetAttribute(encode_kernel<kNS, Codec>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         int(kMainSmem));
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(encode_kernel<kNSDeep, Codec>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 int(kDeepSmem));
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(restream_kernel<Codec>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 int(kMainSmem));
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(spill_kernel<Codec>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sizeof(Buf)));
+    return e;
+}
+
+}  // namespace
+
 int encode_kernel_config(KernelConfig* kc)
 {
     int dev;
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&kc->num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess) e = codec_attributes<CodecLz4>();
+    if (e == cudaSuccess) e = codec_attributes<CodecSnappy>();
+    // residency of the LZ4 instantiations (the Snappy ones are launched with
+    // the same grids: persistent CTAs that take tickets)
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(encode_kernel<kNS>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kMainSmem));
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&kc->enc_blocks_per_sm, encode_kernel<kNS, CodecLz4>,
+                                                          kMThreads, kMainSmem);
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(encode_kernel<kNSDeep>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 int(kDeepSmem));
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&kc->enc_deep_blocks_per_sm,
+                                                          encode_kernel<kNSDeep, CodecLz4>, 32 * kDeepWarps, kDeepSmem);
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(restream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kMainSmem));
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&kc->restream_blocks_per_sm, restream_kernel<CodecLz4>,
+                                                          kMThreads, kMainSmem);
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(spill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sizeof(Buf)));
-    if (e == cudaSuccess)
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&kc->enc_blocks_per_sm, encode_kernel<kNS>, kMThreads,
-                                                          kMainSmem);
-    if (e == cudaSuccess)
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&kc->enc_deep_blocks_per_sm, encode_kernel<kNSDeep>,
-                                                          32 * kDeepWarps, kDeepSmem);
-    if (e == cudaSuccess)
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&kc->restream_blocks_per_sm, restream_kernel, kMThreads,
-                                                          kMainSmem);
-    if (e == cudaSuccess)
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&kc->spill_blocks_per_sm, spill_kernel, kSThreads,
-                                                          sizeof(Buf));
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&kc->spill_blocks_per_sm, spill_kernel<CodecLz4>,
+                                                          kSThreads, sizeof(Buf));
     if (e != cudaSuccess) return cuda_error(e, "encode kernel configuration");
     if (kc->enc_blocks_per_sm < 1 || kc->enc_deep_blocks_per_sm < 1 || kc->restream_blocks_per_sm < 1 ||
         kc->spill_blocks_per_sm < 1)
@@ -1277,11 +1427,16 @@ int encode_launch(const dcr_plan* P, uint32_t mode, uint32_t window, const void*
     unsigned dgrid = (A.chunk_count + kDeepWarps - 1) / kDeepWarps;
     if (dgrid > deep_warps / kDeepWarps) dgrid = deep_warps / kDeepWarps;
     if (dgrid == 0) dgrid = 1;
+    const bool snappy = P->codec == DCR_CODEC_SNAPPY;
     if (P->profiling) cudaEventRecord(P->ev[0], s);
-    if (deep)
-        encode_kernel<kNSDeep><<<dgrid, 32 * kDeepWarps, kDeepSmem, s>>>(A);
+    if (deep && snappy)
+        encode_kernel<kNSDeep, CodecSnappy><<<dgrid, 32 * kDeepWarps, kDeepSmem, s>>>(A);
+    else if (deep)
+        encode_kernel<kNSDeep, CodecLz4><<<dgrid, 32 * kDeepWarps, kDeepSmem, s>>>(A);
+    else if (snappy)
+        encode_kernel<kNS, CodecSnappy><<<grid, kMThreads, kMainSmem, s>>>(A);
     else
-        encode_kernel<kNS><<<grid, kMThreads, kMainSmem, s>>>(A);
+        encode_kernel<kNS, CodecLz4><<<grid, kMThreads, kMainSmem, s>>>(A);
     if (P->profiling) cudaEventRecord(P->ev[1], s);
     scan_kernel<<<1, 1024, 0, s>>>(A, P->hash, base_v, target_v, window);
     unsigned cgrid = (A.chunk_count + 7) / 8;
@@ -1289,8 +1444,14 @@ int encode_launch(const dcr_plan* P, uint32_t mode, uint32_t window, const void*
     copy_kernel<<<cgrid, 256, 0, s>>>(A);
     unsigned rgrid = unsigned(P->kc.num_sms * P->kc.restream_blocks_per_sm);
     if (rgrid > grid) rgrid = grid;
-    restream_kernel<<<rgrid, kMThreads, kMainSmem, s>>>(A);
-    spill_kernel<<<unsigned(P->kc.num_sms * P->kc.spill_blocks_per_sm), kSThreads, sizeof(Buf), s>>>(A);
+    const unsigned sgrid = unsigned(P->kc.num_sms * P->kc.spill_blocks_per_sm);
+    if (snappy) {
+        restream_kernel<CodecSnappy><<<rgrid, kMThreads, kMainSmem, s>>>(A);
+        spill_kernel<CodecSnappy><<<sgrid, kSThreads, sizeof(Buf), s>>>(A);
+    } else {
+        restream_kernel<CodecLz4><<<rgrid, kMThreads, kMainSmem, s>>>(A);
+        spill_kernel<CodecLz4><<<sgrid, kSThreads, sizeof(Buf), s>>>(A);
+    }
     if (P->profiling) cudaEventRecord(P->ev[2], s);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_error(e, "encode launch");

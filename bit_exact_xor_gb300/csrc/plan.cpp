@@ -219,10 +219,13 @@ extern "C" int dcr_plan_build(const dcr_tensor_desc* tensors, size_t n, const dc
         return set_error(DCR_ERR_INVALID, "window_bytes must be in [64 KiB, 256 GiB]");
     const uint32_t encoder = opts ? opts->encoder : uint32_t(DCR_ENCODER_AUTO);
     if (encoder > DCR_ENCODER_DEEP) return set_error(DCR_ERR_INVALID, "unknown encoder variant %u", encoder);
+    const uint32_t codec = opts ? opts->codec : uint32_t(DCR_CODEC_LZ4);
+    if (codec > DCR_CODEC_SNAPPY) return set_error(DCR_ERR_INVALID, "unknown codec %u", codec);
     dcr_plan* P = new (std::nothrow) dcr_plan();
     if (!P) return set_error(DCR_ERR_NOMEM, "dcr_plan_build: out of host memory");
     P->window_bytes = W;
     P->encoder = encoder;
+    P->codec = codec;
     P->tp = tensors[0].tp;
     for (size_t i = 0; i < n; ++i) {
         const char* why;

@@ -99,6 +99,12 @@ enum { DCR_MODE_HYBRID = 0, DCR_MODE_OVERWRITE_ONLY = 1 };
  * warps with twelve landing stages, faster when a window has fewer chunks
  * than the GPU has warp slots; AUTO picks by window size. */
 enum { DCR_ENCODER_AUTO = 0, DCR_ENCODER_WIDE = 1, DCR_ENCODER_DEEP = 2 };
+/* Block codec of XOR masks (dcr_plan_opts.codec).  LZ4 (frame kind 1) is the
+ * default; Snappy (frame kind 5) is the other byte-oriented LZ77 codec the
+ * method's pages compare it with (blog, "A strong baseline with the
+ * Blackwell-native DE"): its copies cover at most 64 bytes, so long zero
+ * runs cost more.  Every receiver decodes both. */
+enum { DCR_CODEC_LZ4 = 0, DCR_CODEC_SNAPPY = 1 };
 
 typedef struct dcr_plan dcr_plan;             /* opaque, library owned */
 typedef struct dcr_recv_state dcr_recv_state; /* opaque, library owned */
@@ -129,7 +135,8 @@ typedef struct {
                                 order; a tensor larger than a window is cut at
                                 chunk boundaries.  At most 256 GiB. */
     uint32_t encoder;        /* DCR_ENCODER_AUTO (0), _WIDE or _DEEP */
-    uint32_t reserved[5];
+    uint32_t codec;          /* DCR_CODEC_LZ4 (0) or DCR_CODEC_SNAPPY */
+    uint32_t reserved[4];
 } dcr_plan_opts;
 
 typedef struct {
