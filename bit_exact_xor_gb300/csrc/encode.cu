@@ -52,7 +52,10 @@
 // from the first one, so their sizes agree by construction (a disagreement
 // is reported).
 //
-// LZ4 parse.  The masks are long zero runs around sparse non-zero bytes, so
+// Parse (LZ4 blocks, or Snappy blocks with the plan's Snappy codec: the
+// CodecLz4 / CodecSnappy policies below give each sequence's bytes; the
+// kernels are instantiated per codec).  The masks are long zero runs around
+// sparse non-zero bytes, so
 // every zero run of at least 4 bytes becomes one match and everything else
 // stays literal.  A run is copied from the longest zero run of the earlier
 // groups when that one is long enough (non-overlapping copy), else it keeps

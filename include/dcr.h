@@ -207,7 +207,8 @@ int dcr_recv_state_version(const dcr_recv_state* state, uint64_t* out);
  * encoding and compression"; paper abstract).  old_shards[r] / new_shards[r]
  * are the trainer arenas of shard r (device, read only).  For each chunk:
  * gather old and new through the plan, mask = old XOR new, count changed
- * elements, then emit an XOR_LZ4 frame (XOR_RAW if LZ4 is not smaller) for
+ * elements, then emit an XOR_LZ4 frame (XOR_SNAPPY with the plan's Snappy
+ * codec; XOR_RAW if the block is not smaller) for
  * affine tensors, or OVERWRITE records (OVERWRITE_DENSE if not smaller) for
  * residual tensors and in DCR_MODE_OVERWRITE_ONLY.  The stream is written to
  * `payload` (device, payload_cap bytes); *payload_size gets its size.
