@@ -468,7 +468,7 @@ def run_gpu(args):
                      "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                      "peak_source": peak_kind,
                      "algorithmic_bytes_per_launch": int(alg_bytes)},
-        "gpu_launches": 9 * nw * args.steps,
+        "gpu_launches": 10 * nw * args.steps,
         "clocks": clocks,
     }
     if e2e:

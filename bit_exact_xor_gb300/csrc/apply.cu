@@ -27,6 +27,9 @@
 //                 body cache or non-zero list (denser masks): the same walk
 //                 with the body read from global memory and the matches
 //                 checked against a bitmap of the non-zero output bytes.
+//   snappy_kernel one warp per ZSRC Snappy frame: serial element walk,
+//                 literal bytes XORed into the receiver, copies checked
+//                 against a bitmap of the non-zero output bytes.
 //   defer_kernel  one CTA per general LZ4 frame (any valid block, e.g. from
 //                 the CPU oracle) or Snappy frame: full decode into a 64 KiB shared buffer
 //                 with warp-parallel literal and match copies (a ZSRC frame
@@ -648,6 +651,10 @@ __global__ void __launch_bounds__(kAThreads) apply_kernel(ApplyArgs A)
             if (!__shfl_sync(0xffffffffu, got, 0)) continue;
             // general LZ4 frames go to the full decode, ZSRC frames larger
             // than the body cache to big_kernel
+            if (kind == kXorSnappy && (fflags & kFrameZsrc)) {   // snappy_kernel
+                if (lane == 0) A.defer[A.defer_len - 1 - atomicAdd(&A.sc->n_big, 1u)] = f;
+                continue;
+            }
             if ((kind == kXorLz4 && !(fflags & kFrameZsrc)) || kind == kXorSnappy) {
                 if (lane == 0) A.defer[atomicAdd(&A.sc->n_defer, 1u)] = f;
                 continue;
@@ -924,6 +931,7 @@ __global__ void __launch_bounds__(kBThreads, 3) big_kernel(ApplyArgs A)
         const uint32_t f = A.defer[A.defer_len - 1 - j];
         const uint64_t fo = ld64(p + idx_off + 8ull * f);
         const uint4 h0 = ld_nc16(p + fo), h1 = ld_nc16(p + fo + 16);
+        if ((h0.y & 0xFFu) == kXorSnappy) continue;   // snappy_kernel's
         const uint32_t c = h0.z, raw = h0.w, bl = h1.x;
         const ChunkDesc cd = A.chunks[c];
         const bool cut = uint64_t(f) == A.abort_at;
@@ -931,6 +939,161 @@ __global__ void __launch_bounds__(kBThreads, 3) big_kernel(ApplyArgs A)
         uint32_t lim = cut ? (A.split < raw ? A.split : raw) : raw;
         lim -= lim % ub;
         const int r = zsrc_apply<true>(A, cd, A.dst + cd.dst_begin, p + fo + kFrameHdr, bl, raw, lim, W, lane);
+        __syncwarp();   // the bitmap is reused by the next frame
+        if (lane == 0) {
+            if (r != 1) {
+                report(A.sc, DCR_ERR_CORRUPT);
+            } else {
+                atomicAdd(&A.sc->applied, 1ull);
+                __threadfence();
+                if (cut) A.sc->aborted = 1;
+                else atomicExch(&A.state[c], (V << 2) | kDone);
+            }
+        }
+    }
+}
+
+// ZSRC Snappy frames (every copy copies zero bytes): one warp per frame walks
+// the elements in order (all lanes read each tag), XORs the non-zero literal
+// bytes into the receiver and marks them in a bitmap of the chunk's output,
+// and checks that each copy's source holds no marked byte.  Returns 1 if
+// applied; 0 if malformed or lying, after undoing the literals it applied
+// (XOR is self-inverse).
+__device__ int snappy_zsrc_apply(const ApplyArgs& A, const ChunkDesc& cd, const Seg* ds, const uint8_t* src,
+                                 uint32_t n, uint32_t raw, uint32_t lim, uint32_t* bits, int lane)
+{
+    const bool one = cd.dst_count == 1;
+    const uint64_t base = one ? ds[0].addr - ds[0].off : 0ull;
+    for (uint32_t w = lane; w < (raw + 31) / 32; w += 32) bits[w] = 0;
+    __syncwarp();
+    uint32_t ip = 0, op = 0;
+    uint64_t v = 0;
+    bool ok = false;
+    for (uint32_t shift = 0; shift <= 28 && ip < n; shift += 7) {
+        const uint64_t b = src[ip++];
+        v |= (b & 127u) << shift;
+        if (!(b & 128u)) {
+            ok = true;
+            break;
+        }
+    }
+    ok = ok && v == raw;
+    const uint32_t first = ip;   // the first element
+    uint32_t applied = ip;       // literal elements before this byte have been applied
+    while (ok && ip < n) {
+        const uint32_t tag = src[ip++];
+        if ((tag & 3u) == 0) {
+            uint64_t len = (tag >> 2) + 1;
+            if ((tag >> 2) >= 60) {
+                const uint32_t nb = (tag >> 2) - 59;
+                if (nb > n - ip) { ok = false; break; }
+                len = 0;
+                for (uint32_t i = 0; i < nb; ++i) len |= uint64_t(src[ip + i]) << (8 * i);
+                len += 1;
+                ip += nb;
+            }
+            if (len > n - ip || len > raw - op) { ok = false; break; }
+            for (uint32_t i = lane; i < uint32_t(len); i += 32) {
+                const uint32_t b = src[ip + i];
+                if (b) {
+                    const uint32_t x = op + i;
+                    atomicOr(&bits[x >> 5], 1u << (x & 31));
+                    if (x < lim) xor_byte(A.target, one ? base + x : dst_of(ds, cd.dst_count, x), b);
+                }
+            }
+            __syncwarp();
+            ip += uint32_t(len);
+            op += uint32_t(len);
+            applied = ip;
+            continue;
+        }
+        uint32_t len, off;
+        if ((tag & 3u) == 1) {
+            if (ip >= n) { ok = false; break; }
+            len = ((tag >> 2) & 7u) + 4;
+            off = ((tag >> 5) << 8) | src[ip++];
+        } else {
+            const uint32_t nb = (tag & 3u) == 2 ? 2u : 4u;
+            if (nb > n - ip) { ok = false; break; }
+            len = (tag >> 2) + 1;
+            off = 0;
+            for (uint32_t i = 0; i < nb; ++i) off |= uint32_t(src[ip + i]) << (8 * i);
+            ip += nb;
+        }
+        if (off == 0 || off > op || len > raw - op) { ok = false; break; }
+        // the copy's source [op - off, + min(len, off)) holds no non-zero byte
+        const uint32_t s0 = op - off, e0 = s0 + (len < off ? len : off);
+        bool viol = false;
+        for (uint32_t w = (s0 >> 5) + lane; w <= (e0 - 1) >> 5; w += 32) {
+            const uint32_t a = (w << 5) > s0 ? 0u : s0 - (w << 5);
+            const uint32_t b = ((w + 1) << 5) < e0 ? 32u : e0 - (w << 5);
+            const uint32_t m = (b == 32 ? 0xFFFFFFFFu : ((1u << b) - 1)) & ~((1u << a) - 1);
+            viol |= (bits[w] & m) != 0;
+        }
+        if (__reduce_or_sync(kFull, uint32_t(viol))) { ok = false; break; }
+        op += len;
+    }
+    ok = ok && op == raw;
+    if (!ok) {
+        // replay the literal elements already applied (validated the first time)
+        for (uint32_t q = first, o = 0; q < applied;) {
+            const uint32_t tag = src[q++];
+            if ((tag & 3u) == 0) {
+                uint32_t len = (tag >> 2) + 1;
+                if ((tag >> 2) >= 60) {
+                    const uint32_t nb = (tag >> 2) - 59;
+                    len = 0;
+                    for (uint32_t i = 0; i < nb; ++i) len |= uint32_t(src[q + i]) << (8 * i);
+                    len += 1;
+                    q += nb;
+                }
+                for (uint32_t i = lane; i < len; i += 32) {
+                    const uint32_t b = src[q + i];
+                    const uint32_t x = o + i;
+                    if (b && x < lim) xor_byte(A.target, one ? base + x : dst_of(ds, cd.dst_count, x), b);
+                }
+                __syncwarp();
+                q += len;
+                o += len;
+            } else {
+                const uint32_t t = tag & 3u;
+                o += t == 1 ? ((tag >> 2) & 7u) + 4 : (tag >> 2) + 1;
+                q += t == 1 ? 1u : t == 2 ? 2u : 4u;
+            }
+        }
+    }
+    return ok ? 1 : 0;
+}
+
+constexpr int kSnWarps = 8;   // 8 KiB bitmap per warp
+
+__global__ void __launch_bounds__(32 * kSnWarps, 3) snappy_kernel(ApplyArgs A)
+{
+    extern __shared__ __align__(16) uint32_t bitmaps[];
+    uint32_t* bits = bitmaps + (threadIdx.x >> 5) * (kChunk / 32);
+    const int lane = threadIdx.x & 31;
+    if (!A.sc->hdr_ok) return;
+    const uint32_t nbig = A.sc->n_big;   // final: written by apply_kernel only
+    if (nbig == 0) return;
+    const uint8_t* p = A.payload;
+    const uint64_t total = ld64(p + 56), nf = ld64(p + 48), idx_off = total - 8 * nf;
+    const uint64_t V = ld64(p + 24);
+    for (;;) {
+        uint32_t j = 0;
+        if (lane == 0) j = atomicAdd(&A.sc->snappy_ticket, 1u);
+        j = __shfl_sync(kFull, j, 0);
+        if (j >= nbig) break;
+        const uint32_t f = A.defer[A.defer_len - 1 - j];
+        const uint64_t fo = ld64(p + idx_off + 8ull * f);
+        const uint4 h0 = ld_nc16(p + fo), h1 = ld_nc16(p + fo + 16);
+        if ((h0.y & 0xFFu) != kXorSnappy) continue;   // big_kernel's
+        const uint32_t c = h0.z, raw = h0.w, bl = h1.x;
+        const ChunkDesc cd = A.chunks[c];
+        const bool cut = uint64_t(f) == A.abort_at;
+        const uint32_t ub = cd.bits == 16 ? 2u : 1u;
+        uint32_t lim = cut ? (A.split < raw ? A.split : raw) : raw;
+        lim -= lim % ub;
+        const int r = snappy_zsrc_apply(A, cd, A.dst + cd.dst_begin, p + fo + kFrameHdr, bl, raw, lim, bits, lane);
         __syncwarp();   // the bitmap is reused by the next frame
         if (lane == 0) {
             if (r != 1) {
@@ -987,7 +1150,14 @@ int apply_kernel_config(KernelConfig* kc)
     if (e == cudaSuccess)
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&kc->big_blocks_per_sm, big_kernel, kBThreads,
                                                           sizeof(BWarp) * kBWarps);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(snappy_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 int(kSnWarps * kChunk / 8));
+    if (e == cudaSuccess)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&kc->snappy_blocks_per_sm, snappy_kernel, 32 * kSnWarps,
+                                                          kSnWarps * kChunk / 8);
     if (e != cudaSuccess) return cuda_error(e, "apply kernel configuration");
+    if (kc->snappy_blocks_per_sm < 1) kc->snappy_blocks_per_sm = 1;
     if (kc->apply_blocks_per_sm < 1) kc->apply_blocks_per_sm = 1;
     if (kc->big_blocks_per_sm < 1) kc->big_blocks_per_sm = 1;
     if (kc->defer_blocks_per_sm < 1) kc->defer_blocks_per_sm = 1;
@@ -1022,6 +1192,7 @@ int apply_launch(const dcr_plan* P, dcr_recv_state* st, const void* payload, siz
     if (P->profiling) cudaEventRecord(P->ev[4], s);
     defer_kernel<<<sms * P->kc.defer_blocks_per_sm, kDThreads, kChunk, s>>>(A);
     big_kernel<<<sms * P->kc.big_blocks_per_sm, kBThreads, sizeof(BWarp) * kBWarps, s>>>(A);
+    snappy_kernel<<<sms * P->kc.snappy_blocks_per_sm, 32 * kSnWarps, kSnWarps * kChunk / 8, s>>>(A);
     if (P->profiling) cudaEventRecord(P->ev[5], s);
     pending_kernel<<<sms, 256, 0, s>>>(A);
     if (P->profiling) cudaEventRecord(P->ev[6], s);
@@ -1112,6 +1283,7 @@ int apply_launch_noalloc(const dcr_plan* P, dcr_recv_state* st, const void* payl
     apply_kernel<<<sms * P->kc.apply_blocks_per_sm, kAThreads, sizeof(ASmem), s>>>(A);
     defer_kernel<<<sms * P->kc.defer_blocks_per_sm, kDThreads, kChunk, s>>>(A);
     big_kernel<<<sms * P->kc.big_blocks_per_sm, kBThreads, sizeof(BWarp) * kBWarps, s>>>(A);
+    snappy_kernel<<<sms * P->kc.snappy_blocks_per_sm, 32 * kSnWarps, kSnWarps * kChunk / 8, s>>>(A);
     pending_kernel<<<sms, 256, 0, s>>>(A);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_error(e, "apply launch");

@@ -107,7 +107,7 @@ struct ApplyScratch {
     uint64_t target_version;
     uint64_t n_frames;
     uint32_t big_ticket;
-    uint32_t pad;
+    uint32_t snappy_ticket; // snappy_kernel's walk over the same list
 };
 
 // Chunk state of a receiver: (target_version << 2) | state.
@@ -128,6 +128,7 @@ struct KernelConfig {
     int apply_blocks_per_sm = 0;
     int defer_blocks_per_sm = 0;
     int big_blocks_per_sm = 0;
+    int snappy_blocks_per_sm = 0;
 };
 
 // host entry points of the kernel translation units
