@@ -72,6 +72,23 @@ def test_pipelined_refit_matches_oracle_and_sequential(name, make):
     assert np.array_equal(t.cpu().numpy()[:exp.size], orc.receiver_dense(olds))
 
 
+def test_pipelined_refit_snappy_codec():
+    wl = configs.mini(5)
+    orc = oracle.Oracle(wl)
+    olds, news = wl.host_arenas()
+    plan = dcr.Plan(descs_of(wl), window_bytes=wl.window_bytes, codec=dcr.CODEC_SNAPPY)
+    d_old, d_new = to_device(olds), to_device(news)
+    dev, host = _buffers(plan)
+    t = _target(plan, wl, d_old)
+    st = dcr.RecvState(plan, 0)
+    rc, stats, _ = dcr.refit_pipelined(plan, st, d_old, d_new, t, dev, host)
+    assert rc == dcr.OK, dcr.last_error()
+    exp = orc.receiver_dense(news)
+    assert np.array_equal(t.cpu().numpy()[:exp.size], exp)
+    assert st.version == 1 and stats.windows == plan.n_windows
+    assert stats.payload_bytes == sum(_sequential_sizes(plan, d_old, d_new))
+
+
 def test_pipelined_refit_rejections_leave_target_untouched():
     wl = configs.mini(5)
     olds, news = wl.host_arenas()
