@@ -437,6 +437,57 @@ def run_gpu(args):
                 "payload_bytes_per_refit": int(last["payload"])}
         del pdev, phost, stage, rxs
 
+    # abort and retry: per window the hybrid stream is applied with a fault
+    # injected at half its frames, then the same change set is re-encoded in
+    # overwrite-only mode and applied with dcr_apply_retry (one GPU)
+    retry = None
+    if args.abort_retry and ws == 1:
+        rpay = []
+        for w in range(nw):   # overwrite-only stream buffers sized from a first encode
+            buf = torch.empty(max(plan.window(w).canonical_bytes // 6, 1 << 20), dtype=torch.uint8, device=dev)
+            rc, rsize, _ = dcr.encode(plan, olds, news, buf, window=w, mode=dcr.MODE_OVERWRITE_ONLY, counts=False)
+            if rc == dcr.ERR_CAPACITY:
+                buf = torch.empty(min(int(rsize * 1.25), caps[w]), dtype=torch.uint8, device=dev)
+            rpay.append(buf)
+        rlast = {}
+
+        def abort_retry_refit():
+            a, b = (olds, news) if d[0] == 0 else (news, olds)
+            rbytes = 0
+            for w in range(nw):
+                rc, size, _ = dcr.encode(plan, a, b, payloads[w], window=w, base_version=ver[0],
+                                         target_version=ver[0] + 1, counts=False, stream=sh)
+                dcr.check(rc)
+                nf = int(payloads[w][48:56].cpu().numpy().view("<u8")[0])
+                rc, _ = dcr.apply(plan, st, payloads[w], size, target, fault=(nf // 2, 1000), stream=sh)
+                assert rc == dcr.ERR_ABORTED, rc
+                rc, rsize, _ = dcr.encode(plan, a, b, rpay[w], window=w, mode=dcr.MODE_OVERWRITE_ONLY,
+                                          base_version=ver[0], target_version=ver[0] + 1, counts=False, stream=sh)
+                dcr.check(rc)
+                rc, res = dcr.apply_retry(plan, st, rpay[w], rsize, target, stream=sh)
+                dcr.check(rc)
+                rbytes += rsize
+            assert st.version == ver[0] + 1
+            rlast["bytes"] = rbytes
+            ver[0] += 1
+            d[0] ^= 1
+
+        k = max(2, min(args.steps, 5))
+        for _ in range(2):
+            abort_retry_refit()
+        torch.cuda.synchronize()
+        r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        r0.record(stream)
+        for _ in range(k):
+            abort_retry_refit()
+        r1.record(stream)
+        torch.cuda.synchronize()
+        rms = r0.elapsed_time(r1) / k
+        retry = {"ms_per_refit": round(rms, 4), "value": round(N / (rms / 1e3) / 1e9, 3), "unit": UNIT,
+                 "abort": "half of each window's frames applied, one split mid-frame",
+                 "retry_payload_bytes_per_refit": int(rlast["bytes"])}
+        del rpay
+
     # the receiver really holds the last step's target weights
     ref = torch.empty_like(target)
     dcr.check(dcr.dense_refit(plan, olds if d[0] == 0 else news, ref))
@@ -475,6 +526,8 @@ def run_gpu(args):
         line["e2e"] = e2e
     if pipe:
         line["pipelined"] = pipe
+    if retry:
+        line["abort_retry"] = retry
     if rank == 0 and not args.no_cpu_baseline:
         cb = cpu_baseline(wl)
         line["payload_vs_oracle"] = round(P / cb.pop("payload_bytes"), 4)
@@ -499,6 +552,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--window-mb", type=int, default=0, help="window size in MiB (0: the workload's)")
     ap.add_argument("--codec", default="lz4", choices=["lz4", "snappy"], help="block codec of the XOR masks")
+    ap.add_argument("--abort-retry", action="store_true",
+                    help="also time refits aborted at half the frames and completed by the overwrite-only retry")
     ap.add_argument("--pipeline", action="store_true",
                     help="also time dcr_refit_pipelined against the same windows in series")
     ap.add_argument("--no-cpu-baseline", action="store_true")
