@@ -159,10 +159,11 @@ def dist_barrier(ws):
 # --------------------------------------------------------------------------
 # CPU oracle leg (baseline and reference arm)
 # --------------------------------------------------------------------------
-def oracle_runner(wl, threads):
+def oracle_runner(wl, threads, codec="lz4"):
     import numpy as np
     import oracle
     orc = oracle.Oracle(wl)
+    oc = oracle.CODEC_SNAPPY if codec == "snappy" else oracle.CODEC_LZ4
     olds, news = wl.host_arenas()
     tgt = orc.receiver_dense(olds)
     state = {"st": orc.state(0), "dir": 0, "v": 0}
@@ -171,7 +172,7 @@ def oracle_runner(wl, threads):
         a, b = (olds, news) if state["dir"] == 0 else (news, olds)
         for w in range(orc.n_windows):
             pl, _ = orc.encode(a, b, window=w, base_version=state["v"], target_version=state["v"] + 1,
-                               threads=threads)
+                               threads=threads, codec=oc)
             rc = orc.apply(state["st"], pl, tgt, threads=threads)
             assert rc == oracle.OK, rc
         state["v"] += 1
@@ -181,9 +182,9 @@ def oracle_runner(wl, threads):
     return step
 
 
-def cpu_baseline(wl, budget_s=12.0):
+def cpu_baseline(wl, budget_s=12.0, codec="lz4"):
     threads = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
-    step = oracle_runner(wl, threads)
+    step = oracle_runner(wl, threads, codec)
     n, t0, payload = 0, time.perf_counter(), 0
     while True:
         payload = step()
@@ -212,7 +213,7 @@ def run_reference(args):
     import oracle
     wl = build_workload(args.workload, args.frac)
     threads = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
-    step = oracle_runner(wl, threads)
+    step = oracle_runner(wl, threads, args.codec)
     for _ in range(args.warmup):
         step()
     t0 = time.perf_counter()
@@ -529,7 +530,7 @@ def run_gpu(args):
     if retry:
         line["abort_retry"] = retry
     if rank == 0 and not args.no_cpu_baseline:
-        cb = cpu_baseline(wl)
+        cb = cpu_baseline(wl, codec=args.codec)
         line["payload_vs_oracle"] = round(P / cb.pop("payload_bytes"), 4)
         line["cpu_baseline"] = cb
     if rank == 0:
