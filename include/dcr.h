@@ -37,8 +37,9 @@
  *     u64 target_version, u32 window, u32 flags (1 = overwrite-only),
  *     u32 chunk_begin, u32 chunk_count, u64 n_frames, u64 total_bytes;
  *   frames, ascending chunk id, each 16-byte aligned: header (32 B) "DCRF",
- *     u8 kind (1 XOR_LZ4, 2 XOR_RAW, 3 OVERWRITE, 4 OVERWRITE_DENSE),
- *     u8 elem_bits, u16 flags (1 = every LZ4 match copies zero bytes),
+ *     u8 kind (1 XOR_LZ4, 2 XOR_RAW, 3 OVERWRITE, 4 OVERWRITE_DENSE,
+ *     5 XOR_SNAPPY), u8 elem_bits, u16 flags (1 = every match / copy
+ *     copies zero bytes),
  *     u32 chunk_id, u32 raw_len, u32 body_len, u32 changed, u64 0; then the
  *     body, zero padded to 16 bytes;
  *   index: n_frames x u64 frame offsets from the stream start.
