@@ -65,9 +65,13 @@ def measured_peak():
         return 6800.0, "fallback"
 
 
-def ncu_traffic():
+def ncu_traffic(args):
     """Per-launch DRAM bytes of the encode kernel from the committed ncu
-    summary, only if the kernel source is unchanged since it was taken."""
+    summary, only for the configuration it was captured on (dense-tp2, its
+    own change rate, LZ4, one window) and only if the kernel source is
+    unchanged since it was taken; None otherwise."""
+    if (args.workload, args.frac, args.codec, args.window_mb) != ("dense", None, "lz4", 0):
+        return None
     path = os.path.join(ROOT, "profiles", "encode_kernel_dense_tp2.md")
     src = os.path.join(ROOT, "bit_exact_xor_gb300", "csrc", "encode.cu")
     try:
@@ -499,7 +503,7 @@ def run_gpu(args):
     peak, peak_kind = measured_peak()
     alg_bytes = 2 * N / nw + P  # per encode launch: read old+new of the window, write payload
     achieved = alg_bytes / (statistics.mean(enc_ms) / 1e3) / 1e9
-    traffic = ncu_traffic()
+    traffic = ncu_traffic(args)
     clocks = clk.summary()
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": ws, "steps": args.steps,

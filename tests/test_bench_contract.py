@@ -25,3 +25,16 @@ def test_reference_arm_prints_one_contract_line():
     assert d["config"]["workload"].startswith("single")
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
+
+
+def test_ncu_traffic_only_for_the_profiled_configuration():
+    import argparse
+    import importlib.util
+    spec = importlib.util.spec_from_file_location("bench_mod", os.path.join(ROOT, "bench.py"))
+    bench = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(bench)
+    base = dict(workload="dense", frac=None, codec="lz4", window_mb=0)
+    t = bench.ncu_traffic(argparse.Namespace(**base))
+    assert t is None or t > 0   # None once encode.cu changed since the capture
+    for k, v in (("workload", "gqa"), ("frac", 0.03), ("codec", "snappy"), ("window_mb", 64)):
+        assert bench.ncu_traffic(argparse.Namespace(**dict(base, **{k: v}))) is None, k
