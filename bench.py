@@ -29,6 +29,16 @@ sys.path.insert(0, os.path.join(ROOT, "tests"))
 
 METRIC = "encode & apply GB/s of weight bytes on 1 GB300 (% HBM peak); payload bytes"
 UNIT = "GB/s"
+L2_BYTES = 129 << 20        # GB300 L2
+FLUSH_BYTES = 512 << 20
+
+
+def l2_resident(n):
+    """Whether an encode's inputs (old + new, 2n bytes) could still sit in L2
+    from the previous step."""
+    return 2 * n < 4 * L2_BYTES
+
+
 WORKLOAD_NAMES = {
     "dense": "dense-tp2: bf16 transformer h1024 l24 ffn4096 v32768, TP=2 shards, 1% low-3-bit changes",
     "single": "single-bf16: one 4096x4096 bf16 tensor, 1% +-1..4 changes + 0.01% signed zeros",
@@ -196,9 +206,24 @@ def cpu_baseline(wl, budget_s=12.0, codec="lz4"):
         if time.perf_counter() - t0 >= budget_s:
             break
     dt = time.perf_counter() - t0
-    return {"value": round(wl.canonical_bytes * n / dt / 1e9, 4), "unit": UNIT, "cores": threads,
-            "kind": "oracle", "sample": "%d full refit steps (encode+apply) of the whole workload, "
-                                        "%.1f s" % (n, dt), "payload_bytes": payload}
+    out = {"value": round(wl.canonical_bytes * n / dt / 1e9, 4), "unit": UNIT, "cores": threads,
+           "kind": "oracle", "sample": "%d full refit steps (encode+apply) of the whole workload, "
+                                       "%.1f s" % (n, dt), "payload_bytes": payload}
+    # the same oracle on one thread, for one step, when that stays bounded
+    est = dt / n * threads
+    if threads == 1:
+        out["value_1_thread"] = out["value"]
+    elif est <= 30.0:
+        one = oracle_runner(wl, 1, codec)
+        t0 = time.perf_counter()
+        one()
+        d1 = time.perf_counter() - t0
+        out["value_1_thread"] = round(wl.canonical_bytes / d1 / 1e9, 4)
+        out["sample_1_thread"] = "1 full refit step on one thread, %.1f s" % d1
+    else:
+        out["value_1_thread"] = None
+        out["sample_1_thread"] = "not run: one step on one thread would take about %.0f s" % est
+    return out
 
 
 def run_config(args, wl, nw, ws):
@@ -206,8 +231,8 @@ def run_config(args, wl, nw, ws):
     N = wl.canonical_bytes
     return {"workload": WORKLOAD_NAMES[args.workload], "canonical_bytes": N, "codec": getattr(args, "codec", "lz4"),
             "tp": wl.tp, "windows": nw, "parallelism": "replicas" if ws > 1 else "single GPU",
-            "l2": "inputs larger than L2 (2N = %.2f GB read per encode)" % (2 * N / 1e9)
-            if 2 * N > 200e6 else "inputs fit in L2"}
+            "l2": "L2 flushed before each timed step (%d MiB written outside the step's events)" % (FLUSH_BYTES >> 20)
+            if l2_resident(N) else "inputs larger than L2 (2N = %.2f GB read per encode)" % (2 * N / 1e9)}
 
 
 def run_reference(args):
@@ -306,18 +331,31 @@ def run_gpu(args):
     # directions), so the timed steps do not read them back
     for i in range(args.warmup):
         step(False, counts=i == args.warmup - 1)
+    # inputs that could stay in L2 between steps: write a 512 MiB buffer
+    # before each timed step, outside that step's events
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev) if l2_resident(N) else None
     torch.cuda.synchronize()
     dist_barrier(ws)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    spans = []
     with Clocks(local) as clk:
         torch.cuda.synchronize()
         ev0.record(stream)
-        for _ in range(args.steps):
-            step(True)
+        for i in range(args.steps):
+            if flush is not None:
+                flush.fill_(i & 0xFF)
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                step(True)
+                b.record(stream)
+                spans.append((a, b))
+            else:
+                step(True)
         ev1.record(stream)
         torch.cuda.synchronize()
     dist_barrier(ws)
-    ms = ev0.elapsed_time(ev1)
+    ms = sum(a.elapsed_time(b) for a, b in spans) if spans else ev0.elapsed_time(ev1)
+    del flush
     ms_max = dist_max(ms, ws)
     value = N * args.steps * ws / (ms_max / 1e3) / 1e9
 
