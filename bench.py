@@ -48,6 +48,17 @@ WORKLOAD_NAMES = {
 }
 
 
+DEFAULT_FRAC = {"dense": 0.01, "single": 0.01, "gqa": 0.03, "sweep": 0.01, "moe": 0.00085}
+
+
+def change_rate(args):
+    """The changed fraction the run uses ("random" for the fully random new
+    buffer of the sweep)."""
+    if args.workload == "sweep" and args.frac is not None and args.frac >= 1.0:
+        return "random"
+    return args.frac if args.frac is not None else DEFAULT_FRAC[args.workload]
+
+
 def build_workload(name, frac=None):
     from synth import configs
     if name == "dense":
@@ -229,7 +240,11 @@ def cpu_baseline(wl, budget_s=12.0, codec="lz4"):
 def run_config(args, wl, nw, ws):
     """The workload description both arms print."""
     N = wl.canonical_bytes
-    return {"workload": WORKLOAD_NAMES[args.workload], "canonical_bytes": N, "codec": getattr(args, "codec", "lz4"),
+    name = WORKLOAD_NAMES[args.workload]
+    if args.frac is not None:
+        name += " [change rate set to %s]" % ("a fully random new buffer" if change_rate(args) == "random"
+                                             else "%g%%" % (100 * args.frac))
+    return {"workload": name, "change_rate": change_rate(args), "canonical_bytes": N, "codec": getattr(args, "codec", "lz4"),
             "tp": wl.tp, "windows": nw, "parallelism": "replicas" if ws > 1 else "single GPU",
             "l2": "L2 flushed before each timed step (%d MiB written outside the step's events)" % (FLUSH_BYTES >> 20)
             if l2_resident(N) else "inputs larger than L2 (2N = %.2f GB read per encode)" % (2 * N / 1e9)}
