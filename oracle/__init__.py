@@ -71,6 +71,8 @@ def lib():
         L.orc_xor.restype = None
         L.orc_count_changed.argtypes = [VP, U64, U32]
         L.orc_count_changed.restype = U64
+        L.orc_fnv1a64.argtypes = [VP, U64]
+        L.orc_fnv1a64.restype = U64
         L.orc_lz4_encode.argtypes = [VP, U64, VP, U64]
         L.orc_lz4_encode.restype = U64
         L.orc_lz4_decode.argtypes = [VP, U64, VP, U64, U32]
@@ -229,6 +231,12 @@ def xor(a, b):
 
 def count_changed(mask, elem_bits):
     return int(lib().orc_count_changed(_ptr(mask), mask.size, elem_bits))
+
+
+def fnv1a64(data):
+    """FNV-1a 64 of a bytes object (the plan hash's step)."""
+    buf = np.frombuffer(bytes(data), dtype=np.uint8) if len(data) else np.zeros(1, dtype=np.uint8)
+    return int(lib().orc_fnv1a64(_ptr(buf), len(data)))
 
 
 def lz4_encode(data):

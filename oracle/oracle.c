@@ -106,6 +106,13 @@ static void fnv64(uint64_t* h, uint64_t v)
     fnv32(h, (uint32_t)(v >> 32));
 }
 
+uint64_t orc_fnv1a64(const uint8_t* p, uint64_t n)
+{
+    uint64_t h = 0xCBF29CE484222325ULL;
+    fnv(&h, p, (size_t)n);
+    return h;
+}
+
 /* Chunks: each canonical part is cut into 64 KiB pieces of its own byte
  * space (a part's last chunk may be short).  Windows: whole tensors are
  * packed in order while the window stays within window_bytes; a tensor larger

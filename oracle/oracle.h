@@ -63,6 +63,8 @@ int orc_receiver_dense(const orc_tensor* t, uint32_t n, const uint8_t* const* sh
 /* primitives */
 void orc_xor(const uint8_t* a, const uint8_t* b, uint8_t* out, uint64_t n);
 uint64_t orc_count_changed(const uint8_t* mask, uint64_t nbytes, uint32_t elem_bits);
+/* FNV-1a 64 of n bytes (the step the plan hash is built from) */
+uint64_t orc_fnv1a64(const uint8_t* p, uint64_t n);
 uint64_t orc_lz4_encode(const uint8_t* in, uint64_t n, uint8_t* out, uint64_t cap);
 int orc_lz4_decode(const uint8_t* in, uint64_t n, uint8_t* out, uint64_t raw_len, uint32_t zsrc);
 uint64_t orc_snappy_encode(const uint8_t* in, uint64_t n, uint8_t* out, uint64_t cap);

@@ -616,3 +616,14 @@ def test_plan_hash_depends_only_on_canonical_description():
     assert oracle.Oracle(a).plan_hash == oracle.Oracle(b).plan_hash
     c = configs.dense(hidden=96, layers=2, ffn=320, vocab=1002)
     assert oracle.Oracle(c).plan_hash != oracle.Oracle(a).plan_hash
+
+
+# The plan hash is FNV-1a 64 (Fowler, Noll and Vo's published definition:
+# offset basis 0xcbf29ce484222325, prime 0x100000001b3, xor then multiply per
+# byte); pinned to the reference values of that definition's test suite.
+def test_fnv1a64_reference_values():
+    assert oracle.fnv1a64(b"") == 0xCBF29CE484222325
+    assert oracle.fnv1a64(b"a") == 0xAF63DC4C8601EC8C
+    assert oracle.fnv1a64(b"foobar") == 0x85944171F73967E8
+    # xor-then-multiply order: FNV-1 (multiply first) gives another value
+    assert oracle.fnv1a64(b"a") != 0xAF63BD4C8601B7BE
