@@ -12,6 +12,12 @@
  *   overwrite records; the receiver decodes and applies in place, with
  *   per-chunk dedup and an idempotent overwrite-only retry.
  * Each function in oracle.c cites the passage it follows.
+ *
+ * Parity unpinned: the plan hash's serialization (which fields, in which
+ * order, go into the FNV-1a 64 hash) is a format convention the pages do not
+ * fix; only its FNV-1a step (orc_fnv1a64) is pinned to published reference
+ * values.  The greedy encoders' payload sizes are pinned as valid LZ4 and
+ * Snappy blocks that round-trip, not to a size the pages print.
  */
 #ifndef DCR_ORACLE_H
 #define DCR_ORACLE_H
