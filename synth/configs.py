@@ -259,6 +259,16 @@ def full(n):
     return {1: single, 2: dense, 3: gqa, 4: sweep, 5: nvfp4_moe}[n]()
 
 
+def oversized_window(window_bytes=700 << 10, seed=0xDC5EED06):
+    """A 2 MiB bf16 tensor (row-split over TP=2) larger than the 700 KiB
+    window, then a 100 KiB tensor (column-split): windows of 10 whole chunks
+    cut the first tensor, and the second packs into the window holding the
+    first one's last two chunks."""
+    ts = [Tensor("big", rows=1024, cols=1024, split=SPLIT_ROWS, rule=RULE_PM4, frac=0.01, **BF),
+          Tensor("after", rows=50, cols=1024, split=SPLIT_COLS, rule=RULE_PM4, frac=0.02, **BF)]
+    return Workload("oversized-window", seed, 2, ts, window_bytes=window_bytes).layout()
+
+
 def mini(n):
     if n == 1:
         return single(rows=300, cols=520, name="mini-single")

@@ -607,6 +607,28 @@ def test_windows_partition_at_tensor_boundaries():
     assert starts == sorted(starts)
 
 
+def test_tensor_larger_than_a_window_is_cut_at_chunks():
+    # windows pack whole tensors while they fit; a larger tensor is cut at
+    # 64 KiB chunk boundaries (700 KiB holds 10 chunks): by hand, chunks
+    # [0, 10), [10, 20), [20, 30) of the 32-chunk tensor, then its last two
+    # with the 2 chunks (64 + 36 KiB) of the 100 KiB tensor after it
+    wl = configs.oversized_window()
+    o = oracle.Oracle(wl)
+    assert o.n_windows == 4
+    assert [tuple(o.window_range(w)) for w in range(4)] == [(0, 10), (10, 10), (20, 10), (30, 4)]
+    assert [o.chunk_info(k)[0] for k in range(30, 34)] == [0, 0, 1, 1]
+    assert o.chunk_info(33)[3] == 100 * 1024 - 65536
+    olds, news = wl.host_arenas()
+    tgt, exp = o.receiver_dense(olds), o.receiver_dense(news)
+    st = o.state(0)
+    for i, w in enumerate([2, 0, 3, 1]):   # any window order; commit after the last
+        pl, _ = o.encode(olds, news, window=w)
+        assert check_structure(pl)[0]["window"] == w
+        assert o.apply(st, pl, tgt) == oracle.OK
+        assert st.version == (1 if i == 3 else 0)
+    assert np.array_equal(tgt, exp)
+
+
 def test_plan_hash_depends_only_on_canonical_description():
     a = configs.mini(2)
     b = configs.mini(2)
