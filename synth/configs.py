@@ -269,6 +269,20 @@ def oversized_window(window_bytes=700 << 10, seed=0xDC5EED06):
     return Workload("oversized-window", seed, 2, ts, window_bytes=window_bytes).layout()
 
 
+def tp16(frac=0.02, seed=0xDC5EED07):
+    """Every split kind at the largest shard count (TP=16): row-split and
+    column-split bf16 (64-column pieces), a fused QKV with one kv group per
+    shard, a replicated norm and a row-split e4m3 tensor."""
+    ts = [Tensor("rows", rows=512, cols=128, split=SPLIT_ROWS, rule=RULE_PM4, frac=frac, **BF),
+          Tensor("cols", rows=64, cols=1024, split=SPLIT_COLS, rule=RULE_LOW3, frac=frac, **BF),
+          Tensor("qkv", rows=(32 + 2 * 16) * 8, cols=128, split=RESIDUAL_QKV, rule=RULE_PM4, frac=frac,
+                 q_heads=32, kv_heads=16, head_dim=8, **BF),
+          Tensor("norm", rows=1, cols=128, split=REPLICATED, rule=RULE_PM4, frac=0.05, **BF),
+          Tensor("e4m3", elem_bits=8, rows=256, cols=512, split=SPLIT_ROWS, value_kind=VAL_E4M3_SCALE,
+                 rule=RULE_BPM4, frac=frac)]
+    return Workload("tp16", seed, 16, ts).layout()
+
+
 def mini(n):
     if n == 1:
         return single(rows=300, cols=520, name="mini-single")

@@ -332,6 +332,36 @@ def test_split_projection_equals_numpy_concatenate():
     assert all(seen.values())
 
 
+def test_tp16_projection_equals_numpy_and_round_trips():
+    # the largest shard count: every split kind against numpy stacking of the
+    # 16 shards (fused QKV: one kv group per shard), then a whole refit
+    wl = configs.tp16()
+    o = oracle.Oracle(wl)
+    olds, news = wl.host_arenas()
+    for k, t in enumerate(wl.tensors):
+        eb = t.elem_bits // 8
+        rl, cl = t.local_shape(wl.tp)
+        parts = [olds[r][t.shard_offset[r]:t.shard_offset[r] + rl * cl * eb].reshape(rl, cl * eb)
+                 for r in t.holders(wl.tp)]
+        if t.split == configs.RESIDUAL_QKV:
+            qpg, D = t.q_heads // t.kv_heads, t.head_dim
+            g = np.concatenate(parts, axis=0).reshape(t.kv_heads, qpg + 2, D, cl * eb)
+            refs = [g[:, :qpg].reshape(-1, cl * eb), g[:, qpg].reshape(-1, cl * eb), g[:, qpg + 1].reshape(-1, cl * eb)]
+        elif t.split == configs.SPLIT_COLS:
+            refs = [np.concatenate(parts, axis=1)]
+        else:
+            refs = [np.concatenate(parts, axis=0)]
+        assert len(parts) == (1 if t.split == configs.REPLICATED else 16)
+        for sub, ref in enumerate(refs):
+            assert np.array_equal(o.canonical(k, sub, olds), ref.reshape(-1)), (t.name, sub)
+    tgt, exp = o.receiver_dense(olds), o.receiver_dense(news)
+    st = o.state(0)
+    pl, ch = o.encode(olds, news)
+    assert int(ch.sum()) > 0
+    assert o.apply(st, pl, tgt) == oracle.OK and st.version == 1
+    assert np.array_equal(tgt, exp)
+
+
 def test_qkv_deinterleave_equals_numpy_reshape():
     wl = configs.mini(3)
     o = oracle.Oracle(wl)
