@@ -67,6 +67,11 @@ def test_plan_rejects_degenerate_tensors():
                        head_dim=8, recv_layout=dcr.LAYOUT_ROWGROUP_INTERLEAVE, recv_group=8), "receiver layout"),
         (dcr.make_desc("group", 16, 60, 64, dcr.REPLICATED, 1, [0], 0, recv_layout=dcr.LAYOUT_ROWGROUP_INTERLEAVE,
                        recv_group=8), "row-group"),
+        (dcr.make_desc("slot2", 16, 64, 64, dcr.REPLICATED, 1, [0], 0, recv_layout=dcr.LAYOUT_ROWGROUP_INTERLEAVE,
+                       recv_group=8, recv_slot=2), "row-group"),
+        (dcr.make_desc("e2m1_shard", 4, 64, 66, dcr.SPLIT_COLS, 2, [0, 0], 0), "shard columns must be even"),
+        (dcr.make_desc("split7", 16, 64, 64, 7, 1, [0], 0), "unknown split"),
+        (dcr.make_desc("layout5", 16, 64, 64, dcr.REPLICATED, 1, [0], 0, recv_layout=5), "unknown receiver layout"),
     ]
     for d, why in cases:
         rc, msg, h = _build([d])
