@@ -6,13 +6,17 @@ values changed with low-mantissa perturbations): dcr_encode of the trainer
 shards (gather + XOR + count + LZ4 + frame compaction) followed by dcr_apply
 on the receiver arena (decode + XOR in place + dedup + commit).  Steps
 alternate direction (old->new, new->old) so the receiver never needs a
-restore.  Inputs (1.4 GB read per encode) are larger than L2.
+restore.  Inputs (1.4 GB read per encode) are larger than L2; workloads
+small enough to stay in L2 get a 512 MiB buffer written before each timed
+step, outside that step's events.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
                   [--workload dense|single|gqa|sweep|moe] [--frac F]
+                  [--window-mb M] [--codec lz4|snappy] [--pipeline] [--abort-retry]
+                  [--no-e2e] [--no-cpu-baseline]
 
-Prints one JSON line.  --impl reference times the CPU oracle (the reference
-arm of this build) on the same workload.
+Prints one JSON line.  --impl reference times the CPU oracle (the
+benchmark's reference arm) on the same workload.
 """
 import argparse
 import hashlib
