@@ -283,6 +283,23 @@ def tp16(frac=0.02, seed=0xDC5EED07):
     return Workload("tp16", seed, 16, ts).layout()
 
 
+def lowbit_pair(seed=0xDC5EED08):
+    """Hand-checkable low-bit layout: an e2m1 gate/up pair [4, 4] and its
+    e4m3 scales [4, 2] paired by the receiver in row groups of 2, then an
+    e2m1 [2, 4] tensor stored canonically.  Receiver arena: fused w13 (16
+    bytes) at 0, fused scales (16 bytes) at 256, the last tensor at 512."""
+    fp4 = lambda n, r, c, **kw: Tensor(n, elem_bits=4, rows=r, cols=c, split=REPLICATED,
+                                       value_kind=VAL_BYTES, rule=RULE_NIBBLE, frac=0.25, **kw)
+    sc = lambda n, r, c, **kw: Tensor(n, elem_bits=8, rows=r, cols=c, split=REPLICATED,
+                                      value_kind=VAL_E4M3_SCALE, rule=RULE_BPM4, frac=0.25, **kw)
+    ts = [fp4("gate", 4, 4, recv_layout=RECV_ROWGROUP, recv_group=2, recv_slot=0, recv_offset=("w13",)),
+          fp4("up", 4, 4, recv_layout=RECV_ROWGROUP, recv_group=2, recv_slot=1, recv_offset=("w13",)),
+          sc("gate_s", 4, 2, recv_layout=RECV_ROWGROUP, recv_group=2, recv_slot=0, recv_offset=("w13s",)),
+          sc("up_s", 4, 2, recv_layout=RECV_ROWGROUP, recv_group=2, recv_slot=1, recv_offset=("w13s",)),
+          fp4("down", 2, 4)]
+    return Workload("lowbit-pair", seed, 1, ts).layout()
+
+
 def mini(n):
     if n == 1:
         return single(rows=300, cols=520, name="mini-single")

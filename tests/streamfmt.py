@@ -67,3 +67,30 @@ def overwrite_records(f):
     pad = (4 - (2 * n) % 4) % 4
     vals = body[4 + 2 * n + pad:4 + 2 * n + pad + n * ub].reshape(n, ub)
     return offs, vals
+
+
+def build_stream(plan_hash, window, chunk_begin, chunk_count, frames, base_version=0, target_version=1,
+                 flags=0):
+    """A stream assembled by hand from the format description: frames is a
+    list of (kind, elem_bits, frame_flags, chunk, raw_len, changed, body)."""
+    out = bytearray(64)
+    offs = []
+    for kind, bits, fflags, chunk, raw, changed, body in frames:
+        body = bytes(body)
+        offs.append(len(out))
+        out += struct.pack("<4sBBHIIIIQ", FRAME_MAGIC, kind, bits, fflags, chunk, raw, len(body), changed, 0)
+        out += body + bytes((-(32 + len(body))) % 16)
+    for o in offs:
+        out += struct.pack("<Q", o)
+    struct.pack_into("<4sIQQQIIIIQQ", out, 0, STREAM_MAGIC, 1, plan_hash, base_version, target_version,
+                     window, flags, chunk_begin, chunk_count, len(offs), len(out))
+    return np.frombuffer(bytes(out), dtype=np.uint8).copy()
+
+
+def overwrite_body(offsets, values, unit):
+    """OVERWRITE body: u32 count, u16 unit offsets, pad to 4, the new units."""
+    n = len(offsets)
+    b = struct.pack("<I", n) + struct.pack("<%dH" % n, *offsets)
+    b += bytes((4 - (2 * n) % 4) % 4)
+    assert len(values) == n * unit
+    return b + bytes(values)

@@ -440,3 +440,22 @@ def test_changes_near_the_end_of_a_chunk(encoder):
     flips += [41 * 65536 + 65536 - 1 - k for k in range(13)]
     g, o = _flip_case(8, 42, 65536, flips, encoder=encoder)
     assert len(frames_by_chunk(g)[1]) == 42
+
+
+@pytest.mark.parametrize("make", ["dense_gate_stream", "record_stream"])
+def test_overwrite_low_bit_rowgroup_hand_vectors(make):
+    # the same hand-built overwrite streams the oracle is pinned with, applied
+    # by the GPU retry path: 4- and 8-bit units land through the row-group remap
+    import lowbit_vectors
+    wl = configs.lowbit_pair()
+    plan = dcr.Plan(descs_of(wl))
+    pl, want = getattr(lowbit_vectors, make)(plan.info.plan_hash)
+    d_pl = torch.from_numpy(pl).to("cuda")
+    for _ in range(2):   # idempotent: a second apply leaves the same bytes
+        tgt = torch.zeros(max(plan.info.recv_bytes, wl.recv_bytes), dtype=torch.uint8, device="cuda")
+        st = dcr.RecvState(plan, 0)
+        rc, res = dcr.apply_retry(plan, st, d_pl, pl.size, tgt)
+        dcr.check(rc)
+        rc, res = dcr.apply_retry(plan, dcr.RecvState(plan, 0), d_pl, pl.size, tgt)
+        dcr.check(rc)
+        assert np.array_equal(tgt.cpu().numpy()[:want.size], want)

@@ -16,6 +16,7 @@ import synth
 from synth import configs
 
 from conftest import read_table
+import lowbit_vectors
 from streamfmt import check_structure, overwrite_records, parse
 
 pytestmark = pytest.mark.filterwarnings("ignore")
@@ -604,6 +605,67 @@ def test_abort_at_every_frame_then_overwrite_retry(n):
             rc = o.apply(st, retry, tgt, retry_only=True)
             assert rc == oracle.OK and st.version == 1
             assert np.array_equal(tgt, exp)
+
+
+# ---- overwrite apply on 8- and 4-bit units, through the row-group remap ----
+# (popular write-up, XOR or overwrite: both reach the new bits exactly;
+# blog, Working with low-precision RL: packed FP4 with fp8 scales, gate/up
+# rows paired in groups)
+@pytest.mark.parametrize("make", [lambda: configs.mini(5), configs.tp16, configs.lowbit_pair],
+                         ids=["mini-moe", "tp16", "lowbit-pair"])
+def test_overwrite_only_stream_reaches_new_on_low_bit_layouts(make):
+    wl = make()
+    o = oracle.Oracle(wl)
+    olds, news = wl.host_arenas()
+    tgt, exp = o.receiver_dense(olds), o.receiver_dense(news)
+    assert not np.array_equal(tgt, exp)
+    st = o.state(0)
+    kinds = set()
+    for w in range(o.n_windows):
+        pl, ch = o.encode(olds, news, window=w, mode=oracle.MODE_OVERWRITE_ONLY)
+        _, frames = check_structure(pl)
+        kinds |= {(f["kind"], f["elem_bits"]) for f in frames}
+        assert o.apply(st, pl, tgt, retry_only=True) == oracle.OK
+    assert np.array_equal(tgt, exp) and st.version == 1
+    assert {b for _, b in kinds} >= ({4, 8} if make is not configs.tp16 else {8, 16})
+
+
+def test_abort_at_every_frame_then_overwrite_retry_low_bit_windows():
+    wl, o, olds, news, tgt0, exp = _setup(5)
+    for w in range(o.n_windows):
+        pl, _ = o.encode(olds, news, window=w)
+        retry, _ = o.encode(olds, news, window=w, mode=oracle.MODE_OVERWRITE_ONLY)
+        nf = parse(pl)[0]["n_frames"]
+        for k in range(0, nf, max(1, nf // 7)):
+            for split in (0, 301, 65536):
+                tgt = tgt0.copy()
+                st = o.state(0)
+                # the other windows applied cleanly, this one aborted at frame k
+                for v in range(o.n_windows):
+                    if v != w:
+                        assert o.apply(st, o.encode(olds, news, window=v)[0], tgt) == oracle.OK
+                assert o.apply(st, pl, tgt, abort_at=k, split=split) == oracle.E_ABORTED
+                assert st.version == 0
+                assert o.apply(st, retry, tgt, retry_only=True) == oracle.OK
+                assert st.version == 1 and np.array_equal(tgt, exp)
+
+
+def _lowbit_apply(pl):
+    wl = configs.lowbit_pair()
+    o = oracle.Oracle(wl)
+    tgt = np.zeros(wl.recv_bytes, dtype=np.uint8)
+    assert o.apply(o.state(0), pl, tgt, retry_only=True) == oracle.OK
+    again = tgt.copy()
+    assert o.apply(o.state(0), pl, again, retry_only=True) == oracle.OK
+    assert np.array_equal(again, tgt), "overwrite is idempotent"
+    return tgt
+
+
+@pytest.mark.parametrize("make", [lowbit_vectors.dense_gate_stream, lowbit_vectors.record_stream],
+                         ids=["dense-e2m1", "records-e2m1-e4m3"])
+def test_overwrite_through_rowgroup_remap_hand_vectors(make):
+    pl, want = make(oracle.Oracle(configs.lowbit_pair()).plan_hash)
+    assert np.array_equal(_lowbit_apply(pl), want)
 
 
 def test_corrupt_frame_is_reported_and_retry_recovers():
