@@ -1,22 +1,27 @@
 """Benchmark: bit-exact delta-compressed refit (encode + apply) on GB300.
 
-One step = one full refit of the dense TP=2 transformer workload (hidden 1024,
-24 layers, FFN 4096, vocab 32768, bf16, 704 MiB canonical, 1 % of stored
-values changed with low-mantissa perturbations): dcr_encode of the trainer
-shards (gather + XOR + count + LZ4 + frame compaction) followed by dcr_apply
-on the receiver arena (decode + XOR in place + dedup + commit).  Steps
-alternate direction (old->new, new->old) so the receiver never needs a
-restore.  Inputs (1.4 GB read per encode) are larger than L2; workloads
-small enough to stay in L2 get a 512 MiB buffer written before each timed
-step, outside that step's events.
+One step = one full refit of the NVFP4 MoE block stack (hidden 6144, 64
+experts, expert FFN 2048, 16 layers; e2m1 values packed two per byte with
+e4m3 scales per 16; 20.25 GiB canonical, streamed in two windows of at most
+16 GiB; 0.085 % of bytes changed; the receiver pairs gate/up rows in groups
+of 64): per window dcr_encode (gather + XOR + count + LZ4 + frame
+compaction) then dcr_apply on the receiver arena (decode + XOR in place
+through the row-group remap + dedup + commit).  This is the largest of the
+five workloads that fits one GPU.  Steps alternate direction (old->new,
+new->old) so the receiver never needs a restore.  Inputs (2N = 43.5 GB read
+per refit) are larger than L2; workloads small enough to stay in L2 get a
+512 MiB buffer written before each timed step, outside that step's events.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
-                  [--workload dense|single|gqa|sweep|moe] [--frac F]
-                  [--window-mb M] [--codec lz4|snappy] [--pipeline] [--abort-retry]
-                  [--no-e2e] [--no-cpu-baseline]
+                  [--workload moe|dense|single|gqa|sweep] [--frac F]
+                  [--moe-layers L] [--window-mb M] [--codec lz4|snappy]
+                  [--pipeline] [--abort-retry] [--no-e2e] [--no-cpu-baseline]
 
 Prints one JSON line.  --impl reference times the CPU oracle (the
-benchmark's reference arm) on the same workload.
+benchmark's reference arm) on the same workload: each of its steps refits a
+bounded sample of it (at most 640 MiB of the workload's own bytes), as does
+the cpu_baseline leg of the GPU arm.  --moe-layers builds a shorter MoE stack
+(the same tensors per layer) for profiler captures.
 """
 import argparse
 import hashlib
@@ -48,7 +53,8 @@ WORKLOAD_NAMES = {
     "single": "single-bf16: one 4096x4096 bf16 tensor, 1% +-1..4 changes + 0.01% signed zeros",
     "gqa": "gqa-tp4: Llama GQA h4096 l32 32q/8kv hd128 ffn14336 v128256, TP=4, fused QKV residual, 3%",
     "sweep": "sweep: one 8 GiB bf16 buffer, +-1..4 changes",
-    "moe": "nvfp4-moe: h6144 64 experts ffn2048 16 layers, e2m1 + e4m3 scales, 0.085%, 16 GiB windows",
+    "moe": "nvfp4-moe: h6144 64 experts ffn2048 %d layers, e2m1 + e4m3 scales, 0.085%%, 16 GiB windows, "
+           "receiver gate/up row groups of 64",
 }
 
 
@@ -63,7 +69,7 @@ def change_rate(args):
     return args.frac if args.frac is not None else DEFAULT_FRAC[args.workload]
 
 
-def build_workload(name, frac=None):
+def build_workload(name, frac=None, moe_layers=16):
     from synth import configs
     if name == "dense":
         return configs.dense(frac=frac if frac is not None else 0.01)
@@ -76,7 +82,7 @@ def build_workload(name, frac=None):
             return configs.sweep(random_new=True)
         return configs.sweep(frac=frac if frac is not None else 0.01)
     if name == "moe":
-        return configs.nvfp4_moe(frac=frac if frac is not None else 0.00085)
+        return configs.nvfp4_moe(frac=frac if frac is not None else 0.00085, layers=moe_layers)
     raise SystemExit("unknown workload " + name)
 
 
@@ -90,25 +96,33 @@ def measured_peak():
         return 6800.0, "fallback"
 
 
-def ncu_traffic(args):
-    """Per-launch DRAM bytes of the encode kernel from the committed ncu
-    summary, only for the configuration it was captured on (dense-tp2, its
-    own change rate, LZ4, one window) and only if the kernel source is
-    unchanged since it was taken; None otherwise."""
-    if (args.workload, args.frac, args.codec, args.window_mb) != ("dense", None, "lz4", 0):
+PROFILED = {"dense": "encode_kernel_dense_tp2.md", "moe": "encode_kernel_nvfp4_moe.md"}
+
+
+def ncu_traffic(args, bytes_per_launch):
+    """Per-launch DRAM bytes (read + write) of the encode kernel from a
+    committed ncu summary, or None.  Only for a workload that has one (its own
+    change rate, LZ4, its own windows) and only while encode.cu is the source
+    that was profiled.  A capture taken on a shorter stack of the same
+    tensors (same dtype mix and change rate) is scaled to this run's
+    canonical bytes per launch."""
+    if args.workload not in PROFILED or (args.frac, args.codec, args.window_mb) != (None, "lz4", 0):
         return None
-    path = os.path.join(ROOT, "profiles", "encode_kernel_dense_tp2.md")
+    path = os.path.join(ROOT, "profiles", PROFILED[args.workload])
     src = os.path.join(ROOT, "bit_exact_xor_gb300", "csrc", "encode.cu")
     try:
         text = open(path).read()
         sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-        fields = dict(l.split(":", 1) for l in text.splitlines() if l.startswith(("traffic_bytes_per_launch:",
-                                                                                   "encode_cu_sha256_16:")))
-        if fields.get("encode_cu_sha256_16:".rstrip(":"), "").strip() == sha:
-            return int(fields["traffic_bytes_per_launch"].strip())
+        keys = ("traffic_bytes_per_launch", "canonical_bytes_per_launch", "encode_cu_sha256_16")
+        fields = {k.strip(): v.strip() for k, v in (l.split(":", 1) for l in text.splitlines()
+                                                    if l.startswith(keys))}
+        if fields.get("encode_cu_sha256_16") != sha:
+            return None
+        t = int(fields["traffic_bytes_per_launch"])
+        c = int(fields.get("canonical_bytes_per_launch", bytes_per_launch))
+        return int(round(t * bytes_per_launch / c))
     except Exception:
-        pass
-    return None
+        return None
 
 
 class Clocks:
@@ -211,9 +225,20 @@ def oracle_runner(wl, threads, codec="lz4"):
     return step
 
 
+ORACLE_SAMPLE_BYTES = 640 << 20    # bytes of the workload one oracle step refits at most
+
+
+def oracle_sample(wl):
+    """(sample workload, description): the workload itself if it is small,
+    else a bounded sample of its own bytes (same generator streams)."""
+    from synth import configs
+    return configs.sample(wl, ORACLE_SAMPLE_BYTES)
+
+
 def cpu_baseline(wl, budget_s=12.0, codec="lz4"):
     threads = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
-    step = oracle_runner(wl, threads, codec)
+    swl, what = oracle_sample(wl)
+    step = oracle_runner(swl, threads, codec)
     n, t0, payload = 0, time.perf_counter(), 0
     while True:
         payload = step()
@@ -221,20 +246,20 @@ def cpu_baseline(wl, budget_s=12.0, codec="lz4"):
         if time.perf_counter() - t0 >= budget_s:
             break
     dt = time.perf_counter() - t0
-    out = {"value": round(wl.canonical_bytes * n / dt / 1e9, 4), "unit": UNIT, "cores": threads,
-           "kind": "oracle", "sample": "%d full refit steps (encode+apply) of the whole workload, "
-                                       "%.1f s" % (n, dt), "payload_bytes": payload}
+    out = {"value": round(swl.canonical_bytes * n / dt / 1e9, 4), "unit": UNIT, "cores": threads,
+           "kind": "oracle", "sample": "%d full refit steps (encode+apply) of %s, %.1f s" % (n, what, dt),
+           "payload_bytes": payload, "sample_bytes": swl.canonical_bytes}
     # the same oracle on one thread, for one step, when that stays bounded
     est = dt / n * threads
     if threads == 1:
         out["value_1_thread"] = out["value"]
     elif est <= 30.0:
-        one = oracle_runner(wl, 1, codec)
+        one = oracle_runner(swl, 1, codec)
         t0 = time.perf_counter()
         one()
         d1 = time.perf_counter() - t0
-        out["value_1_thread"] = round(wl.canonical_bytes / d1 / 1e9, 4)
-        out["sample_1_thread"] = "1 full refit step on one thread, %.1f s" % d1
+        out["value_1_thread"] = round(swl.canonical_bytes / d1 / 1e9, 4)
+        out["sample_1_thread"] = "1 full refit step of the same sample on one thread, %.1f s" % d1
     else:
         out["value_1_thread"] = None
         out["sample_1_thread"] = "not run: one step on one thread would take about %.0f s" % est
@@ -245,6 +270,8 @@ def run_config(args, wl, nw, ws):
     """The workload description both arms print."""
     N = wl.canonical_bytes
     name = WORKLOAD_NAMES[args.workload]
+    if args.workload == "moe":
+        name = name % args.moe_layers
     if args.frac is not None:
         name += " [change rate set to %s]" % ("a fully random new buffer" if change_rate(args) == "random"
                                              else "%g%%" % (100 * args.frac))
@@ -259,25 +286,29 @@ def run_reference(args):
     if rank != 0:
         return 0
     import oracle
-    wl = build_workload(args.workload, args.frac)
+    wl = build_workload(args.workload, args.frac, args.moe_layers)
+    swl, what = oracle_sample(wl)
     threads = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
-    step = oracle_runner(wl, threads, args.codec)
+    step = oracle_runner(swl, threads, args.codec)
     for _ in range(args.warmup):
         step()
     t0 = time.perf_counter()
     for _ in range(args.steps):
         step()
     dt = time.perf_counter() - t0
-    value = wl.canonical_bytes * args.steps / dt / 1e9
+    value = swl.canonical_bytes * args.steps / dt / 1e9
+    sample = "each step one full oracle refit (encode+apply) of %s" % what
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "u8", "data": "synthetic",
             "config": run_config(args, wl, oracle.Oracle(wl).n_windows, 1),
             "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": threads, "kind": "oracle",
-                             "sample": "%d timed oracle refit steps of the whole workload" % args.steps},
+                             "sample": "%d timed steps; %s" % (args.steps, sample)},
             "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
+    line["config"]["oracle_sample"] = sample
+    line["config"]["oracle_sample_bytes"] = swl.canonical_bytes
     print(json.dumps(line))
     return 0
 
@@ -301,7 +332,7 @@ def run_gpu(args):
     dev = torch.device("cuda", torch.cuda.current_device())
     stream = torch.cuda.current_stream()
 
-    wl = build_workload(args.workload, args.frac)
+    wl = build_workload(args.workload, args.frac, args.moe_layers)
     N = wl.canonical_bytes
     plan = dcr.Plan(descs_of(wl), window_bytes=(args.window_mb << 20) or wl.window_bytes,
                     codec=dcr.CODEC_SNAPPY if args.codec == "snappy" else dcr.CODEC_LZ4)
@@ -385,9 +416,14 @@ def run_gpu(args):
     # timed step, the first one included, is inside the timed region.
     e2e = None
     if not args.no_e2e:
-        h_old = [x.cpu().pin_memory() for x in olds]
-        h_new = [x.cpu().pin_memory() for x in news]
-        h_pl = [torch.empty(p.numel(), dtype=torch.uint8).pin_memory() for p in payloads]
+        def pinned_copy(x):   # straight into pinned memory: no pageable staging copy
+            h = torch.empty(x.numel(), dtype=torch.uint8, pin_memory=True)
+            h.copy_(x)
+            return h
+
+        h_old = [pinned_copy(x) for x in olds]
+        h_new = [pinned_copy(x) for x in news]
+        h_pl = [torch.empty(p.numel(), dtype=torch.uint8, pin_memory=True) for p in payloads]
         d_in = [([torch.empty_like(x) for x in olds], [torch.empty_like(x) for x in news]) for _ in range(2)]
         rx = [torch.empty_like(p) for p in payloads]
         cs = torch.cuda.Stream()
@@ -560,7 +596,7 @@ def run_gpu(args):
     peak, peak_kind = measured_peak()
     alg_bytes = 2 * N / nw + P  # per encode launch: read old+new of the window, write payload
     achieved = alg_bytes / (statistics.mean(enc_ms) / 1e3) / 1e9
-    traffic = ncu_traffic(args)
+    traffic = ncu_traffic(args, N / nw)
     clocks = clk.summary()
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
@@ -608,7 +644,8 @@ def main():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
-    ap.add_argument("--workload", default="dense", choices=sorted(WORKLOAD_NAMES))
+    ap.add_argument("--workload", default="moe", choices=sorted(WORKLOAD_NAMES))
+    ap.add_argument("--moe-layers", type=int, default=16, help="layers of the MoE stack (profiler captures)")
     ap.add_argument("--frac", type=float, default=None,
                     help="change rate (sweep: 1 or more = fully random new buffer)")
     ap.add_argument("--no-e2e", action="store_true")

@@ -37,6 +37,7 @@
 //                 XOR sweep.
 //   pending_kernel  counts framed chunks that are not DONE for the target
 //                 version (the commit rule).
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -1156,6 +1157,12 @@ int apply_kernel_config(KernelConfig* kc)
     if (e == cudaSuccess)
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&kc->snappy_blocks_per_sm, snappy_kernel, 32 * kSnWarps,
                                                           kSnWarps * kChunk / 8);
+    if (e == cudaSuccess) {
+        // load the last kernel of the apply too (the others were loaded by
+        // the queries above), so that no apply call loads code lazily
+        cudaFuncAttributes fa;
+        e = cudaFuncGetAttributes(&fa, pending_kernel);
+    }
     if (e != cudaSuccess) return cuda_error(e, "apply kernel configuration");
     if (kc->snappy_blocks_per_sm < 1) kc->snappy_blocks_per_sm = 1;
     if (kc->apply_blocks_per_sm < 1) kc->apply_blocks_per_sm = 1;
@@ -1224,26 +1231,72 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocBytes];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_noalloc_mu;
-void* g_noalloc_ptr[kMaxDevices] = {};
+struct NoallocAddr {
+    unsigned long long ctx;   // unique id of the context the address belongs to (0: unknown)
+    void* ptr;
+};
+NoallocAddr g_noalloc[kMaxDevices] = {};
 
-// Device address of this device's copy of the array, looked up once per
-// device with that device current.  The lookup may load the module, so the
-// first call on each device should come before any stream capture.
+// Unique id of the calling thread's current CUDA context, or 0 if the
+// driver cannot tell.  The two driver calls are looked up through the
+// runtime, so the library does not link the driver library itself.
+unsigned long long current_ctx_id()
+{
+    using GetCur = CUresult (*)(CUcontext*);
+    using GetId = CUresult (*)(CUcontext, unsigned long long*);
+    static GetCur get_cur = nullptr;
+    static GetId get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_cur = reinterpret_cast<GetCur>(f);
+        f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<GetId>(f);
+    });
+    CUcontext c = nullptr;
+    unsigned long long id = 0;
+    if (!get_cur || !get_id || get_cur(&c) != CUDA_SUCCESS || !c || get_id(c, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
+
+// Device address of this device's copy of the array, looked up with that
+// device current and kept with the id of the context it was found in: a
+// new context (after cudaDeviceReset, or a released primary context) gets
+// the address looked up again instead of a stale one.  The lookup may load
+// the module, which allocates; dcr_recv_state_create does it once so that
+// dcr_apply_noalloc itself does not.
 int noalloc_scratch(int dev, void** out)
 {
     if (dev < 0 || dev >= kMaxDevices) return set_error(DCR_ERR_INVALID, "device %d out of range", dev);
+    const unsigned long long ctx = current_ctx_id();
     std::lock_guard<std::mutex> g(g_noalloc_mu);
-    if (!g_noalloc_ptr[dev]) {
+    NoallocAddr& a = g_noalloc[dev];
+    if (!a.ptr || ctx == 0 || a.ctx != ctx) {
         void* ptr = nullptr;
         const cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
         if (e != cudaSuccess) return cuda_error(e, "cudaGetSymbolAddress of the static apply scratch");
-        g_noalloc_ptr[dev] = ptr;
+        a.ptr = ptr;
+        a.ctx = ctx;
     }
-    *out = g_noalloc_ptr[dev];
+    *out = a.ptr;
     return DCR_OK;
 }
 
 }  // namespace
+
+int noalloc_prepare()
+{
+    int dev = -1;
+    const cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_error(e, "cudaGetDevice");
+    void* ptr = nullptr;
+    return noalloc_scratch(dev, &ptr);
+}
 
 int apply_launch_noalloc(const dcr_plan* P, dcr_recv_state* st, const void* payload, size_t size,
                          void* target, ApplyScratch** sc_out, cudaStream_t s)

@@ -48,13 +48,10 @@ struct ChunkDesc {
 };
 constexpr uint32_t kResidualFlag = 1u << 8;
 
-// Look-back record of one chunk of the window being encoded:
-// bits 62-63 status (1 aggregate, 2 inclusive prefix), bits 40-61 frame
-// count, bits 0-39 frame bytes.  Sums of both fields stay in range for a
-// window of at most 256 GiB (2^22 chunks, < 2^40 frame bytes).
-constexpr uint64_t kLbAgg = 1ull << 62;
-constexpr uint64_t kLbInc = 2ull << 62;
-constexpr uint64_t kLbValMask = (1ull << 62) - 1;
+// Frame offset record of one chunk of the window being encoded (written by
+// the frame-size scan): bits 40-63 frames before it, bits 0-39 frame bytes
+// before it.  Both fields stay in range for a window of at most 256 GiB
+// (2^22 chunks, < 2^40 frame bytes).
 constexpr int kLbFrameShift = 40;
 constexpr uint64_t kLbByteMask = (1ull << kLbFrameShift) - 1;
 constexpr uint64_t kMaxWindowBytes = 256ull << 30;
@@ -149,6 +146,9 @@ int encode_result(const struct ::dcr_plan* plan, const void* head, size_t cap, s
 int apply_result(struct ::dcr_recv_state* st, const ApplyScratch& a, dcr_apply_result* result);
 
 void pipe_release(const struct ::dcr_plan* plan);
+// looks up dcr_apply_noalloc's static scratch for the current device and
+// context (loading its module), so that the call itself allocates nothing
+int noalloc_prepare();
 
 int set_error(int code, const char* fmt, ...);
 int cuda_error(cudaError_t e, const char* what);

@@ -6,9 +6,9 @@
 // Per 64 KiB canonical chunk the encoder gathers old and new through the
 // plan's shard->canonical pieces, forms mask = old XOR new, counts changed
 // stored values, encodes the chunk (LZ4 block, raw mask, overwrite records or
-// dense overwrite) and writes the frame straight to its final place in the
-// stream, found by a decoupled look-back over the frame sizes of earlier
-// chunks.
+// dense overwrite) and writes the frame to a slot of its own; once every
+// frame size is known a scan places the frames in chunk order and a copy pass
+// moves them into the stream.
 //
 // Method: "GPU-accelerated weight teleportation", "Delta update algebra"
 // (mask = old XOR new on raw bits) and "A strong baseline with the

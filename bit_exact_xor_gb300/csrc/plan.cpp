@@ -365,8 +365,8 @@ extern "C" int dcr_plan_build(const dcr_tensor_desc* tensors, size_t n, const dc
         delete P;
         return rc;
     }
-    // encode scratch: head = EncScratch + per-tensor counts, then look-back,
-    // sizes, the spill list and the spill kernel's share of it
+    // encode scratch: head = EncScratch + per-tensor counts, then frame
+    // offsets, sizes, the spill list and the spill kernel's share of it
     P->enc_head_bytes = (sizeof(EncScratch) + 8 * n + 255) / 256 * 256;
     size_t lb_bytes = (P->max_window_chunks * 8 + 255) / 256 * 256;
     size_t fs_bytes = (P->max_window_chunks * 4 + 255) / 256 * 256;
@@ -453,6 +453,10 @@ extern "C" int dcr_recv_state_create(const dcr_plan* p, uint64_t version, dcr_re
         (e = cudaMallocHost(&s->h_scratch, sizeof(ApplyScratch))) != cudaSuccess) {
         dcr_recv_state_destroy(s);
         return cuda_error(e, "allocating receiver state");
+    }
+    if (int rc = noalloc_prepare()) {
+        dcr_recv_state_destroy(s);
+        return rc;
     }
     *out = s;
     return DCR_OK;

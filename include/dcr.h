@@ -28,7 +28,7 @@
  *     dcr_apply_retry end with one small device-to-host status read and a
  *     synchronisation of `stream`, so their outputs (sizes, counts, status,
  *     version) are final when they return.
- *   - A plan's scratch (look-back state, counters) and a receiver state's
+ *   - A plan's scratch (frame slots, counters) and a receiver state's
  *     scratch are shared by every call that uses them: calls on one plan, or
  *     on one receiver state, must not overlap in time.
  *
@@ -259,9 +259,15 @@ int dcr_apply_retry(const dcr_plan* plan, dcr_recv_state* state, const void* pay
  *     plans with larger windows get DCR_ERR_CAPACITY before anything runs.
  *   - The counters are cleared by a memset on `stream` at the start of each
  *     call; nothing has to be zeroed by the caller.
- *   - The first call on each device looks up the array's device address
- *     (once, with that device current); make that first call before any
- *     stream capture.
+ *   - dcr_recv_state_create looks up the array's device address on the
+ *     current device (loading the library's apply code there if it is not
+ *     loaded yet, which may allocate), and dcr_plan_build loads the apply
+ *     kernels: a dcr_apply_noalloc call after those loads no code and
+ *     allocates nothing.  The address is kept with the CUDA context it was
+ *     found in; under a new context (after cudaDeviceReset, or a released
+ *     and re-created primary context) the next call looks it up again, which
+ *     may load code then: create the plan and receiver state again after a
+ *     reset.  Do that set-up before any stream capture.
  *   - The static scratch is shared by every call on a device, whatever the
  *     plan or receiver state: calls on one device must not overlap in time
  *     (concurrent calls race on the counters). */

@@ -23,8 +23,19 @@
  *        Blackwell-native DE" (LZ4 block format, CPU-prepared apply plan) and
  *        "Working with low-precision RL" (layout remap of gate/up rows paired
  *        in groups of 64).
- * Readings where the pages are silent (chunking, wire format, greedy match
- * finder, window rule) are listed in the repository's design notes.
+ * Where the pages are silent this file takes the plainest reading:
+ *   - chunks are 64 KiB of each canonical tensor's own row-major bytes and
+ *     never straddle tensors (the last one of a tensor may be short);
+ *   - a changed stored value is an element of the stored width (bf16 word,
+ *     e4m3 byte, e2m1 nibble, low nibble first) whose bits differ;
+ *   - the LZ4 encoder is a plain greedy one: a 2^14-slot table of the latest
+ *     position per multiplicative hash of the 4-byte little-endian word,
+ *     every position inserted, matches extended forward only;
+ *   - windows pack whole tensors in order up to the window size, and a
+ *     tensor larger than a window is cut at chunk boundaries;
+ *   - the wire format (stream header, 16-byte-aligned frames with 32-byte
+ *     headers in ascending chunk order, a trailing index of frame offsets)
+ *     is the library's, restated here from its description.
  */
 #include <pthread.h>
 #include <stdatomic.h>

@@ -241,6 +241,35 @@ def subset(wl, indices):
     return Workload(wl.name + "-subset", wl.seed, wl.tp, ts, window_bytes=1 << 40).layout()
 
 
+def sample(wl, budget_bytes):
+    """A bounded sample of wl with identical bytes (the same generator
+    streams): wl itself if it fits the budget; else its leading tensors up to
+    the budget (at least one, row-group pairs kept whole); a single tensor
+    larger than the budget keeps its leading rows (replicated tensors only:
+    their generator counts elements from the tensor's start).  Returns
+    (workload, description)."""
+    if wl.canonical_bytes <= budget_bytes:
+        return wl, "the whole workload"
+    if len(wl.tensors) == 1:
+        t = wl.tensors[0]
+        assert t.split == REPLICATED, "row sampling needs a replicated tensor"
+        rows = max(1, min(t.rows, budget_bytes // (t.cols * t.elem_bits // 8)))
+        s = subset(wl, [0])
+        s.tensors[0].rows = rows
+        s.layout()
+        return s, "the leading %d of %d rows of %s (%.2f GiB)" % (rows, t.rows, t.name, s.canonical_bytes / 2**30)
+    idx, tot = [], 0
+    for i, t in enumerate(wl.tensors):
+        paired = t.recv_layout == RECV_ROWGROUP and t.recv_slot == 1
+        if idx and tot + t.nbytes > budget_bytes and not paired:
+            break
+        idx.append(i)
+        tot += t.nbytes
+    s = subset(wl, idx)
+    return s, "the first %d of %d tensors (%s .. %s, %.2f GiB)" % (
+        len(idx), len(wl.tensors), wl.tensors[idx[0]].name, wl.tensors[idx[-1]].name, s.canonical_bytes / 2**30)
+
+
 def first_chunks(wl):
     """Global id of the first chunk of every tensor (plan order)."""
     out, c = [], 0

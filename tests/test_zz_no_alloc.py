@@ -62,3 +62,31 @@ def test_noalloc_rejects_windows_beyond_its_limit():
     assert rc == dcr.ERR_CAPACITY
     assert "static scratch limit" in dcr.last_error()
     assert st.version == 0 and bool((t == 7).all())
+
+
+def test_noalloc_after_state_creation_allocates_no_device_memory():
+    # the receiver state's creation looks up the static scratch and the plan
+    # build loads the apply kernels, so the first dcr_apply_noalloc call (and
+    # every later one) leaves the device's free memory exactly as it was
+    wl = configs.mini(2)
+    olds, news = wl.host_arenas()
+    plan = dcr.Plan(descs_of(wl), window_bytes=wl.window_bytes)
+    d_old, d_new = to_device(olds), to_device(news)
+    tgt = _target(plan, wl, d_old)
+    st = dcr.RecvState(plan, 0)
+    pls = []
+    for v, (a, b) in enumerate([(d_old, d_new), (d_new, d_old)]):
+        pl = torch.zeros(plan.window(0).payload_bound, dtype=torch.uint8, device="cuda")
+        rc, size, _ = dcr.encode(plan, a, b, pl, base_version=v, target_version=v + 1)
+        dcr.check(rc)
+        pls.append((pl, size))
+    torch.cuda.synchronize()
+    for pl, size in pls:
+        free0 = torch.cuda.mem_get_info()[0]
+        rc, res = dcr.apply_noalloc(plan, st, pl, size, tgt)
+        torch.cuda.synchronize()
+        free1 = torch.cuda.mem_get_info()[0]
+        assert rc == dcr.OK, dcr.last_error()
+        assert free1 == free0, "dcr_apply_noalloc changed the device's free memory by %d bytes" % (free0 - free1)
+    assert st.version == 2
+    assert np.array_equal(tgt.cpu().numpy()[:wl.recv_bytes], oracle.Oracle(wl).receiver_dense(olds)[:wl.recv_bytes])
