@@ -15,7 +15,7 @@ per refit) are larger than L2; workloads small enough to stay in L2 get a
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
                   [--workload moe|dense|single|gqa|sweep] [--frac F]
                   [--moe-layers L] [--window-mb M] [--codec lz4|snappy]
-                  [--pipeline] [--abort-retry] [--no-e2e] [--no-cpu-baseline]
+                  [--pipeline] [--abort-retry] [--shard] [--no-e2e] [--no-cpu-baseline]
 
 Prints one JSON line.  --impl reference times the CPU oracle (the
 benchmark's reference arm) on the same workload: each of its steps refits a
@@ -213,14 +213,16 @@ def oracle_runner(wl, threads, codec="lz4"):
 
     def step():
         a, b = (olds, news) if state["dir"] == 0 else (news, olds)
+        total = 0
         for w in range(orc.n_windows):
             pl, _ = orc.encode(a, b, window=w, base_version=state["v"], target_version=state["v"] + 1,
                                threads=threads, codec=oc)
             rc = orc.apply(state["st"], pl, tgt, threads=threads)
             assert rc == oracle.OK, rc
+            total += pl.size
         state["v"] += 1
         state["dir"] ^= 1
-        return pl.size
+        return total
 
     return step
 
@@ -248,7 +250,8 @@ def cpu_baseline(wl, budget_s=12.0, codec="lz4"):
     dt = time.perf_counter() - t0
     out = {"value": round(swl.canonical_bytes * n / dt / 1e9, 4), "unit": UNIT, "cores": threads,
            "kind": "oracle", "sample": "%d full refit steps (encode+apply) of %s, %.1f s" % (n, what, dt),
-           "payload_bytes": payload, "sample_bytes": swl.canonical_bytes}
+           "payload_bytes": payload, "sample_bytes": swl.canonical_bytes, "sample_workload": swl,
+           "sample_what": what}
     # the same oracle on one thread, for one step, when that stays bounded
     est = dt / n * threads
     if threads == 1:
@@ -477,8 +480,22 @@ def run_gpu(args):
         t1.record(stream)
         torch.cuda.synchronize()
         ems = dist_max(t0.elapsed_time(t1), ws)
+        per_step_h2d, per_step_d2h = h2d // k, d2h // k
+        # the host link on its own: the same input copies with nothing else
+        # running, timed on the copy stream (context for the e2e figure)
+        torch.cuda.synchronize()
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        c0.record(cs)
+        for i in range(2):
+            copy_inputs(i & 1, i & 1)
+        c1.record(cs)
+        torch.cuda.synchronize()
+        link = 2 * sum(x.numel() for x in h_old + h_new) / (c0.elapsed_time(c1) / 1e3) / 1e9
         e2e = {"value": round(N * k * ws / (ems / 1e3) / 1e9, 3), "unit": UNIT,
-               "h2d_bytes_per_step": h2d // k, "d2h_bytes_per_step": d2h // k}
+               "h2d_bytes_per_step": per_step_h2d, "d2h_bytes_per_step": per_step_d2h,
+               "host_link_h2d_gbs": round(link, 1),
+               "link_bound_value": round(N / ((per_step_h2d + per_step_d2h) / (link * 1e9)) / 1e9, 3)}
+        del h_old, h_new, d_in
 
     # pipelined refit of every window through pinned host memory
     # (dcr_refit_pipelined) against the same windows in series: encode, copy
@@ -586,11 +603,64 @@ def run_gpu(args):
                  "retry_payload_bytes_per_refit": int(rlast["bytes"])}
         del rpay
 
+    # ownership-sharded encode: rank r encodes part r of every window on its
+    # GPU, the compressed parts are gathered to rank 0 (all-gather of sizes,
+    # gather of the frames), which applies the assembled stream
+    shard = None
+    if args.shard:
+        from wl import descs_of as _descs
+        import torch.distributed as dist
+        if ws == 1 and not dist.is_initialized():
+            os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+            os.environ.setdefault("MASTER_PORT", "29512")
+            dist.init_process_group("nccl", rank=0, world_size=1, device_id=dev)
+        splan = dcr.Plan(_descs(wl), window_bytes=(args.window_mb << 20) or wl.window_bytes,
+                         codec=dcr.CODEC_SNAPPY if args.codec == "snappy" else dcr.CODEC_LZ4)
+        slast = {}
+
+        def sharded_refit():
+            a, b = (olds, news) if d[0] == 0 else (news, olds)
+            pbytes = 0
+            for w in range(nw):
+                rc, sz, _ = dcr.encode_part(splan, a, b, rank, ws, window=w, counts=False, stream=sh)
+                dcr.check(rc)
+
+                def write(fo, fr, ix):
+                    dcr.check(dcr.encode_part_write(splan, fo, fr, fr.numel(), ix, stream=sh))
+
+                out = dcr.gather_stream(splan, w, rank, ws, sz, write, ver[0], ver[0] + 1, device=dev)
+                if rank == 0:
+                    rc, _ = dcr.apply(plan, st, out, out.numel(), target, stream=sh)
+                    dcr.check(rc)
+                    pbytes += out.numel()
+            ver[0] += 1
+            d[0] ^= 1
+            slast["payload"] = pbytes
+
+        k = max(2, min(args.steps, 5))
+        for _ in range(2):
+            sharded_refit()
+        torch.cuda.synchronize()
+        dist_barrier(ws)
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        for _ in range(k):
+            sharded_refit()
+        s1.record(stream)
+        torch.cuda.synchronize()
+        sms = dist_max(s0.elapsed_time(s1) / k, ws)
+        shard = {"parts": ws, "ms_per_refit": round(sms, 4), "value": round(N / (sms / 1e3) / 1e9, 3),
+                 "unit": UNIT, "payload_bytes_per_refit": int(slast["payload"]) if rank == 0 else None,
+                 "exchange": "all-gather of part sizes, gather of compressed parts to rank 0 (torch.distributed)"}
+        splan.close()
+
     # the receiver really holds the last step's target weights
-    ref = torch.empty_like(target)
-    dcr.check(dcr.dense_refit(plan, olds if d[0] == 0 else news, ref))
-    assert torch.equal(ref, target), "receiver arena differs from a dense refit"
-    del ref
+    # (with --shard only rank 0 applied the sharded refits)
+    if not (shard and rank != 0):
+        ref = torch.empty_like(target)
+        dcr.check(dcr.dense_refit(plan, olds if d[0] == 0 else news, ref))
+        assert torch.equal(ref, target), "receiver arena differs from a dense refit"
+        del ref
 
     P = statistics.mean(sizes)
     peak, peak_kind = measured_peak()
@@ -626,14 +696,34 @@ def run_gpu(args):
         line["pipelined"] = pipe
     if retry:
         line["abort_retry"] = retry
+    if shard:
+        line["sharded"] = shard
     if rank == 0 and not args.no_cpu_baseline:
         cb = cpu_baseline(wl, codec=args.codec)
-        line["payload_vs_oracle"] = round(P / cb.pop("payload_bytes"), 4)
+        # payload against the oracle's on identical bytes: the GPU encodes the
+        # oracle's sample too (one refit, old -> new)
+        swl = cb.pop("sample_workload")
+        if swl is wl:
+            gpu_sample_payload = P * nw
+        else:
+            splan = dcr.Plan(descs_of(swl), window_bytes=swl.window_bytes,
+                             codec=dcr.CODEC_SNAPPY if args.codec == "snappy" else dcr.CODEC_LZ4)
+            so, sn = swl.device_arenas(torch)
+            gpu_sample_payload = 0
+            for w in range(splan.n_windows):
+                buf = torch.empty(splan.window(w).payload_bound, dtype=torch.uint8, device=dev)
+                rc, size, _ = dcr.encode(splan, so, sn, buf, window=w, counts=False)
+                dcr.check(rc)
+                gpu_sample_payload += size
+            del so, sn, buf
+            splan.close()
+        line["payload_vs_oracle"] = round(gpu_sample_payload / cb.pop("payload_bytes"), 4)
+        line["payload_vs_oracle_on"] = "the oracle's sample: " + cb.pop("sample_what")
         line["cpu_baseline"] = cb
     if rank == 0:
         print(json.dumps(line))
-    if ws > 1:
-        import torch.distributed as dist
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
         dist.destroy_process_group()
     return 0
 
@@ -655,6 +745,9 @@ def main():
                     help="also time refits aborted at half the frames and completed by the overwrite-only retry")
     ap.add_argument("--pipeline", action="store_true",
                     help="also time dcr_refit_pipelined against the same windows in series")
+    ap.add_argument("--shard", action="store_true",
+                    help="also time the ownership-sharded encode: each rank encodes its part of every window, "
+                         "the compressed parts are gathered to rank 0, which applies them")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -27,6 +27,8 @@ LAYOUT_CANONICAL, LAYOUT_ROWGROUP_INTERLEAVE = 0, 1
 MODE_HYBRID, MODE_OVERWRITE_ONLY = 0, 1
 ENCODER_AUTO, ENCODER_WIDE, ENCODER_DEEP = 0, 1, 2
 CODEC_LZ4, CODEC_SNAPPY = 0, 1
+PLAN_HOST_ONLY = 1
+MAX_PARTS = 65536
 
 
 class DcrError(RuntimeError):
@@ -50,7 +52,17 @@ class TensorDesc(ctypes.Structure):
 
 class PlanOpts(ctypes.Structure):
     _fields_ = [("window_bytes", ctypes.c_uint64), ("encoder", ctypes.c_uint32), ("codec", ctypes.c_uint32),
-                ("reserved", ctypes.c_uint32 * 4)]
+                ("flags", ctypes.c_uint32), ("reserved", ctypes.c_uint32 * 3)]
+
+
+class PartInfo(ctypes.Structure):
+    _fields_ = [("chunk_begin", ctypes.c_uint64), ("chunk_count", ctypes.c_uint64),
+                ("canonical_bytes", ctypes.c_uint64), ("shard_mask", ctypes.c_uint32),
+                ("reserved", ctypes.c_uint32)]
+
+
+class PartSize(ctypes.Structure):
+    _fields_ = [("frame_bytes", ctypes.c_uint64), ("n_frames", ctypes.c_uint64)]
 
 
 class PlanInfo(ctypes.Structure):
@@ -95,7 +107,8 @@ EXPORTS = ["dcr_last_error", "dcr_plan_build", "dcr_plan_info_get", "dcr_window_
            "dcr_plan_destroy", "dcr_recv_state_create", "dcr_recv_state_destroy",
            "dcr_recv_state_version", "dcr_encode", "dcr_apply", "dcr_apply_retry",
            "dcr_dense_refit", "dcr_plan_set_profiling", "dcr_plan_last_profile", "dcr_apply_noalloc",
-           "dcr_pipeline_sizes", "dcr_refit_pipelined"]
+           "dcr_pipeline_sizes", "dcr_refit_pipelined", "dcr_part_info_get", "dcr_encode_part",
+           "dcr_encode_part_write", "dcr_stream_layout", "dcr_stream_header"]
 
 _lib = None
 
@@ -128,6 +141,11 @@ def lib():
         L.dcr_pipeline_sizes.argtypes = [VP, P(SZ), P(SZ)]
         L.dcr_refit_pipelined.argtypes = [VP, VP, U32, P(VP), P(VP), U64, U64, VP, VP, SZ, VP, SZ, P(U64),
                                           P(PipelineStats), VP]
+        L.dcr_part_info_get.argtypes = [VP, U32, U32, U32, P(PartInfo)]
+        L.dcr_encode_part.argtypes = [VP, U32, U32, U32, U32, P(VP), P(VP), P(PartSize), P(U64), VP]
+        L.dcr_encode_part_write.argtypes = [VP, U64, VP, SZ, VP, VP]
+        L.dcr_stream_layout.argtypes = [U32, P(PartSize), P(U64), P(U64), P(U64)]
+        L.dcr_stream_header.argtypes = [VP, U32, U32, U64, U64, U64, U64, VP]
         _lib = L
     return _lib
 
@@ -169,10 +187,10 @@ def check(rc):
 class Plan:
     """dcr_plan_build over a list of TensorDesc."""
 
-    def __init__(self, descs, window_bytes=0, encoder=0, codec=0):
+    def __init__(self, descs, window_bytes=0, encoder=0, codec=0, host_only=False):
         arr = (TensorDesc * len(descs))(*descs)
         self._names = [d.name for d in descs]
-        opts = PlanOpts(window_bytes, encoder, codec)
+        opts = PlanOpts(window_bytes, encoder, codec, PLAN_HOST_ONLY if host_only else 0)
         h = ctypes.c_void_p()
         check(lib().dcr_plan_build(arr, len(descs), ctypes.byref(opts), ctypes.byref(h)))
         self.h = h
@@ -187,6 +205,12 @@ class Plan:
         wi = WindowInfo()
         check(lib().dcr_window_info_get(self.h, w, ctypes.byref(wi)))
         return wi
+
+    def part(self, window, part, n_parts):
+        """dcr_part_info_get (host only)."""
+        pi = PartInfo()
+        check(lib().dcr_part_info_get(self.h, window, part, n_parts, ctypes.byref(pi)))
+        return pi
 
     def set_profiling(self, on=True):
         check(lib().dcr_plan_set_profiling(self.h, int(on)))
@@ -285,6 +309,83 @@ def refit_pipelined(plan, state, olds, news, target, device_buf, host_buf, mode=
                                    target_version, _ptr(target), _ptr(device_buf), device_buf.numel(),
                                    _ptr(host_buf), host_buf.numel(), cnt, ctypes.byref(st), _stream(stream))
     return rc, st, (list(cnt) if counts else None)
+
+
+def encode_part(plan, olds, news, part, n_parts, window=0, mode=MODE_HYBRID, counts=True, stream=None):
+    """dcr_encode_part.  Returns (status, (frame_bytes, n_frames), per-tensor changed counts)."""
+    size = PartSize()
+    n = plan.info.n_tensors
+    cnt = (ctypes.c_uint64 * n)() if counts else None
+    rc = lib().dcr_encode_part(plan.h, mode, window, part, n_parts, _ptr_array(olds), _ptr_array(news),
+                               ctypes.byref(size), cnt, _stream(stream))
+    return rc, (size.frame_bytes, size.n_frames), (list(cnt) if counts else None)
+
+
+def encode_part_write(plan, frame_offset, frames, frames_cap, index, stream=None):
+    """dcr_encode_part_write: frames / index are device tensors or raw device addresses."""
+    return lib().dcr_encode_part_write(plan.h, frame_offset, _ptr(frames), frames_cap, _ptr(index),
+                                       _stream(stream))
+
+
+def stream_layout(sizes):
+    """dcr_stream_layout over [(frame_bytes, n_frames), ...] in part order.
+    Returns (frame_offsets, index_offsets, total)."""
+    n = len(sizes)
+    arr = (PartSize * n)(*[PartSize(int(f), int(k)) for f, k in sizes])
+    fo, io, tot = (ctypes.c_uint64 * n)(), (ctypes.c_uint64 * n)(), ctypes.c_uint64()
+    check(lib().dcr_stream_layout(n, arr, fo, io, ctypes.byref(tot)))
+    return list(fo), list(io), tot.value
+
+
+def stream_header(plan, window, base_version, target_version, n_frames, frame_bytes, mode=MODE_HYBRID):
+    """dcr_stream_header: the 64 header bytes (host)."""
+    buf = (ctypes.c_uint8 * 64)()
+    check(lib().dcr_stream_header(plan.h, mode, window, base_version, target_version, n_frames, frame_bytes,
+                                  buf))
+    return bytes(buf)
+
+
+def gather_stream(plan, window, part, n_parts, size, write, base_version=0, target_version=1,
+                  mode=MODE_HYBRID, group=None, dst=0, device="cpu"):
+    """The exchange step of the ownership-sharded encode, one call per rank.
+
+    Every rank owns part `part` (its rank in `group`) of `n_parts` parts of
+    the window and has sized it: `size` = (frame_bytes, n_frames), as
+    encode_part returns.  The ranks all-gather their sizes, take the stream
+    layout from dcr_stream_layout, and each rank calls
+    write(frame_offset, frames, index) to fill a staging tensor with its
+    frames and index entries (on the GPU: encode_part_write).  The staging
+    tensors are gathered to rank `dst`, which places them and the header
+    (dcr_stream_header) into the window's stream.  Returns the stream (a
+    uint8 tensor on `device`) on `dst`, None on the other ranks.  Only
+    compressed frames cross between ranks."""
+    import torch
+    import torch.distributed as dist
+    ws = dist.get_world_size(group)
+    assert ws == n_parts and 0 <= part < n_parts
+    mine = torch.tensor([int(size[0]), int(size[1])], dtype=torch.int64, device=device)
+    allsz = [torch.empty_like(mine) for _ in range(ws)]
+    dist.all_gather(allsz, mine, group=group)
+    sizes = [(int(t[0]), int(t[1])) for t in allsz]
+    fo, io, total = stream_layout(sizes)
+    blob_bytes = [f + 8 * k for f, k in sizes]
+    cap = max(max(blob_bytes), 16)
+    blob = torch.zeros(cap, dtype=torch.uint8, device=device)
+    fb, nf = sizes[part]
+    write(fo[part], blob[:fb], blob[fb:fb + 8 * nf])
+    rank = dist.get_rank(group) if group is not None else dist.get_rank()
+    blobs = [torch.empty_like(blob) for _ in range(ws)] if rank == dst else None
+    dist.gather(blob, blobs, dst=dst, group=group)
+    if rank != dst:
+        return None
+    fbytes, nframes = sum(f for f, _ in sizes), sum(k for _, k in sizes)
+    out = torch.empty(total, dtype=torch.uint8, device=device)
+    hdr = stream_header(plan, window, base_version, target_version, nframes, fbytes, mode)
+    out[:64] = torch.frombuffer(bytearray(hdr), dtype=torch.uint8).to(device)
+    for q, (f, k) in enumerate(sizes):
+        out[fo[q]:fo[q] + f] = blobs[q][:f]
+        out[io[q]:io[q] + 8 * k] = blobs[q][f:f + 8 * k]
+    return out
 
 
 def dense_refit(plan, shards, target, stream=None):

@@ -132,6 +132,14 @@ struct KernelConfig {
 int encode_launch(const struct ::dcr_plan* plan, uint32_t mode, uint32_t window,
                   const void* const* olds, const void* const* news, uint64_t base_version,
                   uint64_t target_version, void* payload, size_t cap, cudaStream_t s);
+// the two passes of one encode over a chunk range, for ownership-sharded
+// encodes: sizing (frames into slots, sizes scanned) and writing (frames to
+// `frames`, index entries frame_base + offset to `index`)
+int encode_size_launch(const struct ::dcr_plan* plan, uint32_t mode, uint64_t chunk_begin, uint64_t chunk_count,
+                       const void* const* olds, const void* const* news, cudaStream_t s);
+int encode_write_launch(const struct ::dcr_plan* plan, uint32_t mode, uint64_t chunk_begin, uint64_t chunk_count,
+                        const void* const* olds, const void* const* news, uint8_t* frames, uint64_t frame_base,
+                        uint64_t* index, cudaStream_t s);
 int encode_kernel_config(KernelConfig* kc);
 int apply_kernel_config(KernelConfig* kc);
 int apply_launch(const struct ::dcr_plan* plan, struct ::dcr_recv_state* st, const void* payload,
@@ -161,6 +169,9 @@ struct dcr_plan {
     std::vector<dcr::Part> parts;
     std::vector<dcr::ChunkDesc> chunks;
     std::vector<uint64_t> win_start;  // n_windows + 1 chunk ids
+    std::vector<uint64_t> chunk_start;   // canonical byte offset of each chunk in the model (+ total)
+    std::vector<uint32_t> chunk_shards;  // per chunk: bit r set iff it reads trainer shard r
+    bool host_only = false;              // built with DCR_PLAN_HOST_ONLY: no device state
     uint64_t window_bytes = 0;
     uint32_t encoder = DCR_ENCODER_AUTO;
     uint32_t codec = DCR_CODEC_LZ4;
@@ -193,6 +204,14 @@ struct dcr_plan {
     cudaEvent_t ev[8] = {};
     mutable dcr_profile prof = {};
     mutable bool prof_encode_due = false, prof_apply_due = false;   // events recorded, durations not read
+    // ownership-sharded encode: the part sized by the last dcr_encode_part
+    struct {
+        bool valid = false;
+        uint32_t mode = 0, window = 0;
+        uint64_t chunk_begin = 0, chunk_count = 0, frame_bytes = 0, n_frames = 0;
+        const void* olds[DCR_MAX_TP] = {};
+        const void* news[DCR_MAX_TP] = {};
+    } mutable part;
     // dcr_refit_pipelined: its copy stream and events (created on first use)
     mutable cudaStream_t pipe_copy = nullptr;
     mutable cudaEvent_t pipe_ev[8] = {};

@@ -103,8 +103,12 @@ struct EncArgs {
     const uint8_t* news[DCR_MAX_TP];
     uint32_t chunk_begin, chunk_count;
     uint32_t mode;
-    uint8_t* payload;
+    uint8_t* payload;          // the stream (header written by scan_kernel when `header`), or null
     uint64_t cap;
+    uint8_t* frames;           // where frame bytes go: frame at relative offset o -> frames + o
+    uint64_t frame_base;       // index entry of that frame: frame_base + o
+    uint64_t* index;           // the frames' index entries (null: at the end of `payload`)
+    uint32_t header;
     EncScratch* sc;
     unsigned long long* counts;
     uint64_t* lb;              // frame offsets: frames before << 40 | bytes before
@@ -985,7 +989,7 @@ __device__ __forceinline__ void restream_chunk(const EncArgs& A, WarpSmem& W, ui
     const Seg* segs = cached ? W.segs : A.src + cd.src_begin;
     const bool vec = (cd.flags & kSrcVec) != 0;
     const uint32_t ub = cd.bits == 16 ? 2u : 1u;
-    uint8_t* f = A.payload + kStreamHdr + (A.lb[R.k] & kLbByteMask);
+    uint8_t* f = A.frames + (A.lb[R.k] & kLbByteMask);
     uint8_t* body = f + kFrameHdr;
     const uint32_t nu = R.n_units;
     const uint32_t voff = 4 + 2 * nu + (4 - (2 * nu) % 4) % 4;
@@ -1110,7 +1114,7 @@ __global__ void __launch_bounds__(1024) scan_kernel(EncArgs A, uint64_t plan_has
         const uint64_t total = kStreamHdr + fbytes + 8 * nframes;
         A.sc->total = total;
         A.sc->n_frames = nframes;
-        if (total <= A.cap && !*(volatile int32_t*)&A.sc->err) {
+        if (A.header && total <= A.cap && !*(volatile int32_t*)&A.sc->err) {
             uint32_t h[16];
             h[0] = kStreamMagic;
             h[1] = kFormat;
@@ -1140,18 +1144,18 @@ __global__ void copy_kernel(EncArgs A)
 {
     const uint64_t total = A.sc->total, nframes = A.sc->n_frames;
     if (total > A.cap || *(volatile int32_t*)&A.sc->err) return;
-    uint64_t* index = reinterpret_cast<uint64_t*>(A.payload + total - 8 * nframes);
+    uint64_t* index = A.index ? A.index : reinterpret_cast<uint64_t*>(A.payload + total - 8 * nframes);
     const int lane = threadIdx.x & 31;
     const uint32_t nw = gridDim.x * (blockDim.x >> 5);
     for (uint32_t k = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); k < A.chunk_count; k += nw) {
         const uint32_t fs = A.fsize[k];
         if (!(fs & ~kSpilled)) continue;
         const uint64_t ex = A.lb[k];
-        const uint64_t foff = kStreamHdr + (ex & kLbByteMask);
-        if (lane == 0) index[ex >> kLbFrameShift] = foff;
+        const uint64_t rel = ex & kLbByteMask;
+        if (lane == 0) index[ex >> kLbFrameShift] = A.frame_base + rel;
         if (fs & kSpilled) continue;
         const uint4* __restrict__ src = reinterpret_cast<const uint4*>(A.slots + size_t(k) * kEncSlot);
-        uint4* __restrict__ dst = reinterpret_cast<uint4*>(A.payload + foff);
+        uint4* __restrict__ dst = reinterpret_cast<uint4*>(A.frames + rel);
         const uint32_t nv = fs / 16;
         for (uint32_t i0 = lane; i0 < nv; i0 += 128) {   // four loads in flight per lane
             uint4 v[4];
@@ -1309,7 +1313,6 @@ __global__ void __launch_bounds__(kSThreads, 2) spill_kernel(EncArgs A)
     if (A.sc->total > A.cap) return;          // final: written by scan_kernel
     for (uint32_t i = blockIdx.x; i < n_deep; i += gridDim.x) {
         const SpillRec R = A.spill[A.deep[i]];
-        const uint64_t foff = kStreamHdr + (A.lb[R.k] & kLbByteMask);
         const ChunkDesc cd = A.chunks[A.chunk_begin + R.k];
         if (warp == 0) {
             if (lane == 0) B.meta.cd = cd;
@@ -1322,7 +1325,7 @@ __global__ void __launch_bounds__(kSThreads, 2) spill_kernel(EncArgs A)
         __syncthreads();
         const int raw = int(cd.raw_len);
         const uint8_t* bytes = reinterpret_cast<const uint8_t*>(B.data);
-        uint8_t* f = A.payload + foff;
+        uint8_t* f = A.frames + (A.lb[R.k] & kLbByteMask);
         uint8_t* body = f + kFrameHdr;
         const uint32_t fsz = (kFrameHdr + R.body_len + 15) / 16 * 16;
         if (threadIdx.x == 0) write_header(f, R.kind, cd.bits, A.chunk_begin + R.k, uint32_t(raw), R.body_len, R.changed);
@@ -1394,9 +1397,10 @@ int encode_kernel_config(KernelConfig* kc)
     return DCR_OK;
 }
 
-int encode_launch(const dcr_plan* P, uint32_t mode, uint32_t window, const void* const* olds,
-                  const void* const* news, uint64_t base_v, uint64_t target_v, void* payload,
-                  size_t cap, cudaStream_t s)
+namespace {
+
+EncArgs make_args(const dcr_plan* P, uint32_t mode, uint64_t chunk_begin, uint64_t chunk_count,
+                  const void* const* olds, const void* const* news)
 {
     EncArgs A{};
     A.chunks = P->d_chunks;
@@ -1405,11 +1409,9 @@ int encode_launch(const dcr_plan* P, uint32_t mode, uint32_t window, const void*
         A.olds[r] = static_cast<const uint8_t*>(olds[r]);
         A.news[r] = static_cast<const uint8_t*>(news[r]);
     }
-    A.chunk_begin = uint32_t(P->win_start[window]);
-    A.chunk_count = uint32_t(P->win_start[window + 1] - P->win_start[window]);
+    A.chunk_begin = uint32_t(chunk_begin);
+    A.chunk_count = uint32_t(chunk_count);
     A.mode = mode;
-    A.payload = static_cast<uint8_t*>(payload);
-    A.cap = payload ? cap : 0;
     A.sc = static_cast<EncScratch*>(P->d_enc);
     A.counts = reinterpret_cast<unsigned long long*>(static_cast<char*>(P->d_enc) + sizeof(EncScratch));
     A.lb = P->d_lb;
@@ -1417,12 +1419,25 @@ int encode_launch(const dcr_plan* P, uint32_t mode, uint32_t window, const void*
     A.spill = P->d_spill;
     A.deep = P->d_deep;
     A.slots = P->d_slots;
+    return A;
+}
+
+// grid of the main encoder pass
+unsigned main_grid(const dcr_plan* P) { return unsigned(P->kc.num_sms * P->kc.enc_blocks_per_sm); }
+
+// The sizing pass: every chunk encoded into its slot (or sized and listed
+// for the write pass), frame sizes scanned into offsets.  With a payload the
+// scan also writes the stream header when the stream fits.
+int launch_size(const dcr_plan* P, EncArgs& A, uint64_t plan_hash, uint64_t base_v, uint64_t target_v,
+                uint32_t window, cudaStream_t s)
+{
     // ticket, error, totals, spill count and per-tensor counts start at zero
     cudaError_t e = cudaMemsetAsync(P->d_enc, 0, P->enc_head_bytes, s);
     if (e != cudaSuccess) return cuda_error(e, "encode scratch reset");
-    const unsigned warps = unsigned(P->kc.num_sms * P->kc.enc_blocks_per_sm * kMWarps);
-    unsigned grid = unsigned(P->kc.num_sms * P->kc.enc_blocks_per_sm);
+    const unsigned warps = unsigned(main_grid(P) * kMWarps);
+    unsigned grid = main_grid(P);
     if (warps > A.chunk_count) grid = (A.chunk_count + kMWarps - 1) / kMWarps;
+    if (grid == 0) grid = 1;
     // a window of few chunks leaves most warp slots empty: then one chunk per
     // warp of the deep variant, spread over all SMs, is faster
     const unsigned deep_warps = unsigned(P->kc.num_sms * P->kc.enc_deep_blocks_per_sm * kDeepWarps);
@@ -1441,24 +1456,75 @@ int encode_launch(const dcr_plan* P, uint32_t mode, uint32_t window, const void*
     else
         encode_kernel<kNS, CodecLz4><<<grid, kMThreads, kMainSmem, s>>>(A);
     if (P->profiling) cudaEventRecord(P->ev[1], s);
-    scan_kernel<<<1, 1024, 0, s>>>(A, P->hash, base_v, target_v, window);
+    scan_kernel<<<1, 1024, 0, s>>>(A, plan_hash, base_v, target_v, window);
+    e = cudaGetLastError();
+    return e == cudaSuccess ? DCR_OK : cuda_error(e, "encode launch");
+}
+
+// The write pass: slot frames copied to their places, index entries written,
+// outgrown bodies re-derived into place.
+int launch_write(const dcr_plan* P, EncArgs& A, cudaStream_t s)
+{
+    // the write pass's own tickets start at zero (it may run more than once
+    // after one sizing pass)
+    cudaError_t e = cudaMemsetAsync(&A.sc->spill_ticket, 0, 2 * sizeof(uint32_t), s);
+    if (e != cudaSuccess) return cuda_error(e, "encode scratch reset");
     unsigned cgrid = (A.chunk_count + 7) / 8;
     if (cgrid > unsigned(P->kc.num_sms * 8)) cgrid = unsigned(P->kc.num_sms * 8);
+    if (cgrid == 0) cgrid = 1;
     copy_kernel<<<cgrid, 256, 0, s>>>(A);
     unsigned rgrid = unsigned(P->kc.num_sms * P->kc.restream_blocks_per_sm);
-    if (rgrid > grid) rgrid = grid;
+    const unsigned mg = (A.chunk_count + kMWarps - 1) / kMWarps;
+    if (rgrid > mg) rgrid = mg ? mg : 1;
     const unsigned sgrid = unsigned(P->kc.num_sms * P->kc.spill_blocks_per_sm);
-    if (snappy) {
+    if (P->codec == DCR_CODEC_SNAPPY) {
         restream_kernel<CodecSnappy><<<rgrid, kMThreads, kMainSmem, s>>>(A);
         spill_kernel<CodecSnappy><<<sgrid, kSThreads, sizeof(Buf), s>>>(A);
     } else {
         restream_kernel<CodecLz4><<<rgrid, kMThreads, kMainSmem, s>>>(A);
         spill_kernel<CodecLz4><<<sgrid, kSThreads, sizeof(Buf), s>>>(A);
     }
-    if (P->profiling) cudaEventRecord(P->ev[2], s);
     e = cudaGetLastError();
-    if (e != cudaSuccess) return cuda_error(e, "encode launch");
-    return DCR_OK;
+    return e == cudaSuccess ? DCR_OK : cuda_error(e, "encode launch");
+}
+
+}  // namespace
+
+int encode_launch(const dcr_plan* P, uint32_t mode, uint32_t window, const void* const* olds,
+                  const void* const* news, uint64_t base_v, uint64_t target_v, void* payload,
+                  size_t cap, cudaStream_t s)
+{
+    EncArgs A = make_args(P, mode, P->win_start[window], P->win_start[window + 1] - P->win_start[window], olds, news);
+    A.payload = static_cast<uint8_t*>(payload);
+    A.cap = payload ? cap : 0;
+    A.frames = A.payload ? A.payload + kStreamHdr : nullptr;
+    A.frame_base = kStreamHdr;
+    A.index = nullptr;
+    A.header = 1;
+    int rc = launch_size(P, A, P->hash, base_v, target_v, window, s);
+    if (rc == DCR_OK) rc = launch_write(P, A, s);
+    if (P->profiling) cudaEventRecord(P->ev[2], s);
+    return rc;
+}
+
+int encode_size_launch(const dcr_plan* P, uint32_t mode, uint64_t chunk_begin, uint64_t chunk_count,
+                       const void* const* olds, const void* const* news, cudaStream_t s)
+{
+    EncArgs A = make_args(P, mode, chunk_begin, chunk_count, olds, news);
+    A.cap = 0;   // no stream: only sizes and offsets
+    return launch_size(P, A, P->hash, 0, 0, 0, s);
+}
+
+int encode_write_launch(const dcr_plan* P, uint32_t mode, uint64_t chunk_begin, uint64_t chunk_count,
+                        const void* const* olds, const void* const* news, uint8_t* frames, uint64_t frame_base,
+                        uint64_t* index, cudaStream_t s)
+{
+    EncArgs A = make_args(P, mode, chunk_begin, chunk_count, olds, news);
+    A.cap = ~0ull;   // the caller checked the frames buffer against the sized frame bytes
+    A.frames = frames;
+    A.frame_base = frame_base;
+    A.index = index;
+    return launch_write(P, A, s);
 }
 
 }  // namespace dcr

@@ -118,6 +118,8 @@ extern "C" int dcr_refit_pipelined(const dcr_plan* p, dcr_recv_state* st, uint32
         return set_error(DCR_ERR_INVALID, "dcr_refit_pipelined: NULL argument");
     if (st->plan != p) return set_error(DCR_ERR_INVALID, "dcr_refit_pipelined: state belongs to another plan");
     if (mode > DCR_MODE_OVERWRITE_ONLY) return set_error(DCR_ERR_INVALID, "dcr_refit_pipelined: bad mode");
+    if (p->host_only) return set_error(DCR_ERR_INVALID, "dcr_refit_pipelined: host-only plan");
+    p->part.valid = false;   // the plan's scratch now holds these encodes
     const Layout L = layout_of(p);
     if (device_bytes < L.dev_bytes || host_bytes < L.host_bytes)
         return set_error(DCR_ERR_INVALID, "dcr_refit_pipelined: buffers too small (need %zu device, %zu host bytes)",

@@ -8,6 +8,7 @@
 // low-precision RL": the mask is remapped like the weights' physical layout)
 // together with the fixed shard -> canonical maps of the NeMo-DCR paper
 // summary ("Direct Projection", "Residual Conversion").
+#include <algorithm>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -221,9 +222,12 @@ extern "C" int dcr_plan_build(const dcr_tensor_desc* tensors, size_t n, const dc
     if (encoder > DCR_ENCODER_DEEP) return set_error(DCR_ERR_INVALID, "unknown encoder variant %u", encoder);
     const uint32_t codec = opts ? opts->codec : uint32_t(DCR_CODEC_LZ4);
     if (codec > DCR_CODEC_SNAPPY) return set_error(DCR_ERR_INVALID, "unknown codec %u", codec);
+    const uint32_t flags = opts ? opts->flags : 0u;
+    if (flags & ~uint32_t(DCR_PLAN_HOST_ONLY)) return set_error(DCR_ERR_INVALID, "unknown plan flags %#x", flags);
     dcr_plan* P = new (std::nothrow) dcr_plan();
     if (!P) return set_error(DCR_ERR_NOMEM, "dcr_plan_build: out of host memory");
     P->window_bytes = W;
+    P->host_only = (flags & DCR_PLAN_HOST_ONLY) != 0;
     P->encoder = encoder;
     P->codec = codec;
     P->tp = tensors[0].tp;
@@ -323,6 +327,8 @@ extern "C" int dcr_plan_build(const dcr_tensor_desc* tensors, size_t n, const dc
     // chunk table with sender and receiver segments
     std::vector<Seg> src, dst;
     P->chunks.resize(chunks);
+    P->chunk_start.resize(chunks + 1);
+    P->chunk_shards.resize(chunks);
     for (const Part& q : P->parts) {
         const dcr_tensor_desc& d = P->descs[q.desc];
         for (uint64_t c = 0; c < q.nchunks; ++c) {
@@ -340,11 +346,14 @@ extern "C" int dcr_plan_build(const dcr_tensor_desc* tensors, size_t n, const dc
             cd.tensor = q.desc;
             cd.bits = q.bits;
             cd.flags = (sv ? kSrcVec : 0u) | (dv ? kDstVec : 0u) | (q.residual ? kResidualFlag : 0u);
+            uint32_t mask = 0;
             for (uint32_t k = cd.src_begin; k < cd.src_begin + cd.src_count; ++k) {
                 uint32_t r = uint32_t(src[k].addr >> kShardShift);
                 uint64_t e = (src[k].addr & kAddrMask) + src[k].len;
                 if (e > P->shard_bytes[r]) P->shard_bytes[r] = e;
+                mask |= 1u << r;
             }
+            P->chunk_shards[q.chunk0 + c] = mask;
             for (uint32_t k = cd.dst_begin; k < cd.dst_begin + cd.dst_count; ++k)
                 if (dst[k].addr + dst[k].len > P->recv_bytes) P->recv_bytes = dst[k].addr + dst[k].len;
         }
@@ -355,6 +364,11 @@ extern "C" int dcr_plan_build(const dcr_tensor_desc* tensors, size_t n, const dc
     }
     P->n_src = src.size();
     P->n_dst = dst.size();
+    for (uint64_t c = 0; c < chunks; ++c) P->chunk_start[c + 1] = P->chunk_start[c] + P->chunks[c].raw_len;
+    if (P->host_only) {   // layout, windows, hash and parts only: nothing on a device
+        *out = P;
+        return DCR_OK;
+    }
 
     cudaError_t e = cudaGetDevice(&P->device);
     if (e != cudaSuccess) { delete P; return cuda_error(e, "cudaGetDevice"); }
@@ -428,6 +442,10 @@ extern "C" int dcr_window_info_get(const dcr_plan* p, uint32_t w, dcr_window_inf
 extern "C" void dcr_plan_destroy(dcr_plan* p)
 {
     if (!p) return;
+    if (p->host_only) {
+        delete p;
+        return;
+    }
     int cur = -1;
     cudaGetDevice(&cur);
     if (cur != p->device) cudaSetDevice(p->device);
@@ -440,6 +458,7 @@ extern "C" int dcr_recv_state_create(const dcr_plan* p, uint64_t version, dcr_re
 {
     if (!p || !out) return set_error(DCR_ERR_INVALID, "dcr_recv_state_create: NULL argument");
     *out = nullptr;
+    if (p->host_only) return set_error(DCR_ERR_INVALID, "dcr_recv_state_create: host-only plan");
     dcr_recv_state* s = new (std::nothrow) dcr_recv_state();
     if (!s) return set_error(DCR_ERR_NOMEM, "dcr_recv_state_create: out of host memory");
     s->plan = p;
@@ -489,6 +508,8 @@ extern "C" int dcr_encode(const dcr_plan* p, uint32_t mode, uint32_t window,
     if (!p || !olds || !news || !payload_size)
         return set_error(DCR_ERR_INVALID, "dcr_encode: NULL argument");
     if (mode > DCR_MODE_OVERWRITE_ONLY) return set_error(DCR_ERR_INVALID, "dcr_encode: bad mode");
+    if (p->host_only) return set_error(DCR_ERR_INVALID, "dcr_encode: host-only plan");
+    p->part.valid = false;   // the plan's scratch now holds this encode
     if (window + 1 >= p->win_start.size())
         return set_error(DCR_ERR_INVALID, "dcr_encode: window %u out of range", window);
     if (payload && !aligned16(payload)) return set_error(DCR_ERR_INVALID, "payload not 16-byte aligned");
@@ -572,6 +593,7 @@ static int apply_common(const dcr_plan* p, dcr_recv_state* st, const void* paylo
     if (result) memset(result, 0, sizeof(*result));
     if (!p || !st || !payload || !target) return set_error(DCR_ERR_INVALID, "dcr_apply: NULL argument");
     if (st->plan != p) return set_error(DCR_ERR_INVALID, "dcr_apply: state belongs to another plan");
+    if (p->host_only) return set_error(DCR_ERR_INVALID, "dcr_apply: host-only plan");
     if (size < kStreamHdr) return set_error(DCR_ERR_CORRUPT, "dcr_apply: stream shorter than its header");
     if (!aligned16(payload) || !aligned16(target))
         return set_error(DCR_ERR_INVALID, "dcr_apply: payload/target not 16-byte aligned");
@@ -606,6 +628,7 @@ extern "C" int dcr_apply_retry(const dcr_plan* p, dcr_recv_state* st, const void
 extern "C" int dcr_plan_set_profiling(dcr_plan* p, int on)
 {
     if (!p) return set_error(DCR_ERR_INVALID, "dcr_plan_set_profiling: NULL plan");
+    if (p->host_only) return set_error(DCR_ERR_INVALID, "dcr_plan_set_profiling: host-only plan");
     if (on && !p->ev[0]) {
         for (cudaEvent_t& e : p->ev) {
             cudaError_t r = cudaEventCreate(&e);
@@ -640,9 +663,179 @@ extern "C" int dcr_plan_last_profile(const dcr_plan* p, dcr_profile* out)
 extern "C" int dcr_dense_refit(const dcr_plan* p, const void* const* shards, void* target, void* stream)
 {
     if (!p || !shards || !target) return set_error(DCR_ERR_INVALID, "dcr_dense_refit: NULL argument");
+    if (p->host_only) return set_error(DCR_ERR_INVALID, "dcr_dense_refit: host-only plan");
     if (!aligned16(target)) return set_error(DCR_ERR_INVALID, "dcr_dense_refit: target not aligned");
     for (uint32_t r = 0; r < p->tp; ++r)
         if (p->shard_bytes[r] && (!shards[r] || !aligned16(shards[r])))
             return set_error(DCR_ERR_INVALID, "dcr_dense_refit: shard %u arena NULL or unaligned", r);
     return dense_launch(p, shards, target, static_cast<cudaStream_t>(stream));
+}
+
+// ---- ownership-sharded encode ----------------------------------------------
+// (blog, "A strong baseline with the Blackwell-native DE": weight ownership
+// is remapped so that the trainer ranks together cover the checkpoint
+// exactly once, each rank compresses what it owns, and only the rank-local
+// compressed payloads are gathered.)
+
+namespace {
+
+// Part `part` of `n_parts` of window w: the chunks whose first canonical
+// byte falls in [part, part + 1) * B / n_parts, B = the window's bytes.
+void part_range(const dcr_plan* p, uint32_t w, uint32_t part, uint32_t n_parts, uint64_t* begin, uint64_t* count)
+{
+    const uint64_t c0 = p->win_start[w], c1 = p->win_start[w + 1];
+    const uint64_t s0 = p->chunk_start[c0], B = p->chunk_start[c1] - s0;
+    auto first_at = [&](uint64_t q) {   // first chunk of the window starting at or after byte q
+        const uint64_t t = s0 + (unsigned __int128)B * q / n_parts;
+        return uint64_t(std::lower_bound(p->chunk_start.begin() + c0, p->chunk_start.begin() + c1, t) -
+                        p->chunk_start.begin());
+    };
+    const uint64_t a = first_at(part), b = first_at(uint64_t(part) + 1);
+    *begin = a;
+    *count = b - a;
+}
+
+int part_args(const dcr_plan* p, uint32_t window, uint32_t part, uint32_t n_parts, const char* who)
+{
+    if (!p) return set_error(DCR_ERR_INVALID, "%s: NULL plan", who);
+    if (window + 1 >= p->win_start.size()) return set_error(DCR_ERR_INVALID, "%s: window %u out of range", who, window);
+    if (n_parts == 0 || n_parts > DCR_MAX_PARTS || part >= n_parts)
+        return set_error(DCR_ERR_INVALID, "%s: part %u of %u (at most %u parts)", who, part, n_parts,
+                         unsigned(DCR_MAX_PARTS));
+    return DCR_OK;
+}
+
+}  // namespace
+
+extern "C" int dcr_part_info_get(const dcr_plan* p, uint32_t window, uint32_t part, uint32_t n_parts,
+                                 dcr_part_info* out)
+{
+    if (int rc = part_args(p, window, part, n_parts, "dcr_part_info_get")) return rc;
+    if (!out) return set_error(DCR_ERR_INVALID, "dcr_part_info_get: NULL argument");
+    memset(out, 0, sizeof(*out));
+    part_range(p, window, part, n_parts, &out->chunk_begin, &out->chunk_count);
+    out->canonical_bytes = p->chunk_start[out->chunk_begin + out->chunk_count] - p->chunk_start[out->chunk_begin];
+    for (uint64_t c = out->chunk_begin; c < out->chunk_begin + out->chunk_count; ++c)
+        out->shard_mask |= p->chunk_shards[c];
+    return DCR_OK;
+}
+
+extern "C" int dcr_encode_part(const dcr_plan* p, uint32_t mode, uint32_t window, uint32_t part, uint32_t n_parts,
+                               const void* const* olds, const void* const* news, dcr_part_size* size,
+                               uint64_t* changed_per_tensor, void* stream)
+{
+    if (int rc = part_args(p, window, part, n_parts, "dcr_encode_part")) return rc;
+    if (!olds || !news || !size) return set_error(DCR_ERR_INVALID, "dcr_encode_part: NULL argument");
+    memset(size, 0, sizeof(*size));
+    if (mode > DCR_MODE_OVERWRITE_ONLY) return set_error(DCR_ERR_INVALID, "dcr_encode_part: bad mode");
+    if (p->host_only) return set_error(DCR_ERR_INVALID, "dcr_encode_part: host-only plan");
+    p->part.valid = false;
+    uint64_t cb, cc;
+    part_range(p, window, part, n_parts, &cb, &cc);
+    uint32_t need = 0;
+    for (uint64_t c = cb; c < cb + cc; ++c) need |= p->chunk_shards[c];
+    for (uint32_t r = 0; r < p->tp; ++r) {
+        if ((need >> r & 1) && (!olds[r] || !news[r]))
+            return set_error(DCR_ERR_INVALID, "dcr_encode_part: part %u reads shard %u, whose arena is NULL", part, r);
+        if ((olds[r] && !aligned16(olds[r])) || (news[r] && !aligned16(news[r])))
+            return set_error(DCR_ERR_INVALID, "dcr_encode_part: shard %u arena not 16-byte aligned", r);
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int rc = encode_size_launch(p, mode, cb, cc, olds, news, s);
+    if (rc) return rc;
+    cudaError_t e = cudaMemcpyAsync(p->h_enc, p->d_enc, p->enc_head_bytes, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_error(e, "dcr_encode_part status read");
+    const EncScratch* hs = static_cast<const EncScratch*>(p->h_enc);
+    if (changed_per_tensor)
+        memcpy(changed_per_tensor, static_cast<const char*>(p->h_enc) + sizeof(EncScratch), p->descs.size() * 8);
+    if (hs->err) return set_error(hs->err, "dcr_encode_part: device error %d", hs->err);
+    size->n_frames = hs->n_frames;
+    size->frame_bytes = hs->total - kStreamHdr - 8 * hs->n_frames;
+    p->part.valid = true;
+    p->part.mode = mode;
+    p->part.window = window;
+    p->part.chunk_begin = cb;
+    p->part.chunk_count = cc;
+    p->part.frame_bytes = size->frame_bytes;
+    p->part.n_frames = size->n_frames;
+    for (uint32_t r = 0; r < DCR_MAX_TP; ++r) {
+        p->part.olds[r] = r < p->tp ? olds[r] : nullptr;
+        p->part.news[r] = r < p->tp ? news[r] : nullptr;
+    }
+    return DCR_OK;
+}
+
+extern "C" int dcr_encode_part_write(const dcr_plan* p, uint64_t frame_offset, void* frames, size_t frames_cap,
+                                     void* index, void* stream)
+{
+    if (!p) return set_error(DCR_ERR_INVALID, "dcr_encode_part_write: NULL plan");
+    if (!p->part.valid)
+        return set_error(DCR_ERR_INVALID, "dcr_encode_part_write: no part sized by dcr_encode_part on this plan");
+    if ((p->part.frame_bytes && !frames) || (p->part.n_frames && !index))
+        return set_error(DCR_ERR_INVALID, "dcr_encode_part_write: NULL buffer");
+    if (frames_cap < p->part.frame_bytes)
+        return set_error(DCR_ERR_CAPACITY, "dcr_encode_part_write: frames need %llu bytes, capacity %zu",
+                         (unsigned long long)p->part.frame_bytes, frames_cap);
+    if ((frames && !aligned16(frames)) || (reinterpret_cast<uintptr_t>(index) & 7) || frame_offset % 16)
+        return set_error(DCR_ERR_INVALID, "dcr_encode_part_write: frames / frame_offset not 16-byte aligned, "
+                                          "or index not 8-byte aligned");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int rc = encode_write_launch(p, p->part.mode, p->part.chunk_begin, p->part.chunk_count, p->part.olds,
+                                 p->part.news, static_cast<uint8_t*>(frames), frame_offset,
+                                 static_cast<uint64_t*>(index), s);
+    if (rc) return rc;
+    cudaError_t e = cudaMemcpyAsync(p->h_enc, p->d_enc, p->enc_head_bytes, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_error(e, "dcr_encode_part_write status read");
+    const EncScratch* hs = static_cast<const EncScratch*>(p->h_enc);
+    if (hs->err) return set_error(hs->err, "dcr_encode_part_write: device error %d", hs->err);
+    return DCR_OK;
+}
+
+extern "C" int dcr_stream_layout(uint32_t n_parts, const dcr_part_size* sizes, uint64_t* frame_offsets,
+                                 uint64_t* index_offsets, uint64_t* total)
+{
+    if (n_parts == 0 || n_parts > DCR_MAX_PARTS || !sizes || !frame_offsets || !index_offsets || !total)
+        return set_error(DCR_ERR_INVALID, "dcr_stream_layout: bad arguments");
+    uint64_t F = 0, NF = 0;
+    for (uint32_t q = 0; q < n_parts; ++q) {
+        if (sizes[q].frame_bytes % 16) return set_error(DCR_ERR_INVALID, "dcr_stream_layout: part %u frame bytes "
+                                                                          "not a multiple of 16", q);
+        frame_offsets[q] = kStreamHdr + F;
+        F += sizes[q].frame_bytes;
+        NF += sizes[q].n_frames;
+    }
+    uint64_t idx = kStreamHdr + F;
+    for (uint32_t q = 0; q < n_parts; ++q) {
+        index_offsets[q] = idx;
+        idx += 8 * sizes[q].n_frames;
+    }
+    *total = idx;
+    return DCR_OK;
+}
+
+extern "C" int dcr_stream_header(const dcr_plan* p, uint32_t mode, uint32_t window, uint64_t base_version,
+                                 uint64_t target_version, uint64_t n_frames, uint64_t frame_bytes, void* header)
+{
+    if (!p || !header) return set_error(DCR_ERR_INVALID, "dcr_stream_header: NULL argument");
+    if (mode > DCR_MODE_OVERWRITE_ONLY) return set_error(DCR_ERR_INVALID, "dcr_stream_header: bad mode");
+    if (window + 1 >= p->win_start.size())
+        return set_error(DCR_ERR_INVALID, "dcr_stream_header: window %u out of range", window);
+    if (frame_bytes % 16) return set_error(DCR_ERR_INVALID, "dcr_stream_header: frame bytes not a multiple of 16");
+    uint8_t* h = static_cast<uint8_t*>(header);
+    auto put32 = [&](int at, uint32_t v) { for (int i = 0; i < 4; ++i) h[at + i] = uint8_t(v >> (8 * i)); };
+    auto put64 = [&](int at, uint64_t v) { put32(at, uint32_t(v)); put32(at + 4, uint32_t(v >> 32)); };
+    put32(0, kStreamMagic);
+    put32(4, kFormat);
+    put64(8, p->hash);
+    put64(16, base_version);
+    put64(24, target_version);
+    put32(32, window);
+    put32(36, mode == DCR_MODE_OVERWRITE_ONLY ? kStreamOverwriteOnly : 0u);
+    put32(40, uint32_t(p->win_start[window]));
+    put32(44, uint32_t(p->win_start[window + 1] - p->win_start[window]));
+    put64(48, n_frames);
+    put64(56, kStreamHdr + frame_bytes + 8 * n_frames);
+    return DCR_OK;
 }

@@ -131,13 +131,21 @@ typedef struct {
     uint64_t recv_offset;
 } dcr_tensor_desc;
 
+/* dcr_plan_opts.flags.  HOST_ONLY: build the layout, windows, plan hash and
+ * ownership parts on the host only, with no CUDA call (a plan for
+ * dcr_plan_info_get, dcr_window_info_get, dcr_part_info_get and
+ * dcr_stream_header, e.g. on a rank or process without a GPU); every call
+ * that runs kernels returns DCR_ERR_INVALID for it. */
+#define DCR_PLAN_HOST_ONLY 1u
+
 typedef struct {
     uint64_t window_bytes;   /* 0 = 16 GiB.  Windows pack whole tensors in
                                 order; a tensor larger than a window is cut at
                                 chunk boundaries.  At most 256 GiB. */
     uint32_t encoder;        /* DCR_ENCODER_AUTO (0), _WIDE or _DEEP */
     uint32_t codec;          /* DCR_CODEC_LZ4 (0) or DCR_CODEC_SNAPPY */
-    uint32_t reserved[4];
+    uint32_t flags;          /* 0 or DCR_PLAN_HOST_ONLY */
+    uint32_t reserved[3];
 } dcr_plan_opts;
 
 typedef struct {
@@ -307,6 +315,80 @@ int dcr_refit_pipelined(const dcr_plan* plan, dcr_recv_state* state, uint32_t mo
                         uint64_t base_version, uint64_t target_version, void* target,
                         void* device_buf, size_t device_bytes, void* host_buf, size_t host_bytes,
                         uint64_t* changed_per_tensor, dcr_pipeline_stats* stats, void* stream);
+
+/* Ownership-sharded encode (blog, "A strong baseline with the
+ * Blackwell-native DE": weight ownership is remapped so that the trainer
+ * ranks together cover the whole checkpoint exactly once, every rank
+ * compresses the part it owns on its own GPU, and only the rank-local
+ * compressed payloads are gathered).  A window's chunks are split into
+ * n_parts contiguous ranges: part q holds the chunks whose first canonical
+ * byte falls in [q, q + 1) * B / n_parts of the window's B bytes, so the
+ * parts cover the window exactly once, in chunk order (a part may be empty).
+ * The stream the parts make is the one dcr_encode writes for the window,
+ * byte for byte:
+ *   header (64 B) | frames of part 0 | ... | frames of part n-1 |
+ *   index entries of part 0 | ... | index entries of part n-1.
+ * Per rank: dcr_encode_part (sizes), an exchange of every part's
+ * dcr_part_size (a gather of 16 bytes per rank), dcr_stream_layout (the
+ * offsets), dcr_encode_part_write (this part's frames and index entries at
+ * those offsets, into a buffer that is then gathered into the stream, or
+ * into the stream itself), and dcr_stream_header by the rank that assembles
+ * the stream.  No kernel reads another GPU's memory; the exchange is the
+ * caller's collective.  At most DCR_MAX_PARTS parts. */
+#define DCR_MAX_PARTS 65536u
+typedef struct {
+    uint64_t chunk_begin, chunk_count;  /* global chunk ids of the part */
+    uint64_t canonical_bytes;           /* weight bytes the part encodes */
+    uint32_t shard_mask;                /* bit r set: the part reads trainer shard r */
+    uint32_t reserved;
+} dcr_part_info;
+typedef struct {
+    uint64_t frame_bytes;   /* bytes of the part's frames (a multiple of 16) */
+    uint64_t n_frames;      /* its frames, i.e. its index entries */
+} dcr_part_size;
+
+/* Host only (no CUDA call): the chunk range of part `part` of `n_parts` of
+ * window `window`, its bytes and the trainer shards it reads.
+ * Errors: DCR_ERR_INVALID. */
+int dcr_part_info_get(const dcr_plan* plan, uint32_t window, uint32_t part, uint32_t n_parts,
+                      dcr_part_info* out);
+
+/* Sizing pass of one part: the same gather, XOR, counts and encode as
+ * dcr_encode, over the part's chunks only, into the plan's scratch.
+ * old_shards / new_shards as in dcr_encode; only the shards in the part's
+ * shard_mask are read (the others may be NULL).  *size gets the part's
+ * frame bytes and frame count, changed_per_tensor (host, nullable) its
+ * changed counts.  The plan remembers the part (and the shard pointers)
+ * until the next encode on it: keep the arenas unchanged until
+ * dcr_encode_part_write.  Errors as dcr_encode (no DCR_ERR_CAPACITY). */
+int dcr_encode_part(const dcr_plan* plan, uint32_t mode, uint32_t window, uint32_t part, uint32_t n_parts,
+                    const void* const* old_shards, const void* const* new_shards, dcr_part_size* size,
+                    uint64_t* changed_per_tensor, void* stream);
+
+/* Write pass of the part sized last on this plan: its frames to `frames`
+ * (device, 16-byte aligned, frames_cap bytes; the frame at offset o of the
+ * part lands at frames + o) and its n_frames index entries, the stream
+ * offsets frame_offset + o, to `index` (device, 8-byte aligned).
+ * frame_offset is where `frames` sits in the stream (dcr_stream_layout's
+ * frame_offsets[part]); `frames` may point there in the stream itself, or
+ * into a staging buffer that the caller gathers into it.  May be called
+ * again for the same part.  Errors: DCR_ERR_INVALID (no part sized,
+ * alignment), DCR_ERR_CAPACITY (frames_cap < frame_bytes), DCR_ERR_CORRUPT,
+ * DCR_ERR_CUDA. */
+int dcr_encode_part_write(const dcr_plan* plan, uint64_t frame_offset, void* frames, size_t frames_cap,
+                          void* index, void* stream);
+
+/* Host only: where each part's frames and index entries go in the window's
+ * stream (byte offsets from the stream start), from every part's size in
+ * part order, and the stream's total size.  Errors: DCR_ERR_INVALID. */
+int dcr_stream_layout(uint32_t n_parts, const dcr_part_size* sizes, uint64_t* frame_offsets,
+                      uint64_t* index_offsets, uint64_t* total);
+
+/* Host only: the 64-byte stream header of window `window` (host memory) for
+ * a stream of n_frames frames taking frame_bytes bytes, the sums over all
+ * parts.  Errors: DCR_ERR_INVALID. */
+int dcr_stream_header(const dcr_plan* plan, uint32_t mode, uint32_t window, uint64_t base_version,
+                      uint64_t target_version, uint64_t n_frames, uint64_t frame_bytes, void* header);
 
 /* Kernel timing (tracing aid).  When on, the library records CUDA events on
  * the caller's stream around each of its kernels; dcr_plan_last_profile

@@ -238,7 +238,7 @@ def subset(wl, indices):
         if t.recv_layout == RECV_ROWGROUP:
             t.recv_offset = ("fused", wl.tensors[i].recv_offset)
         ts.append(t)
-    return Workload(wl.name + "-subset", wl.seed, wl.tp, ts, window_bytes=1 << 40).layout()
+    return Workload(wl.name + "-subset", wl.seed, wl.tp, ts, window_bytes=256 << 30).layout()
 
 
 def sample(wl, budget_bytes):
