@@ -358,6 +358,8 @@ def run_gpu(args):
     ver = [0]
     d = [0]
     enc_ms, app_ms, rest_ms, sizes, changed = [], [], [], [], []
+    parts_ms = {"encode_kernel": [], "encode_write_pass": [], "apply_first_kernel": [], "apply_deferred_kernels": [],
+                "commit_check": []}
 
     sh = stream.cuda_stream
 
@@ -374,6 +376,8 @@ def run_gpu(args):
                 enc_ms.append(p.encode_ms)
                 app_ms.append(p.apply_ms + p.defer_ms)
                 rest_ms.append(p.finalize_ms + p.pending_ms)
+                for k, v in zip(parts_ms, (p.encode_ms, p.finalize_ms, p.apply_ms, p.defer_ms, p.pending_ms)):
+                    parts_ms[k].append(v)
                 sizes.append(size)
             if counts:
                 changed.append(sum(cnt))
@@ -680,6 +684,10 @@ def run_gpu(args):
         # the rest of the library's GPU time per window: frame scan, copy and
         # spill kernels after the encode, commit check after the apply
         "other_kernels_ms": round(statistics.mean(rest_ms), 4),
+        # per window, by launch group: the encoder's main kernel; its scan,
+        # copy and second-pass kernels; the first apply kernel; the deferred
+        # frame kernels; the commit check
+        "kernel_ms_by_group": {k: round(statistics.mean(v), 4) for k, v in parts_ms.items()},
         # apply against the dense byte model (reads N + P, writes N)
         "apply_model_frac": round((2 * N / nw + P) / (statistics.mean(app_ms) / 1e3) / 1e9 / peak, 4),
         "payload_bytes": int(P), "changed_values": int(statistics.mean(changed)) if changed else None,

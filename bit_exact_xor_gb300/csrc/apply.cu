@@ -745,6 +745,396 @@ __global__ void __launch_bounds__(kAThreads) apply_kernel(ApplyArgs A)
     }
 }
 
+// ---- small windows: one CTA per frame ------------------------------------
+// apply_cta_kernel (256 threads): for windows with fewer frames than the GPU has warp
+// slots, where one warp per frame would leave the run as long as one frame's
+// serial token walk.  The CTA copies a ZSRC LZ4 body of up to kCBody bytes
+// into shared memory, works out where a sequence starting at each body byte
+// would end, builds 4- and 16-sequence jump tables by pointer doubling, and
+// one thread follows the chain 16 sequences per step; the threads then
+// expand the starts, decode one sequence each, place them by a prefix sum of
+// their lengths, list the non-zero literal bytes in output order and check
+// every match against that list (ZSRC: a match copies zero bytes only).
+// Only a frame that passed every check is applied, its non-zero bytes XORed
+// into the receiver spread evenly over the threads.  Other frames are
+// applied CTA-wide (raw, overwrite, dense) or listed for the deferred
+// kernels, as apply_kernel does.
+constexpr int kCThreads = 256;
+constexpr int kCWarps = kCThreads / 32;
+constexpr uint32_t kCBody = 4096;               // body bytes walked in shared memory
+constexpr uint32_t kCSeq = kCBody / 3 + 2;      // sequences such a body holds at most
+constexpr uint16_t kCBad = 0xFFFF;              // no valid sequence starts here
+
+struct __align__(16) CSmem {
+    uint8_t body[kCBody + 16];
+    uint16_t nxt[kCBody + 1];     // where the next sequence starts (n: the block ends here)
+    uint16_t j4[kCBody + 1];      // ... four sequences on
+    uint16_t j16[kCBody + 1];     // ... sixteen sequences on
+    uint16_t start[kCSeq];        // every sequence's start
+    uint16_t blk[kCSeq / 16 + 2]; // every sixteenth sequence's start
+    uint32_t opos[kCSeq];         // output position of each sequence's literals
+    uint16_t nz[kCBody];          // output positions of the non-zero literal bytes, ascending
+    uint8_t nzv[kCBody];          // ... and their values
+    unsigned long long wsum[kCWarps];
+    Hdr hdr;
+    uint32_t f, nseq;
+    int ok;
+};
+
+// exclusive prefix sum of v over the CTA (two 32-bit counts packed in one
+// 64-bit value); *total = the sum (every thread)
+__device__ __forceinline__ unsigned long long cta_excl_scan(unsigned long long v, unsigned long long* wsum,
+                                                            unsigned long long* total)
+{
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    unsigned long long incl = v;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const unsigned long long o = __shfl_up_sync(kFull, incl, d);
+        if (lane >= d) incl += o;
+    }
+    if (lane == 31) wsum[w] = incl;
+    __syncthreads();
+    unsigned long long before = 0, tot = 0;
+#pragma unroll
+    for (int i = 0; i < kCWarps; ++i) {
+        const unsigned long long x = wsum[i];
+        before += i < w ? x : 0ull;
+        tot += x;
+    }
+    __syncthreads();   // wsum is reused by the next scan
+    *total = tot;
+    return before + incl - v;
+}
+
+// The ZSRC LZ4 block body[0, n) (in S.body) applied to the chunk's receiver
+// bytes below lim: 1 if applied, 0 if malformed or breaking the ZSRC promise
+// (nothing written then).  Called by the whole CTA.
+__device__ int zsrc_apply_cta(const ApplyArgs& A, const ChunkDesc& cd, const Seg* ds, uint32_t n, uint32_t raw,
+                              uint32_t lim, CSmem& S)
+{
+    const int t = threadIdx.x;
+    if (n == 0) return 0;   // an LZ4 block holds at least one token
+    // where a sequence starting at each byte ends (n: the block's last
+    // sequence; the end position n is absorbing)
+    for (uint32_t p = t; p <= n; p += kCThreads) {
+        uint16_t v = uint16_t(n);
+        if (p < n) {
+            const uint32_t e = seq_end(S.body, n, p);
+            v = e == kEndBad ? kCBad : (e & kEndFinal) ? uint16_t(n) : e >= n ? kCBad : uint16_t(e);
+        }
+        S.nxt[p] = v;
+    }
+    __syncthreads();
+    auto four = [&](const uint16_t* a, uint16_t* out) {   // out = a applied four times
+        for (uint32_t p = t; p <= n; p += kCThreads) {
+            uint16_t q = uint16_t(p);
+#pragma unroll
+            for (int r = 0; r < 4; ++r) q = q == kCBad ? kCBad : a[q];
+            out[p] = q;
+        }
+        __syncthreads();
+    };
+    four(S.nxt, S.j4);
+    four(S.j4, S.j16);
+    if (t == 0) {   // the chain, sixteen sequences per step, then the last ones
+        uint32_t p = 0, i = 0;
+        bool bad = false;
+        for (;;) {
+            S.blk[i >> 4] = uint16_t(p);
+            const uint16_t q = S.j16[p];
+            if (q == kCBad || q == n) break;
+            p = q;
+            i += 16;
+        }
+        for (;;) {
+            const uint16_t q = S.nxt[p];
+            ++i;
+            if (q == kCBad) { bad = true; break; }
+            if (q == n) break;
+            p = q;
+        }
+        S.nseq = bad ? 0u : i;
+    }
+    __syncthreads();
+    const uint32_t nseq = S.nseq;
+    if (nseq == 0) return 0;
+    // every sequence's start, from the sixteenth before it
+    for (uint32_t i = t; i < nseq; i += kCThreads) {
+        uint32_t p = S.blk[i >> 4], r = i & 15;
+        for (; r >= 4; r -= 4) p = S.j4[p];
+        for (; r; --r) p = S.nxt[p];
+        S.start[i] = uint16_t(p);
+    }
+    __syncthreads();
+    // decode one sequence per thread (bytes bounds-checked by seq_end): place
+    // them, check them, and list their non-zero literal bytes in order
+    bool wrong = false;
+    uint64_t carry = 0;
+    uint32_t nzc = 0;
+    for (uint32_t b0 = 0; b0 < nseq; b0 += kCThreads) {
+        const uint32_t i = b0 + t;
+        const bool mine = i < nseq, last = i + 1 == nseq;
+        uint32_t q = 0, ll = 0, ml = 0, off = 0, lit = 0;
+        if (mine) {
+            q = S.start[i];
+            const uint32_t tok = S.body[q++];
+            ll = tok >> 4;
+            if (ll == 15) {
+                uint32_t b;
+                do {
+                    b = S.body[q++];
+                    ll += b;
+                } while (b == 255);
+            }
+            lit = q;
+            q += ll;
+            if (!last) {
+                off = uint32_t(S.body[q]) | (uint32_t(S.body[q + 1]) << 8);
+                q += 2;
+                ml = tok & 15u;
+                if (ml == 15) {
+                    uint32_t b;
+                    do {
+                        b = S.body[q++];
+                        ml += b;
+                    } while (b == 255);
+                }
+                ml += 4;
+            }
+        }
+        // the sequence's output length and its non-zero literal bytes,
+        // scanned together (a length is below 2^21: at most 4096 literals, a
+        // match of at most 19 + 255 bytes per body byte; 256 of them stay
+        // below 2^32)
+        uint32_t c = 0;
+        if (mine)
+            for (uint32_t k = 0; k < ll; ++k) c += S.body[lit + k] != 0;
+        unsigned long long tot;
+        const unsigned long long ex = cta_excl_scan(uint64_t(ll + ml) | (uint64_t(c) << 32), S.wsum, &tot);
+        const uint64_t opl64 = carry + (ex & 0xFFFFFFFFull);
+        const uint32_t opl = opl64 > raw ? raw + 1 : uint32_t(opl64);   // beyond the chunk: rejected below
+        uint32_t at = nzc + uint32_t(ex >> 32);
+        carry += tot & 0xFFFFFFFFull;
+        nzc += uint32_t(tot >> 32);
+        const uint32_t mop = opl + ll;
+        if (mine) {
+            S.opos[i] = opl;
+            if (last) wrong |= opl > raw || ll != raw - opl;
+            else wrong |= opl > raw || ll > raw - opl || off == 0 || off > mop || ml > raw - mop;
+        }
+        if (mine && !wrong)
+            for (uint32_t k = 0; k < ll; ++k) {
+                const uint8_t v = S.body[lit + k];
+                if (v) {
+                    S.nz[at] = uint16_t(opl + k);
+                    S.nzv[at] = v;
+                    ++at;
+                }
+            }
+    }
+    if (__syncthreads_or(wrong)) return 0;
+    // every match copies [mop - off, + min(ml, off)) of the output: no listed
+    // non-zero byte may fall there
+    bool viol = false;
+    for (uint32_t i = t; i + 1 < nseq; i += kCThreads) {
+        uint32_t q = S.start[i];
+        const uint32_t tok = S.body[q++];
+        uint32_t ll = tok >> 4;
+        if (ll == 15) {
+            uint32_t b;
+            do {
+                b = S.body[q++];
+                ll += b;
+            } while (b == 255);
+        }
+        q += ll;
+        const uint32_t off = uint32_t(S.body[q]) | (uint32_t(S.body[q + 1]) << 8);
+        q += 2;
+        uint32_t ml = tok & 15u;
+        if (ml == 15) {
+            uint32_t b;
+            do {
+                b = S.body[q++];
+                ml += b;
+            } while (b == 255);
+        }
+        ml += 4;
+        const uint32_t s0 = S.opos[i] + ll - off, e0 = s0 + (ml < off ? ml : off);
+        uint32_t lo = 0, hi = nzc;   // first listed position >= s0
+        while (lo < hi) {
+            const uint32_t mid = (lo + hi) >> 1;
+            if (S.nz[mid] < s0) lo = mid + 1;
+            else hi = mid;
+        }
+        viol |= lo < nzc && S.nz[lo] < e0;
+    }
+    if (__syncthreads_or(viol)) return 0;
+    // the frame is valid: its non-zero bytes into the receiver
+    const bool one = cd.dst_count == 1;
+    const uint64_t base = one ? ds[0].addr - ds[0].off : 0ull;
+    for (uint32_t j = t; j < nzc; j += kCThreads) {
+        const uint32_t x = S.nz[j];
+        if (x < lim) xor_byte(A.target, one ? base + x : dst_of(ds, cd.dst_count, x), S.nzv[j]);
+    }
+    return 1;
+}
+
+__global__ void __launch_bounds__(kCThreads) apply_cta_kernel(ApplyArgs A)
+{
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    CSmem& S = *reinterpret_cast<CSmem*>(smem_raw);
+    const int t = threadIdx.x;
+    if (t == 0) {
+        const int rc = check_header(A, &S.hdr);
+        S.ok = rc == 0;
+        if (rc) report(A.sc, rc);
+        else if (blockIdx.x == 0) {
+            A.sc->hdr_ok = 1;
+            A.sc->target_version = S.hdr.target_v;
+            A.sc->window = S.hdr.window;
+            A.sc->n_frames = S.hdr.n_frames;
+        }
+    }
+    __syncthreads();
+    if (!S.ok) return;
+    const Hdr H = S.hdr;
+    const uint64_t V = H.target_v;
+    for (;;) {
+        if (t == 0) S.f = atomicAdd(&A.sc->frame_ticket, 1u);
+        __syncthreads();
+        const uint32_t f = S.f;
+        __syncthreads();
+        if (f >= H.n_frames) break;
+        // the frame's checks (every thread reads the same values)
+        const uint64_t fo = ld64(A.payload + H.idx_off + 8ull * f);
+        if (fo < kStreamHdr || fo % 16 || fo + kFrameHdr > H.idx_off) {
+            if (t == 0) report(A.sc, DCR_ERR_CORRUPT);
+            continue;
+        }
+        const uint4 h0 = ld_nc16(A.payload + fo), h1 = ld_nc16(A.payload + fo + 16);
+        const uint32_t kind = h0.y & 0xFFu, fbits = (h0.y >> 8) & 0xFFu, fflags = h0.y >> 16;
+        const uint32_t c = h0.z, raw = h0.w, bl = h1.x;
+        if (h0.x != kFrameMagic || kind < kXorLz4 || kind > kXorSnappy || c < H.chunk_begin ||
+            c >= H.chunk_begin + H.chunk_count || bl > H.idx_off - fo - kFrameHdr) {
+            if (t == 0) report(A.sc, DCR_ERR_CORRUPT);
+            continue;
+        }
+        const ChunkDesc cd = A.chunks[c];
+        if (raw != cd.raw_len || fbits != cd.bits) {
+            if (t == 0) report(A.sc, DCR_ERR_CORRUPT);
+            continue;
+        }
+        const bool is_xor = kind == kXorLz4 || kind == kXorRaw || kind == kXorSnappy;
+        if (A.retry_only && is_xor) {
+            if (t == 0) report(A.sc, DCR_ERR_INVALID);
+            continue;
+        }
+        if (uint64_t(f) > A.abort_at) continue;  // injected fault: never reached
+        const bool cut = uint64_t(f) == A.abort_at;
+        const uint32_t ub = cd.bits == 16 ? 2u : 1u;
+        uint32_t lim = cut ? (A.split < raw ? A.split : raw) : raw;
+        lim -= lim % ub;
+        unsigned long long* st = &A.state[c];
+        if (is_xor) {
+            bool got = false;
+            if (t == 0) {
+                bool to = false;
+                got = claim(st, V, &to);
+                if (to) report(A.sc, DCR_ERR_TIMEOUT);
+                if (!got && !to) atomicAdd(&A.sc->skipped, 1ull);
+            }
+            if (!__syncthreads_or(got)) continue;
+            // Snappy frames and general LZ4 frames to the deferred kernels,
+            // ZSRC LZ4 bodies larger than the shared buffer to big_kernel
+            const bool zs = (fflags & kFrameZsrc) != 0;
+            if (kind == kXorSnappy && zs) {
+                if (t == 0) A.defer[A.defer_len - 1 - atomicAdd(&A.sc->n_big, 1u)] = f;
+                continue;
+            }
+            if ((kind == kXorLz4 && !zs) || kind == kXorSnappy) {
+                if (t == 0) A.defer[atomicAdd(&A.sc->n_defer, 1u)] = f;
+                continue;
+            }
+            if (kind == kXorLz4 && bl > kCBody) {
+                if (t == 0) A.defer[A.defer_len - 1 - atomicAdd(&A.sc->n_big, 1u)] = f;
+                continue;
+            }
+        }
+        const Seg* ds = A.dst + cd.dst_begin;
+        const uint8_t* body = A.payload + fo + kFrameHdr;
+        bool good = true;
+        if (kind == kXorRaw) {
+            good = bl == raw;
+            if (good) {
+                for (uint32_t v = t; v < raw / 16; v += kCThreads) {
+                    const uint4 m = ld_nc16(body + 16 * v);
+                    if (!is_zero(m)) xor_vec(A, cd, ds, 16 * v, m, lim);
+                }
+                for (uint32_t x = (raw & ~15u) + t; x < raw; x += kCThreads)
+                    if (body[x] && x < lim) xor_byte(A.target, dst_of(ds, cd.dst_count, x), body[x]);
+            }
+        } else if (kind == kXorLz4) {
+            for (uint32_t v = t; v < bl / 16; v += kCThreads)
+                reinterpret_cast<uint4*>(S.body)[v] = ld_nc16(body + 16 * v);
+            for (uint32_t x = (bl & ~15u) + t; x < bl; x += kCThreads) S.body[x] = body[x];
+            __syncthreads();
+            good = zsrc_apply_cta(A, cd, ds, bl, raw, lim, S) == 1;
+        } else if (kind == kOverwriteDense) {
+            good = bl == raw;
+            if (good) {
+                for (uint32_t v = t; v < raw / 16; v += kCThreads)
+                    put_vec(A, cd, ds, 16 * v, ld_nc16(body + 16 * v), lim, raw);
+                for (uint32_t x = (raw & ~15u) + t; x < raw; x += kCThreads)
+                    if (x < lim) A.target[dst_of(ds, cd.dst_count, x)] = body[x];
+            }
+        } else {
+            // OVERWRITE records: n, ascending unit offsets, pad, values
+            const uint32_t cnt = bl >= 4 ? *reinterpret_cast<const uint32_t*>(body) : 0u;
+            const uint64_t pad = (4 - (2ull * cnt) % 4) % 4;
+            good = bl >= 4 && 4 + 2ull * cnt + pad + uint64_t(cnt) * ub == bl;
+            const uint16_t* offs = reinterpret_cast<const uint16_t*>(body + 4);
+            const uint8_t* vals = body + 4 + 2 * cnt + pad;
+            if (good) {
+                bool bad = false;
+                for (uint32_t i = t; i < cnt; i += kCThreads) {
+                    const uint32_t u = offs[i];
+                    bad |= (u + 1) * ub > raw || (i && u <= offs[i - 1]);
+                }
+                good = !__syncthreads_or(bad);
+            }
+            if (good) {
+                for (uint32_t i = t; i < cnt; i += kCThreads) {
+                    const uint32_t x = uint32_t(offs[i]) * ub;
+                    if (x >= lim) continue;
+                    const uint64_t a = dst_of(ds, cd.dst_count, x);
+                    if (ub == 2 && (a & 1) == 0 && dst_of(ds, cd.dst_count, x + 1) == a + 1)
+                        *reinterpret_cast<uint16_t*>(A.target + a) =
+                            uint16_t(vals[2 * i] | (uint32_t(vals[2 * i + 1]) << 8));
+                    else
+                        for (uint32_t e = 0; e < ub; ++e)
+                            A.target[dst_of(ds, cd.dst_count, x + e)] = vals[i * ub + e];
+                }
+            }
+        }
+        __syncthreads();   // every thread's writes of this frame precede its DONE mark
+        if (t == 0) {
+            if (!good) {
+                report(A.sc, DCR_ERR_CORRUPT);
+            } else {
+                atomicAdd(&A.sc->applied, 1ull);
+                __threadfence();
+                if (cut) {
+                    A.sc->aborted = 1;
+                    if (!is_xor) atomicExch(st, (V << 2) | kClaimed);
+                } else {
+                    atomicExch(st, (V << 2) | kDone);
+                }
+            }
+        }
+    }
+}
+
 // General LZ4 frames (no ZSRC promise): full decode in shared memory.
 __global__ void __launch_bounds__(kDThreads) defer_kernel(ApplyArgs A)
 {
@@ -1157,6 +1547,11 @@ int apply_kernel_config(KernelConfig* kc)
     if (e == cudaSuccess)
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&kc->snappy_blocks_per_sm, snappy_kernel, 32 * kSnWarps,
                                                           kSnWarps * kChunk / 8);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(apply_cta_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sizeof(CSmem)));
+    if (e == cudaSuccess)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&kc->apply_cta_blocks_per_sm, apply_cta_kernel, kCThreads,
+                                                          sizeof(CSmem));
     if (e == cudaSuccess) {
         // load the last kernel of the apply too (the others were loaded by
         // the queries above), so that no apply call loads code lazily
@@ -1166,13 +1561,34 @@ int apply_kernel_config(KernelConfig* kc)
     if (e != cudaSuccess) return cuda_error(e, "apply kernel configuration");
     if (kc->snappy_blocks_per_sm < 1) kc->snappy_blocks_per_sm = 1;
     if (kc->apply_blocks_per_sm < 1) kc->apply_blocks_per_sm = 1;
+    if (kc->apply_cta_blocks_per_sm < 1) kc->apply_cta_blocks_per_sm = 1;
     if (kc->big_blocks_per_sm < 1) kc->big_blocks_per_sm = 1;
     if (kc->defer_blocks_per_sm < 1) kc->defer_blocks_per_sm = 1;
     return DCR_OK;
 }
 
-int apply_launch(const dcr_plan* P, dcr_recv_state* st, const void* payload, size_t size, void* target,
-                 uint64_t abort_at, uint32_t split, int retry_only, cudaStream_t s)
+namespace {
+
+// The first apply kernel: one CTA per frame for plans whose windows have
+// fewer chunks than the GPU has warp slots (or when the plan asks for it),
+// else one warp per frame.
+void launch_first(const dcr_plan* P, const ApplyArgs& A, cudaStream_t s)
+{
+    const int sms = P->kc.num_sms;
+    const bool cta = P->apply == DCR_APPLY_CTA ||
+                     (P->apply == DCR_APPLY_AUTO && P->max_window_chunks <= uint64_t(P->small_window_chunks));
+    if (cta)
+        apply_cta_kernel<<<sms * P->kc.apply_cta_blocks_per_sm, kCThreads, sizeof(CSmem), s>>>(A);
+    else
+        apply_kernel<<<sms * P->kc.apply_blocks_per_sm, kAThreads, sizeof(ASmem), s>>>(A);
+}
+
+}  // namespace
+
+namespace {
+
+ApplyArgs make_args(const dcr_plan* P, dcr_recv_state* st, const void* payload, size_t size, void* target,
+                    uint64_t abort_at, uint32_t split, int retry_only)
 {
     ApplyArgs A{};
     A.chunks = P->d_chunks;
@@ -1191,21 +1607,54 @@ int apply_launch(const dcr_plan* P, dcr_recv_state* st, const void* payload, siz
     A.version = st->version;
     A.abort_at = abort_at;
     A.split = split;
-    cudaError_t e = cudaMemsetAsync(st->d_scratch, 0, sizeof(ApplyScratch), s);
-    if (e != cudaSuccess) return cuda_error(e, "apply scratch reset");
+    return A;
+}
+
+// the kernels of the frames the first kernel deferred (general LZ4 and
+// Snappy frames, large ZSRC frames, ZSRC Snappy frames)
+void launch_deferred(const dcr_plan* P, const ApplyArgs& A, cudaStream_t s)
+{
     const int sms = P->kc.num_sms;
-    if (P->profiling) cudaEventRecord(P->ev[3], s);
-    apply_kernel<<<sms * P->kc.apply_blocks_per_sm, kAThreads, sizeof(ASmem), s>>>(A);
-    if (P->profiling) cudaEventRecord(P->ev[4], s);
     defer_kernel<<<sms * P->kc.defer_blocks_per_sm, kDThreads, kChunk, s>>>(A);
     big_kernel<<<sms * P->kc.big_blocks_per_sm, kBThreads, sizeof(BWarp) * kBWarps, s>>>(A);
     snappy_kernel<<<sms * P->kc.snappy_blocks_per_sm, 32 * kSnWarps, kSnWarps * kChunk / 8, s>>>(A);
+}
+
+}  // namespace
+
+int apply_launch_part(const dcr_plan* P, dcr_recv_state* st, const void* payload, size_t size, void* target,
+                      uint64_t abort_at, uint32_t split, int retry_only, int part, cudaStream_t s)
+{
+    const ApplyArgs A = make_args(P, st, payload, size, target, abort_at, split, retry_only);
+    cudaError_t e = cudaSuccess;
+    const int sms = P->kc.num_sms;
+    if (part != kApplyDeferred) {
+        e = cudaMemsetAsync(st->d_scratch, 0, sizeof(ApplyScratch), s);
+        if (e != cudaSuccess) return cuda_error(e, "apply scratch reset");
+        if (P->profiling) cudaEventRecord(P->ev[3], s);
+        launch_first(P, A, s);
+        if (P->profiling) cudaEventRecord(P->ev[4], s);
+    }
+    if (part != kApplyFirst) {
+        if (part == kApplyDeferred) {   // the commit check runs again after them
+            e = cudaMemsetAsync(&st->d_scratch->pending, 0, sizeof(st->d_scratch->pending), s);
+            if (e != cudaSuccess) return cuda_error(e, "apply scratch reset");
+            if (P->profiling) cudaEventRecord(P->ev[7], s);
+        }
+        launch_deferred(P, A, s);
+    }
     if (P->profiling) cudaEventRecord(P->ev[5], s);
     pending_kernel<<<sms, 256, 0, s>>>(A);
     if (P->profiling) cudaEventRecord(P->ev[6], s);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_error(e, "apply launch");
     return DCR_OK;
+}
+
+int apply_launch(const dcr_plan* P, dcr_recv_state* st, const void* payload, size_t size, void* target,
+                 uint64_t abort_at, uint32_t split, int retry_only, cudaStream_t s)
+{
+    return apply_launch_part(P, st, payload, size, target, abort_at, split, retry_only, kApplyAll, s);
 }
 
 // ---- apply without allocation ---------------------------------------------
@@ -1333,7 +1782,7 @@ int apply_launch_noalloc(const dcr_plan* P, dcr_recv_state* st, const void* payl
     e = cudaMemsetAsync(A.sc, 0, sizeof(ApplyScratch), s);
     if (e != cudaSuccess) return cuda_error(e, "static apply scratch reset");
     const int sms = P->kc.num_sms;
-    apply_kernel<<<sms * P->kc.apply_blocks_per_sm, kAThreads, sizeof(ASmem), s>>>(A);
+    launch_first(P, A, s);
     defer_kernel<<<sms * P->kc.defer_blocks_per_sm, kDThreads, kChunk, s>>>(A);
     big_kernel<<<sms * P->kc.big_blocks_per_sm, kBThreads, sizeof(BWarp) * kBWarps, s>>>(A);
     snappy_kernel<<<sms * P->kc.snappy_blocks_per_sm, 32 * kSnWarps, kSnWarps * kChunk / 8, s>>>(A);

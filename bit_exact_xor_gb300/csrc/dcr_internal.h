@@ -123,6 +123,7 @@ struct KernelConfig {
     int restream_blocks_per_sm = 0;
     int spill_blocks_per_sm = 0;
     int apply_blocks_per_sm = 0;
+    int apply_cta_blocks_per_sm = 0;
     int defer_blocks_per_sm = 0;
     int big_blocks_per_sm = 0;
     int snappy_blocks_per_sm = 0;
@@ -145,6 +146,13 @@ int apply_kernel_config(KernelConfig* kc);
 int apply_launch(const struct ::dcr_plan* plan, struct ::dcr_recv_state* st, const void* payload,
                  size_t size, void* target, uint64_t abort_at, uint32_t split, int retry_only,
                  cudaStream_t s);
+// one part of an apply: kApplyFirst = the first kernel and the commit check;
+// kApplyDeferred = the deferred-frame kernels and the commit check again;
+// kApplyAll = all of them (what apply_launch launches)
+enum { kApplyAll = 0, kApplyFirst = 1, kApplyDeferred = 2 };
+int apply_launch_part(const struct ::dcr_plan* plan, struct ::dcr_recv_state* st, const void* payload,
+                      size_t size, void* target, uint64_t abort_at, uint32_t split, int retry_only, int part,
+                      cudaStream_t s);
 int dense_launch(const struct ::dcr_plan* plan, const void* const* shards, void* target,
                  cudaStream_t s);
 
@@ -175,6 +183,8 @@ struct dcr_plan {
     uint64_t window_bytes = 0;
     uint32_t encoder = DCR_ENCODER_AUTO;
     uint32_t codec = DCR_CODEC_LZ4;
+    uint32_t apply = DCR_APPLY_AUTO;
+    int small_window_chunks = 0;         // AUTO takes the CTA-per-chunk kernels up to this window size
     uint64_t n_chunks = 0;
     uint64_t canonical_bytes = 0;
     uint64_t hash = 0;
@@ -204,6 +214,7 @@ struct dcr_plan {
     cudaEvent_t ev[8] = {};
     mutable dcr_profile prof = {};
     mutable bool prof_encode_due = false, prof_apply_due = false;   // events recorded, durations not read
+    mutable bool prof_deferred = false;   // the deferred-frame kernels ran after a status read (from ev[7])
     // ownership-sharded encode: the part sized by the last dcr_encode_part
     struct {
         bool valid = false;

@@ -1266,15 +1266,17 @@ __device__ __forceinline__ int list_events(Buf& B, int t, int n, int lane, int* 
     return t;
 }
 
-// LZ4 block of the chunk in B written to body[0, body_len); returns its size.
-// Events are listed in batches; a batch's partial last group moves to the
-// front of the next one, so the groups are those of encode_kernel.
+// LZ4 block of the chunk in B written to body[0, body_len); returns its size
+// (body == nullptr: the size only).  Events are listed in batches; a batch's
+// partial last group moves to the front of the next one, so the groups are
+// those of encode_kernel.
 template <class Codec>
 __device__ uint32_t mask_block(Buf& B, int raw, uint8_t* body, uint32_t body_len, int lane, bool* bad)
 {
     const MaskSrc S{B.ev, reinterpret_cast<const uint8_t*>(B.data)};
     Parse P{-1, 0ull, 0, 0, Codec::preamble(uint32_t(raw))};
-    if (lane == 0) {   // the block's preamble
+    const bool emit = body != nullptr;
+    if (emit && lane == 0) {   // the block's preamble
         uint32_t o = 0;
         auto put = [&](uint32_t v) { body[o++] = uint8_t(v); };
         Codec::emit_preamble(put, uint32_t(raw));
@@ -1287,9 +1289,9 @@ __device__ uint32_t mask_block(Buf& B, int raw, uint8_t* body, uint32_t body_len
         const bool fin = t >= kSteps;
         int g = 0;
         for (; g + 32 <= n; g += 32)
-            parse_group<Codec>(S, g, 32, false, raw, P, body, body_len, true, lane, &over, bad);
+            parse_group<Codec>(S, g, 32, false, raw, P, body, body_len, emit, lane, &over, bad);
         if (fin) {
-            parse_group<Codec>(S, g, n - g, true, raw, P, body, body_len, true, lane, &over, bad);
+            parse_group<Codec>(S, g, n - g, true, raw, P, body, body_len, emit, lane, &over, bad);
             break;
         }
         const int rem = n - g;   // < 32, and g >= 32 since a batch stops only near kEvCap
@@ -1343,6 +1345,301 @@ __global__ void __launch_bounds__(kSThreads, 2) spill_kernel(EncArgs A)
     }
 }
 
+// ------------------------------------------------------- encode_cta_kernel --
+// One CTA of 8 warps per chunk, for windows with fewer chunks than the GPU
+// has warp slots (one warp per chunk would leave the run as long as one
+// chunk's serial parse).  Each warp streams an 8 KiB slice of the chunk
+// (old and new, four 16-byte vectors per lane in flight), XORs, counts the
+// changed values and lists the positions and values of the slice's non-zero
+// bytes in its own region of shared memory; nothing else of the chunk is
+// kept.  The chunk's event e lives in the region of the warp whose events
+// come before it.  The groups of 32 events are then parsed in parallel: the
+// state a group carries in from the groups before it comes from three scans
+// over the groups (the longest earlier zero run, the end of the last earlier
+// match, the output offset), so every group is parsed exactly as the
+// one-warp encoders parse it and the frames are byte-identical.  Frames that
+// fit the slot are written there; raw masks and bodies over the slot are
+// sized here and listed for the write pass.  Overwrite chunks, chunks whose
+// pieces are not 16-byte aligned and slices with more events than their
+// region holds are encoded by warp 0 with the one-warp encoder.
+constexpr int kEWarps = 8;
+constexpr int kEThreads = 32 * kEWarps;
+constexpr int kESlice = kChunk / kEWarps;           // 8 KiB per warp
+constexpr int kEVPL = kESlice / 16 / 32;            // 16 vectors per lane
+constexpr int kEBatch = 4;                          // ... loaded four at a time
+constexpr int kEWarpCap = 1536;                     // events a warp's region holds
+constexpr int kECap = kEWarpCap * kEWarps;
+constexpr int kEGroups = kECap / 32 + 1;
+
+struct __align__(16) CtaSmem {
+    union {
+        struct {
+            uint16_t pos[kECap];
+            uint8_t val[kECap];
+        } ev;
+        WarpSmem w;   // warp 0's one-warp encoder
+    } u;
+    unsigned long long gbest[kEGroups];   // a group's longest zero run, then the longest before it
+    int glit[kEGroups];                   // end of a group's last match (-1: none), then of the last before it
+    int glev[kEGroups];                   // ... and the event at that end (the first pending literal event)
+    uint32_t gsz[kEGroups];               // a group's bytes, then the block bytes before it
+    uint32_t wcnt[kEWarps];               // events per slice
+    uint32_t wchg[kEWarps];               // changed stored values per slice
+    uint32_t base[kEWarps];               // events before each slice
+    Seg segs[kMSegCache];
+    uint32_t total;
+};
+
+// Events of encode_cta_kernel: event e of the chunk is entry e - base[w] of
+// warp w's region, w the last warp with base[w] <= e.
+struct SliceSrc {
+    const uint16_t* pos;
+    const uint8_t* val;
+    const uint32_t* base;
+    __device__ __forceinline__ int slot(int e) const
+    {
+        int w = 0;
+#pragma unroll
+        for (int i = 1; i < kEWarps; ++i) w += e >= int(base[i]);
+        return w * kEWarpCap + e - int(base[w]);
+    }
+    __device__ __forceinline__ int at(int e) const { return pos[slot(e)]; }
+    template <class Put>
+    __device__ __forceinline__ bool lits(int a, int b, int e, int e_end, Put& put) const
+    {
+        for (int q = a; q < b; ++q) {
+            uint32_t v = 0;
+            if (e < e_end) {
+                const int s = slot(e);
+                if (int(pos[s]) == q) {
+                    v = val[s];
+                    ++e;
+                }
+            }
+            put(v);
+        }
+        return e == e_end;
+    }
+};
+
+template <class Codec>
+__global__ void __launch_bounds__(kEThreads, 4) encode_cta_kernel(EncArgs A)
+{
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    CtaSmem& C = *reinterpret_cast<CtaSmem*>(smem_raw);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t k = blockIdx.x;
+    if (k >= A.chunk_count) return;
+    const ChunkDesc cd = A.chunks[A.chunk_begin + k];
+    const int raw = int(cd.raw_len);
+    const int nseg = int(cd.src_count);
+    const bool overwrite = (cd.flags & kResidualFlag) || A.mode == DCR_MODE_OVERWRITE_ONLY;
+    if (overwrite || !(cd.flags & kSrcVec)) {   // the one-warp encoder does these
+        if (warp == 0) encode_chunk<kNS, Codec>(A, C.u.w, k, lane);
+        return;
+    }
+    if (nseg <= kMSegCache)
+        for (int i = threadIdx.x; i < nseg; i += kEThreads) C.segs[i] = A.src[cd.src_begin + i];
+    __syncthreads();
+    const Seg* segs = nseg <= kMSegCache ? C.segs : A.src + cd.src_begin;
+
+    // stream the slice: XOR, count, list the non-zero bytes in order
+    uint16_t* wpos = C.u.ev.pos + warp * kEWarpCap;
+    uint8_t* wval = C.u.ev.val + warp * kEWarpCap;
+    const uint32_t lt = (1u << lane) - 1u;
+    const int v0 = warp * (kESlice / 16);
+    const int nvec = raw >> 4;
+    uint32_t changed = 0, n = 0;
+    int cur = 0;
+    for (int j0 = 0; j0 < kEVPL; j0 += kEBatch) {
+        uint4 o[kEBatch], nw[kEBatch];
+#pragma unroll
+        for (int j = 0; j < kEBatch; ++j) {
+            const int v = v0 + (j0 + j) * 32 + lane;
+            o[j] = nw[j] = make_uint4(0u, 0u, 0u, 0u);
+            if (v < nvec) {
+                const uint32_t x = uint32_t(v) << 4;
+                while (cur + 1 < nseg && segs[cur + 1].off <= x) ++cur;
+                const Seg sg = segs[cur];
+                const uint32_t r = uint32_t(sg.addr >> kShardShift);
+                const uint64_t a = (sg.addr & kAddrMask) + (x - sg.off);
+                o[j] = ld_stream(A.olds[r] + a);
+                nw[j] = ld_stream(A.news[r] + a);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < kEBatch; ++j) {
+            const uint4 m = xor4(o[j], nw[j]);
+            const uint32_t z = nz16(m);
+            if (cd.bits == 16) changed += __popc((z | (z >> 1)) & 0x5555u);
+            else if (cd.bits == 8) changed += __popc(z);
+            else changed += nibbles_nz(m.x) + nibbles_nz(m.y) + nibbles_nz(m.z) + nibbles_nz(m.w);
+            const uint32_t c = __popc(z);
+            const uint32_t incl = warp_incl_sum(c, lane);
+            const uint32_t tot = __shfl_sync(kFull, incl, 31);
+            uint32_t at = n + incl - c;
+            const uint32_t x = uint32_t(v0 + (j0 + j) * 32 + lane) << 4;
+            for (uint32_t b = z; b; b &= b - 1) {
+                const uint32_t i = __ffs(b) - 1;
+                if (at < uint32_t(kEWarpCap)) {
+                    wpos[at] = uint16_t(x + i);
+                    wval[at] = uint8_t(byte_of(m, i));
+                }
+                ++at;
+            }
+            n += tot;
+        }
+    }
+    changed = __reduce_add_sync(kFull, changed);
+    if (lane == 0) {
+        C.wcnt[warp] = n;
+        C.wchg[warp] = changed;
+    }
+    __syncthreads();
+    uint32_t total_ev = 0, chunk_changed = 0;
+    bool overflow = false;
+#pragma unroll
+    for (int w = 0; w < kEWarps; ++w) {
+        const uint32_t c = C.wcnt[w];
+        if (warp == 0 && lane == w) C.base[w] = total_ev;
+        total_ev += c;
+        chunk_changed += C.wchg[w];
+        overflow |= c > uint32_t(kEWarpCap);
+    }
+    if (overflow) {   // a slice outgrew its region: the one-warp encoder takes the chunk
+        __syncthreads();
+        if (warp == 0) encode_chunk<kNS, Codec>(A, C.u.w, k, lane);
+        return;
+    }
+    if (threadIdx.x == 0 && chunk_changed) {
+        atomicAdd(&A.counts[cd.tensor], (unsigned long long)chunk_changed);
+        atomicAdd(reinterpret_cast<unsigned long long*>(&A.sc->changed), (unsigned long long)chunk_changed);
+    }
+    if (chunk_changed == 0) {
+        if (threadIdx.x == 0) A.fsize[k] = 0;
+        return;
+    }
+    __syncthreads();   // base[] written
+    uint8_t* slot = A.slots + size_t(k) * kEncSlot;
+    auto spill = [&](uint32_t kind, uint32_t body_len) {
+        const uint32_t fsz = (kFrameHdr + body_len + 15) / 16 * 16;
+        A.fsize[k] = fsz | kSpilled;
+        A.spill[atomicAdd(&A.sc->n_spill, 1u)] = SpillRec{k, kind, body_len, 0u, chunk_changed, {0u, 0u, 0u}};
+    };
+    const SliceSrc S{C.u.ev.pos, C.u.ev.val, C.base};
+    const int full = int(total_ev / 32), G = full + 1;   // full groups, then the final one (with the end event)
+    auto group = [&](int g, Parse& P, uint8_t* out, uint32_t cap, bool emit, bool* over, bool* bad) {
+        P.prev = g ? S.at(32 * g - 1) : -1;
+        const bool fin = g == full;
+        parse_group<Codec>(S, 32 * g, fin ? int(total_ev) - 32 * g : 32, fin, raw, P, out, cap, emit, lane, over,
+                           bad);
+    };
+    bool over = false, bad = false;
+    // 1. each group's longest zero run (independent of the carried state)
+    for (int g = warp; g < G; g += kEWarps) {
+        Parse P{-1, 0ull, 0, 0, 0u};
+        group(g, P, nullptr, 0, false, &over, &bad);
+        if (lane == 0) C.gbest[g] = P.best;
+    }
+    __syncthreads();
+    if (warp == 0) {   // exclusive prefix maximum
+        unsigned long long run = 0;
+        for (int g0 = 0; g0 < G; g0 += 32) {
+            const int g = g0 + lane;
+            unsigned long long incl = g < G ? C.gbest[g] : 0ull;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const unsigned long long o = __shfl_up_sync(kFull, incl, d);
+                if (lane >= d && o > incl) incl = o;
+            }
+            unsigned long long ex = __shfl_up_sync(kFull, incl, 1);
+            if (lane == 0) ex = 0ull;
+            if (ex < run) ex = run;
+            if (g < G) C.gbest[g] = ex;
+            const unsigned long long last = __shfl_sync(kFull, incl, 31);
+            if (last > run) run = last;
+        }
+    }
+    __syncthreads();
+    // 2. each group's last match, given the longest run before it
+    for (int g = warp; g < G; g += kEWarps) {
+        Parse P{-1, C.gbest[g], -1, 0, 0u};
+        group(g, P, nullptr, 0, false, &over, &bad);
+        if (lane == 0) {
+            C.glit[g] = P.lit;
+            C.glev[g] = P.lit_ev;
+        }
+    }
+    __syncthreads();
+    if (warp == 0) {   // exclusive "latest match end so far", with its event (0, 0 before the first)
+        int run = 0, run_ev = 0;
+        for (int g0 = 0; g0 < G; g0 += 32) {
+            const int g = g0 + lane;
+            const int v = g < G ? C.glit[g] : -1;
+            const int ve = g < G ? C.glev[g] : 0;
+            const uint32_t has = __ballot_sync(kFull, v >= 0);
+            const uint32_t below = has & lt;
+            const int src = below ? 31 - __clz(below) : 0;
+            const int from = __shfl_sync(kFull, v, src), from_ev = __shfl_sync(kFull, ve, src);
+            if (g < G) {
+                C.glit[g] = below ? from : run;
+                C.glev[g] = below ? from_ev : run_ev;
+            }
+            if (has) {
+                run = __shfl_sync(kFull, v, 31 - __clz(has));
+                run_ev = __shfl_sync(kFull, ve, 31 - __clz(has));
+            }
+        }
+    }
+    __syncthreads();
+    // 3. each group's bytes, given both
+    for (int g = warp; g < G; g += kEWarps) {
+        Parse P{-1, C.gbest[g], C.glit[g], C.glev[g], 0u};
+        group(g, P, nullptr, 0, false, &over, &bad);
+        if (lane == 0) C.gsz[g] = P.out;
+    }
+    __syncthreads();
+    if (warp == 0) {   // exclusive prefix sum after the block's preamble
+        uint32_t run = Codec::preamble(uint32_t(raw));
+        for (int g0 = 0; g0 < G; g0 += 32) {
+            const int g = g0 + lane;
+            const uint32_t v = g < G ? C.gsz[g] : 0u;
+            const uint32_t incl = warp_incl_sum(v, lane);
+            if (g < G) C.gsz[g] = run + incl - v;
+            run += __shfl_sync(kFull, incl, 31);
+        }
+        if (lane == 0) C.total = run;
+    }
+    __syncthreads();
+    const uint32_t total = C.total;
+    if (total >= uint32_t(raw)) {
+        if (threadIdx.x == 0) spill(kXorRaw, uint32_t(raw));
+        return;
+    }
+    if (total > kSlotBody) {
+        if (threadIdx.x == 0) spill(Codec::kKind, total);
+        return;
+    }
+    // 4. the block into the slot
+    uint8_t* body = slot + kFrameHdr;
+    if (threadIdx.x == 0) {   // the block's preamble (Snappy: the chunk length)
+        uint32_t o = 0;
+        auto put = [&](uint32_t v) { body[o++] = uint8_t(v); };
+        Codec::emit_preamble(put, uint32_t(raw));
+    }
+    for (int g = warp; g < G; g += kEWarps) {
+        Parse P{-1, C.gbest[g], C.glit[g], C.glev[g], C.gsz[g]};
+        group(g, P, body, kSlotBody, true, &over, &bad);
+    }
+    if (__any_sync(kFull, over || bad) && lane == 0) report(A.sc, DCR_ERR_CORRUPT);
+    const uint32_t fsz = (kFrameHdr + total + 15) / 16 * 16;
+    for (uint32_t i = kFrameHdr + total + threadIdx.x; i < fsz; i += kEThreads) slot[i] = 0;   // padding
+    if (threadIdx.x == 0) {
+        write_header(slot, Codec::kKind, cd.bits, A.chunk_begin + k, uint32_t(raw), total, chunk_changed);
+        A.fsize[k] = fsz;
+    }
+}
+
 constexpr size_t kMainSmem = sizeof(WarpSmem) * kMWarps;
 constexpr size_t kDeepSmem = sizeof(WarpSmemDeep) * kDeepWarps;
 
@@ -1364,6 +1661,9 @@ cudaError_t codec_attributes()
                                  int(kMainSmem));
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(spill_kernel<Codec>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sizeof(Buf)));
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(encode_cta_kernel<Codec>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 int(sizeof(CtaSmem)));
     return e;
 }
 
@@ -1438,16 +1738,23 @@ int launch_size(const dcr_plan* P, EncArgs& A, uint64_t plan_hash, uint64_t base
     unsigned grid = main_grid(P);
     if (warps > A.chunk_count) grid = (A.chunk_count + kMWarps - 1) / kMWarps;
     if (grid == 0) grid = 1;
-    // a window of few chunks leaves most warp slots empty: then one chunk per
-    // warp of the deep variant, spread over all SMs, is faster
+    // a window of few chunks leaves most warp slots empty: then one CTA per
+    // chunk (the CTA variant) is faster than one warp per chunk
     const unsigned deep_warps = unsigned(P->kc.num_sms * P->kc.enc_deep_blocks_per_sm * kDeepWarps);
-    const bool deep = P->encoder == DCR_ENCODER_DEEP || (P->encoder == DCR_ENCODER_AUTO && A.chunk_count <= deep_warps);
+    const bool cta = P->encoder == DCR_ENCODER_CTA ||
+                     (P->encoder == DCR_ENCODER_AUTO && A.chunk_count <= uint32_t(P->small_window_chunks));
+    const bool deep = P->encoder == DCR_ENCODER_DEEP;
     unsigned dgrid = (A.chunk_count + kDeepWarps - 1) / kDeepWarps;
     if (dgrid > deep_warps / kDeepWarps) dgrid = deep_warps / kDeepWarps;
     if (dgrid == 0) dgrid = 1;
     const bool snappy = P->codec == DCR_CODEC_SNAPPY;
     if (P->profiling) cudaEventRecord(P->ev[0], s);
-    if (deep && snappy)
+    const unsigned cgrid = A.chunk_count ? A.chunk_count : 1;
+    if (cta && snappy)
+        encode_cta_kernel<CodecSnappy><<<cgrid, kEThreads, sizeof(CtaSmem), s>>>(A);
+    else if (cta)
+        encode_cta_kernel<CodecLz4><<<cgrid, kEThreads, sizeof(CtaSmem), s>>>(A);
+    else if (deep && snappy)
         encode_kernel<kNSDeep, CodecSnappy><<<dgrid, 32 * kDeepWarps, kDeepSmem, s>>>(A);
     else if (deep)
         encode_kernel<kNSDeep, CodecLz4><<<dgrid, 32 * kDeepWarps, kDeepSmem, s>>>(A);

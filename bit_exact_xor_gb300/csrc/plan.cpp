@@ -219,10 +219,12 @@ extern "C" int dcr_plan_build(const dcr_tensor_desc* tensors, size_t n, const dc
     if (W < kChunk || W > kMaxWindowBytes)
         return set_error(DCR_ERR_INVALID, "window_bytes must be in [64 KiB, 256 GiB]");
     const uint32_t encoder = opts ? opts->encoder : uint32_t(DCR_ENCODER_AUTO);
-    if (encoder > DCR_ENCODER_DEEP) return set_error(DCR_ERR_INVALID, "unknown encoder variant %u", encoder);
+    if (encoder > DCR_ENCODER_CTA) return set_error(DCR_ERR_INVALID, "unknown encoder variant %u", encoder);
     const uint32_t codec = opts ? opts->codec : uint32_t(DCR_CODEC_LZ4);
     if (codec > DCR_CODEC_SNAPPY) return set_error(DCR_ERR_INVALID, "unknown codec %u", codec);
     const uint32_t flags = opts ? opts->flags : 0u;
+    const uint32_t apply = opts ? opts->apply : uint32_t(DCR_APPLY_AUTO);
+    if (apply > DCR_APPLY_CTA) return set_error(DCR_ERR_INVALID, "unknown apply variant %u", apply);
     if (flags & ~uint32_t(DCR_PLAN_HOST_ONLY)) return set_error(DCR_ERR_INVALID, "unknown plan flags %#x", flags);
     dcr_plan* P = new (std::nothrow) dcr_plan();
     if (!P) return set_error(DCR_ERR_NOMEM, "dcr_plan_build: out of host memory");
@@ -230,6 +232,7 @@ extern "C" int dcr_plan_build(const dcr_tensor_desc* tensors, size_t n, const dc
     P->host_only = (flags & DCR_PLAN_HOST_ONLY) != 0;
     P->encoder = encoder;
     P->codec = codec;
+    P->apply = apply;
     P->tp = tensors[0].tp;
     for (size_t i = 0; i < n; ++i) {
         const char* why;
@@ -403,6 +406,7 @@ extern "C" int dcr_plan_build(const dcr_tensor_desc* tensors, size_t n, const dc
         delete P;
         return rc;
     }
+    P->small_window_chunks = P->kc.num_sms * P->kc.enc_deep_blocks_per_sm * 2;
     *out = P;
     return DCR_OK;
 }
@@ -598,12 +602,23 @@ static int apply_common(const dcr_plan* p, dcr_recv_state* st, const void* paylo
     if (!aligned16(payload) || !aligned16(target))
         return set_error(DCR_ERR_INVALID, "dcr_apply: payload/target not 16-byte aligned");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    int rc = apply_launch(p, st, payload, size, target, abort_at, split, retry_only, s);
+    // the first kernel and the commit check; the deferred-frame kernels only
+    // when the first kernel deferred frames to them (a second status read)
+    int rc = apply_launch_part(p, st, payload, size, target, abort_at, split, retry_only, kApplyFirst, s);
     if (rc) return rc;
     cudaError_t e = cudaMemcpyAsync(st->h_scratch, st->d_scratch, sizeof(ApplyScratch),
                                     cudaMemcpyDeviceToHost, s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return cuda_error(e, "dcr_apply status read");
+    p->prof_deferred = false;
+    if (st->h_scratch->hdr_ok && (st->h_scratch->n_defer || st->h_scratch->n_big)) {
+        p->prof_deferred = true;
+        rc = apply_launch_part(p, st, payload, size, target, abort_at, split, retry_only, kApplyDeferred, s);
+        if (rc) return rc;
+        e = cudaMemcpyAsync(st->h_scratch, st->d_scratch, sizeof(ApplyScratch), cudaMemcpyDeviceToHost, s);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+        if (e != cudaSuccess) return cuda_error(e, "dcr_apply status read");
+    }
     if (p->profiling) {
         p->prof_apply_due = true;
         p->prof.apply_valid = 1;
@@ -652,7 +667,7 @@ extern "C" int dcr_plan_last_profile(const dcr_plan* p, dcr_profile* out)
     }
     if (p->prof_apply_due) {
         cudaEventElapsedTime(&p->prof.apply_ms, p->ev[3], p->ev[4]);
-        cudaEventElapsedTime(&p->prof.defer_ms, p->ev[4], p->ev[5]);
+        cudaEventElapsedTime(&p->prof.defer_ms, p->ev[p->prof_deferred ? 7 : 4], p->ev[5]);
         cudaEventElapsedTime(&p->prof.pending_ms, p->ev[5], p->ev[6]);
         p->prof_apply_due = false;
     }

@@ -95,11 +95,18 @@ enum {
 };
 
 enum { DCR_MODE_HYBRID = 0, DCR_MODE_OVERWRITE_ONLY = 1 };
-/* Encoder kernel variant (dcr_plan_opts.encoder); both produce the same
- * frames.  WIDE: many warps per SM, three landing stages each; DEEP: fewer
- * warps with twelve landing stages, faster when a window has fewer chunks
- * than the GPU has warp slots; AUTO picks by window size. */
-enum { DCR_ENCODER_AUTO = 0, DCR_ENCODER_WIDE = 1, DCR_ENCODER_DEEP = 2 };
+/* Encoder kernel variant (dcr_plan_opts.encoder); all produce the same
+ * frames.  WIDE: one warp per chunk, many warps per SM, three landing stages
+ * each; DEEP: one warp per chunk, fewer warps with twelve landing stages;
+ * CTA: one 16-warp CTA per chunk (parallel gather, listing and parse),
+ * faster when a window has fewer chunks than the GPU has warp slots; AUTO
+ * picks WIDE or CTA by window size. */
+enum { DCR_ENCODER_AUTO = 0, DCR_ENCODER_WIDE = 1, DCR_ENCODER_DEEP = 2, DCR_ENCODER_CTA = 3 };
+/* Apply kernel variant (dcr_plan_opts.apply); both apply the same bytes.
+ * WARP: one warp per frame; CTA: one 256-thread CTA per frame (parallel
+ * sequence walk by pointer doubling), faster when windows have fewer frames
+ * than the GPU has warp slots; AUTO picks by the plan's largest window. */
+enum { DCR_APPLY_AUTO = 0, DCR_APPLY_WARP = 1, DCR_APPLY_CTA = 2 };
 /* Block codec of XOR masks (dcr_plan_opts.codec).  LZ4 (frame kind 1) is the
  * default; Snappy (frame kind 5) is the other byte-oriented LZ77 codec the
  * method's pages compare it with (blog, "A strong baseline with the
@@ -142,10 +149,11 @@ typedef struct {
     uint64_t window_bytes;   /* 0 = 16 GiB.  Windows pack whole tensors in
                                 order; a tensor larger than a window is cut at
                                 chunk boundaries.  At most 256 GiB. */
-    uint32_t encoder;        /* DCR_ENCODER_AUTO (0), _WIDE or _DEEP */
+    uint32_t encoder;        /* DCR_ENCODER_AUTO (0), _WIDE, _DEEP or _CTA */
     uint32_t codec;          /* DCR_CODEC_LZ4 (0) or DCR_CODEC_SNAPPY */
     uint32_t flags;          /* 0 or DCR_PLAN_HOST_ONLY */
-    uint32_t reserved[3];
+    uint32_t apply;          /* DCR_APPLY_AUTO (0), _WARP or _CTA */
+    uint32_t reserved[2];
 } dcr_plan_opts;
 
 typedef struct {

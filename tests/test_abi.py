@@ -109,7 +109,13 @@ def test_plan_rejects_unknown_encoder_variant():
     import ctypes
     d = dcr.make_desc("t", 16, 64, 64, dcr.REPLICATED, 1, [0], 0)
     arr = (dcr.TensorDesc * 1)(d)
-    opts = dcr.PlanOpts(0, 3)
+    opts = dcr.PlanOpts(0, dcr.ENCODER_CTA + 1)
     h = ctypes.c_void_p()
     rc = dcr.lib().dcr_plan_build(arr, 1, ctypes.byref(opts), ctypes.byref(h))
     assert rc == dcr.ERR_INVALID and "encoder" in dcr.last_error() and h.value is None
+    opts = dcr.PlanOpts(0, 0, 0, 0, dcr.APPLY_CTA + 1)
+    rc = dcr.lib().dcr_plan_build(arr, 1, ctypes.byref(opts), ctypes.byref(h))
+    assert rc == dcr.ERR_INVALID and "apply" in dcr.last_error() and h.value is None
+    opts = dcr.PlanOpts(0, 0, 0, 2)   # unknown plan flag
+    rc = dcr.lib().dcr_plan_build(arr, 1, ctypes.byref(opts), ctypes.byref(h))
+    assert rc == dcr.ERR_INVALID and "flags" in dcr.last_error() and h.value is None

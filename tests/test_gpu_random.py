@@ -77,7 +77,7 @@ def test_random_workloads_are_valid_for_the_oracle():
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("encoder", ["wide", "deep"])
+@pytest.mark.parametrize("encoder", ["wide", "deep", "cta"])
 @pytest.mark.parametrize("seed", SEEDS)
 def test_random_workload_parity(seed, encoder):
     wl = random_workload(seed)
@@ -88,7 +88,10 @@ def test_random_workload_parity(seed, encoder):
     # the zero-run parse leaves literal (up to ~1.25x there; bit-exact all the same)
     dense_bytes = any(t.elem_bits != 16 and t.frac > 0.1 for t in wl.tensors)
     plan = dcr.Plan(descs_of(wl), window_bytes=wl.window_bytes,
-                    encoder=dcr.ENCODER_WIDE if encoder == "wide" else dcr.ENCODER_DEEP)
+                    encoder={"wide": dcr.ENCODER_WIDE, "deep": dcr.ENCODER_DEEP, "cta": dcr.ENCODER_CTA}[encoder],
+                    # both apply kernels on every route: warp per frame after the wide and CTA
+                    # encoders, CTA per frame after the deep one
+                    apply=dcr.APPLY_CTA if encoder == "deep" else dcr.APPLY_WARP)
     assert plan.info.plan_hash == orc.plan_hash and plan.n_windows == orc.n_windows
     d_old, d_new = to_device(olds), to_device(news)
     exp = orc.receiver_dense(news)

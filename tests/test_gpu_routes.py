@@ -98,7 +98,7 @@ def test_crafted_workload_reaches_every_route():
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("encoder", ["wide", "deep"])
+@pytest.mark.parametrize("encoder", ["wide", "deep", "cta"])
 @pytest.mark.parametrize("mode", ["hybrid", "overwrite"])
 def test_every_route_matches_oracle(mode, encoder):
     torch = pytest.importorskip("torch")
@@ -108,7 +108,10 @@ def test_every_route_matches_oracle(mode, encoder):
     wl, olds, news = crafted()
     orc = oracle.Oracle(wl)
     plan = dcr.Plan(descs_of(wl), window_bytes=wl.window_bytes,
-                    encoder=dcr.ENCODER_WIDE if encoder == "wide" else dcr.ENCODER_DEEP)
+                    encoder={"wide": dcr.ENCODER_WIDE, "deep": dcr.ENCODER_DEEP, "cta": dcr.ENCODER_CTA}[encoder],
+                    # both apply kernels on every route: warp per frame after the wide and CTA
+                    # encoders, CTA per frame after the deep one
+                    apply=dcr.APPLY_CTA if encoder == "deep" else dcr.APPLY_WARP)
     assert plan.info.plan_hash == orc.plan_hash
     d_old, d_new = to_device(olds), to_device(news)
     dm = dcr.MODE_HYBRID if mode == "hybrid" else dcr.MODE_OVERWRITE_ONLY

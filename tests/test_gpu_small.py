@@ -18,11 +18,11 @@ from wl import descs_of, to_device  # noqa: E402
 
 
 class Case:
-    def __init__(self, wl, rule=None, frac=None):
+    def __init__(self, wl, rule=None, frac=None, apply=dcr.APPLY_AUTO):
         self.wl = wl
         self.orc = oracle.Oracle(wl)
         self.olds, self.news = wl.host_arenas(rule_override=rule, frac_override=frac)
-        self.plan = dcr.Plan(descs_of(wl), window_bytes=wl.window_bytes)
+        self.plan = dcr.Plan(descs_of(wl), window_bytes=wl.window_bytes, apply=apply)
         self.d_old, self.d_new = to_device(self.olds), to_device(self.news)
         self.exp = self.orc.receiver_dense(self.news)
         self.start = self.orc.receiver_dense(self.olds)
@@ -45,9 +45,12 @@ class Case:
         return t.cpu().numpy()[:self.exp.size]
 
 
-@pytest.fixture(scope="module", params=[1, 2, 3, 4, 5])
+# every small twin with each apply kernel: one warp per frame, one CTA per frame
+@pytest.fixture(scope="module", params=[(n, a) for n in (1, 2, 3, 4, 5) for a in ("warp", "cta")],
+                ids=lambda p: "%d-%s" % p)
 def case(request):
-    return Case(configs.mini(request.param))
+    n, a = request.param
+    return Case(configs.mini(n), apply=dcr.APPLY_WARP if a == "warp" else dcr.APPLY_CTA)
 
 
 def test_generator_twins_agree():
@@ -425,7 +428,7 @@ def test_tiny_and_ragged_tensors(shape):
     _flip_case(bits, rows, cols, flips)
 
 
-@pytest.mark.parametrize("encoder", [dcr.ENCODER_WIDE, dcr.ENCODER_DEEP])
+@pytest.mark.parametrize("encoder", [dcr.ENCODER_WIDE, dcr.ENCODER_DEEP, dcr.ENCODER_CTA])
 def test_changes_near_the_end_of_a_chunk(encoder):
     # chunk i: one change i + 1 bytes before its end (the block's end rules:
     # last five bytes literal, no match starting in the last twelve), chunks

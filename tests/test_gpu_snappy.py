@@ -76,7 +76,7 @@ def test_snappy_random_workloads(seed):
     _check(wl, olds, news, size_bar=1.15 if sparse else None)
 
 
-@pytest.mark.parametrize("encoder", [dcr.ENCODER_WIDE, dcr.ENCODER_DEEP])
+@pytest.mark.parametrize("encoder", [dcr.ENCODER_WIDE, dcr.ENCODER_DEEP, dcr.ENCODER_CTA])
 def test_snappy_every_route(encoder):
     wl, olds, news = crafted()
     _check(wl, olds, news, encoder=encoder, size_bar=None)   # crafted dense chunks

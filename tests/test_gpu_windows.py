@@ -17,7 +17,7 @@ import bit_exact_xor_gb300 as dcr  # noqa: E402
 from wl import descs_of, to_device  # noqa: E402
 
 
-@pytest.mark.parametrize("encoder", [dcr.ENCODER_WIDE, dcr.ENCODER_DEEP])
+@pytest.mark.parametrize("encoder", [dcr.ENCODER_WIDE, dcr.ENCODER_DEEP, dcr.ENCODER_CTA])
 def test_oversized_tensor_windows(encoder):
     wl = configs.oversized_window()
     orc = oracle.Oracle(wl)
