@@ -66,8 +66,16 @@ struct EncScratch {
     uint32_t n_spill;        // chunks whose frame body did not fit its slot
     uint32_t spill_ticket;   // restream pass: next spill record
     uint32_t n_deep;         // spill records left to the spill kernel
-    uint32_t pad;
+    uint32_t scan_ticket;    // scan_kernel: next tile
 };
+
+// scan_kernel tiles: 8192 chunks each.  Per tile, a status word: bits 62-63
+// 1 = the tile's own sum published, 2 = the inclusive prefix through the
+// tile published; bits 0-61 the value (frames << 40 | frame bytes).
+constexpr uint32_t kScanTile = 8192;
+constexpr uint64_t kTileAgg = 1ull << 62;
+constexpr uint64_t kTileInc = 2ull << 62;
+constexpr uint64_t kTileValMask = (1ull << 62) - 1;
 
 // The encoder writes each chunk's frame into a slot of its own in device
 // scratch (kEncSlot bytes per chunk of the window); a compaction pass copies
@@ -207,6 +215,8 @@ struct dcr_plan {
     uint32_t* d_fsize = nullptr;
     dcr::SpillRec* d_spill = nullptr;  // max_window_chunks
     uint32_t* d_deep = nullptr;        // max_window_chunks spill record ids
+    uint64_t* d_tiles = nullptr;       // scan_kernel tile status words
+    uint32_t max_tiles = 0;
     uint8_t* d_slots = nullptr;        // max_window_chunks * kEncSlot frame slots
     void* h_enc = nullptr;  // pinned mirror of the scratch head
     // kernel timing (dcr_plan_set_profiling)

@@ -1057,28 +1057,48 @@ __global__ void __launch_bounds__(kMThreads, 4) restream_kernel(EncArgs A)
 }
 
 // ---------------------------------------------------------- scan / copy --
-// Frame offsets from the sizes (one CTA), totals and the stream header.
-__global__ void __launch_bounds__(1024) scan_kernel(EncArgs A, uint64_t plan_hash, uint64_t base_v,
+// Frame offsets from the sizes, totals and the stream header.  One CTA per
+// tile of kScanTile chunks, tiles taken in ticket order; a tile's offset
+// comes from a decoupled look-back over the status words of the tiles
+// before it (each already taken by a running CTA, since tickets go in
+// order, so every wait ends; a wait that still runs past its limit reports
+// DCR_ERR_TIMEOUT).  The CTA of the last tile writes the totals and header.
+constexpr uint32_t kScanSpin = 1u << 22;
+
+__device__ __forceinline__ uint64_t ld_acquire64(const uint64_t* p)
+{
+    uint64_t v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__global__ void __launch_bounds__(1024) scan_kernel(EncArgs A, uint64_t* tiles, uint64_t plan_hash, uint64_t base_v,
                                                    uint64_t target_v, uint32_t window)
 {
     __shared__ unsigned long long wsum[32];
+    __shared__ uint32_t s_tile;
+    __shared__ unsigned long long s_excl;
+    __shared__ int s_ok;
     const uint32_t n = A.chunk_count;
-    const uint32_t per = (n + 1023) / 1024;
-    const uint32_t b = threadIdx.x * per, e = b + per < n ? b + per : n;
+    const uint32_t ntiles = n ? (n + kScanTile - 1) / kScanTile : 1u;
+    if (threadIdx.x == 0) s_tile = atomicAdd(&A.sc->scan_ticket, 1u);
+    __syncthreads();
+    const uint32_t tile = s_tile;
+    if (tile >= ntiles) return;
+    constexpr uint32_t per = kScanTile / 1024;
+    const uint32_t b0 = tile * kScanTile + threadIdx.x * per;
+    const uint32_t e = b0 + per < n ? b0 + per : (b0 < n ? n : b0);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     auto rec = [](uint32_t fs) -> unsigned long long {
         fs &= ~kSpilled;
         return fs ? ((1ull << kLbFrameShift) | fs) : 0ull;
     };
-    // sizes read eight at a time (independent loads)
+    uint32_t v[per];
+#pragma unroll
+    for (uint32_t j = 0; j < per; ++j) v[j] = b0 + j < e ? A.fsize[b0 + j] : 0u;
     unsigned long long sum = 0;
-    for (uint32_t k0 = b; k0 < e; k0 += 8) {
-        uint32_t v[8];
 #pragma unroll
-        for (uint32_t j = 0; j < 8; ++j) v[j] = k0 + j < e ? A.fsize[k0 + j] : 0u;
-#pragma unroll
-        for (uint32_t j = 0; j < 8; ++j) sum += rec(v[j]);
-    }
+    for (uint32_t j = 0; j < per; ++j) sum += rec(v[j]);
     // block exclusive scan of the per-thread sums
     unsigned long long incl = sum;
 #pragma unroll
@@ -1096,20 +1116,43 @@ __global__ void __launch_bounds__(1024) scan_kernel(EncArgs A, uint64_t plan_has
             if (lane >= d) wi += o;
         }
         wsum[lane] = wi - w;
-    }
-    __syncthreads();
-    unsigned long long run = wsum[warp] + incl - sum;
-    for (uint32_t k0 = b; k0 < e; k0 += 8) {
-        uint32_t v[8];
-#pragma unroll
-        for (uint32_t j = 0; j < 8; ++j) v[j] = k0 + j < e ? A.fsize[k0 + j] : 0u;
-#pragma unroll
-        for (uint32_t j = 0; j < 8; ++j) {
-            if (k0 + j < e) A.lb[k0 + j] = run;
-            run += rec(v[j]);
+        if (lane == 31) {   // the tile's sum: publish it, then look back for its offset
+            const unsigned long long agg = wi;
+            int ok = 1;
+            unsigned long long excl = 0;
+            if (tile == 0) {
+                atomicExch(reinterpret_cast<unsigned long long*>(&tiles[0]), kTileInc | agg);
+            } else {
+                atomicExch(reinterpret_cast<unsigned long long*>(&tiles[tile]), kTileAgg | agg);
+                for (int64_t j = int64_t(tile) - 1; j >= 0 && ok; --j) {
+                    uint64_t s = ld_acquire64(&tiles[j]);
+                    for (uint32_t spin = 0; !(s >> 62) && ok; ++spin) {
+                        if (spin > kScanSpin || *(volatile int32_t*)&A.sc->err) ok = 0;
+                        else {
+                            __nanosleep(64);
+                            s = ld_acquire64(&tiles[j]);
+                        }
+                    }
+                    if (!ok) break;
+                    excl += s & kTileValMask;
+                    if ((s >> 62) == 2) break;
+                }
+                if (ok) atomicExch(reinterpret_cast<unsigned long long*>(&tiles[tile]), kTileInc | (excl + agg));
+                else atomicCAS(reinterpret_cast<int*>(&A.sc->err), 0, DCR_ERR_TIMEOUT);
+            }
+            s_excl = excl;
+            s_ok = ok;
         }
     }
-    if (threadIdx.x == 1023) {
+    __syncthreads();
+    if (!s_ok) return;
+    unsigned long long run = s_excl + wsum[warp] + incl - sum;
+#pragma unroll
+    for (uint32_t j = 0; j < per; ++j) {
+        if (b0 + j < e) A.lb[b0 + j] = run;
+        run += rec(v[j]);
+    }
+    if (tile == ntiles - 1 && threadIdx.x == 1023) {   // run: the window's frames and bytes
         const uint64_t fbytes = run & kLbByteMask, nframes = run >> kLbFrameShift;
         const uint64_t total = kStreamHdr + fbytes + 8 * nframes;
         A.sc->total = total;
@@ -1366,7 +1409,7 @@ constexpr int kEWarps = 8;
 constexpr int kEThreads = 32 * kEWarps;
 constexpr int kESlice = kChunk / kEWarps;           // 8 KiB per warp
 constexpr int kEVPL = kESlice / 16 / 32;            // 16 vectors per lane
-constexpr int kEBatch = 4;                          // ... loaded four at a time
+constexpr int kEBatch = 2;                          // ... two at a time, the next two in flight
 constexpr int kEWarpCap = 1536;                     // events a warp's region holds
 constexpr int kECap = kEWarpCap * kEWarps;
 constexpr int kEGroups = kECap / 32 + 1;
@@ -1395,13 +1438,17 @@ struct __align__(16) CtaSmem {
 struct SliceSrc {
     const uint16_t* pos;
     const uint8_t* val;
-    const uint32_t* base;
+    int base[kEWarps];   // events before each slice (in registers)
     __device__ __forceinline__ int slot(int e) const
     {
-        int w = 0;
+        int w = 0, b = 0;
 #pragma unroll
-        for (int i = 1; i < kEWarps; ++i) w += e >= int(base[i]);
-        return w * kEWarpCap + e - int(base[w]);
+        for (int i = 1; i < kEWarps; ++i)
+            if (e >= base[i]) {
+                w = i;
+                b = base[i];
+            }
+        return w * kEWarpCap + e - b;
     }
     __device__ __forceinline__ int at(int e) const { return pos[slot(e)]; }
     template <class Put>
@@ -1451,8 +1498,8 @@ __global__ void __launch_bounds__(kEThreads, 4) encode_cta_kernel(EncArgs A)
     const int nvec = raw >> 4;
     uint32_t changed = 0, n = 0;
     int cur = 0;
-    for (int j0 = 0; j0 < kEVPL; j0 += kEBatch) {
-        uint4 o[kEBatch], nw[kEBatch];
+    // vectors j0 .. j0 + kEBatch - 1 of this lane (zero past the chunk)
+    auto load = [&](int j0, uint4* o, uint4* nw) {
 #pragma unroll
         for (int j = 0; j < kEBatch; ++j) {
             const int v = v0 + (j0 + j) * 32 + lane;
@@ -1467,6 +1514,12 @@ __global__ void __launch_bounds__(kEThreads, 4) encode_cta_kernel(EncArgs A)
                 nw[j] = ld_stream(A.news[r] + a);
             }
         }
+    };
+    uint4 o[kEBatch], nw[kEBatch];
+    load(0, o, nw);
+    for (int j0 = 0; j0 < kEVPL; j0 += kEBatch) {
+        uint4 po[kEBatch], pn[kEBatch];   // the next batch, in flight while this one is listed
+        if (j0 + kEBatch < kEVPL) load(j0 + kEBatch, po, pn);
 #pragma unroll
         for (int j = 0; j < kEBatch; ++j) {
             const uint4 m = xor4(o[j], nw[j]);
@@ -1474,9 +1527,19 @@ __global__ void __launch_bounds__(kEThreads, 4) encode_cta_kernel(EncArgs A)
             if (cd.bits == 16) changed += __popc((z | (z >> 1)) & 0x5555u);
             else if (cd.bits == 8) changed += __popc(z);
             else changed += nibbles_nz(m.x) + nibbles_nz(m.y) + nibbles_nz(m.z) + nibbles_nz(m.w);
+            // warp prefix of the per-lane counts: two ballots when no lane has
+            // more than one
             const uint32_t c = __popc(z);
-            const uint32_t incl = warp_incl_sum(c, lane);
-            const uint32_t tot = __shfl_sync(kFull, incl, 31);
+            uint32_t incl, tot;
+            if (__ballot_sync(kFull, c > 1) == 0) {
+                const uint32_t any = __ballot_sync(kFull, c != 0);
+                incl = __popc(any & lt) + c;
+                tot = __popc(any);
+            } else {
+                incl = warp_incl_sum(c, lane);
+                tot = __shfl_sync(kFull, incl, 31);
+            }
+            if (tot == 0) continue;
             uint32_t at = n + incl - c;
             const uint32_t x = uint32_t(v0 + (j0 + j) * 32 + lane) << 4;
             for (uint32_t b = z; b; b &= b - 1) {
@@ -1488,6 +1551,11 @@ __global__ void __launch_bounds__(kEThreads, 4) encode_cta_kernel(EncArgs A)
                 ++at;
             }
             n += tot;
+        }
+#pragma unroll
+        for (int j = 0; j < kEBatch; ++j) {
+            o[j] = po[j];
+            nw[j] = pn[j];
         }
     }
     changed = __reduce_add_sync(kFull, changed);
@@ -1526,7 +1594,9 @@ __global__ void __launch_bounds__(kEThreads, 4) encode_cta_kernel(EncArgs A)
         A.fsize[k] = fsz | kSpilled;
         A.spill[atomicAdd(&A.sc->n_spill, 1u)] = SpillRec{k, kind, body_len, 0u, chunk_changed, {0u, 0u, 0u}};
     };
-    const SliceSrc S{C.u.ev.pos, C.u.ev.val, C.base};
+    SliceSrc S{C.u.ev.pos, C.u.ev.val, {}};
+#pragma unroll
+    for (int w = 0; w < kEWarps; ++w) S.base[w] = int(C.base[w]);
     const int full = int(total_ev / 32), G = full + 1;   // full groups, then the final one (with the end event)
     auto group = [&](int g, Parse& P, uint8_t* out, uint32_t cap, bool emit, bool* over, bool* bad) {
         P.prev = g ? S.at(32 * g - 1) : -1;
@@ -1763,7 +1833,10 @@ int launch_size(const dcr_plan* P, EncArgs& A, uint64_t plan_hash, uint64_t base
     else
         encode_kernel<kNS, CodecLz4><<<grid, kMThreads, kMainSmem, s>>>(A);
     if (P->profiling) cudaEventRecord(P->ev[1], s);
-    scan_kernel<<<1, 1024, 0, s>>>(A, plan_hash, base_v, target_v, window);
+    const uint32_t ntiles = A.chunk_count ? (A.chunk_count + kScanTile - 1) / kScanTile : 1u;
+    e = cudaMemsetAsync(P->d_tiles, 0, ntiles * sizeof(uint64_t), s);
+    if (e != cudaSuccess) return cuda_error(e, "scan tile reset");
+    scan_kernel<<<ntiles, 1024, 0, s>>>(A, P->d_tiles, plan_hash, base_v, target_v, window);
     e = cudaGetLastError();
     return e == cudaSuccess ? DCR_OK : cuda_error(e, "encode launch");
 }

@@ -388,7 +388,9 @@ extern "C" int dcr_plan_build(const dcr_tensor_desc* tensors, size_t n, const dc
     size_t lb_bytes = (P->max_window_chunks * 8 + 255) / 256 * 256;
     size_t fs_bytes = (P->max_window_chunks * 4 + 255) / 256 * 256;
     size_t sp_bytes = (P->max_window_chunks * sizeof(SpillRec) + 255) / 256 * 256;
-    size_t total = P->enc_head_bytes + lb_bytes + fs_bytes + sp_bytes + P->max_window_chunks * 4 + 256;
+    P->max_tiles = uint32_t((P->max_window_chunks + kScanTile - 1) / kScanTile + 1);
+    size_t dp_bytes = (P->max_window_chunks * 4 + 255) / 256 * 256;
+    size_t total = P->enc_head_bytes + lb_bytes + fs_bytes + sp_bytes + dp_bytes + P->max_tiles * 8ull + 256;
     if ((e = cudaMalloc(&P->d_enc, total)) != cudaSuccess ||
         (e = cudaMalloc(&P->d_slots, P->max_window_chunks * size_t(kEncSlot))) != cudaSuccess ||
         (e = cudaMallocHost(&P->h_enc, P->enc_head_bytes)) != cudaSuccess) {
@@ -401,6 +403,7 @@ extern "C" int dcr_plan_build(const dcr_tensor_desc* tensors, size_t n, const dc
     P->d_spill = reinterpret_cast<SpillRec*>(static_cast<char*>(P->d_enc) + P->enc_head_bytes + lb_bytes +
                                              fs_bytes);
     P->d_deep = reinterpret_cast<uint32_t*>(reinterpret_cast<char*>(P->d_spill) + sp_bytes);
+    P->d_tiles = reinterpret_cast<uint64_t*>(reinterpret_cast<char*>(P->d_deep) + dp_bytes);
     if ((rc = encode_kernel_config(&P->kc)) || (rc = apply_kernel_config(&P->kc))) {
         plan_free_device(P);
         delete P;
