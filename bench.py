@@ -14,7 +14,7 @@ per refit) are larger than L2; workloads small enough to stay in L2 get a
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
                   [--workload moe|dense|single|gqa|sweep] [--frac F]
-                  [--moe-layers L] [--window-mb M] [--codec lz4|snappy]
+                  [--moe-layers L] [--window-mb M] [--codec lz4|snappy] [--overflow-kib K]
                   [--pipeline] [--abort-retry] [--shard] [--no-e2e] [--no-cpu-baseline]
 
 Prints one JSON line.  --impl reference times the CPU oracle (the
@@ -338,7 +338,8 @@ def run_gpu(args):
     wl = build_workload(args.workload, args.frac, args.moe_layers)
     N = wl.canonical_bytes
     plan = dcr.Plan(descs_of(wl), window_bytes=(args.window_mb << 20) or wl.window_bytes,
-                    codec=dcr.CODEC_SNAPPY if args.codec == "snappy" else dcr.CODEC_LZ4)
+                    codec=dcr.CODEC_SNAPPY if args.codec == "snappy" else dcr.CODEC_LZ4,
+                    overflow_kib=dcr.NO_OVERFLOW if args.overflow_kib < 0 else args.overflow_kib)
     plan.set_profiling(True)
     olds, news = wl.device_arenas(torch)
     target = torch.empty(max(plan.info.recv_bytes, wl.recv_bytes), dtype=torch.uint8, device=dev)
@@ -749,6 +750,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--window-mb", type=int, default=0, help="window size in MiB (0: the workload's)")
     ap.add_argument("--codec", default="lz4", choices=["lz4", "snappy"], help="block codec of the XOR masks")
+    ap.add_argument("--overflow-kib", type=int, default=0,
+                    help="encoder overflow heap in KiB (0: one eighth of the window, -1: none)")
     ap.add_argument("--abort-retry", action="store_true",
                     help="also time refits aborted at half the frames and completed by the overwrite-only retry")
     ap.add_argument("--pipeline", action="store_true",

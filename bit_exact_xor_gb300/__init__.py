@@ -29,6 +29,7 @@ ENCODER_AUTO, ENCODER_WIDE, ENCODER_DEEP, ENCODER_CTA = 0, 1, 2, 3
 APPLY_AUTO, APPLY_WARP, APPLY_CTA = 0, 1, 2
 CODEC_LZ4, CODEC_SNAPPY = 0, 1
 PLAN_HOST_ONLY = 1
+NO_OVERFLOW = 0xFFFFFFFF
 MAX_PARTS = 65536
 
 
@@ -53,7 +54,8 @@ class TensorDesc(ctypes.Structure):
 
 class PlanOpts(ctypes.Structure):
     _fields_ = [("window_bytes", ctypes.c_uint64), ("encoder", ctypes.c_uint32), ("codec", ctypes.c_uint32),
-                ("flags", ctypes.c_uint32), ("apply", ctypes.c_uint32), ("reserved", ctypes.c_uint32 * 2)]
+                ("flags", ctypes.c_uint32), ("apply", ctypes.c_uint32), ("overflow_kib", ctypes.c_uint32),
+                ("reserved", ctypes.c_uint32)]
 
 
 class PartInfo(ctypes.Structure):
@@ -188,10 +190,10 @@ def check(rc):
 class Plan:
     """dcr_plan_build over a list of TensorDesc."""
 
-    def __init__(self, descs, window_bytes=0, encoder=0, codec=0, host_only=False, apply=0):
+    def __init__(self, descs, window_bytes=0, encoder=0, codec=0, host_only=False, apply=0, overflow_kib=0):
         arr = (TensorDesc * len(descs))(*descs)
         self._names = [d.name for d in descs]
-        opts = PlanOpts(window_bytes, encoder, codec, PLAN_HOST_ONLY if host_only else 0, apply)
+        opts = PlanOpts(window_bytes, encoder, codec, PLAN_HOST_ONLY if host_only else 0, apply, overflow_kib)
         h = ctypes.c_void_p()
         check(lib().dcr_plan_build(arr, len(descs), ctypes.byref(opts), ctypes.byref(h)))
         self.h = h

@@ -67,6 +67,7 @@ struct EncScratch {
     uint32_t spill_ticket;   // restream pass: next spill record
     uint32_t n_deep;         // spill records left to the spill kernel
     uint32_t scan_ticket;    // scan_kernel: next tile
+    uint64_t heap_top;       // bytes reserved in the overflow heap
 };
 
 // scan_kernel tiles: 8192 chunks each.  Per tile, a status word: bits 62-63
@@ -81,7 +82,12 @@ constexpr uint64_t kTileValMask = (1ull << 62) - 1;
 // scratch (kEncSlot bytes per chunk of the window); a compaction pass copies
 // the slots into the stream once the frame offsets are known.
 constexpr uint32_t kEncSlot = 6144;
-constexpr uint32_t kSpilled = 1u << 31;   // frame-size flag: body not in the slot
+constexpr uint32_t kSpilled = 1u << 31;   // frame-size flag: body not in the slot (write pass re-derives it)
+constexpr uint32_t kHeap = 1u << 30;      // frame-size flag: the frame goes on past the slot, in the heap
+constexpr uint32_t kFrameSizeMask = kHeap - 1;
+// A warp's overflow buffer: the part of an XOR block past its slot, moved
+// to the heap at the chunk's end.
+constexpr uint32_t kOvfBytes = 65536;
 
 // A chunk whose frame is sized but whose body did not fit its slot: a
 // restream pass re-derives it and writes the frame into the stream (the
@@ -128,6 +134,8 @@ struct KernelConfig {
     int num_sms = 0;
     int enc_blocks_per_sm = 0;
     int enc_deep_blocks_per_sm = 0;
+    int enc_warps_per_block = 0;        // one chunk per warp: the wide and deep variants
+    int enc_deep_warps_per_block = 0;
     int restream_blocks_per_sm = 0;
     int spill_blocks_per_sm = 0;
     int apply_blocks_per_sm = 0;
@@ -216,6 +224,11 @@ struct dcr_plan {
     dcr::SpillRec* d_spill = nullptr;  // max_window_chunks
     uint32_t* d_deep = nullptr;        // max_window_chunks spill record ids
     uint64_t* d_tiles = nullptr;       // scan_kernel tile status words
+    uint8_t* d_ovf = nullptr;          // per-warp overflow buffers of the one-warp encoders
+    uint8_t* d_heap = nullptr;         // rests of bodies past their slots
+    uint64_t heap_bytes = 0;
+    uint64_t* d_heapoff = nullptr;     // max_window_chunks heap offsets
+    mutable bool overflow_seen = false;   // an encode on this plan had a body outgrow its slot
     uint32_t max_tiles = 0;
     uint8_t* d_slots = nullptr;        // max_window_chunks * kEncSlot frame slots
     void* h_enc = nullptr;  // pinned mirror of the scratch head

@@ -109,6 +109,10 @@ struct EncArgs {
     uint64_t frame_base;       // index entry of that frame: frame_base + o
     uint64_t* index;           // the frames' index entries (null: at the end of `payload`)
     uint32_t header;
+    uint8_t* ovf;              // per-warp overflow buffers (kOvfBytes each; null: none)
+    uint8_t* heap;             // rests of bodies past their slots
+    uint64_t heap_cap;
+    uint64_t* heapoff;         // per chunk: where its rest sits in the heap
     EncScratch* sc;
     unsigned long long* counts;
     uint64_t* lb;              // frame offsets: frames before << 40 | bytes before
@@ -393,6 +397,23 @@ __device__ __forceinline__ void report(EncScratch* sc, int code)
 }
 
 // ------------------------------------------------------------------ parse --
+// Where a block's bytes go: Sink to one buffer; SplitSink bytes [0, split)
+// to a, the rest to b (the slot, then a warp's overflow buffer).
+struct Sink {
+    uint8_t* a;
+    __device__ __forceinline__ void put(uint32_t o, uint32_t v) const { a[o] = uint8_t(v); }
+};
+struct SplitSink {
+    uint8_t* a;
+    uint8_t* b;
+    uint32_t split;
+    __device__ __forceinline__ void put(uint32_t o, uint32_t v) const
+    {
+        if (o < split) a[o] = uint8_t(v);
+        else b[o - split] = uint8_t(v);
+    }
+};
+
 // Carried parse state between groups of 32 events.
 struct Parse {
     int prev;                  // last non-zero byte so far (-1: before the chunk)
@@ -442,11 +463,11 @@ struct MaskSrc {
 // zero run of the earlier groups, so every lane decides with carried state
 // only; the literal start of a match is the end of the nearest earlier match,
 // found with one ballot.  Sizes add up in P.out.  With emit, the sequences
-// are written to out[0, cap); *over is set when one does not fit and *bad
+// are written to out at [0, cap); *over is set when one does not fit and *bad
 // when sizing and writing disagree.
-template <class Codec, class Src>
+template <class Codec, class Src, class Out = Sink>
 __device__ __forceinline__ void parse_group(const Src& S, int e0, int cnt, bool final, int raw, Parse& P,
-                                            uint8_t* out, uint32_t cap, bool emit, int lane, bool* over,
+                                            const Out& out, uint32_t cap, bool emit, int lane, bool* over,
                                             bool* bad)
 {
     const int total = cnt + (final ? 1 : 0);
@@ -508,7 +529,7 @@ __device__ __forceinline__ void parse_group(const Src& S, int e0, int cnt, bool 
         if ((has || last) && !fits) *over = true;
         if ((has || last) && fits) {
             uint32_t o = o0;
-            auto put = [&](uint32_t v) { out[o++] = uint8_t(v); };
+            auto put = [&](uint32_t v) { out.put(o++, v); };
             bool ok = true;
             if (has)
                 Codec::emit_seq(put, uint32_t(ms - lit), [&](decltype(put)& p) { ok &= S.lits(lit, ms, lev, e, p); },
@@ -574,9 +595,9 @@ __device__ __forceinline__ void gather_bytes(const EncArgs& A, const Seg* segs, 
 
 // The stream loop of any chunk (overwrite records, 4-bit elements, pieces
 // that are not 16-byte aligned); stream_fast below is the common case.
-template <int NS, class Codec>
+template <int NS, class Codec, class Out>
 __device__ __forceinline__ void stream_chunk(const EncArgs& A, WarpSmemT<NS>& W, const ChunkDesc& cd, const Seg* segs,
-                                             int lane, uint8_t* body, uint32_t cap, uint8_t* vals, int ncap,
+                                             int lane, const Out& body, uint32_t cap, uint8_t* vals, int ncap,
                                              uint32_t& changed, Parse& P, int& tail, int& np, int& units,
                                              bool& spill, bool& bad)
 {
@@ -675,7 +696,7 @@ __device__ __forceinline__ void stream_chunk(const EncArgs& A, WarpSmemT<NS>& W,
                 const uint32_t i = __ffs(b) - 1;
                 if (r < ncap) {
                     const uint32_t u = (x + i) / ub;
-                    *reinterpret_cast<uint16_t*>(body + 4 + 2 * r) = uint16_t(u);
+                    *reinterpret_cast<uint16_t*>(body.a + 4 + 2 * r) = uint16_t(u);
                     vals[r * int(ub)] = uint8_t(byte_of32(n0, n1, i));
                     if (ub == 2) vals[r * 2 + 1] = uint8_t(byte_of32(n0, n1, i + 1));
                 }
@@ -731,9 +752,9 @@ __device__ __forceinline__ void stream_chunk(const EncArgs& A, WarpSmemT<NS>& W,
 // modulo NS, this lane's copy and read addresses are worked out once, the
 // warp looks up the piece of a step once, and the last groups are parsed
 // after the loop.
-template <int kBits, int NS, class Codec>
+template <int kBits, int NS, class Codec, class Out>
 __device__ __forceinline__ void stream_fast(const EncArgs& A, WarpSmemT<NS>& W, const ChunkDesc& cd, const Seg* segs,
-                                            int lane, uint8_t* body, uint32_t cap, uint32_t& changed, Parse& P,
+                                            int lane, const Out& body, uint32_t cap, uint32_t& changed, Parse& P,
                                             int& tail, int& np, bool& spill, bool& bad)
 {
     const int raw = int(cd.raw_len);
@@ -856,9 +877,18 @@ __device__ __forceinline__ void stream_fast(const EncArgs& A, WarpSmemT<NS>& W, 
     }
 }
 
-template <int NS, class Codec>
-__device__ __forceinline__ void encode_chunk(const EncArgs& A, WarpSmemT<NS>& W, uint32_t k, int lane)
+// kOvf (ovf: this warp's overflow buffer of kOvfBytes): an XOR block that
+// outgrows the slot goes on there, and at the chunk's end its rest moves to
+// an exact reservation in the plan's heap; a chunk for which the heap has no
+// room left is re-derived by the write pass instead (as every outgrown body
+// is without kOvf).
+template <int NS, class Codec, bool kOvf = false>
+__device__ __forceinline__ void encode_chunk(const EncArgs& A, WarpSmemT<NS>& W, uint32_t k, int lane,
+                                             uint8_t* ovf)
 {
+    // whether the heap has room left, read alongside the chunk's descriptor
+    unsigned long long heap_top = 0;
+    if constexpr (kOvf) heap_top = *reinterpret_cast<volatile unsigned long long*>(&A.sc->heap_top);
     const ChunkDesc cd = A.chunks[A.chunk_begin + k];
     const int raw = int(cd.raw_len);
     const int nseg = int(cd.src_count);
@@ -886,13 +916,25 @@ __device__ __forceinline__ void encode_chunk(const EncArgs& A, WarpSmemT<NS>& W,
         auto put = [&](uint32_t v) { body[o++] = uint8_t(v); };
         Codec::emit_preamble(put, uint32_t(raw));
     }
-    if (!overwrite && vec && cd.bits == 16)
-        stream_fast<16, NS, Codec>(A, W, cd, segs, lane, body, kSlotBody, changed, P, tail, np, spill, bad);
-    else if (!overwrite && vec && cd.bits == 8)
-        stream_fast<8, NS, Codec>(A, W, cd, segs, lane, body, kSlotBody, changed, P, tail, np, spill, bad);
-    else
-        stream_chunk<NS, Codec>(A, W, cd, segs, lane, body, kSlotBody, vstage, ncap, changed, P, tail, np, units,
-                                spill, bad);
+    // XOR blocks may go on past the slot, into the overflow buffer, while
+    // the heap has room left
+    bool deep_out = false;
+    if constexpr (kOvf) deep_out = !overwrite && __shfl_sync(kFull, heap_top, 0) < A.heap_cap;
+    auto run = [&](const auto& sink, uint32_t cap) {
+        if (!overwrite && vec && cd.bits == 16)
+            stream_fast<16, NS, Codec>(A, W, cd, segs, lane, sink, cap, changed, P, tail, np, spill, bad);
+        else if (!overwrite && vec && cd.bits == 8)
+            stream_fast<8, NS, Codec>(A, W, cd, segs, lane, sink, cap, changed, P, tail, np, spill, bad);
+        else
+            stream_chunk<NS, Codec>(A, W, cd, segs, lane, sink, cap, vstage, ncap, changed, P, tail, np, units,
+                                    spill, bad);
+    };
+    if constexpr (kOvf) {
+        if (deep_out) run(SplitSink{body, ovf, kSlotBody}, kSlotBody + kOvfBytes);
+        else run(Sink{body}, kSlotBody);
+    } else {
+        run(Sink{body}, kSlotBody);
+    }
     changed = __reduce_add_sync(kFull, changed);
     if (lane == 0 && changed) {
         atomicAdd(&A.counts[cd.tensor], (unsigned long long)changed);
@@ -924,6 +966,26 @@ __device__ __forceinline__ void encode_chunk(const EncArgs& A, WarpSmemT<NS>& W,
     }
     if (__any_sync(kFull, bad) && lane == 0) report(A.sc, DCR_ERR_CORRUPT);
     const uint32_t fsz = kind ? (kFrameHdr + body_len + 15) / 16 * 16 : 0u;
+    // a block past the slot: its rest and the frame's padding (a multiple of
+    // 16 bytes) from the overflow buffer to the heap
+    bool heaped = false;
+    if (kOvf && kind && staged && fsz > kEncSlot) {   // (deep_out: only then can a staged body pass the slot)
+        const uint32_t hl = fsz - kEncSlot, rest = body_len - kSlotBody;
+        unsigned long long off = 0;
+        if (lane == 0) off = atomicAdd(reinterpret_cast<unsigned long long*>(&A.sc->heap_top), (unsigned long long)hl);
+        off = __shfl_sync(kFull, off, 0);
+        if (off + hl <= A.heap_cap) {
+            uint8_t* h = A.heap + off;
+            for (uint32_t v = lane; v < hl / 16; v += 32)
+                reinterpret_cast<uint4*>(h)[v] = reinterpret_cast<const uint4*>(ovf)[v];
+            __syncwarp();
+            for (uint32_t i = rest + lane; i < hl; i += 32) h[i] = 0;
+            if (lane == 0) A.heapoff[k] = off;
+            heaped = true;
+        } else {
+            staged = false;   // the heap is full: the write pass re-derives this body
+        }
+    }
     if (kind && !staged) {
         if (lane == 0) {
             A.fsize[k] = fsz | kSpilled;
@@ -940,14 +1002,15 @@ __device__ __forceinline__ void encode_chunk(const EncArgs& A, WarpSmemT<NS>& W,
         if (lane == 0) *reinterpret_cast<uint32_t*>(body) = nu;
     }
     if (kind) {
-        for (uint32_t i = kFrameHdr + body_len + lane; i < fsz; i += 32) slot[i] = 0;   // padding
+        const uint32_t in_slot = fsz < kEncSlot ? fsz : kEncSlot;
+        for (uint32_t i = kFrameHdr + body_len + lane; i < in_slot; i += 32) slot[i] = 0;   // padding
         if (lane == 0) write_header(slot, kind, cd.bits, A.chunk_begin + k, uint32_t(raw), body_len, changed);
     }
-    if (lane == 0) A.fsize[k] = fsz;
-    __syncwarp();   // the ring is reused by the next chunk
+    if (lane == 0) A.fsize[k] = fsz | (heaped ? kHeap : 0u);
+    __syncwarp();   // the ring and the overflow buffer are reused by the next chunk
 }
 
-template <int NS, class Codec>
+template <int NS, class Codec, bool kOvf>
 __global__ void __launch_bounds__(kMThreads, 4) encode_kernel(EncArgs A)
 {
     extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -961,7 +1024,9 @@ __global__ void __launch_bounds__(kMThreads, 4) encode_kernel(EncArgs A)
         }
         k = __shfl_sync(kFull, k, 0);
         if (k >= A.chunk_count) break;
-        encode_chunk<NS, Codec>(A, W, k, lane);
+        uint8_t* ovf = kOvf ? A.ovf + size_t(blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)) * kOvfBytes
+                            : nullptr;
+        encode_chunk<NS, Codec, kOvf>(A, W, k, lane, ovf);
     }
 }
 
@@ -1003,15 +1068,16 @@ __device__ __forceinline__ void restream_chunk(const EncArgs& A, WarpSmem& W, ui
         auto put = [&](uint32_t v) { body[o++] = uint8_t(v); };
         Codec::emit_preamble(put, cd.raw_len);
     }
+    const Sink sink{body};
     if (R.kind == kOverwrite)
-        stream_chunk<kNS, Codec>(A, W, cd, segs, lane, body, R.body_len, body + voff, int(nu), changed, P, tail, np,
+        stream_chunk<kNS, Codec>(A, W, cd, segs, lane, sink, R.body_len, body + voff, int(nu), changed, P, tail, np,
                                  units, spill, bad);
     else if (vec && cd.bits == 16)
-        stream_fast<16, kNS, Codec>(A, W, cd, segs, lane, body, R.body_len, changed, P, tail, np, spill, bad);
+        stream_fast<16, kNS, Codec>(A, W, cd, segs, lane, sink, R.body_len, changed, P, tail, np, spill, bad);
     else if (vec && cd.bits == 8)
-        stream_fast<8, kNS, Codec>(A, W, cd, segs, lane, body, R.body_len, changed, P, tail, np, spill, bad);
+        stream_fast<8, kNS, Codec>(A, W, cd, segs, lane, sink, R.body_len, changed, P, tail, np, spill, bad);
     else
-        stream_chunk<kNS, Codec>(A, W, cd, segs, lane, body, R.body_len, nullptr, 0, changed, P, tail, np, units,
+        stream_chunk<kNS, Codec>(A, W, cd, segs, lane, sink, R.body_len, nullptr, 0, changed, P, tail, np, units,
                                  spill, bad);
     changed = __reduce_add_sync(kFull, changed);
     if (R.kind == kOverwrite) {
@@ -1090,7 +1156,7 @@ __global__ void __launch_bounds__(1024) scan_kernel(EncArgs A, uint64_t* tiles, 
     const uint32_t e = b0 + per < n ? b0 + per : (b0 < n ? n : b0);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     auto rec = [](uint32_t fs) -> unsigned long long {
-        fs &= ~kSpilled;
+        fs &= kFrameSizeMask;
         return fs ? ((1ull << kLbFrameShift) | fs) : 0ull;
     };
     uint32_t v[per];
@@ -1192,23 +1258,29 @@ __global__ void copy_kernel(EncArgs A)
     const uint32_t nw = gridDim.x * (blockDim.x >> 5);
     for (uint32_t k = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); k < A.chunk_count; k += nw) {
         const uint32_t fs = A.fsize[k];
-        if (!(fs & ~kSpilled)) continue;
+        if (!(fs & kFrameSizeMask)) continue;
         const uint64_t ex = A.lb[k];
         const uint64_t rel = ex & kLbByteMask;
         if (lane == 0) index[ex >> kLbFrameShift] = A.frame_base + rel;
         if (fs & kSpilled) continue;
-        const uint4* __restrict__ src = reinterpret_cast<const uint4*>(A.slots + size_t(k) * kEncSlot);
-        uint4* __restrict__ dst = reinterpret_cast<uint4*>(A.frames + rel);
-        const uint32_t nv = fs / 16;
-        for (uint32_t i0 = lane; i0 < nv; i0 += 128) {   // four loads in flight per lane
-            uint4 v[4];
+        const uint32_t size = fs & kFrameSizeMask;
+        auto copy = [&](const uint4* __restrict__ src, uint4* __restrict__ dst, uint32_t nv) {
+            for (uint32_t i0 = lane; i0 < nv; i0 += 128) {   // four loads in flight per lane
+                uint4 v[4];
 #pragma unroll
-            for (uint32_t j = 0; j < 4; ++j)
-                if (i0 + 32 * j < nv) v[j] = src[i0 + 32 * j];
+                for (uint32_t j = 0; j < 4; ++j)
+                    if (i0 + 32 * j < nv) v[j] = src[i0 + 32 * j];
 #pragma unroll
-            for (uint32_t j = 0; j < 4; ++j)
-                if (i0 + 32 * j < nv) dst[i0 + 32 * j] = v[j];
-        }
+                for (uint32_t j = 0; j < 4; ++j)
+                    if (i0 + 32 * j < nv) dst[i0 + 32 * j] = v[j];
+            }
+        };
+        const uint32_t in_slot = size < kEncSlot ? size : kEncSlot;
+        copy(reinterpret_cast<const uint4*>(A.slots + size_t(k) * kEncSlot), reinterpret_cast<uint4*>(A.frames + rel),
+             in_slot / 16);
+        if (fs & kHeap)   // the body's rest, from the heap
+            copy(reinterpret_cast<const uint4*>(A.heap + A.heapoff[k]),
+                 reinterpret_cast<uint4*>(A.frames + rel + kEncSlot), (size - kEncSlot) / 16);
     }
 }
 
@@ -1332,9 +1404,9 @@ __device__ uint32_t mask_block(Buf& B, int raw, uint8_t* body, uint32_t body_len
         const bool fin = t >= kSteps;
         int g = 0;
         for (; g + 32 <= n; g += 32)
-            parse_group<Codec>(S, g, 32, false, raw, P, body, body_len, emit, lane, &over, bad);
+            parse_group<Codec>(S, g, 32, false, raw, P, Sink{body}, body_len, emit, lane, &over, bad);
         if (fin) {
-            parse_group<Codec>(S, g, n - g, true, raw, P, body, body_len, emit, lane, &over, bad);
+            parse_group<Codec>(S, g, n - g, true, raw, P, Sink{body}, body_len, emit, lane, &over, bad);
             break;
         }
         const int rem = n - g;   // < 32, and g >= 32 since a batch stops only near kEvCap
@@ -1482,7 +1554,7 @@ __global__ void __launch_bounds__(kEThreads, 4) encode_cta_kernel(EncArgs A)
     const int nseg = int(cd.src_count);
     const bool overwrite = (cd.flags & kResidualFlag) || A.mode == DCR_MODE_OVERWRITE_ONLY;
     if (overwrite || !(cd.flags & kSrcVec)) {   // the one-warp encoder does these
-        if (warp == 0) encode_chunk<kNS, Codec>(A, C.u.w, k, lane);
+        if (warp == 0) encode_chunk<kNS, Codec>(A, C.u.w, k, lane, nullptr);
         return;
     }
     if (nseg <= kMSegCache)
@@ -1576,7 +1648,7 @@ __global__ void __launch_bounds__(kEThreads, 4) encode_cta_kernel(EncArgs A)
     }
     if (overflow) {   // a slice outgrew its region: the one-warp encoder takes the chunk
         __syncthreads();
-        if (warp == 0) encode_chunk<kNS, Codec>(A, C.u.w, k, lane);
+        if (warp == 0) encode_chunk<kNS, Codec>(A, C.u.w, k, lane, nullptr);
         return;
     }
     if (threadIdx.x == 0 && chunk_changed) {
@@ -1601,8 +1673,8 @@ __global__ void __launch_bounds__(kEThreads, 4) encode_cta_kernel(EncArgs A)
     auto group = [&](int g, Parse& P, uint8_t* out, uint32_t cap, bool emit, bool* over, bool* bad) {
         P.prev = g ? S.at(32 * g - 1) : -1;
         const bool fin = g == full;
-        parse_group<Codec>(S, 32 * g, fin ? int(total_ev) - 32 * g : 32, fin, raw, P, out, cap, emit, lane, over,
-                           bad);
+        parse_group<Codec>(S, 32 * g, fin ? int(total_ev) - 32 * g : 32, fin, raw, P, Sink{out}, cap, emit, lane,
+                           over, bad);
     };
     bool over = false, bad = false;
     // 1. each group's longest zero run (independent of the carried state)
@@ -1721,11 +1793,11 @@ namespace {
 template <class Codec>
 cudaError_t codec_attributes()
 {
-    cudaError_t e = cudaFuncSetAttribute(encode_kernel<kNS, Codec>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         int(kMainSmem));
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(encode_kernel<kNSDeep, Codec>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 int(kDeepSmem));
+    cudaError_t e = cudaSuccess;
+    for (auto f : {encode_kernel<kNS, Codec, false>, encode_kernel<kNS, Codec, true>})
+        if (e == cudaSuccess) e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kMainSmem));
+    for (auto f : {encode_kernel<kNSDeep, Codec, false>, encode_kernel<kNSDeep, Codec, true>})
+        if (e == cudaSuccess) e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kDeepSmem));
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(restream_kernel<Codec>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  int(kMainSmem));
@@ -1749,17 +1821,20 @@ int encode_kernel_config(KernelConfig* kc)
     // residency of the LZ4 instantiations (the Snappy ones are launched with
     // the same grids: persistent CTAs that take tickets)
     if (e == cudaSuccess)
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&kc->enc_blocks_per_sm, encode_kernel<kNS, CodecLz4>,
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&kc->enc_blocks_per_sm, encode_kernel<kNS, CodecLz4, false>,
                                                           kMThreads, kMainSmem);
     if (e == cudaSuccess)
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&kc->enc_deep_blocks_per_sm,
-                                                          encode_kernel<kNSDeep, CodecLz4>, 32 * kDeepWarps, kDeepSmem);
+                                                          encode_kernel<kNSDeep, CodecLz4, false>, 32 * kDeepWarps,
+                                                          kDeepSmem);
     if (e == cudaSuccess)
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&kc->restream_blocks_per_sm, restream_kernel<CodecLz4>,
                                                           kMThreads, kMainSmem);
     if (e == cudaSuccess)
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&kc->spill_blocks_per_sm, spill_kernel<CodecLz4>,
                                                           kSThreads, sizeof(Buf));
+    kc->enc_warps_per_block = kMWarps;
+    kc->enc_deep_warps_per_block = kDeepWarps;
     if (e != cudaSuccess) return cuda_error(e, "encode kernel configuration");
     if (kc->enc_blocks_per_sm < 1 || kc->enc_deep_blocks_per_sm < 1 || kc->restream_blocks_per_sm < 1 ||
         kc->spill_blocks_per_sm < 1)
@@ -1789,6 +1864,10 @@ EncArgs make_args(const dcr_plan* P, uint32_t mode, uint64_t chunk_begin, uint64
     A.spill = P->d_spill;
     A.deep = P->d_deep;
     A.slots = P->d_slots;
+    A.ovf = P->d_ovf;
+    A.heap = P->d_heap;
+    A.heap_cap = P->heap_bytes;
+    A.heapoff = P->d_heapoff;
     return A;
 }
 
@@ -1818,20 +1897,28 @@ int launch_size(const dcr_plan* P, EncArgs& A, uint64_t plan_hash, uint64_t base
     if (dgrid > deep_warps / kDeepWarps) dgrid = deep_warps / kDeepWarps;
     if (dgrid == 0) dgrid = 1;
     const bool snappy = P->codec == DCR_CODEC_SNAPPY;
+    const bool ovf = P->d_ovf != nullptr && P->overflow_seen;
     if (P->profiling) cudaEventRecord(P->ev[0], s);
     const unsigned cgrid = A.chunk_count ? A.chunk_count : 1;
     if (cta && snappy)
         encode_cta_kernel<CodecSnappy><<<cgrid, kEThreads, sizeof(CtaSmem), s>>>(A);
     else if (cta)
         encode_cta_kernel<CodecLz4><<<cgrid, kEThreads, sizeof(CtaSmem), s>>>(A);
-    else if (deep && snappy)
-        encode_kernel<kNSDeep, CodecSnappy><<<dgrid, 32 * kDeepWarps, kDeepSmem, s>>>(A);
+    // the overflow heap's instantiations once this plan has seen a body
+    // outgrow its slot (sparse windows keep the plain stream loop)
+    else if (ovf) {
+        if (deep && snappy) encode_kernel<kNSDeep, CodecSnappy, true><<<dgrid, 32 * kDeepWarps, kDeepSmem, s>>>(A);
+        else if (deep) encode_kernel<kNSDeep, CodecLz4, true><<<dgrid, 32 * kDeepWarps, kDeepSmem, s>>>(A);
+        else if (snappy) encode_kernel<kNS, CodecSnappy, true><<<grid, kMThreads, kMainSmem, s>>>(A);
+        else encode_kernel<kNS, CodecLz4, true><<<grid, kMThreads, kMainSmem, s>>>(A);
+    } else if (deep && snappy)
+        encode_kernel<kNSDeep, CodecSnappy, false><<<dgrid, 32 * kDeepWarps, kDeepSmem, s>>>(A);
     else if (deep)
-        encode_kernel<kNSDeep, CodecLz4><<<dgrid, 32 * kDeepWarps, kDeepSmem, s>>>(A);
+        encode_kernel<kNSDeep, CodecLz4, false><<<dgrid, 32 * kDeepWarps, kDeepSmem, s>>>(A);
     else if (snappy)
-        encode_kernel<kNS, CodecSnappy><<<grid, kMThreads, kMainSmem, s>>>(A);
+        encode_kernel<kNS, CodecSnappy, false><<<grid, kMThreads, kMainSmem, s>>>(A);
     else
-        encode_kernel<kNS, CodecLz4><<<grid, kMThreads, kMainSmem, s>>>(A);
+        encode_kernel<kNS, CodecLz4, false><<<grid, kMThreads, kMainSmem, s>>>(A);
     if (P->profiling) cudaEventRecord(P->ev[1], s);
     const uint32_t ntiles = A.chunk_count ? (A.chunk_count + kScanTile - 1) / kScanTile : 1u;
     e = cudaMemsetAsync(P->d_tiles, 0, ntiles * sizeof(uint64_t), s);

@@ -194,6 +194,11 @@ void plan_free_device(dcr_plan* p)
     p->d_win = nullptr;
     cudaFree(p->d_enc);
     cudaFree(p->d_slots);
+    cudaFree(p->d_ovf);
+    cudaFree(p->d_heap);
+    cudaFree(p->d_heapoff);
+    p->d_ovf = p->d_heap = nullptr;
+    p->d_heapoff = nullptr;
     if (p->h_enc) cudaFreeHost(p->h_enc);
     p->d_chunks = nullptr;
     p->d_src = p->d_dst = nullptr;
@@ -224,6 +229,7 @@ extern "C" int dcr_plan_build(const dcr_tensor_desc* tensors, size_t n, const dc
     if (codec > DCR_CODEC_SNAPPY) return set_error(DCR_ERR_INVALID, "unknown codec %u", codec);
     const uint32_t flags = opts ? opts->flags : 0u;
     const uint32_t apply = opts ? opts->apply : uint32_t(DCR_APPLY_AUTO);
+    const uint32_t overflow_kib = opts ? opts->overflow_kib : 0u;
     if (apply > DCR_APPLY_CTA) return set_error(DCR_ERR_INVALID, "unknown apply variant %u", apply);
     if (flags & ~uint32_t(DCR_PLAN_HOST_ONLY)) return set_error(DCR_ERR_INVALID, "unknown plan flags %#x", flags);
     dcr_plan* P = new (std::nothrow) dcr_plan();
@@ -409,7 +415,23 @@ extern "C" int dcr_plan_build(const dcr_tensor_desc* tensors, size_t n, const dc
         delete P;
         return rc;
     }
-    P->small_window_chunks = P->kc.num_sms * P->kc.enc_deep_blocks_per_sm * 2;
+    P->small_window_chunks = P->kc.num_sms * P->kc.enc_deep_blocks_per_sm * P->kc.enc_deep_warps_per_block;
+    // overflow buffers (one per warp of the one-warp encoders) and the heap
+    // that XOR bodies past their slots move to
+    if (overflow_kib != DCR_NO_OVERFLOW) {
+        const uint64_t warps =
+            std::max<uint64_t>(uint64_t(P->kc.num_sms) * P->kc.enc_blocks_per_sm * P->kc.enc_warps_per_block,
+                               uint64_t(P->kc.num_sms) * P->kc.enc_deep_blocks_per_sm * P->kc.enc_deep_warps_per_block);
+        const uint64_t win = std::min<uint64_t>(W, P->canonical_bytes ? P->canonical_bytes : 1);
+        P->heap_bytes = overflow_kib ? uint64_t(overflow_kib) << 10 : (win / 8 + 255) / 256 * 256;
+        if ((e = cudaMalloc(&P->d_ovf, warps * kOvfBytes)) != cudaSuccess ||
+            (e = cudaMalloc(&P->d_heap, P->heap_bytes ? P->heap_bytes : 256)) != cudaSuccess ||
+            (e = cudaMalloc(&P->d_heapoff, (P->max_window_chunks ? P->max_window_chunks : 1) * 8)) != cudaSuccess) {
+            plan_free_device(P);
+            delete P;
+            return cuda_error(e, "allocating the encoder's overflow heap");
+        }
+    }
     *out = P;
     return DCR_OK;
 }
@@ -547,6 +569,7 @@ int encode_result(const dcr_plan* p, const void* head, size_t cap, size_t* paylo
 {
     const EncScratch* st = static_cast<const EncScratch*>(head);
     *payload_size = st->total;
+    if (st->n_spill || st->heap_top) p->overflow_seen = true;   // bodies past their slots: use the heap from now on
     if (changed) {
         const uint64_t* cnt = reinterpret_cast<const uint64_t*>(static_cast<const char*>(head) +
                                                                 sizeof(EncScratch));
@@ -765,6 +788,7 @@ extern "C" int dcr_encode_part(const dcr_plan* p, uint32_t mode, uint32_t window
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return cuda_error(e, "dcr_encode_part status read");
     const EncScratch* hs = static_cast<const EncScratch*>(p->h_enc);
+    if (hs->n_spill || hs->heap_top) p->overflow_seen = true;
     if (changed_per_tensor)
         memcpy(changed_per_tensor, static_cast<const char*>(p->h_enc) + sizeof(EncScratch), p->descs.size() * 8);
     if (hs->err) return set_error(hs->err, "dcr_encode_part: device error %d", hs->err);

@@ -144,6 +144,7 @@ typedef struct {
  * dcr_stream_header, e.g. on a rank or process without a GPU); every call
  * that runs kernels returns DCR_ERR_INVALID for it. */
 #define DCR_PLAN_HOST_ONLY 1u
+#define DCR_NO_OVERFLOW 0xFFFFFFFFu
 
 typedef struct {
     uint64_t window_bytes;   /* 0 = 16 GiB.  Windows pack whole tensors in
@@ -153,7 +154,16 @@ typedef struct {
     uint32_t codec;          /* DCR_CODEC_LZ4 (0) or DCR_CODEC_SNAPPY */
     uint32_t flags;          /* 0 or DCR_PLAN_HOST_ONLY */
     uint32_t apply;          /* DCR_APPLY_AUTO (0), _WARP or _CTA */
-    uint32_t reserved[2];
+    uint32_t overflow_kib;    /* device heap for XOR blocks that outgrow their
+                                6 KiB frame slot (masks of a few percent
+                                change and more): 0 = one eighth of
+                                the window size; DCR_NO_OVERFLOW = none (such
+                                blocks are derived again from old and new by
+                                a second pass, as they are once the heap is
+                                full); in KiB.  With a heap the plan also holds one
+                                64 KiB overflow buffer per encoder warp
+                                (about 228 MiB on GB300). */
+    uint32_t reserved;
 } dcr_plan_opts;
 
 typedef struct {

@@ -97,10 +97,14 @@ def test_crafted_workload_reaches_every_route():
     assert fo[a0]["kind"] == K_OVERWRITE and len(fo[a0]["body"]) > SLOT_BODY
 
 
+# overflow heap: the default (bodies past their slot move to the heap), none
+# (the write pass derives them again from old and new), and 16 KiB, which
+# runs out part way through the window (both routes in one encode)
 @pytest.mark.gpu
+@pytest.mark.parametrize("overflow", ["heap", "none", "16kib"])
 @pytest.mark.parametrize("encoder", ["wide", "deep", "cta"])
 @pytest.mark.parametrize("mode", ["hybrid", "overwrite"])
-def test_every_route_matches_oracle(mode, encoder):
+def test_every_route_matches_oracle(mode, encoder, overflow):
     torch = pytest.importorskip("torch")
     import bit_exact_xor_gb300 as dcr
     from wl import descs_of, to_device
@@ -111,7 +115,8 @@ def test_every_route_matches_oracle(mode, encoder):
                     encoder={"wide": dcr.ENCODER_WIDE, "deep": dcr.ENCODER_DEEP, "cta": dcr.ENCODER_CTA}[encoder],
                     # both apply kernels on every route: warp per frame after the wide and CTA
                     # encoders, CTA per frame after the deep one
-                    apply=dcr.APPLY_CTA if encoder == "deep" else dcr.APPLY_WARP)
+                    apply=dcr.APPLY_CTA if encoder == "deep" else dcr.APPLY_WARP,
+                    overflow_kib={"heap": 0, "none": dcr.NO_OVERFLOW, "16kib": 16}[overflow])
     assert plan.info.plan_hash == orc.plan_hash
     d_old, d_new = to_device(olds), to_device(news)
     dm = dcr.MODE_HYBRID if mode == "hybrid" else dcr.MODE_OVERWRITE_ONLY
