@@ -487,7 +487,8 @@ def run_gpu(args):
         ems = dist_max(t0.elapsed_time(t1), ws)
         per_step_h2d, per_step_d2h = h2d // k, d2h // k
         # the host link on its own: the same input copies with nothing else
-        # running, timed on the copy stream (context for the e2e figure)
+        # running, timed on the copy stream (context for the e2e figure; it
+        # varies between boxes and between runs)
         torch.cuda.synchronize()
         c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         c0.record(cs)
@@ -498,8 +499,7 @@ def run_gpu(args):
         link = 2 * sum(x.numel() for x in h_old + h_new) / (c0.elapsed_time(c1) / 1e3) / 1e9
         e2e = {"value": round(N * k * ws / (ems / 1e3) / 1e9, 3), "unit": UNIT,
                "h2d_bytes_per_step": per_step_h2d, "d2h_bytes_per_step": per_step_d2h,
-               "host_link_h2d_gbs": round(link, 1),
-               "link_bound_value": round(N / ((per_step_h2d + per_step_d2h) / (link * 1e9)) / 1e9, 3)}
+               "host_link_h2d_gbs": round(link, 1)}
         del h_old, h_new, d_in
 
     # pipelined refit of every window through pinned host memory
@@ -603,9 +603,38 @@ def run_gpu(args):
         r1.record(stream)
         torch.cuda.synchronize()
         rms = r0.elapsed_time(r1) / k
+        # the retry stream alone, both ways: encoded again from old and new
+        # (overwrite-only mode) or built from the XOR stream and new
+        # (dcr_encode_retry, no read of old); same bytes
+        a, b = (olds, news) if d[0] == 0 else (news, olds)
+        xs = []
+        for w in range(nw):
+            rc, size, _ = dcr.encode(plan, a, b, payloads[w], window=w, counts=False, stream=sh)
+            dcr.check(rc)
+            xs.append(size)
+
+        def time_retry(from_xor):
+            t0 = torch.cuda.Event(enable_timing=True)
+            t1 = torch.cuda.Event(enable_timing=True)
+            t0.record(stream)
+            for _ in range(k):
+                for w in range(nw):
+                    if from_xor:
+                        rc, _ = dcr.encode_retry(plan, payloads[w], xs[w], b, rpay[w], stream=sh)
+                    else:
+                        rc, _, _ = dcr.encode(plan, a, b, rpay[w], window=w, mode=dcr.MODE_OVERWRITE_ONLY,
+                                              counts=False, stream=sh)
+                    dcr.check(rc)
+            t1.record(stream)
+            torch.cuda.synchronize()
+            return t0.elapsed_time(t1) / k
+
+        time_retry(True)
+        ms_ow, ms_x = time_retry(False), time_retry(True)
         retry = {"ms_per_refit": round(rms, 4), "value": round(N / (rms / 1e3) / 1e9, 3), "unit": UNIT,
                  "abort": "half of each window's frames applied, one split mid-frame",
-                 "retry_payload_bytes_per_refit": int(rlast["bytes"])}
+                 "retry_payload_bytes_per_refit": int(rlast["bytes"]),
+                 "retry_stream_ms": {"from_old_and_new": round(ms_ow, 4), "from_xor_stream_and_new": round(ms_x, 4)}}
         del rpay
 
     # ownership-sharded encode: rank r encodes part r of every window on its

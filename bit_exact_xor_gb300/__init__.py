@@ -111,7 +111,7 @@ EXPORTS = ["dcr_last_error", "dcr_plan_build", "dcr_plan_info_get", "dcr_window_
            "dcr_recv_state_version", "dcr_encode", "dcr_apply", "dcr_apply_retry",
            "dcr_dense_refit", "dcr_plan_set_profiling", "dcr_plan_last_profile", "dcr_apply_noalloc",
            "dcr_pipeline_sizes", "dcr_refit_pipelined", "dcr_part_info_get", "dcr_encode_part",
-           "dcr_encode_part_write", "dcr_stream_layout", "dcr_stream_header"]
+           "dcr_encode_part_write", "dcr_stream_layout", "dcr_stream_header", "dcr_encode_retry"]
 
 _lib = None
 
@@ -149,6 +149,7 @@ def lib():
         L.dcr_encode_part_write.argtypes = [VP, U64, VP, SZ, VP, VP]
         L.dcr_stream_layout.argtypes = [U32, P(PartSize), P(U64), P(U64), P(U64)]
         L.dcr_stream_header.argtypes = [VP, U32, U32, U64, U64, U64, U64, VP]
+        L.dcr_encode_retry.argtypes = [VP, VP, SZ, P(VP), VP, SZ, P(SZ), VP]
         _lib = L
     return _lib
 
@@ -312,6 +313,16 @@ def refit_pipelined(plan, state, olds, news, target, device_buf, host_buf, mode=
                                    target_version, _ptr(target), _ptr(device_buf), device_buf.numel(),
                                    _ptr(host_buf), host_buf.numel(), cnt, ctypes.byref(st), _stream(stream))
     return rc, st, (list(cnt) if counts else None)
+
+
+def encode_retry(plan, xor_payload, xor_size, news, payload, cap=None, stream=None):
+    """dcr_encode_retry.  Returns (status, payload_size)."""
+    size = ctypes.c_size_t()
+    if cap is None:
+        cap = payload.numel() if payload is not None and not isinstance(payload, int) else 0
+    rc = lib().dcr_encode_retry(plan.h, _ptr(xor_payload), xor_size, _ptr_array(news), _ptr(payload), cap,
+                                ctypes.byref(size), _stream(stream))
+    return rc, size.value
 
 
 def encode_part(plan, olds, news, part, n_parts, window=0, mode=MODE_HYBRID, counts=True, stream=None):

@@ -58,6 +58,8 @@ constexpr int kAEvCap = 1024;               // non-zero output bytes listed per 
 constexpr int kDThreads = 256;
 constexpr uint32_t kCasLimit = 1u << 16;
 
+#include "decode.cuh"
+
 struct ApplyArgs {
     const ChunkDesc* chunks;
     const Seg* dst;
@@ -1166,112 +1168,9 @@ __global__ void __launch_bounds__(kDThreads) defer_kernel(ApplyArgs A)
         uint32_t lim = cut ? (A.split < raw ? A.split : raw) : raw;
         lim -= lim % ub;
         const uint8_t* src = p + fo + kFrameHdr;
-        if (threadIdx.x < 32 && snappy) {
-            // Snappy block: varint length, then literal and copy elements
-            bool good = false;
-            uint32_t ip = 0, op = 0;
-            uint64_t v = 0;
-            bool pre = false;
-            for (uint32_t shift = 0; shift <= 28 && ip < n; shift += 7) {
-                const uint64_t b = src[ip++];
-                v |= (b & 127u) << shift;
-                if (!(b & 128u)) {
-                    pre = true;
-                    break;
-                }
-            }
-            bool ok = pre && v == raw;
-            while (ok && ip < n) {
-                const uint32_t tag = src[ip++];
-                uint32_t len, off;
-                if ((tag & 3u) == 0) {
-                    len = (tag >> 2) + 1;
-                    if ((tag >> 2) >= 60) {
-                        const uint32_t nb = (tag >> 2) - 59;
-                        if (nb > n - ip) { ok = false; break; }
-                        len = 0;
-                        for (uint32_t i = 0; i < nb; ++i) len |= uint32_t(src[ip + i]) << (8 * i);
-                        len += 1;   // at most 2^32: wraps to 0 only for a 4-byte length, rejected below
-                        ip += nb;
-                    }
-                    if (len == 0 || len > n - ip || len > raw - op) { ok = false; break; }
-                    for (uint32_t i = lane; i < len; i += 32) out[op + i] = src[ip + i];
-                    __syncwarp();
-                    ip += len;
-                    op += len;
-                    continue;
-                }
-                if ((tag & 3u) == 1) {
-                    if (ip >= n) { ok = false; break; }
-                    len = ((tag >> 2) & 7u) + 4;
-                    off = ((tag >> 5) << 8) | src[ip++];
-                } else {
-                    const uint32_t nb = (tag & 3u) == 2 ? 2u : 4u;
-                    if (nb > n - ip) { ok = false; break; }
-                    len = (tag >> 2) + 1;
-                    off = 0;
-                    for (uint32_t i = 0; i < nb; ++i) off |= uint32_t(src[ip + i]) << (8 * i);
-                    ip += nb;
-                }
-                if (off == 0 || off > op || len > raw - op) { ok = false; break; }
-                bool viol = false;   // forward copy semantics: the output repeats with period off
-                for (uint32_t i = lane; i < len; i += 32) {
-                    const uint8_t b = out[op - off + (i % off)];
-                    out[op + i] = b;
-                    viol |= b != 0;
-                }
-                if (__any_sync(kFull, zs && viol)) { ok = false; break; }
-                op += len;
-            }
-            good = ok && op == raw;
-            if (lane == 0) s_good = good;
-        } else if (threadIdx.x < 32) {
-            bool good = false;
-            uint32_t ip = 0, op = 0;
-            for (;;) {
-                if (ip >= n) break;
-                const uint32_t tok = src[ip++];
-                uint32_t ll = tok >> 4;
-                bool ok = true;
-                if (ll == 15) {
-                    for (;;) {
-                        if (ip >= n) { ok = false; break; }
-                        uint32_t b = src[ip++];
-                        ll += b;
-                        if (b != 255) break;
-                    }
-                }
-                if (!ok || ll > n - ip || ll > raw - op) break;
-                for (uint32_t i = lane; i < ll; i += 32) out[op + i] = src[ip + i];
-                __syncwarp();
-                ip += ll;
-                op += ll;
-                if (ip == n) { good = op == raw; break; }
-                if (n - ip < 2) break;
-                const uint32_t off = uint32_t(src[ip]) | (uint32_t(src[ip + 1]) << 8);
-                ip += 2;
-                if (off == 0 || off > op) break;
-                uint32_t ml = tok & 15u;
-                if (ml == 15) {
-                    for (;;) {
-                        if (ip >= n) { ok = false; break; }
-                        uint32_t b = src[ip++];
-                        ml += b;
-                        if (b != 255) break;
-                    }
-                }
-                ml += 4;
-                if (!ok || ml > raw - op) break;
-                // forward copy semantics: the output repeats with period off
-                bool viol = false;
-                for (uint32_t i = lane; i < ml; i += 32) {
-                    const uint8_t b = out[op - off + (i % off)];
-                    out[op + i] = b;
-                    viol |= b != 0;
-                }
-                if (__any_sync(kFull, zs && viol)) break;
-                op += ml;
-            }
+        if (threadIdx.x < 32) {
+            const bool good = snappy ? warp_decode_snappy(src, n, out, raw, zs, lane)
+                                     : warp_decode_lz4(src, n, out, raw, zs, lane);
             if (lane == 0) s_good = good;
         }
         __syncthreads();

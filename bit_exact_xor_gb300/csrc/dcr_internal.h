@@ -134,6 +134,7 @@ struct KernelConfig {
     int num_sms = 0;
     int enc_blocks_per_sm = 0;
     int enc_deep_blocks_per_sm = 0;
+    int retry_blocks_per_sm = 0;
     int enc_warps_per_block = 0;        // one chunk per warp: the wide and deep variants
     int enc_deep_warps_per_block = 0;
     int restream_blocks_per_sm = 0;
@@ -157,6 +158,11 @@ int encode_size_launch(const struct ::dcr_plan* plan, uint32_t mode, uint64_t ch
 int encode_write_launch(const struct ::dcr_plan* plan, uint32_t mode, uint64_t chunk_begin, uint64_t chunk_count,
                         const void* const* olds, const void* const* news, uint8_t* frames, uint64_t frame_base,
                         uint64_t* index, cudaStream_t s);
+// dcr_encode_retry: the overwrite-only stream of a window from its XOR
+// stream (in, index at in_idx, in_frames frames) and new
+int retry_launch(const struct ::dcr_plan* plan, const void* in, uint64_t in_idx, uint64_t in_frames,
+                 uint32_t window, uint64_t base_v, uint64_t target_v, const void* const* news, void* payload,
+                 size_t cap, cudaStream_t s);
 int encode_kernel_config(KernelConfig* kc);
 int apply_kernel_config(KernelConfig* kc);
 int apply_launch(const struct ::dcr_plan* plan, struct ::dcr_recv_state* st, const void* payload,

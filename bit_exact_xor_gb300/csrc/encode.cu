@@ -113,6 +113,9 @@ struct EncArgs {
     uint8_t* heap;             // rests of bodies past their slots
     uint64_t heap_cap;
     uint64_t* heapoff;         // per chunk: where its rest sits in the heap
+    const uint8_t* in;         // dcr_encode_retry: the XOR stream read
+    uint64_t in_idx;           // ... its index offset
+    uint64_t in_frames;        // ... and frame count
     EncScratch* sc;
     unsigned long long* counts;
     uint64_t* lb;              // frame offsets: frames before << 40 | bytes before
@@ -1782,6 +1785,265 @@ __global__ void __launch_bounds__(kEThreads, 4) encode_cta_kernel(EncArgs A)
     }
 }
 
+// ------------------------------------------------------------------ retry --
+// dcr_encode_retry: the overwrite-only stream of a window built from the
+// window's XOR stream and new, without old.  retry_kernel: one CTA per frame
+// of the XOR stream decodes the mask into shared memory (the general
+// decoders), lists the changed units (16-bit words for bf16, else bytes) in
+// order and gathers their new values through the plan's sender pieces:
+// OVERWRITE records that fit the slot are written there; records past the
+// slot, dense chunks (records not smaller than the chunk) and frames that
+// already are overwrite records (copied through) are listed for
+// retry_spill_kernel, which writes them at their final place once the scan
+// has placed every frame.  The frames are those dcr_encode writes in
+// overwrite-only mode, byte for byte.
+#include "decode.cuh"
+
+constexpr int kRThreads = 256;
+constexpr int kRWarps = kRThreads / 32;
+constexpr uint32_t kRBusy = 1;   // frame size of a chunk being built (sizes are multiples of 16)
+
+struct __align__(16) RSmem {
+    uint4 mask[kChunk / 16];
+    uint32_t wsum[kRWarps];
+    Seg segs[kSegCache];
+    uint32_t f, good, n, changed;
+};
+
+// exclusive prefix of v over the CTA; *total = the sum
+__device__ __forceinline__ uint32_t r_excl_scan(uint32_t v, uint32_t* wsum, uint32_t* total)
+{
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const uint32_t incl = warp_incl_sum(v, lane);
+    if (lane == 31) wsum[w] = incl;
+    __syncthreads();
+    uint32_t before = 0, tot = 0;
+#pragma unroll
+    for (int i = 0; i < kRWarps; ++i) {
+        before += i < w ? wsum[i] : 0u;
+        tot += wsum[i];
+    }
+    __syncthreads();
+    *total = tot;
+    return before + incl - v;
+}
+
+// new byte at canonical byte x of the chunk
+__device__ __forceinline__ uint8_t new_byte(const EncArgs& A, const Seg* segs, int nseg, uint32_t x)
+{
+    const Seg sg = segs[find_seg(segs, nseg, x)];
+    return A.news[uint32_t(sg.addr >> kShardShift)][(sg.addr & kAddrMask) + (x - sg.off)];
+}
+
+// The chunk's mask (in S.mask) as OVERWRITE records written to body: unit
+// count, unit offsets, zero pad, new values.  Threads take contiguous ranges
+// of units, so the records come out in order.
+__device__ void retry_records(const EncArgs& A, RSmem& S, const ChunkDesc& cd, const Seg* segs, uint8_t* body)
+{
+    const uint32_t ub = cd.bits == 16 ? 2u : 1u, nu_all = cd.raw_len / ub;
+    const uint32_t per = (nu_all + kRThreads - 1) / kRThreads;
+    const uint32_t u0 = threadIdx.x * per, u1 = u0 + per < nu_all ? u0 + per : nu_all;
+    const uint8_t* m = reinterpret_cast<const uint8_t*>(S.mask);
+    auto changed_unit = [&](uint32_t u) {
+        return ub == 2 ? (m[2 * u] | m[2 * u + 1]) != 0 : m[u] != 0;
+    };
+    uint32_t c = 0;
+    for (uint32_t u = u0; u < u1; ++u) c += changed_unit(u);
+    uint32_t n;
+    uint32_t at = r_excl_scan(c, S.wsum, &n);
+    const uint32_t voff = 4 + 2 * n + (4 - (2 * n) % 4) % 4;
+    const int nseg = int(cd.src_count);
+    for (uint32_t u = u0; u < u1; ++u) {
+        if (!changed_unit(u)) continue;
+        body[4 + 2 * at] = uint8_t(u);
+        body[5 + 2 * at] = uint8_t(u >> 8);
+        for (uint32_t e = 0; e < ub; ++e) body[voff + at * ub + e] = new_byte(A, segs, nseg, u * ub + e);
+        ++at;
+    }
+    if (threadIdx.x == 0) {
+        *reinterpret_cast<uint32_t*>(body) = n;
+        for (uint32_t i = 4 + 2 * n; i < voff; ++i) body[i] = 0;
+    }
+}
+
+// Loads the XOR stream's frame at offset fo into S: its chunk's pieces, and
+// for an XOR frame the decoded mask.  Returns the frame's kind (0:
+// malformed) and fills its chunk and body length.  Called by the whole CTA.
+__device__ uint32_t retry_load_at(const EncArgs& A, RSmem& S, uint64_t fo, uint32_t* k_out, uint32_t* bl_out)
+{
+    const uint8_t* p = A.in;
+    if (fo < kStreamHdr || fo % 16 || fo + kFrameHdr > A.in_idx) return 0;
+    const uint4 h0 = *reinterpret_cast<const uint4*>(p + fo), h1 = *reinterpret_cast<const uint4*>(p + fo + 16);
+    const uint32_t kind = h0.y & 0xFFu, fbits = (h0.y >> 8) & 0xFFu, fflags = h0.y >> 16;
+    const uint32_t c = h0.z, raw = h0.w, bl = h1.x;
+    if (h0.x != kFrameMagic || kind < kXorLz4 || kind > kXorSnappy || c < A.chunk_begin ||
+        c >= A.chunk_begin + A.chunk_count || bl > A.in_idx - fo - kFrameHdr)
+        return 0;
+    const ChunkDesc cd = A.chunks[c];
+    if (raw != cd.raw_len || fbits != cd.bits) return 0;
+    *k_out = c - A.chunk_begin;
+    *bl_out = bl;
+    const uint32_t ns = cd.src_count < uint32_t(kSegCache) ? cd.src_count : uint32_t(kSegCache);
+    for (uint32_t i = threadIdx.x; i < ns; i += kRThreads) S.segs[i] = A.src[cd.src_begin + i];
+    if (kind == kOverwrite || kind == kOverwriteDense) {
+        __syncthreads();
+        return kind;
+    }
+    const uint8_t* body = p + fo + kFrameHdr;
+    uint8_t* m = reinterpret_cast<uint8_t*>(S.mask);
+    if (kind == kXorRaw) {
+        if (bl != raw) return 0;
+        for (uint32_t x = threadIdx.x; x < raw; x += kRThreads) m[x] = body[x];
+        __syncthreads();
+        return kind;
+    }
+    const bool zs = (fflags & kFrameZsrc) != 0;
+    if (threadIdx.x < 32) {
+        const bool good = kind == kXorSnappy ? warp_decode_snappy(body, bl, m, raw, zs, threadIdx.x)
+                                             : warp_decode_lz4(body, bl, m, raw, zs, threadIdx.x);
+        if (threadIdx.x == 0) S.good = good;
+    }
+    __syncthreads();
+    return S.good ? kind : 0u;
+}
+
+// frame f of the XOR stream (its offset from the index)
+__device__ uint32_t retry_load(const EncArgs& A, RSmem& S, uint32_t f, uint64_t* fo_out, uint32_t* k_out,
+                              uint32_t* bl_out)
+{
+    const uint64_t fo = *reinterpret_cast<const uint64_t*>(A.in + A.in_idx + 8ull * f);
+    *fo_out = fo;
+    return retry_load_at(A, S, fo, k_out, bl_out);
+}
+
+__global__ void __launch_bounds__(kRThreads) retry_kernel(EncArgs A)
+{
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    RSmem& S = *reinterpret_cast<RSmem*>(smem_raw);
+    for (;;) {
+        if (threadIdx.x == 0) S.f = atomicAdd(&A.sc->ticket, 1u);
+        __syncthreads();
+        const uint32_t f = S.f;
+        __syncthreads();
+        if (f >= A.in_frames) break;
+        uint64_t fo = 0;
+        uint32_t k = 0, bl = 0;
+        const uint32_t kind = retry_load(A, S, f, &fo, &k, &bl);
+        if (kind == 0) {
+            if (threadIdx.x == 0) report(A.sc, DCR_ERR_CORRUPT);
+            __syncthreads();
+            continue;
+        }
+        // a chunk has one frame: a second one for it is rejected
+        if (threadIdx.x == 0) S.good = atomicCAS(&A.fsize[k], 0u, kRBusy) == 0u;
+        __syncthreads();
+        if (!S.good) {
+            if (threadIdx.x == 0) report(A.sc, DCR_ERR_CORRUPT);
+            __syncthreads();
+            continue;
+        }
+        const ChunkDesc cd = A.chunks[A.chunk_begin + k];
+        const Seg* segs = cd.src_count <= uint32_t(kSegCache) ? S.segs : A.src + cd.src_begin;
+        uint8_t* slot = A.slots + size_t(k) * kEncSlot;
+        const uint8_t* in_frame = A.in + fo;
+        if (kind == kOverwrite || kind == kOverwriteDense) {   // already overwrite records: through
+            const uint32_t fsz = (kFrameHdr + bl + 15) / 16 * 16;
+            if (fsz <= kEncSlot) {
+                for (uint32_t v = threadIdx.x; v < fsz / 16; v += kRThreads)
+                    reinterpret_cast<uint4*>(slot)[v] = reinterpret_cast<const uint4*>(in_frame)[v];
+                __syncthreads();
+                if (threadIdx.x == 0) A.fsize[k] = fsz;
+            } else if (threadIdx.x == 0) {
+                A.fsize[k] = fsz | kSpilled;
+                A.spill[atomicAdd(&A.sc->n_spill, 1u)] =
+                    SpillRec{k, 0u, bl, 0u, 0u, {uint32_t(fo), uint32_t(fo >> 32), 0u}};   // kind 0: copy through
+            }
+            __syncthreads();
+            continue;
+        }
+        // changed units and changed stored values of the mask
+        const uint32_t ub = cd.bits == 16 ? 2u : 1u, raw = cd.raw_len;
+        const uint8_t* m = reinterpret_cast<const uint8_t*>(S.mask);
+        uint32_t units = 0, chg = 0;
+        for (uint32_t u = threadIdx.x; u < raw / ub; u += kRThreads) {
+            if (ub == 2) {
+                units += (m[2 * u] | m[2 * u + 1]) != 0;
+            } else {
+                const uint32_t b = m[u];
+                units += b != 0;
+                chg += cd.bits == 8 ? (b != 0) : ((b & 15u) != 0) + ((b >> 4) != 0);
+            }
+        }
+        uint32_t n, changed;
+        r_excl_scan(units, S.wsum, &n);
+        r_excl_scan(chg, S.wsum, &changed);
+        if (ub == 2) changed = n;
+        if (n == 0) {   // an XOR frame with nothing changed is not what the encoder writes
+            if (threadIdx.x == 0) report(A.sc, DCR_ERR_CORRUPT);
+            __syncthreads();
+            continue;
+        }
+        const uint32_t rec = 4 + 2 * n + (4 - (2 * n) % 4) % 4 + n * ub;
+        const uint32_t kind_out = rec < raw ? kOverwrite : kOverwriteDense;
+        const uint32_t body_len = kind_out == kOverwrite ? rec : raw;
+        const uint32_t fsz = (kFrameHdr + body_len + 15) / 16 * 16;
+        if (kind_out == kOverwrite && fsz <= kEncSlot) {
+            retry_records(A, S, cd, segs, slot + kFrameHdr);
+            for (uint32_t i = kFrameHdr + body_len + threadIdx.x; i < fsz; i += kRThreads) slot[i] = 0;   // padding
+            __syncthreads();
+            if (threadIdx.x == 0) {
+                write_header(slot, kOverwrite, cd.bits, A.chunk_begin + k, raw, body_len, changed);
+                A.fsize[k] = fsz;
+            }
+        } else if (threadIdx.x == 0) {
+            A.fsize[k] = fsz | kSpilled;
+            A.spill[atomicAdd(&A.sc->n_spill, 1u)] =
+                SpillRec{k, kind_out, body_len, n, changed, {uint32_t(fo), uint32_t(fo >> 32), 0u}};
+        }
+        __syncthreads();
+    }
+}
+
+// The frames retry_kernel listed, at their places in the stream: frames
+// copied through, dense chunks (new bytes gathered), and records past the
+// slot (the mask decoded again).
+__global__ void __launch_bounds__(kRThreads) retry_spill_kernel(EncArgs A)
+{
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    RSmem& S = *reinterpret_cast<RSmem*>(smem_raw);
+    const uint32_t n_spill = A.sc->n_spill;   // final: written by retry_kernel only
+    if (A.sc->total > A.cap || *(volatile int32_t*)&A.sc->err) return;
+    for (uint32_t i = blockIdx.x; i < n_spill; i += gridDim.x) {
+        const SpillRec R = A.spill[i];
+        const uint64_t fo = uint64_t(R.pad[0]) | (uint64_t(R.pad[1]) << 32);
+        uint8_t* f = A.frames + (A.lb[R.k] & kLbByteMask);
+        const ChunkDesc cd = A.chunks[A.chunk_begin + R.k];
+        const uint32_t raw = cd.raw_len;
+        if (R.kind == 0) {   // through
+            const uint32_t fsz = (kFrameHdr + R.body_len + 15) / 16 * 16;
+            for (uint32_t v = threadIdx.x; v < fsz / 16; v += kRThreads)
+                reinterpret_cast<uint4*>(f)[v] = reinterpret_cast<const uint4*>(A.in + fo)[v];
+            continue;
+        }
+        const uint32_t ns = cd.src_count < uint32_t(kSegCache) ? cd.src_count : uint32_t(kSegCache);
+        for (uint32_t j = threadIdx.x; j < ns; j += kRThreads) S.segs[j] = A.src[cd.src_begin + j];
+        __syncthreads();
+        const Seg* segs = cd.src_count <= uint32_t(kSegCache) ? S.segs : A.src + cd.src_begin;
+        uint8_t* body = f + kFrameHdr;
+        if (R.kind == kOverwriteDense) {
+            for (uint32_t x = threadIdx.x; x < raw; x += kRThreads) body[x] = new_byte(A, segs, int(cd.src_count), x);
+        } else {   // the records again, from the mask decoded again (retry_kernel checked the frame)
+            uint32_t k2 = 0, bl2 = 0;
+            retry_load_at(A, S, fo, &k2, &bl2);
+            retry_records(A, S, cd, segs, body);
+        }
+        const uint32_t fsz = (kFrameHdr + R.body_len + 15) / 16 * 16;
+        for (uint32_t x = kFrameHdr + R.body_len + threadIdx.x; x < fsz; x += kRThreads) f[x] = 0;   // padding
+        if (threadIdx.x == 0) write_header(f, R.kind, cd.bits, A.chunk_begin + R.k, raw, R.body_len, R.changed);
+        __syncthreads();
+    }
+}
+
 constexpr size_t kMainSmem = sizeof(WarpSmem) * kMWarps;
 constexpr size_t kDeepSmem = sizeof(WarpSmemDeep) * kDeepWarps;
 
@@ -1813,6 +2075,19 @@ cudaError_t codec_attributes()
 
 int encode_kernel_config(KernelConfig* kc)
 {
+    {
+        const cudaError_t r = cudaFuncSetAttribute(retry_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   int(sizeof(RSmem)));
+        const cudaError_t r2 = r == cudaSuccess ? cudaFuncSetAttribute(retry_spill_kernel,
+                                                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                                       int(sizeof(RSmem)))
+                                                : r;
+        if (r2 != cudaSuccess) return cuda_error(r2, "retry kernel configuration");
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&kc->retry_blocks_per_sm, retry_kernel, kRThreads,
+                                                          sizeof(RSmem)) != cudaSuccess ||
+            kc->retry_blocks_per_sm < 1)
+            kc->retry_blocks_per_sm = 1;
+    }
     int dev;
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&kc->num_sms, cudaDevAttrMultiProcessorCount, dev);
@@ -1992,6 +2267,41 @@ int encode_write_launch(const dcr_plan* P, uint32_t mode, uint64_t chunk_begin, 
     A.frame_base = frame_base;
     A.index = index;
     return launch_write(P, A, s);
+}
+
+int retry_launch(const dcr_plan* P, const void* in, uint64_t in_idx, uint64_t in_frames, uint32_t window,
+                 uint64_t base_v, uint64_t target_v, const void* const* news, void* payload, size_t cap,
+                 cudaStream_t s)
+{
+    EncArgs A = make_args(P, DCR_MODE_OVERWRITE_ONLY, P->win_start[window],
+                          P->win_start[window + 1] - P->win_start[window], news, news);
+    A.payload = static_cast<uint8_t*>(payload);
+    A.cap = payload ? cap : 0;
+    A.frames = A.payload ? A.payload + kStreamHdr : nullptr;
+    A.frame_base = kStreamHdr;
+    A.index = nullptr;
+    A.header = 1;
+    A.in = static_cast<const uint8_t*>(in);
+    A.in_idx = in_idx;
+    A.in_frames = in_frames;
+    cudaError_t e = cudaMemsetAsync(P->d_enc, 0, P->enc_head_bytes, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(P->d_fsize, 0, (A.chunk_count ? A.chunk_count : 1) * sizeof(uint32_t), s);
+    const uint32_t ntiles = A.chunk_count ? (A.chunk_count + kScanTile - 1) / kScanTile : 1u;
+    if (e == cudaSuccess) e = cudaMemsetAsync(P->d_tiles, 0, ntiles * sizeof(uint64_t), s);
+    if (e != cudaSuccess) return cuda_error(e, "retry scratch reset");
+    const unsigned rgrid = unsigned(P->kc.num_sms * P->kc.retry_blocks_per_sm);
+    if (P->profiling) cudaEventRecord(P->ev[0], s);
+    retry_kernel<<<rgrid, kRThreads, sizeof(RSmem), s>>>(A);
+    if (P->profiling) cudaEventRecord(P->ev[1], s);
+    scan_kernel<<<ntiles, 1024, 0, s>>>(A, P->d_tiles, P->hash, base_v, target_v, window);
+    unsigned cgrid = (A.chunk_count + 7) / 8;
+    if (cgrid > unsigned(P->kc.num_sms * 8)) cgrid = unsigned(P->kc.num_sms * 8);
+    if (cgrid == 0) cgrid = 1;
+    copy_kernel<<<cgrid, 256, 0, s>>>(A);
+    retry_spill_kernel<<<rgrid, kRThreads, sizeof(RSmem), s>>>(A);
+    if (P->profiling) cudaEventRecord(P->ev[2], s);
+    e = cudaGetLastError();
+    return e == cudaSuccess ? DCR_OK : cuda_error(e, "retry launch");
 }
 
 }  // namespace dcr

@@ -881,3 +881,55 @@ extern "C" int dcr_stream_header(const dcr_plan* p, uint32_t mode, uint32_t wind
     put64(56, kStreamHdr + frame_bytes + 8 * n_frames);
     return DCR_OK;
 }
+
+// ---- overwrite-only retry from the XOR stream -------------------------------
+extern "C" int dcr_encode_retry(const dcr_plan* p, const void* xor_payload, size_t xor_size,
+                                const void* const* news, void* payload, size_t cap, size_t* payload_size,
+                                void* stream)
+{
+    if (!p || !xor_payload || !news || !payload_size)
+        return set_error(DCR_ERR_INVALID, "dcr_encode_retry: NULL argument");
+    *payload_size = 0;
+    if (p->host_only) return set_error(DCR_ERR_INVALID, "dcr_encode_retry: host-only plan");
+    if (xor_size < kStreamHdr) return set_error(DCR_ERR_CORRUPT, "dcr_encode_retry: stream shorter than its header");
+    if (!aligned16(xor_payload) || (payload && !aligned16(payload)))
+        return set_error(DCR_ERR_INVALID, "dcr_encode_retry: stream or payload not 16-byte aligned");
+    for (uint32_t r = 0; r < p->tp; ++r) {
+        if (p->shard_bytes[r] && !news[r])
+            return set_error(DCR_ERR_INVALID, "dcr_encode_retry: shard %u arena is NULL", r);
+        if (news[r] && !aligned16(news[r]))
+            return set_error(DCR_ERR_INVALID, "dcr_encode_retry: shard %u arena not 16-byte aligned", r);
+    }
+    p->part.valid = false;   // the plan's scratch now holds this encode
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t h[64];
+    cudaError_t e = cudaMemcpyAsync(h, xor_payload, sizeof(h), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_error(e, "dcr_encode_retry header read");
+    auto u32 = [&](int at) { uint32_t v; memcpy(&v, h + at, 4); return v; };
+    auto u64 = [&](int at) { uint64_t v; memcpy(&v, h + at, 8); return v; };
+    const uint64_t total = u64(56), nf = u64(48), window = u32(32);
+    if (u32(0) != kStreamMagic || u32(4) != kFormat || total > xor_size || total < kStreamHdr || total % 8 ||
+        nf > (total - kStreamHdr) / 8)
+        return set_error(DCR_ERR_CORRUPT, "dcr_encode_retry: malformed stream header");
+    if (u64(8) != p->hash || window + 1 >= p->win_start.size() || u32(40) != p->win_start[window] ||
+        u32(44) != p->win_start[window + 1] - p->win_start[window])
+        return set_error(DCR_ERR_INVALID, "dcr_encode_retry: stream of another plan or window");
+    int rc = retry_launch(p, xor_payload, total - 8 * nf, nf, uint32_t(window), u64(16), u64(24), news, payload,
+                          payload ? cap : 0, s);
+    if (rc) return rc;
+    e = cudaMemcpyAsync(p->h_enc, p->d_enc, p->enc_head_bytes, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_error(e, "dcr_encode_retry status read");
+    if (p->profiling) {
+        p->prof_encode_due = true;
+        p->prof.encode_valid = 1;
+    }
+    const EncScratch* hs = static_cast<const EncScratch*>(p->h_enc);
+    *payload_size = hs->total;
+    if (hs->err) return set_error(hs->err, "dcr_encode_retry: device error %d", hs->err);
+    if (hs->total > (payload ? cap : 0))
+        return set_error(DCR_ERR_CAPACITY, "dcr_encode_retry: payload needs %llu bytes, capacity %zu",
+                         (unsigned long long)hs->total, payload ? cap : size_t(0));
+    return DCR_OK;
+}

@@ -272,6 +272,26 @@ int dcr_apply(const dcr_plan* plan, dcr_recv_state* state, const void* payload, 
 int dcr_apply_retry(const dcr_plan* plan, dcr_recv_state* state, const void* payload, size_t size,
                     void* target, dcr_apply_result* result, void* stream);
 
+/* Overwrite-only retry stream built from the window's XOR stream (paper
+ * summary, "Recoverable in-place apply": after a failure the change set is
+ * sent again as idempotent overwrites; popular write-up, in-place apply
+ * without a backup copy: the sender need not read old again).  xor_payload
+ * (device, xor_size bytes) is a stream dcr_encode wrote for one window of
+ * this plan; for every frame the mask is decoded, the changed units read off
+ * it (16-bit words of bf16 tensors, bytes otherwise) and their values
+ * gathered from new_shards (device, the trainer arenas of the new version);
+ * frames that already are overwrite records are copied.  The stream written
+ * to `payload` (device, payload_cap bytes; *payload_size its size) carries
+ * the XOR stream's window and versions and equals, byte for byte, what
+ * dcr_encode writes in DCR_MODE_OVERWRITE_ONLY for the same old and new,
+ * without reading old: it reads the XOR stream and the changed units of
+ * new.  Errors: DCR_ERR_INVALID (plan, window or arena mismatch),
+ * DCR_ERR_CORRUPT (malformed or lying frames, a chunk framed twice),
+ * DCR_ERR_CAPACITY (*payload_size = bytes required), DCR_ERR_CUDA. */
+int dcr_encode_retry(const dcr_plan* plan, const void* xor_payload, size_t xor_size,
+                     const void* const* new_shards, void* payload, size_t payload_cap, size_t* payload_size,
+                     void* stream);
+
 /* dcr_apply without allocation.  No counterpart in the method's pages: it is
  * a deployment variant for receivers that cannot allocate device memory when
  * a refit arrives (an inference engine that reserved nearly all free HBM for
