@@ -26,7 +26,7 @@ REPLICATED, SPLIT_ROWS, SPLIT_COLS, RESIDUAL_QKV_INTERLEAVED = 0, 1, 2, 3
 LAYOUT_CANONICAL, LAYOUT_ROWGROUP_INTERLEAVE = 0, 1
 MODE_HYBRID, MODE_OVERWRITE_ONLY = 0, 1
 ENCODER_AUTO, ENCODER_WIDE, ENCODER_DEEP, ENCODER_CTA = 0, 1, 2, 3
-APPLY_AUTO, APPLY_WARP, APPLY_CTA = 0, 1, 2
+APPLY_AUTO, APPLY_WARP, APPLY_CTA, APPLY_LANE = 0, 1, 2, 3
 CODEC_LZ4, CODEC_SNAPPY = 0, 1
 PLAN_HOST_ONLY = 1
 NO_OVERFLOW = 0xFFFFFFFF
@@ -97,7 +97,8 @@ class Profile(ctypes.Structure):
     _fields_ = [("encode_ms", ctypes.c_float), ("finalize_ms", ctypes.c_float),
                 ("apply_ms", ctypes.c_float), ("defer_ms", ctypes.c_float),
                 ("pending_ms", ctypes.c_float), ("encode_valid", ctypes.c_uint32),
-                ("apply_valid", ctypes.c_uint32)]
+                ("apply_valid", ctypes.c_uint32), ("encode_kernels", ctypes.c_uint32),
+                ("apply_kernels", ctypes.c_uint32)]
 
 
 class PipelineStats(ctypes.Structure):

@@ -24,12 +24,11 @@
 //                 non-zero output bytes so far.  A frame that fails part-way is
 //                 undone (XOR is self-inverse) before it is reported.
 //   big_kernel    one warp per ZSRC frame too large for apply_kernel's
-//                 body cache or non-zero list (denser masks): the same walk
-//                 with the body read from global memory and the matches
-//                 checked against a bitmap of the non-zero output bytes.
-//   snappy_kernel one warp per ZSRC Snappy frame: serial element walk,
-//                 literal bytes XORed into the receiver, copies checked
-//                 against a bitmap of the non-zero output bytes.
+//                 body cache or non-zero list (denser masks), and per ZSRC
+//                 Snappy frame: the same walk (Snappy elements in place of
+//                 LZ4 sequences) with the body read from global memory and
+//                 the matches checked against a bitmap of the non-zero
+//                 output bytes.
 //   defer_kernel  one CTA per general LZ4 frame (any valid block, e.g. from
 //                 the CPU oracle) or Snappy frame: full decode into a 64 KiB shared buffer
 //                 with warp-parallel literal and match copies (a ZSRC frame
@@ -72,7 +71,9 @@ struct ApplyArgs {
     unsigned long long* state;
     ApplyScratch* sc;
     uint32_t* defer;          // deferred frames: general LZ4 from the front, large ZSRC from the back
+    uint32_t* lane;           // ZSRC frames for lane_kernel (defer_len entries)
     uint32_t defer_len;
+    uint64_t lane_min;        // frames in a stream from which lane_kernel takes its ZSRC frames
     uint64_t plan_hash;
     uint64_t version;
     uint64_t abort_at;
@@ -341,6 +342,143 @@ __device__ __forceinline__ uint32_t seq_end_ldg(const uint8_t* src, uint32_t n, 
     return q + (mlx ? 3u : 2u);
 }
 
+// How zsrc_apply reads a block: where its first element starts, where the
+// element starting at body byte p ends (| kEndFinal when the block ends
+// there, kEndBad when no valid element starts at p), an element's literal
+// run and match (off, ml; ml == 0: none), and how to replay the literal runs
+// of a frame's first elements (undo).
+//
+// LZ4 ("A strong baseline with the Blackwell-native DE": the LZ4 block
+// format): a sequence is a token, its literals, a 2-byte offset and the
+// match-length bytes; the last sequence is literals only.
+struct Lz4Walk {
+    __device__ static uint32_t first(const uint8_t*, uint32_t, uint32_t) { return 0; }
+    template <bool kGlobal>
+    __device__ static uint32_t end(const uint8_t* src, uint32_t n, uint32_t p)
+    {
+        return kGlobal ? seq_end_ldg(src, n, p) : seq_end(src, n, p);
+    }
+    __device__ static void decode(const uint8_t* src, uint32_t q, bool last, uint32_t& ipl, uint32_t& ll,
+                                  uint32_t& off, uint32_t& ml)
+    {
+        const uint32_t tok = src[q++];
+        ll = tok >> 4;
+        if (ll == 15) {
+            uint32_t b;
+            do {
+                b = src[q++];
+                ll += b;
+            } while (b == 255);
+        }
+        ipl = q;
+        q += ll;
+        off = ml = 0;
+        if (!last) {
+            off = uint32_t(src[q]) | (uint32_t(src[q + 1]) << 8);
+            q += 2;
+            ml = tok & 15u;
+            if (ml == 15) {
+                uint32_t b;
+                do {
+                    b = src[q++];
+                    ml += b;
+                } while (b == 255);
+            }
+            ml += 4;
+        }
+    }
+    __device__ static void undo(const ApplyArgs& A, const ChunkDesc& cd, const Seg* ds, const uint8_t* src, uint32_t,
+                                uint32_t, uint32_t lim, uint32_t runs, int lane)
+    {
+        zsrc_undo(A, cd, ds, src, lim, runs, lane);
+    }
+};
+
+// Snappy (the same section, footnote 4): a varint of the output length, then
+// literal elements (tag (length - 1) << 2, or 60..63 and 1..4 length bytes)
+// and copies (tag 1: length 4..11, 11-bit offset; tag 2 / 3: length 1..64,
+// 2- / 4-byte offset).  An element is a literal run or a copy.
+struct SnappyWalk {
+    __device__ static uint32_t first(const uint8_t* src, uint32_t n, uint32_t raw)
+    {
+        uint64_t v = 0;
+        uint32_t ip = 0;
+        for (uint32_t shift = 0; shift <= 28 && ip < n; shift += 7) {
+            const uint64_t b = src[ip++];
+            v |= (b & 127u) << shift;
+            if (!(b & 128u)) return v == raw ? ip : kEndBad;
+        }
+        return kEndBad;
+    }
+    template <bool>
+    __device__ static uint32_t end(const uint8_t* src, uint32_t n, uint32_t p)
+    {
+        if (p >= n) return kEndBad;
+        const uint32_t tag = src[p], t = tag & 3u;
+        uint64_t e;
+        if (t == 0) {
+            uint64_t len = (tag >> 2) + 1;
+            uint32_t nb = 0;
+            if ((tag >> 2) >= 60) {
+                nb = (tag >> 2) - 59;
+                if (uint64_t(p) + 1 + nb > n) return kEndBad;
+                len = 0;
+                for (uint32_t i = 0; i < nb; ++i) len |= uint64_t(src[p + 1 + i]) << (8 * i);
+                len += 1;
+            }
+            e = uint64_t(p) + 1 + nb + len;
+        } else {
+            e = uint64_t(p) + (t == 1 ? 2u : t == 2 ? 3u : 5u);
+        }
+        if (e > n) return kEndBad;
+        return e == n ? uint32_t(e) | kEndFinal : uint32_t(e);
+    }
+    __device__ static void decode(const uint8_t* src, uint32_t q, bool, uint32_t& ipl, uint32_t& ll, uint32_t& off,
+                                  uint32_t& ml)
+    {
+        const uint32_t tag = src[q], t = tag & 3u;
+        if (t == 0) {
+            uint32_t len = (tag >> 2) + 1, nb = 0;
+            if ((tag >> 2) >= 60) {
+                nb = (tag >> 2) - 59;
+                len = 0;
+                for (uint32_t i = 0; i < nb; ++i) len |= uint32_t(src[q + 1 + i]) << (8 * i);
+                len += 1;
+            }
+            ll = len;
+            ipl = q + 1 + nb;
+            off = ml = 0;
+        } else {
+            ll = 0;
+            ipl = q;
+            if (t == 1) {
+                ml = ((tag >> 2) & 7u) + 4;
+                off = ((tag >> 5) << 8) | src[q + 1];
+            } else {
+                ml = (tag >> 2) + 1;
+                off = 0;
+                for (uint32_t i = 0; i < (t == 2 ? 2u : 4u); ++i) off |= uint32_t(src[q + 1 + i]) << (8 * i);
+            }
+        }
+    }
+    __device__ static void undo(const ApplyArgs& A, const ChunkDesc& cd, const Seg* ds, const uint8_t* src, uint32_t n,
+                                uint32_t raw, uint32_t lim, uint32_t runs, int lane)
+    {
+        uint32_t q = first(src, n, raw), o = 0;
+        for (uint32_t r = 0; r < runs; ++r) {
+            uint32_t ipl, ll, off, ml;
+            decode(src, q, false, ipl, ll, off, ml);
+            for (uint32_t i = lane; i < ll; i += 32) {
+                const uint32_t b = src[ipl + i], x = o + i;
+                if (b && x < lim) xor_byte(A.target, dst_of(ds, cd.dst_count, x), b);
+            }
+            __syncwarp();
+            o += ll + ml;
+            q = end<true>(src, n, q) & ~kEndFinal;
+        }
+    }
+};
+
 // The warp takes the block a window of kWin body bytes at a time (WS::kWin:
 // 128 for apply_kernel, 160 for the denser frames of big_kernel): every lane
 // works out where a sequence starting at each of its window bytes would end
@@ -360,11 +498,13 @@ __device__ __forceinline__ uint32_t seq_end_ldg(const uint8_t* src, uint32_t n, 
 // kBitmap (big_kernel): the non-zero output bytes are kept as a bitmap over
 // the chunk instead of a sorted list, so there is no capacity limit, and src
 // may be the frame body in global memory.
-template <bool kBitmap, class WS>
+template <bool kBitmap, class WS, class Walk = Lz4Walk>
 __device__ int zsrc_apply(const ApplyArgs& A, const ChunkDesc& cd, const Seg* ds, const uint8_t* src,
                           uint32_t n, uint32_t raw, uint32_t lim, WS& W, int lane)
 {
-    if (n == 0) return 0;   // an LZ4 block holds at least one token
+    if (n == 0) return 0;   // a block holds at least one element
+    const uint32_t ip0 = Walk::first(src, n, raw);
+    if (ip0 == kEndBad) return 0;
     constexpr uint32_t kWin = WS::kWin;
     static_assert(kWin % 32 == 0 && kWin < kStop, "window: whole lane groups, offsets below kStop");
     const bool one = cd.dst_count == 1;
@@ -373,7 +513,7 @@ __device__ int zsrc_apply(const ApplyArgs& A, const ChunkDesc& cd, const Seg* ds
         for (uint32_t w = lane; w < (raw + 31) / 32; w += 32) W.bits[w] = 0;
         __syncwarp();
     }
-    uint32_t ip = 0, op = 0;      // next sequence in the body; its output position
+    uint32_t ip = ip0, op = 0;    // next sequence in the body; its output position
     uint32_t nev = 0, runs = 0;   // listed positions, literal runs applied
     uint32_t cs = 0, ce = 0;      // output bytes [cs, ce) known to be zero
     int status = 1;
@@ -381,7 +521,7 @@ __device__ int zsrc_apply(const ApplyArgs& A, const ChunkDesc& cd, const Seg* ds
         uint32_t e[kWin / 32];
 #pragma unroll
         for (uint32_t j = 0; j < kWin / 32; ++j)
-            e[j] = kBitmap ? seq_end_ldg(src, n, ip + 32 * j + lane) : seq_end(src, n, ip + 32 * j + lane);
+            e[j] = Walk::template end<kBitmap>(src, n, ip + 32 * j + lane);
 #pragma unroll
         for (uint32_t j = 0; j < kWin / 32; ++j) {
             const uint32_t x = e[j];
@@ -448,41 +588,16 @@ __device__ int zsrc_apply(const ApplyArgs& A, const ChunkDesc& cd, const Seg* ds
         const bool mine = lane < int(cnt);
         const bool lastseq = fin && lane == int(cnt) - 1;
         uint32_t ipl = 0, ll = 0, off = 0, ml = 0;
-        if (mine) {
-            uint32_t q = W.r_ip[lane];
-            const uint32_t tok = src[q++];
-            ll = tok >> 4;
-            if (ll == 15) {
-                uint32_t b;
-                do {
-                    b = src[q++];
-                    ll += b;
-                } while (b == 255);
-            }
-            ipl = q;
-            q += ll;
-            if (!lastseq) {
-                off = uint32_t(src[q]) | (uint32_t(src[q + 1]) << 8);
-                q += 2;
-                ml = tok & 15u;
-                if (ml == 15) {
-                    uint32_t b;
-                    do {
-                        b = src[q++];
-                        ml += b;
-                    } while (b == 255);
-                }
-                ml += 4;
-            }
-        }
+        if (mine) Walk::decode(src, W.r_ip[lane], lastseq, ipl, ll, off, ml);
         const uint32_t len = ll + ml;
         const uint32_t lincl = warp_incl_sum(len, lane);
         const uint32_t opl = op + lincl - len;   // output position of the literals
         const uint32_t mop = opl + ll;           // ... and of the match
         bool wrong = false;
         if (mine) {
-            if (lastseq) wrong = opl > raw || ll != raw - opl;
-            else wrong = opl > raw || ll > raw - opl || off == 0 || off > mop || ml > raw - mop;
+            wrong = opl > raw || ll > raw - opl;
+            if (ml) wrong = wrong || off == 0 || off > mop || ml > raw - mop;
+            if (lastseq) wrong = wrong || mop + ml != raw;   // the block ends exactly at the chunk's end
         }
         if (__any_sync(kFull, wrong)) {
             status = 0;
@@ -527,7 +642,7 @@ __device__ int zsrc_apply(const ApplyArgs& A, const ChunkDesc& cd, const Seg* ds
         // the match copies [mop - off, mop - off + min(ml, off)), repeated
         bool viol = false;
         if constexpr (kBitmap) {
-            if (mine && !lastseq) {
+            if (mine && ml) {
                 const uint32_t s0 = mop - off, e0 = s0 + (ml < off ? ml : off);
                 for (uint32_t w = s0 >> 5; w <= (e0 - 1) >> 5 && !viol; ++w) {
                     const uint32_t a = (w << 5) > s0 ? 0u : s0 - (w << 5);
@@ -543,7 +658,7 @@ __device__ int zsrc_apply(const ApplyArgs& A, const ChunkDesc& cd, const Seg* ds
             // found that way is kept
             bool look = false;
             uint32_t s0 = 0, e0 = 0, zs = 0, ze = 0;
-            if (mine && !lastseq) {
+            if (mine && ml) {
                 s0 = mop - off;
                 e0 = s0 + (ml < off ? ml : off);
                 if (off <= ll && e0 - s0 <= 4u) {
@@ -582,7 +697,7 @@ __device__ int zsrc_apply(const ApplyArgs& A, const ChunkDesc& cd, const Seg* ds
         if (fin) break;
         __syncwarp();   // the window and the batch are rewritten
     }
-    if (status != 1 && runs) zsrc_undo(A, cd, ds, src, lim, runs, lane);
+    if (status != 1 && runs) Walk::undo(A, cd, ds, src, n, raw, lim, runs, lane);
     return status;
 }
 
@@ -652,17 +767,20 @@ __global__ void __launch_bounds__(kAThreads) apply_kernel(ApplyArgs A)
                 if (!got && !to) atomicAdd(&A.sc->skipped, 1ull);
             }
             if (!__shfl_sync(0xffffffffu, got, 0)) continue;
-            // general LZ4 frames go to the full decode, ZSRC frames larger
-            // than the body cache to big_kernel
-            if (kind == kXorSnappy && (fflags & kFrameZsrc)) {   // snappy_kernel
-                if (lane == 0) A.defer[A.defer_len - 1 - atomicAdd(&A.sc->n_big, 1u)] = f;
-                continue;
-            }
-            if ((kind == kXorLz4 && !(fflags & kFrameZsrc)) || kind == kXorSnappy) {
+            // general LZ4 and Snappy frames go to the full decode.  ZSRC
+            // frames: to lane_kernel when the stream has frames enough to
+            // keep its threads busy; else Snappy ones and LZ4 ones larger
+            // than the body cache to big_kernel, the rest stay here
+            const bool zs = (fflags & kFrameZsrc) != 0;
+            if (kind != kXorRaw && !zs) {
                 if (lane == 0) A.defer[atomicAdd(&A.sc->n_defer, 1u)] = f;
                 continue;
             }
-            if (kind == kXorLz4 && bl > uint32_t(kBodyCache)) {
+            if (kind != kXorRaw && H.n_frames >= A.lane_min) {
+                if (lane == 0) A.lane[atomicAdd(&A.sc->n_lane, 1u)] = f;
+                continue;
+            }
+            if (kind == kXorSnappy || (kind == kXorLz4 && bl > uint32_t(kBodyCache))) {
                 if (lane == 0) A.defer[A.defer_len - 1 - atomicAdd(&A.sc->n_big, 1u)] = f;
                 continue;
             }
@@ -1221,14 +1339,16 @@ __global__ void __launch_bounds__(kBThreads, 3) big_kernel(ApplyArgs A)
         const uint32_t f = A.defer[A.defer_len - 1 - j];
         const uint64_t fo = ld64(p + idx_off + 8ull * f);
         const uint4 h0 = ld_nc16(p + fo), h1 = ld_nc16(p + fo + 16);
-        if ((h0.y & 0xFFu) == kXorSnappy) continue;   // snappy_kernel's
+        const bool sn = (h0.y & 0xFFu) == kXorSnappy;   // ZSRC Snappy frames walk the same way
         const uint32_t c = h0.z, raw = h0.w, bl = h1.x;
         const ChunkDesc cd = A.chunks[c];
         const bool cut = uint64_t(f) == A.abort_at;
         const uint32_t ub = cd.bits == 16 ? 2u : 1u;
         uint32_t lim = cut ? (A.split < raw ? A.split : raw) : raw;
         lim -= lim % ub;
-        const int r = zsrc_apply<true>(A, cd, A.dst + cd.dst_begin, p + fo + kFrameHdr, bl, raw, lim, W, lane);
+        const uint8_t* body = p + fo + kFrameHdr;
+        const int r = sn ? zsrc_apply<true, BWarp, SnappyWalk>(A, cd, A.dst + cd.dst_begin, body, bl, raw, lim, W, lane)
+                         : zsrc_apply<true, BWarp>(A, cd, A.dst + cd.dst_begin, body, bl, raw, lim, W, lane);
         __syncwarp();   // the bitmap is reused by the next frame
         if (lane == 0) {
             if (r != 1) {
@@ -1243,159 +1363,366 @@ __global__ void __launch_bounds__(kBThreads, 3) big_kernel(ApplyArgs A)
     }
 }
 
-// ZSRC Snappy frames (every copy copies zero bytes): one warp per frame walks
-// the elements in order (all lanes read each tag), XORs the non-zero literal
-// bytes into the receiver and marks them in a bitmap of the chunk's output,
-// and checks that each copy's source holds no marked byte.  Returns 1 if
-// applied; 0 if malformed or lying, after undoing the literals it applied
-// (XOR is self-inverse).
-__device__ int snappy_zsrc_apply(const ApplyArgs& A, const ChunkDesc& cd, const Seg* ds, const uint8_t* src,
-                                 uint32_t n, uint32_t raw, uint32_t lim, uint32_t* bits, int lane)
+// ---- ZSRC frames, one thread each -----------------------------------------
+// In a ZSRC block every match (LZ4) or copy (Snappy) copies zero bytes, so
+// the non-zero output bytes are literal bytes.  lane_kernel gives each frame
+// one thread, which walks the block in order as a serial decoder would but
+// writes only the non-zero literal bytes (XORed into the receiver, combined
+// per 32-bit word).  Of the output so far it keeps a few zero stretches:
+// every byte from z1 on (one past the last non-zero byte), the bytes [g0, g1)
+// between the last two non-zero bytes, and the longest zero runs the
+// library's encoder copies from (LaneOut).  A match whose source lies inside
+// one of them provably copies zeros.  For one that does not, and for a malformed
+// block, the thread undoes what it XORed (XOR is self-inverse) and passes the
+// frame to big_kernel, whose bitmap check over the whole output decides.
+// Per element this costs a few dozen instructions of one thread, against a
+// warp's worth in the cooperative walks, which pays when a window has many
+// frames.
+constexpr int kLThreads = 128;
+
+// 16 bytes through the non-coherent path, asking L2 for the 256-byte
+// stretch around them (the walk reads on in order)
+__device__ __forceinline__ uint4 ld_nc16_run(const uint8_t* p)
 {
-    const bool one = cd.dst_count == 1;
-    const uint64_t base = one ? ds[0].addr - ds[0].off : 0ull;
-    for (uint32_t w = lane; w < (raw + 31) / 32; w += 32) bits[w] = 0;
-    __syncwarp();
-    uint32_t ip = 0, op = 0;
-    uint64_t v = 0;
-    bool ok = false;
-    for (uint32_t shift = 0; shift <= 28 && ip < n; shift += 7) {
-        const uint64_t b = src[ip++];
-        v |= (b & 127u) << shift;
-        if (!(b & 128u)) {
-            ok = true;
-            break;
-        }
-    }
-    ok = ok && v == raw;
-    const uint32_t first = ip;   // the first element
-    uint32_t applied = ip;       // literal elements before this byte have been applied
-    while (ok && ip < n) {
-        const uint32_t tag = src[ip++];
-        if ((tag & 3u) == 0) {
-            uint64_t len = (tag >> 2) + 1;
-            if ((tag >> 2) >= 60) {
-                const uint32_t nb = (tag >> 2) - 59;
-                if (nb > n - ip) { ok = false; break; }
-                len = 0;
-                for (uint32_t i = 0; i < nb; ++i) len |= uint64_t(src[ip + i]) << (8 * i);
-                len += 1;
-                ip += nb;
-            }
-            if (len > n - ip || len > raw - op) { ok = false; break; }
-            for (uint32_t i = lane; i < uint32_t(len); i += 32) {
-                const uint32_t b = src[ip + i];
-                if (b) {
-                    const uint32_t x = op + i;
-                    atomicOr(&bits[x >> 5], 1u << (x & 31));
-                    if (x < lim) xor_byte(A.target, one ? base + x : dst_of(ds, cd.dst_count, x), b);
-                }
-            }
-            __syncwarp();
-            ip += uint32_t(len);
-            op += uint32_t(len);
-            applied = ip;
-            continue;
-        }
-        uint32_t len, off;
-        if ((tag & 3u) == 1) {
-            if (ip >= n) { ok = false; break; }
-            len = ((tag >> 2) & 7u) + 4;
-            off = ((tag >> 5) << 8) | src[ip++];
-        } else {
-            const uint32_t nb = (tag & 3u) == 2 ? 2u : 4u;
-            if (nb > n - ip) { ok = false; break; }
-            len = (tag >> 2) + 1;
-            off = 0;
-            for (uint32_t i = 0; i < nb; ++i) off |= uint32_t(src[ip + i]) << (8 * i);
-            ip += nb;
-        }
-        if (off == 0 || off > op || len > raw - op) { ok = false; break; }
-        // the copy's source [op - off, + min(len, off)) holds no non-zero byte
-        const uint32_t s0 = op - off, e0 = s0 + (len < off ? len : off);
-        bool viol = false;
-        for (uint32_t w = (s0 >> 5) + lane; w <= (e0 - 1) >> 5; w += 32) {
-            const uint32_t a = (w << 5) > s0 ? 0u : s0 - (w << 5);
-            const uint32_t b = ((w + 1) << 5) < e0 ? 32u : e0 - (w << 5);
-            const uint32_t m = (b == 32 ? 0xFFFFFFFFu : ((1u << b) - 1)) & ~((1u << a) - 1);
-            viol |= (bits[w] & m) != 0;
-        }
-        if (__reduce_or_sync(kFull, uint32_t(viol))) { ok = false; break; }
-        op += len;
-    }
-    ok = ok && op == raw;
-    if (!ok) {
-        // replay the literal elements already applied (validated the first time)
-        for (uint32_t q = first, o = 0; q < applied;) {
-            const uint32_t tag = src[q++];
-            if ((tag & 3u) == 0) {
-                uint32_t len = (tag >> 2) + 1;
-                if ((tag >> 2) >= 60) {
-                    const uint32_t nb = (tag >> 2) - 59;
-                    len = 0;
-                    for (uint32_t i = 0; i < nb; ++i) len |= uint32_t(src[q + i]) << (8 * i);
-                    len += 1;
-                    q += nb;
-                }
-                for (uint32_t i = lane; i < len; i += 32) {
-                    const uint32_t b = src[q + i];
-                    const uint32_t x = o + i;
-                    if (b && x < lim) xor_byte(A.target, one ? base + x : dst_of(ds, cd.dst_count, x), b);
-                }
-                __syncwarp();
-                q += len;
-                o += len;
-            } else {
-                const uint32_t t = tag & 3u;
-                o += t == 1 ? ((tag >> 2) & 7u) + 4 : (tag >> 2) + 1;
-                q += t == 1 ? 1u : t == 2 ? 2u : 4u;
-            }
-        }
-    }
-    return ok ? 1 : 0;
+    uint4 v;
+    asm("ld.global.nc.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
+        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+        : "l"(p));
+    return v;
 }
 
-constexpr int kSnWarps = 8;   // 8 KiB bitmap per warp
+// The body, read in order 16 bytes at a time with the next 16 in flight.
+struct LaneRd {
+    const uint8_t* b;
+    uint32_t nblk;   // 16-byte blocks of the body (the frame is padded to 16)
+    uint32_t blk;    // block in w0
+    uint4 w0, w1;    // blocks blk, blk + 1
+    __device__ __forceinline__ void init(const uint8_t* body, uint32_t n)
+    {
+        b = body;
+        nblk = (n + 15) >> 4;
+        blk = 0;
+        w0 = nblk > 0 ? ld_nc16_run(b) : make_uint4(0, 0, 0, 0);
+        w1 = nblk > 1 ? ld_nc16_run(b + 16) : make_uint4(0, 0, 0, 0);
+    }
+    __device__ __forceinline__ uint32_t at(uint32_t i)
+    {
+        const uint32_t k = i >> 4;
+        if (k != blk) {
+            w0 = k == blk + 1 ? w1 : ld_nc16_run(b + 16ull * k);
+            blk = k;
+            if (k + 1 < nblk) w1 = ld_nc16_run(b + 16ull * (k + 1));
+        }
+        const uint32_t v = (i & 8) ? ((i & 4) ? w0.w : w0.z) : ((i & 4) ? w0.y : w0.x);
+        return __byte_perm(v, 0, 0x4440u | (i & 3u));
+    }
+};
 
-__global__ void __launch_bounds__(32 * kSnWarps, 3) snappy_kernel(ApplyArgs A)
+// Receiver address of canonical chunk offset x, for x that never decreases.
+struct LaneDst {
+    const Seg* s;
+    uint32_t n, i, next;
+    uint64_t base;
+    __device__ __forceinline__ void init(const Seg* ds, uint32_t cnt)
+    {
+        s = ds;
+        n = cnt;
+        i = 0;
+        base = s[0].addr - s[0].off;
+        next = n > 1 ? s[1].off : 0xFFFFFFFFu;
+    }
+    __device__ __forceinline__ uint64_t addr(uint32_t x)
+    {
+        while (x >= next) {
+            ++i;
+            base = s[i].addr - s[i].off;
+            next = i + 1 < n ? s[i + 1].off : 0xFFFFFFFFu;
+        }
+        return base + x;
+    }
+};
+
+// XOR bytes into the receiver, one reduction per 32-bit word touched in a row.
+struct LaneXor {
+    uint8_t* t;
+    uint64_t wa;
+    uint32_t wv;
+    __device__ __forceinline__ void flush()
+    {
+        if (wv) asm volatile("red.global.xor.b32 [%0], %1;" ::"l"(t + wa), "r"(wv) : "memory");
+        wv = 0;
+    }
+    __device__ __forceinline__ void add(uint64_t a, uint32_t b)
+    {
+        const uint64_t w = a & ~3ull;   // the arena is 16-byte aligned
+        if (w != wa) {
+            flush();
+            wa = w;
+        }
+        wv ^= b << (8 * (a & 3));
+    }
+};
+
+// What a walk knows of the output: op bytes so far, zero from z1 on and in
+// [g0, g1); the literal bytes below `done` have been XORed.  Also the zero
+// stretch before each non-zero byte (its "gap"), counted in groups of 32
+// non-zero bytes: the longest gap of the current group (cur) and of all
+// earlier groups (best), as length << 32 | start.
+struct LaneOut {
+    uint32_t op, z1, g0, g1, done, ev;
+    unsigned long long cur, best;
+};
+
+// One literal run of ll bytes at body offset ip.  kUndo: XOR again the bytes
+// below upto (the first walk's `done`), nothing else.
+//
+// The gaps follow the library's encoder: it copies a zero run from the
+// longest gap of the earlier groups of 32 non-zero bytes, from the gap just
+// before (Snappy), or from a zero it keeps as a literal (offset 1); each of
+// those sources is one of the stretches kept here.
+template <bool kUndo>
+__device__ __forceinline__ void lane_literals(LaneRd& R, LaneDst& D, LaneXor& X, LaneOut& O, uint32_t ip,
+                                              uint32_t ll, uint32_t lim, uint32_t upto)
 {
-    extern __shared__ __align__(16) uint32_t bitmaps[];
-    uint32_t* bits = bitmaps + (threadIdx.x >> 5) * (kChunk / 32);
-    const int lane = threadIdx.x & 31;
+    for (uint32_t q = 0; q < ll; ++q) {
+        const uint32_t b = R.at(ip + q);
+        if (b) {
+            const uint32_t x = O.op + q;
+            if (kUndo && x >= upto) break;
+            if (!kUndo) {
+                const unsigned long long gap = ((unsigned long long)(x - O.z1) << 32) | O.z1;
+                if (gap > O.cur) O.cur = gap;
+                if ((++O.ev & 31u) == 0) {
+                    if (O.cur > O.best) O.best = O.cur;
+                    O.cur = 0;
+                }
+                O.g0 = O.z1;
+                O.g1 = x;
+                O.z1 = x + 1;
+            }
+            if (x < lim) X.add(D.addr(x), b);
+        }
+    }
+    O.op += ll;
+    if (!kUndo) O.done = O.op;
+}
+
+// A match of ml bytes from off back at output O.op: 1 if it is in bounds and
+// provably copies zeros.
+__device__ __forceinline__ bool lane_match(const LaneOut& O, uint32_t off, uint32_t ml, uint32_t raw)
+{
+    if (off == 0 || off > O.op || ml > raw - O.op) return false;
+    const uint32_t s0 = O.op - off, e0 = s0 + (ml < off ? ml : off);
+    const uint32_t bs = uint32_t(O.best), be = bs + uint32_t(O.best >> 32);
+    const uint32_t cs = uint32_t(O.cur), ce = cs + uint32_t(O.cur >> 32);
+    return s0 >= O.z1 || (s0 >= O.g0 && e0 <= O.g1) || (s0 >= bs && e0 <= be) || (s0 >= cs && e0 <= ce);
+}
+
+// A walk's state: the body reader, the receiver pieces, the XOR combiner,
+// what is known of the output, the next body byte.
+struct LaneWalk {
+    LaneRd R;
+    LaneDst D;
+    LaneXor X;
+    LaneOut O;
+    uint32_t ip, n, raw, lim, upto;
+    bool sn;   // Snappy (else LZ4)
+    __device__ __forceinline__ void init(bool snappy, const uint8_t* body, const Seg* ds, uint32_t dcnt,
+                                         uint8_t* target, uint32_t bl, uint32_t raw_len, uint32_t limit,
+                                         uint32_t undo_to)
+    {
+        R.init(body, bl);
+        D.init(ds, dcnt);
+        X = LaneXor{target, ~0ull, 0u};
+        O = LaneOut{0, 0, 0, 0, 0, 0, 0ull, 0ull};
+        ip = 0;
+        n = bl;
+        raw = raw_len;
+        lim = limit;
+        upto = undo_to;
+        sn = snappy;
+    }
+};
+
+// What one step of a walk found.
+enum LaneStep : int { kLGo = 0, kLValid = 1, kLStop = 2 };
+
+// One LZ4 sequence (the same block format as the other walks).  kLStop: the
+// block is malformed or a match is not proven to copy zeros, or (kUndo) the
+// replay has reached `upto`.
+template <bool kUndo>
+__device__ __forceinline__ int lz4_step(LaneWalk& W)
+{
+    if (kUndo && W.O.op >= W.upto) return kLStop;
+    if (W.ip >= W.n) return kLStop;
+    const uint32_t tok = W.R.at(W.ip++);
+    uint32_t ll = tok >> 4;
+    if (ll == 15) {
+        uint32_t b;
+        do {
+            if (W.ip >= W.n) return kLStop;
+            b = W.R.at(W.ip++);
+            ll += b;
+        } while (b == 255);
+    }
+    if (ll > W.n - W.ip || ll > W.raw - W.O.op) return kLStop;
+    lane_literals<kUndo>(W.R, W.D, W.X, W.O, W.ip, ll, W.lim, W.upto);
+    W.ip += ll;
+    if (W.ip == W.n) return W.O.op == W.raw ? kLValid : kLStop;
+    if (kUndo && W.O.op >= W.upto) return kLStop;
+    if (W.n - W.ip < 2) return kLStop;
+    uint32_t off = W.R.at(W.ip);
+    off |= W.R.at(W.ip + 1) << 8;
+    W.ip += 2;
+    uint32_t ml = tok & 15u;
+    if (ml == 15) {
+        uint32_t b;
+        do {
+            if (W.ip >= W.n) return kLStop;
+            b = W.R.at(W.ip++);
+            ml += b;
+        } while (b == 255);
+    }
+    ml += 4;
+    if (!kUndo && !lane_match(W.O, off, ml, W.raw)) return kLStop;
+    W.O.op += ml;
+    return kLGo;
+}
+
+// The Snappy preamble: the output length as a varint, equal to raw.
+__device__ __forceinline__ bool snappy_pre(LaneWalk& W)
+{
+    uint64_t v = 0;
+    for (uint32_t shift = 0; shift <= 28 && W.ip < W.n; shift += 7) {
+        const uint32_t b = W.R.at(W.ip++);
+        v |= uint64_t(b & 127u) << shift;
+        if (!(b & 128u)) return v == W.raw;
+    }
+    return false;
+}
+
+// One Snappy element: a literal run (1..4 length bytes past 60) or a copy.
+template <bool kUndo>
+__device__ __forceinline__ int snappy_step(LaneWalk& W)
+{
+    if (W.ip == W.n) return W.O.op == W.raw ? kLValid : kLStop;
+    if (kUndo && W.O.op >= W.upto) return kLStop;
+    const uint32_t tag = W.R.at(W.ip++), t = tag & 3u;
+    if (t == 0) {
+        uint32_t len = (tag >> 2) + 1;
+        if ((tag >> 2) >= 60) {
+            const uint32_t nb = (tag >> 2) - 59;
+            if (nb > W.n - W.ip) return kLStop;
+            uint64_t L = 0;
+            for (uint32_t i = 0; i < nb; ++i) L |= uint64_t(W.R.at(W.ip + i)) << (8 * i);
+            W.ip += nb;
+            if (L >= W.raw) return kLStop;
+            len = uint32_t(L) + 1;
+        }
+        if (len > W.n - W.ip || len > W.raw - W.O.op) return kLStop;
+        lane_literals<kUndo>(W.R, W.D, W.X, W.O, W.ip, len, W.lim, W.upto);
+        W.ip += len;
+        return kLGo;
+    }
+    uint32_t len, off;
+    if (t == 1) {
+        if (W.ip >= W.n) return kLStop;
+        len = ((tag >> 2) & 7u) + 4;
+        off = ((tag >> 5) << 8) | W.R.at(W.ip++);
+    } else {
+        const uint32_t nb = t == 2 ? 2u : 4u;
+        if (nb > W.n - W.ip) return kLStop;
+        len = (tag >> 2) + 1;
+        off = 0;
+        for (uint32_t i = 0; i < nb; ++i) off |= W.R.at(W.ip + i) << (8 * i);
+        W.ip += nb;
+    }
+    if (!kUndo && !lane_match(W.O, off, len, W.raw)) return kLStop;
+    W.O.op += len;
+    return kLGo;
+}
+
+// The warp's lanes step their walks together, one sequence or element per
+// lane per round, so that the warp runs converged between rounds.
+template <bool kUndo>
+__device__ __forceinline__ void lane_run(LaneWalk& W, bool act, int& res)
+{
+    while (__any_sync(kFull, act)) {
+        if (act) {
+            const int r = W.sn ? snappy_step<kUndo>(W) : lz4_step<kUndo>(W);
+            if (r != kLGo) {
+                act = false;
+                res = r;
+            }
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kLThreads) lane_kernel(ApplyArgs A)
+{
     if (!A.sc->hdr_ok) return;
-    const uint32_t nbig = A.sc->n_big;   // final: written by apply_kernel only
-    if (nbig == 0) return;
+    const uint32_t nl = A.sc->n_lane;   // final: written by apply_kernel only
+    if (nl == 0) return;
     const uint8_t* p = A.payload;
     const uint64_t total = ld64(p + 56), nf = ld64(p + 48), idx_off = total - 8 * nf;
     const uint64_t V = ld64(p + 24);
-    for (;;) {
-        uint32_t j = 0;
-        if (lane == 0) j = atomicAdd(&A.sc->snappy_ticket, 1u);
-        j = __shfl_sync(kFull, j, 0);
-        if (j >= nbig) break;
-        const uint32_t f = A.defer[A.defer_len - 1 - j];
-        const uint64_t fo = ld64(p + idx_off + 8ull * f);
-        const uint4 h0 = ld_nc16(p + fo), h1 = ld_nc16(p + fo + 16);
-        if ((h0.y & 0xFFu) != kXorSnappy) continue;   // big_kernel's
-        const uint32_t c = h0.z, raw = h0.w, bl = h1.x;
-        const ChunkDesc cd = A.chunks[c];
-        const bool cut = uint64_t(f) == A.abort_at;
-        const uint32_t ub = cd.bits == 16 ? 2u : 1u;
-        uint32_t lim = cut ? (A.split < raw ? A.split : raw) : raw;
-        lim -= lim % ub;
-        const int r = snappy_zsrc_apply(A, cd, A.dst + cd.dst_begin, p + fo + kFrameHdr, bl, raw, lim, bits, lane);
-        __syncwarp();   // the bitmap is reused by the next frame
-        if (lane == 0) {
-            if (r != 1) {
-                report(A.sc, DCR_ERR_CORRUPT);
-            } else {
-                atomicAdd(&A.sc->applied, 1ull);
-                __threadfence();
-                if (cut) A.sc->aborted = 1;
-                else atomicExch(&A.state[c], (V << 2) | kDone);
-            }
+    const int lane = threadIdx.x & 31;
+    // 32 consecutive list entries per warp, spread over the blocks first
+    const uint32_t wpb = kLThreads / 32, nw = gridDim.x * wpb;
+    uint32_t applied = 0;
+    for (uint32_t g = (threadIdx.x >> 5) * gridDim.x + blockIdx.x; 32ull * g < nl; g += nw) {
+        const uint32_t j = 32 * g + lane;
+        const bool mine = j < nl;
+        LaneWalk W;
+        uint32_t f = 0, c = 0;
+        bool cut = false, act = false;
+        int res = kLStop;
+        const uint8_t* body = nullptr;
+        const Seg* ds = nullptr;
+        uint32_t dcnt = 1;
+        if (mine) {
+            f = A.lane[j];
+            const uint64_t fo = ld64(p + idx_off + 8ull * f);
+            const uint4 h0 = ld_nc16(p + fo), h1 = ld_nc16(p + fo + 16);
+            const uint32_t raw = h0.w;
+            c = h0.z;
+            const ChunkDesc cd = A.chunks[c];
+            cut = uint64_t(f) == A.abort_at;
+            const uint32_t ub = cd.bits == 16 ? 2u : 1u;
+            uint32_t lim = cut ? (A.split < raw ? A.split : raw) : raw;
+            lim -= lim % ub;
+            body = p + fo + kFrameHdr;
+            ds = A.dst + cd.dst_begin;
+            dcnt = cd.dst_count;
+            W.init((h0.y & 0xFFu) == kXorSnappy, body, ds, dcnt, A.target, h1.x, raw, lim, 0);
+            act = !W.sn || snappy_pre(W);
         }
+        lane_run<false>(W, act, res);
+        if (mine) W.X.flush();
+        const bool ok = mine && res == kLValid;
+        if (ok) {
+            ++applied;
+            __threadfence();
+            if (cut) A.sc->aborted = 1;
+            else atomicExch(&A.state[c], (V << 2) | kDone);
+        }
+        // a frame that is not proven: XOR its literals again (the bytes below
+        // the first walk's `done`), then big_kernel decides
+        const bool undo = mine && !ok && W.O.done > 0;
+        if (__any_sync(kFull, undo)) {
+            bool act2 = false;
+            if (undo) {
+                W.init(W.sn, body, ds, dcnt, A.target, W.n, W.raw, W.lim, W.O.done);
+                act2 = !W.sn || snappy_pre(W);
+            }
+            int r2 = kLStop;
+            lane_run<true>(W, act2, r2);
+            if (undo) W.X.flush();
+        }
+        if (mine && !ok) A.defer[A.defer_len - 1 - atomicAdd(&A.sc->n_big, 1u)] = f;
     }
+    applied = __reduce_add_sync(kFull, applied);
+    if (lane == 0 && applied) atomicAdd(&A.sc->applied, (unsigned long long)applied);
 }
 
 // Commit rule: every chunk with a frame in the stream is DONE for the target.
@@ -1440,12 +1767,10 @@ int apply_kernel_config(KernelConfig* kc)
     if (e == cudaSuccess)
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&kc->big_blocks_per_sm, big_kernel, kBThreads,
                                                           sizeof(BWarp) * kBWarps);
+    if (e == cudaSuccess)   // no shared memory: all of it as L1 for the bodies
+        e = cudaFuncSetAttribute(lane_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 0);
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(snappy_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 int(kSnWarps * kChunk / 8));
-    if (e == cudaSuccess)
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&kc->snappy_blocks_per_sm, snappy_kernel, 32 * kSnWarps,
-                                                          kSnWarps * kChunk / 8);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&kc->lane_blocks_per_sm, lane_kernel, kLThreads, 0);
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(apply_cta_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(sizeof(CSmem)));
     if (e == cudaSuccess)
@@ -1458,10 +1783,10 @@ int apply_kernel_config(KernelConfig* kc)
         e = cudaFuncGetAttributes(&fa, pending_kernel);
     }
     if (e != cudaSuccess) return cuda_error(e, "apply kernel configuration");
-    if (kc->snappy_blocks_per_sm < 1) kc->snappy_blocks_per_sm = 1;
     if (kc->apply_blocks_per_sm < 1) kc->apply_blocks_per_sm = 1;
     if (kc->apply_cta_blocks_per_sm < 1) kc->apply_cta_blocks_per_sm = 1;
     if (kc->big_blocks_per_sm < 1) kc->big_blocks_per_sm = 1;
+    if (kc->lane_blocks_per_sm < 1) kc->lane_blocks_per_sm = 1;
     if (kc->defer_blocks_per_sm < 1) kc->defer_blocks_per_sm = 1;
     return DCR_OK;
 }
@@ -1486,6 +1811,18 @@ void launch_first(const dcr_plan* P, const ApplyArgs& A, cudaStream_t s)
 
 namespace {
 
+// Frames in a stream from which apply_kernel hands its ZSRC frames to
+// lane_kernel.  lane_kernel walks a frame in one thread, several times
+// slower than a big_kernel warp walks it but with a tenth of the
+// instructions: it wins once the stream holds more than about four frames
+// per big_kernel warp.
+uint64_t lane_min_frames(const dcr_plan* P)
+{
+    if (P->apply == DCR_APPLY_LANE) return 0;
+    if (P->apply == DCR_APPLY_WARP) return UINT64_MAX;
+    return 4ull * P->kc.num_sms * P->kc.big_blocks_per_sm * kBWarps;
+}
+
 ApplyArgs make_args(const dcr_plan* P, dcr_recv_state* st, const void* payload, size_t size, void* target,
                     uint64_t abort_at, uint32_t split, int retry_only)
 {
@@ -1501,6 +1838,8 @@ ApplyArgs make_args(const dcr_plan* P, dcr_recv_state* st, const void* payload, 
     A.state = reinterpret_cast<unsigned long long*>(st->d_chunk_state);
     A.sc = st->d_scratch;
     A.defer = st->d_defer;
+    A.lane = st->d_defer + (P->max_window_chunks + 1);
+    A.lane_min = lane_min_frames(P);
     A.defer_len = uint32_t(P->max_window_chunks + 1);
     A.plan_hash = P->hash;
     A.version = st->version;
@@ -1509,14 +1848,16 @@ ApplyArgs make_args(const dcr_plan* P, dcr_recv_state* st, const void* payload, 
     return A;
 }
 
-// the kernels of the frames the first kernel deferred (general LZ4 and
-// Snappy frames, large ZSRC frames, ZSRC Snappy frames)
+// the kernels of the frames the first kernel deferred: general LZ4 and
+// Snappy frames; ZSRC frames for lane_kernel; then the ZSRC frames that
+// lane_kernel could not prove, and those the CTA kernel passes on, for
+// big_kernel
 void launch_deferred(const dcr_plan* P, const ApplyArgs& A, cudaStream_t s)
 {
     const int sms = P->kc.num_sms;
     defer_kernel<<<sms * P->kc.defer_blocks_per_sm, kDThreads, kChunk, s>>>(A);
+    lane_kernel<<<sms * P->kc.lane_blocks_per_sm, kLThreads, 0, s>>>(A);
     big_kernel<<<sms * P->kc.big_blocks_per_sm, kBThreads, sizeof(BWarp) * kBWarps, s>>>(A);
-    snappy_kernel<<<sms * P->kc.snappy_blocks_per_sm, 32 * kSnWarps, kSnWarps * kChunk / 8, s>>>(A);
 }
 
 }  // namespace
@@ -1571,7 +1912,7 @@ namespace {
 constexpr uint32_t kNoallocMaxChunks = 65536;    // window limit: 4 GiB of canonical bytes
 constexpr size_t kNoallocHead = 256;             // ApplyScratch, padded
 static_assert(sizeof(ApplyScratch) <= kNoallocHead, "counters fit the head");
-constexpr size_t kNoallocBytes = kNoallocHead + 4 * (size_t(kNoallocMaxChunks) + 1);   // 256 KiB + 260 B
+constexpr size_t kNoallocBytes = kNoallocHead + 8 * (size_t(kNoallocMaxChunks) + 1);   // 512 KiB + 264 B
 
 // [0, 256): ApplyScratch, cleared by a memset on the caller's stream at the
 // start of every call; [256, ...): deferred frame list, written before read.
@@ -1674,6 +2015,8 @@ int apply_launch_noalloc(const dcr_plan* P, dcr_recv_state* st, const void* payl
     A.sc = static_cast<ApplyScratch*>(base);
     A.defer = reinterpret_cast<uint32_t*>(static_cast<unsigned char*>(base) + kNoallocHead);
     A.defer_len = kNoallocMaxChunks + 1;
+    A.lane = A.defer + A.defer_len;
+    A.lane_min = lane_min_frames(P);
     A.plan_hash = P->hash;
     A.version = st->version;
     A.abort_at = DCR_NO_FAULT;
@@ -1683,8 +2026,8 @@ int apply_launch_noalloc(const dcr_plan* P, dcr_recv_state* st, const void* payl
     const int sms = P->kc.num_sms;
     launch_first(P, A, s);
     defer_kernel<<<sms * P->kc.defer_blocks_per_sm, kDThreads, kChunk, s>>>(A);
+    lane_kernel<<<sms * P->kc.lane_blocks_per_sm, kLThreads, 0, s>>>(A);
     big_kernel<<<sms * P->kc.big_blocks_per_sm, kBThreads, sizeof(BWarp) * kBWarps, s>>>(A);
-    snappy_kernel<<<sms * P->kc.snappy_blocks_per_sm, 32 * kSnWarps, kSnWarps * kChunk / 8, s>>>(A);
     pending_kernel<<<sms, 256, 0, s>>>(A);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_error(e, "apply launch");

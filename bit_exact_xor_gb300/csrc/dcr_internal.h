@@ -118,7 +118,7 @@ struct ApplyScratch {
     uint64_t target_version;
     uint64_t n_frames;
     uint32_t big_ticket;
-    uint32_t snappy_ticket; // snappy_kernel's walk over the same list
+    uint32_t n_lane;        // ZSRC frames listed for lane_kernel
 };
 
 // Chunk state of a receiver: (target_version << 2) | state.
@@ -143,7 +143,7 @@ struct KernelConfig {
     int apply_cta_blocks_per_sm = 0;
     int defer_blocks_per_sm = 0;
     int big_blocks_per_sm = 0;
-    int snappy_blocks_per_sm = 0;
+    int lane_blocks_per_sm = 0;
 };
 
 // host entry points of the kernel translation units
@@ -172,6 +172,11 @@ int apply_launch(const struct ::dcr_plan* plan, struct ::dcr_recv_state* st, con
 // kApplyDeferred = the deferred-frame kernels and the commit check again;
 // kApplyAll = all of them (what apply_launch launches)
 enum { kApplyAll = 0, kApplyFirst = 1, kApplyDeferred = 2 };
+// kernels one call launches: dcr_encode (encode, scan, copy, restream,
+// spill), dcr_encode_retry (retry, scan, copy, retry spill), dcr_apply
+// (first kernel and commit check; with deferred frames also the defer, lane
+// and big kernels and the commit check again)
+constexpr uint32_t kEncodeKernels = 5, kRetryKernels = 4, kApplyKernels = 2, kApplyKernelsDeferred = 6;
 int apply_launch_part(const struct ::dcr_plan* plan, struct ::dcr_recv_state* st, const void* payload,
                       size_t size, void* target, uint64_t abort_at, uint32_t split, int retry_only, int part,
                       cudaStream_t s);
@@ -264,6 +269,6 @@ struct dcr_recv_state {
     std::vector<uint8_t> win_done;
     uint64_t* d_chunk_state = nullptr;  // n_chunks
     dcr::ApplyScratch* d_scratch = nullptr;
-    uint32_t* d_defer = nullptr;        // max_window_chunks
+    uint32_t* d_defer = nullptr;        // 2 x (max_window_chunks + 1): deferred frames, lane_kernel's list
     dcr::ApplyScratch* h_scratch = nullptr;  // pinned
 };

@@ -230,7 +230,7 @@ extern "C" int dcr_plan_build(const dcr_tensor_desc* tensors, size_t n, const dc
     const uint32_t flags = opts ? opts->flags : 0u;
     const uint32_t apply = opts ? opts->apply : uint32_t(DCR_APPLY_AUTO);
     const uint32_t overflow_kib = opts ? opts->overflow_kib : 0u;
-    if (apply > DCR_APPLY_CTA) return set_error(DCR_ERR_INVALID, "unknown apply variant %u", apply);
+    if (apply > DCR_APPLY_LANE) return set_error(DCR_ERR_INVALID, "unknown apply variant %u", apply);
     if (flags & ~uint32_t(DCR_PLAN_HOST_ONLY)) return set_error(DCR_ERR_INVALID, "unknown plan flags %#x", flags);
     dcr_plan* P = new (std::nothrow) dcr_plan();
     if (!P) return set_error(DCR_ERR_NOMEM, "dcr_plan_build: out of host memory");
@@ -497,7 +497,7 @@ extern "C" int dcr_recv_state_create(const dcr_plan* p, uint64_t version, dcr_re
     if ((e = cudaMalloc(&s->d_chunk_state, (p->n_chunks ? p->n_chunks : 1) * 8)) != cudaSuccess ||
         (e = cudaMemset(s->d_chunk_state, 0, (p->n_chunks ? p->n_chunks : 1) * 8)) != cudaSuccess ||
         (e = cudaMalloc(&s->d_scratch, sizeof(ApplyScratch))) != cudaSuccess ||
-        (e = cudaMalloc(&s->d_defer, (p->max_window_chunks + 1) * 4)) != cudaSuccess ||
+        (e = cudaMalloc(&s->d_defer, 2 * (p->max_window_chunks + 1) * 4)) != cudaSuccess ||
         (e = cudaMallocHost(&s->h_scratch, sizeof(ApplyScratch))) != cudaSuccess) {
         dcr_recv_state_destroy(s);
         return cuda_error(e, "allocating receiver state");
@@ -558,6 +558,7 @@ extern "C" int dcr_encode(const dcr_plan* p, uint32_t mode, uint32_t window,
     if (p->profiling) {
         p->prof_encode_due = true;   // durations read from the events when asked for
         p->prof.encode_valid = 1;
+        p->prof.encode_kernels = kEncodeKernels;
     }
     return encode_result(p, p->h_enc, payload ? cap : 0, payload_size, changed_per_tensor, false);
 }
@@ -637,7 +638,7 @@ static int apply_common(const dcr_plan* p, dcr_recv_state* st, const void* paylo
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return cuda_error(e, "dcr_apply status read");
     p->prof_deferred = false;
-    if (st->h_scratch->hdr_ok && (st->h_scratch->n_defer || st->h_scratch->n_big)) {
+    if (st->h_scratch->hdr_ok && (st->h_scratch->n_defer || st->h_scratch->n_big || st->h_scratch->n_lane)) {
         p->prof_deferred = true;
         rc = apply_launch_part(p, st, payload, size, target, abort_at, split, retry_only, kApplyDeferred, s);
         if (rc) return rc;
@@ -648,6 +649,7 @@ static int apply_common(const dcr_plan* p, dcr_recv_state* st, const void* paylo
     if (p->profiling) {
         p->prof_apply_due = true;
         p->prof.apply_valid = 1;
+        p->prof.apply_kernels = p->prof_deferred ? kApplyKernelsDeferred : kApplyKernels;
     }
     return apply_result(st, *st->h_scratch, result);
 }
@@ -924,6 +926,7 @@ extern "C" int dcr_encode_retry(const dcr_plan* p, const void* xor_payload, size
     if (p->profiling) {
         p->prof_encode_due = true;
         p->prof.encode_valid = 1;
+        p->prof.encode_kernels = kRetryKernels;
     }
     const EncScratch* hs = static_cast<const EncScratch*>(p->h_enc);
     *payload_size = hs->total;

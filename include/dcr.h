@@ -102,11 +102,16 @@ enum { DCR_MODE_HYBRID = 0, DCR_MODE_OVERWRITE_ONLY = 1 };
  * faster when a window has fewer chunks than the GPU has warp slots; AUTO
  * picks WIDE or CTA by window size. */
 enum { DCR_ENCODER_AUTO = 0, DCR_ENCODER_WIDE = 1, DCR_ENCODER_DEEP = 2, DCR_ENCODER_CTA = 3 };
-/* Apply kernel variant (dcr_plan_opts.apply); both apply the same bytes.
+/* Apply kernel variant (dcr_plan_opts.apply); all apply the same bytes.
  * WARP: one warp per frame; CTA: one 256-thread CTA per frame (parallel
  * sequence walk by pointer doubling), faster when windows have fewer frames
- * than the GPU has warp slots; AUTO picks by the plan's largest window. */
-enum { DCR_APPLY_AUTO = 0, DCR_APPLY_WARP = 1, DCR_APPLY_CTA = 2 };
+ * than the GPU has warp slots; LANE: one warp per frame for raw and
+ * overwrite frames, one thread per ZSRC LZ4 or Snappy frame (a serial walk
+ * that writes only the non-zero literal bytes: a tenth of the instructions,
+ * so the fastest once a stream has tens of thousands of frames).  AUTO picks
+ * CTA for plans with small windows, else WARP, and LANE for the streams with
+ * about four frames or more per warp slot of the bitmap walk. */
+enum { DCR_APPLY_AUTO = 0, DCR_APPLY_WARP = 1, DCR_APPLY_CTA = 2, DCR_APPLY_LANE = 3 };
 /* Block codec of XOR masks (dcr_plan_opts.codec).  LZ4 (frame kind 1) is the
  * default; Snappy (frame kind 5) is the other byte-oriented LZ77 codec the
  * method's pages compare it with (blog, "A strong baseline with the
@@ -153,7 +158,7 @@ typedef struct {
     uint32_t encoder;        /* DCR_ENCODER_AUTO (0), _WIDE, _DEEP or _CTA */
     uint32_t codec;          /* DCR_CODEC_LZ4 (0) or DCR_CODEC_SNAPPY */
     uint32_t flags;          /* 0 or DCR_PLAN_HOST_ONLY */
-    uint32_t apply;          /* DCR_APPLY_AUTO (0), _WARP or _CTA */
+    uint32_t apply;          /* DCR_APPLY_AUTO (0), _WARP, _CTA or _LANE */
     uint32_t overflow_kib;    /* device heap for XOR blocks that outgrow their
                                 6 KiB frame slot (masks of a few percent
                                 change and more): 0 = one eighth of
@@ -443,6 +448,7 @@ typedef struct {
     float defer_ms;     /* general LZ4 frames */
     float pending_ms;   /* commit check */
     uint32_t encode_valid, apply_valid;
+    uint32_t encode_kernels, apply_kernels;   /* kernels those calls launched */
 } dcr_profile;
 int dcr_plan_set_profiling(dcr_plan* plan, int on);
 int dcr_plan_last_profile(const dcr_plan* plan, dcr_profile* out);

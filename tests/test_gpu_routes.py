@@ -113,9 +113,9 @@ def test_every_route_matches_oracle(mode, encoder, overflow):
     orc = oracle.Oracle(wl)
     plan = dcr.Plan(descs_of(wl), window_bytes=wl.window_bytes,
                     encoder={"wide": dcr.ENCODER_WIDE, "deep": dcr.ENCODER_DEEP, "cta": dcr.ENCODER_CTA}[encoder],
-                    # both apply kernels on every route: warp per frame after the wide and CTA
-                    # encoders, CTA per frame after the deep one
-                    apply=dcr.APPLY_CTA if encoder == "deep" else dcr.APPLY_WARP,
+                    # every apply kernel on every route: warp per frame after the wide encoder,
+                    # CTA per frame after the deep one, thread per ZSRC frame after the CTA one
+                    apply={"wide": dcr.APPLY_WARP, "deep": dcr.APPLY_CTA, "cta": dcr.APPLY_LANE}[encoder],
                     overflow_kib={"heap": 0, "none": dcr.NO_OVERFLOW, "16kib": 16}[overflow])
     assert plan.info.plan_hash == orc.plan_hash
     d_old, d_new = to_device(olds), to_device(news)

@@ -45,12 +45,16 @@ class Case:
         return t.cpu().numpy()[:self.exp.size]
 
 
-# every small twin with each apply kernel: one warp per frame, one CTA per frame
-@pytest.fixture(scope="module", params=[(n, a) for n in (1, 2, 3, 4, 5) for a in ("warp", "cta")],
+# every small twin with each apply kernel: one warp per frame, one CTA per
+# frame, one thread per ZSRC frame
+APPLY = {"warp": dcr.APPLY_WARP, "cta": dcr.APPLY_CTA, "lane": dcr.APPLY_LANE}
+
+
+@pytest.fixture(scope="module", params=[(n, a) for n in (1, 2, 3, 4, 5) for a in APPLY],
                 ids=lambda p: "%d-%s" % p)
 def case(request):
     n, a = request.param
-    return Case(configs.mini(n), apply=dcr.APPLY_WARP if a == "warp" else dcr.APPLY_CTA)
+    return Case(configs.mini(n), apply=APPLY[a])
 
 
 def test_generator_twins_agree():
@@ -139,9 +143,10 @@ def test_overwrite_retry_stream_reaches_new(case):
     assert np.array_equal(case.host(t), case.exp)
 
 
+@pytest.mark.parametrize("apply", ["auto", "lane"])
 @pytest.mark.parametrize("n", [1, 3])
-def test_abort_state_matches_oracle_then_retry(n):
-    c = Case(configs.mini(n))
+def test_abort_state_matches_oracle_then_retry(n, apply):
+    c = Case(configs.mini(n), apply=dcr.APPLY_AUTO if apply == "auto" else APPLY[apply])
     pl, size, _ = c.encode()
     rp, rsize, _ = c.encode(mode=dcr.MODE_OVERWRITE_ONLY)
     nf = parse(pl[:size].cpu().numpy())[0]["n_frames"]
@@ -265,11 +270,12 @@ def _last_match_offset(body):
             ip += 1
 
 
-def test_frame_failing_late_leaves_its_chunk_untouched():
+@pytest.mark.parametrize("apply", ["auto", "lane"])
+def test_frame_failing_late_leaves_its_chunk_untouched(apply):
     # a ZSRC frame whose last match offset is zeroed fails only after most of
     # its literals were XOR-ed in; the chunk must come back exactly as it was,
     # otherwise the overwrite-only retry (changed units only) cannot repair it
-    c = Case(configs.mini(1))
+    c = Case(configs.mini(1), apply=dcr.APPLY_AUTO if apply == "auto" else APPLY[apply])
     pl, size, _ = c.encode()
     g = pl[:size].cpu().numpy()
     _, frames, _ = parse(g)
@@ -293,12 +299,14 @@ def test_frame_failing_late_leaves_its_chunk_untouched():
     assert rc == dcr.OK and st.version == 1 and np.array_equal(c.host(t), c.exp)
 
 
+@pytest.mark.parametrize("apply", ["auto", "lane"])
 @pytest.mark.parametrize("frac", [None, 0.05])
-def test_zsrc_flag_is_verified(frac):
+def test_zsrc_flag_is_verified(frac, apply):
     # a greedy (oracle) block whose matches copy non-zero bytes, relabelled
     # as ZSRC, must be rejected rather than applied as zeros; at 5 % change the
     # bodies are larger than the warp path's cache (the large-frame kernel)
-    c = Case(configs.mini(1) if frac is None else configs.mini(4), frac=frac)
+    c = Case(configs.mini(1) if frac is None else configs.mini(4), frac=frac,
+             apply=dcr.APPLY_AUTO if apply == "auto" else APPLY[apply])
     o, _ = c.orc.encode(c.olds, c.news)
     _, frames, _ = parse(o)
     lied = o.copy()
@@ -336,11 +344,13 @@ def test_no_change_and_capacity():
     assert rc == dcr.OK and size3 == need
 
 
+@pytest.mark.parametrize("apply", ["auto", "lane"])
 @pytest.mark.parametrize("frac", [0.0, 0.00085, 0.05, 0.3, "random"])
-def test_change_rates_parity(frac):
+def test_change_rates_parity(frac, apply):
     wl = configs.mini(4)
     c = Case(wl, rule=synth.RULE_RANDOM if frac == "random" else None,
-             frac=None if frac == "random" else frac)
+             frac=None if frac == "random" else frac,
+             apply=dcr.APPLY_AUTO if apply == "auto" else APPLY[apply])
     pl, size, counts = c.encode()
     g = pl[:size].cpu().numpy()
     o, oc = c.orc.encode(c.olds, c.news)

@@ -26,7 +26,9 @@ from test_gpu_routes import crafted  # noqa: E402
 
 def _check(wl, olds, news, encoder=dcr.ENCODER_AUTO, size_bar=1.15):
     orc = oracle.Oracle(wl)
-    plan = dcr.Plan(descs_of(wl), window_bytes=wl.window_bytes, encoder=encoder, codec=dcr.CODEC_SNAPPY)
+    # the thread-per-frame apply after the CTA encoder, the default after the others
+    plan = dcr.Plan(descs_of(wl), window_bytes=wl.window_bytes, encoder=encoder, codec=dcr.CODEC_SNAPPY,
+                    apply=dcr.APPLY_LANE if encoder == dcr.ENCODER_CTA else dcr.APPLY_AUTO)
     d_old, d_new = to_device(olds), to_device(news)
     exp = orc.receiver_dense(news)
     t = torch.zeros(max(plan.info.recv_bytes, wl.recv_bytes, 16), dtype=torch.uint8, device="cuda")

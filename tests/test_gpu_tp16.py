@@ -24,7 +24,8 @@ def test_tp16_matches_oracle(mode, encoder):
     assert wl.tp == dcr.MAX_TP
     orc = oracle.Oracle(wl)
     olds, news = wl.host_arenas()
-    plan = dcr.Plan(descs_of(wl), window_bytes=wl.window_bytes, encoder=encoder)
+    plan = dcr.Plan(descs_of(wl), window_bytes=wl.window_bytes, encoder=encoder,
+                    apply=dcr.APPLY_LANE if encoder == dcr.ENCODER_CTA else dcr.APPLY_AUTO)
     assert plan.info.plan_hash == orc.plan_hash and plan.info.tp == 16
     d_old, d_new = to_device(olds), to_device(news)
     dm = dcr.MODE_HYBRID if mode == "hybrid" else dcr.MODE_OVERWRITE_ONLY

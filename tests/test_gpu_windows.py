@@ -22,7 +22,8 @@ def test_oversized_tensor_windows(encoder):
     wl = configs.oversized_window()
     orc = oracle.Oracle(wl)
     olds, news = wl.host_arenas()
-    plan = dcr.Plan(descs_of(wl), window_bytes=wl.window_bytes, encoder=encoder)
+    plan = dcr.Plan(descs_of(wl), window_bytes=wl.window_bytes, encoder=encoder,
+                    apply=dcr.APPLY_LANE if encoder == dcr.ENCODER_CTA else dcr.APPLY_AUTO)
     assert plan.info.plan_hash == orc.plan_hash
     assert plan.n_windows == orc.n_windows == 4
     for w in range(plan.n_windows):

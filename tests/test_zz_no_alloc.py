@@ -21,12 +21,12 @@ def _target(plan, wl, shards):
     return t
 
 
-@pytest.mark.parametrize("n,codec", [(1, 0), (2, 0), (3, 0), (3, 1)])
-def test_noalloc_matches_apply_two_calls_in_a_row(n, codec):
+@pytest.mark.parametrize("n,codec,apply", [(1, 0, 0), (2, 0, 0), (3, 0, 0), (3, 1, 0), (2, 0, 3), (3, 1, 3)])
+def test_noalloc_matches_apply_two_calls_in_a_row(n, codec, apply):
     wl = configs.mini(n)
     orc = oracle.Oracle(wl)
     olds, news = wl.host_arenas()
-    plan = dcr.Plan(descs_of(wl), window_bytes=wl.window_bytes, codec=codec)
+    plan = dcr.Plan(descs_of(wl), window_bytes=wl.window_bytes, codec=codec, apply=apply)
     d_old, d_new = to_device(olds), to_device(news)
     ref_t, got_t = _target(plan, wl, d_old), _target(plan, wl, d_old)
     ref_st, got_st = dcr.RecvState(plan, 0), dcr.RecvState(plan, 0)
