@@ -12,8 +12,14 @@
 // model from a host-prepared plan) and "Working with low-precision RL" (the
 // mask is remapped like the physical layout).
 //
-// Kernels:
-//   apply_kernel  one warp per frame, 32 warps per SM.  XOR_RAW, OVERWRITE
+// Kernels (first phase: route_kernel, apply_kernel, lane_kernel, or
+// apply_cta_kernel alone for plans of small windows; then, only
+// when frames were deferred to them, defer_kernel and big_kernel; then the
+// commit check):
+//   route_kernel  one warp per 32 frames, a lane per frame: checks the index
+//                 entry and frame header, claims the chunk (dedup) and lists
+//                 the frame for the kernel that applies it.
+//   apply_kernel  one warp per listed frame, 32 warps per SM.  XOR_RAW, OVERWRITE
 //                 and OVERWRITE_DENSE frames are applied lane-parallel.  LZ4
 //                 frames flagged ZSRC (every match copies zero bytes, as the
 //                 library's encoder produces) have only literal bytes that can
@@ -23,6 +29,10 @@
 //                 arena and check every match against the sorted list of
 //                 non-zero output bytes so far.  A frame that fails part-way is
 //                 undone (XOR is self-inverse) before it is reported.
+//   lane_kernel   one thread per ZSRC frame (streams of many frames): a
+//                 serial walk that XORs the non-zero literal bytes and proves
+//                 each match copies zeros from the zero stretches the
+//                 library's encoder copies from; other frames to big_kernel.
 //   big_kernel    one warp per ZSRC frame too large for apply_kernel's
 //                 body cache or non-zero list (denser masks), and per ZSRC
 //                 Snappy frame: the same walk (Snappy elements in place of
@@ -223,7 +233,7 @@ __device__ __forceinline__ void put_vec(const ApplyArgs& A, const ChunkDesc& cd,
 }
 
 // claim a chunk for target version V: true if this frame may apply its mask
-__device__ bool claim(unsigned long long* st, uint64_t V, bool* timeout)
+__device__ __forceinline__ bool claim(unsigned long long* st, uint64_t V, bool* timeout)
 {
     unsigned long long cur = *reinterpret_cast<volatile unsigned long long*>(st);
     const unsigned long long want = (V << 2) | kClaimed;
@@ -702,7 +712,115 @@ __device__ int zsrc_apply(const ApplyArgs& A, const ChunkDesc& cd, const Seg* ds
 }
 
 // ================================================================ kernels ==
-__global__ void __launch_bounds__(kAThreads) apply_kernel(ApplyArgs A)
+// Where apply_kernel sends a frame.
+enum FrameRoute : int { kRNone = 0, kRSkip, kRWarp, kRDefer, kRLane, kRBig };
+
+// One lane's part of apply_kernel: check frame f's index entry and header
+// (errors reported), skip it past an injected fault, claim its chunk (XOR
+// kinds; kRSkip: already claimed or done for this version), and route it:
+// general LZ4 and Snappy frames to the full decode; ZSRC frames to
+// lane_kernel when the stream has frames enough to keep its threads busy,
+// else Snappy ones and LZ4 ones larger than the body cache to big_kernel;
+// the rest to the warp.
+__device__ __forceinline__ int frame_route(const ApplyArgs& A, const Hdr& H, uint32_t f)
+{
+    const uint64_t fo = ld64(A.payload + H.idx_off + 8ull * f);
+    if (fo < kStreamHdr || fo % 16 || fo + kFrameHdr > H.idx_off) {
+        report(A.sc, DCR_ERR_CORRUPT);
+        return kRNone;
+    }
+    const uint4 h0 = ld_nc16(A.payload + fo), h1 = ld_nc16(A.payload + fo + 16);
+    const uint32_t kind = h0.y & 0xFFu, fbits = (h0.y >> 8) & 0xFFu, fflags = h0.y >> 16;
+    const uint32_t c = h0.z, raw = h0.w, bl = h1.x;
+    if (h0.x != kFrameMagic || kind < kXorLz4 || kind > kXorSnappy || c < H.chunk_begin ||
+        c >= H.chunk_begin + H.chunk_count || bl > H.idx_off - fo - kFrameHdr) {
+        report(A.sc, DCR_ERR_CORRUPT);
+        return kRNone;
+    }
+    const ChunkDesc cd = A.chunks[c];
+    if (raw != cd.raw_len || fbits != cd.bits) {
+        report(A.sc, DCR_ERR_CORRUPT);
+        return kRNone;
+    }
+    const bool is_xor = kind == kXorLz4 || kind == kXorRaw || kind == kXorSnappy;
+    if (A.retry_only && is_xor) {
+        report(A.sc, DCR_ERR_INVALID);
+        return kRNone;
+    }
+    if (uint64_t(f) > A.abort_at) return kRNone;   // injected fault: never reached
+    if (!is_xor) return kRWarp;
+    bool to = false;
+    if (!claim(&A.state[c], H.target_v, &to)) {
+        if (to) report(A.sc, DCR_ERR_TIMEOUT);
+        return to ? kRNone : kRSkip;
+    }
+    const bool zs = (fflags & kFrameZsrc) != 0;
+    if (kind != kXorRaw && !zs) return kRDefer;
+    if (kind != kXorRaw && H.n_frames >= A.lane_min) return kRLane;
+    if (kind == kXorSnappy || (kind == kXorLz4 && bl > uint32_t(kBodyCache))) return kRBig;
+    return kRWarp;
+}
+
+// The warp's frames routed to list r, appended with one atomic per warp.
+__device__ __forceinline__ void push_listed(const ApplyArgs& A, int route, int r, uint32_t f, int lane,
+                                            uint32_t lt)
+{
+    const uint32_t m = __ballot_sync(kFull, route == r);
+    if (!m) return;
+    uint32_t* cnt = r == kRDefer ? &A.sc->n_defer : r == kRLane ? &A.sc->n_lane
+                  : r == kRBig ? &A.sc->n_big : &A.sc->n_warp;
+    uint32_t base = 0;
+    if (lane == 0) base = atomicAdd(cnt, uint32_t(__popc(m)));
+    base = __shfl_sync(kFull, base, 0);
+    if (route != r) return;
+    const uint32_t k = base + __popc(m & lt);
+    if (r == kRDefer) A.defer[k] = f;
+    else if (r == kRLane) A.lane[k] = f;
+    else if (r == kRBig) A.defer[A.defer_len - 1 - k] = f;
+    else A.lane[A.defer_len - 1 - k] = f;
+}
+
+// The first apply kernel of the warp route: one warp per 32 frames, each
+// lane checks, claims and routes one frame (frame_route) into the lists of
+// the kernels after it: apply_kernel (warp list, from the end of the lane
+// list's array), lane_kernel, defer_kernel, big_kernel.
+constexpr int kRtThreads = 256;
+
+__global__ void __launch_bounds__(kRtThreads) route_kernel(ApplyArgs A)
+{
+    __shared__ Hdr hdr;
+    __shared__ int ok;
+    if (threadIdx.x == 0) {
+        const int rc = check_header(A, &hdr);
+        ok = rc == 0;
+        if (rc) report(A.sc, rc);
+        else if (blockIdx.x == 0) {
+            A.sc->hdr_ok = 1;
+            A.sc->target_version = hdr.target_v;
+            A.sc->window = hdr.window;
+            A.sc->n_frames = hdr.n_frames;
+        }
+    }
+    __syncthreads();
+    if (!ok) return;
+    const Hdr H = hdr;
+    const int lane = threadIdx.x & 31;
+    const uint32_t lt = (1u << lane) - 1u;
+    const uint64_t nw = uint64_t(gridDim.x) * (kRtThreads / 32);
+    for (uint64_t f0 = 32 * (uint64_t(blockIdx.x) * (kRtThreads / 32) + (threadIdx.x >> 5)); f0 < H.n_frames;
+         f0 += 32 * nw) {
+        const uint64_t f = f0 + lane;
+        const int route = f < H.n_frames ? frame_route(A, H, uint32_t(f)) : kRNone;
+        const uint32_t sk = __ballot_sync(kFull, route == kRSkip);
+        if (lane == 0 && sk) atomicAdd(&A.sc->skipped, (unsigned long long)__popc(sk));
+        push_listed(A, route, kRDefer, uint32_t(f), lane, lt);
+        push_listed(A, route, kRLane, uint32_t(f), lane, lt);
+        push_listed(A, route, kRBig, uint32_t(f), lane, lt);
+        push_listed(A, route, kRWarp, uint32_t(f), lane, lt);
+    }
+}
+
+__global__ void __launch_bounds__(kAThreads, 2) apply_kernel(ApplyArgs A)
 {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     ASmem& S = *reinterpret_cast<ASmem*>(smem_raw);
@@ -723,68 +841,25 @@ __global__ void __launch_bounds__(kAThreads) apply_kernel(ApplyArgs A)
     const Hdr H = S.hdr;
     const uint64_t V = H.target_v;
     AWarp& W = S.w[wid];
+    const uint32_t nw = A.sc->n_warp;   // final: written by route_kernel
 
     for (;;) {
-        uint32_t f = 0;
-        if (lane == 0) f = atomicAdd(&A.sc->frame_ticket, 1u);
-        f = __shfl_sync(0xffffffffu, f, 0);
-        if (f >= H.n_frames) break;
+        uint32_t j = 0;
+        if (lane == 0) j = atomicAdd(&A.sc->frame_ticket, 1u);
+        j = __shfl_sync(kFull, j, 0);
+        if (j >= nw) break;
+        const uint32_t f = A.lane[A.defer_len - 1 - j];   // the warp list: from the end of lane_kernel's
         const uint64_t fo = ld64(A.payload + H.idx_off + 8ull * f);
-        if (fo < kStreamHdr || fo % 16 || fo + kFrameHdr > H.idx_off) {
-            if (lane == 0) report(A.sc, DCR_ERR_CORRUPT);
-            continue;
-        }
         const uint4 h0 = ld_nc16(A.payload + fo), h1 = ld_nc16(A.payload + fo + 16);
-        const uint32_t kind = h0.y & 0xFFu, fbits = (h0.y >> 8) & 0xFFu, fflags = h0.y >> 16;
+        const uint32_t kind = h0.y & 0xFFu;
         const uint32_t c = h0.z, raw = h0.w, bl = h1.x;
-        if (h0.x != kFrameMagic || kind < kXorLz4 || kind > kXorSnappy || c < H.chunk_begin ||
-            c >= H.chunk_begin + H.chunk_count || bl > H.idx_off - fo - kFrameHdr) {
-            if (lane == 0) report(A.sc, DCR_ERR_CORRUPT);
-            continue;
-        }
         const ChunkDesc cd = A.chunks[c];
-        if (raw != cd.raw_len || fbits != cd.bits) {
-            if (lane == 0) report(A.sc, DCR_ERR_CORRUPT);
-            continue;
-        }
         const bool is_xor = kind == kXorLz4 || kind == kXorRaw || kind == kXorSnappy;
-        if (A.retry_only && is_xor) {
-            if (lane == 0) report(A.sc, DCR_ERR_INVALID);
-            continue;
-        }
-        if (uint64_t(f) > A.abort_at) continue;  // injected fault: never reached
         const bool cut = uint64_t(f) == A.abort_at;
         const uint32_t ub = cd.bits == 16 ? 2u : 1u;
         uint32_t lim = cut ? (A.split < raw ? A.split : raw) : raw;
         lim -= lim % ub;
         unsigned long long* st = &A.state[c];
-        if (is_xor) {
-            int got = 0;
-            if (lane == 0) {
-                bool to = false;
-                got = claim(st, V, &to);
-                if (to) report(A.sc, DCR_ERR_TIMEOUT);
-                if (!got && !to) atomicAdd(&A.sc->skipped, 1ull);
-            }
-            if (!__shfl_sync(0xffffffffu, got, 0)) continue;
-            // general LZ4 and Snappy frames go to the full decode.  ZSRC
-            // frames: to lane_kernel when the stream has frames enough to
-            // keep its threads busy; else Snappy ones and LZ4 ones larger
-            // than the body cache to big_kernel, the rest stay here
-            const bool zs = (fflags & kFrameZsrc) != 0;
-            if (kind != kXorRaw && !zs) {
-                if (lane == 0) A.defer[atomicAdd(&A.sc->n_defer, 1u)] = f;
-                continue;
-            }
-            if (kind != kXorRaw && H.n_frames >= A.lane_min) {
-                if (lane == 0) A.lane[atomicAdd(&A.sc->n_lane, 1u)] = f;
-                continue;
-            }
-            if (kind == kXorSnappy || (kind == kXorLz4 && bl > uint32_t(kBodyCache))) {
-                if (lane == 0) A.defer[A.defer_len - 1 - atomicAdd(&A.sc->n_big, 1u)] = f;
-                continue;
-            }
-        }
         const Seg* ds = A.dst + cd.dst_begin;
         const uint8_t* body = A.payload + fo + kFrameHdr;
         bool good = true;
@@ -1777,10 +1852,11 @@ int apply_kernel_config(KernelConfig* kc)
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&kc->apply_cta_blocks_per_sm, apply_cta_kernel, kCThreads,
                                                           sizeof(CSmem));
     if (e == cudaSuccess) {
-        // load the last kernel of the apply too (the others were loaded by
-        // the queries above), so that no apply call loads code lazily
+        // load the kernels of the apply that no query above touched, so that
+        // no apply call loads code lazily
         cudaFuncAttributes fa;
         e = cudaFuncGetAttributes(&fa, pending_kernel);
+        if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, route_kernel);
     }
     if (e != cudaSuccess) return cuda_error(e, "apply kernel configuration");
     if (kc->apply_blocks_per_sm < 1) kc->apply_blocks_per_sm = 1;
@@ -1793,18 +1869,23 @@ int apply_kernel_config(KernelConfig* kc)
 
 namespace {
 
-// The first apply kernel: one CTA per frame for plans whose windows have
-// fewer chunks than the GPU has warp slots (or when the plan asks for it),
-// else one warp per frame.
-void launch_first(const dcr_plan* P, const ApplyArgs& A, cudaStream_t s)
+// The first phase of an apply: one CTA per frame for plans whose windows
+// have fewer chunks than the GPU has warp slots (or when the plan asks for
+// it), else route_kernel and one warp per frame; then lane_kernel for the
+// ZSRC frames routed to it.  Returns the kernels launched.
+int launch_first(const dcr_plan* P, const ApplyArgs& A, cudaStream_t s)
 {
     const int sms = P->kc.num_sms;
     const bool cta = P->apply == DCR_APPLY_CTA ||
                      (P->apply == DCR_APPLY_AUTO && P->max_window_chunks <= uint64_t(P->small_window_chunks));
-    if (cta)
+    if (cta) {   // lists nothing for lane_kernel
         apply_cta_kernel<<<sms * P->kc.apply_cta_blocks_per_sm, kCThreads, sizeof(CSmem), s>>>(A);
-    else
-        apply_kernel<<<sms * P->kc.apply_blocks_per_sm, kAThreads, sizeof(ASmem), s>>>(A);
+        return 1;
+    }
+    route_kernel<<<sms * 4, kRtThreads, 0, s>>>(A);
+    apply_kernel<<<sms * P->kc.apply_blocks_per_sm, kAThreads, sizeof(ASmem), s>>>(A);
+    lane_kernel<<<sms * P->kc.lane_blocks_per_sm, kLThreads, 0, s>>>(A);
+    return 3;
 }
 
 }  // namespace
@@ -1848,15 +1929,13 @@ ApplyArgs make_args(const dcr_plan* P, dcr_recv_state* st, const void* payload, 
     return A;
 }
 
-// the kernels of the frames the first kernel deferred: general LZ4 and
-// Snappy frames; ZSRC frames for lane_kernel; then the ZSRC frames that
-// lane_kernel could not prove, and those the CTA kernel passes on, for
-// big_kernel
+// the kernels of the frames the first phase deferred: general LZ4 and
+// Snappy frames; the ZSRC frames that lane_kernel could not prove, and those
+// the first kernels pass on, for big_kernel
 void launch_deferred(const dcr_plan* P, const ApplyArgs& A, cudaStream_t s)
 {
     const int sms = P->kc.num_sms;
     defer_kernel<<<sms * P->kc.defer_blocks_per_sm, kDThreads, kChunk, s>>>(A);
-    lane_kernel<<<sms * P->kc.lane_blocks_per_sm, kLThreads, 0, s>>>(A);
     big_kernel<<<sms * P->kc.big_blocks_per_sm, kBThreads, sizeof(BWarp) * kBWarps, s>>>(A);
 }
 
@@ -1872,7 +1951,7 @@ int apply_launch_part(const dcr_plan* P, dcr_recv_state* st, const void* payload
         e = cudaMemsetAsync(st->d_scratch, 0, sizeof(ApplyScratch), s);
         if (e != cudaSuccess) return cuda_error(e, "apply scratch reset");
         if (P->profiling) cudaEventRecord(P->ev[3], s);
-        launch_first(P, A, s);
+        P->apply_kernels = uint32_t(launch_first(P, A, s)) + 1;   // and the commit check
         if (P->profiling) cudaEventRecord(P->ev[4], s);
     }
     if (part != kApplyFirst) {
@@ -1882,6 +1961,7 @@ int apply_launch_part(const dcr_plan* P, dcr_recv_state* st, const void* payload
             if (P->profiling) cudaEventRecord(P->ev[7], s);
         }
         launch_deferred(P, A, s);
+        P->apply_kernels += part == kApplyDeferred ? 3 : 2;
     }
     if (P->profiling) cudaEventRecord(P->ev[5], s);
     pending_kernel<<<sms, 256, 0, s>>>(A);
@@ -2025,9 +2105,7 @@ int apply_launch_noalloc(const dcr_plan* P, dcr_recv_state* st, const void* payl
     if (e != cudaSuccess) return cuda_error(e, "static apply scratch reset");
     const int sms = P->kc.num_sms;
     launch_first(P, A, s);
-    defer_kernel<<<sms * P->kc.defer_blocks_per_sm, kDThreads, kChunk, s>>>(A);
-    lane_kernel<<<sms * P->kc.lane_blocks_per_sm, kLThreads, 0, s>>>(A);
-    big_kernel<<<sms * P->kc.big_blocks_per_sm, kBThreads, sizeof(BWarp) * kBWarps, s>>>(A);
+    launch_deferred(P, A, s);
     pending_kernel<<<sms, 256, 0, s>>>(A);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_error(e, "apply launch");

@@ -119,6 +119,7 @@ struct ApplyScratch {
     uint64_t n_frames;
     uint32_t big_ticket;
     uint32_t n_lane;        // ZSRC frames listed for lane_kernel
+    uint32_t n_warp;        // frames route_kernel lists for apply_kernel
 };
 
 // Chunk state of a receiver: (target_version << 2) | state.
@@ -173,10 +174,9 @@ int apply_launch(const struct ::dcr_plan* plan, struct ::dcr_recv_state* st, con
 // kApplyAll = all of them (what apply_launch launches)
 enum { kApplyAll = 0, kApplyFirst = 1, kApplyDeferred = 2 };
 // kernels one call launches: dcr_encode (encode, scan, copy, restream,
-// spill), dcr_encode_retry (retry, scan, copy, retry spill), dcr_apply
-// (first kernel and commit check; with deferred frames also the defer, lane
-// and big kernels and the commit check again)
-constexpr uint32_t kEncodeKernels = 5, kRetryKernels = 4, kApplyKernels = 2, kApplyKernelsDeferred = 6;
+// spill), dcr_encode_retry (retry, scan, copy, retry spill); dcr_apply counts
+// its own (dcr_plan::apply_kernels)
+constexpr uint32_t kEncodeKernels = 5, kRetryKernels = 4;
 int apply_launch_part(const struct ::dcr_plan* plan, struct ::dcr_recv_state* st, const void* payload,
                       size_t size, void* target, uint64_t abort_at, uint32_t split, int retry_only, int part,
                       cudaStream_t s);
@@ -249,6 +249,7 @@ struct dcr_plan {
     mutable dcr_profile prof = {};
     mutable bool prof_encode_due = false, prof_apply_due = false;   // events recorded, durations not read
     mutable bool prof_deferred = false;   // the deferred-frame kernels ran after a status read (from ev[7])
+    mutable uint32_t apply_kernels = 0;   // kernels the latest apply launched
     // ownership-sharded encode: the part sized by the last dcr_encode_part
     struct {
         bool valid = false;

@@ -638,7 +638,7 @@ static int apply_common(const dcr_plan* p, dcr_recv_state* st, const void* paylo
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return cuda_error(e, "dcr_apply status read");
     p->prof_deferred = false;
-    if (st->h_scratch->hdr_ok && (st->h_scratch->n_defer || st->h_scratch->n_big || st->h_scratch->n_lane)) {
+    if (st->h_scratch->hdr_ok && (st->h_scratch->n_defer || st->h_scratch->n_big)) {
         p->prof_deferred = true;
         rc = apply_launch_part(p, st, payload, size, target, abort_at, split, retry_only, kApplyDeferred, s);
         if (rc) return rc;
@@ -649,7 +649,7 @@ static int apply_common(const dcr_plan* p, dcr_recv_state* st, const void* paylo
     if (p->profiling) {
         p->prof_apply_due = true;
         p->prof.apply_valid = 1;
-        p->prof.apply_kernels = p->prof_deferred ? kApplyKernelsDeferred : kApplyKernels;
+        p->prof.apply_kernels = p->apply_kernels;
     }
     return apply_result(st, *st->h_scratch, result);
 }
