@@ -1466,30 +1466,67 @@ __device__ __forceinline__ uint4 ld_nc16_run(const uint8_t* p)
     return v;
 }
 
-// The body, read in order 16 bytes at a time with the next 16 in flight.
+// The body, read in order: the next bytes sit in a 64-bit register (the
+// byte at the read position lowest, at least 5 of them until the body's
+// last block), refilled a 32-bit word at a time from two 16-byte blocks,
+// the second one in flight.  Words past the body's last block are never
+// loaded (what they hold is never taken: the walks check every read against
+// the body length first).
 struct LaneRd {
     const uint8_t* b;
     uint32_t nblk;   // 16-byte blocks of the body (the frame is padded to 16)
     uint32_t blk;    // block in w0
+    uint32_t wp;     // body offset of the next word to append
+    uint32_t qn;     // bytes held in q
     uint4 w0, w1;    // blocks blk, blk + 1
+    uint64_t q;
+    __device__ __forceinline__ void append()
+    {
+        const uint32_t k = wp >> 4;
+        if (k != blk) {   // k == blk + 1: words are appended in order
+            w0 = w1;
+            blk = k;
+            if (k + 1 < nblk) w1 = ld_nc16_run(b + 16ull * (k + 1));
+        }
+        const uint32_t s = (wp >> 2) & 3u;
+        const uint32_t w = s == 0 ? w0.x : s == 1 ? w0.y : s == 2 ? w0.z : w0.w;
+        q |= uint64_t(w) << (8 * qn);
+        qn += 4;
+        wp += 4;
+    }
+    __device__ __forceinline__ void fill()
+    {
+        if (qn <= 4) {
+            append();
+            if (qn <= 4) append();
+        }
+    }
     __device__ __forceinline__ void init(const uint8_t* body, uint32_t n)
     {
         b = body;
         nblk = (n + 15) >> 4;
         blk = 0;
+        wp = 0;
+        qn = 0;
+        q = 0;
         w0 = nblk > 0 ? ld_nc16_run(b) : make_uint4(0, 0, 0, 0);
         w1 = nblk > 1 ? ld_nc16_run(b + 16) : make_uint4(0, 0, 0, 0);
+        fill();
     }
-    __device__ __forceinline__ uint32_t at(uint32_t i)
+    // the next four bytes (the next byte lowest)
+    __device__ __forceinline__ uint32_t peek() const { return uint32_t(q); }
+    // move past k <= 4 bytes
+    __device__ __forceinline__ void take(uint32_t k)
     {
-        const uint32_t k = i >> 4;
-        if (k != blk) {
-            w0 = k == blk + 1 ? w1 : ld_nc16_run(b + 16ull * k);
-            blk = k;
-            if (k + 1 < nblk) w1 = ld_nc16_run(b + 16ull * (k + 1));
-        }
-        const uint32_t v = (i & 8) ? ((i & 4) ? w0.w : w0.z) : ((i & 4) ? w0.y : w0.x);
-        return __byte_perm(v, 0, 0x4440u | (i & 3u));
+        q >>= 8 * k;
+        qn -= k;
+        fill();
+    }
+    __device__ __forceinline__ uint32_t byte()
+    {
+        const uint32_t v = uint32_t(q) & 0xFFu;
+        take(1);
+        return v;
     }
 };
 
@@ -1542,10 +1579,9 @@ struct LaneXor {
 // [g0, g1); the literal bytes below `done` have been XORed.  Also the zero
 // stretch before each non-zero byte (its "gap"), counted in groups of 32
 // non-zero bytes: the longest gap of the current group (cur) and of all
-// earlier groups (best), as length << 32 | start.
+// earlier groups (best), as length << 16 | start (both below 2^16).
 struct LaneOut {
-    uint32_t op, z1, g0, g1, done, ev;
-    unsigned long long cur, best;
+    uint32_t op, z1, g0, g1, done, ev, cur, best;
 };
 
 // One literal run of ll bytes at body offset ip.  kUndo: XOR again the bytes
@@ -1556,16 +1592,26 @@ struct LaneOut {
 // before (Snappy), or from a zero it keeps as a literal (offset 1); each of
 // those sources is one of the stretches kept here.
 template <bool kUndo>
-__device__ __forceinline__ void lane_literals(LaneRd& R, LaneDst& D, LaneXor& X, LaneOut& O, uint32_t ip,
-                                              uint32_t ll, uint32_t lim, uint32_t upto)
+__device__ __forceinline__ void lane_literals(LaneRd& R, LaneDst& D, LaneXor& X, LaneOut& O, uint32_t ll,
+                                              uint32_t lim, uint32_t upto)
 {
-    for (uint32_t q = 0; q < ll; ++q) {
-        const uint32_t b = R.at(ip + q);
-        if (b) {
-            const uint32_t x = O.op + q;
-            if (kUndo && x >= upto) break;
+    // four bytes at a time; within them only the non-zero ones cost work
+    for (uint32_t q = 0; q < ll; q += 4) {
+        const uint32_t k = ll - q < 4 ? ll - q : 4u;
+        uint32_t v = R.peek();
+        if (k < 4) v &= (1u << (8 * k)) - 1;
+        R.take(k);
+        while (v) {
+            const uint32_t j = uint32_t(__ffs(v) - 1) >> 3;
+            const uint32_t b = (v >> (8 * j)) & 0xFFu;
+            v &= ~(0xFFu << (8 * j));
+            const uint32_t x = O.op + q + j;
+            if (kUndo && x >= upto) {   // the replay is done: the step returns next
+                O.op += ll;
+                return;
+            }
             if (!kUndo) {
-                const unsigned long long gap = ((unsigned long long)(x - O.z1) << 32) | O.z1;
+                const uint32_t gap = ((x - O.z1) << 16) | O.z1;
                 if (gap > O.cur) O.cur = gap;
                 if ((++O.ev & 31u) == 0) {
                     if (O.cur > O.best) O.best = O.cur;
@@ -1588,8 +1634,8 @@ __device__ __forceinline__ bool lane_match(const LaneOut& O, uint32_t off, uint3
 {
     if (off == 0 || off > O.op || ml > raw - O.op) return false;
     const uint32_t s0 = O.op - off, e0 = s0 + (ml < off ? ml : off);
-    const uint32_t bs = uint32_t(O.best), be = bs + uint32_t(O.best >> 32);
-    const uint32_t cs = uint32_t(O.cur), ce = cs + uint32_t(O.cur >> 32);
+    const uint32_t bs = O.best & 0xFFFFu, be = bs + (O.best >> 16);
+    const uint32_t cs = O.cur & 0xFFFFu, ce = cs + (O.cur >> 16);
     return s0 >= O.z1 || (s0 >= O.g0 && e0 <= O.g1) || (s0 >= bs && e0 <= be) || (s0 >= cs && e0 <= ce);
 }
 
@@ -1609,7 +1655,7 @@ struct LaneWalk {
         R.init(body, bl);
         D.init(ds, dcnt);
         X = LaneXor{target, ~0ull, 0u};
-        O = LaneOut{0, 0, 0, 0, 0, 0, 0ull, 0ull};
+        O = LaneOut{0, 0, 0, 0, 0, 0, 0, 0};
         ip = 0;
         n = bl;
         raw = raw_len;
@@ -1625,39 +1671,62 @@ enum LaneStep : int { kLGo = 0, kLValid = 1, kLStop = 2 };
 // One LZ4 sequence (the same block format as the other walks).  kLStop: the
 // block is malformed or a match is not proven to copy zeros, or (kUndo) the
 // replay has reached `upto`.
+// An LZ4 length's extra bytes (255 continues, anything else ends it), added
+// to *len, up to four at a time; false if they run past the body.
+__device__ __forceinline__ bool lane_len_bytes(LaneWalk& W, uint32_t* len)
+{
+    if (W.ip >= W.n) return false;
+    const uint32_t b0 = W.R.peek() & 0xFFu;
+    if (b0 != 255) {   // one byte: the common case
+        *len += b0;
+        ++W.ip;
+        W.R.take(1);
+        return true;
+    }
+    for (;;) {
+        if (W.ip >= W.n) return false;
+        const uint32_t v = W.R.peek();
+        const uint32_t ff = __vcmpeq4(v, 0xFFFFFFFFu);   // 0xFF for each byte of 255
+        const uint32_t avail = W.n - W.ip;
+        if (ff == 0xFFFFFFFFu) {
+            if (avail < 5) return false;   // the length needs a byte after these
+            *len += 4 * 255;
+            W.ip += 4;
+            W.R.take(4);
+            continue;
+        }
+        const uint32_t k = uint32_t(__ffs(~ff) - 1) >> 3;   // the first byte that is not 255
+        if (k >= avail) return false;
+        *len += 255 * k + ((v >> (8 * k)) & 0xFFu);
+        W.ip += k + 1;
+        W.R.take(k + 1);
+        return true;
+    }
+}
+
+// One LZ4 sequence (the same block format as the other walks).  kLStop: the
+// block is malformed or a match is not proven to copy zeros, or (kUndo) the
+// replay has reached `upto`.
 template <bool kUndo>
 __device__ __forceinline__ int lz4_step(LaneWalk& W)
 {
     if (kUndo && W.O.op >= W.upto) return kLStop;
     if (W.ip >= W.n) return kLStop;
-    const uint32_t tok = W.R.at(W.ip++);
+    const uint32_t tok = W.R.byte();
+    ++W.ip;
     uint32_t ll = tok >> 4;
-    if (ll == 15) {
-        uint32_t b;
-        do {
-            if (W.ip >= W.n) return kLStop;
-            b = W.R.at(W.ip++);
-            ll += b;
-        } while (b == 255);
-    }
+    if (ll == 15 && !lane_len_bytes(W, &ll)) return kLStop;
     if (ll > W.n - W.ip || ll > W.raw - W.O.op) return kLStop;
-    lane_literals<kUndo>(W.R, W.D, W.X, W.O, W.ip, ll, W.lim, W.upto);
+    lane_literals<kUndo>(W.R, W.D, W.X, W.O, ll, W.lim, W.upto);
     W.ip += ll;
     if (W.ip == W.n) return W.O.op == W.raw ? kLValid : kLStop;
     if (kUndo && W.O.op >= W.upto) return kLStop;
     if (W.n - W.ip < 2) return kLStop;
-    uint32_t off = W.R.at(W.ip);
-    off |= W.R.at(W.ip + 1) << 8;
+    const uint32_t off = W.R.peek() & 0xFFFFu;
+    W.R.take(2);
     W.ip += 2;
     uint32_t ml = tok & 15u;
-    if (ml == 15) {
-        uint32_t b;
-        do {
-            if (W.ip >= W.n) return kLStop;
-            b = W.R.at(W.ip++);
-            ml += b;
-        } while (b == 255);
-    }
+    if (ml == 15 && !lane_len_bytes(W, &ml)) return kLStop;
     ml += 4;
     if (!kUndo && !lane_match(W.O, off, ml, W.raw)) return kLStop;
     W.O.op += ml;
@@ -1669,7 +1738,8 @@ __device__ __forceinline__ bool snappy_pre(LaneWalk& W)
 {
     uint64_t v = 0;
     for (uint32_t shift = 0; shift <= 28 && W.ip < W.n; shift += 7) {
-        const uint32_t b = W.R.at(W.ip++);
+        const uint32_t b = W.R.byte();
+        ++W.ip;
         v |= uint64_t(b & 127u) << shift;
         if (!(b & 128u)) return v == W.raw;
     }
@@ -1682,20 +1752,21 @@ __device__ __forceinline__ int snappy_step(LaneWalk& W)
 {
     if (W.ip == W.n) return W.O.op == W.raw ? kLValid : kLStop;
     if (kUndo && W.O.op >= W.upto) return kLStop;
-    const uint32_t tag = W.R.at(W.ip++), t = tag & 3u;
+    const uint32_t tag = W.R.byte(), t = tag & 3u;
+    ++W.ip;
     if (t == 0) {
         uint32_t len = (tag >> 2) + 1;
         if ((tag >> 2) >= 60) {
             const uint32_t nb = (tag >> 2) - 59;
             if (nb > W.n - W.ip) return kLStop;
-            uint64_t L = 0;
-            for (uint32_t i = 0; i < nb; ++i) L |= uint64_t(W.R.at(W.ip + i)) << (8 * i);
+            const uint32_t L = W.R.peek() & (nb == 4 ? 0xFFFFFFFFu : (1u << (8 * nb)) - 1);
+            W.R.take(nb);
             W.ip += nb;
             if (L >= W.raw) return kLStop;
-            len = uint32_t(L) + 1;
+            len = L + 1;
         }
         if (len > W.n - W.ip || len > W.raw - W.O.op) return kLStop;
-        lane_literals<kUndo>(W.R, W.D, W.X, W.O, W.ip, len, W.lim, W.upto);
+        lane_literals<kUndo>(W.R, W.D, W.X, W.O, len, W.lim, W.upto);
         W.ip += len;
         return kLGo;
     }
@@ -1703,13 +1774,14 @@ __device__ __forceinline__ int snappy_step(LaneWalk& W)
     if (t == 1) {
         if (W.ip >= W.n) return kLStop;
         len = ((tag >> 2) & 7u) + 4;
-        off = ((tag >> 5) << 8) | W.R.at(W.ip++);
+        off = ((tag >> 5) << 8) | W.R.byte();
+        ++W.ip;
     } else {
         const uint32_t nb = t == 2 ? 2u : 4u;
         if (nb > W.n - W.ip) return kLStop;
         len = (tag >> 2) + 1;
-        off = 0;
-        for (uint32_t i = 0; i < nb; ++i) off |= W.R.at(W.ip + i) << (8 * i);
+        off = W.R.peek() & (nb == 4 ? 0xFFFFFFFFu : 0xFFFFu);
+        W.R.take(nb);
         W.ip += nb;
     }
     if (!kUndo && !lane_match(W.O, off, len, W.raw)) return kLStop;
@@ -1733,7 +1805,7 @@ __device__ __forceinline__ void lane_run(LaneWalk& W, bool act, int& res)
     }
 }
 
-__global__ void __launch_bounds__(kLThreads) lane_kernel(ApplyArgs A)
+__global__ void __launch_bounds__(kLThreads, 7) lane_kernel(ApplyArgs A)
 {
     if (!A.sc->hdr_ok) return;
     const uint32_t nl = A.sc->n_lane;   // final: written by apply_kernel only
