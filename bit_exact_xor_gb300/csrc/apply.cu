@@ -82,8 +82,10 @@ struct ApplyArgs {
     ApplyScratch* sc;
     uint32_t* defer;          // deferred frames: general LZ4 from the front, large ZSRC from the back
     uint32_t* lane;           // ZSRC frames for lane_kernel (defer_len entries)
+    uint32_t* warp;           // frames for apply_kernel (defer_len entries)
     uint32_t defer_len;
     uint64_t lane_min;        // frames in a stream from which lane_kernel takes its ZSRC frames
+    int self_route;           // apply_kernel routes every frame itself (no route_kernel, no lane_kernel)
     uint64_t plan_hash;
     uint64_t version;
     uint64_t abort_at;
@@ -777,13 +779,16 @@ __device__ __forceinline__ void push_listed(const ApplyArgs& A, int route, int r
     if (r == kRDefer) A.defer[k] = f;
     else if (r == kRLane) A.lane[k] = f;
     else if (r == kRBig) A.defer[A.defer_len - 1 - k] = f;
-    else A.lane[A.defer_len - 1 - k] = f;
+    // a well-formed stream holds one frame per chunk and claimed frames
+    // never outnumber the chunks; only repeated overwrite frames (applied
+    // unclaimed) can: more than the list holds is rejected
+    else if (k < A.defer_len) A.warp[k] = f;
+    else report(A.sc, DCR_ERR_CORRUPT);
 }
 
 // The first apply kernel of the warp route: one warp per 32 frames, each
 // lane checks, claims and routes one frame (frame_route) into the lists of
-// the kernels after it: apply_kernel (warp list, from the end of the lane
-// list's array), lane_kernel, defer_kernel, big_kernel.
+// the kernels after it: apply_kernel, lane_kernel, defer_kernel, big_kernel.
 constexpr int kRtThreads = 256;
 
 __global__ void __launch_bounds__(kRtThreads) route_kernel(ApplyArgs A)
@@ -841,14 +846,29 @@ __global__ void __launch_bounds__(kAThreads, 2) apply_kernel(ApplyArgs A)
     const Hdr H = S.hdr;
     const uint64_t V = H.target_v;
     AWarp& W = S.w[wid];
-    const uint32_t nw = A.sc->n_warp;   // final: written by route_kernel
+    // the frames route_kernel listed, or (self_route) every frame of the
+    // stream, each checked, claimed and routed by lane 0 here
+    const uint32_t nw = A.self_route ? 0u : min(A.sc->n_warp, A.defer_len);
 
     for (;;) {
         uint32_t j = 0;
         if (lane == 0) j = atomicAdd(&A.sc->frame_ticket, 1u);
         j = __shfl_sync(kFull, j, 0);
-        if (j >= nw) break;
-        const uint32_t f = A.lane[A.defer_len - 1 - j];   // the warp list: from the end of lane_kernel's
+        uint32_t f = j;
+        if (A.self_route) {
+            if (j >= H.n_frames) break;
+            int route = kRNone;
+            if (lane == 0) {
+                route = frame_route(A, H, j);
+                if (route == kRSkip) atomicAdd(&A.sc->skipped, 1ull);
+                else if (route == kRDefer) A.defer[atomicAdd(&A.sc->n_defer, 1u)] = j;
+                else if (route == kRBig) A.defer[A.defer_len - 1 - atomicAdd(&A.sc->n_big, 1u)] = j;
+            }
+            if (__shfl_sync(kFull, route, 0) != kRWarp) continue;
+        } else {
+            if (j >= nw) break;
+            f = A.warp[j];
+        }
         const uint64_t fo = ld64(A.payload + H.idx_off + 8ull * f);
         const uint4 h0 = ld_nc16(A.payload + fo), h1 = ld_nc16(A.payload + fo + 16);
         const uint32_t kind = h0.y & 0xFFu;
@@ -1954,6 +1974,10 @@ int launch_first(const dcr_plan* P, const ApplyArgs& A, cudaStream_t s)
         apply_cta_kernel<<<sms * P->kc.apply_cta_blocks_per_sm, kCThreads, sizeof(CSmem), s>>>(A);
         return 1;
     }
+    if (A.self_route) {   // no stream of this plan reaches lane_kernel
+        apply_kernel<<<sms * P->kc.apply_blocks_per_sm, kAThreads, sizeof(ASmem), s>>>(A);
+        return 1;
+    }
     route_kernel<<<sms * 4, kRtThreads, 0, s>>>(A);
     apply_kernel<<<sms * P->kc.apply_blocks_per_sm, kAThreads, sizeof(ASmem), s>>>(A);
     lane_kernel<<<sms * P->kc.lane_blocks_per_sm, kLThreads, 0, s>>>(A);
@@ -1972,8 +1996,9 @@ namespace {
 uint64_t lane_min_frames(const dcr_plan* P)
 {
     if (P->apply == DCR_APPLY_LANE) return 0;
-    if (P->apply == DCR_APPLY_WARP) return UINT64_MAX;
-    return 4ull * P->kc.num_sms * P->kc.big_blocks_per_sm * kBWarps;
+    const uint64_t t = 4ull * P->kc.num_sms * P->kc.big_blocks_per_sm * kBWarps;
+    // launch_first leaves lane_kernel out for plans whose windows are smaller
+    return P->apply == DCR_APPLY_WARP || P->max_window_chunks < t ? UINT64_MAX : t;
 }
 
 ApplyArgs make_args(const dcr_plan* P, dcr_recv_state* st, const void* payload, size_t size, void* target,
@@ -1992,7 +2017,9 @@ ApplyArgs make_args(const dcr_plan* P, dcr_recv_state* st, const void* payload, 
     A.sc = st->d_scratch;
     A.defer = st->d_defer;
     A.lane = st->d_defer + (P->max_window_chunks + 1);
+    A.warp = st->d_defer + 2 * (P->max_window_chunks + 1);
     A.lane_min = lane_min_frames(P);
+    A.self_route = A.lane_min == UINT64_MAX;
     A.defer_len = uint32_t(P->max_window_chunks + 1);
     A.plan_hash = P->hash;
     A.version = st->version;
@@ -2064,7 +2091,7 @@ namespace {
 constexpr uint32_t kNoallocMaxChunks = 65536;    // window limit: 4 GiB of canonical bytes
 constexpr size_t kNoallocHead = 256;             // ApplyScratch, padded
 static_assert(sizeof(ApplyScratch) <= kNoallocHead, "counters fit the head");
-constexpr size_t kNoallocBytes = kNoallocHead + 8 * (size_t(kNoallocMaxChunks) + 1);   // 512 KiB + 264 B
+constexpr size_t kNoallocBytes = kNoallocHead + 12 * (size_t(kNoallocMaxChunks) + 1);   // 768 KiB + 268 B
 
 // [0, 256): ApplyScratch, cleared by a memset on the caller's stream at the
 // start of every call; [256, ...): deferred frame list, written before read.
@@ -2168,7 +2195,9 @@ int apply_launch_noalloc(const dcr_plan* P, dcr_recv_state* st, const void* payl
     A.defer = reinterpret_cast<uint32_t*>(static_cast<unsigned char*>(base) + kNoallocHead);
     A.defer_len = kNoallocMaxChunks + 1;
     A.lane = A.defer + A.defer_len;
+    A.warp = A.defer + 2 * A.defer_len;
     A.lane_min = lane_min_frames(P);
+    A.self_route = A.lane_min == UINT64_MAX;
     A.plan_hash = P->hash;
     A.version = st->version;
     A.abort_at = DCR_NO_FAULT;

@@ -270,6 +270,6 @@ struct dcr_recv_state {
     std::vector<uint8_t> win_done;
     uint64_t* d_chunk_state = nullptr;  // n_chunks
     dcr::ApplyScratch* d_scratch = nullptr;
-    uint32_t* d_defer = nullptr;        // 2 x (max_window_chunks + 1): deferred frames, lane_kernel's list
+    uint32_t* d_defer = nullptr;        // 3 x (max_window_chunks + 1): deferred frames, lane and warp lists
     dcr::ApplyScratch* h_scratch = nullptr;  // pinned
 };

@@ -497,7 +497,7 @@ extern "C" int dcr_recv_state_create(const dcr_plan* p, uint64_t version, dcr_re
     if ((e = cudaMalloc(&s->d_chunk_state, (p->n_chunks ? p->n_chunks : 1) * 8)) != cudaSuccess ||
         (e = cudaMemset(s->d_chunk_state, 0, (p->n_chunks ? p->n_chunks : 1) * 8)) != cudaSuccess ||
         (e = cudaMalloc(&s->d_scratch, sizeof(ApplyScratch))) != cudaSuccess ||
-        (e = cudaMalloc(&s->d_defer, 2 * (p->max_window_chunks + 1) * 4)) != cudaSuccess ||
+        (e = cudaMalloc(&s->d_defer, 3 * (p->max_window_chunks + 1) * 4)) != cudaSuccess ||
         (e = cudaMallocHost(&s->h_scratch, sizeof(ApplyScratch))) != cudaSuccess) {
         dcr_recv_state_destroy(s);
         return cuda_error(e, "allocating receiver state");

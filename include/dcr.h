@@ -303,7 +303,7 @@ int dcr_encode_retry(const dcr_plan* plan, const void* xor_payload, size_t xor_s
  * its KV cache at start-up).  Same arguments, decode, dedup, commit rule and
  * errors as dcr_apply with fault == NULL, but the call's scratch (its
  * counters and the list of deferred frames) is a static device array of the
- * library (256 KiB + 260 B per device) instead of the receiver state's
+ * library (768 KiB + 268 B per device) instead of the receiver state's
  * buffers, and the status is read back into a stack buffer: the call
  * neither allocates nor frees device or pinned memory.
  *   - Limit: windows of at most 65536 chunks (4 GiB of canonical bytes);

@@ -193,6 +193,34 @@ def test_duplicate_frames_applied_once():
     assert np.array_equal(c.host(t), c.exp)
 
 
+@pytest.mark.parametrize("apply", ["cta", "warp", "lane"])
+def test_repeated_overwrite_frames(apply):
+    # overwrite frames are applied unclaimed (idempotent): a stream that
+    # repeats them is applied while they fit route_kernel's frame list (one
+    # entry per chunk and one more), and rejected there, with nothing written
+    # out of bounds, once they outnumber it; the CTA kernel and apply_kernel
+    # routing frames itself keep no such list
+    c = Case(configs.mini(1), apply=APPLY[apply])
+    rp, rsize, _ = c.encode(mode=dcr.MODE_OVERWRITE_ONLY)
+    g = rp[:rsize].cpu().numpy()
+    nf = parse(g)[0]["n_frames"]
+    chunks = c.plan.window(0).chunk_count
+    assert 0 < nf <= chunks
+    fits = _reindexed(g, list(range(nf)) + [0] * (chunks + 1 - nf))
+    t = c.target()
+    st = dcr.RecvState(c.plan, 0)
+    rc, _ = dcr.apply_retry(c.plan, st, torch.from_numpy(fits).cuda(), fits.size, t)
+    assert rc == dcr.OK and st.version == 1 and np.array_equal(c.host(t), c.exp)
+    over = _reindexed(g, list(range(nf)) * 3 + [0] * (chunks + 1))
+    t = c.target()
+    st = dcr.RecvState(c.plan, 0)
+    rc, _ = dcr.apply_retry(c.plan, st, torch.from_numpy(over).cuda(), over.size, t)
+    if apply != "lane":
+        assert rc == dcr.OK and st.version == 1 and np.array_equal(c.host(t), c.exp)
+    else:
+        assert rc == dcr.ERR_CORRUPT and st.version == 0
+
+
 def test_duplicate_oracle_frames_applied_once():
     c = Case(configs.mini(1))
     o, _ = c.orc.encode(c.olds, c.news)
