@@ -1988,15 +1988,18 @@ int launch_first(const dcr_plan* P, const ApplyArgs& A, cudaStream_t s)
 
 namespace {
 
-// Frames in a stream from which apply_kernel hands its ZSRC frames to
-// lane_kernel.  lane_kernel walks a frame in one thread, several times
-// slower than a big_kernel warp walks it but with a tenth of the
-// instructions: it wins once the stream holds more than about four frames
-// per big_kernel warp.
+// Frames in a stream from which its ZSRC frames go to lane_kernel.
+// lane_kernel spends a third of apply_kernel's instructions per frame (a
+// tenth of big_kernel's) but walks a frame several times slower: one
+// thread's chain of a few hundred instructions per sequence.  Its run lasts
+// at least one frame's walk, which the warp kernels' whole run undercuts
+// until the stream fills about a quarter of lane_kernel's thread slots
+// (measured: 16 384 frames of 1 % masks, 0.65 ms in lane_kernel against
+// 0.28 ms in apply_kernel; 131 072, 1.4-1.8 against 2.2 ms).
 uint64_t lane_min_frames(const dcr_plan* P)
 {
     if (P->apply == DCR_APPLY_LANE) return 0;
-    const uint64_t t = 4ull * P->kc.num_sms * P->kc.big_blocks_per_sm * kBWarps;
+    const uint64_t t = uint64_t(P->kc.num_sms) * P->kc.lane_blocks_per_sm * kLThreads / 4;
     // launch_first leaves lane_kernel out for plans whose windows are smaller
     return P->apply == DCR_APPLY_WARP || P->max_window_chunks < t ? UINT64_MAX : t;
 }
