@@ -180,8 +180,9 @@ def _reindexed(pl_np, order):
     return out
 
 
-def test_duplicate_frames_applied_once():
-    c = Case(configs.mini(2))
+@pytest.mark.parametrize("apply", ["auto", "warp", "lane"])
+def test_duplicate_frames_applied_once(apply):
+    c = Case(configs.mini(2), apply=dcr.APPLY_AUTO if apply == "auto" else APPLY[apply])
     pl, size, _ = c.encode()
     g = pl[:size].cpu().numpy()
     nf = parse(g)[0]["n_frames"]
@@ -221,8 +222,9 @@ def test_repeated_overwrite_frames(apply):
         assert rc == dcr.ERR_CORRUPT and st.version == 0
 
 
-def test_duplicate_oracle_frames_applied_once():
-    c = Case(configs.mini(1))
+@pytest.mark.parametrize("apply", ["auto", "warp", "lane"])
+def test_duplicate_oracle_frames_applied_once(apply):
+    c = Case(configs.mini(1), apply=dcr.APPLY_AUTO if apply == "auto" else APPLY[apply])
     o, _ = c.orc.encode(c.olds, c.news)
     nf = parse(o)[0]["n_frames"]
     dup = _reindexed(o, list(range(nf)) + list(range(nf)))
@@ -233,8 +235,9 @@ def test_duplicate_oracle_frames_applied_once():
     assert np.array_equal(c.host(t), c.exp)
 
 
-def test_rejections_leave_target_untouched():
-    c = Case(configs.mini(1))
+@pytest.mark.parametrize("apply", ["auto", "warp", "lane"])
+def test_rejections_leave_target_untouched(apply):
+    c = Case(configs.mini(1), apply=dcr.APPLY_AUTO if apply == "auto" else APPLY[apply])
     pl, size, _ = c.encode(base=3, target=4)
     t = c.target()
     before = c.host(t).copy()
@@ -259,8 +262,9 @@ def test_rejections_leave_target_untouched():
     assert np.array_equal(c.host(t), c.exp)
 
 
-def test_corrupt_lz4_frame_reported_and_retry_recovers():
-    c = Case(configs.mini(1))
+@pytest.mark.parametrize("apply", ["auto", "warp", "lane"])
+def test_corrupt_lz4_frame_reported_and_retry_recovers(apply):
+    c = Case(configs.mini(1), apply=dcr.APPLY_AUTO if apply == "auto" else APPLY[apply])
     pl, size, _ = c.encode()
     g = pl[:size].cpu().numpy()
     _, frames, _ = parse(g)
@@ -407,8 +411,15 @@ def test_signed_zero_on_gpu():
     assert rc == dcr.OK and np.array_equal(tgt.cpu().numpy(), new)
 
 
-def test_kernel_timing_profile():
-    c = Case(configs.mini(2))
+# kernels of one apply: the first phase (CTA kernel; apply_kernel routing
+# itself; route, warp and thread kernels) and the commit check, and with
+# deferred frames the defer and big kernels and the commit check again
+FIRST_PHASE = {"auto": 1, "warp": 1, "lane": 3}
+
+
+@pytest.mark.parametrize("apply", ["auto", "warp", "lane"])
+def test_kernel_timing_profile(apply):
+    c = Case(configs.mini(2), apply=dcr.APPLY_AUTO if apply == "auto" else APPLY[apply])
     p0 = c.plan.last_profile()
     assert p0.encode_valid == 0 and p0.apply_valid == 0
     c.plan.set_profiling(True)
@@ -420,6 +431,8 @@ def test_kernel_timing_profile():
     assert p.encode_valid == 1 and p.apply_valid == 1
     assert p.encode_ms > 0 and p.apply_ms > 0 and p.finalize_ms >= 0 and p.pending_ms >= 0
     assert p.encode_ms < 1000 and p.apply_ms < 1000
+    assert p.encode_kernels == 5
+    assert p.apply_kernels in (FIRST_PHASE[apply] + 1, FIRST_PHASE[apply] + 4)
     c.plan.set_profiling(False)
     q = c.plan.last_profile()
     assert q.encode_valid == 0 and q.apply_valid == 0
