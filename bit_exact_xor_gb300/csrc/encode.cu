@@ -1787,10 +1787,18 @@ __global__ void __launch_bounds__(kEThreads, 4) encode_cta_kernel(EncArgs A)
 
 // ------------------------------------------------------------------ retry --
 // dcr_encode_retry: the overwrite-only stream of a window built from the
-// window's XOR stream and new, without old.  retry_kernel: one CTA per frame
-// of the XOR stream decodes the mask into shared memory (the general
-// decoders), lists the changed units (16-bit words for bf16, else bytes) in
-// order and gathers their new values through the plan's sender pieces:
+// window's XOR stream and new, without old.  retry_lane_kernel: one thread
+// per frame of the XOR stream checks it and claims its chunk; a ZSRC frame
+// is walked in order (the one-thread walk of the apply, lane.cuh), which
+// counts the changed units (16-bit words for bf16, else bytes) and changed
+// stored values without materialising the mask; its frame size goes to the
+// scan, and once the scan has placed every frame retry_lane_write_kernel
+// walks it again and writes the records (unit offsets, new values gathered
+// through the plan's sender pieces) at their place.  Frames that walk cannot
+// take (raw and general blocks, matches it cannot prove) go to
+// retry_kernel: one CTA per frame decodes the mask into shared memory (the
+// general decoders), lists the changed units in order and gathers their new
+// values:
 // OVERWRITE records that fit the slot are written there; records past the
 // slot, dense chunks (records not smaller than the chunk) and frames that
 // already are overwrite records (copied through) are listed for
@@ -1798,6 +1806,7 @@ __global__ void __launch_bounds__(kEThreads, 4) encode_cta_kernel(EncArgs A)
 // has placed every frame.  The frames are those dcr_encode writes in
 // overwrite-only mode, byte for byte.
 #include "decode.cuh"
+#include "lane.cuh"
 
 constexpr int kRThreads = 256;
 constexpr int kRWarps = kRThreads / 32;
@@ -1916,28 +1925,22 @@ __device__ uint32_t retry_load(const EncArgs& A, RSmem& S, uint32_t f, uint64_t*
     return retry_load_at(A, S, fo, k_out, bl_out);
 }
 
+// The frames retry_lane_kernel listed (checked, their chunks claimed).
 __global__ void __launch_bounds__(kRThreads) retry_kernel(EncArgs A)
 {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     RSmem& S = *reinterpret_cast<RSmem*>(smem_raw);
+    const uint32_t nl = A.sc->n_deep;   // final: written by retry_lane_kernel
     for (;;) {
         if (threadIdx.x == 0) S.f = atomicAdd(&A.sc->ticket, 1u);
         __syncthreads();
-        const uint32_t f = S.f;
+        const uint32_t j = S.f;
         __syncthreads();
-        if (f >= A.in_frames) break;
+        if (j >= nl) break;
         uint64_t fo = 0;
         uint32_t k = 0, bl = 0;
-        const uint32_t kind = retry_load(A, S, f, &fo, &k, &bl);
-        if (kind == 0) {
-            if (threadIdx.x == 0) report(A.sc, DCR_ERR_CORRUPT);
-            __syncthreads();
-            continue;
-        }
-        // a chunk has one frame: a second one for it is rejected
-        if (threadIdx.x == 0) S.good = atomicCAS(&A.fsize[k], 0u, kRBusy) == 0u;
-        __syncthreads();
-        if (!S.good) {
+        const uint32_t kind = retry_load(A, S, A.deep[j], &fo, &k, &bl);
+        if (kind == 0) {   // a block the walk could not take, rejected by the full decode
             if (threadIdx.x == 0) report(A.sc, DCR_ERR_CORRUPT);
             __syncthreads();
             continue;
@@ -2015,6 +2018,7 @@ __global__ void __launch_bounds__(kRThreads) retry_spill_kernel(EncArgs A)
     if (A.sc->total > A.cap || *(volatile int32_t*)&A.sc->err) return;
     for (uint32_t i = blockIdx.x; i < n_spill; i += gridDim.x) {
         const SpillRec R = A.spill[i];
+        if (R.pad[2]) continue;   // records of a walked frame: retry_lane_write_kernel's
         const uint64_t fo = uint64_t(R.pad[0]) | (uint64_t(R.pad[1]) << 32);
         uint8_t* f = A.frames + (A.lb[R.k] & kLbByteMask);
         const ChunkDesc cd = A.chunks[A.chunk_begin + R.k];
@@ -2041,6 +2045,199 @@ __global__ void __launch_bounds__(kRThreads) retry_spill_kernel(EncArgs A)
         for (uint32_t x = kFrameHdr + R.body_len + threadIdx.x; x < fsz; x += kRThreads) f[x] = 0;   // padding
         if (threadIdx.x == 0) write_header(f, R.kind, cd.bits, A.chunk_begin + R.k, raw, R.body_len, R.changed);
         __syncthreads();
+    }
+}
+
+// ---- the retry's one-thread walks ----------------------------------------
+constexpr int kRLThreads = 128;
+
+// First walk: changed units (16-bit words for bf16, else bytes) and changed
+// stored values (nibbles for 4-bit data) of a ZSRC frame's mask.
+struct RetryCount {
+    uint32_t ushift, bits, last, n, changed;
+    __device__ __forceinline__ void lit(uint32_t x, uint32_t b)
+    {
+        const uint32_t u = x >> ushift;
+        if (u != last) {
+            last = u;
+            ++n;
+        }
+        if (bits == 4) changed += ((b & 15u) != 0) + ((b >> 4) != 0);
+        else changed += 1;
+    }
+};
+
+// New byte at canonical byte x of a chunk, for x that never decreases,
+// through the chunk's sender pieces.
+struct NewCursor {
+    const EncArgs* A;
+    const Seg* s;
+    uint32_t n, i, next;
+    uint64_t base;   // address of canonical byte 0 in the current piece's shard
+    __device__ __forceinline__ void set(uint32_t j)
+    {
+        i = j;
+        base = reinterpret_cast<uint64_t>(A->news[uint32_t(s[j].addr >> kShardShift)]) + (s[j].addr & kAddrMask) -
+               s[j].off;
+        next = j + 1 < n ? s[j + 1].off : 0xFFFFFFFFu;
+    }
+    __device__ __forceinline__ uint32_t at(uint32_t x)
+    {
+        while (x >= next) set(i + 1);
+        return *reinterpret_cast<const uint8_t*>(base + x);
+    }
+};
+
+// Second walk: the records, in unit order: offsets at body + 4, new values
+// at body + voff.
+struct RetryWrite {
+    uint8_t* body;
+    uint32_t ushift, voff, last, at;
+    NewCursor N;
+    __device__ __forceinline__ void lit(uint32_t x, uint32_t)
+    {
+        const uint32_t u = x >> ushift;
+        if (u == last) return;
+        last = u;
+        *reinterpret_cast<uint16_t*>(body + 4 + 2 * at) = uint16_t(u);
+        if (ushift) {
+            const uint32_t lo = N.at(2 * u), hi = N.at(2 * u + 1);
+            *reinterpret_cast<uint16_t*>(body + voff + 2 * at) = uint16_t(lo | (hi << 8));
+        } else {
+            body[voff + at] = uint8_t(N.at(u));
+        }
+        ++at;
+    }
+};
+
+// The XOR stream's frame f: checks its index entry and header as
+// retry_load_at does.  0 if malformed, else its kind.
+__device__ __forceinline__ uint32_t retry_frame(const EncArgs& A, uint32_t f, uint64_t* fo_out, uint32_t* k_out,
+                                                uint32_t* bl_out, uint32_t* flags_out)
+{
+    const uint8_t* p = A.in;
+    const uint64_t fo = *reinterpret_cast<const uint64_t*>(p + A.in_idx + 8ull * f);
+    if (fo < kStreamHdr || fo % 16 || fo + kFrameHdr > A.in_idx) return 0;
+    const uint4 h0 = *reinterpret_cast<const uint4*>(p + fo), h1 = *reinterpret_cast<const uint4*>(p + fo + 16);
+    const uint32_t kind = h0.y & 0xFFu, fbits = (h0.y >> 8) & 0xFFu;
+    const uint32_t c = h0.z, raw = h0.w, bl = h1.x;
+    if (h0.x != kFrameMagic || kind < kXorLz4 || kind > kXorSnappy || c < A.chunk_begin ||
+        c >= A.chunk_begin + A.chunk_count || bl > A.in_idx - fo - kFrameHdr)
+        return 0;
+    const ChunkDesc cd = A.chunks[c];
+    if (raw != cd.raw_len || fbits != cd.bits) return 0;
+    *fo_out = fo;
+    *k_out = c - A.chunk_begin;
+    *bl_out = bl;
+    *flags_out = h0.y >> 16;
+    return kind;
+}
+
+__global__ void __launch_bounds__(kRLThreads) retry_lane_kernel(EncArgs A)
+{
+    const int lane = threadIdx.x & 31;
+    const uint32_t wpb = kRLThreads / 32, nw = gridDim.x * wpb;
+    // 32 consecutive frames per warp, spread over the blocks first
+    for (uint64_t g = uint64_t(threadIdx.x >> 5) * gridDim.x + blockIdx.x; 32 * g < A.in_frames; g += nw) {
+        const uint64_t j = 32 * g + lane;
+        LaneWalk<RetryCount> W;
+        bool act = false;
+        int res = kLStop;
+        uint64_t fo = 0;
+        uint32_t k = 0, bl = 0, fl = 0, kind = 0;
+        bool walk = false;
+        if (j < A.in_frames) {
+            kind = retry_frame(A, uint32_t(j), &fo, &k, &bl, &fl);
+            if (kind == 0) {
+                report(A.sc, DCR_ERR_CORRUPT);
+            } else if (atomicCAS(&A.fsize[k], 0u, kRBusy) != 0u) {   // a chunk has one frame
+                report(A.sc, DCR_ERR_CORRUPT);
+            } else if (kind == kOverwrite || kind == kOverwriteDense) {   // already records: through
+                A.fsize[k] = ((kFrameHdr + bl + 15) / 16 * 16) | kSpilled;
+                A.spill[atomicAdd(&A.sc->n_spill, 1u)] =
+                    SpillRec{k, 0u, bl, 0u, 0u, {uint32_t(fo), uint32_t(fo >> 32), 0u}};
+            } else if ((kind == kXorLz4 || kind == kXorSnappy) && (fl & kFrameZsrc)) {
+                const ChunkDesc cd = A.chunks[A.chunk_begin + k];
+                W.init(kind == kXorSnappy, A.in + fo + kFrameHdr, bl, cd.raw_len, 0);
+                W.K = RetryCount{cd.bits == 16 ? 1u : 0u, cd.bits, 0xFFFFFFFFu, 0u, 0u};
+                act = !W.sn || snappy_pre(W);
+                walk = true;
+            } else {
+                A.deep[atomicAdd(&A.sc->n_deep, 1u)] = uint32_t(j);
+            }
+        }
+        lane_run<false>(W, act, res);
+        if (!walk) continue;
+        if (res != kLValid) {   // the full decode decides
+            A.deep[atomicAdd(&A.sc->n_deep, 1u)] = uint32_t(j);
+            continue;
+        }
+        const ChunkDesc cd = A.chunks[A.chunk_begin + k];
+        const uint32_t n = W.K.n, ub = cd.bits == 16 ? 2u : 1u, raw = cd.raw_len;
+        const uint32_t changed = ub == 2 ? n : W.K.changed;
+        if (n == 0) {   // an XOR frame with nothing changed is not what the encoder writes
+            report(A.sc, DCR_ERR_CORRUPT);
+            continue;
+        }
+        const uint32_t rec = 4 + 2 * n + (4 - (2 * n) % 4) % 4 + n * ub;
+        const uint32_t kind_out = rec < raw ? kOverwrite : kOverwriteDense;
+        const uint32_t body_len = kind_out == kOverwrite ? rec : raw;
+        A.fsize[k] = ((kFrameHdr + body_len + 15) / 16 * 16) | kSpilled;
+        // records: the second walk's (pad[2] = 1); dense: retry_spill_kernel's
+        A.spill[atomicAdd(&A.sc->n_spill, 1u)] = SpillRec{
+            k, kind_out, body_len, n, changed, {uint32_t(fo), uint32_t(fo >> 32), kind_out == kOverwrite ? 1u : 0u}};
+    }
+}
+
+// The records of the frames retry_lane_kernel walked, at their places.
+__global__ void __launch_bounds__(kRLThreads) retry_lane_write_kernel(EncArgs A)
+{
+    const uint32_t n_spill = A.sc->n_spill;   // final
+    if (A.sc->total > A.cap || *(volatile int32_t*)&A.sc->err) return;
+    const int lane = threadIdx.x & 31;
+    const uint32_t wpb = kRLThreads / 32, nw = gridDim.x * wpb;
+    for (uint32_t g = (threadIdx.x >> 5) * gridDim.x + blockIdx.x; 32ull * g < n_spill; g += nw) {
+        const uint32_t i = 32 * g + lane;
+        LaneWalk<RetryWrite> W;
+        bool act = false;
+        int res = kLStop;
+        SpillRec R{};
+        uint8_t* f = nullptr;
+        if (i < n_spill) {
+            R = A.spill[i];
+            if (R.pad[2]) {
+                const uint64_t fo = uint64_t(R.pad[0]) | (uint64_t(R.pad[1]) << 32);
+                const ChunkDesc cd = A.chunks[A.chunk_begin + R.k];
+                f = A.frames + (A.lb[R.k] & kLbByteMask);
+                uint8_t* body = f + kFrameHdr;
+                const uint32_t n = R.n_units, voff = 4 + 2 * n + (4 - (2 * n) % 4) % 4;
+                *reinterpret_cast<uint32_t*>(body) = n;
+                for (uint32_t x = 4 + 2 * n; x < voff; ++x) body[x] = 0;
+                const uint8_t kind = A.in[fo + 4];
+                W.init(kind == kXorSnappy, A.in + fo + kFrameHdr, *reinterpret_cast<const uint32_t*>(A.in + fo + 16),
+                       cd.raw_len, 0);
+                W.K.body = body;
+                W.K.ushift = cd.bits == 16 ? 1u : 0u;
+                W.K.voff = voff;
+                W.K.last = 0xFFFFFFFFu;
+                W.K.at = 0;
+                W.K.N.A = &A;
+                W.K.N.s = A.src + cd.src_begin;
+                W.K.N.n = cd.src_count;
+                W.K.N.set(0);
+                act = !W.sn || snappy_pre(W);
+            }
+        }
+        lane_run<false>(W, act, res);
+        if (!f) continue;
+        if (res != kLValid || W.K.at != R.n_units) {   // the first walk passed this frame
+            report(A.sc, DCR_ERR_CORRUPT);
+            continue;
+        }
+        const ChunkDesc cd = A.chunks[A.chunk_begin + R.k];
+        const uint32_t fsz = (kFrameHdr + R.body_len + 15) / 16 * 16;
+        for (uint32_t x = kFrameHdr + R.body_len; x < fsz; ++x) f[x] = 0;   // padding
+        write_header(f, kOverwrite, cd.bits, A.chunk_begin + R.k, cd.raw_len, R.body_len, R.changed);
     }
 }
 
@@ -2290,7 +2487,9 @@ int retry_launch(const dcr_plan* P, const void* in, uint64_t in_idx, uint64_t in
     if (e == cudaSuccess) e = cudaMemsetAsync(P->d_tiles, 0, ntiles * sizeof(uint64_t), s);
     if (e != cudaSuccess) return cuda_error(e, "retry scratch reset");
     const unsigned rgrid = unsigned(P->kc.num_sms * P->kc.retry_blocks_per_sm);
+    const unsigned lgrid = unsigned(P->kc.num_sms * 8);
     if (P->profiling) cudaEventRecord(P->ev[0], s);
+    retry_lane_kernel<<<lgrid, kRLThreads, 0, s>>>(A);
     retry_kernel<<<rgrid, kRThreads, sizeof(RSmem), s>>>(A);
     if (P->profiling) cudaEventRecord(P->ev[1], s);
     scan_kernel<<<ntiles, 1024, 0, s>>>(A, P->d_tiles, P->hash, base_v, target_v, window);
@@ -2299,6 +2498,7 @@ int retry_launch(const dcr_plan* P, const void* in, uint64_t in_idx, uint64_t in
     if (cgrid == 0) cgrid = 1;
     copy_kernel<<<cgrid, 256, 0, s>>>(A);
     retry_spill_kernel<<<rgrid, kRThreads, sizeof(RSmem), s>>>(A);
+    retry_lane_write_kernel<<<lgrid, kRLThreads, 0, s>>>(A);
     if (P->profiling) cudaEventRecord(P->ev[2], s);
     e = cudaGetLastError();
     return e == cudaSuccess ? DCR_OK : cuda_error(e, "retry launch");
