@@ -197,3 +197,33 @@ def test_truncated_frame_rejected_and_undone(setup, codec):
     assert orc_rc == oracle.E_CORRUPT and rc == dcr.ERR_CORRUPT
     assert np.array_equal(got[2 * CHUNK:3 * CHUNK], start[2 * CHUNK:3 * CHUNK])
     assert np.array_equal(got, ref)
+
+
+@pytest.mark.parametrize("codec", ["lz4", "snappy"])
+def test_retry_stream_from_hand_made_xor_stream(setup, codec):
+    # dcr_encode_retry walks ZSRC frames one thread each too: a valid match it
+    # cannot prove hands the frame to the full decode, which must build the
+    # same records; the retry stream then equals the oracle's overwrite-only
+    # encode of (old, old ^ mask) byte for byte.  A lying frame is rejected.
+    wl, orc, old, plans = setup
+    plan = plans[dcr.CODEC_LZ4 if codec == "lz4" else dcr.CODEC_SNAPPY]
+    for kinds, ok in ((["recent", "old_gap", "plain", "old_gap"], True), (["recent", "lying", "plain", "plain"], False)):
+        rng = np.random.RandomState(11)
+        frames, new = [], old.copy()
+        for c, kind in enumerate(kinds):
+            body = lz4_case(kind, rng) if codec == "lz4" else snappy_case(kind, rng)
+            dec = oracle.lz4_decode if codec == "lz4" else oracle.snappy_decode
+            m = dec(np.frombuffer(body, np.uint8), CHUNK)
+            new[c * CHUNK:(c + 1) * CHUNK] ^= m
+            frames.append((K_XOR_LZ4 if codec == "lz4" else K_XOR_SNAPPY, 8, FRAME_ZSRC, c, CHUNK,
+                           int(np.count_nonzero(m)), body))
+        stream = np.frombuffer(build_stream(orc.plan_hash, 0, 0, N_CHUNKS, frames), np.uint8).copy()
+        d_new = to_device([new])
+        out = torch.zeros(plan.window(0).payload_bound, dtype=torch.uint8, device="cuda")
+        rc, size = dcr.encode_retry(plan, torch.from_numpy(stream).cuda(), stream.size, d_new, out)
+        if not ok:
+            assert rc == dcr.ERR_CORRUPT
+            continue
+        assert rc == dcr.OK, dcr.last_error()
+        ref, _ = orc.encode([old], [new], mode=oracle.MODE_OVERWRITE_ONLY)
+        assert size == ref.size and np.array_equal(out[:size].cpu().numpy(), ref)
