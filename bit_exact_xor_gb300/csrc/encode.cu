@@ -2089,16 +2089,21 @@ struct NewCursor {
 };
 
 // Second walk: the records, in unit order: offsets at body + 4, new values
-// at body + voff.
+// at body + voff; never more than the first walk's n (at counts past it, and
+// the caller rejects the frame).
 struct RetryWrite {
     uint8_t* body;
-    uint32_t ushift, voff, last, at;
+    uint32_t ushift, voff, last, at, n;
     NewCursor N;
     __device__ __forceinline__ void lit(uint32_t x, uint32_t)
     {
         const uint32_t u = x >> ushift;
         if (u == last) return;
         last = u;
+        if (at >= n) {
+            ++at;
+            return;
+        }
         *reinterpret_cast<uint16_t*>(body + 4 + 2 * at) = uint16_t(u);
         if (ushift) {
             const uint32_t lo = N.at(2 * u), hi = N.at(2 * u + 1);
@@ -2221,6 +2226,7 @@ __global__ void __launch_bounds__(kRLThreads) retry_lane_write_kernel(EncArgs A)
                 W.K.voff = voff;
                 W.K.last = 0xFFFFFFFFu;
                 W.K.at = 0;
+                W.K.n = n;
                 W.K.N.A = &A;
                 W.K.N.s = A.src + cd.src_begin;
                 W.K.N.n = cd.src_count;
