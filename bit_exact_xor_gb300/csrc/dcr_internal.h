@@ -175,8 +175,9 @@ int apply_launch(const struct ::dcr_plan* plan, struct ::dcr_recv_state* st, con
 enum { kApplyAll = 0, kApplyFirst = 1, kApplyDeferred = 2 };
 // kernels one call launches: dcr_encode (encode, scan, copy, restream,
 // spill), dcr_encode_retry (retry walk, retry, scan, copy, retry spill,
-// retry write); dcr_apply counts its own (dcr_plan::apply_kernels)
-constexpr uint32_t kEncodeKernels = 5, kRetryKernels = 6;
+// retry write, retry values); dcr_apply counts its own
+// (dcr_plan::apply_kernels)
+constexpr uint32_t kEncodeKernels = 5, kRetryKernels = 7;
 int apply_launch_part(const struct ::dcr_plan* plan, struct ::dcr_recv_state* st, const void* payload,
                       size_t size, void* target, uint64_t abort_at, uint32_t split, int retry_only, int part,
                       cudaStream_t s);

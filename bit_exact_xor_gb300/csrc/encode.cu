@@ -2067,50 +2067,20 @@ struct RetryCount {
     }
 };
 
-// New byte at canonical byte x of a chunk, for x that never decreases,
-// through the chunk's sender pieces.
-struct NewCursor {
-    const EncArgs* A;
-    const Seg* s;
-    uint32_t n, i, next;
-    uint64_t base;   // address of canonical byte 0 in the current piece's shard
-    __device__ __forceinline__ void set(uint32_t j)
-    {
-        i = j;
-        base = reinterpret_cast<uint64_t>(A->news[uint32_t(s[j].addr >> kShardShift)]) + (s[j].addr & kAddrMask) -
-               s[j].off;
-        next = j + 1 < n ? s[j + 1].off : 0xFFFFFFFFu;
-    }
-    __device__ __forceinline__ uint32_t at(uint32_t x)
-    {
-        while (x >= next) set(i + 1);
-        return *reinterpret_cast<const uint8_t*>(base + x);
-    }
-};
-
-// Second walk: the records, in unit order: offsets at body + 4, new values
-// at body + voff; never more than the first walk's n (at counts past it, and
-// the caller rejects the frame).
+// Second walk: the records' unit offsets, in order, at body + 4 (their
+// new values are gathered after it, by retry_values_kernel: a gather in
+// the walk would put a DRAM round trip in its chain for every unit); never
+// more than the first walk's n (at counts past it, and the caller rejects
+// the frame).
 struct RetryWrite {
     uint8_t* body;
-    uint32_t ushift, voff, last, at, n;
-    NewCursor N;
+    uint32_t ushift, last, at, n;
     __device__ __forceinline__ void lit(uint32_t x, uint32_t)
     {
         const uint32_t u = x >> ushift;
         if (u == last) return;
         last = u;
-        if (at >= n) {
-            ++at;
-            return;
-        }
-        *reinterpret_cast<uint16_t*>(body + 4 + 2 * at) = uint16_t(u);
-        if (ushift) {
-            const uint32_t lo = N.at(2 * u), hi = N.at(2 * u + 1);
-            *reinterpret_cast<uint16_t*>(body + voff + 2 * at) = uint16_t(lo | (hi << 8));
-        } else {
-            body[voff + at] = uint8_t(N.at(u));
-        }
+        if (at < n) *reinterpret_cast<uint16_t*>(body + 4 + 2 * at) = uint16_t(u);
         ++at;
     }
 };
@@ -2223,14 +2193,9 @@ __global__ void __launch_bounds__(kRLThreads) retry_lane_write_kernel(EncArgs A)
                        cd.raw_len, 0);
                 W.K.body = body;
                 W.K.ushift = cd.bits == 16 ? 1u : 0u;
-                W.K.voff = voff;
                 W.K.last = 0xFFFFFFFFu;
                 W.K.at = 0;
                 W.K.n = n;
-                W.K.N.A = &A;
-                W.K.N.s = A.src + cd.src_begin;
-                W.K.N.n = cd.src_count;
-                W.K.N.set(0);
                 act = !W.sn || snappy_pre(W);
             }
         }
@@ -2244,6 +2209,28 @@ __global__ void __launch_bounds__(kRLThreads) retry_lane_write_kernel(EncArgs A)
         const uint32_t fsz = (kFrameHdr + R.body_len + 15) / 16 * 16;
         for (uint32_t x = kFrameHdr + R.body_len; x < fsz; ++x) f[x] = 0;   // padding
         write_header(f, kOverwrite, cd.bits, A.chunk_begin + R.k, cd.raw_len, R.body_len, R.changed);
+    }
+}
+
+// The new values of the walked frames' records: one warp per frame, a
+// lane per unit (offsets written by retry_lane_write_kernel).
+__global__ void __launch_bounds__(256) retry_values_kernel(EncArgs A)
+{
+    const uint32_t n_spill = A.sc->n_spill;   // final
+    if (A.sc->total > A.cap || *(volatile int32_t*)&A.sc->err) return;
+    const int lane = threadIdx.x & 31;
+    const uint32_t nw = gridDim.x * (blockDim.x >> 5);
+    for (uint32_t i = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); i < n_spill; i += nw) {
+        const SpillRec R = A.spill[i];
+        if (!R.pad[2]) continue;
+        const ChunkDesc cd = A.chunks[A.chunk_begin + R.k];
+        const uint32_t ub = cd.bits == 16 ? 2u : 1u, n = R.n_units, voff = 4 + 2 * n + (4 - (2 * n) % 4) % 4;
+        uint8_t* body = A.frames + (A.lb[R.k] & kLbByteMask) + kFrameHdr;
+        const Seg* segs = A.src + cd.src_begin;
+        for (uint32_t j = lane; j < n; j += 32) {
+            const uint32_t u = *reinterpret_cast<const uint16_t*>(body + 4 + 2 * j);
+            for (uint32_t e = 0; e < ub; ++e) body[voff + j * ub + e] = new_byte(A, segs, int(cd.src_count), u * ub + e);
+        }
     }
 }
 
@@ -2505,6 +2492,7 @@ int retry_launch(const dcr_plan* P, const void* in, uint64_t in_idx, uint64_t in
     copy_kernel<<<cgrid, 256, 0, s>>>(A);
     retry_spill_kernel<<<rgrid, kRThreads, sizeof(RSmem), s>>>(A);
     retry_lane_write_kernel<<<lgrid, kRLThreads, 0, s>>>(A);
+    retry_values_kernel<<<cgrid, 256, 0, s>>>(A);
     if (P->profiling) cudaEventRecord(P->ev[2], s);
     e = cudaGetLastError();
     return e == cudaSuccess ? DCR_OK : cuda_error(e, "retry launch");
