@@ -1424,7 +1424,7 @@ __global__ void __launch_bounds__(kBThreads, 3) big_kernel(ApplyArgs A)
     const uint8_t* p = A.payload;
     const uint64_t total = ld64(p + 56), nf = ld64(p + 48), idx_off = total - 8 * nf;
     const uint64_t V = ld64(p + 24);
-    const uint32_t nbig = A.sc->n_big;   // final: written by apply_kernel only
+    const uint32_t nbig = A.sc->n_big;   // final: written by the first phase (route, apply, CTA and lane kernels)
     if (nbig == 0) return;
     for (;;) {
         uint32_t j = 0;
@@ -1537,7 +1537,7 @@ struct ApplySink {
 __global__ void __launch_bounds__(kLThreads, 7) lane_kernel(ApplyArgs A)
 {
     if (!A.sc->hdr_ok) return;
-    const uint32_t nl = A.sc->n_lane;   // final: written by apply_kernel only
+    const uint32_t nl = A.sc->n_lane;   // final: written by route_kernel
     if (nl == 0) return;
     const uint8_t* p = A.payload;
     const uint64_t total = ld64(p + 56), nf = ld64(p + 48), idx_off = total - 8 * nf;
