@@ -1356,7 +1356,7 @@ __global__ void __launch_bounds__(kDThreads) defer_kernel(ApplyArgs A)
     extern __shared__ __align__(16) unsigned char smem_raw[];
     uint8_t* out = smem_raw;                       // kChunk bytes
     __shared__ uint32_t s_f, s_good;
-    // final: apply_kernel alone lists deferred frames
+    // final: the first phase (route, apply or CTA kernel) lists deferred frames
     if (!A.sc->hdr_ok || *reinterpret_cast<volatile uint32_t*>(&A.sc->n_defer) == 0) return;
     const uint8_t* p = A.payload;
     const uint64_t total = ld64(p + 56), nf = ld64(p + 48), idx_off = total - 8 * nf;
