@@ -97,6 +97,7 @@ def measured_peak():
 
 
 PROFILED = {"dense": "encode_kernel_dense_tp2.md", "moe": "encode_kernel_nvfp4_moe.md"}
+APPLY_VARIANTS = {"auto": 0, "warp": 1, "cta": 2, "lane": 3}   # dcr_plan_opts.apply
 
 
 def ncu_traffic(args, bytes_per_launch):
@@ -279,6 +280,7 @@ def run_config(args, wl, nw, ws):
         name += " [change rate set to %s]" % ("a fully random new buffer" if change_rate(args) == "random"
                                              else "%g%%" % (100 * args.frac))
     return {"workload": name, "change_rate": change_rate(args), "canonical_bytes": N, "codec": getattr(args, "codec", "lz4"),
+            "apply": getattr(args, "apply", "auto"),
             "tp": wl.tp, "windows": nw, "parallelism": "replicas" if ws > 1 else "single GPU",
             "l2": "L2 flushed before each timed step (%d MiB written outside the step's events)" % (FLUSH_BYTES >> 20)
             if l2_resident(N) else "inputs larger than L2 (2N = %.2f GB read per encode)" % (2 * N / 1e9)}
@@ -339,7 +341,8 @@ def run_gpu(args):
     N = wl.canonical_bytes
     plan = dcr.Plan(descs_of(wl), window_bytes=(args.window_mb << 20) or wl.window_bytes,
                     codec=dcr.CODEC_SNAPPY if args.codec == "snappy" else dcr.CODEC_LZ4,
-                    overflow_kib=dcr.NO_OVERFLOW if args.overflow_kib < 0 else args.overflow_kib)
+                    overflow_kib=dcr.NO_OVERFLOW if args.overflow_kib < 0 else args.overflow_kib,
+                    apply=APPLY_VARIANTS[args.apply])
     plan.set_profiling(True)
     olds, news = wl.device_arenas(torch)
     target = torch.empty(max(plan.info.recv_bytes, wl.recv_bytes), dtype=torch.uint8, device=dev)
@@ -781,6 +784,9 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--window-mb", type=int, default=0, help="window size in MiB (0: the workload's)")
     ap.add_argument("--codec", default="lz4", choices=["lz4", "snappy"], help="block codec of the XOR masks")
+    ap.add_argument("--apply", default="auto", choices=sorted(APPLY_VARIANTS),
+                    help="apply kernels: auto, warp (one warp per frame), cta (one CTA per frame), "
+                         "lane (one thread per ZSRC frame)")
     ap.add_argument("--overflow-kib", type=int, default=0,
                     help="encoder overflow heap in KiB (0: one eighth of the window, -1: none)")
     ap.add_argument("--abort-retry", action="store_true",
