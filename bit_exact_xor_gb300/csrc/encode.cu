@@ -1056,7 +1056,6 @@ __device__ __forceinline__ void restream_chunk(const EncArgs& A, WarpSmem& W, ui
     __syncwarp();
     const Seg* segs = cached ? W.segs : A.src + cd.src_begin;
     const bool vec = (cd.flags & kSrcVec) != 0;
-    const uint32_t ub = cd.bits == 16 ? 2u : 1u;
     uint8_t* f = A.frames + (A.lb[R.k] & kLbByteMask);
     uint8_t* body = f + kFrameHdr;
     const uint32_t nu = R.n_units;
