@@ -43,12 +43,19 @@ WORKLOADS = [("mini-moe", lambda: configs.mini(5)), ("mini-gqa", lambda: configs
             [("random-%d" % s, (lambda s=s: random_workload(s))) for s in (1, 4, 7, 12)]
 
 
-@pytest.mark.parametrize("name,make", WORKLOADS, ids=[w[0] for w in WORKLOADS])
-def test_pipelined_refit_matches_oracle_and_sequential(name, make):
+# the apply kernels AUTO picks for these small windows (one CTA per frame), and
+# the route + warp + thread-per-frame kernels with every deferred kernel
+CASES = [(w, a) for w in WORKLOADS for a in ("auto", "lane")]
+
+
+@pytest.mark.parametrize("name,make,apply", [(w[0], w[1], a) for w, a in CASES],
+                         ids=["%s-%s" % (w[0], a) for w, a in CASES])
+def test_pipelined_refit_matches_oracle_and_sequential(name, make, apply):
     wl = make()
     orc = oracle.Oracle(wl)
     olds, news = wl.host_arenas()
-    plan = dcr.Plan(descs_of(wl), window_bytes=wl.window_bytes)
+    plan = dcr.Plan(descs_of(wl), window_bytes=wl.window_bytes,
+                    apply=dcr.APPLY_LANE if apply == "lane" else dcr.APPLY_AUTO)
     d_old, d_new = to_device(olds), to_device(news)
     dev, host = _buffers(plan)
     t = _target(plan, wl, d_old)
