@@ -25,9 +25,10 @@
  *     payload must be 16-byte aligned.
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *     stream).  Work is stream-ordered; dcr_encode, dcr_apply and
- *     dcr_apply_retry end with one small device-to-host status read and a
- *     synchronisation of `stream`, so their outputs (sizes, counts, status,
- *     version) are final when they return.
+ *     dcr_apply_retry end with a small device-to-host status read and a
+ *     synchronisation of `stream` (dcr_apply with two when frames were
+ *     deferred to its second-phase kernels), so their outputs (sizes,
+ *     counts, status, version) are final when they return.
  *   - A plan's scratch (frame slots, counters) and a receiver state's
  *     scratch are shared by every call that uses them: calls on one plan, or
  *     on one receiver state, must not overlap in time.
@@ -263,7 +264,9 @@ int dcr_encode(const dcr_plan* plan, uint32_t mode, uint32_t window,
  * version advances to target_version once every window of it has all its
  * framed chunks DONE.  fault is test only (nullable); result is nullable.
  * Errors: DCR_ERR_INVALID (plan hash, window, argument), DCR_ERR_VERSION,
- * DCR_ERR_CORRUPT (malformed frames; the others are still applied),
+ * DCR_ERR_CORRUPT (malformed frames; the others are still applied; also a
+ * stream that repeats overwrite frames more often than the window has
+ * chunks, when the plan routes frames through its frame lists),
  * DCR_ERR_ABORTED, DCR_ERR_INCOMPLETE (claimed chunks left unfinished by an
  * earlier abort: run dcr_apply_retry), DCR_ERR_CUDA. */
 int dcr_apply(const dcr_plan* plan, dcr_recv_state* state, const void* payload, size_t size,
@@ -444,8 +447,8 @@ int dcr_stream_header(const dcr_plan* plan, uint32_t mode, uint32_t window, uint
 typedef struct {
     float encode_ms;    /* gather + XOR + count + encode + frame write (main kernel) */
     float finalize_ms;  /* spilled (dense) chunk bodies, frame index, stream header */
-    float apply_ms;     /* warp-per-frame decode and apply */
-    float defer_ms;     /* general LZ4 frames */
+    float apply_ms;     /* first phase: routing, warp- / CTA- / thread-per-frame walks */
+    float defer_ms;     /* deferred frames: general blocks, bitmap walk (0 if none) */
     float pending_ms;   /* commit check */
     uint32_t encode_valid, apply_valid;
     uint32_t encode_kernels, apply_kernels;   /* kernels those calls launched */
