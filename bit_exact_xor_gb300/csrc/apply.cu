@@ -364,6 +364,7 @@ __device__ __forceinline__ uint32_t seq_end_ldg(const uint8_t* src, uint32_t n, 
 // format): a sequence is a token, its literals, a 2-byte offset and the
 // match-length bytes; the last sequence is literals only.
 struct Lz4Walk {
+    static constexpr uint32_t kWin = 256;   // no limit below the warp's window
     __device__ static uint32_t first(const uint8_t*, uint32_t, uint32_t) { return 0; }
     template <bool kGlobal>
     __device__ static uint32_t end(const uint8_t* src, uint32_t n, uint32_t p)
@@ -411,6 +412,8 @@ struct Lz4Walk {
 // and copies (tag 1: length 4..11, 11-bit offset; tag 2 / 3: length 1..64,
 // 2- / 4-byte offset).  An element is a literal run or a copy.
 struct SnappyWalk {
+    // elements average under 3 bytes: 96 bytes hold the 32 a batch takes
+    static constexpr uint32_t kWin = 96;
     __device__ static uint32_t first(const uint8_t* src, uint32_t n, uint32_t raw)
     {
         uint64_t v = 0;
@@ -517,7 +520,7 @@ __device__ int zsrc_apply(const ApplyArgs& A, const ChunkDesc& cd, const Seg* ds
     if (n == 0) return 0;   // a block holds at least one element
     const uint32_t ip0 = Walk::first(src, n, raw);
     if (ip0 == kEndBad) return 0;
-    constexpr uint32_t kWin = WS::kWin;
+    constexpr uint32_t kWin = Walk::kWin < WS::kWin ? Walk::kWin : WS::kWin;
     static_assert(kWin % 32 == 0 && kWin < kStop, "window: whole lane groups, offsets below kStop");
     const bool one = cd.dst_count == 1;
     const uint64_t base = one ? ds[0].addr - ds[0].off : 0ull;   // single receiver piece
