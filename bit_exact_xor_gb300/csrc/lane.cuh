@@ -71,7 +71,7 @@ struct LaneRd {
     }
     // the next four bytes (the next byte lowest)
     __device__ __forceinline__ uint32_t peek() const { return uint32_t(q); }
-    // move past k <= 5 bytes (never more than are held)
+    // move past k <= 4 bytes
     __device__ __forceinline__ void take(uint32_t k)
     {
         q >>= 8 * k;
@@ -103,20 +103,6 @@ struct LaneOut {
 // longest gap of the earlier groups of 32 non-zero bytes, from the gap just
 // before (Snappy), or from a zero it keeps as a literal (offset 1); each of
 // those sources is one of the stretches kept here.
-// The zero-stretch bookkeeping of a non-zero literal byte at output x.
-__device__ __forceinline__ void lane_seen(LaneOut& O, uint32_t x)
-{
-    const uint32_t gap = ((x - O.z1) << 16) | O.z1;
-    if (gap > O.cur) O.cur = gap;
-    if ((++O.ev & 31u) == 0) {
-        if (O.cur > O.best) O.best = O.cur;
-        O.cur = 0;
-    }
-    O.g0 = O.z1;
-    O.g1 = x;
-    O.z1 = x + 1;
-}
-
 template <bool kUndo, class Sink>
 __device__ __forceinline__ void lane_literals(LaneRd& R, Sink& K, LaneOut& O, uint32_t ll, uint32_t upto)
 {
@@ -135,7 +121,17 @@ __device__ __forceinline__ void lane_literals(LaneRd& R, Sink& K, LaneOut& O, ui
                 O.op += ll;
                 return;
             }
-            if (!kUndo) lane_seen(O, x);
+            if (!kUndo) {
+                const uint32_t gap = ((x - O.z1) << 16) | O.z1;
+                if (gap > O.cur) O.cur = gap;
+                if ((++O.ev & 31u) == 0) {
+                    if (O.cur > O.best) O.best = O.cur;
+                    O.cur = 0;
+                }
+                O.g0 = O.z1;
+                O.g1 = x;
+                O.z1 = x + 1;
+            }
             K.lit(x, b);
         }
     }
@@ -221,36 +217,6 @@ __device__ __forceinline__ int lz4_step(LaneWalk<Sink>& W)
 {
     if (kUndo && W.O.op >= W.upto) return kLStop;
     if (W.ip >= W.n) return kLStop;
-    if (!kUndo) {
-        // the common shape in one piece: token, one or two literal bytes and
-        // the offset, all in the reader's register (it holds at least 5
-        // bytes), taken at once
-        const uint64_t q = W.R.q;
-        const uint32_t tok = uint32_t(q) & 0xFFu, ll = tok >> 4;
-        if (ll - 1 < 2 && W.n - W.ip >= 3 + ll && ll <= W.raw - W.O.op) {
-            const uint32_t b0 = uint32_t(q >> 8) & 0xFFu, b1 = ll == 2 ? uint32_t(q >> 16) & 0xFFu : 0u;
-            const uint32_t off = uint32_t(q >> (8 + 8 * ll)) & 0xFFFFu;
-            W.R.take(3 + ll);
-            W.ip += 3 + ll;
-            const uint32_t x = W.O.op;
-            if (b0) {
-                lane_seen(W.O, x);
-                W.K.lit(x, b0);
-            }
-            if (b1) {
-                lane_seen(W.O, x + 1);
-                W.K.lit(x + 1, b1);
-            }
-            W.O.op += ll;
-            W.O.done = W.O.op;
-            uint32_t ml = tok & 15u;
-            if (ml == 15 && !lane_len_bytes(W, &ml)) return kLStop;
-            ml += 4;
-            if (!lane_match(W.O, off, ml, W.raw)) return kLStop;
-            W.O.op += ml;
-            return kLGo;
-        }
-    }
     const uint32_t tok = W.R.byte();
     ++W.ip;
     uint32_t ll = tok >> 4;
