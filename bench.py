@@ -15,6 +15,7 @@ per refit) are larger than L2; workloads small enough to stay in L2 get a
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
                   [--workload moe|dense|single|gqa|sweep] [--frac F]
                   [--moe-layers L] [--window-mb M] [--codec lz4|snappy] [--overflow-kib K]
+                  [--apply auto|warp|cta|lane]
                   [--pipeline] [--abort-retry] [--shard] [--no-e2e] [--no-cpu-baseline]
 
 Prints one JSON line.  --impl reference times the CPU oracle (the
