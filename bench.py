@@ -15,7 +15,7 @@ per refit) are larger than L2; workloads small enough to stay in L2 get a
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
                   [--workload moe|dense|single|gqa|sweep] [--frac F]
                   [--moe-layers L] [--window-mb M] [--codec lz4|snappy] [--overflow-kib K]
-                  [--apply auto|warp|cta|lane]
+                  [--encoder auto|wide|deep|cta] [--apply auto|warp|cta|lane]
                   [--pipeline] [--abort-retry] [--shard] [--no-e2e] [--no-cpu-baseline]
 
 Prints one JSON line.  --impl reference times the CPU oracle (the
@@ -99,6 +99,7 @@ def measured_peak():
 
 PROFILED = {"dense": "encode_kernel_dense_tp2.md", "moe": "encode_kernel_nvfp4_moe.md"}
 APPLY_VARIANTS = {"auto": 0, "warp": 1, "cta": 2, "lane": 3}   # dcr_plan_opts.apply
+ENCODER_VARIANTS = {"auto": 0, "wide": 1, "deep": 2, "cta": 3}   # dcr_plan_opts.encoder
 
 
 def ncu_traffic(args, bytes_per_launch):
@@ -281,7 +282,7 @@ def run_config(args, wl, nw, ws):
         name += " [change rate set to %s]" % ("a fully random new buffer" if change_rate(args) == "random"
                                              else "%g%%" % (100 * args.frac))
     return {"workload": name, "change_rate": change_rate(args), "canonical_bytes": N, "codec": getattr(args, "codec", "lz4"),
-            "apply": getattr(args, "apply", "auto"),
+            "encoder": getattr(args, "encoder", "auto"), "apply": getattr(args, "apply", "auto"),
             "tp": wl.tp, "windows": nw, "parallelism": "replicas" if ws > 1 else "single GPU",
             "l2": "L2 flushed before each timed step (%d MiB written outside the step's events)" % (FLUSH_BYTES >> 20)
             if l2_resident(N) else "inputs larger than L2 (2N = %.2f GB read per encode)" % (2 * N / 1e9)}
@@ -343,7 +344,7 @@ def run_gpu(args):
     plan = dcr.Plan(descs_of(wl), window_bytes=(args.window_mb << 20) or wl.window_bytes,
                     codec=dcr.CODEC_SNAPPY if args.codec == "snappy" else dcr.CODEC_LZ4,
                     overflow_kib=dcr.NO_OVERFLOW if args.overflow_kib < 0 else args.overflow_kib,
-                    apply=APPLY_VARIANTS[args.apply])
+                    apply=APPLY_VARIANTS[args.apply], encoder=ENCODER_VARIANTS[args.encoder])
     plan.set_profiling(True)
     olds, news = wl.device_arenas(torch)
     target = torch.empty(max(plan.info.recv_bytes, wl.recv_bytes), dtype=torch.uint8, device=dev)
@@ -785,6 +786,9 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--window-mb", type=int, default=0, help="window size in MiB (0: the workload's)")
     ap.add_argument("--codec", default="lz4", choices=["lz4", "snappy"], help="block codec of the XOR masks")
+    ap.add_argument("--encoder", default="auto", choices=sorted(ENCODER_VARIANTS),
+                    help="encoder kernel: auto, wide (warp per chunk), deep (warp per chunk, 12 landing "
+                         "stages), cta (CTA per chunk)")
     ap.add_argument("--apply", default="auto", choices=sorted(APPLY_VARIANTS),
                     help="apply kernels: auto, warp (one warp per frame), cta (one CTA per frame), "
                          "lane (one thread per ZSRC frame)")
