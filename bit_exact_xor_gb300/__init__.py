@@ -29,6 +29,7 @@ ENCODER_AUTO, ENCODER_WIDE, ENCODER_DEEP, ENCODER_CTA = 0, 1, 2, 3
 APPLY_AUTO, APPLY_WARP, APPLY_CTA, APPLY_LANE = 0, 1, 2, 3
 CODEC_LZ4, CODEC_SNAPPY = 0, 1
 PLAN_HOST_ONLY = 1
+PLAN_TEST_STALL_SCAN = 2   # test only: the encoder's offset scan waits out its limit
 NO_OVERFLOW = 0xFFFFFFFF
 MAX_PARTS = 65536
 
@@ -192,10 +193,12 @@ def check(rc):
 class Plan:
     """dcr_plan_build over a list of TensorDesc."""
 
-    def __init__(self, descs, window_bytes=0, encoder=0, codec=0, host_only=False, apply=0, overflow_kib=0):
+    def __init__(self, descs, window_bytes=0, encoder=0, codec=0, host_only=False, apply=0, overflow_kib=0,
+                 flags=0):
         arr = (TensorDesc * len(descs))(*descs)
         self._names = [d.name for d in descs]
-        opts = PlanOpts(window_bytes, encoder, codec, PLAN_HOST_ONLY if host_only else 0, apply, overflow_kib)
+        flags |= PLAN_HOST_ONLY if host_only else 0
+        opts = PlanOpts(window_bytes, encoder, codec, flags, apply, overflow_kib)
         h = ctypes.c_void_p()
         check(lib().dcr_plan_build(arr, len(descs), ctypes.byref(opts), ctypes.byref(h)))
         self.h = h

@@ -208,6 +208,7 @@ struct dcr_plan {
     std::vector<uint64_t> chunk_start;   // canonical byte offset of each chunk in the model (+ total)
     std::vector<uint32_t> chunk_shards;  // per chunk: bit r set iff it reads trainer shard r
     bool host_only = false;              // built with DCR_PLAN_HOST_ONLY: no device state
+    bool stall_scan = false;             // DCR_PLAN_TEST_STALL_SCAN: scan tile 0 never publishes
     uint64_t window_bytes = 0;
     uint32_t encoder = DCR_ENCODER_AUTO;
     uint32_t codec = DCR_CODEC_LZ4;

@@ -20,10 +20,10 @@
 // encode_kernel.  One warp per chunk, chunks taken in ticket order, 24 warps
 // per SM.  The warp streams its chunk in 1 KiB steps: cp.async copies old
 // and new into a three-stage landing buffer in shared memory, so two steps
-// are in flight while one is processed.  (A second instantiation with twelve
-// stages and 2-warp CTAs serves windows with fewer chunks than warp slots.)  It XORs and counts, and appends the
-// positions and values of the non-zero mask bytes ("events") to a ring in
-// shared memory.  Every 32 events it runs one parse group (one event per
+// are in flight while one is processed.  (A second instantiation with
+// twelve stages and 2-warp CTAs serves windows with fewer chunks than warp
+// slots.)  It XORs and counts, and appends the positions and values of the
+// non-zero mask bytes ("events") to a ring in shared memory.  Every 32 events it runs one parse group (one event per
 // lane, connected by ballots and warp sums) that writes the LZ4 sequences
 // straight into the chunk's frame slot in device scratch.  Overwrite chunks
 // write their records there instead.  A chunk whose body or pending literals
@@ -31,9 +31,11 @@
 // without writing) and is listed for the restream pass.  No warp waits for
 // another: frame sizes go to a per-chunk array.
 //
-// scan_kernel / copy_kernel.  One CTA scans the frame sizes into offsets
-// and writes the stream header; then one warp per chunk copies its slot to
-// its place in the stream with 16-byte stores and writes its index entry.
+// scan_kernel / copy_kernel.  One CTA per tile of 8192 chunks scans the
+// tile's frame sizes into offsets, taking the tile's start from the tiles
+// before it (a decoupled look-back), and the last tile writes the stream
+// header; then one warp per chunk copies its slot to its place in the
+// stream with 16-byte stores and writes its index entry.
 //
 // restream_kernel.  One warp per chunk whose body outgrew its slot (masks
 // above a few percent change): it runs the chunk's stream loop again, now
@@ -123,6 +125,7 @@ struct EncArgs {
     SpillRec* spill;
     uint32_t* deep;            // spill records left to spill_kernel
     uint8_t* slots;            // kEncSlot bytes per chunk
+    uint32_t stall;            // test only: scan tile 0 never publishes its total
 };
 
 // encode_kernel: one warp's shared memory with NS landing stages
@@ -1129,9 +1132,18 @@ __global__ void __launch_bounds__(kMThreads, 4) restream_kernel(EncArgs A)
 // tile of kScanTile chunks, tiles taken in ticket order; a tile's offset
 // comes from a decoupled look-back over the status words of the tiles
 // before it (each already taken by a running CTA, since tickets go in
-// order, so every wait ends; a wait that still runs past its limit reports
-// DCR_ERR_TIMEOUT).  The CTA of the last tile writes the totals and header.
-constexpr uint32_t kScanSpin = 1u << 22;
+// order, so every wait ends; a wait that still runs past its limit, one
+// second on the global timer or kScanSpin polls, reports DCR_ERR_TIMEOUT).
+// The CTA of the last tile writes the totals and header.
+constexpr uint32_t kScanSpin = 1u << 24;
+constexpr uint64_t kScanWaitNs = 1000000000ull;
+
+__device__ __forceinline__ uint64_t global_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
 
 __device__ __forceinline__ uint64_t ld_acquire64(const uint64_t* p)
 {
@@ -1189,13 +1201,15 @@ __global__ void __launch_bounds__(1024) scan_kernel(EncArgs A, uint64_t* tiles, 
             int ok = 1;
             unsigned long long excl = 0;
             if (tile == 0) {
-                atomicExch(reinterpret_cast<unsigned long long*>(&tiles[0]), kTileInc | agg);
+                if (!A.stall) atomicExch(reinterpret_cast<unsigned long long*>(&tiles[0]), kTileInc | agg);
             } else {
                 atomicExch(reinterpret_cast<unsigned long long*>(&tiles[tile]), kTileAgg | agg);
+                const uint64_t t0 = global_ns();
                 for (int64_t j = int64_t(tile) - 1; j >= 0 && ok; --j) {
                     uint64_t s = ld_acquire64(&tiles[j]);
                     for (uint32_t spin = 0; !(s >> 62) && ok; ++spin) {
-                        if (spin > kScanSpin || *(volatile int32_t*)&A.sc->err) ok = 0;
+                        if (spin > kScanSpin || global_ns() - t0 > kScanWaitNs || *(volatile int32_t*)&A.sc->err)
+                            ok = 0;
                         else {
                             __nanosleep(64);
                             s = ld_acquire64(&tiles[j]);
@@ -1429,7 +1443,9 @@ __global__ void __launch_bounds__(kSThreads, 2) spill_kernel(EncArgs A)
     Buf& B = *reinterpret_cast<Buf*>(smem_raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t n_deep = A.sc->n_deep;     // final: written by restream_kernel only
-    if (A.sc->total > A.cap) return;          // final: written by scan_kernel
+    // total: final, written by scan_kernel; after a scan that gave up, the
+    // offsets of the tiles after the stalled one were never written
+    if (A.sc->total > A.cap || *(volatile int32_t*)&A.sc->err) return;
     for (uint32_t i = blockIdx.x; i < n_deep; i += gridDim.x) {
         const SpillRec R = A.spill[A.deep[i]];
         const ChunkDesc cd = A.chunks[A.chunk_begin + R.k];
@@ -2332,6 +2348,7 @@ EncArgs make_args(const dcr_plan* P, uint32_t mode, uint64_t chunk_begin, uint64
     A.heap = P->d_heap;
     A.heap_cap = P->heap_bytes;
     A.heapoff = P->d_heapoff;
+    A.stall = P->stall_scan ? 1u : 0u;
     return A;
 }
 

@@ -231,11 +231,13 @@ extern "C" int dcr_plan_build(const dcr_tensor_desc* tensors, size_t n, const dc
     const uint32_t apply = opts ? opts->apply : uint32_t(DCR_APPLY_AUTO);
     const uint32_t overflow_kib = opts ? opts->overflow_kib : 0u;
     if (apply > DCR_APPLY_LANE) return set_error(DCR_ERR_INVALID, "unknown apply variant %u", apply);
-    if (flags & ~uint32_t(DCR_PLAN_HOST_ONLY)) return set_error(DCR_ERR_INVALID, "unknown plan flags %#x", flags);
+    if (flags & ~uint32_t(DCR_PLAN_HOST_ONLY | DCR_PLAN_TEST_STALL_SCAN))
+        return set_error(DCR_ERR_INVALID, "unknown plan flags %#x", flags);
     dcr_plan* P = new (std::nothrow) dcr_plan();
     if (!P) return set_error(DCR_ERR_NOMEM, "dcr_plan_build: out of host memory");
     P->window_bytes = W;
     P->host_only = (flags & DCR_PLAN_HOST_ONLY) != 0;
+    P->stall_scan = (flags & DCR_PLAN_TEST_STALL_SCAN) != 0;
     P->encoder = encoder;
     P->codec = codec;
     P->apply = apply;

@@ -150,6 +150,13 @@ typedef struct {
  * dcr_stream_header, e.g. on a rank or process without a GPU); every call
  * that runs kernels returns DCR_ERR_INVALID for it. */
 #define DCR_PLAN_HOST_ONLY 1u
+/* Test only: the encoder's offset scan (one CTA per tile of 8192 chunks,
+ * each waiting, with a bounded wait, for the running totals of the tiles
+ * before it) runs with tile 0 never publishing its total, so in a window of
+ * more than 8192 chunks every later tile's wait runs out: dcr_encode,
+ * dcr_encode_part and dcr_encode_retry return DCR_ERR_TIMEOUT after about a
+ * second and write no stream byte.  A window of one tile is unaffected. */
+#define DCR_PLAN_TEST_STALL_SCAN 2u
 #define DCR_NO_OVERFLOW 0xFFFFFFFFu
 
 typedef struct {
@@ -158,7 +165,7 @@ typedef struct {
                                 chunk boundaries.  At most 256 GiB. */
     uint32_t encoder;        /* DCR_ENCODER_AUTO (0), _WIDE, _DEEP or _CTA */
     uint32_t codec;          /* DCR_CODEC_LZ4 (0) or DCR_CODEC_SNAPPY */
-    uint32_t flags;          /* 0 or DCR_PLAN_HOST_ONLY */
+    uint32_t flags;          /* 0, DCR_PLAN_HOST_ONLY, DCR_PLAN_TEST_STALL_SCAN */
     uint32_t apply;          /* DCR_APPLY_AUTO (0), _WARP, _CTA or _LANE */
     uint32_t overflow_kib;    /* device heap for XOR blocks that outgrow their
                                 6 KiB frame slot (masks of a few percent

@@ -116,6 +116,6 @@ def test_plan_rejects_unknown_encoder_variant():
     opts = dcr.PlanOpts(0, 0, 0, 0, dcr.APPLY_LANE + 1)
     rc = dcr.lib().dcr_plan_build(arr, 1, ctypes.byref(opts), ctypes.byref(h))
     assert rc == dcr.ERR_INVALID and "apply" in dcr.last_error() and h.value is None
-    opts = dcr.PlanOpts(0, 0, 0, 2)   # unknown plan flag
+    opts = dcr.PlanOpts(0, 0, 0, 4)   # unknown plan flag
     rc = dcr.lib().dcr_plan_build(arr, 1, ctypes.byref(opts), ctypes.byref(h))
     assert rc == dcr.ERR_INVALID and "flags" in dcr.last_error() and h.value is None
