@@ -38,7 +38,9 @@
 //                 Snappy frame: the same walk (Snappy elements in place of
 //                 LZ4 sequences) with the body read from global memory and
 //                 the matches checked against a bitmap of the non-zero
-//                 output bytes.
+//                 output bytes.  On plans of the Snappy codec, bodies up to
+//                 8 KiB take the split walk instead: the lanes walk 32
+//                 stretches of the body at once and join them (split_apply).
 //   defer_kernel  one CTA per general LZ4 frame (any valid block, e.g. from
 //                 the CPU oracle) or Snappy frame: full decode into a 64 KiB shared buffer
 //                 with warp-parallel literal and match copies (a ZSRC frame
@@ -121,14 +123,43 @@ struct __align__(16) AWarp {
 // output bytes, which has no capacity limit.
 struct __align__(16) BWarp {
     static constexpr uint32_t kWin = kWinB;   // denser masks: ~32 sequences per window
+    static constexpr bool kSplit = false;
+    static constexpr int kWarps = 8;
     uint32_t bits[kChunk / 32];
     uint32_t nxt[kWin];
     uint32_t r_ip[32];
     uint8_t jmp[3][kWin];
     uint32_t base[8];
 };
-constexpr int kBWarps = 8;
-constexpr int kBThreads = 32 * kBWarps;
+
+// big_kernel on plans of the Snappy codec: bodies up to kSBody bytes are
+// copied to shared memory and taken by the split walk (split_apply), which
+// also keeps a bitmap of the element starts its lanes pass and the joins of
+// the lanes' stretches; larger ones take the windowed walk.
+constexpr uint32_t kSBody = 6144;
+constexpr uint32_t kSChains = 4;   // walks per stretch, from its first four bytes
+constexpr uint8_t kNoWalk = 0xFF;
+struct __align__(16) SWarp {
+    static constexpr uint32_t kWin = kWinB;
+    static constexpr bool kSplit = true;
+    static constexpr int kWarps = 5;
+    union {
+        uint32_t bits[kChunk / 32];            // the non-zero output bytes (both walks)
+        uint8_t walker[kSBody];                // split walk, until the joins: per body byte, which walk of
+                                               // its stretch passed an element start there (kNoWalk: none)
+    };
+    union {
+        uint8_t body[kSBody + 16];             // split walk: the frame body (Walk::elem reads a byte past an element)
+        struct {                               // windowed walk
+            uint32_t nxt[kWin];
+            uint32_t r_ip[32];
+            uint8_t jmp[3][kWin];
+            uint32_t base[8];
+        };
+    };
+    uint32_t ex[32 * kSChains];                // split walk: where each walk leaves its stretch
+    uint32_t T[33];                            // ... and the joins
+};
 
 struct __align__(16) ASmem {
     AWarp w[kAWarps];
@@ -405,6 +436,38 @@ struct Lz4Walk {
     {
         zsrc_undo(A, cd, ds, src, lim, runs, lane);
     }
+    // one sequence at p whose bounds end() has checked: its fields and where
+    // the next starts (| kEndFinal after the block's last)
+    __device__ static uint32_t elem(const uint8_t* src, uint32_t n, uint32_t p, uint32_t& ipl, uint32_t& ll,
+                                    uint32_t& off, uint32_t& ml)
+    {
+        const uint32_t tok = src[p];
+        uint32_t q = p + 1;
+        ll = tok >> 4;
+        if (ll == 15) {
+            uint32_t b;
+            do {
+                b = src[q++];
+                ll += b;
+            } while (b == 255);
+        }
+        ipl = q;
+        q += ll;
+        off = ml = 0;
+        if (q == n) return q | kEndFinal;
+        off = uint32_t(src[q]) | (uint32_t(src[q + 1]) << 8);
+        q += 2;
+        ml = tok & 15u;
+        if (ml == 15) {
+            uint32_t b;
+            do {
+                b = src[q++];
+                ml += b;
+            } while (b == 255);
+        }
+        ml += 4;
+        return q;
+    }
 };
 
 // Snappy (the same section, footnote 4): a varint of the output length, then
@@ -425,28 +488,28 @@ struct SnappyWalk {
         }
         return kEndBad;
     }
+    // end() of a literal with 1..4 length bytes
+    __device__ static __noinline__ uint32_t end_long(const uint8_t* src, uint32_t n, uint32_t p)
+    {
+        const uint32_t nb = (src[p] >> 2) - 59;
+        if (uint64_t(p) + 1 + nb > n) return kEndBad;
+        uint64_t len = 0;
+        for (uint32_t i = 0; i < nb; ++i) len |= uint64_t(src[p + 1 + i]) << (8 * i);
+        const uint64_t e = uint64_t(p) + 1 + nb + len + 1;
+        if (e > n) return kEndBad;
+        return e == n ? uint32_t(e) | kEndFinal : uint32_t(e);
+    }
     template <bool>
     __device__ static uint32_t end(const uint8_t* src, uint32_t n, uint32_t p)
     {
         if (p >= n) return kEndBad;
         const uint32_t tag = src[p], t = tag & 3u;
-        uint64_t e;
-        if (t == 0) {
-            uint64_t len = (tag >> 2) + 1;
-            uint32_t nb = 0;
-            if ((tag >> 2) >= 60) {
-                nb = (tag >> 2) - 59;
-                if (uint64_t(p) + 1 + nb > n) return kEndBad;
-                len = 0;
-                for (uint32_t i = 0; i < nb; ++i) len |= uint64_t(src[p + 1 + i]) << (8 * i);
-                len += 1;
-            }
-            e = uint64_t(p) + 1 + nb + len;
-        } else {
-            e = uint64_t(p) + (t == 1 ? 2u : t == 2 ? 3u : 5u);
+        if (t != 0 || tag < 240u) {   // a copy (2, 3 or 5 bytes) or a literal of up to 60 bytes
+            const uint32_t e = p + (t ? (0x5320u >> (4 * t)) & 15u : 2u + (tag >> 2));
+            if (e > n) return kEndBad;
+            return e == n ? e | kEndFinal : e;
         }
-        if (e > n) return kEndBad;
-        return e == n ? uint32_t(e) | kEndFinal : uint32_t(e);
+        return end_long(src, n, p);
     }
     __device__ static void decode(const uint8_t* src, uint32_t q, bool, uint32_t& ipl, uint32_t& ll, uint32_t& off,
                                   uint32_t& ml)
@@ -475,6 +538,37 @@ struct SnappyWalk {
                 for (uint32_t i = 0; i < (t == 2 ? 2u : 4u); ++i) off |= uint32_t(src[q + 1 + i]) << (8 * i);
             }
         }
+    }
+    // one element at p whose bounds end() has checked: its fields and where
+    // the next starts (| kEndFinal after the block's last)
+    __device__ static uint32_t elem(const uint8_t* src, uint32_t n, uint32_t p, uint32_t& ipl, uint32_t& ll,
+                                    uint32_t& off, uint32_t& ml)
+    {
+        const uint32_t tag = src[p], t = tag & 3u;
+        uint32_t q;
+        if (t == 0 && tag >= 240u) {   // a literal with 1..4 length bytes
+            const uint32_t nb = (tag >> 2) - 59;
+            uint32_t len = 0;
+            for (uint32_t i = 0; i < nb; ++i) len |= uint32_t(src[p + 1 + i]) << (8 * i);
+            ipl = p + 1 + nb;
+            ll = len + 1;
+            off = ml = 0;
+            q = ipl + ll;
+        } else {
+            // the other shapes without branches; the element holds at least
+            // two bytes, and for copies of one offset byte the second one
+            // read belongs to the next element or to the buffer's padding
+            // (unused)
+            const uint32_t b1 = src[p + 1], b2 = src[p + 2];
+            const bool lit = t == 0;
+            ipl = p + (lit ? 1u : 0u);
+            ll = lit ? (tag >> 2) + 1 : 0u;
+            ml = lit ? 0u : t == 1 ? ((tag >> 2) & 7u) + 4 : (tag >> 2) + 1;
+            off = lit ? 0u : t == 1 ? ((tag >> 5) << 8) | b1 : b1 | (b2 << 8);
+            q = lit ? p + 1 + ll : p + ((0x5320u >> (4 * t)) & 15u);
+            if (t == 3) off |= (uint32_t(src[p + 3]) << 16) | (uint32_t(src[p + 4]) << 24);
+        }
+        return q == n ? q | kEndFinal : q;
     }
     __device__ static void undo(const ApplyArgs& A, const ChunkDesc& cd, const Seg* ds, const uint8_t* src, uint32_t n,
                                 uint32_t raw, uint32_t lim, uint32_t runs, int lane)
@@ -714,6 +808,186 @@ __device__ int zsrc_apply(const ApplyArgs& A, const ChunkDesc& cd, const Seg* ds
     }
     if (status != 1 && runs) Walk::undo(A, cd, ds, src, n, raw, lim, runs, lane);
     return status;
+}
+
+// The split walk.  A chain of elements (LZ4 sequences or Snappy elements) is
+// a function of where it starts: two walks that meet at one start go on
+// together.  So the body after the block's preamble is cut into 32 stretches
+// of equal length, one per lane, and every lane walks its stretch at once
+// from each of its first four bytes as though an element started there
+// (a walk that meets one of the lane's earlier walks stops, as it would go
+// on the same way), marking the starts it passes and which walk passed them;
+// lane 0's first walk starts at the block's first element and is the true
+// one.  Four walks, since in the runs of equal short elements the library's
+// encoder writes a walk that starts inside an element can stay out of step
+// with the true chain.  Lane 0 then joins the stretches in order: the true
+// chain enters stretch i where the walk of stretch i - 1 leaves it, and from
+// the first start there that lane i marked it is that walk of lane i's, so
+// only the elements before that join are walked again.  Every element of the
+// chain has passed the bounds checks of Walk::end once this is done, and a
+// chain that does not end with the block's last element exactly at the end
+// of the body is rejected before anything is written.  Each lane then takes
+// the true elements that start in its stretch: it sums their output lengths
+// (a warp prefix sum gives its first output position; the sum must be the
+// chunk's length), XORs their non-zero literal bytes into the receiver while
+// marking them in a bitmap of the chunk, and, once every lane has marked its
+// literals, checks that each match or copy reads only unmarked bytes below
+// its own position: all other output bytes are copies of zeros.  A frame that
+// breaks that promise is undone by XORing the same literal bytes again.
+// src is the body in shared memory (n <= kSBody); 1 if the frame was applied,
+// 0 if it is malformed or lying (nothing of it left applied).
+template <class Walk, class WS>
+__device__ int split_apply(const ApplyArgs& A, const ChunkDesc& cd, const Seg* ds, const uint8_t* src, uint32_t n,
+                           uint32_t raw, uint32_t lim, WS& W, int lane)
+{
+    if (n == 0) return 0;
+    const uint32_t ip0 = Walk::first(src, n, raw);
+    if (ip0 >= n) return 0;   // kEndBad too; a block holds at least one element
+    const uint32_t span = n - ip0, S = (span + 31) / 32;
+    auto edge = [&](uint32_t i) { return ip0 + (i * S < span ? i * S : span); };   // stretch i is [edge(i), edge(i + 1))
+    const uint32_t s0 = edge(lane), s1 = edge(lane + 1);
+    auto bad_end = [&](uint32_t x) { return x == kEndBad || (!(x & kEndFinal) && x >= n); };
+    for (uint32_t v = lane; v < (n + 15) / 16; v += 32)
+        reinterpret_cast<uint4*>(W.walker)[v] = make_uint4(~0u, ~0u, ~0u, ~0u);
+    __syncwarp();
+    // 1. the lane's walks of its stretch; a walk's exit is the first start at
+    //    or past the stretch's end, the block's end | kEndFinal, or kEndBad
+    //    (one element per round, the lane's walks one after another)
+    {
+        uint32_t c = 0, p = s0;
+        while (c < kSChains) {
+            uint32_t ex = 0;
+            bool done = true;
+            const uint32_t by = p < s1 ? W.walker[p] : kNoWalk;
+            if (p >= s1) {
+                ex = s1;   // a stretch shorter than its walks
+            } else if (by != kNoWalk) {   // an earlier walk of this lane passed p: the same from here
+                ex = W.ex[kSChains * lane + by];
+            } else {
+                W.walker[p] = uint8_t(c);
+                const uint32_t x = Walk::template end<false>(src, n, p);
+                if (bad_end(x)) ex = kEndBad;
+                else if ((x & kEndFinal) || x >= s1) ex = x;
+                else {
+                    p = x;
+                    done = false;
+                }
+            }
+            if (done) {
+                W.ex[kSChains * lane + c] = ex;
+                ++c;
+                p = s0 + c;
+            }
+        }
+    }
+    __syncwarp();
+    // 2. the joins: T[i] is the first true start at or past edge(i) (or the
+    //    chain's end), T[32] the chain's end
+    if (lane == 0) {
+        uint32_t t = W.ex[0];
+        W.T[0] = ip0;
+        for (uint32_t i = 1; i < 32; ++i) {
+            W.T[i] = t;
+            const uint32_t b = edge(i + 1);
+            if (t == kEndBad || (t & kEndFinal) || t >= b) continue;
+            for (uint32_t q = t;;) {
+                const uint32_t by = W.walker[q];
+                if (by != kNoWalk) {   // joined one of lane i's walks
+                    t = W.ex[kSChains * i + by];
+                    break;
+                }
+                const uint32_t x = Walk::template end<false>(src, n, q);
+                if (bad_end(x)) {
+                    t = kEndBad;
+                    break;
+                }
+                if ((x & kEndFinal) || x >= b) {
+                    t = x;
+                    break;
+                }
+                q = x;
+            }
+        }
+        W.T[32] = t;
+    }
+    __syncwarp();
+    if (W.T[32] != (n | kEndFinal)) return 0;
+    // this lane's true elements: those that start in [T[lane], s1), each
+    // bounds-checked by Walk::end in step 1 or 2
+    const uint32_t t0 = W.T[lane];
+    auto walk = [&](auto&& fn) {
+        if (t0 & kEndFinal) return;   // (kEndBad cannot occur past a good chain)
+        for (uint32_t p = t0; p < s1;) {
+            uint32_t ipl, ll, off, ml;
+            const uint32_t x = Walk::elem(src, n, p, ipl, ll, off, ml);
+            fn(ipl, ll, off, ml);
+            if (x & kEndFinal) break;
+            p = x;
+        }
+    };
+    // 3. output positions
+    uint32_t len = 0;
+    walk([&](uint32_t, uint32_t ll, uint32_t, uint32_t ml) { len += ll + ml; });
+    const uint32_t incl = warp_incl_sum(len, lane);
+    if (__shfl_sync(kFull, incl, 31) != raw) return 0;
+    const uint32_t op0 = incl - len;
+    // 4. literals: XOR the non-zero bytes into the receiver (mark: and into
+    //    the bitmap); every output position is below raw
+    for (uint32_t v = lane; v < (raw + 127) / 128; v += 32) reinterpret_cast<uint4*>(W.bits)[v] = make_uint4(0u, 0u, 0u, 0u);
+    __syncwarp();
+    const bool one = cd.dst_count == 1;
+    const uint64_t base = one ? ds[0].addr - ds[0].off : 0ull;
+    auto literals = [&](bool mark) {
+        uint32_t op = op0;
+        walk([&](uint32_t ipl, uint32_t ll, uint32_t, uint32_t ml) {
+            for (uint32_t q = 0; q < ll; ++q) {
+                const uint32_t b = src[ipl + q];
+                if (b) {
+                    const uint32_t x = op + q;
+                    if (mark) atomicOr(&W.bits[x >> 5], 1u << (x & 31));
+                    if (x < lim) xor_byte(A.target, one ? base + x : dst_of(ds, cd.dst_count, x), b);
+                }
+            }
+            op += ll + ml;
+        });
+    };
+    literals(true);
+    __syncwarp();
+    // 5. every match or copy reads [mop - off, mop - off + min(ml, off)),
+    //    repeated: no marked byte may fall there
+    bool viol = false;
+    {
+        uint32_t op = op0;
+        const uint32_t nw = (raw + 31) / 32;
+        walk([&](uint32_t, uint32_t ll, uint32_t off, uint32_t ml) {
+            const uint32_t mop = op + ll;
+            op = mop + ml;
+            // literal runs (ml = 0) check nothing: L = 0
+            const bool good = off != 0 && off <= mop;
+            viol |= ml != 0 && !good;
+            const uint32_t a0 = good ? mop - off : 0u, L = ml == 0 || !good ? 0u : ml < off ? ml : off;
+            if (L <= 64) {   // the 64 bits from a0 on, from three words (past the chunk: none)
+                const uint32_t w = a0 >> 5, sh = a0 & 31;
+                const uint64_t lo = uint64_t(W.bits[w]) | (w + 1 < nw ? uint64_t(W.bits[w + 1]) << 32 : 0ull);
+                uint64_t v = lo >> sh;
+                if (sh && w + 2 < nw) v |= uint64_t(W.bits[w + 2]) << (64 - sh);
+                viol |= (v & (L == 64 ? ~0ull : (1ull << L) - 1)) != 0;
+            } else {
+                const uint32_t e0 = a0 + L;
+                for (uint32_t w = a0 >> 5; w <= (e0 - 1) >> 5 && !viol; ++w) {
+                    const uint32_t a = (w << 5) > a0 ? 0u : a0 - (w << 5);
+                    const uint32_t b = ((w + 1) << 5) < e0 ? 32u : e0 - (w << 5);
+                    const uint32_t m = (b == 32 ? 0xFFFFFFFFu : ((1u << b) - 1)) & ~((1u << a) - 1);
+                    viol = (W.bits[w] & m) != 0;
+                }
+            }
+        });
+    }
+    if (__any_sync(kFull, viol)) {
+        literals(false);   // XOR is its own inverse
+        return 0;
+    }
+    return 1;
 }
 
 // ================================================================ kernels ==
@@ -1418,10 +1692,11 @@ __global__ void __launch_bounds__(kDThreads) defer_kernel(ApplyArgs A)
 // list holds): one warp per frame, body read from global memory, matches
 // checked against a bitmap of the non-zero output bytes.  The frames were
 // validated and claimed by apply_kernel.
-__global__ void __launch_bounds__(kBThreads, 3) big_kernel(ApplyArgs A)
+template <class WS>
+__global__ void __launch_bounds__(32 * WS::kWarps, 3) big_kernel(ApplyArgs A)
 {
     extern __shared__ __align__(16) unsigned char smem_raw[];
-    BWarp& W = reinterpret_cast<BWarp*>(smem_raw)[threadIdx.x >> 5];
+    WS& W = reinterpret_cast<WS*>(smem_raw)[threadIdx.x >> 5];
     const int lane = threadIdx.x & 31;
     if (!A.sc->hdr_ok) return;
     const uint8_t* p = A.payload;
@@ -1445,8 +1720,23 @@ __global__ void __launch_bounds__(kBThreads, 3) big_kernel(ApplyArgs A)
         uint32_t lim = cut ? (A.split < raw ? A.split : raw) : raw;
         lim -= lim % ub;
         const uint8_t* body = p + fo + kFrameHdr;
-        const int r = sn ? zsrc_apply<true, BWarp, SnappyWalk>(A, cd, A.dst + cd.dst_begin, body, bl, raw, lim, W, lane)
-                         : zsrc_apply<true, BWarp>(A, cd, A.dst + cd.dst_begin, body, bl, raw, lim, W, lane);
+        const Seg* ds = A.dst + cd.dst_begin;
+        int r = 0;
+        if (WS::kSplit && bl <= kSBody) {
+            if constexpr (WS::kSplit) {
+                // the body into shared memory: whole vectors, then the bytes after them
+                const uint32_t nv = bl / 16;
+                for (uint32_t v = lane; v < nv; v += 32)
+                    reinterpret_cast<uint4*>(W.body)[v] = ld_nc16(body + 16 * v);
+                for (uint32_t i = 16 * nv + lane; i < bl; i += 32) W.body[i] = body[i];
+                __syncwarp();
+                r = sn ? split_apply<SnappyWalk>(A, cd, ds, W.body, bl, raw, lim, W, lane)
+                       : split_apply<Lz4Walk>(A, cd, ds, W.body, bl, raw, lim, W, lane);
+            }
+        } else {
+            r = sn ? zsrc_apply<true, WS, SnappyWalk>(A, cd, ds, body, bl, raw, lim, W, lane)
+                   : zsrc_apply<true, WS>(A, cd, ds, body, bl, raw, lim, W, lane);
+        }
         __syncwarp();   // the bitmap is reused by the next frame
         if (lane == 0) {
             if (r != 1) {
@@ -1646,11 +1936,17 @@ int apply_kernel_config(KernelConfig* kc)
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&kc->defer_blocks_per_sm, defer_kernel, kDThreads,
                                                           kChunk);
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(big_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 int(sizeof(BWarp) * kBWarps));
+        e = cudaFuncSetAttribute(big_kernel<BWarp>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 int(sizeof(BWarp) * BWarp::kWarps));
     if (e == cudaSuccess)
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&kc->big_blocks_per_sm, big_kernel, kBThreads,
-                                                          sizeof(BWarp) * kBWarps);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&kc->big_blocks_per_sm, big_kernel<BWarp>,
+                                                          32 * BWarp::kWarps, sizeof(BWarp) * BWarp::kWarps);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(big_kernel<SWarp>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 int(sizeof(SWarp) * SWarp::kWarps));
+    if (e == cudaSuccess)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&kc->split_blocks_per_sm, big_kernel<SWarp>,
+                                                          32 * SWarp::kWarps, sizeof(SWarp) * SWarp::kWarps);
     if (e == cudaSuccess)   // no shared memory: all of it as L1 for the bodies
         e = cudaFuncSetAttribute(lane_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 0);
     if (e == cudaSuccess)
@@ -1671,6 +1967,7 @@ int apply_kernel_config(KernelConfig* kc)
     if (kc->apply_blocks_per_sm < 1) kc->apply_blocks_per_sm = 1;
     if (kc->apply_cta_blocks_per_sm < 1) kc->apply_cta_blocks_per_sm = 1;
     if (kc->big_blocks_per_sm < 1) kc->big_blocks_per_sm = 1;
+    if (kc->split_blocks_per_sm < 1) kc->split_blocks_per_sm = 1;
     if (kc->lane_blocks_per_sm < 1) kc->lane_blocks_per_sm = 1;
     if (kc->defer_blocks_per_sm < 1) kc->defer_blocks_per_sm = 1;
     return DCR_OK;
@@ -1755,7 +2052,10 @@ void launch_deferred(const dcr_plan* P, const ApplyArgs& A, cudaStream_t s)
 {
     const int sms = P->kc.num_sms;
     defer_kernel<<<sms * P->kc.defer_blocks_per_sm, kDThreads, kChunk, s>>>(A);
-    big_kernel<<<sms * P->kc.big_blocks_per_sm, kBThreads, sizeof(BWarp) * kBWarps, s>>>(A);
+    if (P->codec == DCR_CODEC_SNAPPY)
+        big_kernel<SWarp><<<sms * P->kc.split_blocks_per_sm, 32 * SWarp::kWarps, sizeof(SWarp) * SWarp::kWarps, s>>>(A);
+    else
+        big_kernel<BWarp><<<sms * P->kc.big_blocks_per_sm, 32 * BWarp::kWarps, sizeof(BWarp) * BWarp::kWarps, s>>>(A);
 }
 
 }  // namespace

@@ -144,6 +144,7 @@ struct KernelConfig {
     int apply_cta_blocks_per_sm = 0;
     int defer_blocks_per_sm = 0;
     int big_blocks_per_sm = 0;
+    int split_blocks_per_sm = 0;       // big_kernel with the split walk (Snappy plans)
     int lane_blocks_per_sm = 0;
 };
 

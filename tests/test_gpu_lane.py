@@ -1,13 +1,19 @@
-"""ZSRC frames applied one thread per frame (the LANE apply variant): hand-
-made LZ4 and Snappy blocks, checked byte for byte against the oracle's apply
-of the same stream.
+"""ZSRC frames through the walks that take large or Snappy frames: one
+thread per frame (the LANE apply variant), the split walk (big_kernel on
+plans of the Snappy codec) and the windowed walk (big_kernel on plans of the
+LZ4 codec).  Hand-made LZ4 and Snappy blocks are checked byte for byte
+against the oracle's apply of the same stream.
 
 The thread proves a match copies zeros only when its source lies after the
 last non-zero output byte or between the last two.  The blocks below also
 hold valid matches whose source lies in an older zero stretch (the walk must
 undo its XORs and hand the frame to the bitmap walk, which applies it), a
-match that copies a non-zero byte late in the block (rejected, the chunk
-left as it was), and truncated bodies."""
+match that copies a non-zero byte late in the block and one whose source
+starts before the chunk (rejected, the chunk left as it was), and truncated
+bodies.  Each block opens with 3200 random literal bytes, so the split
+walk's lanes start their stretches inside literal data and must be joined;
+random single-byte corruptions of the blocks check every walk against the
+oracle's verdict."""
 import numpy as np
 import pytest
 
@@ -93,6 +99,7 @@ def _rand_lit(rng, n):
 #   lying    source covers the 5: copies a non-zero byte
 #   recent   source between the 6 and the 7: provable
 #   plain    the zero literal after the 7 (offset 1): provable
+#   far      source starts 10 bytes before the chunk: malformed
 
 
 def lz4_case(kind, rng):
@@ -108,7 +115,8 @@ def lz4_case(kind, rng):
         seqs.append((b"\x07\x00", 1, 40))
         op += 2 + 40
     else:
-        back, ml = {"old_gap": (3386 - 3205, 40), "lying": (3386 - 3300, 40), "recent": (3386 - 3370, 10)}[kind]
+        back, ml = {"old_gap": (3386 - 3205, 40), "lying": (3386 - 3300, 40), "recent": (3386 - 3370, 10),
+                    "far": (3386 + 10, 40)}[kind]
         seqs.append((b"\x07", back, ml))
         op += 1 + ml
     seqs.append((b"\x00", 1, CHUNK - op - 1 - 5))
@@ -127,7 +135,8 @@ def snappy_case(kind, rng):
         el += [("lit", b"\x07\x00"), ("copy", 1, 40)]
         op += 2 + 40
     else:
-        back, ln = {"old_gap": (483 - 305, 40), "lying": (483 - 400, 40), "recent": (483 - 476, 4)}[kind]
+        back, ln = {"old_gap": (483 - 305, 40), "lying": (483 - 400, 40), "recent": (483 - 476, 4),
+                    "far": (483 + 10, 40)}[kind]
         el += [("lit", b"\x07"), ("copy", back, ln)]
         op += 1 + ln
     el += [("lit", b"\x00"), ("copy", 1, CHUNK - op - 1)]
@@ -143,60 +152,113 @@ def setup():
     assert orc.n_chunks == N_CHUNKS and all(orc.chunk_info(c)[3] == CHUNK for c in range(N_CHUNKS))
     rng = np.random.RandomState(5)
     old = rng.randint(0, 256, size=wl.shard_bytes[0]).astype(np.uint8)
-    plans = {c: dcr.Plan(descs_of(wl), apply=dcr.APPLY_LANE, codec=c) for c in (dcr.CODEC_LZ4, dcr.CODEC_SNAPPY)}
+    # walk -> (plan codec, apply variant) whose big_kernel (or lane_kernel) takes the frames
+    plans = {
+        "lane-lz4": dcr.Plan(descs_of(wl), apply=dcr.APPLY_LANE, codec=dcr.CODEC_LZ4),
+        "lane-snappy": dcr.Plan(descs_of(wl), apply=dcr.APPLY_LANE, codec=dcr.CODEC_SNAPPY),
+        "split": dcr.Plan(descs_of(wl), apply=dcr.APPLY_WARP, codec=dcr.CODEC_SNAPPY),
+        "window": dcr.Plan(descs_of(wl), apply=dcr.APPLY_WARP, codec=dcr.CODEC_LZ4),
+    }
     return wl, orc, old, plans
 
 
-def _run(setup, codec, kinds, truncate=None):
-    wl, orc, old, plans = setup
+WALKS = ["lane", "split", "window"]
+
+
+def _plan(plans, walk, codec):
+    return plans["%s-%s" % (walk, codec)] if walk == "lane" else plans[walk]
+
+
+def _blocks(codec, kinds):
     rng = np.random.RandomState(11)
-    frames = []
-    for c, kind in enumerate(kinds):
+    out = []
+    for kind in kinds:
         body = lz4_case(kind, rng) if codec == "lz4" else snappy_case(kind, rng)
         dec = oracle.lz4_decode if codec == "lz4" else oracle.snappy_decode
         m = dec(np.frombuffer(body, np.uint8), CHUNK)
-        assert m is not None and m.size == CHUNK                   # a well-formed block
-        zs = dec(np.frombuffer(body, np.uint8), CHUNK, zsrc=True)
-        assert (zs is None) == (kind == "lying")                   # every match copies zeros, but in "lying"
+        assert (m is None) == (kind == "far")                      # a well-formed block, but in "far"
+        if m is not None:
+            assert m.size == CHUNK
+            zs = dec(np.frombuffer(body, np.uint8), CHUNK, zsrc=True)
+            assert (zs is None) == (kind == "lying")               # every match copies zeros, but in "lying"
         if codec == "lz4":
             assert len(body) > 3072                                # above the warp kernel's body cache
-        if truncate is not None and c == truncate:
-            body = body[:-3]
-        frames.append((K_XOR_LZ4 if codec == "lz4" else K_XOR_SNAPPY, 8, FRAME_ZSRC, c, CHUNK,
-                       int(np.count_nonzero(m)), body))
+        out.append((body, 0 if m is None else int(np.count_nonzero(m))))
+    return out
+
+
+def _apply_both(setup, walk, codec, bodies):
+    wl, orc, old, plans = setup
+    frames = [(K_XOR_LZ4 if codec == "lz4" else K_XOR_SNAPPY, 8, FRAME_ZSRC, c, CHUNK, chg, body)
+              for c, (body, chg) in enumerate(bodies)]
     stream = np.frombuffer(build_stream(orc.plan_hash, 0, 0, N_CHUNKS, frames), np.uint8).copy()
     start = orc.receiver_dense([old])
     ref = start.copy()
     orc_rc = orc.apply(orc.state(0), stream, ref)
-    plan = plans[dcr.CODEC_LZ4 if codec == "lz4" else dcr.CODEC_SNAPPY]
+    plan = _plan(plans, walk, codec)
     t = to_device([start])[0]
     rc, _ = dcr.apply(plan, dcr.RecvState(plan, 0), torch.from_numpy(stream).cuda(), stream.size, t)
     got = t.cpu().numpy()[:start.size]
     return orc_rc, rc, got, ref, start
 
 
+def _run(setup, walk, codec, kinds, truncate=None):
+    bodies = _blocks(codec, kinds)
+    if truncate is not None:
+        bodies[truncate] = (bodies[truncate][0][:-3], bodies[truncate][1])
+    return _apply_both(setup, walk, codec, bodies)
+
+
+@pytest.mark.parametrize("walk", WALKS)
 @pytest.mark.parametrize("codec", ["lz4", "snappy"])
-def test_valid_frames_proven_or_handed_on(setup, codec):
-    orc_rc, rc, got, ref, start = _run(setup, codec, ["recent", "old_gap", "plain", "old_gap"])
+def test_valid_frames_proven_or_handed_on(setup, walk, codec):
+    orc_rc, rc, got, ref, start = _run(setup, walk, codec, ["recent", "old_gap", "plain", "old_gap"])
     assert orc_rc == oracle.OK and rc == dcr.OK
     assert np.array_equal(got, ref) and not np.array_equal(got, start)
 
 
+@pytest.mark.parametrize("walk", WALKS)
 @pytest.mark.parametrize("codec", ["lz4", "snappy"])
-def test_lying_frame_rejected_and_undone(setup, codec):
-    orc_rc, rc, got, ref, start = _run(setup, codec, ["recent", "lying", "old_gap", "plain"])
+@pytest.mark.parametrize("bad", ["lying", "far"])
+def test_lying_frame_rejected_and_undone(setup, walk, codec, bad):
+    orc_rc, rc, got, ref, start = _run(setup, walk, codec, ["recent", bad, "old_gap", "plain"])
     assert orc_rc == oracle.E_CORRUPT and rc == dcr.ERR_CORRUPT
-    # the other frames applied, the lying one's chunk exactly as it was
+    # the other frames applied, the rejected one's chunk exactly as it was
     assert np.array_equal(got[CHUNK:2 * CHUNK], start[CHUNK:2 * CHUNK])
     assert np.array_equal(got, ref)
 
 
+@pytest.mark.parametrize("walk", WALKS)
 @pytest.mark.parametrize("codec", ["lz4", "snappy"])
-def test_truncated_frame_rejected_and_undone(setup, codec):
-    orc_rc, rc, got, ref, start = _run(setup, codec, ["plain", "recent", "old_gap", "plain"], truncate=2)
+def test_truncated_frame_rejected_and_undone(setup, walk, codec):
+    orc_rc, rc, got, ref, start = _run(setup, walk, codec, ["plain", "recent", "old_gap", "plain"], truncate=2)
     assert orc_rc == oracle.E_CORRUPT and rc == dcr.ERR_CORRUPT
     assert np.array_equal(got[2 * CHUNK:3 * CHUNK], start[2 * CHUNK:3 * CHUNK])
     assert np.array_equal(got, ref)
+
+
+@pytest.mark.parametrize("walk", WALKS)
+@pytest.mark.parametrize("codec", ["lz4", "snappy"])
+def test_corrupted_bytes_follow_the_oracle(setup, walk, codec):
+    # one byte of one frame replaced, 48 times: whether the frame is still a
+    # valid ZSRC block (then applied) or not (then rejected, its chunk as it
+    # was) is the oracle's call; the receiver bytes must agree either way
+    base = _blocks(codec, ["recent", "old_gap", "plain", "old_gap"])
+    rng = np.random.RandomState(1000 + 10 * WALKS.index(walk) + (codec == "snappy"))
+    verdicts = set()
+    for _ in range(48):
+        bodies = list(base)
+        f = int(rng.randint(len(bodies)))
+        b = bytearray(bodies[f][0])
+        # half of the hits on the structure after the random literal prefix
+        i = int(rng.randint(len(b))) if rng.rand() < 0.5 else int(rng.randint(len(b) - 120, len(b)))
+        b[i] = (b[i] + int(rng.randint(1, 256))) % 256
+        bodies[f] = (bytes(b), bodies[f][1])
+        orc_rc, rc, got, ref, _ = _apply_both(setup, walk, codec, bodies)
+        assert (orc_rc == oracle.OK) == (rc == dcr.OK), (f, i, orc_rc, rc)
+        assert np.array_equal(got, ref), (f, i)
+        verdicts.add(rc)
+    assert verdicts == {dcr.OK, dcr.ERR_CORRUPT}
 
 
 @pytest.mark.parametrize("codec", ["lz4", "snappy"])
@@ -206,7 +268,7 @@ def test_retry_stream_from_hand_made_xor_stream(setup, codec):
     # same records; the retry stream then equals the oracle's overwrite-only
     # encode of (old, old ^ mask) byte for byte.  A lying frame is rejected.
     wl, orc, old, plans = setup
-    plan = plans[dcr.CODEC_LZ4 if codec == "lz4" else dcr.CODEC_SNAPPY]
+    plan = _plan(plans, "lane", codec)
     for kinds, ok in ((["recent", "old_gap", "plain", "old_gap"], True), (["recent", "lying", "plain", "plain"], False)):
         rng = np.random.RandomState(11)
         frames, new = [], old.copy()
