@@ -15,7 +15,7 @@ per refit) are larger than L2; workloads small enough to stay in L2 get a
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
                   [--workload moe|dense|single|gqa|sweep] [--frac F]
                   [--moe-layers L] [--window-mb M] [--codec lz4|snappy] [--overflow-kib K]
-                  [--encoder auto|wide|deep|cta] [--apply auto|warp|cta|lane]
+                  [--encoder auto|wide|deep|cta] [--apply auto|warp|cta|lane|split]
                   [--pipeline] [--abort-retry] [--shard] [--no-e2e] [--no-cpu-baseline]
 
 Prints one JSON line.  --impl reference times the CPU oracle (the
@@ -98,7 +98,7 @@ def measured_peak():
 
 
 PROFILED = {"dense": "encode_kernel_dense_tp2.md", "moe": "encode_kernel_nvfp4_moe.md"}
-APPLY_VARIANTS = {"auto": 0, "warp": 1, "cta": 2, "lane": 3}   # dcr_plan_opts.apply
+APPLY_VARIANTS = {"auto": 0, "warp": 1, "cta": 2, "lane": 3, "split": 4}   # dcr_plan_opts.apply
 ENCODER_VARIANTS = {"auto": 0, "wide": 1, "deep": 2, "cta": 3}   # dcr_plan_opts.encoder
 
 

@@ -26,7 +26,7 @@ REPLICATED, SPLIT_ROWS, SPLIT_COLS, RESIDUAL_QKV_INTERLEAVED = 0, 1, 2, 3
 LAYOUT_CANONICAL, LAYOUT_ROWGROUP_INTERLEAVE = 0, 1
 MODE_HYBRID, MODE_OVERWRITE_ONLY = 0, 1
 ENCODER_AUTO, ENCODER_WIDE, ENCODER_DEEP, ENCODER_CTA = 0, 1, 2, 3
-APPLY_AUTO, APPLY_WARP, APPLY_CTA, APPLY_LANE = 0, 1, 2, 3
+APPLY_AUTO, APPLY_WARP, APPLY_CTA, APPLY_LANE, APPLY_SPLIT = 0, 1, 2, 3, 4
 CODEC_LZ4, CODEC_SNAPPY = 0, 1
 PLAN_HOST_ONLY = 1
 PLAN_TEST_STALL_SCAN = 2   # test only: the encoder's offset scan waits out its limit

@@ -88,6 +88,7 @@ struct ApplyArgs {
     uint32_t defer_len;
     uint64_t lane_min;        // frames in a stream from which lane_kernel takes its ZSRC frames
     int self_route;           // apply_kernel routes every frame itself (no route_kernel, no lane_kernel)
+    int split_all;            // every ZSRC frame to big_kernel's split walk (DCR_APPLY_SPLIT)
     uint64_t plan_hash;
     uint64_t version;
     uint64_t abort_at;
@@ -1035,6 +1036,7 @@ __device__ __forceinline__ int frame_route(const ApplyArgs& A, const Hdr& H, uin
     }
     const bool zs = (fflags & kFrameZsrc) != 0;
     if (kind != kXorRaw && !zs) return kRDefer;
+    if (kind != kXorRaw && A.split_all) return kRBig;
     if (kind != kXorRaw && H.n_frames >= A.lane_min) return kRLane;
     if (kind == kXorSnappy || (kind == kXorLz4 && bl > uint32_t(kBodyCache))) return kRBig;
     return kRWarp;
@@ -2015,7 +2017,7 @@ uint64_t lane_min_frames(const dcr_plan* P)
     if (P->apply == DCR_APPLY_LANE) return 0;
     const uint64_t t = uint64_t(P->kc.num_sms) * P->kc.lane_blocks_per_sm * kLThreads / 4;
     // launch_first leaves lane_kernel out for plans whose windows are smaller
-    return P->apply == DCR_APPLY_WARP || P->max_window_chunks < t ? UINT64_MAX : t;
+    return P->apply == DCR_APPLY_WARP || P->apply == DCR_APPLY_SPLIT || P->max_window_chunks < t ? UINT64_MAX : t;
 }
 
 ApplyArgs make_args(const dcr_plan* P, dcr_recv_state* st, const void* payload, size_t size, void* target,
@@ -2037,6 +2039,7 @@ ApplyArgs make_args(const dcr_plan* P, dcr_recv_state* st, const void* payload, 
     A.warp = st->d_defer + 2 * (P->max_window_chunks + 1);
     A.lane_min = lane_min_frames(P);
     A.self_route = A.lane_min == UINT64_MAX;
+    A.split_all = P->apply == DCR_APPLY_SPLIT;
     A.defer_len = uint32_t(P->max_window_chunks + 1);
     A.plan_hash = P->hash;
     A.version = st->version;
@@ -2052,7 +2055,7 @@ void launch_deferred(const dcr_plan* P, const ApplyArgs& A, cudaStream_t s)
 {
     const int sms = P->kc.num_sms;
     defer_kernel<<<sms * P->kc.defer_blocks_per_sm, kDThreads, kChunk, s>>>(A);
-    if (P->codec == DCR_CODEC_SNAPPY)
+    if (P->codec == DCR_CODEC_SNAPPY || P->apply == DCR_APPLY_SPLIT)
         big_kernel<SWarp><<<sms * P->kc.split_blocks_per_sm, 32 * SWarp::kWarps, sizeof(SWarp) * SWarp::kWarps, s>>>(A);
     else
         big_kernel<BWarp><<<sms * P->kc.big_blocks_per_sm, 32 * BWarp::kWarps, sizeof(BWarp) * BWarp::kWarps, s>>>(A);
@@ -2218,6 +2221,7 @@ int apply_launch_noalloc(const dcr_plan* P, dcr_recv_state* st, const void* payl
     A.warp = A.defer + 2 * A.defer_len;
     A.lane_min = lane_min_frames(P);
     A.self_route = A.lane_min == UINT64_MAX;
+    A.split_all = P->apply == DCR_APPLY_SPLIT;
     A.plan_hash = P->hash;
     A.version = st->version;
     A.abort_at = DCR_NO_FAULT;

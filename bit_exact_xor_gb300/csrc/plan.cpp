@@ -230,7 +230,7 @@ extern "C" int dcr_plan_build(const dcr_tensor_desc* tensors, size_t n, const dc
     const uint32_t flags = opts ? opts->flags : 0u;
     const uint32_t apply = opts ? opts->apply : uint32_t(DCR_APPLY_AUTO);
     const uint32_t overflow_kib = opts ? opts->overflow_kib : 0u;
-    if (apply > DCR_APPLY_LANE) return set_error(DCR_ERR_INVALID, "unknown apply variant %u", apply);
+    if (apply > DCR_APPLY_SPLIT) return set_error(DCR_ERR_INVALID, "unknown apply variant %u", apply);
     if (flags & ~uint32_t(DCR_PLAN_HOST_ONLY | DCR_PLAN_TEST_STALL_SCAN))
         return set_error(DCR_ERR_INVALID, "unknown plan flags %#x", flags);
     dcr_plan* P = new (std::nothrow) dcr_plan();

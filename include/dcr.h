@@ -111,8 +111,13 @@ enum { DCR_ENCODER_AUTO = 0, DCR_ENCODER_WIDE = 1, DCR_ENCODER_DEEP = 2, DCR_ENC
  * that writes only the non-zero literal bytes: a tenth of the instructions,
  * so the fastest once a stream has tens of thousands of frames).  AUTO picks
  * CTA for plans with small windows, else WARP, and LANE for the streams with
- * about four frames or more per warp slot of the bitmap walk. */
-enum { DCR_APPLY_AUTO = 0, DCR_APPLY_WARP = 1, DCR_APPLY_CTA = 2, DCR_APPLY_LANE = 3 };
+ * about four frames or more per warp slot of the bitmap walk.  SPLIT: one
+ * warp per raw and overwrite frame, and one warp per ZSRC LZ4 or Snappy
+ * frame whose lanes walk 32 stretches of the body at once and join them
+ * (bodies up to 6 KiB; the windowed walk above that).  Plans of the Snappy
+ * codec take that walk for their ZSRC Snappy frames in every variant but
+ * LANE and CTA. */
+enum { DCR_APPLY_AUTO = 0, DCR_APPLY_WARP = 1, DCR_APPLY_CTA = 2, DCR_APPLY_LANE = 3, DCR_APPLY_SPLIT = 4 };
 /* Block codec of XOR masks (dcr_plan_opts.codec).  LZ4 (frame kind 1) is the
  * default; Snappy (frame kind 5) is the other byte-oriented LZ77 codec the
  * method's pages compare it with (blog, "A strong baseline with the
@@ -166,7 +171,7 @@ typedef struct {
     uint32_t encoder;        /* DCR_ENCODER_AUTO (0), _WIDE, _DEEP or _CTA */
     uint32_t codec;          /* DCR_CODEC_LZ4 (0) or DCR_CODEC_SNAPPY */
     uint32_t flags;          /* 0, DCR_PLAN_HOST_ONLY, DCR_PLAN_TEST_STALL_SCAN */
-    uint32_t apply;          /* DCR_APPLY_AUTO (0), _WARP, _CTA or _LANE */
+    uint32_t apply;          /* DCR_APPLY_AUTO (0), _WARP, _CTA, _LANE or _SPLIT */
     uint32_t overflow_kib;    /* device heap for XOR blocks that outgrow their
                                 6 KiB frame slot (masks of a few percent
                                 change and more): 0 = one eighth of

@@ -113,7 +113,7 @@ def test_plan_rejects_unknown_encoder_variant():
     h = ctypes.c_void_p()
     rc = dcr.lib().dcr_plan_build(arr, 1, ctypes.byref(opts), ctypes.byref(h))
     assert rc == dcr.ERR_INVALID and "encoder" in dcr.last_error() and h.value is None
-    opts = dcr.PlanOpts(0, 0, 0, 0, dcr.APPLY_LANE + 1)
+    opts = dcr.PlanOpts(0, 0, 0, 0, dcr.APPLY_SPLIT + 1)
     rc = dcr.lib().dcr_plan_build(arr, 1, ctypes.byref(opts), ctypes.byref(h))
     assert rc == dcr.ERR_INVALID and "apply" in dcr.last_error() and h.value is None
     opts = dcr.PlanOpts(0, 0, 0, 4)   # unknown plan flag

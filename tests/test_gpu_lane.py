@@ -157,12 +157,13 @@ def setup():
         "lane-lz4": dcr.Plan(descs_of(wl), apply=dcr.APPLY_LANE, codec=dcr.CODEC_LZ4),
         "lane-snappy": dcr.Plan(descs_of(wl), apply=dcr.APPLY_LANE, codec=dcr.CODEC_SNAPPY),
         "split": dcr.Plan(descs_of(wl), apply=dcr.APPLY_WARP, codec=dcr.CODEC_SNAPPY),
+        "split-all": dcr.Plan(descs_of(wl), apply=dcr.APPLY_SPLIT, codec=dcr.CODEC_LZ4),
         "window": dcr.Plan(descs_of(wl), apply=dcr.APPLY_WARP, codec=dcr.CODEC_LZ4),
     }
     return wl, orc, old, plans
 
 
-WALKS = ["lane", "split", "window"]
+WALKS = ["lane", "split", "split-all", "window"]
 
 
 def _plan(plans, walk, codec):

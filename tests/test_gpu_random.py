@@ -89,9 +89,11 @@ def test_random_workload_parity(seed, encoder):
     dense_bytes = any(t.elem_bits != 16 and t.frac > 0.1 for t in wl.tensors)
     plan = dcr.Plan(descs_of(wl), window_bytes=wl.window_bytes,
                     encoder={"wide": dcr.ENCODER_WIDE, "deep": dcr.ENCODER_DEEP, "cta": dcr.ENCODER_CTA}[encoder],
-                    # every apply kernel on every route: warp per frame after the wide encoder,
-                    # CTA per frame after the deep one, thread per ZSRC frame after the CTA one
-                    apply={"wide": dcr.APPLY_WARP, "deep": dcr.APPLY_CTA, "cta": dcr.APPLY_LANE}[encoder])
+                    # every apply kernel on every route: warp per frame (odd seeds: the split walk)
+                    # after the wide encoder, CTA per frame after the deep one, thread per ZSRC frame
+                    # after the CTA one
+                    apply={"wide": dcr.APPLY_SPLIT if seed % 2 else dcr.APPLY_WARP, "deep": dcr.APPLY_CTA,
+                           "cta": dcr.APPLY_LANE}[encoder])
     assert plan.info.plan_hash == orc.plan_hash and plan.n_windows == orc.n_windows
     d_old, d_new = to_device(olds), to_device(news)
     exp = orc.receiver_dense(news)

@@ -46,8 +46,8 @@ class Case:
 
 
 # every small twin with each apply kernel: one warp per frame, one CTA per
-# frame, one thread per ZSRC frame
-APPLY = {"warp": dcr.APPLY_WARP, "cta": dcr.APPLY_CTA, "lane": dcr.APPLY_LANE}
+# frame, one thread per ZSRC frame, the split walk of every ZSRC frame
+APPLY = {"warp": dcr.APPLY_WARP, "cta": dcr.APPLY_CTA, "lane": dcr.APPLY_LANE, "split": dcr.APPLY_SPLIT}
 
 
 @pytest.fixture(scope="module", params=[(n, a) for n in (1, 2, 3, 4, 5) for a in APPLY],
@@ -143,7 +143,7 @@ def test_overwrite_retry_stream_reaches_new(case):
     assert np.array_equal(case.host(t), case.exp)
 
 
-@pytest.mark.parametrize("apply", ["auto", "lane"])
+@pytest.mark.parametrize("apply", ["auto", "lane", "split"])
 @pytest.mark.parametrize("n", [1, 3])
 def test_abort_state_matches_oracle_then_retry(n, apply):
     c = Case(configs.mini(n), apply=dcr.APPLY_AUTO if apply == "auto" else APPLY[apply])
@@ -180,7 +180,7 @@ def _reindexed(pl_np, order):
     return out
 
 
-@pytest.mark.parametrize("apply", ["auto", "warp", "lane"])
+@pytest.mark.parametrize("apply", ["auto", "warp", "lane", "split"])
 def test_duplicate_frames_applied_once(apply):
     c = Case(configs.mini(2), apply=dcr.APPLY_AUTO if apply == "auto" else APPLY[apply])
     pl, size, _ = c.encode()
@@ -194,7 +194,7 @@ def test_duplicate_frames_applied_once(apply):
     assert np.array_equal(c.host(t), c.exp)
 
 
-@pytest.mark.parametrize("apply", ["cta", "warp", "lane"])
+@pytest.mark.parametrize("apply", ["cta", "warp", "lane", "split"])
 def test_repeated_overwrite_frames(apply):
     # overwrite frames are applied unclaimed (idempotent): a stream that
     # repeats them is applied while they fit route_kernel's frame list (one
@@ -222,7 +222,7 @@ def test_repeated_overwrite_frames(apply):
         assert rc == dcr.ERR_CORRUPT and st.version == 0
 
 
-@pytest.mark.parametrize("apply", ["auto", "warp", "lane"])
+@pytest.mark.parametrize("apply", ["auto", "warp", "lane", "split"])
 def test_duplicate_oracle_frames_applied_once(apply):
     c = Case(configs.mini(1), apply=dcr.APPLY_AUTO if apply == "auto" else APPLY[apply])
     o, _ = c.orc.encode(c.olds, c.news)
@@ -235,7 +235,7 @@ def test_duplicate_oracle_frames_applied_once(apply):
     assert np.array_equal(c.host(t), c.exp)
 
 
-@pytest.mark.parametrize("apply", ["auto", "warp", "lane"])
+@pytest.mark.parametrize("apply", ["auto", "warp", "lane", "split"])
 def test_rejections_leave_target_untouched(apply):
     c = Case(configs.mini(1), apply=dcr.APPLY_AUTO if apply == "auto" else APPLY[apply])
     pl, size, _ = c.encode(base=3, target=4)
@@ -262,7 +262,7 @@ def test_rejections_leave_target_untouched(apply):
     assert np.array_equal(c.host(t), c.exp)
 
 
-@pytest.mark.parametrize("apply", ["auto", "warp", "lane"])
+@pytest.mark.parametrize("apply", ["auto", "warp", "lane", "split"])
 def test_corrupt_lz4_frame_reported_and_retry_recovers(apply):
     c = Case(configs.mini(1), apply=dcr.APPLY_AUTO if apply == "auto" else APPLY[apply])
     pl, size, _ = c.encode()
@@ -302,7 +302,7 @@ def _last_match_offset(body):
             ip += 1
 
 
-@pytest.mark.parametrize("apply", ["auto", "lane"])
+@pytest.mark.parametrize("apply", ["auto", "lane", "split"])
 def test_frame_failing_late_leaves_its_chunk_untouched(apply):
     # a ZSRC frame whose last match offset is zeroed fails only after most of
     # its literals were XOR-ed in; the chunk must come back exactly as it was,
@@ -331,7 +331,7 @@ def test_frame_failing_late_leaves_its_chunk_untouched(apply):
     assert rc == dcr.OK and st.version == 1 and np.array_equal(c.host(t), c.exp)
 
 
-@pytest.mark.parametrize("apply", ["auto", "lane"])
+@pytest.mark.parametrize("apply", ["auto", "lane", "split"])
 @pytest.mark.parametrize("frac", [None, 0.05])
 def test_zsrc_flag_is_verified(frac, apply):
     # a greedy (oracle) block whose matches copy non-zero bytes, relabelled
@@ -376,7 +376,7 @@ def test_no_change_and_capacity():
     assert rc == dcr.OK and size3 == need
 
 
-@pytest.mark.parametrize("apply", ["auto", "lane"])
+@pytest.mark.parametrize("apply", ["auto", "lane", "split"])
 @pytest.mark.parametrize("frac", [0.0, 0.00085, 0.05, 0.3, "random"])
 def test_change_rates_parity(frac, apply):
     wl = configs.mini(4)
@@ -414,10 +414,10 @@ def test_signed_zero_on_gpu():
 # kernels of one apply: the first phase (CTA kernel; apply_kernel routing
 # itself; route, warp and thread kernels) and the commit check, and with
 # deferred frames the defer and big kernels and the commit check again
-FIRST_PHASE = {"auto": 1, "warp": 1, "lane": 3}
+FIRST_PHASE = {"auto": 1, "warp": 1, "lane": 3, "split": 1}
 
 
-@pytest.mark.parametrize("apply", ["auto", "warp", "lane"])
+@pytest.mark.parametrize("apply", ["auto", "warp", "lane", "split"])
 def test_kernel_timing_profile(apply):
     c = Case(configs.mini(2), apply=dcr.APPLY_AUTO if apply == "auto" else APPLY[apply])
     p0 = c.plan.last_profile()
