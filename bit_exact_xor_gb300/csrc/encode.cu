@@ -471,10 +471,21 @@ struct MaskSrc {
 // found with one ballot.  Sizes add up in P.out.  With emit, the sequences
 // are written to out at [0, cap); *over is set when one does not fit and *bad
 // when sizing and writing disagree.
+// What a group's block bytes owe to the literal start carried in from the
+// groups before it (parse_group's sizing pass can report it): only its first
+// match's sequence and, in a final group without a match, the tail; the rest
+// the group fixes by itself.
+struct GroupSplit {
+    uint32_t indep;      // bytes that do not depend on the carried literal start
+    int ms0;             // the first match's start (-1: the group has none)
+    uint32_t ml0, off0;  // ... its length and offset
+    bool tail_dep;       // final group without a match: the tail's literals start there
+};
+
 template <class Codec, class Src, class Out = Sink>
 __device__ __forceinline__ void parse_group(const Src& S, int e0, int cnt, bool final, int raw, Parse& P,
                                             const Out& out, uint32_t cap, bool emit, int lane, bool* over,
-                                            bool* bad)
+                                            bool* bad, GroupSplit* split = nullptr)
 {
     const int total = cnt + (final ? 1 : 0);
     const uint32_t lt = (1u << lane) - 1u;
@@ -547,6 +558,19 @@ __device__ __forceinline__ void parse_group(const Src& S, int e0, int cnt, bool 
         }
     } else {
         gsum = __reduce_add_sync(kFull, sz);
+        if (split) {
+            const bool dep = has && !below;            // the first match: literals from the carried start
+            const bool tdep = last && !has && !below;  // no match in the group: nor the tail's
+            const uint32_t tl = last ? Codec::tail(uint32_t(raw - flit)) : 0u;
+            const uint32_t sq = sz - tl;
+            split->indep = __reduce_add_sync(kFull, (dep ? 0u : sq) + (tdep ? 0u : tl));
+            const int f = M ? __ffs(M) - 1 : 0;
+            const int ms0 = __shfl_sync(kFull, ms, f);
+            split->ms0 = M ? ms0 : -1;
+            split->ml0 = uint32_t(__shfl_sync(kFull, me, f) - ms0);
+            split->off0 = uint32_t(__shfl_sync(kFull, off, f));
+            split->tail_dep = __any_sync(kFull, tdep);
+        }
     }
     // carry to the next group
     P.prev = __shfl_sync(kFull, p, total - 1);
@@ -1515,7 +1539,9 @@ struct __align__(16) CtaSmem {
     unsigned long long gbest[kEGroups];   // a group's longest zero run, then the longest before it
     int glit[kEGroups];                   // end of a group's last match (-1: none), then of the last before it
     int glev[kEGroups];                   // ... and the event at that end (the first pending literal event)
-    uint32_t gsz[kEGroups];               // a group's bytes, then the block bytes before it
+    uint32_t gsz[kEGroups];               // a group's bytes but its first match's sequence, then the block bytes before it
+    uint32_t gm0[kEGroups];               // its first match: start << 16 | length (~0u: none)
+    uint32_t goff0[kEGroups];             // ... offset, | 1 << 31 when its tail starts at the carried literal start
     uint32_t wcnt[kEWarps];               // events per slice
     uint32_t wchg[kEWarps];               // changed stored values per slice
     uint32_t base[kEWarps];               // events before each slice
@@ -1559,6 +1585,14 @@ struct SliceSrc {
     }
 };
 
+// encode_cta_kernel's fallback to the one-warp encoder, out of line: the
+// CTA kernel's own code stays small enough for the instruction cache
+template <class Codec>
+__device__ __noinline__ void encode_chunk_cold(const EncArgs& A, WarpSmem& W, uint32_t k, int lane)
+{
+    encode_chunk<kNS, Codec>(A, W, k, lane, nullptr);
+}
+
 template <class Codec>
 __global__ void __launch_bounds__(kEThreads, 4) encode_cta_kernel(EncArgs A)
 {
@@ -1572,7 +1606,7 @@ __global__ void __launch_bounds__(kEThreads, 4) encode_cta_kernel(EncArgs A)
     const int nseg = int(cd.src_count);
     const bool overwrite = (cd.flags & kResidualFlag) || A.mode == DCR_MODE_OVERWRITE_ONLY;
     if (overwrite || !(cd.flags & kSrcVec)) {   // the one-warp encoder does these
-        if (warp == 0) encode_chunk<kNS, Codec>(A, C.u.w, k, lane, nullptr);
+        if (warp == 0) encode_chunk_cold<Codec>(A, C.u.w, k, lane);
         return;
     }
     if (nseg <= kMSegCache)
@@ -1666,7 +1700,7 @@ __global__ void __launch_bounds__(kEThreads, 4) encode_cta_kernel(EncArgs A)
     }
     if (overflow) {   // a slice outgrew its region: the one-warp encoder takes the chunk
         __syncthreads();
-        if (warp == 0) encode_chunk<kNS, Codec>(A, C.u.w, k, lane, nullptr);
+        if (warp == 0) encode_chunk_cold<Codec>(A, C.u.w, k, lane);
         return;
     }
     if (threadIdx.x == 0 && chunk_changed) {
@@ -1688,18 +1722,29 @@ __global__ void __launch_bounds__(kEThreads, 4) encode_cta_kernel(EncArgs A)
 #pragma unroll
     for (int w = 0; w < kEWarps; ++w) S.base[w] = int(C.base[w]);
     const int full = int(total_ev / 32), G = full + 1;   // full groups, then the final one (with the end event)
-    auto group = [&](int g, Parse& P, uint8_t* out, uint32_t cap, bool emit, bool* over, bool* bad) {
+    auto group = [&](int g, Parse& P, uint8_t* out, uint32_t cap, bool emit, bool* over, bool* bad,
+                     GroupSplit* split) {
         P.prev = g ? S.at(32 * g - 1) : -1;
         const bool fin = g == full;
         parse_group<Codec>(S, 32 * g, fin ? int(total_ev) - 32 * g : 32, fin, raw, P, Sink{out}, cap, emit, lane,
-                           over, bad);
+                           over, bad, split);
     };
     bool over = false, bad = false;
-    // 1. each group's longest zero run (independent of the carried state)
+    // 1. each group's longest zero run (independent of the carried state):
+    //    the run before each of its events (and, in the final group, before
+    //    the chunk's end), as parse_group measures it, without the parse
     for (int g = warp; g < G; g += kEWarps) {
-        Parse P{-1, 0ull, 0, 0, 0u};
-        group(g, P, nullptr, 0, false, &over, &bad);
-        if (lane == 0) C.gbest[g] = P.best;
+        const bool fin = g == full;
+        const int total = (fin ? int(total_ev) - 32 * g : 32) + (fin ? 1 : 0);
+        const bool active = lane < total;
+        const int p = (!active || (fin && lane == total - 1)) ? raw : S.at(32 * g + lane);
+        int pp = __shfl_up_sync(kFull, p, 1);
+        if (lane == 0) pp = g ? S.at(32 * g - 1) : -1;
+        const int gs = pp + 1, L = p - gs;
+        const uint32_t clen = active && L > 0 ? uint32_t(L) : 0u;
+        const uint32_t mlen = __reduce_max_sync(kFull, clen);
+        const uint32_t mst = __reduce_max_sync(kFull, clen == mlen && mlen ? uint32_t(gs) : 0u);
+        if (lane == 0) C.gbest[g] = ((unsigned long long)mlen << 32) | mst;
     }
     __syncthreads();
     if (warp == 0) {   // exclusive prefix maximum
@@ -1721,18 +1766,27 @@ __global__ void __launch_bounds__(kEThreads, 4) encode_cta_kernel(EncArgs A)
         }
     }
     __syncthreads();
-    // 2. each group's last match, given the longest run before it
+    // 2. each group's last match, given the longest run before it, and its
+    //    bytes but those that depend on the literal start carried in
     for (int g = warp; g < G; g += kEWarps) {
         Parse P{-1, C.gbest[g], -1, 0, 0u};
-        group(g, P, nullptr, 0, false, &over, &bad);
+        GroupSplit Sp;
+        group(g, P, nullptr, 0, false, &over, &bad, &Sp);
         if (lane == 0) {
             C.glit[g] = P.lit;
             C.glev[g] = P.lit_ev;
+            C.gsz[g] = Sp.indep;
+            C.gm0[g] = Sp.ms0 < 0 ? ~0u : (uint32_t(Sp.ms0) << 16) | Sp.ml0;
+            C.goff0[g] = Sp.off0 | (Sp.tail_dep ? 1u << 31 : 0u);
         }
     }
     __syncthreads();
-    if (warp == 0) {   // exclusive "latest match end so far", with its event (0, 0 before the first)
+    if (warp == 0) {
+        // exclusive "latest match end so far", with its event (0, 0 before
+        // the first); with it each group's bytes, and their exclusive prefix
+        // sum after the block's preamble
         int run = 0, run_ev = 0;
+        uint32_t orun = Codec::preamble(uint32_t(raw));
         for (int g0 = 0; g0 < G; g0 += 32) {
             const int g = g0 + lane;
             const int v = g < G ? C.glit[g] : -1;
@@ -1741,34 +1795,25 @@ __global__ void __launch_bounds__(kEThreads, 4) encode_cta_kernel(EncArgs A)
             const uint32_t below = has & lt;
             const int src = below ? 31 - __clz(below) : 0;
             const int from = __shfl_sync(kFull, v, src), from_ev = __shfl_sync(kFull, ve, src);
+            uint32_t sz = 0;
             if (g < G) {
-                C.glit[g] = below ? from : run;
+                const int lit_in = below ? from : run;
+                C.glit[g] = lit_in;
                 C.glev[g] = below ? from_ev : run_ev;
+                const uint32_t m0 = C.gm0[g], o0 = C.goff0[g];
+                sz = C.gsz[g];
+                if (m0 != ~0u) sz += Codec::seq(uint32_t(int(m0 >> 16) - lit_in), m0 & 0xFFFFu, o0 & 0x7FFFFFFFu);
+                if (o0 >> 31) sz += Codec::tail(uint32_t(raw - lit_in));
             }
+            const uint32_t incl = warp_incl_sum(sz, lane);
+            if (g < G) C.gsz[g] = orun + incl - sz;
+            orun += __shfl_sync(kFull, incl, 31);
             if (has) {
                 run = __shfl_sync(kFull, v, 31 - __clz(has));
                 run_ev = __shfl_sync(kFull, ve, 31 - __clz(has));
             }
         }
-    }
-    __syncthreads();
-    // 3. each group's bytes, given both
-    for (int g = warp; g < G; g += kEWarps) {
-        Parse P{-1, C.gbest[g], C.glit[g], C.glev[g], 0u};
-        group(g, P, nullptr, 0, false, &over, &bad);
-        if (lane == 0) C.gsz[g] = P.out;
-    }
-    __syncthreads();
-    if (warp == 0) {   // exclusive prefix sum after the block's preamble
-        uint32_t run = Codec::preamble(uint32_t(raw));
-        for (int g0 = 0; g0 < G; g0 += 32) {
-            const int g = g0 + lane;
-            const uint32_t v = g < G ? C.gsz[g] : 0u;
-            const uint32_t incl = warp_incl_sum(v, lane);
-            if (g < G) C.gsz[g] = run + incl - v;
-            run += __shfl_sync(kFull, incl, 31);
-        }
-        if (lane == 0) C.total = run;
+        if (lane == 0) C.total = orun;
     }
     __syncthreads();
     const uint32_t total = C.total;
@@ -1789,7 +1834,7 @@ __global__ void __launch_bounds__(kEThreads, 4) encode_cta_kernel(EncArgs A)
     }
     for (int g = warp; g < G; g += kEWarps) {
         Parse P{-1, C.gbest[g], C.glit[g], C.glev[g], C.gsz[g]};
-        group(g, P, body, kSlotBody, true, &over, &bad);
+        group(g, P, body, kSlotBody, true, &over, &bad, nullptr);
     }
     if (__any_sync(kFull, over || bad) && lane == 0) report(A.sc, DCR_ERR_CORRUPT);
     const uint32_t fsz = (kFrameHdr + total + 15) / 16 * 16;
