@@ -119,3 +119,42 @@ def test_plan_rejects_unknown_encoder_variant():
     opts = dcr.PlanOpts(0, 0, 0, 4)   # unknown plan flag
     rc = dcr.lib().dcr_plan_build(arr, 1, ctypes.byref(opts), ctypes.byref(h))
     assert rc == dcr.ERR_INVALID and "flags" in dcr.last_error() and h.value is None
+
+
+def header_constants():
+    """Every DCR_* constant of include/dcr.h: enumerators (implicit values
+    count on from the previous one) and integer #defines."""
+    src = re.sub(r"/\*.*?\*/", "", open(os.path.join(ROOT, "include", "dcr.h")).read(), flags=re.S)
+    out = {}
+    for body in re.findall(r"enum\s*\{(.*?)\}", src, flags=re.S):
+        nxt = 0
+        for item in body.split(","):
+            m = re.match(r"\s*(DCR_\w+)\s*(?:=\s*(-?\w+))?\s*$", item)
+            if not m:
+                continue
+            nxt = int(m.group(2), 0) if m.group(2) else nxt
+            out[m.group(1)] = nxt
+            nxt += 1
+    for name, val in re.findall(r"#define\s+(DCR_\w+)\s+(0x[0-9A-Fa-f]+|\d+)u?\s*$", src, flags=re.M):
+        out[name] = int(val, 0)
+    return out
+
+
+def test_header_constants_match_binding_and_bench():
+    h = header_constants()
+    # the binding's names are the header's without the DCR_ prefix
+    for name, val in h.items():
+        py = name[len("DCR_"):]
+        if py in ("CHUNK_BYTES", "STREAM_HEADER_BYTES", "FRAME_HEADER_BYTES", "H"):
+            continue
+        assert hasattr(dcr, py), name
+        assert getattr(dcr, py) == val, (name, val, getattr(dcr, py))
+    for v in ("AUTO", "WARP", "CTA", "LANE", "SPLIT"):
+        assert "DCR_APPLY_" + v in h
+    assert h["DCR_CHUNK_BYTES"] == dcr.CHUNK_BYTES
+    import sys
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.APPLY_VARIANTS == {k.lower()[len("DCR_APPLY_"):]: v for k, v in h.items() if k.startswith("DCR_APPLY_")}
+    assert bench.ENCODER_VARIANTS == {k.lower()[len("DCR_ENCODER_"):]: v for k, v in h.items()
+                                      if k.startswith("DCR_ENCODER_")}
